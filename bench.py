@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark: SGEMM C = alpha*A*B + beta*C on one GB300, through the C ABI.
+
+Default workload: the compute-bound 8192^3 case (alpha = 1, beta = 0, seed 4,
+U[-1, 1) inputs).  One step = one sgemm_run over the whole problem.  Prints
+one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-cpu-baseline] [--no-workloads]
+
+--impl reference times the FP64 CPU oracle (the only other implementation
+here) on the same workload and metric, on the host cores, each step a bounded
+sample of output rows.
+
+Timing: CUDA events on the launching stream around exactly K back-to-back
+steps, after W warm-up steps, with a barrier and a device synchronize on both
+sides; the 8192^3 working set (768 MiB) is larger than L2 (129 MB).  For
+N > 1 (torchrun) every rank runs its own replica and the slowest rank's time
+is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOP/s (2MNK/t) at 4096³ and 8192³; % of GB300 FP32 peak"
+UNIT = "TFLOP/s"
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture, keyed by the SHA-256 of the kernel source it was taken on; any
+# other source gives traffic = null.  See profiles/.
+TRAFFIC_BY_SOURCE = {}
+KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma.cu",
+                  "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
+    p.add_argument("--e2e-steps", type=int, default=10)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.lines: list[str] = []
+        self.proc = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "sm_mhz_min": min(sm), "power_w_max": max(power)}
+
+
+def nvsmi_id(torch, dev: int) -> str | None:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- oracle arm
+
+def cpu_oracle_rate(cfg, prob, seconds: float, rows_hint: int | None = None):
+    """Time the oracle on a bounded sample of output rows; returns (TFLOP/s, rows, secs, cores)."""
+    import oracle
+    cores = oracle.num_threads()
+    rows = rows_hint or max(1, min(cfg.M, cores))
+    while True:
+        sel = list(range(rows))
+        t0 = time.perf_counter()
+        oracle.sgemm_rows(sel, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb, cfg.beta,
+                          prob.C0, cfg.ldc)
+        dt = time.perf_counter() - t0
+        if dt >= seconds * 0.5 or rows >= cfg.M:
+            break
+        rows = min(cfg.M, max(rows + 1, int(rows * seconds / max(dt, 1e-3))))
+    flops = 2.0 * rows * cfg.N * cfg.K
+    return flops / dt / 1e12, rows, dt, cores
+
+
+def reference_arm(args, cfg, rank, world):
+    if rank != 0:
+        return
+    from dense_fp32_matrix_09_gb300 import inputs
+    import oracle
+    prob = inputs.make_problem(cfg)
+    cores = oracle.num_threads()
+    # size one step: ~1 s of oracle work, so W + K steps stay within a few minutes
+    _, rows, dt, _ = cpu_oracle_rate(cfg, prob, seconds=1.0)
+    budget = 150.0
+    per_step = min(1.0, budget / max(1, args.steps + args.warmup))
+    rows = max(1, int(rows * per_step / max(dt, 1e-3)))
+    rows = min(rows, cfg.M)
+    sel = list(range(rows))
+
+    def step():
+        oracle.sgemm_rows(sel, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb, cfg.beta,
+                          prob.C0, cfg.ldc)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = 2.0 * rows * cfg.N * cfg.K * args.steps / dt / 1e12
+    sample = f"{rows} of {cfg.M} output rows per step (x {cfg.N} columns, K = {cfg.K}), FP64 oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K, "alpha": cfg.alpha,
+                   "beta": cfg.beta, "seed": cfg.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+# ---------------------------------------------------------------- our arm
+
+def flush_l2(torch, buf):
+    buf.add_(1.0)
+
+
+def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
+    """Median / mean per-call ms of one workload on device-resident inputs."""
+    from dense_fp32_matrix_09_gb300 import inputs
+    prob = inputs.make_problem(cfg)
+    A = torch.from_numpy(prob.A).cuda()
+    B = torch.from_numpy(prob.B).cuda()
+    C0 = torch.from_numpy(prob.C0).cuda()
+    C = C0.clone()
+    stream = torch.cuda.current_stream()
+
+    def call():
+        sg.sgemm_run(h, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, B, cfg.ldb, cfg.beta, C, cfg.ldc, stream)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        if cfg.beta != 0:
+            C.copy_(C0)
+        if cold:
+            flush_l2(torch, flush_buf)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    # back-to-back (hot L2) mean, beta == 0 only (in-place updates would compound)
+    hot = None
+    if cfg.beta == 0:
+        n = max(10, reps)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(n):
+            call()
+        e.record(stream)
+        e.synchronize()
+        hot = s.elapsed_time(e) / n
+    variant, splits = sg.sgemm_last_variant(h)
+    med = statistics.median(ms)
+    out = {"ms_median": med, "ms_min": min(ms), "tflops": cfg.flops / (med * 1e-3) / 1e12,
+           "gbs_compulsory": cfg.compulsory_bytes / (med * 1e-3) / 1e9, "reps": reps,
+           "l2": "flushed before each rep" if cold else "warm", "variant": sg.variant_name(variant)}
+    if splits > 1:
+        out["splits"] = splits
+    if hot is not None:
+        out["ms_back_to_back"] = hot
+        out["tflops_back_to_back"] = cfg.flops / (hot * 1e-3) / 1e12
+    del A, B, C, C0
+    return out
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from dense_fp32_matrix_09_gb300 import inputs
+    cfg = inputs.CONFIG_BY_NAME[args.workload] if args.workload else inputs.HEADLINE
+
+    if args.impl == "reference":
+        reference_arm(args, cfg, rank, world)
+        return
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from dense_fp32_matrix_09_gb300 import build, sgemm as sg
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    h = sg.sgemm_create()
+    prob = inputs.make_problem(cfg)
+    A = torch.from_numpy(prob.A).cuda()
+    B = torch.from_numpy(prob.B).cuda()
+    C0 = torch.from_numpy(prob.C0).cuda()
+    C = C0.clone()
+    stream = torch.cuda.current_stream()
+    in_place = cfg.beta != 0
+
+    def step():
+        sg.sgemm_run(h, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, B, cfg.ldb, cfg.beta, C, cfg.ldc, stream)
+
+    for _ in range(args.warmup):
+        if in_place:
+            C.copy_(C0)
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed region: K steps, events around each launch on the launching stream
+    sampler = ClockSampler(nvsmi_id(torch, local))
+    sampler.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if in_place:
+            C.copy_(C0)  # restore C outside the event pair
+        ev[2 * i].record(stream)
+        step()
+        ev[2 * i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    total_ms = sum(launch_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = cfg.flops * world / (ms_step * 1e-3) / 1e12
+    variant, splits = sg.sgemm_last_variant(h)
+    status = sg.sgemm_get_device_status(h)
+    if status != sg.OK:
+        raise SystemExit(f"device status after the timed region: {sg.status_string(status)}")
+
+    # ---- end to end: pinned host buffers -> device, sgemm_run, result -> host, every step
+    hA = torch.from_numpy(prob.A).pin_memory()
+    hB = torch.from_numpy(prob.B).pin_memory()
+    hC0 = torch.from_numpy(prob.C0).pin_memory()
+    hC = torch.empty_like(hC0).pin_memory()
+    h2d = hA.numel() * 4 + hB.numel() * 4 + (hC0.numel() * 4 if in_place else 0)
+    d2h = hC.numel() * 4
+
+    def e2e_step():
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
+        if in_place:
+            C.copy_(hC0, non_blocking=True)
+        step()
+        hC.copy_(C, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e.record(stream)
+    e.synchronize()
+    barrier()
+    e2e_ms = s.elapsed_time(e) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = cfg.flops * world / (e2e_ms * 1e-3) / 1e12
+
+    # ---- roofline of the dominant kernel (the only kernel of a step)
+    props = torch.cuda.get_device_properties(local)
+    sms = props.multi_processor_count
+    max_mhz = clocks.get("sm_max_mhz") or 2070.0
+    peak = 2 * 128 * sms * max_mhz * 1e6 / 1e12
+    achieved = cfg.flops / (statistics.mean(launch_ms) * 1e-3) / 1e12
+    src_hash = kernel_source_hash()
+    roofline = {
+        "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+        "traffic": TRAFFIC_BY_SOURCE.get(src_hash),
+        "kernel": f"sgemm_tma_kernel ({sg.variant_name(variant)})",
+        "peak_basis": f"FP32 FFMA: 2 FLOP x 128 lanes x {sms} SMs x {max_mhz:.0f} MHz (max SM clock)",
+    }
+    if clocks.get("sm_mhz"):
+        roofline["frac_at_measured_clock"] = achieved / (2 * 128 * sms * clocks["sm_mhz"] * 1e6 / 1e12)
+    roofline["algorithmic_flops_per_launch"] = cfg.flops
+    roofline["kernel_source_sha256_16"] = src_hash
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "M": cfg.M, "N": cfg.N, "K": cfg.K, "lda": cfg.lda,
+                   "ldb": cfg.ldb, "ldc": cfg.ldc, "alpha": cfg.alpha, "beta": cfg.beta, "seed": cfg.seed,
+                   "inputs": "i.i.d. U[-1,1) float32",
+                   "l2": "inputs larger than L2 (working set %d MiB)" % ((prob.A.nbytes + prob.B.nbytes + prob.C0.nbytes) >> 20),
+                   "variant": sg.variant_name(variant), "splits": splits,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": args.e2e_steps},
+        "gpu_launches": args.steps,
+        "roofline": roofline,
+        "clocks": clocks,
+        "gpu": {"name": props.name, "sms": sms},
+    }
+
+    # ---- per-workload table (device-resident; not part of the headline value)
+    if not args.no_workloads and rank == 0:
+        flush_buf = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
+        table = {}
+        for w, reps in zip(inputs.CONFIGS, (200, 200, 50, 50, 20)):
+            cold = (w.compulsory_bytes < 2 * 129e6)
+            table[w.name] = time_workload(torch, sg, h, w, reps, cold, flush_buf)
+        out["workloads"] = table
+        del flush_buf
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, rows, dt, cores = cpu_oracle_rate(cfg, prob, seconds=12.0)
+        out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"{rows} of {cfg.M} output rows (x {cfg.N} columns, K = {cfg.K}) "
+                                         f"in {dt:.1f} s, FP64 accumulation"}
+    sg.sgemm_destroy(h)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,56 @@
+// Internal interface between the C-ABI layer (sgemm_api.cu) and the kernel
+// translation units.  Nothing here is exported from the shared library.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sg {
+
+// Bit set in a handle's device status word when a kernel gives up a bounded wait.
+constexpr int kDevTimeoutBit = 1;
+
+// One call's arguments after validation (sizes > 0, alpha != 0, K > 0 for the
+// GEMM kernels).
+struct GemmArgs {
+    int M, N, K;
+    float alpha, beta;
+    const float *A;
+    int lda;
+    const float *B;
+    int ldb;
+    float *C;
+    int ldc;
+    bool vec_c;   // C is 16-byte aligned and ldc % 4 == 0: float4 epilogue
+    int *status;  // device status word of the handle
+};
+
+// Static description of a TMA-fed SIMT variant.
+struct TmaShape {
+    int bm, bn, bk;     // CTA tile and K step per pipeline stage
+    int threads;        // consumer threads + one producer warp
+    int smem_bytes;     // dynamic shared memory per CTA
+    int min_ctas_per_sm;
+};
+
+// Split-K bookkeeping (only for the split-K variant).
+struct SplitK {
+    int splits;             // number of K ranges (CTAs per output tile)
+    int k_tiles_per_split;  // K steps of bk per range
+    float *ws;              // splits * tiles * bm * bn partial sums
+    int *counters;          // one arrival counter per output tile, zero between calls
+};
+
+// variant ids are the public sgemm_variant_t values of the TMA variants
+bool tma_shape(int variant, TmaShape *out);
+cudaError_t tma_prepare(int variant);
+cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA,
+                       const CUtensorMap &tmB, const SplitK &sk, int smem_override,
+                       cudaStream_t stream);
+
+cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream);
+cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);
+cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);
+
+}  // namespace sg

@@ -1,0 +1,342 @@
+// C ABI of the SGEMM library (declared in include/sgemm.h): handle life
+// cycle, argument validation, the choice of kernel variant and the TMA
+// descriptors.  Every computation is done by the kernels in sgemm_tma.cu and
+// sgemm_aux.cu; this file only validates, chooses and launches.
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <unordered_set>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "sgemm.h"
+
+struct sgemm_ctx {
+    int device;
+    int num_sms;
+    int *d_status;
+    float *d_ws;
+    size_t ws_floats;
+    int *d_counters;
+    int n_counters;
+    int pinned;
+    int last_variant;
+    int last_splits;
+    int smem_override;
+};
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = size_t(32) << 20;  // split-K partial tiles
+constexpr int kCounters = 16384;                      // split-K output tiles per call
+
+std::mutex g_mu;
+std::unordered_set<sgemm_ctx *> g_live;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool alive(sgemm_ctx *h) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return h != nullptr && g_live.count(h) != 0;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// [lo, hi) byte range of a rows x cols window with leading dimension ld.
+inline void window(const void *p, int rows, int cols, int ld, uintptr_t *lo, uintptr_t *hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + (static_cast<uintptr_t>(rows - 1) * static_cast<uintptr_t>(ld) + cols) * sizeof(float);
+}
+
+inline bool overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+int from_cuda(cudaError_t e) {
+    switch (e) {
+        case cudaSuccess: return SGEMM_OK;
+        case cudaErrorInvalidValue:
+        case cudaErrorInvalidConfiguration:
+        case cudaErrorLaunchOutOfResources:
+        case cudaErrorInvalidDeviceFunction:
+        case cudaErrorNoKernelImageForDevice: return SGEMM_ERR_LAUNCH;
+        default: return SGEMM_ERR_CUDA;
+    }
+}
+
+bool load_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return true;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+// 2-D row-major float32 matrix (rows x cols, leading dimension ld) as a TMA
+// tensor; box = box_cols x box_rows elements.
+bool encode_2d(CUtensorMap *map, const float *base, int rows, int cols, int ld, int box_cols,
+               int box_rows, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * sizeof(float)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Variant for a TMA-eligible call: large tiles while they fill the GPU several
+// times over, smaller tiles when they do not, split-K when even 64 x 64 tiles
+// leave most SMs idle and K is long enough to split.
+int choose_variant(const sgemm_ctx *h, int M, int N, int K) {
+    const int sms = h->num_sms;
+    const long long tL = 1LL * cdiv(M, 128) * cdiv(N, 256);
+    const long long tM = 1LL * cdiv(M, 128) * cdiv(N, 128);
+    const long long tS = 1LL * cdiv(M, 64) * cdiv(N, 64);
+    const int k_tiles = cdiv(K, 32);
+    if (tL >= 2LL * sms) return SGEMM_VARIANT_TMA_128x256;
+    if (tM >= sms) return SGEMM_VARIANT_TMA_128x128;
+    if (tS >= sms || k_tiles < 4) return SGEMM_VARIANT_TMA_64x64;
+    return SGEMM_VARIANT_TMA_64x64_SPLITK;
+}
+
+// Split count for the split-K variant: enough CTAs for two per SM, at least
+// one K step per split, and the partial tiles must fit the workspace.
+void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
+    const long long tiles = 1LL * cdiv(M, 64) * cdiv(N, 64);
+    const int k_tiles = cdiv(K, 32);
+    long long want = (2LL * h->num_sms + tiles - 1) / tiles;
+    want = std::min<long long>(std::min<long long>(want, k_tiles), 32);
+    const long long fit = static_cast<long long>(h->ws_floats / (tiles * 64 * 64));
+    want = std::min(want, fit);
+    if (tiles > h->n_counters) want = 1;
+    if (want < 1) want = 1;
+    const int kps = cdiv(k_tiles, static_cast<int>(want));
+    sk->k_tiles_per_split = kps;
+    sk->splits = cdiv(k_tiles, kps);
+    sk->ws = h->d_ws;
+    sk->counters = h->d_counters;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgemm_version(void) { return 10000; }
+
+const char *sgemm_status_string(int s) {
+    switch (s) {
+        case SGEMM_OK: return "SGEMM_OK";
+        case SGEMM_ERR_NULL: return "SGEMM_ERR_NULL: a required pointer is NULL";
+        case SGEMM_ERR_INVALID_VALUE: return "SGEMM_ERR_INVALID_VALUE: negative size, leading dimension too small or bad enum";
+        case SGEMM_ERR_ALIAS: return "SGEMM_ERR_ALIAS: C overlaps A or B";
+        case SGEMM_ERR_BAD_HANDLE: return "SGEMM_ERR_BAD_HANDLE: not a live handle";
+        case SGEMM_ERR_UNSUPPORTED_DEVICE: return "SGEMM_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3";
+        case SGEMM_ERR_LAUNCH: return "SGEMM_ERR_LAUNCH: kernel launch rejected";
+        case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: CUDA runtime error";
+        case SGEMM_ERR_DEVICE_TIMEOUT: return "SGEMM_ERR_DEVICE_TIMEOUT: a kernel abandoned a bounded wait";
+        case SGEMM_ERR_WRONG_DEVICE: return "SGEMM_ERR_WRONG_DEVICE: current device differs from the handle's";
+        default: return "SGEMM_ERR_UNKNOWN";
+    }
+}
+
+const char *sgemm_variant_name(int v) {
+    switch (v) {
+        case SGEMM_VARIANT_AUTO: return "auto";
+        case SGEMM_VARIANT_TMA_128x256: return "tma_128x256";
+        case SGEMM_VARIANT_TMA_128x128: return "tma_128x128";
+        case SGEMM_VARIANT_TMA_64x64: return "tma_64x64";
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return "tma_64x64_splitk";
+        case SGEMM_VARIANT_GENERIC: return "generic";
+        case SGEMM_VARIANT_SCALE: return "scale";
+        default: return "unknown";
+    }
+}
+
+int sgemm_check_args(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                     float beta, const float *C, int ldc) {
+    (void)beta;
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N)) return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr) return SGEMM_ERR_NULL;
+    const bool reads_ab = (alpha != 0.f) && K > 0;
+    if (!reads_ab) return SGEMM_OK;
+    if (A == nullptr || B == nullptr) return SGEMM_ERR_NULL;
+    uintptr_t c0, c1, a0, a1, b0, b1;
+    window(C, M, N, ldc, &c0, &c1);
+    window(A, M, K, lda, &a0, &a1);
+    window(B, K, N, ldb, &b0, &b1);
+    if (overlap(c0, c1, a0, a1) || overlap(c0, c1, b0, b1)) return SGEMM_ERR_ALIAS;
+    return SGEMM_OK;
+}
+
+int sgemm_create(sgemm_handle_t *out) {
+    if (out == nullptr) return SGEMM_ERR_NULL;
+    *out = nullptr;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return SGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!load_encoder()) return SGEMM_ERR_CUDA;
+    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
+                  SGEMM_VARIANT_TMA_64x64_SPLITK})
+        if (sg::tma_prepare(v) != cudaSuccess) return SGEMM_ERR_CUDA;
+
+    sgemm_ctx *h = new (std::nothrow) sgemm_ctx();
+    if (!h) return SGEMM_ERR_CUDA;
+    h->device = dev;
+    h->num_sms = prop.multiProcessorCount;
+    h->ws_floats = kWorkspaceBytes / sizeof(float);
+    h->n_counters = kCounters;
+    h->last_variant = -1;
+    bool ok = cudaMalloc(&h->d_status, sizeof(int)) == cudaSuccess &&
+              cudaMalloc(&h->d_ws, kWorkspaceBytes) == cudaSuccess &&
+              cudaMalloc(&h->d_counters, kCounters * sizeof(int)) == cudaSuccess &&
+              cudaMemset(h->d_status, 0, sizeof(int)) == cudaSuccess &&
+              cudaMemset(h->d_counters, 0, kCounters * sizeof(int)) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+        cudaFree(h->d_status);
+        cudaFree(h->d_ws);
+        cudaFree(h->d_counters);
+        delete h;
+        cudaGetLastError();
+        return SGEMM_ERR_CUDA;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_live.insert(h);
+    }
+    *out = h;
+    return SGEMM_OK;
+}
+
+int sgemm_destroy(sgemm_handle_t h) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (h == nullptr || g_live.erase(h) == 0) return SGEMM_ERR_BAD_HANDLE;
+    }
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    const cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(h->d_status);
+    cudaFree(h->d_ws);
+    cudaFree(h->d_counters);
+    if (prev != h->device) cudaSetDevice(prev);
+    delete h;
+    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
+}
+
+int sgemm_set_variant(sgemm_handle_t h, int variant) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (variant < 0 || variant >= SGEMM_VARIANT_COUNT_ || variant == SGEMM_VARIANT_SCALE)
+        return SGEMM_ERR_INVALID_VALUE;
+    h->pinned = variant;
+    return SGEMM_OK;
+}
+
+int sgemm_last_variant(sgemm_handle_t h, int *splits) {
+    if (!alive(h)) return -1;
+    if (splits) *splits = h->last_splits;
+    return h->last_variant;
+}
+
+int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (bytes < 0) return SGEMM_ERR_INVALID_VALUE;
+    h->smem_override = bytes;
+    return SGEMM_OK;
+}
+
+int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+              int ldb, float beta, float *C, int ldc, void *stream_) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    const int st = sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != SGEMM_OK) return st;
+    h->last_variant = -1;
+    h->last_splits = 1;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+
+    sg::GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc,
+                   aligned16(C) && (ldc % 4) == 0, h->d_status};
+    if (alpha == 0.f || K == 0) {
+        // C = beta*C (C = 0 when beta == 0); beta == 1 leaves C as it is.
+        int rc = SGEMM_OK;
+        if (beta != 1.f) rc = from_cuda(sg::launch_scale(g, stream));
+        if (rc == SGEMM_OK) h->last_variant = SGEMM_VARIANT_SCALE;
+        return rc;
+    }
+    const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0;
+    int variant = h->pinned != SGEMM_VARIANT_AUTO ? h->pinned : choose_variant(h, M, N, K);
+    if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
+
+    if (variant == SGEMM_VARIANT_GENERIC) {
+        const int rc = from_cuda(sg::launch_generic(g, stream));
+        if (rc == SGEMM_OK) h->last_variant = variant;
+        return rc;
+    }
+
+    sg::TmaShape sh;
+    if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
+    sg::SplitK sk{1, cdiv(K, sh.bk), nullptr, nullptr};
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+        plan_splits(h, M, N, K, &sk);
+        if (sk.splits <= 1) {
+            variant = SGEMM_VARIANT_TMA_64x64;
+            sk = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr};
+        }
+    }
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, B, K, N, ldb, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return SGEMM_ERR_CUDA;
+    const int rc = from_cuda(sg::launch_tma(variant, g, tmA, tmB, sk, h->smem_override, stream));
+    if (rc == SGEMM_OK) {
+        h->last_variant = variant;
+        h->last_splits = sk.splits;
+    }
+    return rc;
+}
+
+int sgemm_get_device_status(sgemm_handle_t h) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (prev != h->device) cudaSetDevice(h->device);
+    int word = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&word, h->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (prev != h->device) cudaSetDevice(prev);
+    if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+    return (word & sg::kDevTimeoutBit) ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    limit_ns = std::min(std::max(limit_ns, 1000LL), 1000000000LL);
+    return from_cuda(sg::launch_timeout_probe(h->d_status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// Auxiliary kernels of the SGEMM library:
+//
+//  * sgemm_generic_kernel -- the any-alignment SIMT path, used when A or B
+//    cannot be described to TMA (pointer not 16-byte aligned or lda / ldb not
+//    a multiple of 4).  64 x 64 CTA tile, K step 16, 256 threads with a 4 x 4
+//    register block each.  Tiles are staged through shared memory with scalar
+//    loads; elements outside the matrices are filled with 0 at load (page
+//    m.lqnn.cn/news/94381 section 2.3, boundary handling by zero-fill at load;
+//    page mlqm.cn/news/1180856 section 4.2, the tiled version), A is stored
+//    k-major so that the inner loop reads both operands from shared memory
+//    without bank conflicts (the padded layout of page m.lqnn.cn/news/94381
+//    section 4.3), and the epilogue applies alpha and beta (page "Deep dive
+//    into the sgemmNN algorithm", write-back section).
+//  * sgemm_scale_kernel -- the alpha == 0 or K == 0 quick path: C = beta*C,
+//    or C = 0 without reading C when beta == 0 (BLAS convention).
+//  * timeout_probe_kernel -- waits on an mbarrier that nothing completes,
+//    gives up after a short limit and records the timeout, to test the
+//    device-side timeout reporting without faulting or hanging the GPU.
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace sg {
+namespace {
+
+constexpr int GB = 64, GK = 16, GT = 256;
+
+__global__ void __launch_bounds__(GT) sgemm_generic_kernel(const GemmArgs g) {
+    __shared__ float As[GK][GB + 4];  // A tile stored k-major: As[k][m]
+    __shared__ float Bs[GK][GB + 4];  // B tile: Bs[k][n]
+    const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+    const int m0 = blockIdx.y * GB, n0 = blockIdx.x * GB;
+    float acc[4][4] = {};
+    for (int k0 = 0; k0 < g.K; k0 += GK) {
+#pragma unroll
+        for (int r = 0; r < (GB * GK) / GT; ++r) {
+            const int e = tid + r * GT;
+            // A: 64 rows x 16 k; consecutive threads walk k (coalesced along rows)
+            const int am = e / GK, ak = e % GK;
+            const int gm = m0 + am, gk = k0 + ak;
+            As[ak][am] = (gm < g.M && gk < g.K) ? g.A[static_cast<size_t>(gm) * g.lda + gk] : 0.f;
+            // B: 16 k x 64 cols; consecutive threads walk n
+            const int bk = e / GB, bn = e % GB;
+            const int hk = k0 + bk, hn = n0 + bn;
+            Bs[bk][bn] = (hk < g.K && hn < g.N) ? g.B[static_cast<size_t>(hk) * g.ldb + hn] : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < GK; ++k) {
+            float a[4], b[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) b[j] = Bs[k][tx + 16 * j];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int row = m0 + ty + 16 * i;
+        if (row >= g.M) continue;
+        float *crow = g.C + static_cast<size_t>(row) * g.ldc;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = n0 + tx + 16 * j;
+            if (col >= g.N) continue;
+            float r = g.alpha * acc[i][j];
+            if (g.beta != 0.f) r = fmaf(g.beta, crow[col], r);
+            crow[col] = r;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
+    const int stride_x = gridDim.x * blockDim.x * 4;
+    for (int row = blockIdx.y; row < g.M; row += gridDim.y) {
+        float *crow = g.C + static_cast<size_t>(row) * g.ldc;
+        for (int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4; col < g.N; col += stride_x) {
+            if (g.vec_c && col + 3 < g.N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + col);
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (g.beta != 0.f) {
+                    v = *p;
+                    v.x *= g.beta; v.y *= g.beta; v.z *= g.beta; v.w *= g.beta;
+                }
+                *p = v;
+            } else {
+                for (int v = 0; v < 4 && col + v < g.N; ++v)
+                    crow[col + v] = g.beta != 0.f ? g.beta * crow[col + v] : 0.f;
+            }
+        }
+    }
+}
+
+__global__ void timeout_probe_kernel(int *status, long long limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Phase 0 never completes: nobody arrives on the barrier.
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, status, static_cast<unsigned long long>(limit_ns));
+}
+
+}  // namespace
+
+cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream) {
+    const dim3 grid((g.N + GB - 1) / GB, (g.M + GB - 1) / GB);
+    sgemm_generic_kernel<<<grid, GT, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
+    const int gx = min((g.N + 1023) / 1024, 8);
+    const int gy = min(g.M, 8192);
+    sgemm_scale_kernel<<<dim3(gx, gy), 256, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream) {
+    timeout_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace sg

@@ -1,0 +1,207 @@
+"""ctypes binding of libsgemm.so, with the entry-point names of include/sgemm.h.
+
+Argument marshalling only: every step of C = alpha*A*B + beta*C runs in the
+CUDA library.  Matrix arguments may be raw device addresses (int) or objects
+with ``data_ptr()`` (torch tensors); streams may be an int handle, a
+``torch.cuda.Stream`` or ``None`` (torch's current stream).  A non-zero
+status raises ``SgemmError``.  If the library has not been built the first
+call raises -- there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+OK = 0
+ERR_NULL = 1
+ERR_INVALID_VALUE = 2
+ERR_ALIAS = 3
+ERR_BAD_HANDLE = 4
+ERR_UNSUPPORTED_DEVICE = 5
+ERR_LAUNCH = 6
+ERR_CUDA = 7
+ERR_DEVICE_TIMEOUT = 8
+ERR_WRONG_DEVICE = 9
+
+VARIANT_AUTO = 0
+VARIANT_TMA_128x256 = 1
+VARIANT_TMA_128x128 = 2
+VARIANT_TMA_64x64 = 3
+VARIANT_TMA_64x64_SPLITK = 4
+VARIANT_GENERIC = 5
+VARIANT_SCALE = 6
+GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
+                 VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC)
+
+#: Every exported entry point of include/sgemm.h.
+EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",
+           "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
+           "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
+           "sgemm_version")
+
+
+class SgemmError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}" if where else status_string(status))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library (raises if it was never built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (dense_fp32_matrix_09_gb300.build.build())")
+        L = ctypes.CDLL(path)
+        vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.sgemm_create.argtypes = [ctypes.POINTER(vp)]
+        L.sgemm_run.argtypes = [vp, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
+        L.sgemm_check_args.argtypes = [i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32]
+        L.sgemm_destroy.argtypes = [vp]
+        L.sgemm_set_variant.argtypes = [vp, i32]
+        L.sgemm_last_variant.argtypes = [vp, ctypes.POINTER(i32)]
+        L.sgemm_get_device_status.argtypes = [vp]
+        L.sgemm_debug_timeout_probe.argtypes = [vp, ctypes.c_longlong, vp]
+        L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
+        L.sgemm_status_string.argtypes = [i32]
+        L.sgemm_status_string.restype = ctypes.c_char_p
+        L.sgemm_variant_name.argtypes = [i32]
+        L.sgemm_variant_name.restype = ctypes.c_char_p
+        L.sgemm_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def _check(rc: int, where: str) -> int:
+    if rc != OK:
+        raise SgemmError(rc, where)
+    return rc
+
+
+def status_string(status: int) -> str:
+    return lib().sgemm_status_string(int(status)).decode()
+
+
+def variant_name(variant: int) -> str:
+    return lib().sgemm_variant_name(int(variant)).decode()
+
+
+def sgemm_version() -> int:
+    return lib().sgemm_version()
+
+
+def sgemm_create() -> ctypes.c_void_p:
+    h = ctypes.c_void_p()
+    _check(lib().sgemm_create(ctypes.byref(h)), "sgemm_create")
+    return h
+
+
+def sgemm_destroy(h) -> None:
+    _check(lib().sgemm_destroy(h), "sgemm_destroy")
+
+
+def sgemm_run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """C <- alpha*A*B + beta*C on device buffers (row-major, leading dims)."""
+    _check(lib().sgemm_run(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
+                           int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream)), "sgemm_run")
+
+
+def sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
+    """Host-only validation; returns the status sgemm_run would return for these arguments."""
+    return lib().sgemm_check_args(int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
+                                  int(ldb), float(beta), _ptr(C), int(ldc))
+
+
+def sgemm_set_variant(h, variant: int) -> None:
+    _check(lib().sgemm_set_variant(h, int(variant)), "sgemm_set_variant")
+
+
+def sgemm_last_variant(h) -> tuple[int, int]:
+    splits = ctypes.c_int(0)
+    v = lib().sgemm_last_variant(h, ctypes.byref(splits))
+    return v, splits.value
+
+
+def sgemm_get_device_status(h) -> int:
+    return lib().sgemm_get_device_status(h)
+
+
+def sgemm_debug_timeout_probe(h, limit_ns: int, stream=None) -> None:
+    _check(lib().sgemm_debug_timeout_probe(h, int(limit_ns), _stream(stream)), "sgemm_debug_timeout_probe")
+
+
+def sgemm_debug_set_smem_override(h, nbytes: int) -> None:
+    _check(lib().sgemm_debug_set_smem_override(h, int(nbytes)), "sgemm_debug_set_smem_override")
+
+
+class Sgemm:
+    """A handle as a context manager: ``with Sgemm() as g: g.run(...)``."""
+
+    def __init__(self, variant: int = VARIANT_AUTO):
+        self.h = sgemm_create()
+        if variant != VARIANT_AUTO:
+            sgemm_set_variant(self.h, variant)
+
+    def run(self, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+        sgemm_run(self.h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+
+    def matmul(self, A, B, C, alpha=1.0, beta=0.0, stream=None):
+        """C <- alpha*A@B + beta*C for 2-D row-major torch tensors (unit column stride)."""
+        M, K = A.shape
+        K2, N = B.shape
+        if K2 != K or tuple(C.shape) != (M, N):
+            raise ValueError(f"shape mismatch: {tuple(A.shape)} @ {tuple(B.shape)} -> {tuple(C.shape)}")
+        for t in (A, B, C):
+            if t.dim() != 2 or (t.numel() and t.stride(1) != 1):
+                raise ValueError("operands must be 2-D with unit column stride")
+        sgemm_run(self.h, M, N, K, alpha, A, max(A.stride(0), 1), B, max(B.stride(0), 1), beta, C,
+                  max(C.stride(0), 1), stream)
+        return C
+
+    @property
+    def last_variant(self):
+        return sgemm_last_variant(self.h)
+
+    def set_variant(self, v):
+        sgemm_set_variant(self.h, v)
+
+    def device_status(self) -> int:
+        return sgemm_get_device_status(self.h)
+
+    def close(self):
+        if self.h is not None:
+            sgemm_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

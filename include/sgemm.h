@@ -1,0 +1,153 @@
+/*
+ * sgemm.h -- C ABI of the GB300 (sm_103a) single-precision GEMM library.
+ *
+ * Operation (the definition on the page "Deep dive into the sgemmNN
+ * algorithm" (lazypool blog), section "Why SGEMM matters"; argument list in
+ * the style of the sgemmNN kernel signature on the same page, section
+ * "The whole kernel"):
+ *
+ *     C <- alpha * A * B + beta * C
+ *
+ * with A an M x K, B a K x N and C an M x N matrix of 32-bit floats, all
+ * ROW-MAJOR with leading dimensions (element strides between rows):
+ *
+ *     A[i][p] = A[i*lda + p],  B[p][j] = B[p*ldb + j],  C[i][j] = C[i*ldc + j]
+ *
+ * (row-major as in the naive kernel of page m.lqnn.cn/news/94381, section
+ * 1.1).  Accumulation is in FP32 on the GPU; the summation order is the
+ * library's and is fixed per kernel variant, so repeated calls with the same
+ * inputs and the same variant give bit-identical results.
+ *
+ * Conventions (BLAS, where the pages are silent):
+ *   - beta == 0: C is output only and is never read (NaN/Inf in C do not
+ *     propagate).
+ *   - alpha == 0 or K == 0: A and B are not read (may be NULL); C <- beta*C.
+ *   - M == 0 or N == 0: nothing is done; every pointer may be NULL.
+ *   - Cells outside the M x K, K x N, M x N windows (columns K..lda-1 of A,
+ *     N..ldb-1 of B, N..ldc-1 of C) are never read or written.
+ *
+ * Memory and streams: all matrix pointers are DEVICE pointers owned by the
+ * caller.  sgemm_run never allocates and never synchronizes: it validates
+ * its arguments on the host, enqueues kernels on `stream` (a cudaStream_t
+ * cast to void*, NULL for the legacy default stream) and returns.  The
+ * returned status covers only what is known at enqueue time; a fault found
+ * later by a kernel is reported by sgemm_get_device_status.
+ *
+ * Threading: one handle may be used from one host thread at a time, and its
+ * calls must be ordered on the GPU (one stream, or streams ordered by
+ * events): calls of the same handle share its split-K workspace.  Use one
+ * handle per concurrently running stream.
+ *
+ * Every function returns an sgemm_status_t value (as int) unless noted.
+ */
+#ifndef SGEMM_H
+#define SGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct sgemm_ctx *sgemm_handle_t;
+
+typedef enum {
+    SGEMM_OK = 0,
+    SGEMM_ERR_NULL = 1,               /* a required pointer argument is NULL          */
+    SGEMM_ERR_INVALID_VALUE = 2,      /* negative size, ld below its minimum, bad enum */
+    SGEMM_ERR_ALIAS = 3,              /* C overlaps A or B                             */
+    SGEMM_ERR_BAD_HANDLE = 4,         /* not a live handle (never created, destroyed)  */
+    SGEMM_ERR_UNSUPPORTED_DEVICE = 5, /* current device is not compute capability 10.3 */
+    SGEMM_ERR_LAUNCH = 6,             /* the kernel launch was rejected                */
+    SGEMM_ERR_CUDA = 7,               /* another CUDA runtime error                    */
+    SGEMM_ERR_DEVICE_TIMEOUT = 8,     /* a kernel gave up a bounded wait (device side) */
+    SGEMM_ERR_WRONG_DEVICE = 9        /* current device differs from the handle's      */
+} sgemm_status_t;
+
+/* Kernel variants.  SGEMM_VARIANT_AUTO lets sgemm_run choose from the shape
+ * and the alignment of the operands; the others pin one variant (for tests
+ * and measurements).  A pinned variant whose preconditions a call does not
+ * meet (TMA variants need 16-byte aligned A and B and lda, ldb multiples of
+ * 4) is replaced by the generic variant for that call. */
+typedef enum {
+    SGEMM_VARIANT_AUTO = 0,
+    SGEMM_VARIANT_TMA_128x256 = 1,   /* TMA-fed SIMT, 128 x 256 CTA tile, 8 x 16 per thread */
+    SGEMM_VARIANT_TMA_128x128 = 2,   /* TMA-fed SIMT, 128 x 128 CTA tile, 8 x 8 per thread  */
+    SGEMM_VARIANT_TMA_64x64 = 3,     /* TMA-fed SIMT, 64 x 64 CTA tile, 8 x 4 per thread    */
+    SGEMM_VARIANT_TMA_64x64_SPLITK = 4, /* 64 x 64 tiles, K split over CTAs, fixed-order sum */
+    SGEMM_VARIANT_GENERIC = 5,       /* scalar loads, any alignment, 64 x 64 CTA tile       */
+    SGEMM_VARIANT_SCALE = 6,         /* reported only: the C <- beta*C quick path ran       */
+    SGEMM_VARIANT_COUNT_ = 7
+} sgemm_variant_t;
+
+/* Create a handle bound to the CURRENT CUDA device.  Requires compute
+ * capability 10.3 (GB300); otherwise returns SGEMM_ERR_UNSUPPORTED_DEVICE and
+ * sets *out to NULL.  Allocates the handle's device-side status word and its
+ * split-K workspace (a few MiB, zeroed) and sets the kernels' shared-memory
+ * limits.  `out` must be non-NULL (else SGEMM_ERR_NULL). */
+int sgemm_create(sgemm_handle_t *out);
+
+/* C <- alpha*A*B + beta*C, enqueued on `stream`; see the conventions above.
+ * Argument checks, in order: handle (SGEMM_ERR_BAD_HANDLE), current device
+ * (SGEMM_ERR_WRONG_DEVICE), then the rules of sgemm_check_args.  On any
+ * error nothing is enqueued and C is unchanged. */
+int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha,
+              const float *A, int lda, const float *B, int ldb,
+              float beta, float *C, int ldc, void *stream);
+
+/* Host-only validation with exactly the rules sgemm_run applies (no CUDA call,
+ * no handle): SGEMM_ERR_INVALID_VALUE if M, N or K < 0, lda < max(1, K),
+ * ldb < max(1, N) or ldc < max(1, N); then, unless M == 0 or N == 0,
+ * SGEMM_ERR_NULL if C is NULL, or if A or B is NULL while alpha != 0 and
+ * K > 0; then SGEMM_ERR_ALIAS if the byte range of C's window overlaps that
+ * of A's or B's window (only when A, B are read). */
+int sgemm_check_args(int M, int N, int K, float alpha, const float *A, int lda,
+                     const float *B, int ldb, float beta, const float *C, int ldc);
+
+/* Synchronize the handle's device, then destroy it and free its device
+ * memory.  SGEMM_ERR_BAD_HANDLE for NULL or an already destroyed handle. */
+int sgemm_destroy(sgemm_handle_t h);
+
+/* Pin a kernel variant for later calls of this handle (SGEMM_VARIANT_AUTO to
+ * let the library choose).  SGEMM_ERR_INVALID_VALUE for an unknown value or
+ * SGEMM_VARIANT_SCALE, which is chosen only by the alpha == 0 / K == 0 rule. */
+int sgemm_set_variant(sgemm_handle_t h, int variant);
+
+/* The variant the handle's last successful sgemm_run enqueued (an
+ * sgemm_variant_t), or -1 if there was none or `h` is not a live handle.
+ * For the split-K variant, *splits (if non-NULL) receives the split count. */
+int sgemm_last_variant(sgemm_handle_t h, int *splits);
+
+/* Wait for the handle's device to finish its work, then read and clear the
+ * handle's device-side status word.  Returns SGEMM_OK, or
+ * SGEMM_ERR_DEVICE_TIMEOUT if any kernel of the handle abandoned a bounded
+ * wait (its output is then undefined), or SGEMM_ERR_CUDA. */
+int sgemm_get_device_status(sgemm_handle_t h);
+
+/* Test hook: enqueue one small kernel that waits on a barrier nothing will
+ * complete, gives up after `limit_ns` nanoseconds (clamped to [1e3, 1e9]),
+ * records SGEMM_ERR_DEVICE_TIMEOUT in the handle's status word and returns.
+ * It exercises the timeout path without faulting or hanging the GPU. */
+int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream);
+
+/* Test hook: when `bytes` > 0, later launches of the handle's TMA variants
+ * request `bytes` of dynamic shared memory instead of their own size, so a
+ * value above the device limit makes the launch fail on the host
+ * (SGEMM_ERR_LAUNCH) before anything runs.  0 restores normal launches. */
+int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
+
+/* Human-readable name of a status value (never NULL). */
+const char *sgemm_status_string(int status);
+
+/* Human-readable name of a variant value (never NULL). */
+const char *sgemm_variant_name(int variant);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_H */

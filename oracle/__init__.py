@@ -136,17 +136,26 @@ def sgemm_f64(M, N, K, alpha, A, lda, B, ldb, beta, C0, ldc0, *, library=None):
 def sgemm_rows(rows, N, K, alpha, A, lda, B, ldb, beta, C0, ldc, *, library=None):
     """Float results of the output rows ``rows`` only, as a (len(rows), N) array.
 
-    Each listed row i is computed exactly as ``sgemm`` would compute it, by
-    calling the oracle on the 1 x K row slice of A and the matching row of C0.
-    This is how outputs of shapes too large for the full oracle are sampled.
+    The listed rows of A (and of C0) are gathered into a contiguous
+    len(rows) x K matrix and passed to the oracle in one call; each output
+    row is computed exactly as a full ``sgemm`` call would compute it (rows
+    are independent).  This is how outputs of shapes too large for the full
+    oracle are sampled.
     """
-    out = np.empty((len(rows), N), dtype=np.float32)
-    for r, i in enumerate(rows):
-        a_row = np.ascontiguousarray(A[i * lda:i * lda + K]) if (alpha != 0 and K > 0) else None
-        c_row = np.ascontiguousarray(C0[i * ldc:i * ldc + N]) if beta != 0 else np.full(N, np.nan, np.float32)
-        sgemm(1, N, K, alpha, a_row, max(K, 1), B, ldb, beta, c_row, max(N, 1), library=library)
-        out[r] = c_row
-    return out
+    rows = [int(i) for i in rows]
+    R = len(rows)
+    reads_ab = alpha != 0 and K > 0
+    a = np.empty((R, max(K, 1)), dtype=np.float32)
+    if reads_ab:
+        for r, i in enumerate(rows):
+            a[r, :K] = A[i * lda:i * lda + K]
+    c = np.full((R, max(N, 1)), np.nan, dtype=np.float32)
+    if beta != 0:
+        for r, i in enumerate(rows):
+            c[r, :N] = C0[i * ldc:i * ldc + N]
+    sgemm(R, N, K, alpha, a.reshape(-1) if reads_ab else None, max(K, 1), B, ldb, beta,
+          c.reshape(-1), max(N, 1), library=library)
+    return c[:, :N]
 
 
 def num_threads(library=None) -> int:

@@ -1,0 +1,122 @@
+"""The C-ABI library on the CPU: it builds for sm_103a, exports every entry
+point include/sgemm.h declares, and its host-only logic (argument checks,
+handle checks, status strings) behaves as documented.  No compute call is
+made here; those are the GPU tests."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dense_fp32_matrix_09_gb300 import build, sgemm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sgemm.h")
+
+OK, NULL_, INVALID, ALIAS = sgemm.OK, sgemm.ERR_NULL, sgemm.ERR_INVALID_VALUE, sgemm.ERR_ALIAS
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return sgemm.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12, names
+    assert set(names) == set(sgemm.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_built_for_sm103a_only():
+    assert "arch=compute_103a,code=sm_103a" in build.GENCODE
+
+
+def test_status_and_variant_strings(lib):
+    for s in range(10):
+        assert sgemm.status_string(s).startswith("SGEMM_")
+    assert sgemm.status_string(99) == "SGEMM_ERR_UNKNOWN"
+    assert sgemm.variant_name(sgemm.VARIANT_TMA_128x256) == "tma_128x256"
+    assert sgemm.sgemm_version() == 10000
+
+
+# Fake, never-dereferenced device addresses (only compared by the checks).
+A0, B0, C0 = 0x10000000, 0x20000000, 0x30000000
+
+
+def chk(M, N, K, alpha=1.0, A=A0, lda=None, B=B0, ldb=None, beta=0.0, C=C0, ldc=None):
+    lda = max(K, 1) if lda is None else lda
+    ldb = max(N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    return sgemm.sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+
+
+def test_check_args_sizes_and_leading_dims(lib):
+    assert chk(4, 5, 6) == OK
+    assert chk(-1, 5, 6) == INVALID
+    assert chk(4, -5, 6) == INVALID
+    assert chk(4, 5, -6) == INVALID
+    assert chk(4, 5, 6, lda=5) == INVALID      # lda < K
+    assert chk(4, 5, 6, ldb=4) == INVALID      # ldb < N
+    assert chk(4, 5, 6, ldc=4) == INVALID      # ldc < N
+    assert chk(4, 5, 0, lda=0) == INVALID      # lda < max(1, K)
+    assert chk(4, 5, 6, lda=7, ldb=9, ldc=8) == OK
+    assert chk(1000, 1500, 777, lda=780, ldb=1504, ldc=1504) == OK
+
+
+def test_check_args_null_rules(lib):
+    assert chk(0, 5, 6, A=None, B=None, C=None) == OK            # M == 0: nothing referenced
+    assert chk(4, 0, 6, A=None, B=None, C=None) == OK
+    assert chk(4, 5, 6, C=None) == NULL_
+    assert chk(4, 5, 6, A=None) == NULL_
+    assert chk(4, 5, 6, B=None) == NULL_
+    assert chk(4, 5, 6, alpha=0.0, A=None, B=None, beta=2.0) == OK  # A, B not referenced
+    assert chk(4, 5, 0, A=None, B=None) == OK
+
+
+def test_check_args_alias(lib):
+    M, N, K = 4, 5, 6
+    # C starting inside A's window
+    assert chk(M, N, K, C=A0 + 8) == ALIAS
+    # C ending exactly where B starts: no overlap
+    c_bytes = ((M - 1) * N + N) * 4
+    assert chk(M, N, K, C=B0 - c_bytes) == OK
+    assert chk(M, N, K, C=B0 - c_bytes + 4) == ALIAS
+    # alpha == 0: A and B are not read, so no aliasing rule applies
+    assert chk(M, N, K, alpha=0.0, C=A0) == OK
+
+
+def test_bad_handles_are_rejected_without_dereference(lib):
+    assert lib.sgemm_run(None, 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_run(ctypes.c_void_p(0x1234), 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == \
+        sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_destroy(None) == sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_destroy(ctypes.c_void_p(0x1234)) == sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_set_variant(None, 1) == sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_last_variant(None, None) == -1
+    assert lib.sgemm_get_device_status(None) == sgemm.ERR_BAD_HANDLE
+    assert lib.sgemm_create(None) == sgemm.ERR_NULL
+
+
+def test_create_without_gpu_reports_unsupported(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p(0xdead)
+    assert lib.sgemm_create(ctypes.byref(h)) == sgemm.ERR_UNSUPPORTED_DEVICE
+    assert h.value is None
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(sgemm, "_lib", None)
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        sgemm.lib()

@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA library (through its C ABI) against the oracle.
+
+Sizes the oracle finishes in seconds are compared element by element; the
+4096^3 and 8192^3 workloads, in the launch configuration the benchmark times
+(automatic variant choice), are compared on sampled rows the oracle computes
+one by one.  Tolerance: max |C_gpu - C_ref| <= 1e-3 for K <= 1024 and <= 1e-2
+for K <= 8192; exact for integer-valued inputs.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from dense_fp32_matrix_09_gb300 import inputs, sgemm
+from tests.gpu_util import (DeviceBuf, check_untouched, max_abs_err, oracle_full, run_gpu,
+                            sample_rows, tolerance)
+
+pytestmark = pytest.mark.gpu
+
+V = sgemm
+TMA_VARIANTS = (V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64,
+                V.VARIANT_TMA_64x64_SPLITK)
+
+
+@pytest.fixture(scope="module")
+def handle():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from dense_fp32_matrix_09_gb300 import build
+    build.build()
+    h = sgemm.sgemm_create()
+    yield h
+    sgemm.sgemm_destroy(h)
+
+
+@pytest.fixture
+def variant(handle, request):
+    """Pin a variant for one test and restore automatic choice afterwards."""
+    def pin(v):
+        sgemm.sgemm_set_variant(handle, v)
+    yield pin
+    sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
+
+
+def _cfg(M, N, K, alpha=1.0, beta=0.0, seed=7, pad=(4, 8, 4), mult4=True):
+    r4 = (lambda x: (x + 3) // 4 * 4) if mult4 else (lambda x: x)
+    lda = r4(max(K, 1)) + pad[0]
+    ldb = r4(max(N, 1)) + pad[1]
+    ldc = r4(max(N, 1)) + pad[2]
+    return inputs.GemmConfig(f"t{M}x{N}x{K}", M, N, K, lda, ldb, ldc, seed, alpha, beta)
+
+
+# ----------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("cfg", inputs.CONFIGS[:2] + inputs.CONFIGS[3:4], ids=lambda c: c.name)
+def test_workload_full_oracle(handle, cfg):
+    prob = inputs.make_problem(cfg)
+    C_gpu, bufs = run_gpu(handle, cfg, prob)
+    C_ref = oracle_full(cfg, prob)
+    err = max_abs_err(cfg, C_gpu, C_ref)
+    assert err <= tolerance(cfg.K), (cfg.name, err, sgemm.sgemm_last_variant(handle))
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("cfg", [inputs.CONFIGS[2], inputs.CONFIGS[4]], ids=lambda c: c.name)
+def test_workload_sampled_rows(handle, cfg):
+    prob = inputs.make_problem(cfg)
+    C_gpu, bufs = run_gpu(handle, cfg, prob)
+    rows = sample_rows(cfg.M)
+    ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
+                            cfg.beta, prob.C0, cfg.ldc)
+    got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows]
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= tolerance(cfg.K), (cfg.name, err)
+    assert np.all(np.isfinite(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)))
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=lambda c: c.name)
+def test_workload_integer_exact(handle, cfg):
+    """Integer entries in [-2, 2]: every partial sum is exact in float32, so
+    the GPU result must equal the oracle bit for bit at every workload shape."""
+    prob = inputs.make_problem(cfg, kind="integer")
+    C_gpu, _ = run_gpu(handle, cfg, prob)
+    if cfg.M * cfg.N * cfg.K <= 1024 ** 3:
+        ref = inputs.dense(oracle_full(cfg, prob), cfg.M, cfg.N, cfg.ldc)
+        got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)
+    else:
+        rows = sample_rows(cfg.M, n_random=8)
+        ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
+                                cfg.beta, prob.C0, cfg.ldc)
+        got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows]
+    assert np.array_equal(np.ascontiguousarray(got).view(np.uint32),
+                          np.ascontiguousarray(ref).view(np.uint32)), cfg.name
+
+
+# ------------------------------------------------------------ shape sweeps
+
+SHAPES = [(1, 1, 1), (1, 5, 3), (7, 13, 5), (31, 33, 17), (64, 64, 32), (65, 63, 31),
+          (128, 256, 32), (129, 257, 33), (127, 255, 100), (200, 300, 260), (256, 256, 256),
+          (100, 7, 513), (3, 700, 64), (333, 129, 1000), (64, 64, 2048)]
+COEFS = [(1.0, 0.0), (1.5, 0.5), (-0.75, 1.0)]
+
+
+@pytest.mark.parametrize("v", V.GEMM_VARIANTS, ids=lambda v: sgemm.variant_name(v))
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_variant_shape_sweep(handle, variant, v, shape):
+    variant(v)
+    M, N, K = shape
+    for i, (alpha, beta) in enumerate(COEFS):
+        cfg = _cfg(M, N, K, alpha, beta, seed=100 + i, mult4=v != V.VARIANT_GENERIC,
+                   pad=(1, 3, 2) if v == V.VARIANT_GENERIC else (4, 8, 4))
+        prob = inputs.make_problem(cfg)
+        C_gpu, bufs = run_gpu(handle, cfg, prob)
+        ran, _ = sgemm.sgemm_last_variant(handle)
+        if v == V.VARIANT_TMA_64x64_SPLITK:
+            assert ran in (V.VARIANT_TMA_64x64_SPLITK, V.VARIANT_TMA_64x64)
+        else:
+            assert ran == v, (ran, v)
+        err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
+        assert err <= tolerance(K), (shape, alpha, beta, err)
+        check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("v", V.GEMM_VARIANTS, ids=lambda v: sgemm.variant_name(v))
+def test_variant_integer_exact(handle, variant, v):
+    variant(v)
+    for shape in [(129, 257, 33), (200, 300, 260), (64, 64, 2048), (1000, 1500, 777)]:
+        cfg = _cfg(*shape, alpha=1.5, beta=0.5, seed=3, mult4=v != V.VARIANT_GENERIC)
+        prob = inputs.make_problem(cfg, kind="integer")
+        C_gpu, _ = run_gpu(handle, cfg, prob)
+        ref = oracle_full(cfg, prob)
+        g = np.ascontiguousarray(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc))
+        r = np.ascontiguousarray(inputs.dense(ref, cfg.M, cfg.N, cfg.ldc))
+        assert np.array_equal(g.view(np.uint32), r.view(np.uint32)), shape
+
+
+def test_splitk_really_splits(handle, variant):
+    variant(V.VARIANT_TMA_64x64_SPLITK)
+    cfg = _cfg(64, 64, 2048, 1.0, 0.0)
+    prob = inputs.make_problem(cfg)
+    C_gpu, _ = run_gpu(handle, cfg, prob)
+    ran, splits = sgemm.sgemm_last_variant(handle)
+    assert ran == V.VARIANT_TMA_64x64_SPLITK and splits > 1
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_alpha_zero_and_k_zero_quick_path(handle):
+    cfg = _cfg(37, 45, 19, alpha=0.0, beta=0.5)
+    prob = inputs.make_problem(cfg)
+    prob.A[:] = np.nan  # not read
+    prob.B[:] = np.nan
+    C_gpu, bufs = run_gpu(handle, cfg, prob)
+    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_SCALE
+    want = prob.C0.copy()
+    oracle.sgemm(cfg.M, cfg.N, cfg.K, 0.0, None, cfg.lda, None, cfg.ldb, 0.5, want, cfg.ldc)
+    g = np.ascontiguousarray(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc))
+    w = np.ascontiguousarray(inputs.dense(want, cfg.M, cfg.N, cfg.ldc))
+    assert np.array_equal(g.view(np.uint32), w.view(np.uint32))
+    check_untouched(cfg, prob, C_gpu, bufs)
+    # beta == 0 as well: exact zeros, C (NaN-filled) not read
+    cfg0 = _cfg(37, 45, 0, alpha=1.0, beta=0.0)
+    prob0 = inputs.make_problem(cfg0)
+    C0, _ = run_gpu(handle, cfg0, prob0)
+    assert np.all(inputs.dense(C0, cfg0.M, cfg0.N, cfg0.ldc) == 0)
+
+
+def test_beta_zero_output_only_c(handle):
+    cfg = _cfg(130, 260, 70, alpha=1.0, beta=0.0)
+    prob = inputs.make_problem(cfg)   # C0 is all NaN sentinel
+    assert np.all(np.isnan(prob.C0))
+    C_gpu, _ = run_gpu(handle, cfg, prob)
+    assert np.all(np.isfinite(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)))
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+
+
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (1, 1, 1)])
+def test_unaligned_pointers(handle, offsets):
+    """Operands that TMA cannot describe take the generic GPU variant; an
+    unaligned C takes the scalar epilogue.  Never a CPU path."""
+    cfg = _cfg(150, 170, 90, 1.5, 0.5)
+    prob = inputs.make_problem(cfg)
+    C_gpu, bufs = run_gpu(handle, cfg, prob, offsets=offsets)
+    ran = sgemm.sgemm_last_variant(handle)[0]
+    if offsets[0] or offsets[1]:
+        assert ran == V.VARIANT_GENERIC
+    else:
+        assert ran != V.VARIANT_GENERIC
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+def test_odd_leading_dims_use_generic(handle):
+    cfg = inputs.GemmConfig("odd_ld", 77, 99, 55, 57, 101, 103, 5, 1.0, 1.0)
+    prob = inputs.make_problem(cfg)
+    C_gpu, bufs = run_gpu(handle, cfg, prob)
+    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_GENERIC
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("v", V.GEMM_VARIANTS, ids=lambda v: sgemm.variant_name(v))
+def test_deterministic_repeat(handle, variant, v):
+    """Same inputs, same variant: bit-identical results (a race between
+    threads or CTAs would show up as run-to-run differences)."""
+    import torch
+    variant(v)
+    cfg = _cfg(300, 500, 1200, 1.0, 0.0, mult4=True)
+    prob = inputs.make_problem(cfg)
+    dA, dB = DeviceBuf(prob.A), DeviceBuf(prob.B)
+    outs = []
+    for _ in range(3):
+        dC = DeviceBuf(prob.C0)
+        sgemm.sgemm_run(handle, cfg.M, cfg.N, cfg.K, 1.0, dA.ptr, cfg.lda, dB.ptr, cfg.ldb, 0.0,
+                        dC.ptr, cfg.ldc)
+        torch.cuda.synchronize()
+        outs.append(dC.interior().view(np.uint32).copy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_empty_problems_are_noops(handle):
+    import torch
+    c = DeviceBuf(np.full(16, 3.0, np.float32))
+    sgemm.sgemm_run(handle, 0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4)
+    sgemm.sgemm_run(handle, 4, 0, 4, 1.0, None, 4, None, 1, 0.0, c.ptr, 1)
+    torch.cuda.synchronize()
+    assert np.all(c.interior() == 3.0) and c.guards_intact()
+
+
+def test_alias_is_rejected_and_c_unchanged(handle):
+    import torch
+    buf = DeviceBuf(np.ones(64 * 64, np.float32))
+    with pytest.raises(sgemm.SgemmError) as e:
+        sgemm.sgemm_run(handle, 32, 32, 32, 1.0, buf.ptr, 32, buf.ptr + 4 * 32 * 32, 32, 0.0, buf.ptr, 32)
+    assert e.value.status == V.ERR_ALIAS
+    torch.cuda.synchronize()
+    assert np.all(buf.interior() == 1.0)
+
+
+def test_nondefault_stream(handle):
+    import torch
+    cfg = _cfg(257, 129, 300, 1.0, 1.0)
+    prob = inputs.make_problem(cfg)
+    dA, dB, dC = DeviceBuf(prob.A), DeviceBuf(prob.B), DeviceBuf(prob.C0)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        sgemm.sgemm_run(handle, cfg.M, cfg.N, cfg.K, 1.0, dA.ptr, cfg.lda, dB.ptr, cfg.ldb, 1.0,
+                        dC.ptr, cfg.ldc)   # stream=None -> torch's current stream (s)
+    s.synchronize()
+    assert max_abs_err(cfg, dC.interior(), oracle_full(cfg, prob)) <= tolerance(cfg.K)
+
+
+# ------------------------------------------------- failure reporting (no fault)
+
+def test_device_timeout_is_reported_and_recoverable(handle):
+    """A kernel whose wait can never complete gives up after 1 ms, records the
+    timeout in the handle's status word and returns; the context stays usable."""
+    assert sgemm.sgemm_get_device_status(handle) == V.OK
+    sgemm.sgemm_debug_timeout_probe(handle, 1_000_000)
+    assert sgemm.sgemm_get_device_status(handle) == V.ERR_DEVICE_TIMEOUT
+    assert sgemm.sgemm_get_device_status(handle) == V.OK   # read clears it
+    cfg = _cfg(65, 65, 65, 1.0, 0.0)
+    prob = inputs.make_problem(cfg)
+    C_gpu, _ = run_gpu(handle, cfg, prob)
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+
+
+def test_launch_failure_is_reported_on_the_host(handle, variant):
+    """Requesting more shared memory than an SM has makes the launch fail on
+    the host before anything runs; C is untouched and later calls work."""
+    import torch
+    variant(V.VARIANT_TMA_128x128)
+    cfg = _cfg(128, 128, 64, 1.0, 0.0)
+    prob = inputs.make_problem(cfg)
+    dA, dB, dC = DeviceBuf(prob.A), DeviceBuf(prob.B), DeviceBuf(prob.C0)
+    sgemm.sgemm_debug_set_smem_override(handle, 1 << 20)
+    try:
+        with pytest.raises(sgemm.SgemmError) as e:
+            sgemm.sgemm_run(handle, cfg.M, cfg.N, cfg.K, 1.0, dA.ptr, cfg.lda, dB.ptr, cfg.ldb, 0.0,
+                            dC.ptr, cfg.ldc)
+        assert e.value.status == V.ERR_LAUNCH
+    finally:
+        sgemm.sgemm_debug_set_smem_override(handle, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(dC.interior().view(np.uint32), prob.C0.view(np.uint32))
+    C_gpu, _ = run_gpu(handle, cfg, prob)
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK
+
+
+def test_torch_tensor_interface(handle):
+    import torch
+    g = torch.Generator().manual_seed(5)
+    A = (torch.rand(96, 80, generator=g) * 2 - 1).cuda()
+    B = (torch.rand(80, 112, generator=g) * 2 - 1).cuda()
+    C = torch.empty(96, 112, device="cuda")
+    with sgemm.Sgemm() as s:
+        s.matmul(A, B, C)
+    torch.cuda.synchronize()
+    a, b = A.cpu().numpy().reshape(-1), B.cpu().numpy().reshape(-1)
+    ref = np.full(96 * 112, np.nan, np.float32)
+    oracle.sgemm(96, 112, 80, 1.0, a, 80, b, 112, 0.0, ref, 112)
+    assert float(np.max(np.abs(C.cpu().numpy().reshape(-1) - ref))) <= 1e-3
