@@ -57,7 +57,9 @@ def parse():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
-    p.add_argument("--workload", default=None, help="workload name (default: the 8192^3 case)")
+    p.add_argument("--workload", default=None,
+                   help="workload name, or MxNxK for an ad-hoc alpha=1 beta=0 problem (default: 8192^3)")
+    p.add_argument("--variant", default="auto", help="pin a kernel variant by name (default: auto)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
@@ -258,7 +260,13 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     from dense_fp32_matrix_09_gb300 import inputs
-    cfg = inputs.CONFIG_BY_NAME[args.workload] if args.workload else inputs.HEADLINE
+    if args.workload and args.workload in inputs.CONFIG_BY_NAME:
+        cfg = inputs.CONFIG_BY_NAME[args.workload]
+    elif args.workload:
+        M, N, K = (int(x) for x in args.workload.lower().split("x"))
+        cfg = inputs.GemmConfig(f"sgemm_{M}x{N}x{K}", M, N, K, K, N, N, 0, 1.0, 0.0)
+    else:
+        cfg = inputs.HEADLINE
 
     if args.impl == "reference":
         reference_arm(args, cfg, rank, world)
@@ -281,6 +289,9 @@ def main():
             dist.barrier()
 
     h = sg.sgemm_create()
+    if args.variant != "auto":
+        names = {sg.variant_name(v): v for v in sg.GEMM_VARIANTS}
+        sg.sgemm_set_variant(h, names[args.variant])
     prob = inputs.make_problem(cfg)
     A = torch.from_numpy(prob.A).cuda()
     B = torch.from_numpy(prob.B).cuda()
