@@ -145,6 +145,7 @@ const char *sgemm_status_string(int s) {
         case SGEMM_ERR_CUDA: return "SGEMM_ERR_CUDA: CUDA runtime error";
         case SGEMM_ERR_DEVICE_TIMEOUT: return "SGEMM_ERR_DEVICE_TIMEOUT: a kernel abandoned a bounded wait";
         case SGEMM_ERR_WRONG_DEVICE: return "SGEMM_ERR_WRONG_DEVICE: current device differs from the handle's";
+        case SGEMM_ERR_SCRATCH_TOO_SMALL: return "SGEMM_ERR_SCRATCH_TOO_SMALL: more than 512 64x64 output tiles for sgemm_run_noalloc";
         default: return "SGEMM_ERR_UNKNOWN";
     }
 }

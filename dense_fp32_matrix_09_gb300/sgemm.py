@@ -24,6 +24,7 @@ ERR_LAUNCH = 6
 ERR_CUDA = 7
 ERR_DEVICE_TIMEOUT = 8
 ERR_WRONG_DEVICE = 9
+ERR_SCRATCH_TOO_SMALL = 10
 
 VARIANT_AUTO = 0
 VARIANT_TMA_128x256 = 1
@@ -39,7 +40,7 @@ GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
-           "sgemm_version")
+           "sgemm_version", "sgemm_run_noalloc")
 
 
 class SgemmError(RuntimeError):
@@ -78,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_variant_name.argtypes = [i32]
         L.sgemm_variant_name.restype = ctypes.c_char_p
         L.sgemm_version.argtypes = []
+        L.sgemm_run_noalloc.argtypes = [i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         _lib = L
     return _lib
 
@@ -131,6 +133,15 @@ def sgemm_run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> N
     """C <- alpha*A*B + beta*C on device buffers (row-major, leading dims)."""
     _check(lib().sgemm_run(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
                            int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream)), "sgemm_run")
+
+
+def sgemm_run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """C <- alpha*A*B + beta*C without allocating anything (no handle; fixed
+    in-library scratch, at most 512 output tiles of 64 x 64).  For callers that
+    cannot allocate GPU memory; see include/sgemm.h for the sharing rules."""
+    _check(lib().sgemm_run_noalloc(int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
+                                   int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream)),
+           "sgemm_run_noalloc")
 
 
 def sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:

@@ -62,7 +62,8 @@ typedef enum {
     SGEMM_ERR_LAUNCH = 6,             /* the kernel launch was rejected                */
     SGEMM_ERR_CUDA = 7,               /* another CUDA runtime error                    */
     SGEMM_ERR_DEVICE_TIMEOUT = 8,     /* a kernel gave up a bounded wait (device side) */
-    SGEMM_ERR_WRONG_DEVICE = 9        /* current device differs from the handle's      */
+    SGEMM_ERR_WRONG_DEVICE = 9,       /* current device differs from the handle's      */
+    SGEMM_ERR_SCRATCH_TOO_SMALL = 10  /* sgemm_run_noalloc: problem exceeds its scratch */
 } sgemm_status_t;
 
 /* Kernel variants.  SGEMM_VARIANT_AUTO lets sgemm_run choose from the shape
@@ -136,6 +137,30 @@ int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream
  * value above the device limit makes the launch fail on the host
  * (SGEMM_ERR_LAUNCH) before anything runs.  0 restores normal launches. */
 int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
+
+/* C <- alpha*A*B + beta*C without allocating anything, for callers that cannot
+ * allocate GPU memory (allocator implementations that must not re-enter the
+ * allocator, frameworks whose allocator has reserved the device memory, hosts
+ * that forbid device allocation after start-up).  The pages have no
+ * counterpart: this is a deployment convenience, not part of the method.
+ *
+ * Same arguments, rules and results as sgemm_run, but no handle: it runs the
+ * 64 x 64 split-K kernel with its partial tiles, tile counters and status word
+ * in a fixed scratch array compiled into the library (8 MiB + 4 KiB + 256 B,
+ * held on every GPU that loads the library until the process exits).
+ * Limit: at most 512 output tiles of 64 x 64, i.e. ceil(M/64)*ceil(N/64) <= 512;
+ * larger problems return SGEMM_ERR_SCRATCH_TOO_SMALL and enqueue nothing.
+ * alpha == 0 or K == 0, and operands TMA cannot describe, take the same
+ * scratch-free kernels as sgemm_run.  It calls no cudaMalloc or cudaFree.
+ * All calls share the scratch and it keeps the last call's contents: each call
+ * clears the counters and status word it uses on `stream` first, and calls that
+ * overlap on the GPU (unordered streams) race and give wrong results.  The
+ * first call on a device, with that device current, looks up the scratch's
+ * device address and sets the kernel up; make that first call before any
+ * stream capture.  A device-side timeout leaves C unwritten and cannot be
+ * reported by this entry point. */
+int sgemm_run_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
+                      const float *B, int ldb, float beta, float *C, int ldc, void *stream);
 
 /* Human-readable name of a status value (never NULL). */
 const char *sgemm_status_string(int status);
