@@ -30,7 +30,10 @@
 //  * Consumer warps are arranged WARPS_M x WARPS_N; each lane owns a TM x TN
 //    register block (rows strided by the lanes along M, columns as float4
 //    groups strided by the lanes along N) and performs TM*TN independent
-//    FFMA chains per k.
+//    FMA chains per k.  The FMAs are issued as packed FP32x2 FMAs
+//    (__ffma2_rn: A value broadcast to both halves, two adjacent B columns):
+//    two FMAs per instruction halve the issue slots the FMA pipe needs, which
+//    is what lets the pipe, rather than instruction issue, bound the loop.
 //  * Epilogue: C = alpha*acc + beta*C with float4 accesses when C is 16-byte
 //    aligned and ldc % 4 == 0 (scalar at the ragged N edge); C is not read
 //    when beta == 0.
@@ -71,8 +74,11 @@ struct Cfg {
     static_assert(BM <= 256 && BN <= 256, "TMA box extents are at most 256");
 };
 
+// Tile rows per raster group (see tile_coords).
+constexpr int kGroupM = 8;
+
 using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
-using CfgM = Cfg<128, 128, 2, 4, 8, 8, 4, 1>;    // SGEMM_VARIANT_TMA_128x128
+using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
 using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 2>;      // SGEMM_VARIANT_TMA_64x64 (+ split-K)
 
 template <class C>
@@ -113,10 +119,25 @@ __device__ __forceinline__ void epilogue(float (&acc)[C::TM][C::TN], const GemmA
     }
 }
 
+// Grouped tile order: CTA `pid` of a 1-D grid works on output tile (tm, tn).
+// Tiles are taken in groups of `group_m` tile rows, walking down the rows of
+// a group first, so the CTAs resident at one time cover a compact block of C
+// and share A row-panels and B column-panels in L2.
+__device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, int group_m, int &tm,
+                                            int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int grp = pid / per_group;
+    const int first_m = grp * group_m;
+    const int rows = min(tiles_m - first_m, group_m);
+    const int r = pid - grp * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
 template <class C, bool SPLIT>
 __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const GemmArgs g, const SplitK sk) {
+                 const GemmArgs g, const SplitK sk, const int group_m) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B.
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -128,7 +149,10 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.y * C::BM, n0 = blockIdx.x * C::BN;
+    const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
+    int tm, tn;
+    tile_coords(blockIdx.x, tiles_m, tiles_n, group_m, tm, tn);
+    const int m0 = tm * C::BM, n0 = tn * C::BN;
     const int k_tiles = (g.K + C::BK - 1) / C::BK;
     int kt0 = 0, nkt = k_tiles;
     if (SPLIT) {
@@ -209,12 +233,19 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 #pragma unroll
                 for (int ii = 0; ii < C::TM; ++ii) {
                     const float av = kk == 0 ? a[ii].x : kk == 1 ? a[ii].y : kk == 2 ? a[ii].z : a[ii].w;
+                    const float2 a2 = make_float2(av, av);
 #pragma unroll
                     for (int jj = 0; jj < C::TN4; ++jj) {
-                        acc[ii][4 * jj + 0] = fmaf(av, b[jj].x, acc[ii][4 * jj + 0]);
-                        acc[ii][4 * jj + 1] = fmaf(av, b[jj].y, acc[ii][4 * jj + 1]);
-                        acc[ii][4 * jj + 2] = fmaf(av, b[jj].z, acc[ii][4 * jj + 2]);
-                        acc[ii][4 * jj + 3] = fmaf(av, b[jj].w, acc[ii][4 * jj + 3]);
+                        // packed FP32x2 FMA: two independent round-to-nearest FMAs
+                        // per instruction (the same results as two fmaf calls)
+                        const float2 lo = __ffma2_rn(a2, make_float2(b[jj].x, b[jj].y),
+                                                     make_float2(acc[ii][4 * jj + 0], acc[ii][4 * jj + 1]));
+                        const float2 hi = __ffma2_rn(a2, make_float2(b[jj].z, b[jj].w),
+                                                     make_float2(acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
+                        acc[ii][4 * jj + 0] = lo.x;
+                        acc[ii][4 * jj + 1] = lo.y;
+                        acc[ii][4 * jj + 2] = hi.x;
+                        acc[ii][4 * jj + 3] = hi.y;
                     }
                 }
             }
@@ -237,7 +268,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // All consumers reach this barrier (every wait above is bounded), so an
     // abort by any of them is seen by all and the tile is left untouched.
     if (named_barrier_or(1, C::kConsumers, aborted)) return;
-    const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+    const int tile = blockIdx.x;
     constexpr int kQ = C::TM * C::TN4;  // float4 groups per thread
     float *part = sk.ws + (static_cast<size_t>(tile) * sk.splits) * (C::BM * C::BN);
     {
@@ -300,9 +331,10 @@ cudaError_t prepare_one() {
 template <class C, bool SPLIT>
 cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const SplitK &sk, int smem_override, cudaStream_t stream) {
-    const dim3 grid((g.N + C::BN - 1) / C::BN, (g.M + C::BM - 1) / C::BM, SPLIT ? sk.splits : 1);
+    const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
+    const dim3 grid(tiles, 1, SPLIT ? sk.splits : 1);
     const int smem = smem_override > 0 ? smem_override : C::kSmemBytes;
-    sgemm_tma_kernel<C, SPLIT><<<grid, C::kThreads, smem, stream>>>(tmA, tmB, g, sk);
+    sgemm_tma_kernel<C, SPLIT><<<grid, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
     return cudaGetLastError();
 }
 
