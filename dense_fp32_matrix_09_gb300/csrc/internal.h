@@ -34,17 +34,23 @@ struct TmaShape {
     int min_ctas_per_sm;
 };
 
-// Split-K bookkeeping (only for the split-K variant).
+// Split-K bookkeeping.  Tiles [0, dp_tiles) (in raster order) are computed
+// whole by one CTA each; every later tile is split into `splits` K ranges
+// computed by separate CTAs and summed by the last of them to finish.
+// splits == 1 means no tile is split (ws and counters unused).
 struct SplitK {
-    int splits;             // number of K ranges (CTAs per output tile)
+    int splits;             // number of K ranges per split tile
     int k_tiles_per_split;  // K steps of bk per range
-    float *ws;              // splits * tiles * bm * bn partial sums
-    int *counters;          // one arrival counter per output tile, zero between calls
+    float *ws;              // (tiles - dp_tiles) * splits * bm * bn partial sums
+    int *counters;          // one arrival counter per split tile, zero between calls
+    int dp_tiles;           // leading tiles computed whole (0: every tile is split)
 };
 
 // variant ids are the public sgemm_variant_t values of the TMA variants
 bool tma_shape(int variant, TmaShape *out);
 cudaError_t tma_prepare(int variant);
+// Resident CTAs per SM of a variant's kernel (0 on error).
+int tma_ctas_per_sm(int variant);
 cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA,
                        const CUtensorMap &tmB, const SplitK &sk, int smem_override,
                        cudaStream_t stream);

@@ -3,6 +3,7 @@
 // descriptors.  Every computation is done by the kernels in sgemm_tma.cu and
 // sgemm_aux.cu; this file only validates, chooses and launches.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -29,6 +30,7 @@ struct sgemm_ctx {
     int last_variant;
     int last_splits;
     int smem_override;
+    int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
 };
 
 namespace {
@@ -94,22 +96,6 @@ bool encode_2d(CUtensorMap *map, const float *base, int rows, int cols, int ld, 
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Variant for a TMA-eligible call: 128 x 128 tiles (two CTAs per SM) when
-// there is at least one per SM, 64 x 64 tiles when there are not, split-K when
-// even 64 x 64 tiles leave most SMs idle and K is long enough to split.  (The
-// 128 x 256 variant measured no faster at any shape; it stays for pinning.)
-int choose_variant(const sgemm_ctx *h, int M, int N, int K) {
-    const int sms = h->num_sms;
-    const long long tL = 1LL * cdiv(M, 128) * cdiv(N, 256);
-    const long long tM = 1LL * cdiv(M, 128) * cdiv(N, 128);
-    const long long tS = 1LL * cdiv(M, 64) * cdiv(N, 64);
-    const int k_tiles = cdiv(K, 32);
-    (void)tL;
-    if (tM >= sms) return SGEMM_VARIANT_TMA_128x128;
-    if (tS >= sms || k_tiles < 4) return SGEMM_VARIANT_TMA_64x64;
-    return SGEMM_VARIANT_TMA_64x64_SPLITK;
-}
-
 // Split count for the split-K variant: enough CTAs for two per SM, at least
 // one K step per split, and the partial tiles must fit the workspace.
 void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
@@ -126,6 +112,78 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     sk->splits = cdiv(k_tiles, kps);
     sk->ws = h->d_ws;
     sk->counters = h->d_counters;
+    sk->dp_tiles = 0;
+}
+
+// Tail plan for the whole-tile variants.  With T tiles and P resident CTA
+// slots, T = full*P + rem: the first full*P tiles run whole (complete waves)
+// and the rem tiles of the last, partly empty wave are split along K into S
+// ranges, S = P / rem (so the tail fills the slots), at least 2 K steps per
+// range and at most 8 ranges, within the workspace and counter capacity.
+// Without this the last wave runs rem whole tiles on a mostly idle GPU.
+void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K,
+               sg::SplitK *sk) {
+    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn);
+    const int k_tiles = cdiv(K, sh.bk);
+    *sk = sg::SplitK{1, k_tiles, nullptr, nullptr, static_cast<int>(tiles)};
+    const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[variant]);
+    const long long full = tiles / slots, rem = tiles - full * slots;
+    if (rem == 0 || rem > h->n_counters) return;
+    long long S = std::min<long long>(slots / rem, 8);
+    S = std::min<long long>(S, k_tiles / 2);
+    S = std::min<long long>(S, static_cast<long long>(h->ws_floats / (rem * sh.bm * sh.bn)));
+    if (S < 2) return;
+    const int kps = cdiv(k_tiles, static_cast<int>(S));
+    sk->splits = cdiv(k_tiles, kps);
+    sk->k_tiles_per_split = kps;
+    sk->ws = h->d_ws;
+    sk->counters = h->d_counters;
+    sk->dp_tiles = static_cast<int>(full * slots);
+    if (sk->splits < 2) *sk = sg::SplitK{1, k_tiles, nullptr, nullptr, static_cast<int>(tiles)};
+}
+
+// Estimated cost of running the call with `variant` (arbitrary units, lower
+// is better): the FLOP of one tile times the CTA slots the call occupies,
+// divided by the variant's main-loop efficiency measured on GB300 (fraction
+// of FP32 peak with the GPU full: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
+// 0.73).  Complete waves occupy all P = SMs x CTAs-per-SM slots; a split
+// tail of S ranges occupies P / S; an unsplit partial wave occupies P.  The
+// split-K variant runs tiles x splits CTAs of 1/splits of a tile each.
+double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, sg::SplitK *plan) {
+    sg::TmaShape sh;
+    if (!sg::tma_shape(variant, &sh)) return 1e300;
+    const double eff = variant == SGEMM_VARIANT_TMA_128x256 ? 0.81
+                     : variant == SGEMM_VARIANT_TMA_128x128 ? 0.80 : 0.73;
+    const double P = static_cast<double>(h->num_sms) * std::max(1, h->ctas_per_sm[variant]);
+    const double tile_flop = 2.0 * sh.bm * sh.bn * static_cast<double>(K);
+    const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn);
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+        plan_splits(h, M, N, K, plan);
+        const double ctas = tiles * plan->splits;
+        return tile_flop / plan->splits * std::ceil(ctas / P) * P / eff;
+    }
+    sg::TmaShape shape = sh;
+    plan_tail(h, variant, shape, M, N, K, plan);
+    const double full = std::floor(tiles / P), rem = tiles - full * P;
+    const double tail = rem == 0 ? 0.0 : (plan->splits >= 2 ? P / plan->splits : P);
+    return tile_flop * (full * P + tail) / eff;
+}
+
+// Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
+// larger tile (listed first).
+int choose_variant(const sgemm_ctx *h, int M, int N, int K) {
+    int best = SGEMM_VARIANT_TMA_128x256;
+    double best_cost = 1e300;
+    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
+                  SGEMM_VARIANT_TMA_64x64_SPLITK}) {
+        sg::SplitK plan;
+        const double c = variant_cost(h, v, M, N, K, &plan);
+        if (c < best_cost * 0.999) {
+            best_cost = c;
+            best = v;
+        }
+    }
+    return best;
 }
 
 }  // namespace
@@ -194,9 +252,13 @@ int sgemm_create(sgemm_handle_t *out) {
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     if (prop.major != 10 || prop.minor != 3) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!load_encoder()) return SGEMM_ERR_CUDA;
+    int occupancy[SGEMM_VARIANT_COUNT_] = {};
     for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
-                  SGEMM_VARIANT_TMA_64x64_SPLITK})
+                  SGEMM_VARIANT_TMA_64x64_SPLITK}) {
         if (sg::tma_prepare(v) != cudaSuccess) return SGEMM_ERR_CUDA;
+        occupancy[v] = sg::tma_ctas_per_sm(v);
+        if (occupancy[v] < 1) return SGEMM_ERR_CUDA;
+    }
 
     sgemm_ctx *h = new (std::nothrow) sgemm_ctx();
     if (!h) return SGEMM_ERR_CUDA;
@@ -205,6 +267,7 @@ int sgemm_create(sgemm_handle_t *out) {
     h->ws_floats = kWorkspaceBytes / sizeof(float);
     h->n_counters = kCounters;
     h->last_variant = -1;
+    for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) h->ctas_per_sm[v] = occupancy[v];
     bool ok = cudaMalloc(&h->d_status, sizeof(int)) == cudaSuccess &&
               cudaMalloc(&h->d_ws, kWorkspaceBytes) == cudaSuccess &&
               cudaMalloc(&h->d_counters, kCounters * sizeof(int)) == cudaSuccess &&
@@ -298,14 +361,12 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
 
     sg::TmaShape sh;
     if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
-    sg::SplitK sk{1, cdiv(K, sh.bk), nullptr, nullptr};
+    sg::SplitK sk{1, cdiv(K, sh.bk), nullptr, nullptr, 0};
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
         plan_splits(h, M, N, K, &sk);
-        if (sk.splits <= 1) {
-            variant = SGEMM_VARIANT_TMA_64x64;
-            sk = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr};
-        }
+        if (sk.splits <= 1) variant = SGEMM_VARIANT_TMA_64x64;
     }
+    if (variant != SGEMM_VARIANT_TMA_64x64_SPLITK) plan_tail(h, variant, sh, M, N, K, &sk);
     CUtensorMap tmA, tmB;
     if (!encode_2d(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmB, B, K, N, ldb, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE))

@@ -150,13 +150,22 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
-    int tm, tn;
-    tile_coords(blockIdx.x, tiles_m, tiles_n, group_m, tm, tn);
-    const int m0 = tm * C::BM, n0 = tn * C::BN;
     const int k_tiles = (g.K + C::BK - 1) / C::BK;
+    // CTAs [0, dp_tiles) take whole tiles; the rest take one of `splits` K
+    // ranges of the remaining tiles (split index z).
+    int tile = blockIdx.x, z = 0, nsplit = 1;
+    if (SPLIT && tile >= sk.dp_tiles) {
+        const int q = tile - sk.dp_tiles;
+        tile = sk.dp_tiles + q / sk.splits;
+        z = q % sk.splits;
+        nsplit = sk.splits;
+    }
+    int tm, tn;
+    tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+    const int m0 = tm * C::BM, n0 = tn * C::BN;
     int kt0 = 0, nkt = k_tiles;
-    if (SPLIT) {
-        kt0 = blockIdx.z * sk.k_tiles_per_split;
+    if (nsplit > 1) {
+        kt0 = z * sk.k_tiles_per_split;
         nkt = min(k_tiles - kt0, sk.k_tiles_per_split);  // >= 1: the host sizes the splits
     }
 
@@ -259,61 +268,56 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int t = max(0, issued - C::STAGES); t < issued; ++t)
             mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
     }
-    if (!SPLIT) {
+    if (nsplit == 1) {  // uniform per CTA
         if (!aborted) epilogue<C>(acc, g, m0, n0, wm, wn, lane_m, lane_n);
         return;
     }
 
     // ------------------------------------------------------- split-K tail
-    // All consumers reach this barrier (every wait above is bounded), so an
+    // All threads reach this barrier (every wait above is bounded), so an
     // abort by any of them is seen by all and the tile is left untouched.
     if (named_barrier_or(1, C::kConsumers, aborted)) return;
-    const int tile = blockIdx.x;
-    constexpr int kQ = C::TM * C::TN4;  // float4 groups per thread
-    float *part = sk.ws + (static_cast<size_t>(tile) * sk.splits) * (C::BM * C::BN);
+    const int slot = tile - sk.dp_tiles;  // index among the split tiles
+    constexpr int kQ = C::TM * C::TN4;    // float4 groups per thread
+    constexpr size_t kTileFloats = static_cast<size_t>(C::BM) * C::BN;
+    const float4 *part = reinterpret_cast<const float4 *>(sk.ws + static_cast<size_t>(slot) * nsplit * kTileFloats);
     {
-        float *mine = part + static_cast<size_t>(blockIdx.z) * (C::BM * C::BN);
+        // partial tile of split z, thread-major: float4 group q of thread t at [q * threads + t]
+        float4 *mine = reinterpret_cast<float4 *>(sk.ws + (static_cast<size_t>(slot) * nsplit + z) * kTileFloats);
 #pragma unroll
         for (int q = 0; q < kQ; ++q) {
             const int ii = q / C::TN4, jj = q % C::TN4;
-            __stcg(reinterpret_cast<float4 *>(mine) + q * C::kConsumers + tid,
-                   make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1], acc[ii][4 * jj + 2],
-                               acc[ii][4 * jj + 3]));
+            __stcg(mine + q * C::kConsumers + tid, make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1],
+                                                               acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
         }
     }
     __threadfence();
     named_barrier_sync(1, C::kConsumers);
     if (tid == 0) {
-        const int prev = atomicAdd(&sk.counters[tile], 1);
-        *s_flag = (prev == sk.splits - 1);
+        const int prev = atomicAdd(&sk.counters[slot], 1);
+        *s_flag = (prev == nsplit - 1);
     }
     named_barrier_sync(1, C::kConsumers);
     if (!*s_flag) return;
     __threadfence();
-    // Last CTA of this tile: sum the partials in ascending split order.
+    // Last CTA of this tile: sum all partials (its own read back too) in
+    // ascending split order, so the result does not depend on arrival order.
+    for (int zz = 0; zz < nsplit; ++zz) {
+        const float4 *pz = part + static_cast<size_t>(zz) * (kTileFloats / 4);
 #pragma unroll
-    for (int q = 0; q < kQ; ++q) {
-        const int ii = q / C::TN4, jj = q % C::TN4;
-        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int z = 0; z < sk.splits; ++z) {
-            float4 p;
-            if (z == static_cast<int>(blockIdx.z))
-                p = make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1], acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]);
-            else
-                p = __ldcg(reinterpret_cast<const float4 *>(part + static_cast<size_t>(z) * (C::BM * C::BN)) +
-                           q * C::kConsumers + tid);
-            if (z == 0) {
-                t = p;
+        for (int q = 0; q < kQ; ++q) {
+            const int ii = q / C::TN4, jj = q % C::TN4;
+            const float4 p = __ldcg(pz + q * C::kConsumers + tid);
+            if (zz == 0) {
+                acc[ii][4 * jj] = p.x; acc[ii][4 * jj + 1] = p.y;
+                acc[ii][4 * jj + 2] = p.z; acc[ii][4 * jj + 3] = p.w;
             } else {
-                t.x += p.x; t.y += p.y; t.z += p.z; t.w += p.w;
+                acc[ii][4 * jj] += p.x; acc[ii][4 * jj + 1] += p.y;
+                acc[ii][4 * jj + 2] += p.z; acc[ii][4 * jj + 3] += p.w;
             }
         }
-        acc[ii][4 * jj] = t.x;
-        acc[ii][4 * jj + 1] = t.y;
-        acc[ii][4 * jj + 2] = t.z;
-        acc[ii][4 * jj + 3] = t.w;
     }
-    if (tid == 0) sk.counters[tile] = 0;  // ready for the next call
+    if (tid == 0) sk.counters[slot] = 0;  // ready for the next call
     epilogue<C>(acc, g, m0, n0, wm, wn, lane_m, lane_n);
 }
 
@@ -322,19 +326,37 @@ TmaShape shape_of() {
     return TmaShape{C::BM, C::BN, C::BK, C::kThreads, C::kSmemBytes, C::MIN_CTAS};
 }
 
-template <class C, bool SPLIT>
+template <class C>
 cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(sgemm_tma_kernel<C, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tma_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 C::kSmemBytes);
 }
 
-template <class C, bool SPLIT>
+template <class C>
+int ctas_per_sm_one() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm_tma_kernel<C, false>, C::kThreads,
+                                                      C::kSmemBytes) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Whole tiles only when sk.splits == 1; otherwise the hybrid grid: dp_tiles
+// whole-tile CTAs, then `splits` CTAs for each remaining tile.
+template <class C>
 cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const SplitK &sk, int smem_override, cudaStream_t stream) {
     const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
-    const dim3 grid(tiles, 1, SPLIT ? sk.splits : 1);
     const int smem = smem_override > 0 ? smem_override : C::kSmemBytes;
-    sgemm_tma_kernel<C, SPLIT><<<grid, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+    if (sk.splits <= 1) {
+        sgemm_tma_kernel<C, false><<<tiles, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+    } else {
+        const int ctas = sk.dp_tiles + (tiles - sk.dp_tiles) * sk.splits;
+        sgemm_tma_kernel<C, true><<<ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+    }
     return cudaGetLastError();
 }
 
@@ -352,21 +374,31 @@ bool tma_shape(int variant, TmaShape *out) {
 
 cudaError_t tma_prepare(int variant) {
     switch (variant) {
-        case SGEMM_VARIANT_TMA_128x256: return prepare_one<CfgL, false>();
-        case SGEMM_VARIANT_TMA_128x128: return prepare_one<CfgM, false>();
-        case SGEMM_VARIANT_TMA_64x64: return prepare_one<CfgS, false>();
-        case SGEMM_VARIANT_TMA_64x64_SPLITK: return prepare_one<CfgS, true>();
+        case SGEMM_VARIANT_TMA_128x256: return prepare_one<CfgL>();
+        case SGEMM_VARIANT_TMA_128x128: return prepare_one<CfgM>();
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return prepare_one<CfgS>();
         default: return cudaErrorInvalidValue;
+    }
+}
+
+int tma_ctas_per_sm(int variant) {
+    switch (variant) {
+        case SGEMM_VARIANT_TMA_128x256: return ctas_per_sm_one<CfgL>();
+        case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<CfgM>();
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return ctas_per_sm_one<CfgS>();
+        default: return 0;
     }
 }
 
 cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const SplitK &sk, int smem_override, cudaStream_t stream) {
     switch (variant) {
-        case SGEMM_VARIANT_TMA_128x256: return launch_one<CfgL, false>(g, tmA, tmB, sk, smem_override, stream);
-        case SGEMM_VARIANT_TMA_128x128: return launch_one<CfgM, false>(g, tmA, tmB, sk, smem_override, stream);
-        case SGEMM_VARIANT_TMA_64x64: return launch_one<CfgS, false>(g, tmA, tmB, sk, smem_override, stream);
-        case SGEMM_VARIANT_TMA_64x64_SPLITK: return launch_one<CfgS, true>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_128x256: return launch_one<CfgL>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_128x128: return launch_one<CfgM>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return launch_one<CfgS>(g, tmA, tmB, sk, smem_override, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -304,3 +304,36 @@ def test_torch_tensor_interface(handle):
     ref = np.full(96 * 112, np.nan, np.float32)
     oracle.sgemm(96, 112, 80, 1.0, a, 80, b, 112, 0.0, ref, 112)
     assert float(np.max(np.abs(C.cpu().numpy().reshape(-1) - ref))) <= 1e-3
+
+
+@pytest.mark.parametrize("v", [V.VARIANT_TMA_128x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_64x64],
+                         ids=lambda v: sgemm.variant_name(v))
+def test_whole_waves_plus_split_tail(handle, variant, v):
+    """Enough tiles for one or more complete waves plus a partial one: the
+    complete waves run whole tiles and the tail tiles are split along K and
+    reduced by the last CTA of each.  Checked bit-exact on integer inputs and
+    within tolerance on uniform inputs (sampled rows across every tile row)."""
+    import torch
+    variant(v)
+    bm, bn = {V.VARIANT_TMA_128x128: (128, 128), V.VARIANT_TMA_128x256: (128, 256),
+              V.VARIANT_TMA_64x64: (64, 64)}[v]
+    # 12*SMs + 16 tiles: with 1, 2, 3 or 4 CTAs per SM the last wave holds 16 tiles
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles_m = 8
+    tiles_n = (12 * sms + 16) // tiles_m
+    M, N = bm * tiles_m, bn * tiles_n
+    for kind, alpha, beta in (("integer", 1.5, 0.5), ("uniform", 1.0, 1.0)):
+        cfg = inputs.GemmConfig("tail", M, N, 520, 524, N + 4, N, 31, alpha, beta)
+        prob = inputs.make_problem(cfg, kind=kind)
+        C_gpu, bufs = run_gpu(handle, cfg, prob)
+        ran, splits = sgemm.sgemm_last_variant(handle)
+        assert ran == v and splits > 1, (ran, splits)
+        rows = sorted(set(range(0, M, bm // 4)) | {M - 1})
+        ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
+                                cfg.beta, prob.C0, cfg.ldc)
+        got = np.ascontiguousarray(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows])
+        if kind == "integer":
+            assert np.array_equal(got.view(np.uint32), np.ascontiguousarray(ref).view(np.uint32))
+        else:
+            assert float(np.max(np.abs(got.astype(np.float64) - ref))) <= tolerance(cfg.K)
+        check_untouched(cfg, prob, C_gpu, bufs)
