@@ -55,6 +55,13 @@ cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA,
                        const CUtensorMap &tmB, const SplitK &sk, int smem_override,
                        cudaStream_t stream);
 
+// 3xTF32 tensor-core kernel (sgemm_tc.cu): A box 32 x 128 and B boxes 32 x 32,
+// both with the 128-byte swizzle.
+bool tc3x_shape(TmaShape *out);
+cudaError_t tc3x_prepare();
+cudaError_t launch_tc3x(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
+                        cudaStream_t stream);
+
 cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream);
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);
 cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);

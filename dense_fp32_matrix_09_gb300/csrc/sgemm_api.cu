@@ -218,6 +218,7 @@ const char *sgemm_variant_name(int v) {
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return "tma_64x64_splitk";
         case SGEMM_VARIANT_GENERIC: return "generic";
         case SGEMM_VARIANT_SCALE: return "scale";
+        case SGEMM_VARIANT_TC_3XTF32: return "tc_3xtf32";
         default: return "unknown";
     }
 }
@@ -259,6 +260,8 @@ int sgemm_create(sgemm_handle_t *out) {
         occupancy[v] = sg::tma_ctas_per_sm(v);
         if (occupancy[v] < 1) return SGEMM_ERR_CUDA;
     }
+    if (sg::tc3x_prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
+    occupancy[SGEMM_VARIANT_TC_3XTF32] = 1;
 
     sgemm_ctx *h = new (std::nothrow) sgemm_ctx();
     if (!h) return SGEMM_ERR_CUDA;
@@ -355,6 +358,18 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
 
     if (variant == SGEMM_VARIANT_GENERIC) {
         const int rc = from_cuda(sg::launch_generic(g, stream));
+        if (rc == SGEMM_OK) h->last_variant = variant;
+        return rc;
+    }
+
+    if (variant == SGEMM_VARIANT_TC_3XTF32) {
+        sg::TmaShape ts;
+        sg::tc3x_shape(&ts);
+        CUtensorMap tA, tB;
+        if (!encode_2d(&tA, A, M, K, lda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tB, B, K, N, ldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return SGEMM_ERR_CUDA;
+        const int rc = from_cuda(sg::launch_tc3x(g, tA, tB, h->smem_override, stream));
         if (rc == SGEMM_OK) h->last_variant = variant;
         return rc;
     }

@@ -1,0 +1,338 @@
+// 3xTF32 tensor-core GEMM for sm_103a: C = alpha*A*B + beta*C, row-major,
+// FP32 inputs and outputs, computed on the 5th-generation tensor cores
+// (tcgen05.mma .kind::tf32, accumulator in tensor memory).
+//
+// Split-precision method (Ootomo & Yokota, "Recovering single precision
+// accuracy from Tensor Cores while surpassing the FP32 theoretical peak
+// performance", 2022): every FP32 operand x is written as x = x_hi + x_lo with
+//     x_hi = tf32(x),  x_lo = tf32(x - x_hi)          (round to nearest)
+// and A*B is accumulated in FP32 as A_hi*B_hi + A_hi*B_lo + A_lo*B_hi, dropping
+// only A_lo*B_lo (relative size ~2^-22).  The pages mention TF32 tensor cores
+// only in passing (page "GPU-accelerated matrix computation optimisation and
+// CUDA programming practice", section 1; page "GEMM advanced: co-optimising
+// instruction-level parallelism and bank conflicts", section 5.3); the FP32
+// contract (max-abs tolerance) is the same as for the SIMT kernels.
+//
+// One CTA computes a 128 x 256 tile of C with 6 warps:
+//   warp 0      TMA producer (one lane): A tile [128 m][32 k] with the 128-byte
+//               swizzle (K-major) into stage s of a 2-stage ring, and the FP32 B
+//               tile as 8 boxes [32 k][32 n] with the 128-byte swizzle into one
+//               landing buffer;
+//   warp 1      owns the tensor memory (all 512 columns: two 128 x 256 FP32
+//               accumulators) and one lane issues the MMAs: per 8-k step three
+//               128 x 256 x 8 MMAs -- lo*hi and hi*lo into the correction
+//               accumulator, hi*hi into the main one -- then tcgen05.commit
+//               frees the stage.  The tensor core's FP32 accumulation is not
+//               round-to-nearest (measured: the error of one accumulator grows
+//               linearly with K), so the main accumulator receives only K/8
+//               additions and the correction terms, about 2^-11 times smaller,
+//               carry their rounding error at that scale; the epilogue adds the
+//               two with a round-to-nearest FP32 addition;
+//   warps 2-5   split each landed tile into hi and lo: A elementwise (hi in
+//               place, lo in a second buffer with the same layout), B transposed
+//               on the way into K-major B_hi / B_lo tiles [256 n][32 k] with the
+//               128-byte swizzle; then, after the last K step, read the
+//               accumulator (tcgen05.ld, one tensor-memory lane per thread) and
+//               apply alpha/beta.
+// Both MMA operands are K-major with the 128-byte swizzle: 8-row groups 1024 B
+// apart, and an 8-k step is +32 B on the descriptor's start address.  Every
+// wait is bounded; on a timeout the kernel records it, waits (bounded) for
+// its own copies and MMAs in flight, frees the tensor memory and returns
+// without writing C.
+#include "device_common.cuh"
+#include "internal.h"
+#include "sgemm.h"
+#include "tcgen05.cuh"
+
+namespace sg {
+namespace {
+
+constexpr int TBM = 128, TBN = 256, TBK = 32, TSTAGES = 2;
+constexpr int kTcThreads = 192;                       // 6 warps
+constexpr int kConvThreads = 128;                     // warps 2-5
+constexpr int kABytesTc = TBM * TBK * 4;              // 16 KiB
+constexpr int kBBytesTc = TBK * TBN * 4;              // 32 KiB
+constexpr int kStageTc = 2 * kABytesTc + 2 * kBBytesTc;  // A(hi), A_lo, B_hi, B_lo: 96 KiB
+constexpr int kTmemCols = 512;          // main accumulator at column 0, correction at TBN
+constexpr int kSmemTc = TSTAGES * kStageTc + kBBytesTc + 1024 + 256;  // + FP32 B landing buffer
+constexpr int kGroupMTc = 8;
+constexpr uint32_t kIdesc = tc::idesc_tf32(TBM, TBN, false, false);
+static_assert(kSmemTc <= 232448, "dynamic shared memory above the per-CTA limit");
+
+struct TcSmem {
+    uint64_t full[TSTAGES];   // A tile landed (1 arrival + bytes)
+    uint64_t conv[TSTAGES];   // hi/lo written (kConvThreads arrivals)
+    uint64_t empty[TSTAGES];  // MMAs of the stage finished (tcgen05.commit)
+    uint64_t bfull;           // FP32 B tile landed in the landing buffer
+    uint64_t bfree;           // landing buffer read (kConvThreads arrivals)
+    uint64_t acc_full;        // all MMAs finished (tcgen05.commit)
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ void tile_coords_tc(int pid, int tiles_m, int tiles_n, int &tm, int &tn) {
+    const int per_group = kGroupMTc * tiles_n;
+    const int grp = pid / per_group;
+    const int first_m = grp * kGroupMTc;
+    const int rows = min(tiles_m - first_m, kGroupMTc);
+    const int r = pid - grp * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+// hi / lo split of one 16-byte group, hi written back in place.
+__device__ __forceinline__ void split4(float4 *hi_io, float4 *lo_out) {
+    const float4 v = *hi_io;
+    float4 h, l;
+    h.x = tc::to_tf32(v.x); l.x = tc::to_tf32(v.x - h.x);
+    h.y = tc::to_tf32(v.y); l.y = tc::to_tf32(v.y - h.y);
+    h.z = tc::to_tf32(v.z); l.z = tc::to_tf32(v.z - h.z);
+    h.w = tc::to_tf32(v.w); l.w = tc::to_tf32(v.w - h.w);
+    *hi_io = h;
+    *lo_out = l;
+}
+
+// B landing buffer (8 boxes of [32 k][32 n], 128-byte swizzle: 16-byte chunk c
+// of row k at chunk c ^ (k & 7)) -> K-major B_hi / B_lo [256 n][32 k], 128-byte
+// swizzle (chunk c of row n at c ^ (n & 7)).  Converter thread ct handles, per
+// step, a 4 k x 4 n block: lane bits 0-2 pick the 4-column group of a box and
+// bits 3-4 the 4-row group, so every 16-byte shared access of a warp is spread
+// over all banks (4 wavefronts per warp-wide 16-byte access, the minimum).
+__device__ __forceinline__ void split_transpose_b(const uint8_t *bland, uint8_t *bhi, uint8_t *blo, int ct) {
+    const int lane = ct & 31, w = ct >> 5;       // w = 0..3
+    const int nb = lane & 7;                     // 4-column group within a box (0..7)
+    const int kq = lane >> 3;                    // 4-row group within a 16-row half (0..3)
+#pragma unroll 1
+    for (int it = 0; it < 4; ++it) {
+        const int region = w * 4 + it;           // 16 regions: 8 boxes x 2 halves of 16 k
+        const int box = region >> 1;
+        const int kb = (region & 1) * 4 + kq;    // 4-row group within the 32 k (0..7)
+        float4 r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int k = kb * 4 + i;
+            r[i] = *reinterpret_cast<const float4 *>(bland + box * 4096 + k * 128 + ((nb ^ (k & 7)) << 4));
+        }
+        const float col[4][4] = {{r[0].x, r[1].x, r[2].x, r[3].x},
+                                 {r[0].y, r[1].y, r[2].y, r[3].y},
+                                 {r[0].z, r[1].z, r[2].z, r[3].z},
+                                 {r[0].w, r[1].w, r[2].w, r[3].w}};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = box * 32 + nb * 4 + j;
+            float4 h, l;
+            h.x = tc::to_tf32(col[j][0]); l.x = tc::to_tf32(col[j][0] - h.x);
+            h.y = tc::to_tf32(col[j][1]); l.y = tc::to_tf32(col[j][1] - h.y);
+            h.z = tc::to_tf32(col[j][2]); l.z = tc::to_tf32(col[j][2] - h.z);
+            h.w = tc::to_tf32(col[j][3]); l.w = tc::to_tf32(col[j][3] - h.w);
+            const int off = n * 128 + ((kb ^ (n & 7)) << 4);
+            *reinterpret_cast<float4 *>(bhi + off) = h;
+            *reinterpret_cast<float4 *>(blo + off) = l;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *base = smem_raw + pad;
+    uint8_t *bland = base + TSTAGES * kStageTc;  // FP32 B tile, 8 swizzled boxes [32 k][32 n]
+    TcSmem *sh = reinterpret_cast<TcSmem *>(bland + kBBytesTc);
+    auto stA = [&](int s) { return base + s * kStageTc; };
+    auto stAlo = [&](int s) { return base + s * kStageTc + kABytesTc; };
+    auto stB = [&](int s) { return base + s * kStageTc + 2 * kABytesTc; };
+    auto stBlo = [&](int s) { return base + s * kStageTc + 2 * kABytesTc + kBBytesTc; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles_m = (g.M + TBM - 1) / TBM, tiles_n = (g.N + TBN - 1) / TBN;
+    int tm, tn;
+    tile_coords_tc(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    const int m0 = tm * TBM, n0 = tn * TBN;
+    const int nkt = (g.K + TBK - 1) / TBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < TSTAGES; ++s) {
+            mbar_init(&sh->full[s], 1);
+            mbar_init(&sh->conv[s], kConvThreads);
+            mbar_init(&sh->empty[s], 1);
+        }
+        mbar_init(&sh->bfull, 1);
+        mbar_init(&sh->bfree, kConvThreads);
+        mbar_init(&sh->acc_full, 1);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(&sh->tmem_base, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = sh->tmem_base;
+    volatile int *abort_flag = &sh->abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tmA);
+            prefetch_tensormap(&tmB);
+            int issued = 0, issued_b = 0;  // A loads, B loads in flight or landed
+            for (int t = 0; t < nkt; ++t) {
+                const int s = t % TSTAGES;
+                if (t >= TSTAGES && !mbar_wait(&sh->empty[s], ((t / TSTAGES) - 1) & 1, g.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const int kc = t * TBK;
+                mbar_arrive_expect_tx(&sh->full[s], kABytesTc);
+                tma_load_2d(stA(s), &tmA, &sh->full[s], kc, m0);
+                ++issued;
+                if (t >= 1 && !mbar_wait(&sh->bfree, (t - 1) & 1, g.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_arrive_expect_tx(&sh->bfull, kBBytesTc);
+#pragma unroll
+                for (int j = 0; j < TBN / 32; ++j)
+                    tma_load_2d(bland + j * 4096, &tmB, &sh->bfull, n0 + 32 * j, kc);
+                ++issued_b;
+            }
+            // every issued load lands before the CTA may exit (no-op when all were consumed)
+            for (int t = max(0, issued - TSTAGES); t < issued; ++t)
+                mbar_wait(&sh->full[t % TSTAGES], (t / TSTAGES) & 1, g.status);
+            if (issued_b > 0) mbar_wait(&sh->bfull, (issued_b - 1) & 1, g.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            for (int t = 0; t < nkt; ++t) {
+                const int s = t % TSTAGES;
+                if (!mbar_wait(&sh->conv[s], (t / TSTAGES) & 1, g.status) || *abort_flag) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t a_hi = smem_u32(stA(s)), a_lo = smem_u32(stAlo(s));
+                const uint32_t b_hi = smem_u32(stB(s)), b_lo = smem_u32(stBlo(s));
+#pragma unroll
+                for (int kk = 0; kk < TBK / 8; ++kk) {
+                    // A: K-major, 8-row groups 1024 B apart, k step of 8 = 32 B
+                    const uint64_t dah = tc::smem_desc(a_hi + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint64_t dal = tc::smem_desc(a_lo + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    // B_hi / B_lo: [256 n][32 k], same K-major layout
+                    const uint64_t dbh = tc::smem_desc(b_hi + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint64_t dbl = tc::smem_desc(b_lo + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    tc::mma_tf32(tmem + TBN, dal, dbh, kIdesc, acc);  // corr += lo * hi
+                    tc::mma_tf32(tmem + TBN, dah, dbl, kIdesc, 1u);   // corr += hi * lo
+                    tc::mma_tf32(tmem, dah, dbh, kIdesc, acc);        // main += hi * hi
+                }
+                tc::commit(&sh->empty[s]);
+            }
+            // arrives once every MMA issued above has completed (at once if none was)
+            tc::commit(&sh->acc_full);
+            if (!ok) mbar_wait(&sh->acc_full, 0, g.status);  // no teardown under a running MMA
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ hi/lo split, then epilogue
+        const int ct = tid - 64;
+        bool ok = true;
+        for (int t = 0; t < nkt; ++t) {
+            const int s = t % TSTAGES;
+            if (!mbar_wait(&sh->full[s], (t / TSTAGES) & 1, g.status) ||
+                !mbar_wait(&sh->bfull, t & 1, g.status) || *abort_flag) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            float4 *a = reinterpret_cast<float4 *>(stA(s));
+            float4 *al = reinterpret_cast<float4 *>(stAlo(s));
+#pragma unroll 4
+            for (int i = ct; i < kABytesTc / 16; i += kConvThreads) split4(a + i, al + i);
+            split_transpose_b(bland, stB(s), stBlo(s), ct);
+            mbar_arrive(&sh->bfree);  // release: this thread's landing-buffer reads are done
+            tc::fence_proxy_async_smem();
+            mbar_arrive(&sh->conv[s]);
+        }
+        if (ok) ok = mbar_wait(&sh->acc_full, 0, g.status) && !*abort_flag;
+        // tcgen05.ld is warp-collective: the whole warp stores or none of it
+        if (__all_sync(0xffffffffu, ok)) {
+            tc::fence_after_sync();
+            const int q = warp & 3;  // tensor-memory lane quadrant this warp can read
+            const int row = m0 + q * 32 + lane;
+            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            float *crow = g.C + static_cast<size_t>(row) * g.ldc;
+#pragma unroll 1
+            for (int c = 0; c < TBN / 16; ++c) {
+                float v[16], w[16];
+                tc::tmem_ld16(trow + c * 16, v);
+                tc::tmem_ld16(trow + TBN + c * 16, w);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] += w[j];
+                const int col0 = n0 + c * 16;
+                if (row >= g.M || col0 >= g.N) continue;
+                if (g.vec_c && col0 + 15 < g.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+                        float4 o = make_float4(g.alpha * v[j], g.alpha * v[j + 1], g.alpha * v[j + 2],
+                                               g.alpha * v[j + 3]);
+                        if (g.beta != 0.f) {
+                            const float4 cv = *p;
+                            o.x = fmaf(g.beta, cv.x, o.x);
+                            o.y = fmaf(g.beta, cv.y, o.y);
+                            o.z = fmaf(g.beta, cv.z, o.z);
+                            o.w = fmaf(g.beta, cv.w, o.w);
+                        }
+                        *p = o;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (col0 + j < g.N) {
+                            float o = g.alpha * v[j];
+                            if (g.beta != 0.f) o = fmaf(g.beta, crow[col0 + j], o);
+                            crow[col0 + j] = o;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    // ---------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool tc3x_shape(TmaShape *out) {
+    *out = TmaShape{TBM, TBN, TBK, kTcThreads, kSmemTc, 1};
+    return true;
+}
+
+cudaError_t tc3x_prepare() {
+    return cudaFuncSetAttribute(sgemm_tc3x_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+}
+
+cudaError_t launch_tc3x(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
+                        cudaStream_t stream) {
+    const int tiles = ((g.M + TBM - 1) / TBM) * ((g.N + TBN - 1) / TBN);
+    const int smem = smem_override > 0 ? smem_override : kSmemTc;
+    sgemm_tc3x_kernel<<<tiles, kTcThreads, smem, stream>>>(tmA, tmB, g);
+    return cudaGetLastError();
+}
+
+}  // namespace sg

@@ -33,8 +33,9 @@ VARIANT_TMA_64x64 = 3
 VARIANT_TMA_64x64_SPLITK = 4
 VARIANT_GENERIC = 5
 VARIANT_SCALE = 6
+VARIANT_TC_3XTF32 = 7
 GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
-                 VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC)
+                 VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32)
 
 #: Every exported entry point of include/sgemm.h.
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",

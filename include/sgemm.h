@@ -79,7 +79,9 @@ typedef enum {
     SGEMM_VARIANT_TMA_64x64_SPLITK = 4, /* 64 x 64 tiles, K split over CTAs, fixed-order sum */
     SGEMM_VARIANT_GENERIC = 5,       /* scalar loads, any alignment, 64 x 64 CTA tile       */
     SGEMM_VARIANT_SCALE = 6,         /* reported only: the C <- beta*C quick path ran       */
-    SGEMM_VARIANT_COUNT_ = 7
+    SGEMM_VARIANT_TC_3XTF32 = 7,     /* tensor cores (tcgen05, TMEM), 3xTF32 split precision,
+                                        128 x 256 CTA tile; FP32 inputs, outputs, tolerance   */
+    SGEMM_VARIANT_COUNT_ = 8
 } sgemm_variant_t;
 
 /* Create a handle bound to the CURRENT CUDA device.  Requires compute
