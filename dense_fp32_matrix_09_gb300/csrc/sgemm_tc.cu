@@ -13,11 +13,10 @@
 // instruction-level parallelism and bank conflicts", section 5.3); the FP32
 // contract (max-abs tolerance) is the same as for the SIMT kernels.
 //
-// One CTA computes a 128 x 256 tile of C with 6 warps:
-//   warp 0      TMA producer (one lane): A tile [128 m][32 k] with the 128-byte
-//               swizzle (K-major) into stage s of a 2-stage ring, and the FP32 B
-//               tile as 8 boxes [32 k][32 n] with the 128-byte swizzle into one
-//               landing buffer;
+// One CTA computes a 128 x 256 tile of C with 10 warps:
+//   warp 0      TMA producer (one lane): into stage s of a 2-stage ring, the A
+//               tile [128 m][32 k] with the 128-byte swizzle (K-major) and the
+//               FP32 B tile as 8 boxes [32 k][32 n] with the 128-byte swizzle;
 //   warp 1      owns the tensor memory (all 512 columns: two 128 x 256 FP32
 //               accumulators) and one lane issues the MMAs: per 8-k step three
 //               128 x 256 x 8 MMAs -- lo*hi and hi*lo into the correction
@@ -28,12 +27,16 @@
 //               additions and the correction terms, about 2^-11 times smaller,
 //               carry their rounding error at that scale; the epilogue adds the
 //               two with a round-to-nearest FP32 addition;
-//   warps 2-5   split each landed tile into hi and lo: A elementwise (hi in
+//   warps 2-9   split each landed tile into hi and lo: A elementwise (hi in
 //               place, lo in a second buffer with the same layout), B transposed
 //               on the way into K-major B_hi / B_lo tiles [256 n][32 k] with the
-//               128-byte swizzle; then, after the last K step, read the
-//               accumulator (tcgen05.ld, one tensor-memory lane per thread) and
-//               apply alpha/beta.
+//               128-byte swizzle (B_hi in place: every converter thread first
+//               loads its part of the FP32 tile into registers, a named barrier
+//               separates those reads from the writes); then, after the last K
+//               step, read the
+//               accumulators (tcgen05.ld, one tensor-memory lane per thread; the
+//               two warps of each lane quadrant take half of the columns each)
+//               and apply alpha/beta.
 // Both MMA operands are K-major with the 128-byte swizzle: 8-row groups 1024 B
 // apart, and an 8-k step is +32 B on the descriptor's start address.  Every
 // wait is bounded; on a timeout the kernel records it, waits (bounded) for
@@ -48,23 +51,21 @@ namespace sg {
 namespace {
 
 constexpr int TBM = 128, TBN = 256, TBK = 32, TSTAGES = 2;
-constexpr int kTcThreads = 192;                       // 6 warps
-constexpr int kConvThreads = 128;                     // warps 2-5
+constexpr int kTcThreads = 320;                       // 10 warps
+constexpr int kConvThreads = 256;                     // warps 2-9
 constexpr int kABytesTc = TBM * TBK * 4;              // 16 KiB
 constexpr int kBBytesTc = TBK * TBN * 4;              // 32 KiB
 constexpr int kStageTc = 2 * kABytesTc + 2 * kBBytesTc;  // A(hi), A_lo, B_hi, B_lo: 96 KiB
 constexpr int kTmemCols = 512;          // main accumulator at column 0, correction at TBN
-constexpr int kSmemTc = TSTAGES * kStageTc + kBBytesTc + 1024 + 256;  // + FP32 B landing buffer
+constexpr int kSmemTc = TSTAGES * kStageTc + 1024 + 256;
 constexpr int kGroupMTc = 8;
 constexpr uint32_t kIdesc = tc::idesc_tf32(TBM, TBN, false, false);
 static_assert(kSmemTc <= 232448, "dynamic shared memory above the per-CTA limit");
 
 struct TcSmem {
-    uint64_t full[TSTAGES];   // A tile landed (1 arrival + bytes)
+    uint64_t full[TSTAGES];   // A and B tiles landed (1 arrival + bytes)
     uint64_t conv[TSTAGES];   // hi/lo written (kConvThreads arrivals)
     uint64_t empty[TSTAGES];  // MMAs of the stage finished (tcgen05.commit)
-    uint64_t bfull;           // FP32 B tile landed in the landing buffer
-    uint64_t bfree;           // landing buffer read (kConvThreads arrivals)
     uint64_t acc_full;        // all MMAs finished (tcgen05.commit)
     uint32_t tmem_base;
     int abort;
@@ -92,39 +93,60 @@ __device__ __forceinline__ void split4(float4 *hi_io, float4 *lo_out) {
     *lo_out = l;
 }
 
-// B landing buffer (8 boxes of [32 k][32 n], 128-byte swizzle: 16-byte chunk c
-// of row k at chunk c ^ (k & 7)) -> K-major B_hi / B_lo [256 n][32 k], 128-byte
-// swizzle (chunk c of row n at c ^ (n & 7)).  Converter thread ct handles, per
-// step, a 4 k x 4 n block: lane bits 0-2 pick the 4-column group of a box and
-// bits 3-4 the 4-row group, so every 16-byte shared access of a warp is spread
-// over all banks (4 wavefronts per warp-wide 16-byte access, the minimum).
-__device__ __forceinline__ void split_transpose_b(const uint8_t *bland, uint8_t *bhi, uint8_t *blo, int ct) {
-    const int lane = ct & 31, w = ct >> 5;       // w = 0..3
-    const int nb = lane & 7;                     // 4-column group within a box (0..7)
-    const int kq = lane >> 3;                    // 4-row group within a 16-row half (0..3)
-#pragma unroll 1
-    for (int it = 0; it < 4; ++it) {
-        const int region = w * 4 + it;           // 16 regions: 8 boxes x 2 halves of 16 k
-        const int box = region >> 1;
-        const int kb = (region & 1) * 4 + kq;    // 4-row group within the 32 k (0..7)
-        float4 r[4];
+// FP32 B tile in the stage's B_hi slot (8 boxes of [32 k][32 n], 128-byte
+// swizzle: 16-byte chunk c of row k at chunk c ^ (k & 7)) -> K-major B_hi /
+// B_lo [256 n][32 k], 128-byte swizzle (chunk c of row n at c ^ (n & 7)).  A
+// thread handles two 4 k x 4 n blocks (row group kb, column group nb of a box).
+// 16-byte shared accesses are served eight lanes at a time, so the eight lanes
+// of each quarter-warp must touch eight different 16-byte bank groups both
+// when reading (chunk nb ^ (k & 7)) and when writing (chunk kb ^ (n & 7)).  The
+// diagonal assignment kb = i, nb = (i + c) mod 8 for lane i of a quarter and a
+// per-quarter shift c does both (checked for every shift); 16 regions of 4
+// shifts cover each box's 8 x 8 blocks.
+struct BBlocks {
+    float4 r[2][4];
+};
+
+__device__ __forceinline__ void b_block(int ct, int it, int &box, int &kb, int &nb) {
+    const int lane = ct & 31, w = ct >> 5;  // w = 0..7
+    const int region = w * 2 + it;          // 16 regions: 8 boxes x 2 groups of 4 shifts
+    box = region >> 1;
+    const int c = (region & 1) * 4 + (lane >> 3);
+    kb = lane & 7;
+    nb = (kb + c) & 7;
+}
+
+__device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBlocks &b) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int k = kb * 4 + i;
-            r[i] = *reinterpret_cast<const float4 *>(bland + box * 4096 + k * 128 + ((nb ^ (k & 7)) << 4));
+    for (int it = 0; it < 2; ++it) {
+        int box, kb, nb;
+        b_block(ct, it, box, kb, nb);
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+            const int k = kb * 4 + ii;
+            b.r[it][ii] = *reinterpret_cast<const float4 *>(braw + box * 4096 + k * 128 + ((nb ^ (k & 7)) << 4));
         }
+    }
+}
+
+__device__ __forceinline__ void store_b_split(uint8_t *bhi, uint8_t *blo, int ct, const BBlocks &b) {
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        int box, kb, nb;
+        b_block(ct, it, box, kb, nb);
+        const float4 *r = b.r[it];
         const float col[4][4] = {{r[0].x, r[1].x, r[2].x, r[3].x},
                                  {r[0].y, r[1].y, r[2].y, r[3].y},
                                  {r[0].z, r[1].z, r[2].z, r[3].z},
                                  {r[0].w, r[1].w, r[2].w, r[3].w}};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = box * 32 + nb * 4 + j;
+        for (int jj = 0; jj < 4; ++jj) {
+            const int n = box * 32 + nb * 4 + jj;
             float4 h, l;
-            h.x = tc::to_tf32(col[j][0]); l.x = tc::to_tf32(col[j][0] - h.x);
-            h.y = tc::to_tf32(col[j][1]); l.y = tc::to_tf32(col[j][1] - h.y);
-            h.z = tc::to_tf32(col[j][2]); l.z = tc::to_tf32(col[j][2] - h.z);
-            h.w = tc::to_tf32(col[j][3]); l.w = tc::to_tf32(col[j][3] - h.w);
+            h.x = tc::to_tf32(col[jj][0]); l.x = tc::to_tf32(col[jj][0] - h.x);
+            h.y = tc::to_tf32(col[jj][1]); l.y = tc::to_tf32(col[jj][1] - h.y);
+            h.z = tc::to_tf32(col[jj][2]); l.z = tc::to_tf32(col[jj][2] - h.z);
+            h.w = tc::to_tf32(col[jj][3]); l.w = tc::to_tf32(col[jj][3] - h.w);
             const int off = n * 128 + ((kb ^ (n & 7)) << 4);
             *reinterpret_cast<float4 *>(bhi + off) = h;
             *reinterpret_cast<float4 *>(blo + off) = l;
@@ -138,8 +160,7 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *base = smem_raw + pad;
-    uint8_t *bland = base + TSTAGES * kStageTc;  // FP32 B tile, 8 swizzled boxes [32 k][32 n]
-    TcSmem *sh = reinterpret_cast<TcSmem *>(bland + kBBytesTc);
+    TcSmem *sh = reinterpret_cast<TcSmem *>(base + TSTAGES * kStageTc);
     auto stA = [&](int s) { return base + s * kStageTc; };
     auto stAlo = [&](int s) { return base + s * kStageTc + kABytesTc; };
     auto stB = [&](int s) { return base + s * kStageTc + 2 * kABytesTc; };
@@ -158,8 +179,6 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(&sh->conv[s], kConvThreads);
             mbar_init(&sh->empty[s], 1);
         }
-        mbar_init(&sh->bfull, 1);
-        mbar_init(&sh->bfree, kConvThreads);
         mbar_init(&sh->acc_full, 1);
         sh->abort = 0;
         fence_barrier_init();
@@ -179,7 +198,7 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (lane == 0) {
             prefetch_tensormap(&tmA);
             prefetch_tensormap(&tmB);
-            int issued = 0, issued_b = 0;  // A loads, B loads in flight or landed
+            int issued = 0;
             for (int t = 0; t < nkt; ++t) {
                 const int s = t % TSTAGES;
                 if (t >= TSTAGES && !mbar_wait(&sh->empty[s], ((t / TSTAGES) - 1) & 1, g.status)) {
@@ -188,23 +207,16 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
                 if (*abort_flag) break;
                 const int kc = t * TBK;
-                mbar_arrive_expect_tx(&sh->full[s], kABytesTc);
+                mbar_arrive_expect_tx(&sh->full[s], kABytesTc + kBBytesTc);
                 tma_load_2d(stA(s), &tmA, &sh->full[s], kc, m0);
-                ++issued;
-                if (t >= 1 && !mbar_wait(&sh->bfree, (t - 1) & 1, g.status)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                mbar_arrive_expect_tx(&sh->bfull, kBBytesTc);
 #pragma unroll
                 for (int j = 0; j < TBN / 32; ++j)
-                    tma_load_2d(bland + j * 4096, &tmB, &sh->bfull, n0 + 32 * j, kc);
-                ++issued_b;
+                    tma_load_2d(stB(s) + j * 4096, &tmB, &sh->full[s], n0 + 32 * j, kc);
+                ++issued;
             }
             // every issued load lands before the CTA may exit (no-op when all were consumed)
             for (int t = max(0, issued - TSTAGES); t < issued; ++t)
                 mbar_wait(&sh->full[t % TSTAGES], (t / TSTAGES) & 1, g.status);
-            if (issued_b > 0) mbar_wait(&sh->bfull, (issued_b - 1) & 1, g.status);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -247,8 +259,9 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         bool ok = true;
         for (int t = 0; t < nkt; ++t) {
             const int s = t % TSTAGES;
-            if (!mbar_wait(&sh->full[s], (t / TSTAGES) & 1, g.status) ||
-                !mbar_wait(&sh->bfull, t & 1, g.status) || *abort_flag) {
+            // all converters agree on an abort, so none waits at a barrier another left
+            const bool bad = !mbar_wait(&sh->full[s], (t / TSTAGES) & 1, g.status) || *abort_flag;
+            if (named_barrier_or(1, kConvThreads, bad)) {
                 *abort_flag = 1;
                 ok = false;
                 break;
@@ -257,8 +270,10 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             float4 *al = reinterpret_cast<float4 *>(stAlo(s));
 #pragma unroll 4
             for (int i = ct; i < kABytesTc / 16; i += kConvThreads) split4(a + i, al + i);
-            split_transpose_b(bland, stB(s), stBlo(s), ct);
-            mbar_arrive(&sh->bfree);  // release: this thread's landing-buffer reads are done
+            BBlocks bb;
+            load_b_blocks(stB(s), ct, bb);
+            named_barrier_sync(2, kConvThreads);  // every read of the FP32 B tile is done
+            store_b_split(stB(s), stBlo(s), ct, bb);
             tc::fence_proxy_async_smem();
             mbar_arrive(&sh->conv[s]);
         }
@@ -266,12 +281,13 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // tcgen05.ld is warp-collective: the whole warp stores or none of it
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
-            const int q = warp & 3;  // tensor-memory lane quadrant this warp can read
+            const int q = warp & 3;             // tensor-memory lane quadrant this warp can read
+            const int half = (warp - 2) >> 2;   // which 128 of the 256 columns
             const int row = m0 + q * 32 + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
             float *crow = g.C + static_cast<size_t>(row) * g.ldc;
 #pragma unroll 1
-            for (int c = 0; c < TBN / 16; ++c) {
+            for (int c = half * (TBN / 32); c < (half + 1) * (TBN / 32); ++c) {
                 float v[16], w[16];
                 tc::tmem_ld16(trow + c * 16, v);
                 tc::tmem_ld16(trow + TBN + c * 16, w);
