@@ -52,6 +52,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def measured_bf16_tflops() -> dict:
+    """Dense BF16 tensor throughput: the burst figure the driver measured on
+    this pool (MEASURED_PEAKS.json), else the profiling recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return {"value": float(json.load(f)["bf16_tflops"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"value": 1900.0, "source": "fallback"}
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -64,6 +74,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
     p.add_argument("--e2e-steps", type=int, default=10)
+    p.add_argument("--no-tensor", action="store_true", help="skip the 3xTF32 tensor-core block")
+    p.add_argument("--tensor-steps", type=int, default=50)
     return p.parse_args()
 
 
@@ -407,6 +419,37 @@ def main():
         "clocks": clocks,
         "gpu": {"name": props.name, "sms": sms},
     }
+
+    # ---- the optional tensor-core path (3xTF32) on the same workload, same timing method
+    if not args.no_tensor:
+        sg.sgemm_set_variant(h, sg.VARIANT_TC_3XTF32)
+        for _ in range(args.warmup):
+            if in_place:
+                C.copy_(C0)
+            step()
+        torch.cuda.synchronize()
+        tc_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.tensor_steps)]
+        for i in range(args.tensor_steps):
+            if in_place:
+                C.copy_(C0)
+            tc_ev[2 * i].record(stream)
+            step()
+            tc_ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        tc_ms = statistics.mean(tc_ev[2 * i].elapsed_time(tc_ev[2 * i + 1]) for i in range(args.tensor_steps))
+        sg.sgemm_set_variant(h, sg.VARIANT_AUTO)
+        bf16 = measured_bf16_tflops()
+        tf32_peak = bf16["value"] * 1.1 / 2.25
+        tc_tflops = cfg.flops / (tc_ms * 1e-3) / 1e12
+        out["tensor_3xtf32"] = {
+            "variant": "tc_3xtf32", "ms_per_step": tc_ms, "value": tc_tflops, "unit": UNIT,
+            "steps": args.tensor_steps, "gpu_launches": args.tensor_steps,
+            "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": tf32_peak / 3, "unit": "TFLOP/s",
+                         "frac": tc_tflops / (tf32_peak / 3), "traffic": None,
+                         "peak_basis": f"TF32 dense = {bf16['source']} BF16 {bf16['value']:.1f} TFLOP/s x 1.1/2.25 "
+                                       f"(nominal ratio) = {tf32_peak:.1f}; 3 TF32 MMAs per FP32 product",
+                         "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
+        }
 
     # ---- per-workload table (device-resident; not part of the headline value)
     if not args.no_workloads and rank == 0:

@@ -31,6 +31,7 @@ struct sgemm_ctx {
     int last_splits;
     int smem_override;
     int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
+    int math_mode;                          // sgemm_math_mode_t
 };
 
 namespace {
@@ -318,6 +319,13 @@ int sgemm_set_variant(sgemm_handle_t h, int variant) {
     return SGEMM_OK;
 }
 
+int sgemm_set_math_mode(sgemm_handle_t h, int mode) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (mode != SGEMM_MATH_FP32 && mode != SGEMM_MATH_3XTF32) return SGEMM_ERR_INVALID_VALUE;
+    h->math_mode = mode;
+    return SGEMM_OK;
+}
+
 int sgemm_last_variant(sgemm_handle_t h, int *splits) {
     if (!alive(h)) return -1;
     if (splits) *splits = h->last_splits;
@@ -353,7 +361,16 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
         return rc;
     }
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0;
-    int variant = h->pinned != SGEMM_VARIANT_AUTO ? h->pinned : choose_variant(h, M, N, K);
+    int variant = h->pinned;
+    if (variant == SGEMM_VARIANT_AUTO) {
+        // 3xTF32 mode: the tensor-core kernel once there is at least about one
+        // 128 x 256 tile per SM and K is long enough to fill its pipeline
+        const long long tc_tiles = 1LL * cdiv(M, 128) * cdiv(N, 256);
+        if (h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 2 && K >= 256)
+            variant = SGEMM_VARIANT_TC_3XTF32;
+        else
+            variant = choose_variant(h, M, N, K);
+    }
     if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
 
     if (variant == SGEMM_VARIANT_GENERIC) {

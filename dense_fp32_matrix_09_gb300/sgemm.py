@@ -34,6 +34,8 @@ VARIANT_TMA_64x64_SPLITK = 4
 VARIANT_GENERIC = 5
 VARIANT_SCALE = 6
 VARIANT_TC_3XTF32 = 7
+MATH_FP32 = 0
+MATH_3XTF32 = 1
 GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
                  VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32)
 
@@ -41,7 +43,7 @@ GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
-           "sgemm_version", "sgemm_run_noalloc")
+           "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode")
 
 
 class SgemmError(RuntimeError):
@@ -80,6 +82,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_variant_name.argtypes = [i32]
         L.sgemm_variant_name.restype = ctypes.c_char_p
         L.sgemm_version.argtypes = []
+        L.sgemm_set_math_mode.argtypes = [vp, i32]
         L.sgemm_run_noalloc.argtypes = [i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         _lib = L
     return _lib
@@ -153,6 +156,10 @@ def sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
 
 def sgemm_set_variant(h, variant: int) -> None:
     _check(lib().sgemm_set_variant(h, int(variant)), "sgemm_set_variant")
+
+
+def sgemm_set_math_mode(h, mode: int) -> None:
+    _check(lib().sgemm_set_math_mode(h, int(mode)), "sgemm_set_math_mode")
 
 
 def sgemm_last_variant(h) -> tuple[int, int]:

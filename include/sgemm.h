@@ -84,6 +84,18 @@ typedef enum {
     SGEMM_VARIANT_COUNT_ = 8
 } sgemm_variant_t;
 
+/* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32
+ * contract (max |C - C_exact| within 1e-3 for K <= 1024 and 1e-2 for K <= 8192
+ * on U[-1,1) data).  SGEMM_MATH_FP32 (the default) runs FP32 FMAs on the CUDA
+ * cores.  SGEMM_MATH_3XTF32 lets the library use the tensor cores with the
+ * 3xTF32 split-precision method (A*B = A_hi*B_hi + A_hi*B_lo + A_lo*B_hi) for
+ * problems large enough to profit; its rounding errors are larger than the
+ * FP32 path's (about 5x at K = 8192) but still inside the contract. */
+typedef enum {
+    SGEMM_MATH_FP32 = 0,
+    SGEMM_MATH_3XTF32 = 1
+} sgemm_math_mode_t;
+
 /* Create a handle bound to the CURRENT CUDA device.  Requires compute
  * capability 10.3 (GB300); otherwise returns SGEMM_ERR_UNSUPPORTED_DEVICE and
  * sets *out to NULL.  Allocates the handle's device-side status word and its
@@ -116,6 +128,10 @@ int sgemm_destroy(sgemm_handle_t h);
  * let the library choose).  SGEMM_ERR_INVALID_VALUE for an unknown value or
  * SGEMM_VARIANT_SCALE, which is chosen only by the alpha == 0 / K == 0 rule. */
 int sgemm_set_variant(sgemm_handle_t h, int variant);
+
+/* Set the handle's math mode (an sgemm_math_mode_t) for SGEMM_VARIANT_AUTO.
+ * SGEMM_ERR_INVALID_VALUE for an unknown mode. */
+int sgemm_set_math_mode(sgemm_handle_t h, int mode);
 
 /* The variant the handle's last successful sgemm_run enqueued (an
  * sgemm_variant_t), or -1 if there was none or `h` is not a live handle.

@@ -337,3 +337,32 @@ def test_whole_waves_plus_split_tail(handle, variant, v):
         else:
             assert float(np.max(np.abs(got.astype(np.float64) - ref))) <= tolerance(cfg.K)
         check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=lambda c: c.name)
+def test_math_mode_3xtf32_workloads(handle, cfg):
+    """3xTF32 math mode on every workload: the tensor-core kernel where the
+    problem is large enough, the FP32 kernels otherwise; same tolerance."""
+    sgemm.sgemm_set_math_mode(handle, V.MATH_3XTF32)
+    try:
+        prob = inputs.make_problem(cfg)
+        C_gpu, bufs = run_gpu(handle, cfg, prob)
+        ran, _ = sgemm.sgemm_last_variant(handle)
+    finally:
+        sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
+    if cfg.M * cfg.N >= 2048 * 2048:
+        assert ran == V.VARIANT_TC_3XTF32, sgemm.variant_name(ran)
+    if cfg.M * cfg.N * cfg.K <= 2.5e9:
+        err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
+    else:
+        rows = sample_rows(cfg.M)
+        ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
+                                cfg.beta, prob.C0, cfg.ldc)
+        err = float(np.max(np.abs(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows].astype(np.float64) - ref)))
+    assert err <= tolerance(cfg.K), (cfg.name, sgemm.variant_name(ran), err)
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+def test_math_mode_rejects_unknown(handle):
+    with pytest.raises(sgemm.SgemmError):
+        sgemm.sgemm_set_math_mode(handle, 7)
