@@ -13,7 +13,7 @@
 // instruction-level parallelism and bank conflicts", section 5.3); the FP32
 // contract (max-abs tolerance) is the same as for the SIMT kernels.
 //
-// One CTA computes a 128 x 256 tile of C with 10 warps:
+// One CTA computes a 128 x 256 tile of C with 2 + kConvWarps warps:
 //   warp 0      TMA producer (one lane): into stage s of a 2-stage ring, the A
 //               tile [128 m][32 k] with the 128-byte swizzle (K-major) and the
 //               FP32 B tile as 8 boxes [32 k][32 n] with the 128-byte swizzle;
@@ -27,7 +27,7 @@
 //               additions and the correction terms, about 2^-11 times smaller,
 //               carry their rounding error at that scale; the epilogue adds the
 //               two with a round-to-nearest FP32 addition;
-//   warps 2-9   split each landed tile into hi and lo: A elementwise (hi in
+//   the rest    split each landed tile into hi and lo: A elementwise (hi in
 //               place, lo in a second buffer with the same layout), B transposed
 //               on the way into K-major B_hi / B_lo tiles [256 n][32 k] with the
 //               128-byte swizzle (B_hi in place: every converter thread first
@@ -35,7 +35,7 @@
 //               separates those reads from the writes); then, after the last K
 //               step, read the
 //               accumulators (tcgen05.ld, one tensor-memory lane per thread; the
-//               two warps of each lane quadrant take half of the columns each)
+//               warps of each lane quadrant share the columns)
 //               and apply alpha/beta.
 // Both MMA operands are K-major with the 128-byte swizzle: 8-row groups 1024 B
 // apart, and an 8-k step is +32 B on the descriptor's start address.  Every
@@ -51,8 +51,10 @@ namespace sg {
 namespace {
 
 constexpr int TBM = 128, TBN = 256, TBK = 32, TSTAGES = 2;
-constexpr int kTcThreads = 320;                       // 10 warps
-constexpr int kConvThreads = 256;                     // warps 2-9
+constexpr int kConvWarps = 8;                         // split / epilogue warps (a multiple of 4)
+constexpr int kConvThreads = 32 * kConvWarps;         // warps 2 .. 1 + kConvWarps
+constexpr int kTcThreads = 64 + kConvThreads;
+static_assert(kConvWarps % 4 == 0 && 16 % kConvWarps == 0, "warps must cover the lane quadrants and B regions");
 constexpr int kABytesTc = TBM * TBK * 4;              // 16 KiB
 constexpr int kBBytesTc = TBK * TBN * 4;              // 32 KiB
 constexpr int kStageTc = 2 * kABytesTc + 2 * kBBytesTc;  // A(hi), A_lo, B_hi, B_lo: 96 KiB
@@ -103,13 +105,15 @@ __device__ __forceinline__ void split4(float4 *hi_io, float4 *lo_out) {
 // diagonal assignment kb = i, nb = (i + c) mod 8 for lane i of a quarter and a
 // per-quarter shift c does both (checked for every shift); 16 regions of 4
 // shifts cover each box's 8 x 8 blocks.
+constexpr int kBIters = 16 / kConvWarps;  // B regions per converter warp
+
 struct BBlocks {
-    float4 r[2][4];
+    float4 r[kBIters][4];
 };
 
 __device__ __forceinline__ void b_block(int ct, int it, int &box, int &kb, int &nb) {
-    const int lane = ct & 31, w = ct >> 5;  // w = 0..7
-    const int region = w * 2 + it;          // 16 regions: 8 boxes x 2 groups of 4 shifts
+    const int lane = ct & 31, w = ct >> 5;  // w = 0 .. kConvWarps-1
+    const int region = w * kBIters + it;    // 16 regions: 8 boxes x 2 groups of 4 shifts
     box = region >> 1;
     const int c = (region & 1) * 4 + (lane >> 3);
     kb = lane & 7;
@@ -118,7 +122,7 @@ __device__ __forceinline__ void b_block(int ct, int it, int &box, int &kb, int &
 
 __device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBlocks &b) {
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
+    for (int it = 0; it < kBIters; ++it) {
         int box, kb, nb;
         b_block(ct, it, box, kb, nb);
 #pragma unroll
@@ -131,7 +135,7 @@ __device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBloc
 
 __device__ __forceinline__ void store_b_split(uint8_t *bhi, uint8_t *blo, int ct, const BBlocks &b) {
 #pragma unroll
-    for (int it = 0; it < 2; ++it) {
+    for (int it = 0; it < kBIters; ++it) {
         int box, kb, nb;
         b_block(ct, it, box, kb, nb);
         const float4 *r = b.r[it];
@@ -213,6 +217,14 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int j = 0; j < TBN / 32; ++j)
                     tma_load_2d(stB(s) + j * 4096, &tmB, &sh->full[s], n0 + 32 * j, kc);
                 ++issued;
+                // warm L2 with the tiles two steps ahead: with two stages their
+                // loads are issued only when this stage's MMAs have finished
+                if (t + TSTAGES < nkt) {
+                    const int kp = (t + TSTAGES) * TBK;
+                    tma_prefetch_2d(&tmA, kp, m0);
+#pragma unroll
+                    for (int j = 0; j < TBN / 32; ++j) tma_prefetch_2d(&tmB, n0 + 32 * j, kp);
+                }
             }
             // every issued load lands before the CTA may exit (no-op when all were consumed)
             for (int t = max(0, issued - TSTAGES); t < issued; ++t)
@@ -282,12 +294,13 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
             const int q = warp & 3;             // tensor-memory lane quadrant this warp can read
-            const int half = (warp - 2) >> 2;   // which 128 of the 256 columns
+            constexpr int kColChunks = (TBN / 16) / (kConvWarps / 4);  // 16-column chunks per warp
+            const int part = (warp - 2) >> 2;   // which share of the 256 columns
             const int row = m0 + q * 32 + lane;
             const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
             float *crow = g.C + static_cast<size_t>(row) * g.ldc;
 #pragma unroll 1
-            for (int c = half * (TBN / 32); c < (half + 1) * (TBN / 32); ++c) {
+            for (int c = part * kColChunks; c < (part + 1) * kColChunks; ++c) {
                 float v[16], w[16];
                 tc::tmem_ld16(trow + c * 16, v);
                 tc::tmem_ld16(trow + TBN + c * 16, w);
