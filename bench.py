@@ -39,14 +39,19 @@ UNIT = "TFLOP/s"
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture, keyed by the SHA-256 of the kernel source it was taken on; any
 # other source gives traffic = null.  See profiles/.
-TRAFFIC_BY_SOURCE = {}
+# (profiles/sgemm_8192cube_dram.md, 8192^3 launches)
+TRAFFIC_BY_SOURCE = {"728b753fefc20bac": 3.116e9}
+TC_TRAFFIC_BY_SOURCE = {"d8ac4d90e2415f26": 3.112e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma.cu",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
+TC_KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tc.cu",
+                     "dense_fp32_matrix_09_gb300/csrc/tcgen05.cuh",
+                     "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in files:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -393,7 +398,7 @@ def main():
     src_hash = kernel_source_hash()
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-        "traffic": TRAFFIC_BY_SOURCE.get(src_hash),
+        "traffic": TRAFFIC_BY_SOURCE.get(src_hash) if cfg.name == inputs.HEADLINE.name else None,
         "kernel": f"sgemm_tma_kernel ({sg.variant_name(variant)})",
         "peak_basis": f"FP32 FFMA: 2 FLOP x 128 lanes x {sms} SMs x {max_mhz:.0f} MHz (max SM clock)",
     }
@@ -445,7 +450,10 @@ def main():
             "variant": "tc_3xtf32", "ms_per_step": tc_ms, "value": tc_tflops, "unit": UNIT,
             "steps": args.tensor_steps, "gpu_launches": args.tensor_steps,
             "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": tf32_peak / 3, "unit": "TFLOP/s",
-                         "frac": tc_tflops / (tf32_peak / 3), "traffic": None,
+                         "frac": tc_tflops / (tf32_peak / 3),
+                         "traffic": (TC_TRAFFIC_BY_SOURCE.get(kernel_source_hash(TC_KERNEL_SOURCES))
+                                     if cfg.name == inputs.HEADLINE.name else None),
+                         "kernel_source_sha256_16": kernel_source_hash(TC_KERNEL_SOURCES),
                          "peak_basis": f"TF32 dense = {bf16['source']} BF16 {bf16['value']:.1f} TFLOP/s x 1.1/2.25 "
                                        f"(nominal ratio) = {tf32_peak:.1f}; 3 TF32 MMAs per FP32 product",
                          "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
