@@ -427,7 +427,7 @@ def main():
 
     # ---- the optional tensor-core path (3xTF32) on the same workload, same timing method
     if not args.no_tensor:
-        sg.sgemm_set_variant(h, sg.VARIANT_TC_3XTF32)
+        sg.sgemm_set_variant(h, sg.VARIANT_TC_3XTF32_PAIR)
         for _ in range(args.warmup):
             if in_place:
                 C.copy_(C0)
@@ -447,7 +447,7 @@ def main():
         tf32_peak = bf16["value"] * 1.1 / 2.25
         tc_tflops = cfg.flops / (tc_ms * 1e-3) / 1e12
         out["tensor_3xtf32"] = {
-            "variant": "tc_3xtf32", "ms_per_step": tc_ms, "value": tc_tflops, "unit": UNIT,
+            "variant": "tc_3xtf32_pair", "ms_per_step": tc_ms, "value": tc_tflops, "unit": UNIT,
             "steps": args.tensor_steps, "gpu_launches": args.tensor_steps,
             "roofline": {"bound": "tensor", "achieved": tc_tflops, "peak": tf32_peak / 3, "unit": "TFLOP/s",
                          "frac": tc_tflops / (tf32_peak / 3),

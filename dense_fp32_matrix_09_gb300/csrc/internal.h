@@ -61,6 +61,10 @@ bool tc3x_shape(TmaShape *out);
 cudaError_t tc3x_prepare();
 cudaError_t launch_tc3x(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
                         cudaStream_t stream);
+// CTA-pair version (cta_group::2, 256 x 256 tile per cluster of two CTAs); same boxes.
+cudaError_t tc3x_pair_prepare();
+cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                             int smem_override, cudaStream_t stream);
 
 cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream);
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);

@@ -220,6 +220,7 @@ const char *sgemm_variant_name(int v) {
         case SGEMM_VARIANT_GENERIC: return "generic";
         case SGEMM_VARIANT_SCALE: return "scale";
         case SGEMM_VARIANT_TC_3XTF32: return "tc_3xtf32";
+        case SGEMM_VARIANT_TC_3XTF32_PAIR: return "tc_3xtf32_pair";
         default: return "unknown";
     }
 }
@@ -261,8 +262,9 @@ int sgemm_create(sgemm_handle_t *out) {
         occupancy[v] = sg::tma_ctas_per_sm(v);
         if (occupancy[v] < 1) return SGEMM_ERR_CUDA;
     }
-    if (sg::tc3x_prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (sg::tc3x_prepare() != cudaSuccess || sg::tc3x_pair_prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
     occupancy[SGEMM_VARIANT_TC_3XTF32] = 1;
+    occupancy[SGEMM_VARIANT_TC_3XTF32_PAIR] = 1;
 
     sgemm_ctx *h = new (std::nothrow) sgemm_ctx();
     if (!h) return SGEMM_ERR_CUDA;
@@ -363,11 +365,11 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0;
     int variant = h->pinned;
     if (variant == SGEMM_VARIANT_AUTO) {
-        // 3xTF32 mode: the tensor-core kernel once there is at least about one
-        // 128 x 256 tile per SM and K is long enough to fill its pipeline
-        const long long tc_tiles = 1LL * cdiv(M, 128) * cdiv(N, 256);
-        if (h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 2 && K >= 256)
-            variant = SGEMM_VARIANT_TC_3XTF32;
+        // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
+        // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
+        const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
+        if (h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
+            variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
         else
             variant = choose_variant(h, M, N, K);
     }
@@ -379,14 +381,16 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
         return rc;
     }
 
-    if (variant == SGEMM_VARIANT_TC_3XTF32) {
+    if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
         sg::TmaShape ts;
         sg::tc3x_shape(&ts);
         CUtensorMap tA, tB;
         if (!encode_2d(&tA, A, M, K, lda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&tB, B, K, N, ldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
             return SGEMM_ERR_CUDA;
-        const int rc = from_cuda(sg::launch_tc3x(g, tA, tB, h->smem_override, stream));
+        const int rc = from_cuda(variant == SGEMM_VARIANT_TC_3XTF32
+                                     ? sg::launch_tc3x(g, tA, tB, h->smem_override, stream)
+                                     : sg::launch_tc3x_pair(g, tA, tB, h->smem_override, stream));
         if (rc == SGEMM_OK) h->last_variant = variant;
         return rc;
     }

@@ -95,36 +95,41 @@ __device__ __forceinline__ void split4(float4 *hi_io, float4 *lo_out) {
     *lo_out = l;
 }
 
-// FP32 B tile in the stage's B_hi slot (8 boxes of [32 k][32 n], 128-byte
+// FP32 B tile in the stage's B_hi slot (NBOX boxes of [32 k][32 n], 128-byte
 // swizzle: 16-byte chunk c of row k at chunk c ^ (k & 7)) -> K-major B_hi /
-// B_lo [256 n][32 k], 128-byte swizzle (chunk c of row n at c ^ (n & 7)).  A
-// thread handles two 4 k x 4 n blocks (row group kb, column group nb of a box).
+// B_lo [32*NBOX n][32 k], 128-byte swizzle (chunk c of row n at c ^ (n & 7)).
+// A thread handles 4 k x 4 n blocks (row group kb, column group nb of a box).
 // 16-byte shared accesses are served eight lanes at a time, so the eight lanes
 // of each quarter-warp must touch eight different 16-byte bank groups both
 // when reading (chunk nb ^ (k & 7)) and when writing (chunk kb ^ (n & 7)).  The
 // diagonal assignment kb = i, nb = (i + c) mod 8 for lane i of a quarter and a
-// per-quarter shift c does both (checked for every shift); 16 regions of 4
-// shifts cover each box's 8 x 8 blocks.
-constexpr int kBIters = 16 / kConvWarps;  // B regions per converter warp
+// per-quarter shift c does both (checked for every shift); 2*NBOX regions of 4
+// shifts cover each box's 8 x 8 blocks, kBIters<NBOX, NW> regions per warp when NW
+// warps share the tile.
+template <int NBOX, int NW = kConvWarps>
+constexpr int kBIters = 2 * NBOX / NW;
 
-struct BBlocks {
-    float4 r[kBIters][4];
-};
-
+template <int NBOX, int NW = kConvWarps>
 __device__ __forceinline__ void b_block(int ct, int it, int &box, int &kb, int &nb) {
-    const int lane = ct & 31, w = ct >> 5;  // w = 0 .. kConvWarps-1
-    const int region = w * kBIters + it;    // 16 regions: 8 boxes x 2 groups of 4 shifts
+    const int lane = ct & 31, w = ct >> 5;      // w = 0 .. NW-1 (warps sharing the tile)
+    const int region = w * kBIters<NBOX, NW> + it;  // 2*NBOX regions: NBOX boxes x 2 groups of 4 shifts
     box = region >> 1;
     const int c = (region & 1) * 4 + (lane >> 3);
     kb = lane & 7;
     nb = (kb + c) & 7;
 }
 
-__device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBlocks &b) {
+template <int NBOX, int NW = kConvWarps>
+struct BBlocks {
+    float4 r[kBIters<NBOX, NW>][4];
+};
+
+template <int NBOX, int NW = kConvWarps>
+__device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBlocks<NBOX, NW> &b) {
 #pragma unroll
-    for (int it = 0; it < kBIters; ++it) {
+    for (int it = 0; it < kBIters<NBOX, NW>; ++it) {
         int box, kb, nb;
-        b_block(ct, it, box, kb, nb);
+        b_block<NBOX, NW>(ct, it, box, kb, nb);
 #pragma unroll
         for (int ii = 0; ii < 4; ++ii) {
             const int k = kb * 4 + ii;
@@ -133,11 +138,12 @@ __device__ __forceinline__ void load_b_blocks(const uint8_t *braw, int ct, BBloc
     }
 }
 
-__device__ __forceinline__ void store_b_split(uint8_t *bhi, uint8_t *blo, int ct, const BBlocks &b) {
+template <int NBOX, int NW = kConvWarps>
+__device__ __forceinline__ void store_b_split(uint8_t *bhi, uint8_t *blo, int ct, const BBlocks<NBOX, NW> &b) {
 #pragma unroll
-    for (int it = 0; it < kBIters; ++it) {
+    for (int it = 0; it < kBIters<NBOX, NW>; ++it) {
         int box, kb, nb;
-        b_block(ct, it, box, kb, nb);
+        b_block<NBOX, NW>(ct, it, box, kb, nb);
         const float4 *r = b.r[it];
         const float col[4][4] = {{r[0].x, r[1].x, r[2].x, r[3].x},
                                  {r[0].y, r[1].y, r[2].y, r[3].y},
@@ -154,6 +160,49 @@ __device__ __forceinline__ void store_b_split(uint8_t *bhi, uint8_t *blo, int ct
             const int off = n * 128 + ((kb ^ (n & 7)) << 4);
             *reinterpret_cast<float4 *>(bhi + off) = h;
             *reinterpret_cast<float4 *>(blo + off) = l;
+        }
+    }
+}
+
+// Epilogue of one warp: rows of its tensor-memory lane quadrant, columns
+// [c_begin, c_end) x 16 of the tile, C = alpha * (main + corr) + beta * C.
+__device__ __forceinline__ void tc_epilogue(const GemmArgs &g, uint32_t tmem, int q, int lane, int row0,
+                                            int n0, int c_begin, int c_end) {
+    const int row = row0 + q * 32 + lane;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    float *crow = g.C + static_cast<size_t>(row) * g.ldc;
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
+        float v[16], w[16];
+        tc::tmem_ld16(trow + c * 16, v);
+        tc::tmem_ld16(trow + TBN + c * 16, w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += w[j];
+        const int col0 = n0 + c * 16;
+        if (row >= g.M || col0 >= g.N) continue;
+        if (g.vec_c && col0 + 15 < g.N) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
+                float4 o = make_float4(g.alpha * v[j], g.alpha * v[j + 1], g.alpha * v[j + 2], g.alpha * v[j + 3]);
+                if (g.beta != 0.f) {
+                    const float4 cv = *p;
+                    o.x = fmaf(g.beta, cv.x, o.x);
+                    o.y = fmaf(g.beta, cv.y, o.y);
+                    o.z = fmaf(g.beta, cv.z, o.z);
+                    o.w = fmaf(g.beta, cv.w, o.w);
+                }
+                *p = o;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                if (col0 + j < g.N) {
+                    float o = g.alpha * v[j];
+                    if (g.beta != 0.f) o = fmaf(g.beta, crow[col0 + j], o);
+                    crow[col0 + j] = o;
+                }
+            }
         }
     }
 }
@@ -282,10 +331,10 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             float4 *al = reinterpret_cast<float4 *>(stAlo(s));
 #pragma unroll 4
             for (int i = ct; i < kABytesTc / 16; i += kConvThreads) split4(a + i, al + i);
-            BBlocks bb;
-            load_b_blocks(stB(s), ct, bb);
+            BBlocks<TBN / 32> bb;
+            load_b_blocks<TBN / 32>(stB(s), ct, bb);
             named_barrier_sync(2, kConvThreads);  // every read of the FP32 B tile is done
-            store_b_split(stB(s), stBlo(s), ct, bb);
+            store_b_split<TBN / 32>(stB(s), stBlo(s), ct, bb);
             tc::fence_proxy_async_smem();
             mbar_arrive(&sh->conv[s]);
         }
@@ -293,47 +342,9 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         // tcgen05.ld is warp-collective: the whole warp stores or none of it
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
-            const int q = warp & 3;             // tensor-memory lane quadrant this warp can read
             constexpr int kColChunks = (TBN / 16) / (kConvWarps / 4);  // 16-column chunks per warp
             const int part = (warp - 2) >> 2;   // which share of the 256 columns
-            const int row = m0 + q * 32 + lane;
-            const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
-            float *crow = g.C + static_cast<size_t>(row) * g.ldc;
-#pragma unroll 1
-            for (int c = part * kColChunks; c < (part + 1) * kColChunks; ++c) {
-                float v[16], w[16];
-                tc::tmem_ld16(trow + c * 16, v);
-                tc::tmem_ld16(trow + TBN + c * 16, w);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) v[j] += w[j];
-                const int col0 = n0 + c * 16;
-                if (row >= g.M || col0 >= g.N) continue;
-                if (g.vec_c && col0 + 15 < g.N) {
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        float4 *p = reinterpret_cast<float4 *>(crow + col0 + j);
-                        float4 o = make_float4(g.alpha * v[j], g.alpha * v[j + 1], g.alpha * v[j + 2],
-                                               g.alpha * v[j + 3]);
-                        if (g.beta != 0.f) {
-                            const float4 cv = *p;
-                            o.x = fmaf(g.beta, cv.x, o.x);
-                            o.y = fmaf(g.beta, cv.y, o.y);
-                            o.z = fmaf(g.beta, cv.z, o.z);
-                            o.w = fmaf(g.beta, cv.w, o.w);
-                        }
-                        *p = o;
-                    }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (col0 + j < g.N) {
-                            float o = g.alpha * v[j];
-                            if (g.beta != 0.f) o = fmaf(g.beta, crow[col0 + j], o);
-                            crow[col0 + j] = o;
-                        }
-                    }
-                }
-            }
+            tc_epilogue(g, tmem, warp & 3, lane, m0, n0, part * kColChunks, (part + 1) * kColChunks);
         }
     }
     // ---------------------------------------------------- teardown
@@ -345,7 +356,204 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
+// ============================================================================
+// CTA-pair version (tcgen05 cta_group::2): a cluster of two CTAs computes a
+// 256 x 256 tile of C with one MMA per step, M = 256, N = 256, K = 8.  Each CTA
+// holds 128 rows of A and 128 columns of B (K-major, 128-byte swizzle, same
+// shared offsets in both CTAs), splits only that half, and owns 128 rows of the
+// accumulators in its own tensor memory.  The even CTA's MMA lane waits until
+// the split warps of both CTAs have arrived on its `conv` barrier, issues the
+// MMAs for the pair and signals completion to the `empty` / `acc_full`
+// barriers of both CTAs (multicast commit).  Per SM this halves the B split
+// and the B operand traffic of the one-CTA kernel, which leaves shared-memory
+// room for three stages.
+constexpr int PSTAGES = 3;
+constexpr int PBN = 128;                                 // B columns per CTA (256 per pair)
+constexpr int kPBBytes = TBK * PBN * 4;                  // 16 KiB
+constexpr int kPStage = 2 * kABytesTc + 2 * kPBBytes;    // A(hi), A_lo, B_hi, B_lo: 64 KiB
+// + 32 KiB never written: operand reads stay inside the allocation even if an
+// MMA addressed more than one stage's worth of rows past its start.
+constexpr int kSmemTcPair = PSTAGES * kPStage + 256 + 32768 + 1024;
+constexpr uint32_t kIdescPair = tc::idesc_tf32(2 * TBM, 2 * PBN, false, false);
+static_assert(kSmemTcPair <= 232448, "dynamic shared memory above the per-CTA limit");
+
+struct TcPairSmem {
+    uint64_t full[PSTAGES];   // this CTA's A and B tiles landed
+    uint64_t conv[PSTAGES];   // (even CTA) hi/lo written: one arrival from each CTA of the pair
+    uint64_t empty[PSTAGES];  // MMAs of the stage finished (multicast commit)
+    uint64_t acc_full;        // all MMAs finished (multicast commit)
+    uint32_t tmem_base;
+    int abort;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *base = smem_raw + pad;  // same offset in both CTAs (same kernel, same layout)
+    TcPairSmem *sh = reinterpret_cast<TcPairSmem *>(base + PSTAGES * kPStage);
+    auto stA = [&](int s) { return base + s * kPStage; };
+    auto stAlo = [&](int s) { return base + s * kPStage + kABytesTc; };
+    auto stB = [&](int s) { return base + s * kPStage + 2 * kABytesTc; };
+    auto stBlo = [&](int s) { return base + s * kPStage + 2 * kABytesTc + kPBBytes; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = tc::cluster_ctarank();  // 0: issues the MMAs
+    const int tiles_m = (g.M + 2 * TBM - 1) / (2 * TBM), tiles_n = (g.N + 2 * PBN - 1) / (2 * PBN);
+    int tm, tn;
+    tile_coords_tc(blockIdx.x >> 1, tiles_m, tiles_n, tm, tn);
+    const int m0 = tm * 2 * TBM + static_cast<int>(rank) * TBM;  // this CTA's rows of A and C
+    const int n0 = tn * 2 * PBN;                                 // the tile's columns of C
+    const int nb0 = n0 + static_cast<int>(rank) * PBN;           // this CTA's columns of B
+    const int nkt = (g.K + TBK - 1) / TBK;
+
+    if (tid == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(&sh->full[s], 1);
+            mbar_init(&sh->conv[s], 2);  // one arrival per CTA of the pair
+            mbar_init(&sh->empty[s], 1);
+        }
+        mbar_init(&sh->acc_full, 1);
+        sh->abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc_pair(&sh->tmem_base, kTmemCols);
+        tc::tmem_relinquish_pair();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync_all();  // both CTAs' barriers are initialised before any cross-CTA arrive
+    tc::fence_after_sync();
+    const uint32_t tmem = sh->tmem_base;
+    volatile int *abort_flag = &sh->abort;
+    const uint32_t conv_even = tc::map_shared_rank(smem_u32(&sh->conv[0]), 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (each CTA)
+        if (lane == 0) {
+            prefetch_tensormap(&tmA);
+            prefetch_tensormap(&tmB);
+            int issued = 0;
+            for (int t = 0; t < nkt; ++t) {
+                const int s = t % PSTAGES;
+                if (t >= PSTAGES && !mbar_wait(&sh->empty[s], ((t / PSTAGES) - 1) & 1, g.status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const int kc = t * TBK;
+                mbar_arrive_expect_tx(&sh->full[s], kABytesTc + kPBBytes);
+                tma_load_2d(stA(s), &tmA, &sh->full[s], kc, m0);
+#pragma unroll
+                for (int j = 0; j < PBN / 32; ++j)
+                    tma_load_2d(stB(s) + j * 4096, &tmB, &sh->full[s], nb0 + 32 * j, kc);
+                ++issued;
+                if (t + PSTAGES < nkt) {
+                    const int kp = (t + PSTAGES) * TBK;
+                    tma_prefetch_2d(&tmA, kp, m0);
+#pragma unroll
+                    for (int j = 0; j < PBN / 32; ++j) tma_prefetch_2d(&tmB, nb0 + 32 * j, kp);
+                }
+            }
+            for (int t = max(0, issued - PSTAGES); t < issued; ++t)
+                mbar_wait(&sh->full[t % PSTAGES], (t / PSTAGES) & 1, g.status);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            bool ok = true;
+            for (int t = 0; t < nkt; ++t) {
+                const int s = t % PSTAGES;
+                if (!tc::mbar_wait_cluster(&sh->conv[s], (t / PSTAGES) & 1, g.status) || *abort_flag) {
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t a_hi = smem_u32(stA(s)), a_lo = smem_u32(stAlo(s));
+                const uint32_t b_hi = smem_u32(stB(s)), b_lo = smem_u32(stBlo(s));
+#pragma unroll
+                for (int kk = 0; kk < TBK / 8; ++kk) {
+                    const uint64_t dah = tc::smem_desc(a_hi + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint64_t dal = tc::smem_desc(a_lo + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint64_t dbh = tc::smem_desc(b_hi + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint64_t dbl = tc::smem_desc(b_lo + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
+                    const uint32_t acc = (t > 0 || kk > 0) ? 1u : 0u;
+                    tc::mma_tf32_pair(tmem + TBN, dal, dbh, kIdescPair, acc);  // corr += lo * hi
+                    tc::mma_tf32_pair(tmem + TBN, dah, dbl, kIdescPair, 1u);   // corr += hi * lo
+                    tc::mma_tf32_pair(tmem, dah, dbh, kIdescPair, acc);        // main += hi * hi
+                }
+                tc::commit_pair(&sh->empty[s], 0x3);
+            }
+            tc::commit_pair(&sh->acc_full, 0x3);
+            if (!ok) mbar_wait(&sh->acc_full, 0, g.status);  // no teardown under a running MMA
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ hi/lo split, then epilogue (each CTA)
+        // Two groups of kConvWarps/2 warps take alternate K steps, so the split
+        // of one step overlaps that of the next; each group has its own named
+        // barriers (ids 1-3 and 4-6).
+        constexpr int kGroupThreads = kConvThreads / 2, kGroupWarps = kConvWarps / 2;
+        const int ct = tid - 64;
+        const int grp = ct / kGroupThreads, gt = ct % kGroupThreads;
+        const int bar0 = 1 + 3 * grp;
+        bool ok = true;
+        for (int t = grp; t < nkt; t += 2) {
+            const int s = t % PSTAGES;
+            const bool bad = !mbar_wait(&sh->full[s], (t / PSTAGES) & 1, g.status) || *abort_flag;
+            if (named_barrier_or(bar0, kGroupThreads, bad)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            float4 *a = reinterpret_cast<float4 *>(stA(s));
+            float4 *al = reinterpret_cast<float4 *>(stAlo(s));
+#pragma unroll 4
+            for (int i = gt; i < kABytesTc / 16; i += kGroupThreads) split4(a + i, al + i);
+            BBlocks<PBN / 32, kGroupWarps> bb;
+            load_b_blocks<PBN / 32, kGroupWarps>(stB(s), gt, bb);
+            named_barrier_sync(bar0 + 1, kGroupThreads);  // every read of the FP32 B tile is done
+            store_b_split<PBN / 32, kGroupWarps>(stB(s), stBlo(s), gt, bb);
+            tc::fence_proxy_async_smem();
+            named_barrier_sync(bar0 + 2, kGroupThreads);  // this group's half of the stage is written
+            if (gt == 0) tc::mbar_arrive_cluster(conv_even + s * 8);  // the even CTA's conv[s]
+        }
+        if (ok) ok = mbar_wait(&sh->acc_full, 0, g.status) && !*abort_flag;
+        if (__all_sync(0xffffffffu, ok)) {
+            tc::fence_after_sync();
+            constexpr int kColChunks = (2 * PBN / 16) / (kConvWarps / 4);
+            const int part = (warp - 2) >> 2;
+            tc_epilogue(g, tmem, warp & 3, lane, m0, n0, part * kColChunks, (part + 1) * kColChunks);
+        }
+    }
+    // ---------------------------------------------------- teardown
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync_all();  // the peer is done with this CTA's shared memory and barriers
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
 }  // namespace
+
+cudaError_t tc3x_pair_prepare() {
+    return cudaFuncSetAttribute(sgemm_tc3x_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTcPair);
+}
+
+// Two CTAs (one cluster) per 256 x 256 tile; the cluster shape is part of the kernel.
+cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
+                             cudaStream_t stream) {
+    const int tiles = ((g.M + 2 * TBM - 1) / (2 * TBM)) * ((g.N + 2 * PBN - 1) / (2 * PBN));
+    const int smem = smem_override > 0 ? smem_override : kSmemTcPair;
+    sgemm_tc3x_pair_kernel<<<2 * tiles, kTcThreads, smem, stream>>>(tmA, tmB, g);
+    return cudaGetLastError();
+}
 
 bool tc3x_shape(TmaShape *out) {
     *out = TmaShape{TBM, TBN, TBK, kTcThreads, kSmemTc, 1};

@@ -34,10 +34,11 @@ VARIANT_TMA_64x64_SPLITK = 4
 VARIANT_GENERIC = 5
 VARIANT_SCALE = 6
 VARIANT_TC_3XTF32 = 7
+VARIANT_TC_3XTF32_PAIR = 8
 MATH_FP32 = 0
 MATH_3XTF32 = 1
 GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
-                 VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32)
+                 VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32, VARIANT_TC_3XTF32_PAIR)
 
 #: Every exported entry point of include/sgemm.h.
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",

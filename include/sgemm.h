@@ -81,7 +81,9 @@ typedef enum {
     SGEMM_VARIANT_SCALE = 6,         /* reported only: the C <- beta*C quick path ran       */
     SGEMM_VARIANT_TC_3XTF32 = 7,     /* tensor cores (tcgen05, TMEM), 3xTF32 split precision,
                                         128 x 256 CTA tile; FP32 inputs, outputs, tolerance   */
-    SGEMM_VARIANT_COUNT_ = 8
+    SGEMM_VARIANT_TC_3XTF32_PAIR = 8,/* as TC_3XTF32 on CTA pairs (cta_group::2): 256 x 256
+                                        tile per cluster of two CTAs                          */
+    SGEMM_VARIANT_COUNT_ = 9
 } sgemm_variant_t;
 
 /* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32
@@ -90,7 +92,9 @@ typedef enum {
  * cores.  SGEMM_MATH_3XTF32 lets the library use the tensor cores with the
  * 3xTF32 split-precision method (A*B = A_hi*B_hi + A_hi*B_lo + A_lo*B_hi) for
  * problems large enough to profit; its rounding errors are larger than the
- * FP32 path's (about 5x at K = 8192) but still inside the contract. */
+ * FP32 path's (about 5x at K = 8192) but still inside the contract.  In this
+ * mode SGEMM_VARIANT_AUTO takes SGEMM_VARIANT_TC_3XTF32_PAIR when there are at
+ * least SMs/4 tiles of 256 x 256 and K >= 256, and the FP32 kernels otherwise. */
 typedef enum {
     SGEMM_MATH_FP32 = 0,
     SGEMM_MATH_3XTF32 = 1

@@ -351,7 +351,7 @@ def test_math_mode_3xtf32_workloads(handle, cfg):
     finally:
         sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
     if cfg.M * cfg.N >= 2048 * 2048:
-        assert ran == V.VARIANT_TC_3XTF32, sgemm.variant_name(ran)
+        assert ran == V.VARIANT_TC_3XTF32_PAIR, sgemm.variant_name(ran)
     if cfg.M * cfg.N * cfg.K <= 2.5e9:
         err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
     else:
