@@ -375,6 +375,17 @@ constexpr int kPStage = 2 * kABytesTc + 2 * kPBBytes;    // A(hi), A_lo, B_hi, B
 // MMA addressed more than one stage's worth of rows past its start.
 constexpr int kSmemTcPair = PSTAGES * kPStage + 256 + 32768 + 1024;
 constexpr uint32_t kIdescPair = tc::idesc_tf32(2 * TBM, 2 * PBN, false, false);
+// Split groups take K steps in turn.  One group per stage: group g handles the
+// K steps t = g, g + PSTAGES, ... and so waits for every phase of full[g], in
+// order.  (With more groups than stages a group could start waiting for step
+// t on a stage whose previous phase, owned by another group, has not landed
+// yet, and the parity test would pass one phase early.)
+constexpr int kPairGroups = PSTAGES;
+constexpr int kPairConvWarps = 4 * kPairGroups;      // split / epilogue warps, all groups
+constexpr int kPairConvThreads = 32 * kPairConvWarps;
+constexpr int kPairThreads = 64 + kPairConvThreads;
+static_assert(kPairConvWarps % 4 == 0, "whole lane quadrants");
+static_assert(1 + 3 * kPairGroups <= 16, "named barrier ids");
 static_assert(kSmemTcPair <= 232448, "dynamic shared memory above the per-CTA limit");
 
 struct TcPairSmem {
@@ -386,7 +397,7 @@ struct TcPairSmem {
     int abort;
 };
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmArgs g) {
     extern __shared__ uint8_t smem_raw[];
@@ -494,15 +505,15 @@ sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         __syncwarp();
     } else {
         // ------------------------------------------------ hi/lo split, then epilogue (each CTA)
-        // Two groups of kConvWarps/2 warps take alternate K steps, so the split
-        // of one step overlaps that of the next; each group has its own named
-        // barriers (ids 1-3 and 4-6).
-        constexpr int kGroupThreads = kConvThreads / 2, kGroupWarps = kConvWarps / 2;
+        // kPairGroups groups of warps take K steps in turn (group g owns stage g),
+        // so the splits of consecutive steps overlap; each group has its own
+        // three named barriers.
+        constexpr int kGroupThreads = kPairConvThreads / kPairGroups, kGroupWarps = kPairConvWarps / kPairGroups;
         const int ct = tid - 64;
         const int grp = ct / kGroupThreads, gt = ct % kGroupThreads;
         const int bar0 = 1 + 3 * grp;
         bool ok = true;
-        for (int t = grp; t < nkt; t += 2) {
+        for (int t = grp; t < nkt; t += kPairGroups) {
             const int s = t % PSTAGES;
             const bool bad = !mbar_wait(&sh->full[s], (t / PSTAGES) & 1, g.status) || *abort_flag;
             if (named_barrier_or(bar0, kGroupThreads, bad)) {
@@ -525,9 +536,9 @@ sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         if (ok) ok = mbar_wait(&sh->acc_full, 0, g.status) && !*abort_flag;
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
-            constexpr int kColChunks = (2 * PBN / 16) / (kConvWarps / 4);
-            const int part = (warp - 2) >> 2;
-            tc_epilogue(g, tmem, warp & 3, lane, m0, n0, part * kColChunks, (part + 1) * kColChunks);
+            constexpr int kChunks = 2 * PBN / 16, kParts = kPairConvWarps / 4;
+            const int part = (warp - 2) >> 2;  // warps of one lane quadrant share the columns
+            tc_epilogue(g, tmem, warp & 3, lane, m0, n0, part * kChunks / kParts, (part + 1) * kChunks / kParts);
         }
     }
     // ---------------------------------------------------- teardown
@@ -551,7 +562,7 @@ cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CU
                              cudaStream_t stream) {
     const int tiles = ((g.M + 2 * TBM - 1) / (2 * TBM)) * ((g.N + 2 * PBN - 1) / (2 * PBN));
     const int smem = smem_override > 0 ? smem_override : kSmemTcPair;
-    sgemm_tc3x_pair_kernel<<<2 * tiles, kTcThreads, smem, stream>>>(tmA, tmB, g);
+    sgemm_tc3x_pair_kernel<<<2 * tiles, kPairThreads, smem, stream>>>(tmA, tmB, g);
     return cudaGetLastError();
 }
 
