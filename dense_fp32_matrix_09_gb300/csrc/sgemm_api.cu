@@ -32,6 +32,9 @@ struct sgemm_ctx {
     int smem_override;
     int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
     int math_mode;                          // sgemm_math_mode_t
+    cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
+    cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
+    cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
 };
 
 namespace {
@@ -288,6 +291,30 @@ int sgemm_create(sgemm_handle_t *out) {
         cudaGetLastError();
         return SGEMM_ERR_CUDA;
     }
+    bool ev_ok = cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
+                 cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t *e : {&h->ev_start, &h->ev_done})
+        ev_ok = ev_ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 16; ++i)
+        ev_ok = ev_ok && cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ev_ok) {
+        cudaGetLastError();
+        // free what was made; streams/events that failed are null and skipped
+        if (h->copy_in) cudaStreamDestroy(h->copy_in);
+        if (h->copy_out) cudaStreamDestroy(h->copy_out);
+        for (cudaEvent_t e : {h->ev_start, h->ev_done})
+            if (e) cudaEventDestroy(e);
+        for (int i = 0; i < 16; ++i) {
+            if (h->ev_in[i]) cudaEventDestroy(h->ev_in[i]);
+            if (h->ev_out[i]) cudaEventDestroy(h->ev_out[i]);
+        }
+        cudaFree(h->d_status);
+        cudaFree(h->d_ws);
+        cudaFree(h->d_counters);
+        delete h;
+        return SGEMM_ERR_CUDA;
+    }
     {
         std::lock_guard<std::mutex> lk(g_mu);
         g_live.insert(h);
@@ -305,6 +332,13 @@ int sgemm_destroy(sgemm_handle_t h) {
     cudaGetDevice(&prev);
     if (prev != h->device) cudaSetDevice(h->device);
     const cudaError_t e = cudaDeviceSynchronize();
+    cudaStreamDestroy(h->copy_in);
+    cudaStreamDestroy(h->copy_out);
+    for (cudaEvent_t ev : {h->ev_start, h->ev_done}) cudaEventDestroy(ev);
+    for (int i = 0; i < 16; ++i) {
+        cudaEventDestroy(h->ev_in[i]);
+        cudaEventDestroy(h->ev_out[i]);
+    }
     cudaFree(h->d_status);
     cudaFree(h->d_ws);
     cudaFree(h->d_counters);
@@ -413,6 +447,59 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
         h->last_splits = sk.splits;
     }
     return rc;
+}
+
+int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                   int ldb, float beta, float *C, int ldc, float *dA, float *dB, float *dC, void *stream_) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    int st = sgemm_check_args(M, N, K, alpha, dA, lda, dB, ldb, beta, dC, ldc);
+    if (st != SGEMM_OK) return st;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    const bool reads_ab = alpha != 0.f && K > 0;
+    if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const size_t f = sizeof(float);
+    // Row panels: multiples of 256 rows, at most 8 (and at most 16 events).
+    const int panels = std::max(1, std::min(8, M / 1024));
+    const int rows = ((cdiv(M, panels) + 255) / 256) * 256;
+    const int np = cdiv(M, rows);
+    if (np > 16) return SGEMM_ERR_INVALID_VALUE;
+
+    auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+    // nothing of this call starts before the caller's earlier work on `stream`
+    if (!ok(cudaEventRecord(h->ev_start, stream)) || !ok(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0)) ||
+        !ok(cudaStreamWaitEvent(h->copy_out, h->ev_start, 0)))
+        return SGEMM_ERR_CUDA;
+    // B first: every panel needs all of it (the copy stream is in order, so
+    // panel 0's event also covers B)
+    if (reads_ab && !ok(cudaMemcpy2DAsync(dB, ldb * f, B, ldb * f, N * f, K, cudaMemcpyHostToDevice, h->copy_in)))
+        return SGEMM_ERR_CUDA;
+    for (int p = 0; p < np; ++p) {
+        const int r0 = p * rows, nr = std::min(rows, M - r0);
+        if (reads_ab && !ok(cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * lda, lda * f,
+                                              A + static_cast<size_t>(r0) * lda, lda * f, K * f, nr,
+                                              cudaMemcpyHostToDevice, h->copy_in)))
+            return SGEMM_ERR_CUDA;
+        if (beta != 0.f && !ok(cudaMemcpy2DAsync(dC + static_cast<size_t>(r0) * ldc, ldc * f,
+                                                 C + static_cast<size_t>(r0) * ldc, ldc * f, N * f, nr,
+                                                 cudaMemcpyHostToDevice, h->copy_in)))
+            return SGEMM_ERR_CUDA;
+        if (!ok(cudaEventRecord(h->ev_in[p], h->copy_in)) || !ok(cudaStreamWaitEvent(stream, h->ev_in[p], 0)))
+            return SGEMM_ERR_CUDA;
+        st = sgemm_run(h, nr, N, K, alpha, dA + static_cast<size_t>(r0) * lda, lda, dB, ldb, beta,
+                       dC + static_cast<size_t>(r0) * ldc, ldc, stream_);
+        if (st != SGEMM_OK) return st;
+        if (!ok(cudaEventRecord(h->ev_out[p], stream)) || !ok(cudaStreamWaitEvent(h->copy_out, h->ev_out[p], 0)) ||
+            !ok(cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc, ldc * f, dC + static_cast<size_t>(r0) * ldc,
+                                  ldc * f, N * f, nr, cudaMemcpyDeviceToHost, h->copy_out)))
+            return SGEMM_ERR_CUDA;
+    }
+    // the caller's stream reaches this point only when every panel is back on the host
+    if (!ok(cudaEventRecord(h->ev_done, h->copy_out)) || !ok(cudaStreamWaitEvent(stream, h->ev_done, 0)))
+        return SGEMM_ERR_CUDA;
+    return SGEMM_OK;
 }
 
 int sgemm_get_device_status(sgemm_handle_t h) {

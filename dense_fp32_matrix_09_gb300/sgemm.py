@@ -44,7 +44,7 @@ GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
-           "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode")
+           "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host")
 
 
 class SgemmError(RuntimeError):
@@ -84,17 +84,21 @@ def lib() -> ctypes.CDLL:
         L.sgemm_variant_name.restype = ctypes.c_char_p
         L.sgemm_version.argtypes = []
         L.sgemm_set_math_mode.argtypes = [vp, i32]
+        L.sgemm_run_host.argtypes = [vp, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp, vp, vp]
         L.sgemm_run_noalloc.argtypes = [i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         _lib = L
     return _lib
 
 
 def _ptr(x) -> int | None:
+    """Address of a buffer: an int, a torch tensor (data_ptr) or a numpy array."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return int(x.data_ptr())
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x.__array_interface__["data"][0])
 
 
 def _stream(s) -> int:
@@ -147,6 +151,15 @@ def sgemm_run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None)
     _check(lib().sgemm_run_noalloc(int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
                                    int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream)),
            "sgemm_run_noalloc")
+
+
+def sgemm_run_host(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dA, dB, dC, stream=None) -> None:
+    """C <- alpha*A*B + beta*C with A, B, C in host memory (page-locked for
+    overlap), through the device staging buffers dA, dB, dC; copies overlap
+    the per-panel GEMMs.  C is complete once `stream` has reached the call."""
+    _check(lib().sgemm_run_host(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb),
+                                float(beta), _ptr(C), int(ldc), _ptr(dA), _ptr(dB), _ptr(dC), _stream(stream)),
+           "sgemm_run_host")
 
 
 def sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:

@@ -115,6 +115,24 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha,
               const float *A, int lda, const float *B, int ldb,
               float beta, float *C, int ldc, void *stream);
 
+/* C <- alpha*A*B + beta*C with A, B, C in HOST memory, transfers overlapped
+ * with compute.  dA, dB, dC are caller-owned DEVICE buffers of the same
+ * shapes and leading dimensions (M*lda, K*ldb, M*ldc floats at least); the
+ * library copies B to dB, then A (and C when beta != 0) in row panels to dA
+ * (dC) on one handle-owned copy stream, runs each panel's GEMM on `stream` as
+ * soon as its rows have landed (the same kernels and rules as sgemm_run), and
+ * copies each finished panel of dC back to C on a second copy stream while the
+ * next panel computes.  Returns after enqueueing; C is complete when `stream`
+ * reaches the point of the call (e.g. after cudaStreamSynchronize(stream)).
+ * Page-locked host buffers give asynchronous copies; pageable ones work but
+ * serialise.  The host and device windows must not be touched until then.
+ * Same argument checks as sgemm_run (on the device pointers; SGEMM_ERR_NULL
+ * also if a host pointer that is read or written is NULL).  No allocation. */
+int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha,
+                   const float *A, int lda, const float *B, int ldb,
+                   float beta, float *C, int ldc,
+                   float *dA, float *dB, float *dC, void *stream);
+
 /* Host-only validation with exactly the rules sgemm_run applies (no CUDA call,
  * no handle): SGEMM_ERR_INVALID_VALUE if M, N or K < 0, lda < max(1, K),
  * ldb < max(1, N) or ldc < max(1, N); then, unless M == 0 or N == 0,
