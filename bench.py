@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 # (profiles/sgemm_8192cube_dram.md, 8192^3 launches)
 TRAFFIC_BY_SOURCE = {"728b753fefc20bac": 3.116e9}
 TC_TRAFFIC_BY_SOURCE = {"d8ac4d90e2415f26": 3.112e9}
-KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma.cu",
+KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
 TC_KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tc.cu",
                      "dense_fp32_matrix_09_gb300/csrc/tcgen05.cuh",
@@ -67,6 +67,16 @@ def measured_bf16_tflops() -> dict:
         return {"value": 1900.0, "source": "fallback"}
 
 
+def measured_hbm_gbs() -> dict:
+    """HBM copy bandwidth measured on this machine (MEASURED_PEAKS.json), else
+    the profiling recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return {"value": float(json.load(f)["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"value": 6800.0, "source": "fallback"}
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -81,6 +91,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-tensor", action="store_true", help="skip the 3xTF32 tensor-core block")
     p.add_argument("--tensor-steps", type=int, default=50)
+    p.add_argument("--no-ex", action="store_true",
+                   help="skip the transposed-layout and strided-batched block (sgemm_run_ex)")
     return p.parse_args()
 
 
@@ -269,6 +281,64 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
         out["tflops_back_to_back"] = cfg.flops / (hot * 1e-3) / 1e12
     del A, B, C, C0
     return out
+
+
+def time_calls(torch, stream, call, reps: int, warmup: int, flush_buf=None) -> list[float]:
+    """Per-call device ms (CUDA events on the launching stream), L2 flushed
+    before each call when flush_buf is given."""
+    for _ in range(max(3, warmup)):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(reps):
+        if flush_buf is not None:
+            flush_l2(torch, flush_buf)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        ms.append(s.elapsed_time(e))
+    return ms
+
+
+def bench_ex(torch, sg, h, cfg, A, B, C, stream, warmup: int) -> dict:
+    n = cfg.M
+    flops = 2.0 * n * n * n
+    res = {}
+    for name, ta, tb in (("NN", 0, 0), ("NT", 0, 1), ("TN", 1, 0), ("TT", 1, 1)):
+        def call(ta=ta, tb=tb):
+            sg.sgemm_run_ex(h, ta, tb, n, n, n, 1.0, A, n, 0, B, n, 0, 0.0, C, n, 0, 1, stream)
+        ms = time_calls(torch, stream, call, 10, warmup)
+        v, splits = sg.sgemm_last_variant(h)
+        med = statistics.median(ms)
+        res[name] = {"ms_median": med, "tflops": flops / (med * 1e-3) / 1e12, "variant": sg.variant_name(v)}
+    # strided batch: 1024 x (64 x 64) x (64 x 64), contiguous; 48 MiB < L2, so L2 is flushed before each call
+    bs, m = 1024, 64
+    g = torch.Generator(device="cpu").manual_seed(3)
+    bA = (torch.rand(bs * m * m, generator=g) * 2 - 1).cuda()
+    bB = (torch.rand(bs * m * m, generator=g) * 2 - 1).cuda()
+    bC = torch.empty(bs * m * m, device="cuda")
+    flush_buf = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
+
+    def bcall():
+        sg.sgemm_run_ex(h, 0, 0, m, m, m, 1.0, bA, m, m * m, bB, m, m * m, 0.0, bC, m, m * m, bs, stream)
+    ms = time_calls(torch, stream, bcall, 50, warmup, flush_buf)
+    v, _ = sg.sgemm_last_variant(h)
+    med = statistics.median(ms)
+    bflops = 2.0 * bs * m * m * m
+    bbytes = 3 * bs * m * m * 4  # A and B read once, C written once (beta = 0)
+    hbm = measured_hbm_gbs()
+    res["batched_1024x64cube"] = {
+        "ms_median": med, "ms_min": min(ms), "tflops": bflops / (med * 1e-3) / 1e12,
+        "gbs_compulsory": bbytes / (med * 1e-3) / 1e9, "variant": sg.variant_name(v), "batch": bs,
+        "l2": "flushed before each call", "compulsory_bytes": bbytes,
+        "hbm_frac": (bbytes / (med * 1e-3) / 1e9) / hbm["value"] if hbm else None,
+        "hbm_peak_gbs": hbm["value"] if hbm else None,
+        "hbm_peak_source": hbm["source"] if hbm else None,
+    }
+    del bA, bB, bC, flush_buf
+    return res
 
 
 def main():
@@ -461,6 +531,11 @@ def main():
                                        f"(nominal ratio) = {tf32_peak:.1f}; 3 TF32 MMAs per FP32 product",
                          "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
         }
+
+    # ---- sgemm_run_ex: the four operand layouts on the headline shape, and a
+    # strided batch of 1024 products of 64 x 64 matrices (device-resident)
+    if not args.no_ex and rank == 0 and cfg.M == cfg.N == cfg.K == cfg.lda == cfg.ldb == cfg.ldc:
+        out["layouts_and_batched"] = bench_ex(torch, sg, h, cfg, A, B, C, stream, args.warmup)
 
     # ---- per-workload table (device-resident; not part of the headline value)
     if not args.no_workloads and rank == 0:

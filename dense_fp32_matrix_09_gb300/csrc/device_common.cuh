@@ -88,6 +88,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// 3-D tile load (x innermost, z outermost), otherwise as tma_load_2d.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y,
+                                            int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Prefetch a 2-D tile of a TMA tensor into L2 (no shared-memory destination,
 // no completion signal); the later TMA load of the same box then hits L2.
 __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {

@@ -24,6 +24,11 @@ struct GemmArgs {
     int ldc;
     bool vec_c;   // C is 16-byte aligned and ldc % 4 == 0: float4 epilogue
     int *status;  // device status word of the handle
+    // general form (sgemm_run_ex): matrix b of X starts at X + b * sX
+    int batch = 1;
+    long long sA = 0, sB = 0, sC = 0;
+    int transA = 0, transB = 0;  // A stored K x M / B stored N x K
+    int c_trans = 0;             // the kernel's M x N result is C^T: write element (i, j) to C[j][i]
 };
 
 // Static description of a TMA-fed SIMT variant.
@@ -46,14 +51,31 @@ struct SplitK {
     int dp_tiles;           // leading tiles computed whole (0: every tile is split)
 };
 
+// Operand layouts of the TMA-fed SIMT kernels: NN (A stored M x K, B K x N),
+// TN (A stored K x M) and NT (B stored N x K).  A map: box 32 x bm with the
+// 128-byte swizzle (NN, NT) or bm x 32 unswizzled (TN); B map: box bn x 32
+// unswizzled (NN, TN) or 32 x bn with the 128-byte swizzle (NT).  With
+// batch > 1 an operand whose batch stride is nonzero has a 3-D map (batch
+// outermost, box depth 1).
+constexpr int kTmaOpNN = 0, kTmaOpTN = 1, kTmaOpNT = 2;
+
 // variant ids are the public sgemm_variant_t values of the TMA variants
 bool tma_shape(int variant, TmaShape *out);
-cudaError_t tma_prepare(int variant);
+cudaError_t tma_prepare(int variant);  // every operand layout
 // Resident CTAs per SM of a variant's kernel (0 on error).
 int tma_ctas_per_sm(int variant);
 cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA,
                        const CUtensorMap &tmB, const SplitK &sk, int smem_override,
-                       cudaStream_t stream);
+                       cudaStream_t stream);  // NN
+cudaError_t launch_tma_op(int op, int variant, const GemmArgs &g, const CUtensorMap &tmA,
+                          const CUtensorMap &tmB, const SplitK &sk, int smem_override,
+                          cudaStream_t stream);
+cudaError_t tma_prepare_tn(int variant);
+cudaError_t launch_tma_tn(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const SplitK &sk, int smem_override, cudaStream_t stream);
+cudaError_t tma_prepare_nt(int variant);
+cudaError_t launch_tma_nt(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const SplitK &sk, int smem_override, cudaStream_t stream);
 
 // 3xTF32 tensor-core kernel (sgemm_tc.cu): A box 32 x 128 and B boxes 32 x 32,
 // both with the 128-byte swizzle.

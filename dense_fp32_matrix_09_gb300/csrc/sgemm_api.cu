@@ -100,6 +100,22 @@ bool encode_2d(CUtensorMap *map, const float *base, int rows, int cols, int ld, 
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One operand as a TMA tensor: rows x cols row-major (leading dimension ld);
+// with batch > 1 and a nonzero batch stride, 3-D with the batch outermost.
+bool encode_operand(CUtensorMap *map, const float *base, int rows, int cols, int ld, int batch, long long stride,
+                    int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+    if (batch <= 1 || stride == 0) return encode_2d(map, base, rows, cols, ld, box_cols, box_rows, swz);
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batch)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * sizeof(float),
+                             static_cast<cuuint64_t>(stride) * sizeof(float)};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Split count for the split-K variant: enough CTAs for two per SM, at least
 // one K step per split, and the partial tiles must fit the workspace.
 void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
@@ -152,36 +168,44 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
 // of FP32 peak with the GPU full: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
 // 0.73).  Complete waves occupy all P = SMs x CTAs-per-SM slots; a split
 // tail of S ranges occupies P / S; an unsplit partial wave occupies P.  The
-// split-K variant runs tiles x splits CTAs of 1/splits of a tile each.
-double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, sg::SplitK *plan) {
+// split-K variant runs tiles x splits CTAs of 1/splits of a tile each.  A
+// batch multiplies the tiles; batched calls are not split.
+double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, sg::SplitK *plan) {
     sg::TmaShape sh;
     if (!sg::tma_shape(variant, &sh)) return 1e300;
     const double eff = variant == SGEMM_VARIANT_TMA_128x256 ? 0.81
                      : variant == SGEMM_VARIANT_TMA_128x128 ? 0.80 : 0.73;
     const double P = static_cast<double>(h->num_sms) * std::max(1, h->ctas_per_sm[variant]);
     const double tile_flop = 2.0 * sh.bm * sh.bn * static_cast<double>(K);
-    const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn);
+    const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn) * batch;
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+        if (batch > 1) return 1e300;
         plan_splits(h, M, N, K, plan);
         const double ctas = tiles * plan->splits;
         return tile_flop / plan->splits * std::ceil(ctas / P) * P / eff;
     }
-    sg::TmaShape shape = sh;
-    plan_tail(h, variant, shape, M, N, K, plan);
+    if (batch > 1) {
+        *plan = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr, cdiv(M, sh.bm) * cdiv(N, sh.bn)};
+    } else {
+        sg::TmaShape shape = sh;
+        plan_tail(h, variant, shape, M, N, K, plan);
+    }
     const double full = std::floor(tiles / P), rem = tiles - full * P;
     const double tail = rem == 0 ? 0.0 : (plan->splits >= 2 ? P / plan->splits : P);
     return tile_flop * (full * P + tail) / eff;
 }
 
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
-// larger tile (listed first).
-int choose_variant(const sgemm_ctx *h, int M, int N, int K) {
+// larger tile (listed first).  The NT layout skips 128 x 128 (its kernel
+// exceeds the 128 registers a thread may use at two CTAs per SM).
+int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int op = sg::kTmaOpNN) {
     int best = SGEMM_VARIANT_TMA_128x256;
     double best_cost = 1e300;
     for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
                   SGEMM_VARIANT_TMA_64x64_SPLITK}) {
+        if (op == sg::kTmaOpNT && v == SGEMM_VARIANT_TMA_128x128) continue;
         sg::SplitK plan;
-        const double c = variant_cost(h, v, M, N, K, &plan);
+        const double c = variant_cost(h, v, M, N, K, batch, &plan);
         if (c < best_cost * 0.999) {
             best_cost = c;
             best = v;
@@ -228,22 +252,41 @@ const char *sgemm_variant_name(int v) {
     }
 }
 
-int sgemm_check_args(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
-                     float beta, const float *C, int ldc) {
+int sgemm_check_args_ex(int transA, int transB, int M, int N, int K, float alpha, const float *A, int lda,
+                        long long strideA, const float *B, int ldb, long long strideB, float beta, const float *C,
+                        int ldc, long long strideC, int batch) {
     (void)beta;
-    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
-    if (lda < std::max(1, K) || ldb < std::max(1, N) || ldc < std::max(1, N)) return SGEMM_ERR_INVALID_VALUE;
-    if (M == 0 || N == 0) return SGEMM_OK;
+    if (M < 0 || N < 0 || K < 0 || batch < 0) return SGEMM_ERR_INVALID_VALUE;
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return SGEMM_ERR_INVALID_VALUE;
+    const int a_rows = transA ? K : M, a_cols = transA ? M : K;  // A as stored
+    const int b_rows = transB ? N : K, b_cols = transB ? K : N;  // B as stored
+    if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
+        return SGEMM_ERR_INVALID_VALUE;
+    if (strideA < 0 || strideB < 0 || strideC < 0) return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
     if (C == nullptr) return SGEMM_ERR_NULL;
+    uintptr_t c0, c1;
+    window(C, M, N, ldc, &c0, &c1);
+    if (batch > 1) {
+        if (strideC < static_cast<long long>(c1 - c0) / static_cast<long long>(sizeof(float)))
+            return SGEMM_ERR_INVALID_VALUE;  // C matrices of the batch would overlap
+        c1 += static_cast<uintptr_t>(batch - 1) * static_cast<uintptr_t>(strideC) * sizeof(float);
+    }
     const bool reads_ab = (alpha != 0.f) && K > 0;
     if (!reads_ab) return SGEMM_OK;
     if (A == nullptr || B == nullptr) return SGEMM_ERR_NULL;
-    uintptr_t c0, c1, a0, a1, b0, b1;
-    window(C, M, N, ldc, &c0, &c1);
-    window(A, M, K, lda, &a0, &a1);
-    window(B, K, N, ldb, &b0, &b1);
+    uintptr_t a0, a1, b0, b1;
+    window(A, a_rows, a_cols, lda, &a0, &a1);
+    window(B, b_rows, b_cols, ldb, &b0, &b1);
+    a1 += static_cast<uintptr_t>(batch - 1) * static_cast<uintptr_t>(strideA) * sizeof(float);
+    b1 += static_cast<uintptr_t>(batch - 1) * static_cast<uintptr_t>(strideB) * sizeof(float);
     if (overlap(c0, c1, a0, a1) || overlap(c0, c1, b0, b1)) return SGEMM_ERR_ALIAS;
     return SGEMM_OK;
+}
+
+int sgemm_check_args(int M, int N, int K, float alpha, const float *A, int lda, const float *B, int ldb,
+                     float beta, const float *C, int ldc) {
+    return sgemm_check_args_ex(0, 0, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1);
 }
 
 int sgemm_create(sgemm_handle_t *out) {
@@ -377,18 +420,32 @@ int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes) {
 
 int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A, int lda, const float *B,
               int ldb, float beta, float *C, int ldc, void *stream_) {
+    return sgemm_run_ex(h, 0, 0, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1, stream_);
+}
+
+int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, float alpha, const float *A,
+                 int lda, long long strideA, const float *B, int ldb, long long strideB, float beta, float *C,
+                 int ldc, long long strideC, int batch, void *stream_) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
-    const int st = sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    const int st = sgemm_check_args_ex(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+                                       ldc, strideC, batch);
     if (st != SGEMM_OK) return st;
     h->last_variant = -1;
     h->last_splits = 1;
-    if (M == 0 || N == 0) return SGEMM_OK;
+    if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (batch == 1) strideA = strideB = strideC = 0;  // unused: keep the kernels on 2-D maps
 
     sg::GemmArgs g{M, N, K, alpha, beta, A, lda, B, ldb, C, ldc,
-                   aligned16(C) && (ldc % 4) == 0, h->d_status};
+                   aligned16(C) && (ldc % 4) == 0 && (strideC % 4) == 0, h->d_status};
+    g.batch = batch;
+    g.sA = strideA;
+    g.sB = strideB;
+    g.sC = strideC;
+    g.transA = transA;
+    g.transB = transB;
     if (alpha == 0.f || K == 0) {
         // C = beta*C (C = 0 when beta == 0); beta == 1 leaves C as it is.
         int rc = SGEMM_OK;
@@ -396,24 +453,39 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
         if (rc == SGEMM_OK) h->last_variant = SGEMM_VARIANT_SCALE;
         return rc;
     }
-    const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0;
+
+    // Arguments of the TMA kernels: A^T B^T runs as the NN kernel on the
+    // swapped operands (C^T = B_s A_s) with a transposed epilogue.
+    sg::GemmArgs k = g;
+    int op = transA ? (transB ? sg::kTmaOpNN : sg::kTmaOpTN) : (transB ? sg::kTmaOpNT : sg::kTmaOpNN);
+    if (transA && transB) {
+        k.M = N;
+        k.N = M;
+        k.A = B;
+        k.lda = ldb;
+        k.sA = strideB;
+        k.B = A;
+        k.ldb = lda;
+        k.sB = strideA;
+        k.c_trans = 1;
+        k.vec_c = false;
+    }
+    const bool nn1 = !transA && !transB && batch == 1;
+    const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
+                        (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
     int variant = h->pinned;
+    if (!nn1 && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
+        variant = SGEMM_VARIANT_AUTO;  // the tensor-core kernels serve NN with batch 1
     if (variant == SGEMM_VARIANT_AUTO) {
         // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
         // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
         const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
-        if (h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
+        if (nn1 && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
             variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
         else
-            variant = choose_variant(h, M, N, K);
+            variant = choose_variant(h, k.M, k.N, K, batch, op);
     }
     if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
-
-    if (variant == SGEMM_VARIANT_GENERIC) {
-        const int rc = from_cuda(sg::launch_generic(g, stream));
-        if (rc == SGEMM_OK) h->last_variant = variant;
-        return rc;
-    }
 
     if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
         sg::TmaShape ts;
@@ -430,18 +502,30 @@ int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha, const float *A
     }
 
     sg::TmaShape sh;
-    if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
-    sg::SplitK sk{1, cdiv(K, sh.bk), nullptr, nullptr, 0};
-    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
-        plan_splits(h, M, N, K, &sk);
-        if (sk.splits <= 1) variant = SGEMM_VARIANT_TMA_64x64;
-    }
-    if (variant != SGEMM_VARIANT_TMA_64x64_SPLITK) plan_tail(h, variant, sh, M, N, K, &sk);
     CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, B, K, N, ldb, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE))
-        return SGEMM_ERR_CUDA;
-    const int rc = from_cuda(sg::launch_tma(variant, g, tmA, tmB, sk, h->smem_override, stream));
+    sg::SplitK sk{1, cdiv(K, 32), nullptr, nullptr, 0};
+    if (variant != SGEMM_VARIANT_GENERIC) {
+        if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
+        sk = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn)};
+        if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+            if (batch == 1) plan_splits(h, k.M, k.N, K, &sk);
+            if (sk.splits <= 1) variant = SGEMM_VARIANT_TMA_64x64;
+        }
+        if (variant != SGEMM_VARIANT_TMA_64x64_SPLITK && batch == 1) plan_tail(h, variant, sh, k.M, k.N, K, &sk);
+        const bool a_ok = op == sg::kTmaOpTN
+            ? encode_operand(&tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
+            : encode_operand(&tmA, k.A, k.M, K, k.lda, batch, k.sA, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B);
+        const bool b_ok = op == sg::kTmaOpNT
+            ? encode_operand(&tmB, k.B, k.N, K, k.ldb, batch, k.sB, sh.bk, sh.bn, CU_TENSOR_MAP_SWIZZLE_128B)
+            : encode_operand(&tmB, k.B, K, k.N, k.ldb, batch, k.sB, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!a_ok || !b_ok) variant = SGEMM_VARIANT_GENERIC;  // a layout TMA cannot describe
+    }
+    if (variant == SGEMM_VARIANT_GENERIC) {
+        const int rc = from_cuda(sg::launch_generic(g, stream));
+        if (rc == SGEMM_OK) h->last_variant = variant;
+        return rc;
+    }
+    const int rc = from_cuda(sg::launch_tma_op(op, variant, k, tmA, tmB, sk, h->smem_override, stream));
     if (rc == SGEMM_OK) {
         h->last_variant = variant;
         h->last_splits = sk.splits;

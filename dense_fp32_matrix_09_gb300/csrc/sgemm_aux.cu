@@ -29,55 +29,67 @@ __global__ void __launch_bounds__(GT) sgemm_generic_kernel(const GemmArgs g) {
     __shared__ float Bs[GK][GB + 4];  // B tile: Bs[k][n]
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     const int m0 = blockIdx.y * GB, n0 = blockIdx.x * GB;
-    float acc[4][4] = {};
-    for (int k0 = 0; k0 < g.K; k0 += GK) {
+    for (int b = blockIdx.z; b < g.batch; b += gridDim.z) {
+        const float *Ab = g.A + b * g.sA, *Bb = g.B + b * g.sB;
+        float *Cb = g.C + b * g.sC;
+        float acc[4][4] = {};
+        for (int k0 = 0; k0 < g.K; k0 += GK) {
 #pragma unroll
-        for (int r = 0; r < (GB * GK) / GT; ++r) {
-            const int e = tid + r * GT;
-            // A: 64 rows x 16 k; consecutive threads walk k (coalesced along rows)
-            const int am = e / GK, ak = e % GK;
-            const int gm = m0 + am, gk = k0 + ak;
-            As[ak][am] = (gm < g.M && gk < g.K) ? g.A[static_cast<size_t>(gm) * g.lda + gk] : 0.f;
-            // B: 16 k x 64 cols; consecutive threads walk n
-            const int bk = e / GB, bn = e % GB;
-            const int hk = k0 + bk, hn = n0 + bn;
-            Bs[bk][bn] = (hk < g.K && hn < g.N) ? g.B[static_cast<size_t>(hk) * g.ldb + hn] : 0.f;
+            for (int r = 0; r < (GB * GK) / GT; ++r) {
+                const int e = tid + r * GT;
+                // consecutive threads walk the contiguous index of each stored operand
+                int am, ak;
+                if (g.transA) { ak = e / GB; am = e % GB; } else { am = e / GK; ak = e % GK; }
+                const int gm = m0 + am, gk = k0 + ak;
+                float av = 0.f;
+                if (gm < g.M && gk < g.K)
+                    av = g.transA ? Ab[static_cast<size_t>(gk) * g.lda + gm] : Ab[static_cast<size_t>(gm) * g.lda + gk];
+                As[ak][am] = av;
+                int bk, bn;
+                if (g.transB) { bn = e / GK; bk = e % GK; } else { bk = e / GB; bn = e % GB; }
+                const int hk = k0 + bk, hn = n0 + bn;
+                float bv = 0.f;
+                if (hk < g.K && hn < g.N)
+                    bv = g.transB ? Bb[static_cast<size_t>(hn) * g.ldb + hk] : Bb[static_cast<size_t>(hk) * g.ldb + hn];
+                Bs[bk][bn] = bv;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 0; k < GK; ++k) {
+                float a[4], bb[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) bb[j] = Bs[k][tx + 16 * j];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bb[j], acc[i][j]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
 #pragma unroll
-        for (int k = 0; k < GK; ++k) {
-            float a[4], b[4];
+        for (int i = 0; i < 4; ++i) {
+            const int row = m0 + ty + 16 * i;
+            if (row >= g.M) continue;
+            float *crow = Cb + static_cast<size_t>(row) * g.ldc;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = As[k][ty + 16 * i];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) b[j] = Bs[k][tx + 16 * j];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int row = m0 + ty + 16 * i;
-        if (row >= g.M) continue;
-        float *crow = g.C + static_cast<size_t>(row) * g.ldc;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int col = n0 + tx + 16 * j;
-            if (col >= g.N) continue;
-            float r = g.alpha * acc[i][j];
-            if (g.beta != 0.f) r = fmaf(g.beta, crow[col], r);
-            crow[col] = r;
+            for (int j = 0; j < 4; ++j) {
+                const int col = n0 + tx + 16 * j;
+                if (col >= g.N) continue;
+                float r = g.alpha * acc[i][j];
+                if (g.beta != 0.f) r = fmaf(g.beta, crow[col], r);
+                crow[col] = r;
+            }
         }
     }
 }
 
 __global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
     const int stride_x = gridDim.x * blockDim.x * 4;
+    for (int b = blockIdx.z; b < g.batch; b += gridDim.z)
     for (int row = blockIdx.y; row < g.M; row += gridDim.y) {
-        float *crow = g.C + static_cast<size_t>(row) * g.ldc;
+        float *crow = g.C + b * g.sC + static_cast<size_t>(row) * g.ldc;
         for (int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4; col < g.N; col += stride_x) {
             if (g.vec_c && col + 3 < g.N) {
                 float4 *p = reinterpret_cast<float4 *>(crow + col);
@@ -109,7 +121,7 @@ __global__ void timeout_probe_kernel(int *status, long long limit_ns) {
 }  // namespace
 
 cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream) {
-    const dim3 grid((g.N + GB - 1) / GB, (g.M + GB - 1) / GB);
+    const dim3 grid((g.N + GB - 1) / GB, (g.M + GB - 1) / GB, min(g.batch, 65535));
     sgemm_generic_kernel<<<grid, GT, 0, stream>>>(g);
     return cudaGetLastError();
 }
@@ -117,7 +129,8 @@ cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream) {
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
     const int gx = min((g.N + 1023) / 1024, 8);
     const int gy = min(g.M, 8192);
-    sgemm_scale_kernel<<<dim3(gx, gy), 256, 0, stream>>>(g);
+    const int gz = min(g.batch, max(1, 65535 / gy));
+    sgemm_scale_kernel<<<dim3(gx, gy, gz), 256, 0, stream>>>(g);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,567 @@
+// TMA-fed SIMT FP32 GEMM for sm_103a: C = alpha*A*B + beta*C, row-major.
+//
+// Design (restated for GB300 from the tiling ideas on the pages: shared-memory
+// tiles with zero-filled edges -- page m.lqnn.cn/news/94381 sections 2.3 and
+// 3; padded / rearranged shared memory against bank conflicts -- same page
+// section 4.3 and the page "GEMM advanced: co-optimising instruction-level
+// parallelism and bank conflicts" section 3; a multi-buffered pipeline --
+// that page's section 2; register-blocked outer products with an alpha/beta
+// epilogue -- page "Deep dive into the sgemmNN algorithm", main-loop and
+// write-back sections):
+//
+//  * One CTA computes a BM x BN tile of C.  K is streamed in steps of BK = 32
+//    through an S-stage ring of shared-memory buffers filled by 2-D TMA
+//    loads; a full/empty mbarrier pair per stage hands buffers between the
+//    TMA engine and the warps.  Thread 0 issues the loads: S tiles up front,
+//    then, at the start of step i, the refill of the stage that step i-1
+//    used, once every thread has released it (S-1 steps of look-ahead).  No
+//    warp is set aside for this: with 8 warps every SM sub-partition holds 2
+//    warps and each thread may use up to 255 registers, which the 128
+//    accumulators of the largest tile need.  TMA
+//    zero-fills every element outside [0,M) x [0,K) and [0,K) x [0,N), so
+//    ragged edges need no code in the main loop and padding cells of the
+//    leading dimensions are never read.
+//  * The A stage is BM rows of 32 floats (128 B) as TMA writes them with the
+//    128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
+//    A thread reads A[r][k..k+3] with one 16-byte shared load; the rows one
+//    warp-wide load touches are 8 (or 4) consecutive rows, which the swizzle
+//    spreads over distinct banks.  The B stage is 32 rows of BN floats
+//    (no swizzle); a warp-wide load reads contiguous 16-byte chunks.
+//  * Consumer warps are arranged WARPS_M x WARPS_N; each lane owns a TM x TN
+//    register block (rows strided by the lanes along M, columns as float4
+//    groups strided by the lanes along N) and performs TM*TN independent
+//    FMA chains per k.  The FMAs are issued as packed FP32x2 FMAs
+//    (__ffma2_rn: A value broadcast to both halves, two adjacent B columns):
+//    two FMAs per instruction halve the issue slots the FMA pipe needs, which
+//    is what lets the pipe, rather than instruction issue, bound the loop.
+//  * Epilogue: C = alpha*acc + beta*C with float4 accesses when C is 16-byte
+//    aligned and ldc % 4 == 0 (scalar at the ragged N edge); C is not read
+//    when beta == 0.
+//  * Split-K variant: CTAs along grid z take disjoint K ranges, write their
+//    partial tiles to a workspace, and the last CTA of a tile to arrive
+//    (arrival counter) adds the partials in ascending split order -- a fixed
+//    order, so results are deterministic -- and runs the epilogue.
+//
+//  * Operand layouts (template parameter OP).  NN: A stored M x K and B
+//    stored K x N, as above.  TN: A stored K x M; its stage is BK rows of BM
+//    floats (no swizzle) and each thread owns groups of 4 consecutive rows,
+//    so one 16-byte load gives the A values of 4 rows at one k.  NT: B
+//    stored N x K; its stage is BN rows of 32 floats with the 128-byte
+//    swizzle, a 16-byte load gives 4 k values of one column, and the packed
+//    FMAs pair two rows of A (built in registers) with one broadcast B value;
+//    lanes are arranged so the 4 column rows one quarter-warp reads fall in
+//    distinct swizzle rows.  In every layout each accumulator takes its
+//    products in ascending k with one rounding per FMA, so NN, TN and NT give
+//    the same bits for the same logical operands.  A x B with both operands
+//    transposed runs as the NN kernel on the swapped operands (C^T = B_s A_s,
+//    with B_s the stored N x K matrix and A_s the stored K x M one) with an
+//    epilogue that writes the tile transposed (GemmArgs::c_trans).
+//  * Strided batches: grid y is the batch index; an operand with a nonzero
+//    batch stride is described by a 3-D tensor map (batch outermost), one
+//    with stride 0 by a 2-D map shared by all products, and C of product b
+//    starts at C + b * strideC.
+//
+// Every wait is bounded (device_common.cuh); on a timeout the kernel records
+// it in the status word and returns without writing C.
+#pragma once
+
+#include <cstdio>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "sgemm.h"
+
+namespace sg {
+namespace {
+
+// Operand layouts of the kernel (OP).
+constexpr int kOpNN = 0, kOpTN = 1, kOpNT = 2;
+
+template <int BM_, int BN_, int WARPS_M_, int WARPS_N_, int TM_, int TN_, int STAGES_, int MIN_CTAS_>
+struct Cfg {
+    static constexpr int BM = BM_, BN = BN_, BK = 32;
+    static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_;
+    static constexpr int TM = TM_, TN = TN_, STAGES = STAGES_, MIN_CTAS = MIN_CTAS_;
+    static constexpr int kConsumerWarps = WARPS_M * WARPS_N;
+    static constexpr int kConsumers = 32 * kConsumerWarps;
+    static constexpr int kThreads = kConsumers;
+    static constexpr int WTM = BM / WARPS_M, WTN = BN / WARPS_N;
+    static constexpr int LANES_M = WTM / TM, LANES_N = WTN / TN;
+    static constexpr int TN4 = TN / 4;
+    static constexpr int kABytes = BM * BK * 4;  // one stage of A: BM rows of 128 B
+    static constexpr int kBBytes = BK * BN * 4;  // one stage of B: BK rows of BN floats
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 16 + 1024;
+    static_assert(LANES_M * LANES_N == 32, "warp tile must map onto 32 lanes");
+    static_assert(WTM % TM == 0 && WTN % TN == 0 && TN % 4 == 0, "bad thread tile");
+    static_assert(BM % 8 == 0 && (kABytes % 1024) == 0, "A stages must stay 1024-byte aligned");
+    static_assert(BM <= 256 && BN <= 256, "TMA box extents are at most 256");
+    static_assert(LANES_M % 4 == 0 && LANES_N % 2 == 0, "NT lane layout needs 4 x 2 lanes per quarter-warp");
+    static_assert(TM % 4 == 0 && (kBBytes % 1024) == 0, "TN row groups / NT swizzled B stages");
+};
+
+// Tile rows per raster group (see tile_coords).
+constexpr int kGroupM = 8;
+
+using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
+using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
+using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 2>;      // SGEMM_VARIANT_TMA_64x64 (+ split-K)
+
+// Lane coordinates inside the warp tile.  NT: each quarter-warp holds 4
+// lane rows x 2 lane columns, so the column rows of B it reads (4 apart)
+// fall in distinct 128-byte-swizzle rows; otherwise lanes run along N first.
+template <class C, int OP>
+__device__ __forceinline__ void lane_coords(int lane, int &lane_m, int &lane_n) {
+    if (OP == kOpNT) {
+        constexpr int a = C::LANES_M / 4;
+        lane_m = (lane & 3) + 4 * ((lane >> 3) % a);
+        lane_n = ((lane >> 2) & 1) + 2 * ((lane >> 3) / a);
+    } else {
+        lane_m = lane / C::LANES_N;
+        lane_n = lane % C::LANES_N;
+    }
+}
+
+// Tile row of a thread's accumulator row ii: rows strided by the lanes along
+// M, or (TN) groups of 4 consecutive rows strided by 4 x the lanes along M.
+template <class C, int OP>
+__device__ __forceinline__ int tile_row(int wm, int lane_m, int ii) {
+    if (OP == kOpTN) return wm * C::WTM + (ii / 4) * C::LANES_M * 4 + lane_m * 4 + (ii & 3);
+    return wm * C::WTM + ii * C::LANES_M + lane_m;
+}
+
+// Tile column of accumulator column j: groups of 4 consecutive columns.
+template <class C>
+__device__ __forceinline__ int tile_col(int wn, int lane_n, int j) {
+    return wn * C::WTN + (j / 4) * C::LANES_N * 4 + lane_n * 4 + (j & 3);
+}
+
+template <class C, int OP>
+__device__ __forceinline__ void epilogue(float (&acc)[C::TM][C::TN], const GemmArgs &g, float *Cb, int m0,
+                                         int n0, int wm, int wn, int lane_m, int lane_n) {
+    if (g.c_trans) {
+        // the tile is of C^T: element (row, col) goes to C[col][row]
+#pragma unroll
+        for (int ii = 0; ii < C::TM; ++ii) {
+            const int row = m0 + tile_row<C, OP>(wm, lane_m, ii);
+            if (row >= g.M) continue;
+#pragma unroll
+            for (int j = 0; j < C::TN; ++j) {
+                const int col = n0 + tile_col<C>(wn, lane_n, j);
+                if (col >= g.N) continue;
+                float *p = Cb + static_cast<size_t>(col) * g.ldc + row;
+                float r = g.alpha * acc[ii][j];
+                if (g.beta != 0.f) r = fmaf(g.beta, *p, r);
+                *p = r;
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int ii = 0; ii < C::TM; ++ii) {
+        const int row = m0 + tile_row<C, OP>(wm, lane_m, ii);
+        if (row >= g.M) continue;
+        float *crow = Cb + static_cast<size_t>(row) * g.ldc;
+#pragma unroll
+        for (int jj = 0; jj < C::TN4; ++jj) {
+            const int col = n0 + tile_col<C>(wn, lane_n, 4 * jj);
+            float o[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o[v] = g.alpha * acc[ii][4 * jj + v];
+            if (g.vec_c && col + 3 < g.N) {
+                float4 *p = reinterpret_cast<float4 *>(crow + col);
+                if (g.beta != 0.f) {
+                    const float4 c = *p;
+                    o[0] = fmaf(g.beta, c.x, o[0]);
+                    o[1] = fmaf(g.beta, c.y, o[1]);
+                    o[2] = fmaf(g.beta, c.z, o[2]);
+                    o[3] = fmaf(g.beta, c.w, o[3]);
+                }
+                *p = make_float4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    if (col + v < g.N) {
+                        float r = o[v];
+                        if (g.beta != 0.f) r = fmaf(g.beta, crow[col + v], r);
+                        crow[col + v] = r;
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Component kk (0..3) of a float4 (kk is a compile-time constant after unrolling).
+__device__ __forceinline__ float comp(const float4 &v, int kk) {
+    return kk == 0 ? v.x : kk == 1 ? v.y : kk == 2 ? v.z : v.w;
+}
+
+// Packed FP32x2 FMA: two independent round-to-nearest FMAs per instruction
+// (the same results as two fmaf calls).
+__device__ __forceinline__ void fma2(float a0, float a1, float b0, float b1, float &c0, float &c1) {
+    const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(c0, c1));
+    c0 = r.x;
+    c1 = r.y;
+}
+
+// Grouped tile order: CTA `pid` of a 1-D grid works on output tile (tm, tn).
+// Tiles are taken in groups of `group_m` tile rows, walking down the rows of
+// a group first, so the CTAs resident at one time cover a compact block of C
+// and share A row-panels and B column-panels in L2.
+__device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, int group_m, int &tm,
+                                            int &tn) {
+    const int per_group = group_m * tiles_n;
+    const int grp = pid / per_group;
+    const int first_m = grp * group_m;
+    const int rows = min(tiles_m - first_m, group_m);
+    const int r = pid - grp * per_group;
+    tm = first_m + r % rows;
+    tn = r / rows;
+}
+
+// One pipeline stage (BK = 32 k values) of the outer products, NN layout:
+// A stage = BM rows of 32 floats (128-byte swizzle), B stage = 32 rows of BN
+// floats.  A 16-byte load gives 4 k values of one A row (broadcast to both
+// halves of the packed FMA) and 4 columns of B at one k (two column pairs).
+template <class C>
+__device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
+                                            int wm, int wn, int lane_m, int lane_n) {
+    const uint8_t *a_thr = a_st + (wm * C::WTM + lane_m) * 128;
+    const float *b_thr = reinterpret_cast<const float *>(b_st) + wn * C::WTN + lane_n * 4;
+#pragma unroll
+    for (int kb = 0; kb < C::BK / 4; ++kb) {
+        float4 a[C::TM];
+#pragma unroll
+        for (int ii = 0; ii < C::TM; ++ii) {
+            const int rx = (ii * C::LANES_M + lane_m) & 7;  // row & 7 (WTM is a multiple of 8)
+            a[ii] = *reinterpret_cast<const float4 *>(a_thr + ii * C::LANES_M * 128 + ((kb ^ rx) << 4));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            float4 b[C::TN4];
+#pragma unroll
+            for (int jj = 0; jj < C::TN4; ++jj)
+                b[jj] = *reinterpret_cast<const float4 *>(b_thr + (kb * 4 + kk) * C::BN + jj * C::LANES_N * 4);
+#pragma unroll
+            for (int ii = 0; ii < C::TM; ++ii) {
+                const float av = comp(a[ii], kk);
+#pragma unroll
+                for (int jj = 0; jj < C::TN4; ++jj) {
+                    fma2(av, av, b[jj].x, b[jj].y, acc[ii][4 * jj + 0], acc[ii][4 * jj + 1]);
+                    fma2(av, av, b[jj].z, b[jj].w, acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]);
+                }
+            }
+        }
+    }
+}
+
+// TN layout: A stage = 32 rows (k) of BM floats, no swizzle.  A 16-byte load
+// gives one k of 4 consecutive A rows of the thread (its row groups); B as NN.
+template <class C>
+__device__ __forceinline__ void mainloop_tn(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
+                                            int wm, int wn, int lane_m, int lane_n) {
+    const float *a_thr = reinterpret_cast<const float *>(a_st) + wm * C::WTM + lane_m * 4;
+    const float *b_thr = reinterpret_cast<const float *>(b_st) + wn * C::WTN + lane_n * 4;
+#pragma unroll
+    for (int k = 0; k < C::BK; ++k) {
+        float4 a[C::TM / 4], b[C::TN4];
+#pragma unroll
+        for (int q = 0; q < C::TM / 4; ++q)
+            a[q] = *reinterpret_cast<const float4 *>(a_thr + k * C::BM + q * C::LANES_M * 4);
+#pragma unroll
+        for (int jj = 0; jj < C::TN4; ++jj)
+            b[jj] = *reinterpret_cast<const float4 *>(b_thr + k * C::BN + jj * C::LANES_N * 4);
+#pragma unroll
+        for (int ii = 0; ii < C::TM; ++ii) {
+            const float av = comp(a[ii / 4], ii & 3);
+#pragma unroll
+            for (int jj = 0; jj < C::TN4; ++jj) {
+                fma2(av, av, b[jj].x, b[jj].y, acc[ii][4 * jj + 0], acc[ii][4 * jj + 1]);
+                fma2(av, av, b[jj].z, b[jj].w, acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]);
+            }
+        }
+    }
+}
+
+// NT layout: A as NN; B stage = BN rows (columns of op(B)) of 32 floats with
+// the 128-byte swizzle.  A 16-byte load gives 4 k values of one column; the
+// packed FMA takes two A rows (paired in registers) and one broadcast B value.
+template <class C>
+__device__ __forceinline__ void mainloop_nt(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
+                                            int wm, int wn, int lane_m, int lane_n) {
+    const uint8_t *a_thr = a_st + (wm * C::WTM + lane_m) * 128;
+    const int nb = wn * C::WTN + lane_n * 4;  // the thread's first column row; other groups are 8-row aligned
+#pragma unroll
+    for (int kb = 0; kb < C::BK / 4; ++kb) {
+        float4 a[C::TM];
+#pragma unroll
+        for (int ii = 0; ii < C::TM; ++ii) {
+            const int rx = (ii * C::LANES_M + lane_m) & 7;
+            a[ii] = *reinterpret_cast<const float4 *>(a_thr + ii * C::LANES_M * 128 + ((kb ^ rx) << 4));
+        }
+#pragma unroll
+        for (int jj = 0; jj < C::TN4; ++jj) {
+            float4 b[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int n = nb + jj * C::LANES_N * 4 + v;
+                b[v] = *reinterpret_cast<const float4 *>(b_st + n * 128 + ((kb ^ (n & 7)) << 4));
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int p = 0; p < C::TM / 2; ++p) {
+                    const float a0 = comp(a[2 * p], kk), a1 = comp(a[2 * p + 1], kk);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const float bv = comp(b[v], kk);
+                        fma2(a0, a1, bv, bv, acc[2 * p][4 * jj + v], acc[2 * p + 1][4 * jj + v]);
+                    }
+                }
+        }
+    }
+}
+
+template <class C, bool SPLIT, int OP>
+__global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
+sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const GemmArgs g, const SplitK sk, const int group_m) {
+    extern __shared__ uint8_t smem_raw[];
+    // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B.
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    uint8_t *sA = smem;                                  // STAGES x kABytes
+    uint8_t *sB = smem + C::STAGES * C::kABytes;         // STAGES x kBBytes
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::kStageBytes);
+    uint64_t *empty = full + C::STAGES;
+    int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
+    const int k_tiles = (g.K + C::BK - 1) / C::BK;
+    // CTAs [0, dp_tiles) take whole tiles; the rest take one of `splits` K
+    // ranges of the remaining tiles (split index z).  Split only with batch 1.
+    int tile = blockIdx.x, z = 0, nsplit = 1;
+    if (SPLIT && tile >= sk.dp_tiles) {
+        const int q = tile - sk.dp_tiles;
+        tile = sk.dp_tiles + q / sk.splits;
+        z = q % sk.splits;
+        nsplit = sk.splits;
+    }
+    int tm, tn;
+    tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+    const int m0 = tm * C::BM, n0 = tn * C::BN;
+    int kt0 = 0, nkt = k_tiles;
+    if (nsplit > 1) {
+        kt0 = z * sk.k_tiles_per_split;
+        nkt = min(k_tiles - kt0, sk.k_tiles_per_split);  // >= 1: the host sizes the splits
+    }
+    // batch entry of this CTA; an operand with a batch stride has a 3-D map
+    const int bat = blockIdx.y;
+    const bool a3 = g.batch > 1 && g.sA != 0, b3 = g.batch > 1 && g.sB != 0;
+    float *Cb = g.C + static_cast<long long>(bat) * g.sC;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kConsumers);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Thread 0 issues the TMA loads of k-step t into stage t % STAGES.
+    auto issue = [&](int t) {
+        const int s = t % C::STAGES;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        const int kc = (kt0 + t) * C::BK;
+        const int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
+        const int bx = OP == kOpNT ? kc : n0, by = OP == kOpNT ? n0 : kc;
+        if (a3) tma_load_3d(sA + s * C::kABytes, &tmA, &full[s], ax, ay, bat);
+        else tma_load_2d(sA + s * C::kABytes, &tmA, &full[s], ax, ay);
+        if (b3) tma_load_3d(sB + s * C::kBBytes, &tmB, &full[s], bx, by, bat);
+        else tma_load_2d(sB + s * C::kBBytes, &tmB, &full[s], bx, by);
+    };
+    int issued = 0;
+    if (tid == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+        for (; issued < min(nkt, C::STAGES); ++issued) issue(issued);
+    }
+
+    // ---------------------------------------------------- consumer warps
+    const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
+    int lane_m, lane_n;
+    lane_coords<C, OP>(lane, lane_m, lane_n);
+
+    float acc[C::TM][C::TN];
+#pragma unroll
+    for (int ii = 0; ii < C::TM; ++ii)
+#pragma unroll
+        for (int j = 0; j < C::TN; ++j) acc[ii][j] = 0.f;
+
+    bool aborted = false;
+    for (int i = 0; i < nkt; ++i) {
+        const int s = i % C::STAGES;
+        if (tid == 0 && i >= 1 && i - 1 + C::STAGES < nkt) {
+            // refill the stage step i-1 used once all threads have released it
+            const int t = i - 1;
+            if (!mbar_wait(&empty[t % C::STAGES], (t / C::STAGES) & 1, g.status)) {
+                aborted = true;
+                break;
+            }
+            issue(t + C::STAGES);
+            ++issued;
+        }
+        if (!mbar_wait(&full[s], (i / C::STAGES) & 1, g.status)) {
+            aborted = true;
+            break;
+        }
+        const uint8_t *a_st = sA + s * C::kABytes;
+        const uint8_t *b_st = sB + s * C::kBBytes;
+        if constexpr (OP == kOpNN) mainloop_nn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+        else if constexpr (OP == kOpTN) mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+        else mainloop_nt<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+        mbar_arrive(&empty[s]);
+    }
+
+    if (aborted && tid == 0) {
+        // Wait (bounded) for the loads still in flight so that the CTA never
+        // exits while TMA writes into its shared memory.
+        for (int t = max(0, issued - C::STAGES); t < issued; ++t)
+            mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
+    }
+    if (nsplit == 1) {  // uniform per CTA
+        if (!aborted) epilogue<C, OP>(acc, g, Cb, m0, n0, wm, wn, lane_m, lane_n);
+        return;
+    }
+
+    // ------------------------------------------------------- split-K tail
+    // All threads reach this barrier (every wait above is bounded), so an
+    // abort by any of them is seen by all and the tile is left untouched.
+    if (named_barrier_or(1, C::kConsumers, aborted)) return;
+    const int slot = tile - sk.dp_tiles;  // index among the split tiles
+    constexpr int kQ = C::TM * C::TN4;    // float4 groups per thread
+    constexpr size_t kTileFloats = static_cast<size_t>(C::BM) * C::BN;
+    const float4 *part = reinterpret_cast<const float4 *>(sk.ws + static_cast<size_t>(slot) * nsplit * kTileFloats);
+    {
+        // partial tile of split z, thread-major: float4 group q of thread t at [q * threads + t]
+        float4 *mine = reinterpret_cast<float4 *>(sk.ws + (static_cast<size_t>(slot) * nsplit + z) * kTileFloats);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+            const int ii = q / C::TN4, jj = q % C::TN4;
+            __stcg(mine + q * C::kConsumers + tid, make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1],
+                                                               acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
+        }
+    }
+    __threadfence();
+    named_barrier_sync(1, C::kConsumers);
+    if (tid == 0) {
+        const int prev = atomicAdd(&sk.counters[slot], 1);
+        *s_flag = (prev == nsplit - 1);
+    }
+    named_barrier_sync(1, C::kConsumers);
+    if (!*s_flag) return;
+    __threadfence();
+    // Last CTA of this tile: sum all partials (its own read back too) in
+    // ascending split order, so the result does not depend on arrival order.
+    for (int zz = 0; zz < nsplit; ++zz) {
+        const float4 *pz = part + static_cast<size_t>(zz) * (kTileFloats / 4);
+#pragma unroll
+        for (int q = 0; q < kQ; ++q) {
+            const int ii = q / C::TN4, jj = q % C::TN4;
+            const float4 p = __ldcg(pz + q * C::kConsumers + tid);
+            if (zz == 0) {
+                acc[ii][4 * jj] = p.x; acc[ii][4 * jj + 1] = p.y;
+                acc[ii][4 * jj + 2] = p.z; acc[ii][4 * jj + 3] = p.w;
+            } else {
+                acc[ii][4 * jj] += p.x; acc[ii][4 * jj + 1] += p.y;
+                acc[ii][4 * jj + 2] += p.z; acc[ii][4 * jj + 3] += p.w;
+            }
+        }
+    }
+    if (tid == 0) sk.counters[slot] = 0;  // ready for the next call
+    epilogue<C, OP>(acc, g, Cb, m0, n0, wm, wn, lane_m, lane_n);
+}
+
+template <class C>
+TmaShape shape_of() {
+    return TmaShape{C::BM, C::BN, C::BK, C::kThreads, C::kSmemBytes, C::MIN_CTAS};
+}
+
+template <class C, int OP>
+cudaError_t prepare_one() {
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, false, OP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tma_kernel<C, true, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                C::kSmemBytes);
+}
+
+template <class C, int OP>
+int ctas_per_sm_one() {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm_tma_kernel<C, false, OP>, C::kThreads,
+                                                      C::kSmemBytes) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Whole tiles only when sk.splits == 1; otherwise the hybrid grid: dp_tiles
+// whole-tile CTAs, then `splits` CTAs for each remaining tile.  Grid y runs
+// over the batch (split plans are made for batch 1 only).
+template <class C, int OP>
+cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, const SplitK &sk,
+                       int smem_override, cudaStream_t stream) {
+    const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
+    const int smem = smem_override > 0 ? smem_override : C::kSmemBytes;
+    if (g.batch < 1 || g.batch > 65535 || (sk.splits > 1 && g.batch != 1)) return cudaErrorInvalidValue;
+    if (sk.splits <= 1) {
+        sgemm_tma_kernel<C, false, OP><<<dim3(tiles, g.batch), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
+                                                                                           kGroupM);
+    } else {
+        const int ctas = sk.dp_tiles + (tiles - sk.dp_tiles) * sk.splits;
+        sgemm_tma_kernel<C, true, OP><<<ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+    }
+    return cudaGetLastError();
+}
+
+// The three variants' kernels for one operand layout.
+template <int OP>
+cudaError_t prepare_op(int variant) {
+    switch (variant) {
+        case SGEMM_VARIANT_TMA_128x256: return prepare_one<CfgL, OP>();
+        case SGEMM_VARIANT_TMA_128x128: return prepare_one<CfgM, OP>();
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return prepare_one<CfgS, OP>();
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int OP>
+int ctas_per_sm_op(int variant) {
+    switch (variant) {
+        case SGEMM_VARIANT_TMA_128x256: return ctas_per_sm_one<CfgL, OP>();
+        case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<CfgM, OP>();
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return ctas_per_sm_one<CfgS, OP>();
+        default: return 0;
+    }
+}
+
+template <int OP>
+cudaError_t launch_op(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                      const SplitK &sk, int smem_override, cudaStream_t stream) {
+    switch (variant) {
+        case SGEMM_VARIANT_TMA_128x256: return launch_one<CfgL, OP>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_128x128: return launch_one<CfgM, OP>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK:
+            return launch_one<CfgS, OP>(g, tmA, tmB, sk, smem_override, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+}  // namespace sg

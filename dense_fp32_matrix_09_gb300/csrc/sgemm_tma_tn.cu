@@ -1,0 +1,13 @@
+// TMA-fed SIMT kernels for the TN operand layout (kernel in sgemm_tma_kernel.cuh).
+#include "sgemm_tma_kernel.cuh"
+
+namespace sg {
+
+cudaError_t tma_prepare_tn(int variant) { return prepare_op<kOpTN>(variant); }
+
+cudaError_t launch_tma_tn(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const SplitK &sk, int smem_override, cudaStream_t stream) {
+    return launch_op<kOpTN>(variant, g, tmA, tmB, sk, smem_override, stream);
+}
+
+}  // namespace sg

@@ -44,7 +44,8 @@ GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
 EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sgemm_set_variant",
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
-           "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host")
+           "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
+           "sgemm_run_ex", "sgemm_check_args_ex")
 
 
 class SgemmError(RuntimeError):
@@ -84,6 +85,11 @@ def lib() -> ctypes.CDLL:
         L.sgemm_variant_name.restype = ctypes.c_char_p
         L.sgemm_version.argtypes = []
         L.sgemm_set_math_mode.argtypes = [vp, i32]
+        i64 = ctypes.c_longlong
+        L.sgemm_run_ex.argtypes = [vp, i32, i32, i32, i32, i32, f32, vp, i32, i64, vp, i32, i64, f32, vp, i32, i64,
+                                   i32, vp]
+        L.sgemm_check_args_ex.argtypes = [i32, i32, i32, i32, i32, f32, vp, i32, i64, vp, i32, i64, f32, vp, i32,
+                                          i64, i32]
         L.sgemm_run_host.argtypes = [vp, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp, vp, vp, vp]
         L.sgemm_run_noalloc.argtypes = [i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         _lib = L
@@ -160,6 +166,21 @@ def sgemm_run_host(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dA, dB, dC, 
     _check(lib().sgemm_run_host(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb),
                                 float(beta), _ptr(C), int(ldc), _ptr(dA), _ptr(dB), _ptr(dC), _stream(stream)),
            "sgemm_run_host")
+
+
+def sgemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+                 batch=1, stream=None) -> None:
+    """C_b <- alpha*op(A_b)*op(B_b) + beta*C_b, b = 0..batch-1 (see include/sgemm.h)."""
+    _check(lib().sgemm_run_ex(h, int(transA), int(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
+                              int(strideA), _ptr(B), int(ldb), int(strideB), float(beta), _ptr(C), int(ldc),
+                              int(strideC), int(batch), _stream(stream)), "sgemm_run_ex")
+
+
+def sgemm_check_args_ex(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
+                        batch=1) -> int:
+    return lib().sgemm_check_args_ex(int(transA), int(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                     int(lda), int(strideA), _ptr(B), int(ldb), int(strideB), float(beta), _ptr(C),
+                                     int(ldc), int(strideC), int(batch))
 
 
 def sgemm_check_args(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:

@@ -84,6 +84,11 @@ typedef enum {
     SGEMM_VARIANT_TC_3XTF32_PAIR = 8,/* as TC_3XTF32 on CTA pairs (cta_group::2): 256 x 256
                                         tile per cluster of two CTAs                          */
     SGEMM_VARIANT_COUNT_ = 9
+    /* sgemm_run_ex: the TMA variants serve transA = 0 with transB = 0 (any
+     * batch) and the 128 x 256 and 64 x 64 ones also transA = 1, transB = 0;
+     * the tensor-core variants serve transA = transB = 0, batch = 1; every
+     * other case, or a pinned variant that does not serve it, runs on the
+     * generic variant. */
 } sgemm_variant_t;
 
 /* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32
@@ -114,6 +119,29 @@ int sgemm_create(sgemm_handle_t *out);
 int sgemm_run(sgemm_handle_t h, int M, int N, int K, float alpha,
               const float *A, int lda, const float *B, int ldb,
               float beta, float *C, int ldc, void *stream);
+
+/* The general form: C_b <- alpha * op(A_b) * op(B_b) + beta * C_b for b = 0 ..
+ * batch-1, where op(X) = X (trans = 0) or X^T (trans = 1), op(A) is M x K,
+ * op(B) is K x N, and matrix b of each operand starts `stride` elements after
+ * matrix b-1 (X_b = X + b*strideX).  Row-major storage as above: A is stored
+ * M x K (lda >= max(1, K)) when transA = 0 and K x M (lda >= max(1, M)) when
+ * transA = 1; B is stored K x N (ldb >= max(1, N)) when transB = 0 and N x K
+ * (ldb >= max(1, K)) when transB = 1.  `sgemm_run` is the case transA = transB
+ * = 0, batch = 1.  Strides must be >= 0; with batch > 1 the C matrices must not
+ * overlap one another (strideC at least the extent of one C window), else
+ * SGEMM_ERR_INVALID_VALUE.  batch == 0 is a no-op.  The pages' sgemmNN kernel
+ * (page "Deep dive into the sgemmNN algorithm") is the NN case; the transposed
+ * and batched forms are the BLAS / cuBLAS conventions the pages' batched call
+ * (page "GPU-accelerated matrix computation optimisation and CUDA programming
+ * practice", section 4.2) uses. */
+int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, float alpha,
+                 const float *A, int lda, long long strideA, const float *B, int ldb, long long strideB,
+                 float beta, float *C, int ldc, long long strideC, int batch, void *stream);
+
+/* Host-only validation of sgemm_run_ex's arguments (same rules, no CUDA call). */
+int sgemm_check_args_ex(int transA, int transB, int M, int N, int K, float alpha, const float *A, int lda,
+                        long long strideA, const float *B, int ldb, long long strideB, float beta,
+                        const float *C, int ldc, long long strideC, int batch);
 
 /* C <- alpha*A*B + beta*C with A, B, C in HOST memory, transfers overlapped
  * with compute.  dA, dB, dC are caller-owned DEVICE buffers of the same

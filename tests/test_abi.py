@@ -94,6 +94,47 @@ def test_check_args_alias(lib):
     assert chk(M, N, K, alpha=0.0, C=A0) == OK
 
 
+def chk_ex(tA, tB, M, N, K, alpha=1.0, A=A0, lda=None, sA=0, B=B0, ldb=None, sB=0, beta=0.0, C=C0, ldc=None,
+           sC=0, batch=1):
+    lda = max(M if tA else K, 1) if lda is None else lda
+    ldb = max(K if tB else N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    return sgemm.sgemm_check_args_ex(tA, tB, M, N, K, alpha, A, lda, sA, B, ldb, sB, beta, C, ldc, sC, batch)
+
+
+def test_check_args_ex_leading_dims_follow_the_stored_shape(lib):
+    # op(A) = A^T: A is stored K x M, so lda >= M (not K)
+    assert chk_ex(1, 0, 4, 5, 6, lda=4) == OK
+    assert chk_ex(1, 0, 4, 5, 6, lda=3) == INVALID
+    assert chk_ex(0, 0, 4, 5, 6, lda=4) == INVALID
+    # op(B) = B^T: B is stored N x K, so ldb >= K
+    assert chk_ex(0, 1, 4, 5, 6, ldb=6) == OK
+    assert chk_ex(0, 1, 4, 5, 6, ldb=5) == INVALID
+    assert chk_ex(1, 1, 4, 5, 6) == OK
+    assert chk_ex(2, 0, 4, 5, 6) == INVALID       # trans flags are 0 or 1
+    assert chk_ex(0, -1, 4, 5, 6) == INVALID
+
+
+def test_check_args_ex_batch_rules(lib):
+    c_elems = 3 * 5 + 5                              # M=4, N=5, ldc=5: window of 20 cells
+    assert chk_ex(0, 0, 4, 5, 6, batch=-1) == INVALID
+    assert chk_ex(0, 0, 4, 5, 6, batch=0, A=None, B=None, C=None) == OK
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=24, sB=30, sC=c_elems) == OK
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=24, sB=30, sC=c_elems - 1) == INVALID   # outputs overlap
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=0, sB=0, sC=c_elems) == OK             # shared A and B
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=-1, sC=c_elems) == INVALID
+    assert chk_ex(0, 0, 4, 5, 6, batch=1, sC=0) == OK                                 # stride unused
+    # C of the second batch entry reaching into A's batch window
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=24, C=A0 - 4 * c_elems, sC=c_elems) == ALIAS
+    assert chk_ex(0, 0, 4, 5, 6, batch=2, sA=24, C=A0 - 8 * c_elems, sC=c_elems) == OK
+
+
+def test_check_args_is_the_nn_batch1_case(lib):
+    for args in [(4, 5, 6), (0, 5, 6), (4, 5, 0), (4, -5, 6)]:
+        assert chk(*args) == chk_ex(0, 0, *args)
+    assert chk(4, 5, 6, C=A0 + 8) == chk_ex(0, 0, 4, 5, 6, C=A0 + 8) == ALIAS
+
+
 def test_bad_handles_are_rejected_without_dereference(lib):
     assert lib.sgemm_run(None, 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == sgemm.ERR_BAD_HANDLE
     assert lib.sgemm_run(ctypes.c_void_p(0x1234), 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == \
