@@ -165,16 +165,19 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
 // Estimated cost of running the call with `variant` (arbitrary units, lower
 // is better): the FLOP of one tile times the CTA slots the call occupies,
 // divided by the variant's main-loop efficiency measured on GB300 (fraction
-// of FP32 peak with the GPU full: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
-// 0.73).  Complete waves occupy all P = SMs x CTAs-per-SM slots; a split
-// tail of S ranges occupies P / S; an unsplit partial wave occupies P.  The
-// split-K variant runs tiles x splits CTAs of 1/splits of a tile each.  A
-// batch multiplies the tiles; batched calls are not split.
-double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, sg::SplitK *plan) {
+// of FP32 peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128
+// 0.80, 64 x 64 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63).
+// Complete waves occupy all P = SMs x CTAs-per-SM slots; a split tail of S
+// ranges occupies P / S; an unsplit partial wave occupies P.  The split-K
+// variant runs tiles x splits CTAs of 1/splits of a tile each.  A batch
+// multiplies the tiles; batched calls are not split.
+double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
+                    sg::SplitK *plan) {
     sg::TmaShape sh;
     if (!sg::tma_shape(variant, &sh)) return 1e300;
-    const double eff = variant == SGEMM_VARIANT_TMA_128x256 ? 0.81
-                     : variant == SGEMM_VARIANT_TMA_128x128 ? 0.80 : 0.73;
+    static const double kEff[3][3] = {{0.81, 0.80, 0.73}, {0.84, 0.84, 0.80}, {0.76, 0.75, 0.63}};
+    const int vi = variant == SGEMM_VARIANT_TMA_128x256 ? 0 : variant == SGEMM_VARIANT_TMA_128x128 ? 1 : 2;
+    const double eff = kEff[op][vi];
     const double P = static_cast<double>(h->num_sms) * std::max(1, h->ctas_per_sm[variant]);
     const double tile_flop = 2.0 * sh.bm * sh.bn * static_cast<double>(K);
     const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn) * batch;
@@ -196,16 +199,14 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
 }
 
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
-// larger tile (listed first).  The NT layout skips 128 x 128 (its kernel
-// exceeds the 128 registers a thread may use at two CTAs per SM).
+// larger tile (listed first).
 int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int op = sg::kTmaOpNN) {
     int best = SGEMM_VARIANT_TMA_128x256;
     double best_cost = 1e300;
     for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
                   SGEMM_VARIANT_TMA_64x64_SPLITK}) {
-        if (op == sg::kTmaOpNT && v == SGEMM_VARIANT_TMA_128x128) continue;
         sg::SplitK plan;
-        const double c = variant_cost(h, v, M, N, K, batch, &plan);
+        const double c = variant_cost(h, v, M, N, K, batch, op, &plan);
         if (c < best_cost * 0.999) {
             best_cost = c;
             best = v;

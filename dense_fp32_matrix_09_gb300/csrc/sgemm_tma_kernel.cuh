@@ -41,18 +41,19 @@
 //    partial tiles to a workspace, and the last CTA of a tile to arrive
 //    (arrival counter) adds the partials in ascending split order -- a fixed
 //    order, so results are deterministic -- and runs the epilogue.
-//
 //  * Operand layouts (template parameter OP).  NN: A stored M x K and B
 //    stored K x N, as above.  TN: A stored K x M; its stage is BK rows of BM
 //    floats (no swizzle) and each thread owns groups of 4 consecutive rows,
 //    so one 16-byte load gives the A values of 4 rows at one k.  NT: B
 //    stored N x K; its stage is BN rows of 32 floats with the 128-byte
-//    swizzle, a 16-byte load gives 4 k values of one column, and the packed
-//    FMAs pair two rows of A (built in registers) with one broadcast B value;
-//    lanes are arranged so the 4 column rows one quarter-warp reads fall in
-//    distinct swizzle rows.  In every layout each accumulator takes its
-//    products in ascending k with one rounding per FMA, so NN, TN and NT give
-//    the same bits for the same logical operands.  A x B with both operands
+//    swizzle (k contiguous), which the outer products cannot use directly.
+//    The warps first transpose it, in 4 x 4 blocks, into a [k][n] buffer
+//    whose 16-byte chunks are XOR-swizzled by (k / 4) (so both the block
+//    writes and the main loop's reads are free of bank conflicts), then run
+//    the NN main loop on it; two such buffers alternate, with one barrier
+//    per K step.  Every layout takes each product in ascending k with one
+//    rounding per FMA, so NN, TN and NT give the same bits for the same
+//    logical operands.  A x B with both operands
 //    transposed runs as the NN kernel on the swapped operands (C^T = B_s A_s,
 //    with B_s the stored N x K matrix and A_s the stored K x M one) with an
 //    epilogue that writes the tile transposed (GemmArgs::c_trans).
@@ -66,6 +67,7 @@
 #pragma once
 
 #include <cstdio>
+#include <type_traits>
 
 #include "device_common.cuh"
 #include "internal.h"
@@ -96,7 +98,6 @@ struct Cfg {
     static_assert(WTM % TM == 0 && WTN % TN == 0 && TN % 4 == 0, "bad thread tile");
     static_assert(BM % 8 == 0 && (kABytes % 1024) == 0, "A stages must stay 1024-byte aligned");
     static_assert(BM <= 256 && BN <= 256, "TMA box extents are at most 256");
-    static_assert(LANES_M % 4 == 0 && LANES_N % 2 == 0, "NT lane layout needs 4 x 2 lanes per quarter-warp");
     static_assert(TM % 4 == 0 && (kBBytes % 1024) == 0, "TN row groups / NT swizzled B stages");
 };
 
@@ -106,20 +107,15 @@ constexpr int kGroupM = 8;
 using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
 using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
 using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 2>;      // SGEMM_VARIANT_TMA_64x64 (+ split-K)
+// NT adds two B-sized transpose buffers, so its two larger tiles keep fewer
+// stages within the shared memory of one (128 x 256) or two (128 x 128) CTAs.
+using CfgLnt = Cfg<128, 256, 2, 4, 8, 16, 3, 1>;
+using CfgMnt = Cfg<128, 128, 2, 4, 8, 8, 2, 2>;
 
-// Lane coordinates inside the warp tile.  NT: each quarter-warp holds 4
-// lane rows x 2 lane columns, so the column rows of B it reads (4 apart)
-// fall in distinct 128-byte-swizzle rows; otherwise lanes run along N first.
+// Dynamic shared memory of the kernel for layout OP.
 template <class C, int OP>
-__device__ __forceinline__ void lane_coords(int lane, int &lane_m, int &lane_n) {
-    if (OP == kOpNT) {
-        constexpr int a = C::LANES_M / 4;
-        lane_m = (lane & 3) + 4 * ((lane >> 3) % a);
-        lane_n = ((lane >> 2) & 1) + 2 * ((lane >> 3) / a);
-    } else {
-        lane_m = lane / C::LANES_N;
-        lane_n = lane % C::LANES_N;
-    }
+constexpr int smem_bytes() {
+    return C::kSmemBytes + (OP == kOpNT ? 2 * C::kBBytes : 0);
 }
 
 // Tile row of a thread's accumulator row ii: rows strided by the lanes along
@@ -224,11 +220,14 @@ __device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, i
 // A stage = BM rows of 32 floats (128-byte swizzle), B stage = 32 rows of BN
 // floats.  A 16-byte load gives 4 k values of one A row (broadcast to both
 // halves of the packed FMA) and 4 columns of B at one k (two column pairs).
-template <class C>
+// BSWZ: the B stage is the NT transpose buffer, whose row k holds 16-byte
+// chunk q of the row at chunk q ^ (k / 4 % 8).
+template <class C, bool BSWZ>
 __device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
                                             int wm, int wn, int lane_m, int lane_n) {
     const uint8_t *a_thr = a_st + (wm * C::WTM + lane_m) * 128;
-    const float *b_thr = reinterpret_cast<const float *>(b_st) + wn * C::WTN + lane_n * 4;
+    const float *b_thr = reinterpret_cast<const float *>(b_st) + (BSWZ ? 0 : wn * C::WTN + lane_n * 4);
+    const int q0 = (wn * C::WTN) / 4 + lane_n;  // BSWZ: the thread's first chunk of a B row
 #pragma unroll
     for (int kb = 0; kb < C::BK / 4; ++kb) {
         float4 a[C::TM];
@@ -241,8 +240,13 @@ __device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const ui
         for (int kk = 0; kk < 4; ++kk) {
             float4 b[C::TN4];
 #pragma unroll
-            for (int jj = 0; jj < C::TN4; ++jj)
-                b[jj] = *reinterpret_cast<const float4 *>(b_thr + (kb * 4 + kk) * C::BN + jj * C::LANES_N * 4);
+            for (int jj = 0; jj < C::TN4; ++jj) {
+                if (BSWZ)
+                    b[jj] = *reinterpret_cast<const float4 *>(b_thr + (kb * 4 + kk) * C::BN +
+                                                              (((q0 + jj * C::LANES_N) ^ kb) << 2));
+                else
+                    b[jj] = *reinterpret_cast<const float4 *>(b_thr + (kb * 4 + kk) * C::BN + jj * C::LANES_N * 4);
+            }
 #pragma unroll
             for (int ii = 0; ii < C::TM; ++ii) {
                 const float av = comp(a[ii], kk);
@@ -284,41 +288,32 @@ __device__ __forceinline__ void mainloop_tn(float (&acc)[C::TM][C::TN], const ui
     }
 }
 
-// NT layout: A as NN; B stage = BN rows (columns of op(B)) of 32 floats with
-// the 128-byte swizzle.  A 16-byte load gives 4 k values of one column; the
-// packed FMA takes two A rows (paired in registers) and one broadcast B value.
+// NT: transpose one B stage (BN rows n of 32 floats k, 128-byte swizzle:
+// chunk c of row n at chunk c ^ (n % 8)) into the [k][n] buffer the NN main
+// loop reads with BSWZ (chunk q of row k at q ^ (k / 4 % 8)).  Work unit:
+// the 4 x 4 block of rows 4nq..4nq+3 and k chunk c; eight consecutive lanes
+// take the eight chunks of one nq, so both the four 16-byte reads (one row,
+// eight distinct chunks) and the four 16-byte writes (eight rows, chunks
+// nq ^ c all distinct) touch each bank once per quarter-warp.
 template <class C>
-__device__ __forceinline__ void mainloop_nt(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
-                                            int wm, int wn, int lane_m, int lane_n) {
-    const uint8_t *a_thr = a_st + (wm * C::WTM + lane_m) * 128;
-    const int nb = wn * C::WTN + lane_n * 4;  // the thread's first column row; other groups are 8-row aligned
+__device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, int tid) {
+    constexpr int kBlocks = C::BN * (C::BK / 4) / 4;
+    static_assert(kBlocks % C::kConsumers == 0, "whole blocks per thread");
 #pragma unroll
-    for (int kb = 0; kb < C::BK / 4; ++kb) {
-        float4 a[C::TM];
+    for (int u = 0; u < kBlocks / C::kConsumers; ++u) {
+        const int id = tid + u * C::kConsumers;
+        const int c = id & 7, nq = id >> 3;
+        float4 v[4];
 #pragma unroll
-        for (int ii = 0; ii < C::TM; ++ii) {
-            const int rx = (ii * C::LANES_M + lane_m) & 7;
-            a[ii] = *reinterpret_cast<const float4 *>(a_thr + ii * C::LANES_M * 128 + ((kb ^ rx) << 4));
+        for (int r = 0; r < 4; ++r) {
+            const int n = 4 * nq + r;
+            v[r] = *reinterpret_cast<const float4 *>(b_raw + n * 128 + ((c ^ (n & 7)) << 4));
         }
 #pragma unroll
-        for (int jj = 0; jj < C::TN4; ++jj) {
-            float4 b[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int n = nb + jj * C::LANES_N * 4 + v;
-                b[v] = *reinterpret_cast<const float4 *>(b_st + n * 128 + ((kb ^ (n & 7)) << 4));
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int p = 0; p < C::TM / 2; ++p) {
-                    const float a0 = comp(a[2 * p], kk), a1 = comp(a[2 * p + 1], kk);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const float bv = comp(b[v], kk);
-                        fma2(a0, a1, bv, bv, acc[2 * p][4 * jj + v], acc[2 * p + 1][4 * jj + v]);
-                    }
-                }
+        for (int kk = 0; kk < 4; ++kk) {
+            const int k = 4 * c + kk;
+            *reinterpret_cast<float4 *>(b_t + k * C::BN * 4 + ((nq ^ c) << 4)) =
+                make_float4(comp(v[0], kk), comp(v[1], kk), comp(v[2], kk), comp(v[3], kk));
         }
     }
 }
@@ -333,7 +328,8 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint8_t *smem = smem_raw + pad;
     uint8_t *sA = smem;                                  // STAGES x kABytes
     uint8_t *sB = smem + C::STAGES * C::kABytes;         // STAGES x kBBytes
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::STAGES * C::kStageBytes);
+    uint8_t *sBt = smem + C::STAGES * C::kStageBytes;    // NT: 2 x kBBytes transpose buffers
+    uint64_t *full = reinterpret_cast<uint64_t *>(sBt + (OP == kOpNT ? 2 * C::kBBytes : 0));
     uint64_t *empty = full + C::STAGES;
     int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);
 
@@ -392,8 +388,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     // ---------------------------------------------------- consumer warps
     const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
-    int lane_m, lane_n;
-    lane_coords<C, OP>(lane, lane_m, lane_n);
+    const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
 
     float acc[C::TM][C::TN];
 #pragma unroll
@@ -404,25 +399,39 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     bool aborted = false;
     for (int i = 0; i < nkt; ++i) {
         const int s = i % C::STAGES;
+        bool bad = false;
         if (tid == 0 && i >= 1 && i - 1 + C::STAGES < nkt) {
             // refill the stage step i-1 used once all threads have released it
             const int t = i - 1;
-            if (!mbar_wait(&empty[t % C::STAGES], (t / C::STAGES) & 1, g.status)) {
+            if (mbar_wait(&empty[t % C::STAGES], (t / C::STAGES) & 1, g.status)) {
+                issue(t + C::STAGES);
+                ++issued;
+            } else {
+                bad = true;
+            }
+        }
+        if (!bad) bad = !mbar_wait(&full[s], (i / C::STAGES) & 1, g.status);
+        const uint8_t *a_st = sA + s * C::kABytes;
+        const uint8_t *b_st = sB + s * C::kBBytes;
+        if constexpr (OP == kOpNT) {
+            // transpose into buffer i % 2: its last readers (step i - 2) all
+            // passed step i - 1's barrier; every thread reaches this barrier
+            // (all waits above are bounded), so an abort is seen by all
+            uint8_t *bt = sBt + (i & 1) * C::kBBytes;
+            if (!bad) transpose_b<C>(b_st, bt, tid);
+            if (named_barrier_or(1, C::kConsumers, bad)) {
                 aborted = true;
                 break;
             }
-            issue(t + C::STAGES);
-            ++issued;
+            mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
+        } else {
+            if (bad) {
+                aborted = true;
+                break;
+            }
+            if constexpr (OP == kOpNN) mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+            else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
         }
-        if (!mbar_wait(&full[s], (i / C::STAGES) & 1, g.status)) {
-            aborted = true;
-            break;
-        }
-        const uint8_t *a_st = sA + s * C::kABytes;
-        const uint8_t *b_st = sB + s * C::kBBytes;
-        if constexpr (OP == kOpNN) mainloop_nn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
-        else if constexpr (OP == kOpTN) mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
-        else mainloop_nt<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
         mbar_arrive(&empty[s]);
     }
 
@@ -493,17 +502,17 @@ TmaShape shape_of() {
 template <class C, int OP>
 cudaError_t prepare_one() {
     cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, false, OP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<C, OP>());
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(sgemm_tma_kernel<C, true, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                C::kSmemBytes);
+                                smem_bytes<C, OP>());
 }
 
 template <class C, int OP>
 int ctas_per_sm_one() {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm_tma_kernel<C, false, OP>, C::kThreads,
-                                                      C::kSmemBytes) != cudaSuccess)
+                                                      smem_bytes<C, OP>()) != cudaSuccess)
         return 0;
     return n;
 }
@@ -515,7 +524,7 @@ template <class C, int OP>
 cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, const SplitK &sk,
                        int smem_override, cudaStream_t stream) {
     const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
-    const int smem = smem_override > 0 ? smem_override : C::kSmemBytes;
+    const int smem = smem_override > 0 ? smem_override : smem_bytes<C, OP>();
     if (g.batch < 1 || g.batch > 65535 || (sk.splits > 1 && g.batch != 1)) return cudaErrorInvalidValue;
     if (sk.splits <= 1) {
         sgemm_tma_kernel<C, false, OP><<<dim3(tiles, g.batch), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
@@ -527,12 +536,18 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
     return cudaGetLastError();
 }
 
-// The three variants' kernels for one operand layout.
+// The three variants' kernels for one operand layout (NT: fewer stages on
+// the two larger tiles).
+template <int OP>
+using LCfg = typename std::conditional<OP == kOpNT, CfgLnt, CfgL>::type;
+template <int OP>
+using MCfg = typename std::conditional<OP == kOpNT, CfgMnt, CfgM>::type;
+
 template <int OP>
 cudaError_t prepare_op(int variant) {
     switch (variant) {
-        case SGEMM_VARIANT_TMA_128x256: return prepare_one<CfgL, OP>();
-        case SGEMM_VARIANT_TMA_128x128: return prepare_one<CfgM, OP>();
+        case SGEMM_VARIANT_TMA_128x256: return prepare_one<LCfg<OP>, OP>();
+        case SGEMM_VARIANT_TMA_128x128: return prepare_one<MCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return prepare_one<CfgS, OP>();
         default: return cudaErrorInvalidValue;
@@ -542,8 +557,8 @@ cudaError_t prepare_op(int variant) {
 template <int OP>
 int ctas_per_sm_op(int variant) {
     switch (variant) {
-        case SGEMM_VARIANT_TMA_128x256: return ctas_per_sm_one<CfgL, OP>();
-        case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<CfgM, OP>();
+        case SGEMM_VARIANT_TMA_128x256: return ctas_per_sm_one<LCfg<OP>, OP>();
+        case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<MCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return ctas_per_sm_one<CfgS, OP>();
         default: return 0;
@@ -554,8 +569,10 @@ template <int OP>
 cudaError_t launch_op(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                       const SplitK &sk, int smem_override, cudaStream_t stream) {
     switch (variant) {
-        case SGEMM_VARIANT_TMA_128x256: return launch_one<CfgL, OP>(g, tmA, tmB, sk, smem_override, stream);
-        case SGEMM_VARIANT_TMA_128x128: return launch_one<CfgM, OP>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_128x256:
+            return launch_one<LCfg<OP>, OP>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_128x128:
+            return launch_one<MCfg<OP>, OP>(g, tmA, tmB, sk, smem_override, stream);
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK:
             return launch_one<CfgS, OP>(g, tmA, tmB, sk, smem_override, stream);

@@ -84,11 +84,11 @@ typedef enum {
     SGEMM_VARIANT_TC_3XTF32_PAIR = 8,/* as TC_3XTF32 on CTA pairs (cta_group::2): 256 x 256
                                         tile per cluster of two CTAs                          */
     SGEMM_VARIANT_COUNT_ = 9
-    /* sgemm_run_ex: the TMA variants serve transA = 0 with transB = 0 (any
-     * batch) and the 128 x 256 and 64 x 64 ones also transA = 1, transB = 0;
-     * the tensor-core variants serve transA = transB = 0, batch = 1; every
-     * other case, or a pinned variant that does not serve it, runs on the
-     * generic variant. */
+    /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
+     * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
+     * for batch > 1, strideA, strideB) are multiples of 4; otherwise the
+     * generic variant runs.  The tensor-core variants serve transA = transB
+     * = 0 with batch 1; pinned for any other call they act as AUTO. */
 } sgemm_variant_t;
 
 /* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32
