@@ -91,6 +91,8 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=10)
     p.add_argument("--no-tensor", action="store_true", help="skip the 3xTF32 tensor-core block")
     p.add_argument("--tensor-steps", type=int, default=50)
+    p.add_argument("--op", default="NN", choices=["NN", "NT", "TN", "TT"],
+                   help="operand layout of the timed step (sgemm_run_ex; square unpadded workloads only)")
     p.add_argument("--no-ex", action="store_true",
                    help="skip the transposed-layout and strided-batched block (sgemm_run_ex)")
     return p.parse_args()
@@ -387,8 +389,19 @@ def main():
     stream = torch.cuda.current_stream()
     in_place = cfg.beta != 0
 
-    def step():
-        sg.sgemm_run(h, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, B, cfg.ldb, cfg.beta, C, cfg.ldc, stream)
+    if args.op == "NN":
+        def step():
+            sg.sgemm_run(h, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, B, cfg.ldb, cfg.beta, C, cfg.ldc, stream)
+    else:
+        # the same buffers read as the stored transposes (values are i.i.d., so
+        # the transposed operands are as random as the originals)
+        if not (cfg.M == cfg.N == cfg.K == cfg.lda == cfg.ldb == cfg.ldc):
+            raise SystemExit("--op needs a square workload without padding")
+        ta, tb = int(args.op[0] == "T"), int(args.op[1] == "T")
+
+        def step():
+            sg.sgemm_run_ex(h, ta, tb, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, 0, B, cfg.ldb, 0, cfg.beta,
+                            C, cfg.ldc, 0, 1, stream)
 
     for _ in range(args.warmup):
         if in_place:
@@ -478,6 +491,16 @@ def main():
         roofline["frac_at_measured_clock"] = achieved / (2 * 128 * sms * clocks["sm_mhz"] * 1e6 / 1e12)
     roofline["algorithmic_flops_per_launch"] = cfg.flops
     roofline["kernel_source_sha256_16"] = src_hash
+    if variant in (sg.VARIANT_TC_3XTF32, sg.VARIANT_TC_3XTF32_PAIR):
+        # a pinned tensor-core variant: its roofline is the tensor pipe's
+        bf16 = measured_bf16_tflops()
+        tc_peak = bf16["value"] * 1.1 / 2.25 / 3
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tc_peak, "traffic": None,
+                    "kernel": f"{sg.variant_name(variant)}",
+                    "peak_basis": f"TF32 dense = {bf16['source']} BF16 x 1.1/2.25, / 3 TF32 MMAs per FP32 product",
+                    "algorithmic_flops_per_launch": cfg.flops,
+                    "kernel_source_sha256_16": kernel_source_hash(TC_KERNEL_SOURCES)}
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -487,7 +510,7 @@ def main():
                    "ldb": cfg.ldb, "ldc": cfg.ldc, "alpha": cfg.alpha, "beta": cfg.beta, "seed": cfg.seed,
                    "inputs": "i.i.d. U[-1,1) float32",
                    "l2": "inputs larger than L2 (working set %d MiB)" % ((prob.A.nbytes + prob.B.nbytes + prob.C0.nbytes) >> 20),
-                   "variant": sg.variant_name(variant), "splits": splits,
+                   "variant": sg.variant_name(variant), "splits": splits, "op": args.op,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": args.e2e_steps,

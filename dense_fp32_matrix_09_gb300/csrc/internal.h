@@ -39,16 +39,19 @@ struct TmaShape {
     int min_ctas_per_sm;
 };
 
-// Split-K bookkeeping.  Tiles [0, dp_tiles) (in raster order) are computed
-// whole by one CTA each; every later tile is split into `splits` K ranges
-// computed by separate CTAs and summed by the last of them to finish.
-// splits == 1 means no tile is split (ws and counters unused).
+// Stream-K bookkeeping.  Tiles [0, dp_tiles) (in raster order) are computed
+// whole by one CTA each.  The K steps of the remaining tiles -- T = (tiles -
+// dp_tiles) * ceil(K / bk) iterations, taken tile by tile -- are shared by
+// sk_ctas further CTAs: CTA q gets iterations [floor(q*T/G), floor((q+1)*T/G))
+// (G = sk_ctas <= T), so a tile's K range may be split over consecutive CTAs;
+// the parts are summed in ascending k order by the last of them to finish.
+// sk_ctas == 0 means no stream-K part (ws and counters unused).
 struct SplitK {
-    int splits;             // number of K ranges per split tile
-    int k_tiles_per_split;  // K steps of bk per range
-    float *ws;              // (tiles - dp_tiles) * splits * bm * bn partial sums
-    int *counters;          // one arrival counter per split tile, zero between calls
-    int dp_tiles;           // leading tiles computed whole (0: every tile is split)
+    int dp_tiles;   // leading tiles computed whole
+    int sk_ctas;    // stream-K CTAs after them
+    float *ws;      // (tiles - dp_tiles + sk_ctas) * bm * bn partial sums
+    int *counters;  // one arrival counter per stream-K tile, zero between calls
+    int cta0 = 0;   // index of this launch's first CTA in the dp_tiles + sk_ctas sequence
 };
 
 // Operand layouts of the TMA-fed SIMT kernels: NN (A stored M x K, B K x N),

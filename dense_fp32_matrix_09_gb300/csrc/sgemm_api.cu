@@ -39,8 +39,8 @@ struct sgemm_ctx {
 
 namespace {
 
-constexpr size_t kWorkspaceBytes = size_t(32) << 20;  // split-K partial tiles
-constexpr int kCounters = 16384;                      // split-K output tiles per call
+constexpr size_t kWorkspaceBytes = size_t(48) << 20;  // stream-K partial tiles
+constexpr int kCounters = 16384;                      // stream-K output tiles per call
 
 std::mutex g_mu;
 std::unordered_set<sgemm_ctx *> g_live;
@@ -116,50 +116,54 @@ bool encode_operand(CUtensorMap *map, const float *base, int rows, int cols, int
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Split count for the split-K variant: enough CTAs for two per SM, at least
-// one K step per split, and the partial tiles must fit the workspace.
+// Stream-K CTA count for T iterations of `sk_tiles` tiles: at most `slots`
+// CTAs, at least `min_iters` iterations each, and the sk_tiles + G partial
+// tiles of `tile_floats` floats within the workspace.
+long long sk_ctas_for(const sgemm_ctx *h, long long T, long long sk_tiles, long long slots, long long tile_floats,
+                      int min_iters) {
+    long long G = std::min(slots, T / min_iters);
+    G = std::min(G, static_cast<long long>(h->ws_floats / tile_floats) - sk_tiles);
+    return std::max(G, 0LL);
+}
+
+// The 64 x 64 split variant: every tile's K steps shared by up to one wave
+// of stream-K CTAs (one K step each at least), when that gives more CTAs
+// than tiles.
 void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     const long long tiles = 1LL * cdiv(M, 64) * cdiv(N, 64);
-    const int k_tiles = cdiv(K, 32);
-    long long want = (2LL * h->num_sms + tiles - 1) / tiles;
-    want = std::min<long long>(std::min<long long>(want, k_tiles), 32);
-    const long long fit = static_cast<long long>(h->ws_floats / (tiles * 64 * 64));
-    want = std::min(want, fit);
-    if (tiles > h->n_counters) want = 1;
-    if (want < 1) want = 1;
-    const int kps = cdiv(k_tiles, static_cast<int>(want));
-    sk->k_tiles_per_split = kps;
-    sk->splits = cdiv(k_tiles, kps);
-    sk->ws = h->d_ws;
-    sk->counters = h->d_counters;
-    sk->dp_tiles = 0;
+    const long long kt = cdiv(K, 32);
+    *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
+    if (tiles > h->n_counters) return;
+    const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[SGEMM_VARIANT_TMA_64x64_SPLITK]);
+    const long long G = sk_ctas_for(h, tiles * kt, tiles, slots, 64 * 64, 1);
+    if (G <= tiles) return;
+    *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
 }
 
 // Tail plan for the whole-tile variants.  With T tiles and P resident CTA
 // slots, T = full*P + rem: the first full*P tiles run whole (complete waves)
-// and the rem tiles of the last, partly empty wave are split along K into S
-// ranges, S = P / rem (so the tail fills the slots), at least 2 K steps per
-// range and at most 8 ranges, within the workspace and counter capacity.
-// Without this the last wave runs rem whole tiles on a mostly idle GPU.
+// and the K steps of the rem tiles of the last, partly empty wave are shared
+// evenly by G stream-K CTAs (G <= P, at least 2 K steps each, within the
+// workspace), so the last wave keeps every slot busy for rem*kt/G steps
+// instead of leaving P - rem slots idle for a whole tile.  Used when G is at
+// least 1.25 rem (less would save little over whole tiles).
 void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K,
                sg::SplitK *sk) {
     const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn);
-    const int k_tiles = cdiv(K, sh.bk);
-    *sk = sg::SplitK{1, k_tiles, nullptr, nullptr, static_cast<int>(tiles)};
+    const long long kt = cdiv(K, sh.bk);
+    *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
     const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[variant]);
     const long long full = tiles / slots, rem = tiles - full * slots;
     if (rem == 0 || rem > h->n_counters) return;
-    long long S = std::min<long long>(slots / rem, 8);
-    S = std::min<long long>(S, k_tiles / 2);
-    S = std::min<long long>(S, static_cast<long long>(h->ws_floats / (rem * sh.bm * sh.bn)));
-    if (S < 2) return;
-    const int kps = cdiv(k_tiles, static_cast<int>(S));
-    sk->splits = cdiv(k_tiles, kps);
-    sk->k_tiles_per_split = kps;
-    sk->ws = h->d_ws;
-    sk->counters = h->d_counters;
-    sk->dp_tiles = static_cast<int>(full * slots);
-    if (sk->splits < 2) *sk = sg::SplitK{1, k_tiles, nullptr, nullptr, static_cast<int>(tiles)};
+    const long long G = sk_ctas_for(h, rem * kt, rem, slots, 1LL * sh.bm * sh.bn, 2);
+    if (G * 4 < rem * 5) return;
+    *sk = sg::SplitK{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
+}
+
+// CTAs per stream-K tile (rounded up; 1 without stream-K), for reporting.
+int splits_of(const sg::SplitK &sk, int tiles) {
+    if (sk.sk_ctas <= 0) return 1;
+    return std::max(2, cdiv(sk.sk_ctas, std::max(1, tiles - sk.dp_tiles)));
 }
 
 // Estimated cost of running the call with `variant` (arbitrary units, lower
@@ -167,9 +171,9 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
 // divided by the variant's main-loop efficiency measured on GB300 (fraction
 // of FP32 peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128
 // 0.80, 64 x 64 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63).
-// Complete waves occupy all P = SMs x CTAs-per-SM slots; a split tail of S
-// ranges occupies P / S; an unsplit partial wave occupies P.  The split-K
-// variant runs tiles x splits CTAs of 1/splits of a tile each.  A batch
+// Complete waves occupy all P = SMs x CTAs-per-SM slots for a tile's time;
+// a stream-K part occupies them for ceil(T/G) K steps plus about one step of
+// fixup; an unsplit partial wave occupies them for a whole tile.  A batch
 // multiplies the tiles; batched calls are not split.
 double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
                     sg::SplitK *plan) {
@@ -180,22 +184,28 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
     const double eff = kEff[op][vi];
     const double P = static_cast<double>(h->num_sms) * std::max(1, h->ctas_per_sm[variant]);
     const double tile_flop = 2.0 * sh.bm * sh.bn * static_cast<double>(K);
+    const double kt = cdiv(K, sh.bk);
     const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn) * batch;
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
         if (batch > 1) return 1e300;
         plan_splits(h, M, N, K, plan);
-        const double ctas = tiles * plan->splits;
-        return tile_flop / plan->splits * std::ceil(ctas / P) * P / eff;
+        if (plan->sk_ctas == 0) return tile_flop * std::ceil(tiles / P) * P / eff;
+        // every slot busy for ceil(T/G) K steps, plus about one step for the fixup
+        return tile_flop / kt * (std::ceil(tiles * kt / plan->sk_ctas) + 1) * P / eff;
     }
     if (batch > 1) {
-        *plan = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr, cdiv(M, sh.bm) * cdiv(N, sh.bn)};
+        *plan = sg::SplitK{cdiv(M, sh.bm) * cdiv(N, sh.bn), 0, nullptr, nullptr};
     } else {
         sg::TmaShape shape = sh;
         plan_tail(h, variant, shape, M, N, K, plan);
     }
     const double full = std::floor(tiles / P), rem = tiles - full * P;
-    const double tail = rem == 0 ? 0.0 : (plan->splits >= 2 ? P / plan->splits : P);
-    return tile_flop * (full * P + tail) / eff;
+    double tail = 0.0;
+    if (plan->sk_ctas > 0)
+        tail = tile_flop / kt * (std::ceil(rem * kt / plan->sk_ctas) + 1) * P;
+    else if (rem > 0)
+        tail = tile_flop * P;
+    return (tile_flop * full * P + tail) / eff;
 }
 
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
@@ -504,15 +514,16 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
 
     sg::TmaShape sh;
     CUtensorMap tmA, tmB;
-    sg::SplitK sk{1, cdiv(K, 32), nullptr, nullptr, 0};
+    sg::SplitK sk{0, 0, nullptr, nullptr};
     if (variant != SGEMM_VARIANT_GENERIC) {
         if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
-        sk = sg::SplitK{1, cdiv(K, sh.bk), nullptr, nullptr, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn)};
+        sk = sg::SplitK{cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn), 0, nullptr, nullptr};
         if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
             if (batch == 1) plan_splits(h, k.M, k.N, K, &sk);
-            if (sk.splits <= 1) variant = SGEMM_VARIANT_TMA_64x64;
+            if (sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
+        } else if (batch == 1) {
+            plan_tail(h, variant, sh, k.M, k.N, K, &sk);
         }
-        if (variant != SGEMM_VARIANT_TMA_64x64_SPLITK && batch == 1) plan_tail(h, variant, sh, k.M, k.N, K, &sk);
         const bool a_ok = op == sg::kTmaOpTN
             ? encode_operand(&tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
             : encode_operand(&tmA, k.A, k.M, K, k.lda, batch, k.sA, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -529,7 +540,7 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     const int rc = from_cuda(sg::launch_tma_op(op, variant, k, tmA, tmB, sk, h->smem_override, stream));
     if (rc == SGEMM_OK) {
         h->last_variant = variant;
-        h->last_splits = sk.splits;
+        h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn));
     }
     return rc;
 }

@@ -1,6 +1,6 @@
-// sgemm_run_noalloc: the split-K GEMM for callers that cannot allocate GPU memory.
+// sgemm_run_noalloc: the stream-K GEMM for callers that cannot allocate GPU memory.
 //
-// Who needs this.  sgemm_create allocates a handle's status word, split-K
+// Who needs this.  sgemm_create allocates a handle's status word, stream-K
 // workspace and counters with cudaMalloc.  Some callers cannot do that: code
 // that runs inside a memory-pool or caching-allocator implementation and must
 // not re-enter the allocator; frameworks whose own allocator has reserved the
@@ -13,13 +13,13 @@
 // The scratch area.  `g_noalloc_scratch` below is a file-scope static
 // __device__ array of kScratchBytes (8 MiB + 4 KiB + 256 B).  Every GPU that
 // loads the library holds it until the process exits.  It holds:
-//   - the split-K partial tiles, at most kMaxPartialTiles = 512 tiles of 64 x 64 floats (8 MiB);
+//   - the stream-K partial tiles, at most kMaxPartialTiles = 512 tiles of 64 x 64 floats (8 MiB);
 //   - one arrival counter per output tile, at most kMaxTiles = 512 counters;
 //   - one device status word (a kernel that abandons a bounded wait records it there).
 // A problem needs ceil(M/64) * ceil(N/64) output tiles; more than 512 (for
 // example M * N above 2,097,152 elements when both are multiples of 64) is
 // rejected with SGEMM_ERR_SCRATCH_TOO_SMALL and nothing is enqueued.  The
-// split count is chosen so that splits * tiles <= 512.
+// stream-K CTA count G is chosen so that tiles + G <= 512.
 //
 // Sharing.  Every call, on any stream, uses the same array, which keeps the
 // last call's contents.  Each call clears the counters and the status word it
@@ -37,9 +37,9 @@
 //
 // Paths: alpha == 0 or K == 0 takes the C = beta*C kernel and operands that
 // TMA cannot describe take the generic kernel (neither uses scratch); every
-// other call runs the 64 x 64 split-K kernel of sgemm_tma.cu with its
+// other call runs the 64 x 64 stream-K kernel (sgemm_tma_kernel.cuh) with its
 // workspace, counters and status word in the scratch area.  Results are
-// deterministic for a given split count.  A device-side timeout (the GPU
+// deterministic for a given stream-K CTA count.  A device-side timeout (the GPU
 // stalling for seconds) leaves C unwritten and is recorded only in the
 // scratch status word, which this entry point cannot report.
 #include <algorithm>
@@ -55,7 +55,7 @@
 
 namespace {
 
-constexpr int kTile = 64;                       // split-K CTA tile (64 x 64)
+constexpr int kTile = 64;                       // stream-K CTA tile (64 x 64)
 constexpr int kMaxPartialTiles = 512;           // partial 64 x 64 tiles the scratch holds
 constexpr int kMaxTiles = 512;                  // output tiles (one counter each)
 constexpr size_t kPartialFloats = size_t(kMaxPartialTiles) * kTile * kTile;
@@ -161,16 +161,15 @@ extern "C" int sgemm_run_noalloc(int M, int N, int K, float alpha, const float *
 
     sg::TmaShape sh;
     if (!sg::tma_shape(SGEMM_VARIANT_TMA_64x64_SPLITK, &sh)) return SGEMM_ERR_CUDA;
-    // enough CTAs for about two per SM, at least one K step per split, and
-    // splits * tiles partial tiles must fit the scratch
+    // stream-K over every tile: about two CTAs per SM, at least one K step
+    // each, and the tiles + G partial tiles must fit the scratch; whole tiles
+    // when that gives no more CTAs than tiles
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SGEMM_ERR_CUDA;
-    const int k_tiles = cdiv(K, sh.bk);
-    long long want = (2LL * sms + tiles - 1) / tiles;
-    want = std::min<long long>({want, static_cast<long long>(k_tiles), 32LL, kMaxPartialTiles / tiles});
-    if (want < 1) want = 1;
-    const int kps = cdiv(k_tiles, static_cast<int>(want));
-    const sg::SplitK sk{cdiv(k_tiles, kps), kps, scratch, counters};
+    const long long T = static_cast<long long>(tiles) * cdiv(K, sh.bk);
+    const long long G = std::min<long long>({2LL * sms, T, static_cast<long long>(kMaxPartialTiles) - tiles});
+    const sg::SplitK sk = G > tiles ? sg::SplitK{0, static_cast<int>(G), scratch, counters}
+                                    : sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
 
     CUtensorMap tmA, tmB;
     if (!encode(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -37,10 +37,14 @@
 //  * Epilogue: C = alpha*acc + beta*C with float4 accesses when C is 16-byte
 //    aligned and ldc % 4 == 0 (scalar at the ragged N edge); C is not read
 //    when beta == 0.
-//  * Split-K variant: CTAs along grid z take disjoint K ranges, write their
-//    partial tiles to a workspace, and the last CTA of a tile to arrive
-//    (arrival counter) adds the partials in ascending split order -- a fixed
-//    order, so results are deterministic -- and runs the epilogue.
+//  * Stream-K tail: complete waves of whole tiles come first; the K steps of
+//    the tiles left for the last, partial wave are divided evenly over up to
+//    a wave of CTAs, each of which walks a contiguous range of (tile, K step)
+//    iterations with its TMA pipeline running across tile boundaries.  A
+//    tile whose K range is split stores each part in a workspace slot, and
+//    the last CTA of the tile to arrive (arrival counter) adds the parts in
+//    ascending k order -- a fixed order, so results are deterministic -- and
+//    runs the epilogue.  The 64 x 64 split variant runs every tile this way.
 //  * Operand layouts (template parameter OP).  NN: A stored M x K and B
 //    stored K x N, as above.  TN: A stored K x M; its stage is BK rows of BM
 //    floats (no swizzle) and each thread owns groups of 4 consecutive rows,
@@ -132,60 +136,63 @@ __device__ __forceinline__ int tile_col(int wn, int lane_n, int j) {
     return wn * C::WTN + (j / 4) * C::LANES_N * 4 + lane_n * 4 + (j & 3);
 }
 
+// Epilogue of one float4 group of a thread's accumulators (row ii, columns
+// 4jj..4jj+3): C = alpha*v + beta*C, C not read when beta == 0; float4
+// accesses when C allows them, scalar at the ragged N edge; with c_trans the
+// tile is of C^T and element (row, col) goes to C[col][row].
 template <class C, int OP>
-__device__ __forceinline__ void epilogue(float (&acc)[C::TM][C::TN], const GemmArgs &g, float *Cb, int m0,
-                                         int n0, int wm, int wn, int lane_m, int lane_n) {
+__device__ __forceinline__ void epilogue_group(const GemmArgs &g, float *Cb, int m0, int n0, int wm, int wn,
+                                               int lane_m, int lane_n, int ii, int jj, const float (&v)[4]) {
+    const int row = m0 + tile_row<C, OP>(wm, lane_m, ii);
+    const int col = n0 + tile_col<C>(wn, lane_n, 4 * jj);
+    if (row >= g.M) return;
     if (g.c_trans) {
-        // the tile is of C^T: element (row, col) goes to C[col][row]
 #pragma unroll
-        for (int ii = 0; ii < C::TM; ++ii) {
-            const int row = m0 + tile_row<C, OP>(wm, lane_m, ii);
-            if (row >= g.M) continue;
-#pragma unroll
-            for (int j = 0; j < C::TN; ++j) {
-                const int col = n0 + tile_col<C>(wn, lane_n, j);
-                if (col >= g.N) continue;
-                float *p = Cb + static_cast<size_t>(col) * g.ldc + row;
-                float r = g.alpha * acc[ii][j];
-                if (g.beta != 0.f) r = fmaf(g.beta, *p, r);
-                *p = r;
-            }
+        for (int e = 0; e < 4; ++e) {
+            if (col + e >= g.N) continue;
+            float *p = Cb + static_cast<size_t>(col + e) * g.ldc + row;
+            float r = g.alpha * v[e];
+            if (g.beta != 0.f) r = fmaf(g.beta, *p, r);
+            *p = r;
         }
         return;
     }
+    float *crow = Cb + static_cast<size_t>(row) * g.ldc;
+    float o[4];
 #pragma unroll
-    for (int ii = 0; ii < C::TM; ++ii) {
-        const int row = m0 + tile_row<C, OP>(wm, lane_m, ii);
-        if (row >= g.M) continue;
-        float *crow = Cb + static_cast<size_t>(row) * g.ldc;
+    for (int e = 0; e < 4; ++e) o[e] = g.alpha * v[e];
+    if (g.vec_c && col + 3 < g.N) {
+        float4 *p = reinterpret_cast<float4 *>(crow + col);
+        if (g.beta != 0.f) {
+            const float4 c = *p;
+            o[0] = fmaf(g.beta, c.x, o[0]);
+            o[1] = fmaf(g.beta, c.y, o[1]);
+            o[2] = fmaf(g.beta, c.z, o[2]);
+            o[3] = fmaf(g.beta, c.w, o[3]);
+        }
+        *p = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
 #pragma unroll
-        for (int jj = 0; jj < C::TN4; ++jj) {
-            const int col = n0 + tile_col<C>(wn, lane_n, 4 * jj);
-            float o[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) o[v] = g.alpha * acc[ii][4 * jj + v];
-            if (g.vec_c && col + 3 < g.N) {
-                float4 *p = reinterpret_cast<float4 *>(crow + col);
-                if (g.beta != 0.f) {
-                    const float4 c = *p;
-                    o[0] = fmaf(g.beta, c.x, o[0]);
-                    o[1] = fmaf(g.beta, c.y, o[1]);
-                    o[2] = fmaf(g.beta, c.z, o[2]);
-                    o[3] = fmaf(g.beta, c.w, o[3]);
-                }
-                *p = make_float4(o[0], o[1], o[2], o[3]);
-            } else {
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    if (col + v < g.N) {
-                        float r = o[v];
-                        if (g.beta != 0.f) r = fmaf(g.beta, crow[col + v], r);
-                        crow[col + v] = r;
-                    }
-                }
+        for (int e = 0; e < 4; ++e) {
+            if (col + e < g.N) {
+                float r = o[e];
+                if (g.beta != 0.f) r = fmaf(g.beta, crow[col + e], r);
+                crow[col + e] = r;
             }
         }
     }
+}
+
+template <class C, int OP>
+__device__ __forceinline__ void epilogue(float (&acc)[C::TM][C::TN], const GemmArgs &g, float *Cb, int m0,
+                                         int n0, int wm, int wn, int lane_m, int lane_n) {
+#pragma unroll
+    for (int ii = 0; ii < C::TM; ++ii)
+#pragma unroll
+        for (int jj = 0; jj < C::TN4; ++jj) {
+            const float v[4] = {acc[ii][4 * jj], acc[ii][4 * jj + 1], acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]};
+            epilogue_group<C, OP>(g, Cb, m0, n0, wm, wn, lane_m, lane_n, ii, jj, v);
+        }
 }
 
 // Component kk (0..3) of a float4 (kk is a compile-time constant after unrolling).
@@ -318,6 +325,58 @@ __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, 
     }
 }
 
+// Stream-K: the CTAs of one tile are the consecutive q with iterations in
+// [tl*kt, (tl+1)*kt) of the T = stream-K tiles x kt iterations, where CTA q
+// holds [floor(q*T/G), floor((q+1)*T/G)).  First such q: the largest with
+// floor(q*T/G) <= x, i.e. ceil((x+1)*G/T) - 1 for x = tl*kt.
+__device__ __forceinline__ int sk_first_cta(long long x, long long T, int G) {
+    return static_cast<int>(((x + 1) * G + T - 1) / T) - 1;
+}
+
+// Last CTA of a split tile: add the parts in slots tl + q_first .. tl +
+// q_last in ascending k order -- a fixed order, so the result does not
+// depend on which CTA finished last -- a chunk of float4 groups at a time,
+// and run the epilogue on each sum.  The caller's accumulators are dead here
+// (its own part is already in the workspace), so the chunk reuses their
+// registers.
+template <class C, int OP>
+__device__ __forceinline__ void sk_reduce_epilogue(const GemmArgs g, const float *ws, float *Cb, int tl, int q_first,
+                                                int q_last, int m0, int n0) {
+    constexpr size_t kTileFloats = static_cast<size_t>(C::BM) * C::BN;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
+    const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
+    // groups in chunks of kChunk: the chunk's loads of one part are
+    // independent of one another, so they are in flight together
+    constexpr int kGroups = C::TM * C::TN4;
+    constexpr int kChunk = kGroups < 8 ? kGroups : 8;
+    static_assert(kGroups % kChunk == 0, "whole chunks");
+#pragma unroll 1
+    for (int u0 = 0; u0 < kGroups; u0 += kChunk) {
+        float4 sum[kChunk];
+        for (int qq = q_first; qq <= q_last; ++qq) {
+            const float4 *part = reinterpret_cast<const float4 *>(ws + static_cast<size_t>(tl + qq) * kTileFloats) +
+                                 u0 * C::kConsumers + tid;
+            float4 p[kChunk];
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) p[c] = __ldcg(part + c * C::kConsumers);
+#pragma unroll
+            for (int c = 0; c < kChunk; ++c) {
+                if (qq == q_first) {
+                    sum[c] = p[c];
+                } else {
+                    sum[c].x += p[c].x; sum[c].y += p[c].y; sum[c].z += p[c].z; sum[c].w += p[c].w;
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c) {
+            const float v[4] = {sum[c].x, sum[c].y, sum[c].z, sum[c].w};
+            epilogue_group<C, OP>(g, Cb, m0, n0, wm, wn, lane_m, lane_n, (u0 + c) / C::TN4, (u0 + c) % C::TN4, v);
+        }
+    }
+}
+
 template <class C, bool SPLIT, int OP>
 __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -335,23 +394,25 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
-    const int k_tiles = (g.K + C::BK - 1) / C::BK;
-    // CTAs [0, dp_tiles) take whole tiles; the rest take one of `splits` K
-    // ranges of the remaining tiles (split index z).  Split only with batch 1.
-    int tile = blockIdx.x, z = 0, nsplit = 1;
-    if (SPLIT && tile >= sk.dp_tiles) {
-        const int q = tile - sk.dp_tiles;
-        tile = sk.dp_tiles + q / sk.splits;
-        z = q % sk.splits;
-        nsplit = sk.splits;
-    }
-    int tm, tn;
-    tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
-    const int m0 = tm * C::BM, n0 = tn * C::BN;
-    int kt0 = 0, nkt = k_tiles;
-    if (nsplit > 1) {
-        kt0 = z * sk.k_tiles_per_split;
-        nkt = min(k_tiles - kt0, sk.k_tiles_per_split);  // >= 1: the host sizes the splits
+    const int kt = (g.K + C::BK - 1) / C::BK;
+    // This CTA's work, as one or two segments (a tile and a K range of it).
+    // CTAs below sk.dp_tiles (all CTAs without SPLIT) take one whole tile.
+    // Stream-K CTA q takes iterations [floor(q*T/G), floor((q+1)*T/G)) of the
+    // T = (tiles - dp_tiles) * kt iterations of the remaining tiles, taken
+    // tile by tile (G = sk.sk_ctas); the host keeps G >= the number of those
+    // tiles, so a range is at most kt long and touches at most two tiles.
+    const int cta = static_cast<int>(blockIdx.x) + (SPLIT ? sk.cta0 : 0);
+    int tile0 = cta, k00 = 0, n0it = kt, n_iter = kt, q = -1;
+    long long T = 0;
+    if (SPLIT && cta >= sk.dp_tiles) {
+        q = cta - sk.dp_tiles;
+        T = static_cast<long long>(tiles_m * tiles_n - sk.dp_tiles) * kt;
+        const long long b = q * T / sk.sk_ctas, e = (q + 1) * T / sk.sk_ctas;
+        const int tl = static_cast<int>(b / kt);
+        tile0 = sk.dp_tiles + tl;
+        k00 = static_cast<int>(b - static_cast<long long>(tl) * kt);
+        n_iter = static_cast<int>(e - b);  // >= 1: the host keeps G <= T
+        n0it = min(n_iter, kt - k00);      // the rest (if any) is the next tile from k = 0
     }
     // batch entry of this CTA; an operand with a batch stride has a 3-D map
     const int bat = blockIdx.y;
@@ -367,11 +428,25 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
     __syncthreads();
 
-    // Thread 0 issues the TMA loads of k-step t into stage t % STAGES.
+    // Thread 0 issues the TMA loads of the CTA's t-th iteration into stage t % STAGES.
+    int m0w, n0w;  // the first segment's tile
+    {
+        int tm, tn;
+        tile_coords(tile0, tiles_m, tiles_n, group_m, tm, tn);
+        m0w = tm * C::BM;
+        n0w = tn * C::BN;
+    }
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
+        int m0 = m0w, n0 = n0w, kc = (k00 + t) * C::BK;
+        if (SPLIT && t >= n0it) {  // second segment: the next tile from k = 0
+            int tm, tn;
+            tile_coords(tile0 + 1, tiles_m, tiles_n, group_m, tm, tn);
+            m0 = tm * C::BM;
+            n0 = tn * C::BN;
+            kc = (t - n0it) * C::BK;
+        }
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        const int kc = (kt0 + t) * C::BK;
         const int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
         const int bx = OP == kOpNT ? kc : n0, by = OP == kOpNT ? n0 : kc;
         if (a3) tma_load_3d(sA + s * C::kABytes, &tmA, &full[s], ax, ay, bat);
@@ -383,7 +458,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (tid == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        for (; issued < min(nkt, C::STAGES); ++issued) issue(issued);
+        for (; issued < min(n_iter, C::STAGES); ++issued) issue(issued);
     }
 
     // ---------------------------------------------------- consumer warps
@@ -391,48 +466,85 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
 
     float acc[C::TM][C::TN];
-#pragma unroll
-    for (int ii = 0; ii < C::TM; ++ii)
-#pragma unroll
-        for (int j = 0; j < C::TN; ++j) acc[ii][j] = 0.f;
 
+    // Aborts (a bounded wait gave up): without SPLIT a thread leaves the loop
+    // at once (no barrier follows inside it).  With SPLIT a thread that gave
+    // up keeps pace without waiting or computing until the end of its
+    // segment, where all threads agree on the abort (every thread reaches
+    // that barrier) and leave together.  NT agrees at its per-step barrier.
     bool aborted = false;
-    for (int i = 0; i < nkt; ++i) {
-        const int s = i % C::STAGES;
-        bool bad = false;
-        if (tid == 0 && i >= 1 && i - 1 + C::STAGES < nkt) {
-            // refill the stage step i-1 used once all threads have released it
-            const int t = i - 1;
-            if (mbar_wait(&empty[t % C::STAGES], (t / C::STAGES) & 1, g.status)) {
-                issue(t + C::STAGES);
-                ++issued;
+    const int nseg = n0it < n_iter ? 2 : 1;
+    int i = 0, nseg_done = 0;  // stream-K: parts stored in the workspace
+    unsigned split_last = 0;   // stream-K: bit seg set when this CTA delivered that tile's last part
+    for (int seg = 0; seg < nseg; ++seg) {
+#pragma unroll
+        for (int ii = 0; ii < C::TM; ++ii)
+#pragma unroll
+            for (int j = 0; j < C::TN; ++j) acc[ii][j] = 0.f;
+        const int i_end = seg == 0 ? n0it : n_iter;
+        for (; i < i_end; ++i) {
+            const int s = i % C::STAGES;
+            bool bad = aborted;
+            if (!bad && tid == 0 && i >= 1 && i - 1 + C::STAGES < n_iter) {
+                // refill the stage step i-1 used once all threads have released it
+                const int t = i - 1;
+                if (mbar_wait(&empty[t % C::STAGES], (t / C::STAGES) & 1, g.status)) {
+                    issue(t + C::STAGES);
+                    ++issued;
+                } else {
+                    bad = true;
+                }
+            }
+            if (!bad) bad = !mbar_wait(&full[s], (i / C::STAGES) & 1, g.status);
+            const uint8_t *a_st = sA + s * C::kABytes;
+            const uint8_t *b_st = sB + s * C::kBBytes;
+            if constexpr (OP == kOpNT) {
+                // transpose into buffer i % 2: its last readers (step i - 2)
+                // all passed step i - 1's barrier
+                uint8_t *bt = sBt + (i & 1) * C::kBBytes;
+                if (!bad) transpose_b<C>(b_st, bt, tid);
+                if (named_barrier_or(1, C::kConsumers, bad)) {
+                    aborted = true;
+                    break;
+                }
+                mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
             } else {
-                bad = true;
+                if (bad) {
+                    aborted = true;
+                    if (!SPLIT) break;
+                    continue;
+                }
+                if constexpr (OP == kOpNN) mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+            }
+            mbar_arrive(&empty[s]);
+        }
+        if (!SPLIT || q < 0) break;  // one whole tile: epilogue below
+        // ---- end of a stream-K segment (reached by every thread)
+        if (named_barrier_or(1, C::kConsumers, aborted)) {
+            aborted = true;
+            break;
+        }
+        const int tl = tile0 + seg - sk.dp_tiles;
+        const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
+        const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+        if (q_first == q_last) break;  // this CTA has the whole tile (one segment): epilogue below
+        // store this part (thread-major float4 groups) in slot tl + q and count it
+        {
+            float4 *mine = reinterpret_cast<float4 *>(sk.ws + static_cast<size_t>(tl + q) * C::BM * C::BN);
+#pragma unroll
+            for (int u = 0; u < C::TM * C::TN4; ++u) {
+                const int ii = u / C::TN4, jj = u % C::TN4;
+                __stcg(mine + u * C::kConsumers + tid, make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1],
+                                                                   acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
             }
         }
-        if (!bad) bad = !mbar_wait(&full[s], (i / C::STAGES) & 1, g.status);
-        const uint8_t *a_st = sA + s * C::kABytes;
-        const uint8_t *b_st = sB + s * C::kBBytes;
-        if constexpr (OP == kOpNT) {
-            // transpose into buffer i % 2: its last readers (step i - 2) all
-            // passed step i - 1's barrier; every thread reaches this barrier
-            // (all waits above are bounded), so an abort is seen by all
-            uint8_t *bt = sBt + (i & 1) * C::kBBytes;
-            if (!bad) transpose_b<C>(b_st, bt, tid);
-            if (named_barrier_or(1, C::kConsumers, bad)) {
-                aborted = true;
-                break;
-            }
-            mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
-        } else {
-            if (bad) {
-                aborted = true;
-                break;
-            }
-            if constexpr (OP == kOpNN) mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
-            else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
-        }
-        mbar_arrive(&empty[s]);
+        __threadfence();
+        named_barrier_sync(1, C::kConsumers);
+        if (tid == 0) s_flag[seg] = (atomicAdd(&sk.counters[tl], 1) == q_last - q_first);
+        named_barrier_sync(1, C::kConsumers);
+        split_last |= static_cast<unsigned>(s_flag[seg] != 0) << seg;
+        ++nseg_done;
     }
 
     if (aborted && tid == 0) {
@@ -441,57 +553,25 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int t = max(0, issued - C::STAGES); t < issued; ++t)
             mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
     }
-    if (nsplit == 1) {  // uniform per CTA
-        if (!aborted) epilogue<C, OP>(acc, g, Cb, m0, n0, wm, wn, lane_m, lane_n);
+    if (aborted) return;
+    if (!SPLIT || q < 0 || nseg_done == 0) {
+        // a whole tile, in acc
+        epilogue<C, OP>(acc, g, Cb, m0w, n0w, wm, wn, lane_m, lane_n);
         return;
     }
-
-    // ------------------------------------------------------- split-K tail
-    // All threads reach this barrier (every wait above is bounded), so an
-    // abort by any of them is seen by all and the tile is left untouched.
-    if (named_barrier_or(1, C::kConsumers, aborted)) return;
-    const int slot = tile - sk.dp_tiles;  // index among the split tiles
-    constexpr int kQ = C::TM * C::TN4;    // float4 groups per thread
-    constexpr size_t kTileFloats = static_cast<size_t>(C::BM) * C::BN;
-    const float4 *part = reinterpret_cast<const float4 *>(sk.ws + static_cast<size_t>(slot) * nsplit * kTileFloats);
-    {
-        // partial tile of split z, thread-major: float4 group q of thread t at [q * threads + t]
-        float4 *mine = reinterpret_cast<float4 *>(sk.ws + (static_cast<size_t>(slot) * nsplit + z) * kTileFloats);
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-            const int ii = q / C::TN4, jj = q % C::TN4;
-            __stcg(mine + q * C::kConsumers + tid, make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1],
-                                                               acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
-        }
+    // stream-K: finish each split tile whose last part this CTA delivered
+#pragma unroll 1
+    for (int seg = 0; seg < 2; ++seg) {
+        if (!((split_last >> seg) & 1)) continue;
+        const int tile = tile0 + seg, tl = tile - sk.dp_tiles;
+        int tm, tn;
+        tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+        __threadfence();
+        sk_reduce_epilogue<C, OP>(g, sk.ws, Cb, tl, sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas),
+                                  sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas),
+                                  tm * C::BM, tn * C::BN);
+        if (tid == 0) sk.counters[tl] = 0;  // ready for the next call
     }
-    __threadfence();
-    named_barrier_sync(1, C::kConsumers);
-    if (tid == 0) {
-        const int prev = atomicAdd(&sk.counters[slot], 1);
-        *s_flag = (prev == nsplit - 1);
-    }
-    named_barrier_sync(1, C::kConsumers);
-    if (!*s_flag) return;
-    __threadfence();
-    // Last CTA of this tile: sum all partials (its own read back too) in
-    // ascending split order, so the result does not depend on arrival order.
-    for (int zz = 0; zz < nsplit; ++zz) {
-        const float4 *pz = part + static_cast<size_t>(zz) * (kTileFloats / 4);
-#pragma unroll
-        for (int q = 0; q < kQ; ++q) {
-            const int ii = q / C::TN4, jj = q % C::TN4;
-            const float4 p = __ldcg(pz + q * C::kConsumers + tid);
-            if (zz == 0) {
-                acc[ii][4 * jj] = p.x; acc[ii][4 * jj + 1] = p.y;
-                acc[ii][4 * jj + 2] = p.z; acc[ii][4 * jj + 3] = p.w;
-            } else {
-                acc[ii][4 * jj] += p.x; acc[ii][4 * jj + 1] += p.y;
-                acc[ii][4 * jj + 2] += p.z; acc[ii][4 * jj + 3] += p.w;
-            }
-        }
-    }
-    if (tid == 0) sk.counters[slot] = 0;  // ready for the next call
-    epilogue<C, OP>(acc, g, Cb, m0, n0, wm, wn, lane_m, lane_n);
 }
 
 template <class C>
@@ -517,21 +597,25 @@ int ctas_per_sm_one() {
     return n;
 }
 
-// Whole tiles only when sk.splits == 1; otherwise the hybrid grid: dp_tiles
-// whole-tile CTAs, then `splits` CTAs for each remaining tile.  Grid y runs
-// over the batch (split plans are made for batch 1 only).
+// Whole tiles only when sk.sk_ctas == 0; otherwise the hybrid grid: dp_tiles
+// whole-tile CTAs, then sk_ctas stream-K CTAs sharing the remaining tiles'
+// K steps.  Grid y runs over the batch (stream-K plans are for batch 1 only).
 template <class C, int OP>
 cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, const SplitK &sk,
                        int smem_override, cudaStream_t stream) {
     const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
     const int smem = smem_override > 0 ? smem_override : smem_bytes<C, OP>();
-    if (g.batch < 1 || g.batch > 65535 || (sk.splits > 1 && g.batch != 1)) return cudaErrorInvalidValue;
-    if (sk.splits <= 1) {
+    if (g.batch < 1 || g.batch > 65535 || (sk.sk_ctas > 0 && g.batch != 1)) return cudaErrorInvalidValue;
+    if (sk.sk_ctas <= 0) {
         sgemm_tma_kernel<C, false, OP><<<dim3(tiles, g.batch), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
                                                                                            kGroupM);
     } else {
-        const int ctas = sk.dp_tiles + (tiles - sk.dp_tiles) * sk.splits;
-        sgemm_tma_kernel<C, true, OP><<<ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+        // the complete waves with the whole-tile kernel, then the stream-K CTAs
+        if (sk.dp_tiles > 0)
+            sgemm_tma_kernel<C, false, OP><<<sk.dp_tiles, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+        SplitK s2 = sk;
+        s2.cta0 = sk.dp_tiles;
+        sgemm_tma_kernel<C, true, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
     }
     return cudaGetLastError();
 }

@@ -35,7 +35,7 @@
  *
  * Threading: one handle may be used from one host thread at a time, and its
  * calls must be ordered on the GPU (one stream, or streams ordered by
- * events): calls of the same handle share its split-K workspace.  Use one
+ * events): calls of the same handle share its stream-K workspace.  Use one
  * handle per concurrently running stream.
  *
  * Every function returns an sgemm_status_t value (as int) unless noted.
@@ -76,7 +76,7 @@ typedef enum {
     SGEMM_VARIANT_TMA_128x256 = 1,   /* TMA-fed SIMT, 128 x 256 CTA tile, 8 x 16 per thread */
     SGEMM_VARIANT_TMA_128x128 = 2,   /* TMA-fed SIMT, 128 x 128 CTA tile, 8 x 8 per thread  */
     SGEMM_VARIANT_TMA_64x64 = 3,     /* TMA-fed SIMT, 64 x 64 CTA tile, 8 x 4 per thread    */
-    SGEMM_VARIANT_TMA_64x64_SPLITK = 4, /* 64 x 64 tiles, K split over CTAs, fixed-order sum */
+    SGEMM_VARIANT_TMA_64x64_SPLITK = 4, /* 64 x 64 tiles, stream-K over all tiles, fixed-order sum */
     SGEMM_VARIANT_GENERIC = 5,       /* scalar loads, any alignment, 64 x 64 CTA tile       */
     SGEMM_VARIANT_SCALE = 6,         /* reported only: the C <- beta*C quick path ran       */
     SGEMM_VARIANT_TC_3XTF32 = 7,     /* tensor cores (tcgen05, TMEM), 3xTF32 split precision,
@@ -108,7 +108,7 @@ typedef enum {
 /* Create a handle bound to the CURRENT CUDA device.  Requires compute
  * capability 10.3 (GB300); otherwise returns SGEMM_ERR_UNSUPPORTED_DEVICE and
  * sets *out to NULL.  Allocates the handle's device-side status word and its
- * split-K workspace (a few MiB, zeroed) and sets the kernels' shared-memory
+ * stream-K workspace (48 MiB) and arrival counters (zeroed) and sets the kernels' shared-memory
  * limits.  `out` must be non-NULL (else SGEMM_ERR_NULL). */
 int sgemm_create(sgemm_handle_t *out);
 
@@ -185,7 +185,8 @@ int sgemm_set_math_mode(sgemm_handle_t h, int mode);
 
 /* The variant the handle's last successful sgemm_run enqueued (an
  * sgemm_variant_t), or -1 if there was none or `h` is not a live handle.
- * For the split-K variant, *splits (if non-NULL) receives the split count. */
+ * *splits (if non-NULL) receives the number of CTAs that share the K range of
+ * a stream-K tile (rounded up; 1 when no tile was split). */
 int sgemm_last_variant(sgemm_handle_t h, int *splits);
 
 /* Wait for the handle's device to finish its work, then read and clear the
@@ -213,7 +214,7 @@ int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
  * counterpart: this is a deployment convenience, not part of the method.
  *
  * Same arguments, rules and results as sgemm_run, but no handle: it runs the
- * 64 x 64 split-K kernel with its partial tiles, tile counters and status word
+ * 64 x 64 stream-K kernel with its partial tiles, tile counters and status word
  * in a fixed scratch array compiled into the library (8 MiB + 4 KiB + 256 B,
  * held on every GPU that loads the library until the process exits).
  * Limit: at most 512 output tiles of 64 x 64, i.e. ceil(M/64)*ceil(N/64) <= 512;

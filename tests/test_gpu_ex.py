@@ -230,25 +230,31 @@ def test_op_batched_tma(handle, variant, op, v):
     assert sgemm.sgemm_last_variant(handle)[0] == v
 
 
-@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
-def test_layouts_give_the_nn_bits(handle, variant, op):
+@pytest.mark.parametrize("op,K", [((0, 1), 300), ((1, 0), 300), ((1, 1), 64)], ids=["NT", "TN", "TT"])
+def test_layouts_give_the_nn_bits(handle, variant, op, K):
     """Every layout takes each product in ascending k with one rounding per
-    FMA, so (without a split) it returns the NN kernel's bits exactly."""
+    FMA, so it returns the NN kernel's bits exactly: NT and TN run the same
+    tile grid and stream-K plan as NN (K = 300: the tail's K steps are shared
+    by stream-K CTAs); TT runs on the transposed grid, so it matches where no
+    tile is split (K = 64: two K steps, too few to share)."""
     M = N = 264
-    K = 96  # 3 K steps: the tail plan never splits
     ref = ExProblem(0, 0, M, N, K, batch=1, seed=51, pad=(4, 4, 4))
     p = ExProblem(op[0], op[1], M, N, K, batch=1, seed=51, pad=(4, 4, 4))
-    # same logical operands as ref
-    for b in range(1):
-        a = ref.a_nn(b)
-        p._view(p.A, 0, p.ar, p.ac, p.lda)[:] = a.T if op[0] else a
-        bb = ref.b_nn(b)
-        p._view(p.B, 0, p.br, p.bc, p.ldb)[:] = bb.T if op[1] else bb
+    a = ref.a_nn(0)
+    p._view(p.A, 0, p.ar, p.ac, p.lda)[:] = a.T if op[0] else a
+    bb = ref.b_nn(0)
+    p._view(p.B, 0, p.br, p.bc, p.ldb)[:] = bb.T if op[1] else bb
     for v in (V.VARIANT_TMA_128x256, V.VARIANT_TMA_64x64):
         variant(v)
         C_ref, _ = ref.run(handle)
+        splits_ref = sgemm.sgemm_last_variant(handle)[1]
         C, bufs = p.run(handle)
-        assert sgemm.sgemm_last_variant(handle)[0] == v
+        ran, splits = sgemm.sgemm_last_variant(handle)
+        assert ran == v
+        if op != (1, 1):
+            assert splits == splits_ref
+        else:
+            assert splits == splits_ref == 1
         assert np.array_equal(ref.c_view(C_ref, 0).view(np.uint32), p.c_view(C, 0).view(np.uint32))
         p.check(C, bufs)
 
