@@ -127,8 +127,9 @@ long long sk_ctas_for(const sgemm_ctx *h, long long T, long long sk_tiles, long 
 }
 
 // The 64 x 64 split variant: every tile's K steps shared by up to one wave
-// of stream-K CTAs (one K step each at least), when that gives more CTAs
-// than tiles.
+// of stream-K CTAs (one K step each at least), when that gives at least two
+// CTAs per tile (with fewer, most tiles would stay whole and whole tiles
+// measure faster).
 void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     const long long tiles = 1LL * cdiv(M, 64) * cdiv(N, 64);
     const long long kt = cdiv(K, 32);
@@ -136,7 +137,7 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     if (tiles > h->n_counters) return;
     const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[SGEMM_VARIANT_TMA_64x64_SPLITK]);
     const long long G = sk_ctas_for(h, tiles * kt, tiles, slots, 64 * 64, 1);
-    if (G <= tiles) return;
+    if (G < 2 * tiles) return;
     *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
 }
 
@@ -166,15 +167,16 @@ int splits_of(const sg::SplitK &sk, int tiles) {
     return std::max(2, cdiv(sk.sk_ctas, std::max(1, tiles - sk.dp_tiles)));
 }
 
-// Estimated cost of running the call with `variant` (arbitrary units, lower
-// is better): the FLOP of one tile times the CTA slots the call occupies,
-// divided by the variant's main-loop efficiency measured on GB300 (fraction
-// of FP32 peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128
-// 0.80, 64 x 64 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63).
-// Complete waves occupy all P = SMs x CTAs-per-SM slots for a tile's time;
-// a stream-K part occupies them for ceil(T/G) K steps plus about one step of
-// fixup; an unsplit partial wave occupies them for a whole tile.  A batch
-// multiplies the tiles; batched calls are not split.
+// Estimated time of the call with `variant`, in microseconds (only the
+// ranking matters).  A K step of one CTA takes bm*bn*32 FMAs at the
+// variant's main-loop efficiency measured on GB300 (fraction of FP32 peak
+// with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
+// 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63), shared with the other
+// CTAs resident on its SM (fewer in a thin last wave).  Complete waves take
+// kt steps; a stream-K part takes ceil(T/G) steps plus its fixup (storing
+// and summing the parts: measured at about 15 us for the 128-row tiles and 2
+// us for 64 x 64, and 2 us for the second launch); an unsplit partial wave
+// takes kt steps.  A batch multiplies the tiles; batched calls are not split.
 double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
                     sg::SplitK *plan) {
     sg::TmaShape sh;
@@ -182,16 +184,21 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
     static const double kEff[3][3] = {{0.81, 0.80, 0.73}, {0.84, 0.84, 0.80}, {0.76, 0.75, 0.63}};
     const int vi = variant == SGEMM_VARIANT_TMA_128x256 ? 0 : variant == SGEMM_VARIANT_TMA_128x128 ? 1 : 2;
     const double eff = kEff[op][vi];
-    const double P = static_cast<double>(h->num_sms) * std::max(1, h->ctas_per_sm[variant]);
-    const double tile_flop = 2.0 * sh.bm * sh.bn * static_cast<double>(K);
+    const double cps = std::max(1, h->ctas_per_sm[variant]);
+    const double sms = h->num_sms, P = sms * cps;
+    const double t_step = static_cast<double>(sh.bm) * sh.bn * sh.bk * cps / (128.0 * eff * 2000.0);
+    const double fixup = vi == 2 ? 2.0 : 15.0;
     const double kt = cdiv(K, sh.bk);
     const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn) * batch;
+    // `ctas` CTAs for `steps` K steps each, as one wave
+    auto wave = [&](double ctas, double steps) {
+        return steps * t_step * std::min(cps, std::ceil(ctas / sms)) / cps;
+    };
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
         if (batch > 1) return 1e300;
         plan_splits(h, M, N, K, plan);
-        if (plan->sk_ctas == 0) return tile_flop * std::ceil(tiles / P) * P / eff;
-        // every slot busy for ceil(T/G) K steps, plus about one step for the fixup
-        return tile_flop / kt * (std::ceil(tiles * kt / plan->sk_ctas) + 1) * P / eff;
+        if (plan->sk_ctas == 0) return 1e300;  // runs as the whole-tile 64 x 64 variant
+        return wave(plan->sk_ctas, std::ceil(tiles * kt / plan->sk_ctas)) + fixup;
     }
     if (batch > 1) {
         *plan = sg::SplitK{cdiv(M, sh.bm) * cdiv(N, sh.bn), 0, nullptr, nullptr};
@@ -200,12 +207,12 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
         plan_tail(h, variant, shape, M, N, K, plan);
     }
     const double full = std::floor(tiles / P), rem = tiles - full * P;
-    double tail = 0.0;
+    double t = full * kt * t_step;
     if (plan->sk_ctas > 0)
-        tail = tile_flop / kt * (std::ceil(rem * kt / plan->sk_ctas) + 1) * P;
+        t += wave(plan->sk_ctas, std::ceil(rem * kt / plan->sk_ctas)) + fixup + (full > 0 ? 2.0 : 0.0);
     else if (rem > 0)
-        tail = tile_flop * P;
-    return (tile_flop * full * P + tail) / eff;
+        t += wave(rem, kt);
+    return t;
 }
 
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the

@@ -110,7 +110,7 @@ constexpr int kGroupM = 8;
 
 using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
 using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
-using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 2>;      // SGEMM_VARIANT_TMA_64x64 (+ split-K)
+using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 3>;      // SGEMM_VARIANT_TMA_64x64 (+ stream-K variant)
 // NT adds two B-sized transpose buffers, so its two larger tiles keep fewer
 // stages within the shared memory of one (128 x 256) or two (128 x 128) CTAs.
 using CfgLnt = Cfg<128, 256, 2, 4, 8, 16, 3, 1>;
@@ -346,27 +346,45 @@ __device__ __forceinline__ void sk_reduce_epilogue(const GemmArgs g, const float
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
     const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
-    // groups in chunks of kChunk: the chunk's loads of one part are
-    // independent of one another, so they are in flight together
+    // groups in chunks of kChunk, parts kU at a time: the kChunk * kU loads of
+    // a round are independent, so they are in flight together (a split tile
+    // has several parts and each round costs an L2 round trip)
     constexpr int kGroups = C::TM * C::TN4;
     constexpr int kChunk = kGroups < 8 ? kGroups : 8;
+    constexpr int kU = 4;
     static_assert(kGroups % kChunk == 0, "whole chunks");
+    const size_t part_stride = kTileFloats / 4;  // float4s per part
+    const float4 *base = reinterpret_cast<const float4 *>(ws) + static_cast<size_t>(tl) * part_stride + tid;
 #pragma unroll 1
     for (int u0 = 0; u0 < kGroups; u0 += kChunk) {
         float4 sum[kChunk];
-        for (int qq = q_first; qq <= q_last; ++qq) {
-            const float4 *part = reinterpret_cast<const float4 *>(ws + static_cast<size_t>(tl + qq) * kTileFloats) +
-                                 u0 * C::kConsumers + tid;
+        const float4 *pc = base + u0 * C::kConsumers;
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c) sum[c] = __ldcg(pc + static_cast<size_t>(q_first) * part_stride + c * C::kConsumers);
+        int qq = q_first + 1;
+#pragma unroll 1
+        for (; qq + kU - 1 <= q_last; qq += kU) {
+            float4 p[kU][kChunk];
+#pragma unroll
+            for (int r = 0; r < kU; ++r)
+#pragma unroll
+                for (int c = 0; c < kChunk; ++c)
+                    p[r][c] = __ldcg(pc + static_cast<size_t>(qq + r) * part_stride + c * C::kConsumers);
+#pragma unroll
+            for (int r = 0; r < kU; ++r)  // ascending k
+#pragma unroll
+                for (int c = 0; c < kChunk; ++c) {
+                    sum[c].x += p[r][c].x; sum[c].y += p[r][c].y; sum[c].z += p[r][c].z; sum[c].w += p[r][c].w;
+                }
+        }
+#pragma unroll 1
+        for (; qq <= q_last; ++qq) {
             float4 p[kChunk];
 #pragma unroll
-            for (int c = 0; c < kChunk; ++c) p[c] = __ldcg(part + c * C::kConsumers);
+            for (int c = 0; c < kChunk; ++c) p[c] = __ldcg(pc + static_cast<size_t>(qq) * part_stride + c * C::kConsumers);
 #pragma unroll
             for (int c = 0; c < kChunk; ++c) {
-                if (qq == q_first) {
-                    sum[c] = p[c];
-                } else {
-                    sum[c].x += p[c].x; sum[c].y += p[c].y; sum[c].z += p[c].z; sum[c].w += p[c].w;
-                }
+                sum[c].x += p[c].x; sum[c].y += p[c].y; sum[c].z += p[c].z; sum[c].w += p[c].w;
             }
         }
 #pragma unroll
@@ -554,24 +572,27 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
     }
     if (aborted) return;
-    if (!SPLIT || q < 0 || nseg_done == 0) {
-        // a whole tile, in acc
-        epilogue<C, OP>(acc, g, Cb, m0w, n0w, wm, wn, lane_m, lane_n);
-        return;
-    }
-    // stream-K: finish each split tile whose last part this CTA delivered
+    if constexpr (SPLIT) {
+        if (q >= 0 && nseg_done > 0) {
+            // stream-K: finish each split tile whose last part this CTA delivered
 #pragma unroll 1
-    for (int seg = 0; seg < 2; ++seg) {
-        if (!((split_last >> seg) & 1)) continue;
-        const int tile = tile0 + seg, tl = tile - sk.dp_tiles;
-        int tm, tn;
-        tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
-        __threadfence();
-        sk_reduce_epilogue<C, OP>(g, sk.ws, Cb, tl, sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas),
-                                  sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas),
-                                  tm * C::BM, tn * C::BN);
-        if (tid == 0) sk.counters[tl] = 0;  // ready for the next call
+            for (int sg2 = 0; sg2 < 2; ++sg2) {
+                if (!((split_last >> sg2) & 1)) continue;
+                const int tile = tile0 + sg2, tl = tile - sk.dp_tiles;
+                int tm, tn;
+                tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+                __threadfence();
+                sk_reduce_epilogue<C, OP>(g, sk.ws, Cb, tl,
+                                          sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas),
+                                          sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas),
+                                          tm * C::BM, tn * C::BN);
+                if (tid == 0) sk.counters[tl] = 0;  // ready for the next call
+            }
+            return;
+        }
     }
+    // a whole tile, in acc
+    epilogue<C, OP>(acc, g, Cb, m0w, n0w, wm, wn, lane_m, lane_n);
 }
 
 template <class C>
