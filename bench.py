@@ -36,12 +36,13 @@ sys.path.insert(0, ROOT)
 METRIC = "SGEMM TFLOP/s (2MNK/t) at 4096³ and 8192³; % of GB300 FP32 peak"
 UNIT = "TFLOP/s"
 
-# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture, keyed by the SHA-256 of the kernel source it was taken on; any
-# other source gives traffic = null.  See profiles/.
-# (profiles/sgemm_8192cube_dram.md, 8192^3 launches)
-TRAFFIC_BY_SOURCE = {"728b753fefc20bac": 3.116e9}
-TC_TRAFFIC_BY_SOURCE = {"d8ac4d90e2415f26": 3.112e9}
+# DRAM bytes (read + write) per step of the dominant kernel at 8192^3, from
+# one ncu capture, keyed by the SHA-256 of the kernel source it was taken on;
+# any other source gives traffic = null (profiles/sgemm_8192cube_dram.md).
+# The SIMT step is two launches of the same kernel template (13 complete
+# waves of whole tiles: 2.988 GB; the stream-K last wave: 0.493 GB).
+TRAFFIC_BY_SOURCE = {"97d6521bf15e27bb": 3.481e9}
+TC_TRAFFIC_BY_SOURCE = {"1a7b6ea63a862088": 2.534e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
 TC_KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tc.cu",
@@ -434,6 +435,7 @@ def main():
     ms_step = total_ms / args.steps
     value = cfg.flops * world / (ms_step * 1e-3) / 1e12
     variant, splits = sg.sgemm_last_variant(h)
+    launches_per_step = sg.sgemm_last_launches(h)
     status = sg.sgemm_get_device_status(h)
     if status != sg.OK:
         raise SystemExit(f"device status after the timed region: {sg.status_string(status)}")
@@ -511,11 +513,12 @@ def main():
                    "inputs": "i.i.d. U[-1,1) float32",
                    "l2": "inputs larger than L2 (working set %d MiB)" % ((prob.A.nbytes + prob.B.nbytes + prob.C0.nbytes) >> 20),
                    "variant": sg.variant_name(variant), "splits": splits, "op": args.op,
+                   "launches_per_step": launches_per_step,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                 "api": "sgemm_run_host (page-locked host buffers, copies overlapped with row-panel GEMMs)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "roofline": roofline,
         "clocks": clocks,
         "gpu": {"name": props.name, "sms": sms},

@@ -29,6 +29,7 @@ struct sgemm_ctx {
     int pinned;
     int last_variant;
     int last_splits;
+    int last_launches;  // kernel launches the last successful call enqueued
     int smem_override;
     int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
     int math_mode;                          // sgemm_math_mode_t
@@ -429,6 +430,11 @@ int sgemm_last_variant(sgemm_handle_t h, int *splits) {
     return h->last_variant;
 }
 
+int sgemm_last_launches(sgemm_handle_t h) {
+    if (!alive(h)) return -1;
+    return h->last_launches;
+}
+
 int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
     if (bytes < 0) return SGEMM_ERR_INVALID_VALUE;
@@ -452,6 +458,7 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     if (st != SGEMM_OK) return st;
     h->last_variant = -1;
     h->last_splits = 1;
+    h->last_launches = 0;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (batch == 1) strideA = strideB = strideC = 0;  // unused: keep the kernels on 2-D maps
@@ -468,7 +475,10 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         // C = beta*C (C = 0 when beta == 0); beta == 1 leaves C as it is.
         int rc = SGEMM_OK;
         if (beta != 1.f) rc = from_cuda(sg::launch_scale(g, stream));
-        if (rc == SGEMM_OK) h->last_variant = SGEMM_VARIANT_SCALE;
+        if (rc == SGEMM_OK) {
+            h->last_variant = SGEMM_VARIANT_SCALE;
+            h->last_launches = beta != 1.f ? 1 : 0;
+        }
         return rc;
     }
 
@@ -515,7 +525,10 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         const int rc = from_cuda(variant == SGEMM_VARIANT_TC_3XTF32
                                      ? sg::launch_tc3x(g, tA, tB, h->smem_override, stream)
                                      : sg::launch_tc3x_pair(g, tA, tB, h->smem_override, stream));
-        if (rc == SGEMM_OK) h->last_variant = variant;
+        if (rc == SGEMM_OK) {
+            h->last_variant = variant;
+            h->last_launches = 1;
+        }
         return rc;
     }
 
@@ -541,13 +554,17 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     }
     if (variant == SGEMM_VARIANT_GENERIC) {
         const int rc = from_cuda(sg::launch_generic(g, stream));
-        if (rc == SGEMM_OK) h->last_variant = variant;
+        if (rc == SGEMM_OK) {
+            h->last_variant = variant;
+            h->last_launches = 1;
+        }
         return rc;
     }
     const int rc = from_cuda(sg::launch_tma_op(op, variant, k, tmA, tmB, sk, h->smem_override, stream));
     if (rc == SGEMM_OK) {
         h->last_variant = variant;
         h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn));
+        h->last_launches = sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1;  // whole-tile waves, then stream-K
     }
     return rc;
 }

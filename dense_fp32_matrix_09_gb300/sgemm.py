@@ -45,7 +45,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
-           "sgemm_run_ex", "sgemm_check_args_ex")
+           "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches")
 
 
 class SgemmError(RuntimeError):
@@ -76,6 +76,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_destroy.argtypes = [vp]
         L.sgemm_set_variant.argtypes = [vp, i32]
         L.sgemm_last_variant.argtypes = [vp, ctypes.POINTER(i32)]
+        L.sgemm_last_launches.argtypes = [vp]
         L.sgemm_get_device_status.argtypes = [vp]
         L.sgemm_debug_timeout_probe.argtypes = [vp, ctypes.c_longlong, vp]
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
@@ -201,6 +202,10 @@ def sgemm_last_variant(h) -> tuple[int, int]:
     splits = ctypes.c_int(0)
     v = lib().sgemm_last_variant(h, ctypes.byref(splits))
     return v, splits.value
+
+
+def sgemm_last_launches(h) -> int:
+    return lib().sgemm_last_launches(h)
 
 
 def sgemm_get_device_status(h) -> int:

@@ -189,6 +189,12 @@ int sgemm_set_math_mode(sgemm_handle_t h, int mode);
  * a stream-K tile (rounded up; 1 when no tile was split). */
 int sgemm_last_variant(sgemm_handle_t h, int *splits);
 
+/* Number of kernel launches the handle's last successful sgemm_run /
+ * sgemm_run_ex enqueued: 0 (nothing to do), 1, or 2 (complete waves of whole
+ * tiles, then the stream-K CTAs of the last wave, on the same stream); -1 if
+ * `h` is not a live handle. */
+int sgemm_last_launches(sgemm_handle_t h);
+
 /* Wait for the handle's device to finish its work, then read and clear the
  * handle's device-side status word.  Returns SGEMM_OK, or
  * SGEMM_ERR_DEVICE_TIMEOUT if any kernel of the handle abandoned a bounded
