@@ -282,3 +282,16 @@ def test_unaligned_batch_stride_uses_generic(handle):
     C, bufs = p.run(handle)
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_GENERIC
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_batch_with_more_tiles_than_slots(handle, variant, op):
+    """A batch with more 64 x 64 tiles than resident CTA slots (several waves on
+    grid y): ragged 40 x 72 x 50 matrices, two tiles each, gaps between batch
+    matrices, every layout."""
+    variant(V.VARIANT_TMA_64x64)
+    p = ExProblem(op[0], op[1], 40, 72, 50, batch=500, seed=91, alpha=0.5, beta=1.5, pad=(4, 4, 4),
+                  gap=(8, 12, 4), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TMA_64x64
