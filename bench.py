@@ -94,6 +94,8 @@ def parse():
     p.add_argument("--tensor-steps", type=int, default=50)
     p.add_argument("--op", default="NN", choices=["NN", "NT", "TN", "TT"],
                    help="operand layout of the timed step (sgemm_run_ex; square unpadded workloads only)")
+    p.add_argument("--no-mixed", action="store_true",
+                   help="skip the 16-bit-input (BF16 / FP16, FP32 accumulation) block (sgemm_run_mixed)")
     p.add_argument("--no-ex", action="store_true",
                    help="skip the transposed-layout and strided-batched block (sgemm_run_ex)")
     return p.parse_args()
@@ -344,6 +346,35 @@ def bench_ex(torch, sg, h, cfg, A, B, C, stream, warmup: int) -> dict:
     return res
 
 
+def bench_mixed(torch, sg, h, cfg, C, stream, warmup: int) -> dict:
+    """16-bit A and B (i.i.d. U[-1,1) rounded to BF16 / FP16), FP32 C, n^3, all
+    four layouts for BF16 and NN for FP16; roofline = the measured dense BF16
+    tensor throughput (the same for FP16)."""
+    n = cfg.M
+    flops = 2.0 * n * n * n
+    g = torch.Generator(device="cpu").manual_seed(5)
+    res = {}
+    peak = measured_bf16_tflops()
+    for tname, in_type, dt in (("bf16", sg.IN_BF16, torch.bfloat16), ("f16", sg.IN_F16, torch.float16)):
+        A16 = (torch.rand(n * n, generator=g) * 2 - 1).to(dt).cuda()
+        B16 = (torch.rand(n * n, generator=g) * 2 - 1).to(dt).cuda()
+        for name, ta, tb in (("NN", 0, 0), ("NT", 0, 1), ("TN", 1, 0), ("TT", 1, 1)):
+            if tname == "f16" and name != "NN":
+                continue
+            def call(ta=ta, tb=tb):
+                sg.sgemm_run_mixed(h, in_type, ta, tb, n, n, n, 1.0, A16, n, B16, n, 0.0, C, n, stream)
+            ms = time_calls(torch, stream, call, 20, warmup)
+            v, _ = sg.sgemm_last_variant(h)
+            med = statistics.median(ms)
+            tf = flops / (med * 1e-3) / 1e12
+            res[f"{tname}_{name}"] = {"ms_median": med, "tflops": tf, "variant": sg.variant_name(v),
+                                      "frac_of_bf16_peak": tf / peak["value"]}
+        del A16, B16
+    res["roofline"] = {"bound": "tensor", "peak": peak["value"], "unit": "TFLOP/s", "peak_source": peak["source"],
+                       "peak_basis": "dense BF16 (FP16 is the same rate), burst, MEASURED_PEAKS.json"}
+    return res
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -562,6 +593,10 @@ def main():
     # strided batch of 1024 products of 64 x 64 matrices (device-resident)
     if not args.no_ex and rank == 0 and cfg.M == cfg.N == cfg.K == cfg.lda == cfg.ldb == cfg.ldc:
         out["layouts_and_batched"] = bench_ex(torch, sg, h, cfg, A, B, C, stream, args.warmup)
+
+    # ---- sgemm_run_mixed: BF16 / FP16 inputs, FP32 accumulation, at the headline size
+    if not args.no_mixed and rank == 0 and cfg.M == cfg.N == cfg.K == cfg.lda == cfg.ldb == cfg.ldc:
+        out["mixed_16bit"] = bench_mixed(torch, sg, h, cfg, C, stream, args.warmup)
 
     # ---- per-workload table (device-resident; not part of the headline value)
     if not args.no_workloads and rank == 0:

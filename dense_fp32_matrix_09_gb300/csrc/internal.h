@@ -91,7 +91,16 @@ cudaError_t tc3x_pair_prepare();
 cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                              int smem_override, cudaStream_t stream);
 
-cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream);
+// in_type: 0 FP32 inputs, else SGEMM_IN_BF16 / SGEMM_IN_F16 (A and B hold 16-bit values)
+cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream, int in_type = 0);
+
+// 16-bit-input tensor-core kernel (sgemm_tc16.cu), CTA pairs, 256 x 256 tiles:
+// A map box 64 k x 128 m (K-major, A stored M x K) or 64 m x 64 k (A stored
+// K x M, g.transA); B map box 64 n x 64 k (B stored K x N) or 64 k x 128 n
+// (B stored N x K, g.transB); 16-bit elements, 128-byte swizzle.
+cudaError_t tc16_prepare();
+cudaError_t launch_tc16(bool bf16, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                        int smem_override, cudaStream_t stream);
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);
 cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);
 

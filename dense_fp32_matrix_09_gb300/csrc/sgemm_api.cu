@@ -55,10 +55,11 @@ bool alive(sgemm_ctx *h) {
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline int cdiv(int a, int b) { return (a + b - 1) / b; }
 
-// [lo, hi) byte range of a rows x cols window with leading dimension ld.
-inline void window(const void *p, int rows, int cols, int ld, uintptr_t *lo, uintptr_t *hi) {
+// [lo, hi) byte range of a rows x cols window with leading dimension ld
+// (elements of `esize` bytes, FP32 by default).
+inline void window(const void *p, int rows, int cols, int ld, uintptr_t *lo, uintptr_t *hi, size_t esize = 4) {
     *lo = reinterpret_cast<uintptr_t>(p);
-    *hi = *lo + (static_cast<uintptr_t>(rows - 1) * static_cast<uintptr_t>(ld) + cols) * sizeof(float);
+    *hi = *lo + (static_cast<uintptr_t>(rows - 1) * static_cast<uintptr_t>(ld) + cols) * esize;
 }
 
 inline bool overlap(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
@@ -98,6 +99,19 @@ bool encode_2d(CUtensorMap *map, const float *base, int rows, int cols, int ld, 
     cuuint32_t estr[2] = {1, 1};
     return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D row-major matrix of 16-bit elements (BF16 or FP16) as a TMA tensor.
+bool encode_2d_16(CUtensorMap *map, bool bf16, const void *base, int rows, int cols, int ld, int box_cols,
+                  int box_rows) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -267,6 +281,8 @@ const char *sgemm_variant_name(int v) {
         case SGEMM_VARIANT_SCALE: return "scale";
         case SGEMM_VARIANT_TC_3XTF32: return "tc_3xtf32";
         case SGEMM_VARIANT_TC_3XTF32_PAIR: return "tc_3xtf32_pair";
+        case SGEMM_VARIANT_TC_F16_PAIR: return "tc_f16_pair";
+        case SGEMM_VARIANT_GENERIC_F16: return "generic_f16";
         default: return "unknown";
     }
 }
@@ -327,9 +343,12 @@ int sgemm_create(sgemm_handle_t *out) {
         occupancy[v] = sg::tma_ctas_per_sm(v);
         if (occupancy[v] < 1) return SGEMM_ERR_CUDA;
     }
-    if (sg::tc3x_prepare() != cudaSuccess || sg::tc3x_pair_prepare() != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (sg::tc3x_prepare() != cudaSuccess || sg::tc3x_pair_prepare() != cudaSuccess ||
+        sg::tc16_prepare() != cudaSuccess)
+        return SGEMM_ERR_CUDA;
     occupancy[SGEMM_VARIANT_TC_3XTF32] = 1;
     occupancy[SGEMM_VARIANT_TC_3XTF32_PAIR] = 1;
+    occupancy[SGEMM_VARIANT_TC_F16_PAIR] = 1;
 
     sgemm_ctx *h = new (std::nothrow) sgemm_ctx();
     if (!h) return SGEMM_ERR_CUDA;
@@ -566,6 +585,73 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn));
         h->last_launches = sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1;  // whole-tile waves, then stream-K
     }
+    return rc;
+}
+
+int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, int K, float alpha, const void *A,
+                           int lda, const void *B, int ldb, float beta, const float *C, int ldc) {
+    (void)beta;
+    if (in_type != SGEMM_IN_BF16 && in_type != SGEMM_IN_F16) return SGEMM_ERR_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return SGEMM_ERR_INVALID_VALUE;
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1)) return SGEMM_ERR_INVALID_VALUE;
+    const int a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
+        return SGEMM_ERR_INVALID_VALUE;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    if (C == nullptr) return SGEMM_ERR_NULL;
+    if (alpha == 0.f || K == 0) return SGEMM_OK;
+    if (A == nullptr || B == nullptr) return SGEMM_ERR_NULL;
+    uintptr_t a0, a1, b0, b1, c0, c1;
+    window(A, a_rows, a_cols, lda, &a0, &a1, 2);
+    window(B, b_rows, b_cols, ldb, &b0, &b1, 2);
+    window(C, M, N, ldc, &c0, &c1);
+    if (overlap(c0, c1, a0, a1) || overlap(c0, c1, b0, b1)) return SGEMM_ERR_ALIAS;
+    return SGEMM_OK;
+}
+
+int sgemm_run_mixed(sgemm_handle_t h, int in_type, int transA, int transB, int M, int N, int K, float alpha,
+                    const void *A, int lda, const void *B, int ldb, float beta, float *C, int ldc, void *stream_) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    const int st = sgemm_check_args_mixed(in_type, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
+    if (st != SGEMM_OK) return st;
+    h->last_variant = -1;
+    h->last_splits = 1;
+    h->last_launches = 0;
+    if (M == 0 || N == 0) return SGEMM_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    sg::GemmArgs g{M, N, K, alpha, beta, static_cast<const float *>(A), lda, static_cast<const float *>(B), ldb,
+                   C, ldc, aligned16(C) && (ldc % 4) == 0, h->d_status};
+    g.transA = transA;
+    g.transB = transB;
+    int rc = SGEMM_OK, variant;
+    if (alpha == 0.f || K == 0) {
+        // C = beta*C (C = 0 when beta == 0); beta == 1 leaves C as it is.
+        if (beta != 1.f) rc = from_cuda(sg::launch_scale(g, stream));
+        variant = SGEMM_VARIANT_SCALE;
+        if (rc == SGEMM_OK) h->last_launches = beta != 1.f ? 1 : 0;
+    } else {
+        const bool bf16 = in_type == SGEMM_IN_BF16;
+        const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 8) == 0 && (ldb % 8) == 0;
+        variant = tma_ok && h->pinned != SGEMM_VARIANT_GENERIC ? SGEMM_VARIANT_TC_F16_PAIR
+                                                               : SGEMM_VARIANT_GENERIC_F16;
+        CUtensorMap tmA, tmB;
+        if (variant == SGEMM_VARIANT_TC_F16_PAIR) {
+            const bool a_ok = transA ? encode_2d_16(&tmA, bf16, A, K, M, lda, 64, 64)   // A stored K x M
+                                     : encode_2d_16(&tmA, bf16, A, M, K, lda, 64, 128);
+            const bool b_ok = transB ? encode_2d_16(&tmB, bf16, B, N, K, ldb, 64, 128)  // B stored N x K
+                                     : encode_2d_16(&tmB, bf16, B, K, N, ldb, 64, 64);
+            if (!a_ok || !b_ok) variant = SGEMM_VARIANT_GENERIC_F16;  // a layout TMA cannot describe
+        }
+        if (variant == SGEMM_VARIANT_TC_F16_PAIR)
+            rc = from_cuda(sg::launch_tc16(bf16, g, tmA, tmB, h->smem_override, stream));
+        else
+            rc = from_cuda(sg::launch_generic(g, stream, in_type));
+        if (rc == SGEMM_OK) h->last_launches = 1;
+    }
+    if (rc == SGEMM_OK) h->last_variant = variant;
     return rc;
 }
 

@@ -2,7 +2,8 @@
 //
 //  * sgemm_generic_kernel -- the any-alignment SIMT path, used when A or B
 //    cannot be described to TMA (pointer not 16-byte aligned or lda / ldb not
-//    a multiple of 4).  64 x 64 CTA tile, K step 16, 256 threads with a 4 x 4
+//    a multiple of 16 bytes); A and B may be FP32, BF16 or FP16 (converted
+//    exactly to FP32 on load), any layout and batch.  64 x 64 CTA tile, K step 16, 256 threads with a 4 x 4
 //    register block each.  Tiles are staged through shared memory with scalar
 //    loads; elements outside the matrices are filled with 0 at load (page
 //    m.lqnn.cn/news/94381 section 2.3, boundary handling by zero-fill at load;
@@ -16,21 +17,42 @@
 //  * timeout_probe_kernel -- waits on an mbarrier that nothing completes,
 //    gives up after a short limit and records the timeout, to test the
 //    device-side timeout reporting without faulting or hanging the GPU.
+#include <cuda_fp16.h>
+
 #include "device_common.cuh"
 #include "internal.h"
+#include "sgemm.h"
 
 namespace sg {
 namespace {
 
 constexpr int GB = 64, GK = 16, GT = 256;
 
+// Stored element types of A and B: FP32, or the bits of a BF16 / FP16 value
+// (converted exactly to FP32 on load).
+struct InF32 {
+    using T = float;
+    __device__ static float get(float x) { return x; }
+};
+struct InBF16 {
+    using T = uint16_t;
+    __device__ static float get(uint16_t x) { return __uint_as_float(static_cast<uint32_t>(x) << 16); }
+};
+struct InF16 {
+    using T = uint16_t;
+    __device__ static float get(uint16_t x) { return __half2float(__ushort_as_half(x)); }
+};
+
+template <class In>
 __global__ void __launch_bounds__(GT) sgemm_generic_kernel(const GemmArgs g) {
+    using T = typename In::T;
     __shared__ float As[GK][GB + 4];  // A tile stored k-major: As[k][m]
     __shared__ float Bs[GK][GB + 4];  // B tile: Bs[k][n]
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     const int m0 = blockIdx.y * GB, n0 = blockIdx.x * GB;
+    const T *A = reinterpret_cast<const T *>(g.A), *B = reinterpret_cast<const T *>(g.B);
     for (int b = blockIdx.z; b < g.batch; b += gridDim.z) {
-        const float *Ab = g.A + b * g.sA, *Bb = g.B + b * g.sB;
+        const T *Ab = A + b * g.sA, *Bb = B + b * g.sB;
         float *Cb = g.C + b * g.sC;
         float acc[4][4] = {};
         for (int k0 = 0; k0 < g.K; k0 += GK) {
@@ -43,14 +65,16 @@ __global__ void __launch_bounds__(GT) sgemm_generic_kernel(const GemmArgs g) {
                 const int gm = m0 + am, gk = k0 + ak;
                 float av = 0.f;
                 if (gm < g.M && gk < g.K)
-                    av = g.transA ? Ab[static_cast<size_t>(gk) * g.lda + gm] : Ab[static_cast<size_t>(gm) * g.lda + gk];
+                    av = In::get(g.transA ? Ab[static_cast<size_t>(gk) * g.lda + gm]
+                                          : Ab[static_cast<size_t>(gm) * g.lda + gk]);
                 As[ak][am] = av;
                 int bk, bn;
                 if (g.transB) { bn = e / GK; bk = e % GK; } else { bk = e / GB; bn = e % GB; }
                 const int hk = k0 + bk, hn = n0 + bn;
                 float bv = 0.f;
                 if (hk < g.K && hn < g.N)
-                    bv = g.transB ? Bb[static_cast<size_t>(hn) * g.ldb + hk] : Bb[static_cast<size_t>(hk) * g.ldb + hn];
+                    bv = In::get(g.transB ? Bb[static_cast<size_t>(hn) * g.ldb + hk]
+                                          : Bb[static_cast<size_t>(hk) * g.ldb + hn]);
                 Bs[bk][bn] = bv;
             }
             __syncthreads();
@@ -120,9 +144,11 @@ __global__ void timeout_probe_kernel(int *status, long long limit_ns) {
 
 }  // namespace
 
-cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream) {
+cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream, int in_type) {
     const dim3 grid((g.N + GB - 1) / GB, (g.M + GB - 1) / GB, min(g.batch, 65535));
-    sgemm_generic_kernel<<<grid, GT, 0, stream>>>(g);
+    if (in_type == SGEMM_IN_BF16) sgemm_generic_kernel<InBF16><<<grid, GT, 0, stream>>>(g);
+    else if (in_type == SGEMM_IN_F16) sgemm_generic_kernel<InF16><<<grid, GT, 0, stream>>>(g);
+    else sgemm_generic_kernel<InF32><<<grid, GT, 0, stream>>>(g);
     return cudaGetLastError();
 }
 

@@ -139,3 +139,13 @@ def with_guards(buf: np.ndarray, guard: int = 64) -> np.ndarray:
     out.view(np.uint32)[:] = GUARD_BITS
     out[guard:guard + buf.size] = buf
     return out
+
+
+def to_half_bits(x: np.ndarray, in_type: str) -> tuple[np.ndarray, np.ndarray]:
+    """Round float32 values to 16 bits (round to nearest even) for 16-bit-input
+    GEMMs: returns (the 16-bit patterns as uint16, the same values as float32,
+    exactly).  in_type: "bf16" or "f16".  Input preparation only."""
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    h = t.to(torch.bfloat16 if in_type == "bf16" else torch.float16)
+    return h.view(torch.int16).numpy().view(np.uint16).copy(), h.to(torch.float32).numpy().copy()
+

@@ -35,8 +35,12 @@ VARIANT_GENERIC = 5
 VARIANT_SCALE = 6
 VARIANT_TC_3XTF32 = 7
 VARIANT_TC_3XTF32_PAIR = 8
+VARIANT_TC_F16_PAIR = 9
+VARIANT_GENERIC_F16 = 10
 MATH_FP32 = 0
 MATH_3XTF32 = 1
+IN_BF16 = 1
+IN_F16 = 2
 GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
                  VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32, VARIANT_TC_3XTF32_PAIR)
 
@@ -45,7 +49,8 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_last_variant", "sgemm_get_device_status", "sgemm_debug_timeout_probe",
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
-           "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches")
+           "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
+           "sgemm_check_args_mixed")
 
 
 class SgemmError(RuntimeError):
@@ -77,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.sgemm_set_variant.argtypes = [vp, i32]
         L.sgemm_last_variant.argtypes = [vp, ctypes.POINTER(i32)]
         L.sgemm_last_launches.argtypes = [vp]
+        L.sgemm_run_mixed.argtypes = [vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
+        L.sgemm_check_args_mixed.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32]
         L.sgemm_get_device_status.argtypes = [vp]
         L.sgemm_debug_timeout_probe.argtypes = [vp, ctypes.c_longlong, vp]
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
@@ -202,6 +209,19 @@ def sgemm_last_variant(h) -> tuple[int, int]:
     splits = ctypes.c_int(0)
     v = lib().sgemm_last_variant(h, ctypes.byref(splits))
     return v, splits.value
+
+
+def sgemm_run_mixed(h, in_type, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
+    """C <- alpha*op(A)*op(B) + beta*C with 16-bit A, B and FP32 C (see include/sgemm.h)."""
+    _check(lib().sgemm_run_mixed(h, int(in_type), int(transA), int(transB), int(M), int(N), int(K), float(alpha),
+                                 _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc),
+                                 _stream(stream)), "sgemm_run_mixed")
+
+
+def sgemm_check_args_mixed(in_type, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc) -> int:
+    return lib().sgemm_check_args_mixed(int(in_type), int(transA), int(transB), int(M), int(N), int(K),
+                                        float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C),
+                                        int(ldc))
 
 
 def sgemm_last_launches(h) -> int:

@@ -83,7 +83,11 @@ typedef enum {
                                         128 x 256 CTA tile; FP32 inputs, outputs, tolerance   */
     SGEMM_VARIANT_TC_3XTF32_PAIR = 8,/* as TC_3XTF32 on CTA pairs (cta_group::2): 256 x 256
                                         tile per cluster of two CTAs                          */
-    SGEMM_VARIANT_COUNT_ = 9
+    SGEMM_VARIANT_TC_F16_PAIR = 9,   /* sgemm_run_mixed only: BF16 / FP16 A and B on the tensor
+                                        cores (kind::f16), FP32 accumulation, CTA pairs       */
+    SGEMM_VARIANT_GENERIC_F16 = 10,  /* sgemm_run_mixed only: the generic variant on 16-bit
+                                        inputs (any alignment)                                */
+    SGEMM_VARIANT_COUNT_ = 11
     /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
      * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
      * for batch > 1, strideA, strideB) are multiples of 4; otherwise the
@@ -104,6 +108,12 @@ typedef enum {
     SGEMM_MATH_FP32 = 0,
     SGEMM_MATH_3XTF32 = 1
 } sgemm_math_mode_t;
+
+/* Element type of A and B for sgemm_run_mixed (C is always FP32). */
+typedef enum {
+    SGEMM_IN_BF16 = 1,  /* bfloat16: 1 sign, 8 exponent, 7 fraction bits */
+    SGEMM_IN_F16 = 2    /* IEEE binary16 */
+} sgemm_input_t;
 
 /* Create a handle bound to the CURRENT CUDA device.  Requires compute
  * capability 10.3 (GB300); otherwise returns SGEMM_ERR_UNSUPPORTED_DEVICE and
@@ -142,6 +152,29 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
 int sgemm_check_args_ex(int transA, int transB, int M, int N, int K, float alpha, const float *A, int lda,
                         long long strideA, const float *B, int ldb, long long strideB, float beta,
                         const float *C, int ldc, long long strideC, int batch);
+
+/* Mixed precision: C <- alpha * op(A) * op(B) + beta * C with A and B holding
+ * 16-bit values (`in_type`: SGEMM_IN_BF16 or SGEMM_IN_F16; 2 bytes per element,
+ * leading dimensions in elements) and C in FP32.  op and the stored shapes as
+ * in sgemm_run_ex (batch 1).  Every product of two 16-bit values is exact in
+ * FP32; the products are summed in FP32 (on the tensor cores, whose FP32
+ * accumulation is not round-to-nearest), then alpha, beta and C as in
+ * sgemm_run.  Error contract: max |C - C_exact| within 1e-3 for K <= 1024
+ * and 1e-2 for K <= 8192 on inputs of magnitude <= 1, where C_exact is the
+ * exact result for the 16-bit inputs as given (the caller's rounding to 16 bits
+ * is not part of it).  Page "GPU-accelerated matrix computation optimisation
+ * and CUDA programming practice", section 4.1, uses this split (16-bit inputs,
+ * FP32 accumulation) through a library call; here it is a kernel of this
+ * library.  Runs SGEMM_VARIANT_TC_F16_PAIR when A and B are 16-byte aligned and
+ * lda, ldb are multiples of 8, else SGEMM_VARIANT_GENERIC_F16 (a pinned
+ * GENERIC variant also selects it).  Errors as sgemm_run_ex, plus
+ * SGEMM_ERR_INVALID_VALUE for an unknown in_type. */
+int sgemm_run_mixed(sgemm_handle_t h, int in_type, int transA, int transB, int M, int N, int K, float alpha,
+                    const void *A, int lda, const void *B, int ldb, float beta, float *C, int ldc, void *stream);
+
+/* Host-only validation of sgemm_run_mixed's arguments (same rules, no CUDA call). */
+int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, int K, float alpha, const void *A,
+                           int lda, const void *B, int ldb, float beta, const float *C, int ldc);
 
 /* C <- alpha*A*B + beta*C with A, B, C in HOST memory, transfers overlapped
  * with compute.  dA, dB, dC are caller-owned DEVICE buffers of the same

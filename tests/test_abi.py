@@ -135,6 +135,28 @@ def test_check_args_is_the_nn_batch1_case(lib):
     assert chk(4, 5, 6, C=A0 + 8) == chk_ex(0, 0, 4, 5, 6, C=A0 + 8) == ALIAS
 
 
+def chk_mixed(t, tA, tB, M, N, K, alpha=1.0, A=A0, lda=None, B=B0, ldb=None, beta=0.0, C=C0, ldc=None):
+    lda = max(M if tA else K, 1) if lda is None else lda
+    ldb = max(K if tB else N, 1) if ldb is None else ldb
+    ldc = max(N, 1) if ldc is None else ldc
+    return sgemm.sgemm_check_args_mixed(t, tA, tB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc)
+
+
+def test_check_args_mixed(lib):
+    for t in (sgemm.IN_BF16, sgemm.IN_F16):
+        assert chk_mixed(t, 0, 0, 4, 5, 6) == OK
+        assert chk_mixed(t, 1, 1, 4, 5, 6) == OK
+        assert chk_mixed(t, 1, 0, 4, 5, 6, lda=3) == INVALID      # A stored K x M: lda >= M
+        assert chk_mixed(t, 0, 1, 4, 5, 6, ldb=5) == INVALID      # B stored N x K: ldb >= K
+        assert chk_mixed(t, 0, 0, 4, 5, 6, C=None) == NULL_
+        assert chk_mixed(t, 0, 0, 4, 5, 6, alpha=0.0, A=None, B=None) == OK
+        # 16-bit windows: A = 4 x 6 halves = 48 bytes; C just past it is fine, inside it aliases
+        assert chk_mixed(t, 0, 0, 4, 5, 6, C=A0 + 48) == OK
+        assert chk_mixed(t, 0, 0, 4, 5, 6, C=A0 + 46) == ALIAS
+    assert chk_mixed(0, 0, 0, 4, 5, 6) == INVALID
+    assert chk_mixed(3, 0, 0, 4, 5, 6) == INVALID
+
+
 def test_bad_handles_are_rejected_without_dereference(lib):
     assert lib.sgemm_run(None, 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == sgemm.ERR_BAD_HANDLE
     assert lib.sgemm_run(ctypes.c_void_p(0x1234), 1, 1, 1, 1.0, A0, 1, B0, 1, 0.0, C0, 1, None) == \
