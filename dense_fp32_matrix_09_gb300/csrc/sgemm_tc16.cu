@@ -7,16 +7,21 @@
 // a kernel.  A product of two 16-bit values is exact in FP32, so the only
 // rounding is the FP32 accumulation.
 //
-// A cluster of two CTAs computes a 256 x 256 tile of C (tcgen05 cta_group::2):
-// each CTA holds 128 rows of A and 128 columns of B per stage, and one MMA of
-// M = 256, N = 256, K = 16 issued by the even CTA reads both CTAs' halves and
-// writes each CTA's 128 x 256 FP32 accumulator in its own tensor memory.
-//   warp 0    TMA producer (one lane, each CTA): stage s of a 6-stage ring gets
-//             this CTA's A and B tiles, 64 k deep (one 128-byte swizzle row of
+// A cluster of two CTAs computes a 256 x NP tile of C (tcgen05 cta_group::2;
+// NP = 512 when N >= 512, else 256): each CTA holds 128 rows of A and NP/2
+// columns of B per stage, and per K = 16 step the even CTA issues NP/256 MMAs
+// of M = 256, N = 256 (each reading 128 columns of B from either CTA), which
+// write each CTA's 128 x NP FP32 accumulator in its own tensor memory.  The
+// 256 x 512 tile moves 25 % fewer operand bytes per MAC than 256 x 256; the
+// kernel is bound by that operand traffic (measured: without the MMAs it runs
+// as fast; without the loads its MMAs reach 87 % of the measured BF16 peak).
+//   warp 0    TMA producer (one lane, each CTA): stage s of the ring (6 stages
+//             of 32 KiB for NP = 256, 4 of 48 KiB for NP = 512) gets this
+//             CTA's A and B tiles, 64 k deep (one 128-byte swizzle row of
 //             16-bit values), straight in the MMA's operand layout;
-//   warp 1    owns the tensor memory (256 columns); in the even CTA one lane
-//             issues the MMAs -- four K = 16 steps per stage -- and commits each
-//             stage to both CTAs' `empty` barriers (multicast);
+//   warp 1    owns the tensor memory (NP columns); in the even CTA one lane
+//             issues the MMAs and commits each stage to both CTAs' `empty`
+//             barriers (multicast);
 //   warp 2    (one lane, each CTA) waits for its CTA's stage to land and
 //             arrives on the even CTA's `ready` barrier of that stage, which
 //             the MMA lane waits for (two arrivals: both halves present);
@@ -42,26 +47,36 @@ namespace sg {
 namespace {
 
 constexpr int HBM_ = 128;                    // rows of A (and C) per CTA
-constexpr int HBN = 128;                     // columns of B per CTA (256 per pair)
 constexpr int HBK = 64;                      // k per stage
-constexpr int HSTAGES = 6;
 constexpr int kHABytes = HBM_ * HBK * 2;     // 16 KiB
-constexpr int kHBBytes = HBN * HBK * 2;      // 16 KiB
-constexpr int kHStage = kHABytes + kHBBytes;
 constexpr int kHThreads = 256;
-constexpr uint32_t kHTmemCols = 256;         // one 128 x 256 FP32 accumulator
+constexpr int kMaxStages = 6;
+
+// Pair tile 256 x NP (NP = 256 or 512): each CTA holds NP/2 columns of B per
+// stage, as NP/256 groups of 128 columns (one N = 256 MMA per group and K
+// step: CTA 0 gives the group's first 128 columns, CTA 1 the next 128), and
+// an FP32 accumulator of 128 rows x NP columns in tensor memory.  The wider
+// tile moves 25 % fewer operand bytes per MAC through L2 and TMA.
+template <int NP>
+struct Tc16Cfg {
+    static constexpr int kGroups = NP / 256;
+    static constexpr int kBBytes = kGroups * 128 * HBK * 2;          // 16 or 32 KiB
+    static constexpr int kStage = kHABytes + kBBytes;
+    static constexpr int kStages = NP == 256 ? 6 : 4;                // 192 KiB of stages
+    static constexpr uint32_t kTmemCols = NP;
+    static constexpr int kSmem = kStages * kStage + 256 + 1024;
+    static_assert(kSmem <= 232448, "dynamic shared memory above the per-CTA limit");
+};
 
 struct Tc16Smem {
-    uint64_t full[HSTAGES];   // this CTA's A and B tiles landed
-    uint64_t ready[HSTAGES];  // (even CTA) both CTAs' tiles landed: one arrival per CTA
-    uint64_t empty[HSTAGES];  // MMAs of the stage finished (multicast commit)
-    uint64_t acc_full;        // all MMAs finished
+    uint64_t full[kMaxStages];   // this CTA's A and B tiles landed
+    uint64_t ready[kMaxStages];  // (even CTA) both CTAs' tiles landed: one arrival per CTA
+    uint64_t empty[kMaxStages];  // MMAs of the stage finished (multicast commit)
+    uint64_t acc_full;           // all MMAs finished
     uint32_t tmem_base;
     int abort;
 };
-constexpr int kSmemTc16 = HSTAGES * kHStage + 256 + 1024;
 static_assert(sizeof(Tc16Smem) <= 256, "barrier block");
-static_assert(kSmemTc16 <= 232448, "dynamic shared memory above the per-CTA limit");
 
 // Instruction descriptor of tcgen05.mma .kind::f16: D FP32 (bits 4-5 = 1),
 // A and B format at bits 7-9 / 10-12 (0 FP16, 1 BF16), A / B major at bits
@@ -101,13 +116,14 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t base, int kk) {
     return tc::smem_desc(base + kk * 32, 16, 1024, tc::kLayoutSwizzle128);
 }
 
-// Epilogue of one lane quadrant q: row m0 + 32q + lane, 256 columns from n0.
-__device__ __forceinline__ void tc16_epilogue(const GemmArgs &g, uint32_t tmem, int q, int lane, int m0, int n0) {
+// Epilogue of one lane quadrant q: row m0 + 32q + lane, `cols` columns from n0.
+__device__ __forceinline__ void tc16_epilogue(const GemmArgs &g, uint32_t tmem, int q, int lane, int m0, int n0,
+                                              int cols) {
     const int row = m0 + q * 32 + lane;
     const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
     float *crow = g.C + static_cast<size_t>(row) * g.ldc;
 #pragma unroll 1
-    for (int c = 0; c < 2 * HBN / 16; ++c) {
+    for (int c = 0; c < cols / 16; ++c) {
         float v[16];
         tc::tmem_ld16(trow + c * 16, v);  // every lane of the warp takes part
         const int col0 = n0 + c * 16;
@@ -139,29 +155,30 @@ __device__ __forceinline__ void tc16_epilogue(const GemmArgs &g, uint32_t tmem, 
     }
 }
 
-template <bool BF16, bool A_MN, bool B_MN>
+template <bool BF16, bool A_MN, bool B_MN, int NP>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHThreads, 1)
 sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmArgs g) {
+    using Cf = Tc16Cfg<NP>;
+    constexpr int S = Cf::kStages;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *base = smem_raw + pad;  // same offset in both CTAs (same kernel, same layout)
-    Tc16Smem *sh = reinterpret_cast<Tc16Smem *>(base + HSTAGES * kHStage);
-    auto stA = [&](int s) { return base + s * kHStage; };
-    auto stB = [&](int s) { return base + s * kHStage + kHABytes; };
+    Tc16Smem *sh = reinterpret_cast<Tc16Smem *>(base + S * Cf::kStage);
+    auto stA = [&](int s) { return base + s * Cf::kStage; };
+    auto stB = [&](int s) { return base + s * Cf::kStage + kHABytes; };  // group j at + j * 16 KiB
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = tc::cluster_ctarank();  // 0: issues the MMAs
-    const int tiles_m = (g.M + 2 * HBM_ - 1) / (2 * HBM_), tiles_n = (g.N + 2 * HBN - 1) / (2 * HBN);
+    const int tiles_m = (g.M + 2 * HBM_ - 1) / (2 * HBM_), tiles_n = (g.N + NP - 1) / NP;
     int tm, tn;
     tile_coords16(blockIdx.x >> 1, tiles_m, tiles_n, tm, tn);
     const int m0 = tm * 2 * HBM_ + static_cast<int>(rank) * HBM_;  // this CTA's rows of A and C
-    const int n0 = tn * 2 * HBN;                                   // the tile's columns of C
-    const int nb0 = n0 + static_cast<int>(rank) * HBN;             // this CTA's columns of B
+    const int n0 = tn * NP;                                         // the tile's columns of C
     const int nkt = (g.K + HBK - 1) / HBK;
 
     if (tid == 0) {
-        for (int s = 0; s < HSTAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&sh->full[s], 1);
             mbar_init(&sh->ready[s], 2);  // one arrival per CTA of the pair
             mbar_init(&sh->empty[s], 1);
@@ -171,7 +188,7 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         fence_barrier_init();
     }
     if (warp == 1) {
-        tc::tmem_alloc_pair(&sh->tmem_base, kHTmemCols);
+        tc::tmem_alloc_pair(&sh->tmem_base, Cf::kTmemCols);
         tc::tmem_relinquish_pair();
     }
     tc::fence_before_sync();
@@ -188,40 +205,45 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             prefetch_tensormap(&tmB);
             int issued = 0;
             for (int t = 0; t < nkt; ++t) {
-                const int s = t % HSTAGES;
-                if (t >= HSTAGES && !mbar_wait(&sh->empty[s], ((t / HSTAGES) - 1) & 1, g.status)) {
+                const int s = t % S;
+                if (t >= S && !mbar_wait(&sh->empty[s], ((t / S) - 1) & 1, g.status)) {
                     *abort_flag = 1;
                     break;
                 }
                 if (*abort_flag) break;
                 const int kc = t * HBK;
-                mbar_arrive_expect_tx(&sh->full[s], kHStage);
+                mbar_arrive_expect_tx(&sh->full[s], Cf::kStage);
                 if (A_MN) {  // A stored K x M: two boxes of 64 m x 64 k
                     tma_load_2d(stA(s), &tmA, &sh->full[s], m0, kc);
                     tma_load_2d(stA(s) + 8192, &tmA, &sh->full[s], m0 + 64, kc);
                 } else {
                     tma_load_2d(stA(s), &tmA, &sh->full[s], kc, m0);
                 }
-                if (B_MN) {  // B stored K x N: two boxes of 64 n x 64 k
-                    tma_load_2d(stB(s), &tmB, &sh->full[s], nb0, kc);
-                    tma_load_2d(stB(s) + 8192, &tmB, &sh->full[s], nb0 + 64, kc);
-                } else {
-                    tma_load_2d(stB(s), &tmB, &sh->full[s], kc, nb0);
+#pragma unroll
+                for (int j = 0; j < Cf::kGroups; ++j) {
+                    const int nb = n0 + j * 256 + static_cast<int>(rank) * 128;  // this CTA's 128 columns
+                    uint8_t *dst = stB(s) + j * 16384;
+                    if (B_MN) {  // B stored K x N: two boxes of 64 n x 64 k
+                        tma_load_2d(dst, &tmB, &sh->full[s], nb, kc);
+                        tma_load_2d(dst + 8192, &tmB, &sh->full[s], nb + 64, kc);
+                    } else {
+                        tma_load_2d(dst, &tmB, &sh->full[s], kc, nb);
+                    }
                 }
                 ++issued;
             }
-            for (int t = max(0, issued - HSTAGES); t < issued; ++t)
-                mbar_wait(&sh->full[t % HSTAGES], (t / HSTAGES) & 1, g.status);
+            for (int t = max(0, issued - S); t < issued; ++t)
+                mbar_wait(&sh->full[t % S], (t / S) & 1, g.status);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && rank == 0) {
-            constexpr uint32_t idesc = idesc_f16(2 * HBM_, 2 * HBN, BF16, A_MN, B_MN);
+            constexpr uint32_t idesc = idesc_f16(2 * HBM_, 256, BF16, A_MN, B_MN);
             bool ok = true;
             for (int t = 0; t < nkt; ++t) {
-                const int s = t % HSTAGES;
-                if (!tc::mbar_wait_cluster(&sh->ready[s], (t / HSTAGES) & 1, g.status) || *abort_flag) {
+                const int s = t % S;
+                if (!tc::mbar_wait_cluster(&sh->ready[s], (t / S) & 1, g.status) || *abort_flag) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -230,8 +252,10 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const uint32_t a = smem_u32(stA(s)), b = smem_u32(stB(s));
 #pragma unroll
                 for (int kk = 0; kk < HBK / 16; ++kk)
-                    mma_f16_pair(tmem, operand_desc<A_MN>(a, kk), operand_desc<B_MN>(b, kk), idesc,
-                                 (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                    for (int j = 0; j < Cf::kGroups; ++j)
+                        mma_f16_pair(tmem + j * 256, operand_desc<A_MN>(a, kk),
+                                     operand_desc<B_MN>(b + j * 16384, kk), idesc, (t > 0 || kk > 0) ? 1u : 0u);
                 tc::commit_pair(&sh->empty[s], 0x3);
             }
             tc::commit_pair(&sh->acc_full, 0x3);
@@ -243,8 +267,8 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         if (lane == 0) {
             const uint32_t ready_even = tc::map_shared_rank(smem_u32(&sh->ready[0]), 0);
             for (int t = 0; t < nkt; ++t) {
-                const int s = t % HSTAGES;
-                if (!mbar_wait(&sh->full[s], (t / HSTAGES) & 1, g.status) || *abort_flag) {
+                const int s = t % S;
+                if (!mbar_wait(&sh->full[s], (t / S) & 1, g.status) || *abort_flag) {
                     *abort_flag = 1;
                     break;
                 }
@@ -257,7 +281,7 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         bool ok = mbar_wait(&sh->acc_full, 0, g.status) && !*abort_flag;
         if (__all_sync(0xffffffffu, ok)) {
             tc::fence_after_sync();
-            tc16_epilogue(g, tmem, warp & 3, lane, m0, n0);
+            tc16_epilogue(g, tmem, warp & 3, lane, m0, n0, NP);
         }
     }
     // ---------------------------------------------------- teardown
@@ -266,21 +290,33 @@ sgemm_tc16_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     tc::cluster_sync_all();  // the peer is done with this CTA's shared memory and barriers
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc_pair(tmem, kHTmemCols);
+        tc::tmem_dealloc_pair(tmem, Cf::kTmemCols);
     }
 }
 
 template <bool BF16, bool A_MN, bool B_MN>
 cudaError_t prepare_tc16_one() {
-    return cudaFuncSetAttribute(sgemm_tc16_pair_kernel<BF16, A_MN, B_MN>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc16);
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tc16_pair_kernel<BF16, A_MN, B_MN, 256>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Tc16Cfg<256>::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tc16_pair_kernel<BF16, A_MN, B_MN, 512>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Tc16Cfg<512>::kSmem);
 }
 
+// 256 x 512 pair tiles when N reaches 512, else 256 x 256.
 template <bool BF16, bool A_MN, bool B_MN>
-cudaError_t launch_tc16_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem,
+cudaError_t launch_tc16_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
                             cudaStream_t stream) {
-    const int tiles = ((g.M + 2 * HBM_ - 1) / (2 * HBM_)) * ((g.N + 2 * HBN - 1) / (2 * HBN));
-    sgemm_tc16_pair_kernel<BF16, A_MN, B_MN><<<2 * tiles, kHThreads, smem, stream>>>(tmA, tmB, g);
+    const int tm = (g.M + 2 * HBM_ - 1) / (2 * HBM_);
+    if (g.N >= 512) {
+        const int smem = smem_override > 0 ? smem_override : Tc16Cfg<512>::kSmem;
+        sgemm_tc16_pair_kernel<BF16, A_MN, B_MN, 512><<<2 * tm * ((g.N + 511) / 512), kHThreads, smem, stream>>>(
+            tmA, tmB, g);
+    } else {
+        const int smem = smem_override > 0 ? smem_override : Tc16Cfg<256>::kSmem;
+        sgemm_tc16_pair_kernel<BF16, A_MN, B_MN, 256><<<2 * tm * ((g.N + 255) / 256), kHThreads, smem, stream>>>(
+            tmA, tmB, g);
+    }
     return cudaGetLastError();
 }
 
@@ -299,8 +335,7 @@ cudaError_t tc16_prepare() {
 // g.transA / g.transB give the stored layouts: A stored K x M (MN-major) when
 // transA, B stored K x N (MN-major) when !transB.
 cudaError_t launch_tc16(bool bf16, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                        int smem_override, cudaStream_t stream) {
-    const int smem = smem_override > 0 ? smem_override : kSmemTc16;
+                        int smem, cudaStream_t stream) {
     const bool a_mn = g.transA != 0, b_mn = g.transB == 0;
     if (bf16) {
         if (!a_mn && !b_mn) return launch_tc16_one<true, false, false>(g, tmA, tmB, smem, stream);
