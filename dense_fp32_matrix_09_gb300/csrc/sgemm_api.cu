@@ -667,40 +667,82 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     if (C == nullptr || (reads_ab && (A == nullptr || B == nullptr))) return SGEMM_ERR_NULL;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     const size_t f = sizeof(float);
-    // Row panels: multiples of 256 rows, at most 8 (and at most 16 events).
+    // Row panels of A and C: multiples of 256 rows, at most 8.  B goes over in
+    // up to 8 column chunks (multiples of 256 columns) right after the first
+    // A panel; the first panel is computed chunk by chunk as B's chunks land,
+    // and the last panel in the same column blocks, each copied back as soon
+    // as it is done -- so only the first A panel and B chunk wait before any
+    // compute, and only the last block's copy after it.
     const int panels = std::max(1, std::min(8, M / 1024));
     const int rows = ((cdiv(M, panels) + 255) / 256) * 256;
     const int np = cdiv(M, rows);
-    if (np > 16) return SGEMM_ERR_INVALID_VALUE;
+    const int chunks = N >= 4096 ? 8 : N >= 2048 ? 4 : 1;
+    const int cols = ((cdiv(N, chunks) + 255) / 256) * 256;
+    const int nq = cdiv(N, cols);
+    if (np > 8 || nq > 8) return SGEMM_ERR_INVALID_VALUE;
+    cudaEvent_t *ev_a = h->ev_in, *ev_b = h->ev_in + 8;  // A (and C) panel p landed; B chunk q landed
+    // output piece computed: the 16 events are used in turn (a stream wait
+    // binds to an event's record at the time of the wait call, so an event can
+    // be recorded again once the copy stream's wait on it is enqueued)
+    int n_out = 0;
+    auto ev_c = [&]() { return h->ev_out[n_out++ % 16]; };
 
     auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-    // nothing of this call starts before the caller's earlier work on `stream`
-    if (!ok(cudaEventRecord(h->ev_start, stream)) || !ok(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0)) ||
-        !ok(cudaStreamWaitEvent(h->copy_out, h->ev_start, 0)))
-        return SGEMM_ERR_CUDA;
-    // B first: every panel needs all of it (the copy stream is in order, so
-    // panel 0's event also covers B)
-    if (reads_ab && !ok(cudaMemcpy2DAsync(dB, ldb * f, B, ldb * f, N * f, K, cudaMemcpyHostToDevice, h->copy_in)))
-        return SGEMM_ERR_CUDA;
-    for (int p = 0; p < np; ++p) {
+    auto copy_in_panel = [&](int p) {  // A panel p (and C panel p when beta != 0)
         const int r0 = p * rows, nr = std::min(rows, M - r0);
         if (reads_ab && !ok(cudaMemcpy2DAsync(dA + static_cast<size_t>(r0) * lda, lda * f,
                                               A + static_cast<size_t>(r0) * lda, lda * f, K * f, nr,
                                               cudaMemcpyHostToDevice, h->copy_in)))
-            return SGEMM_ERR_CUDA;
+            return false;
         if (beta != 0.f && !ok(cudaMemcpy2DAsync(dC + static_cast<size_t>(r0) * ldc, ldc * f,
                                                  C + static_cast<size_t>(r0) * ldc, ldc * f, N * f, nr,
                                                  cudaMemcpyHostToDevice, h->copy_in)))
+            return false;
+        return ok(cudaEventRecord(ev_a[p], h->copy_in));
+    };
+    // GEMM of rows [r0, r0+nr) x columns [c0, c0+nc) on `stream`, then its copy back after event `ev`
+    auto block = [&](int r0, int nr, int c0, int nc, cudaEvent_t ev) {
+        const int st2 = sgemm_run(h, nr, nc, K, alpha, dA + static_cast<size_t>(r0) * lda, lda, dB + c0, ldb, beta,
+                                  dC + static_cast<size_t>(r0) * ldc + c0, ldc, stream_);
+        if (st2 != SGEMM_OK) return st2;
+        if (!ok(cudaEventRecord(ev, stream)) || !ok(cudaStreamWaitEvent(h->copy_out, ev, 0)) ||
+            !ok(cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc + c0, ldc * f,
+                                  dC + static_cast<size_t>(r0) * ldc + c0, ldc * f, nc * f, nr,
+                                  cudaMemcpyDeviceToHost, h->copy_out)))
+            return static_cast<int>(SGEMM_ERR_CUDA);
+        return static_cast<int>(SGEMM_OK);
+    };
+    // nothing of this call starts before the caller's earlier work on `stream`
+    if (!ok(cudaEventRecord(h->ev_start, stream)) || !ok(cudaStreamWaitEvent(h->copy_in, h->ev_start, 0)) ||
+        !ok(cudaStreamWaitEvent(h->copy_out, h->ev_start, 0)))
+        return SGEMM_ERR_CUDA;
+    // copy stream: A panel 0, the B chunks, then the other panels (in order)
+    if (!copy_in_panel(0)) return SGEMM_ERR_CUDA;
+    for (int q = 0; q < nq; ++q) {
+        const int c0 = q * cols, nc = std::min(cols, N - c0);
+        if (reads_ab && !ok(cudaMemcpy2DAsync(dB + c0, ldb * f, B + c0, ldb * f, nc * f, K,
+                                              cudaMemcpyHostToDevice, h->copy_in)))
             return SGEMM_ERR_CUDA;
-        if (!ok(cudaEventRecord(h->ev_in[p], h->copy_in)) || !ok(cudaStreamWaitEvent(stream, h->ev_in[p], 0)))
-            return SGEMM_ERR_CUDA;
-        st = sgemm_run(h, nr, N, K, alpha, dA + static_cast<size_t>(r0) * lda, lda, dB, ldb, beta,
-                       dC + static_cast<size_t>(r0) * ldc, ldc, stream_);
-        if (st != SGEMM_OK) return st;
-        if (!ok(cudaEventRecord(h->ev_out[p], stream)) || !ok(cudaStreamWaitEvent(h->copy_out, h->ev_out[p], 0)) ||
-            !ok(cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc, ldc * f, dC + static_cast<size_t>(r0) * ldc,
-                                  ldc * f, N * f, nr, cudaMemcpyDeviceToHost, h->copy_out)))
-            return SGEMM_ERR_CUDA;
+        if (!ok(cudaEventRecord(ev_b[q], h->copy_in))) return SGEMM_ERR_CUDA;
+    }
+    for (int p = 1; p < np; ++p)
+        if (!copy_in_panel(p)) return SGEMM_ERR_CUDA;
+    // compute stream
+    for (int p = 0; p < np; ++p) {
+        const int r0 = p * rows, nr = std::min(rows, M - r0);
+        if (!ok(cudaStreamWaitEvent(stream, ev_a[p], 0))) return SGEMM_ERR_CUDA;
+        if (p == 0 || p == np - 1) {  // column blocks: the first panel follows B's chunks
+            for (int q = 0; q < nq; ++q) {
+                const int c0 = q * cols, nc = std::min(cols, N - c0);
+                if (!ok(cudaStreamWaitEvent(stream, ev_b[q], 0))) return SGEMM_ERR_CUDA;
+                st = block(r0, nr, c0, nc, ev_c());
+                if (st != SGEMM_OK) return st;
+            }
+        } else {
+            if (!ok(cudaStreamWaitEvent(stream, ev_b[nq - 1], 0))) return SGEMM_ERR_CUDA;
+            st = block(r0, nr, 0, N, ev_c());
+            if (st != SGEMM_OK) return st;
+        }
     }
     // the caller's stream reaches this point only when every panel is back on the host
     if (!ok(cudaEventRecord(h->ev_done, h->copy_out)) || !ok(cudaStreamWaitEvent(stream, h->ev_done, 0)))

@@ -178,12 +178,14 @@ int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, in
 
 /* C <- alpha*A*B + beta*C with A, B, C in HOST memory, transfers overlapped
  * with compute.  dA, dB, dC are caller-owned DEVICE buffers of the same
- * shapes and leading dimensions (M*lda, K*ldb, M*ldc floats at least); the
- * library copies B to dB, then A (and C when beta != 0) in row panels to dA
- * (dC) on one handle-owned copy stream, runs each panel's GEMM on `stream` as
- * soon as its rows have landed (the same kernels and rules as sgemm_run), and
- * copies each finished panel of dC back to C on a second copy stream while the
- * next panel computes.  Returns after enqueueing; C is complete when `stream`
+ * shapes and leading dimensions (M*lda, K*ldb, M*ldc floats at least).  On a
+ * handle-owned copy stream the library copies the first row panel of A (and
+ * of C when beta != 0), then B in up to 8 column chunks, then the other row
+ * panels; on `stream` it runs each piece of the GEMM (the same kernels and
+ * rules as sgemm_run) as soon as its operands have landed -- the first row
+ * panel chunk by chunk as B's chunks arrive -- and on a second copy stream it
+ * copies each finished panel (the last one block by block) back to C while
+ * the rest computes.  Returns after enqueueing; C is complete when `stream`
  * reaches the point of the call (e.g. after cudaStreamSynchronize(stream)).
  * Page-locked host buffers give asynchronous copies; pageable ones work but
  * serialise.  The host and device windows must not be touched until then.

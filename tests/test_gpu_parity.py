@@ -371,7 +371,13 @@ def test_math_mode_rejects_unknown(handle):
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 @pytest.mark.parametrize("cfg", [inputs.CONFIGS[3],
                                  inputs.GemmConfig("host_3000x520x300", 3000, 520, 300, 304, 524, 528, 41, 1.5, 0.5),
-                                 inputs.GemmConfig("host_2048x256x64_b0", 2048, 256, 64, 64, 256, 256, 42, 1.0, 0.0)],
+                                 inputs.GemmConfig("host_2048x256x64_b0", 2048, 256, 64, 64, 256, 256, 42, 1.0, 0.0),
+                                 # 2 row panels, B in 8 column chunks of 768 (the last 132 wide)
+                                 inputs.GemmConfig("host_2500x4500x300", 2500, 4500, 300, 304, 4504, 4508, 43,
+                                                   0.5, -1.0),
+                                 # 1 row panel (first and last), B in 4 chunks
+                                 inputs.GemmConfig("host_1200x2100x200_b0", 1200, 2100, 200, 200, 2100, 2104, 44,
+                                                   1.0, 0.0)],
                          ids=lambda c: c.name)
 def test_run_host_buffers(handle, cfg, pinned):
     """sgemm_run_host: host A, B, C; device staging buffers; copies overlap the
