@@ -546,6 +546,22 @@ def main():
         roofline["frac_at_measured_clock"] = achieved / (2 * 128 * sms * clocks["sm_mhz"] * 1e6 / 1e12)
     roofline["algorithmic_flops_per_launch"] = cfg.flops
     roofline["kernel_source_sha256_16"] = src_hash
+    # the FP32 FMA rate with no memory traffic (the library's FMA probe), as a second reference
+    sink = torch.empty(4 * sms * 256, device="cuda")
+    fma_ms = []
+    for i in range(8):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        probe_flops = sg.sgemm_debug_fma_probe(h, sink, iters=16384, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            fma_ms.append(e0.elapsed_time(e1))
+    fma_tflops = probe_flops / (statistics.median(fma_ms) * 1e-3) / 1e12
+    roofline["fma_microbench"] = {"tflops": fma_tflops, "frac": achieved / fma_tflops,
+                                  "what": "sgemm_debug_fma_probe: 4 CTAs of 256 threads per SM, 16 independent "
+                                          "packed FP32x2 FMA chains per thread, registers only"}
+    del sink
     if variant in (sg.VARIANT_TC_3XTF32, sg.VARIANT_TC_3XTF32_PAIR):
         # a pinned tensor-core variant: its roofline is the tensor pipe's
         bf16 = measured_bf16_tflops()
@@ -636,6 +652,22 @@ def main():
         out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                                "sample": f"{rows} of {cfg.M} output rows (x {cfg.N} columns, K = {cfg.K}) "
                                          f"in {dt:.1f} s, FP64 accumulation"}
+        # the oracle on every workload (all host cores, about a second each), and on one
+        # core for the two smallest
+        import oracle
+        per = {}
+        for w in inputs.CONFIGS:
+            wp = prob if w.name == cfg.name else inputs.make_problem(w)
+            r, n_rows, t, c = cpu_oracle_rate(w, wp, seconds=1.0)
+            per[w.name] = {"gflops": r * 1e3, "cores": c, "rows": n_rows, "seconds": t}
+            if w.M * w.N * w.K <= 1024 ** 3:
+                oracle.set_num_threads(1)
+                try:
+                    r1, n1, t1, _ = cpu_oracle_rate(w, wp, seconds=1.0)
+                finally:
+                    oracle.set_num_threads(c)
+                per[w.name]["gflops_1_thread"] = r1 * 1e3
+        out["cpu_baseline"]["workloads"] = per
     sg.sgemm_destroy(h)
     if rank == 0:
         print(json.dumps(out))

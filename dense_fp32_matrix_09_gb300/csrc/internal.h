@@ -103,5 +103,9 @@ cudaError_t launch_tc16(bool bf16, const GemmArgs &g, const CUtensorMap &tmA, co
                         int smem_override, cudaStream_t stream);
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);
 cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);
+// Returns the FLOP the launch performs (-1 on a launch error); sink: ctas * 256 floats.
+long long launch_fma_probe(float *sink, int ctas, int iters, cudaStream_t stream);
+// sink: ctas * 32 floats.
+cudaError_t launch_bank_probe(float *sink, int padded, int ctas, int iters, cudaStream_t stream);
 
 }  // namespace sg

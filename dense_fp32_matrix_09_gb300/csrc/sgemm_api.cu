@@ -773,4 +773,27 @@ int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream
     return from_cuda(sg::launch_timeout_probe(h->d_status, limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
+int sgemm_debug_fma_probe(sgemm_handle_t h, int ctas, int iters, float *sink, long long *flops, void *stream) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    if (sink == nullptr) return SGEMM_ERR_NULL;
+    if (ctas == 0) ctas = 4 * h->num_sms;
+    if (ctas < 0 || iters < 1) return SGEMM_ERR_INVALID_VALUE;
+    const long long f = sg::launch_fma_probe(sink, ctas, iters, static_cast<cudaStream_t>(stream));
+    if (f < 0) return SGEMM_ERR_LAUNCH;
+    if (flops) *flops = f;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_bank_probe(sgemm_handle_t h, int padded, int ctas, int iters, float *sink, void *stream) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    if (sink == nullptr) return SGEMM_ERR_NULL;
+    if (ctas == 0) ctas = h->num_sms;
+    if (ctas < 0 || iters < 1) return SGEMM_ERR_INVALID_VALUE;
+    return from_cuda(sg::launch_bank_probe(sink, padded != 0, ctas, iters, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -14,6 +14,9 @@
 //    into the sgemmNN algorithm", write-back section).
 //  * sgemm_scale_kernel -- the alpha == 0 or K == 0 quick path: C = beta*C,
 //    or C = 0 without reading C when beta == 0 (BLAS convention).
+//  * fma_probe_kernel, bank_probe_kernel -- measurement probes: the FP32 FMA
+//    rate with no memory traffic, and a shared-memory access with and
+//    without bank conflicts (a control for the profiler's counters);
 //  * timeout_probe_kernel -- waits on an mbarrier that nothing completes,
 //    gives up after a short limit and records the timeout, to test the
 //    device-side timeout reporting without faulting or hanging the GPU.
@@ -131,6 +134,52 @@ __global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
     }
 }
 
+// FP32 FMA throughput probe: every thread runs kFmaChains independent chains
+// of packed FP32x2 FMAs (acc = a*acc + b) in registers, `iters` times, and
+// writes one sum (so nothing is dead code).  No memory traffic in the loop:
+// the FMA rate the GEMM main loop is compared against.
+constexpr int kFmaChains = 16, kFmaThreads = 256;
+
+__global__ void __launch_bounds__(kFmaThreads) fma_probe_kernel(float *sink, int iters) {
+    const int t = blockIdx.x * blockDim.x + threadIdx.x;
+    const float2 a = make_float2(0.999f + 1e-7f * (t & 7), 0.999f);
+    const float2 b = make_float2(1e-3f, 1e-3f + 1e-9f * (t & 3));
+    float2 acc[kFmaChains];
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c) acc[c] = make_float2(0.01f * c, 0.02f * c + 1e-6f * t);
+#pragma unroll 1
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+            for (int c = 0; c < kFmaChains; ++c) acc[c] = __ffma2_rn(a, acc[c], b);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kFmaChains; ++c) s += acc[c].x + acc[c].y;
+    sink[t] = s;
+}
+
+// Shared-memory bank probe (the transposed-operand access of a 32 x 32 tile):
+// lane l reads Bs[l][k] for k = 0..31.  With row stride 32 floats every lane
+// of a warp hits the same bank (a 32-way conflict per load); padding the rows
+// to 33 floats puts the lanes in 32 distinct banks.  A negative control for
+// the bank-conflict counters, not part of any GEMM.
+template <int PAD>
+__global__ void __launch_bounds__(32) bank_probe_kernel(float *sink, int iters) {
+    __shared__ float Bs[32][32 + PAD];
+    const int l = threadIdx.x;
+    for (int r = 0; r < 32; ++r) Bs[r][l] = 0.001f * (r * 32 + l);
+    __syncwarp();
+    float acc = 0.f;
+#pragma unroll 1
+    for (int i = 0; i < iters; ++i) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc += *reinterpret_cast<volatile float *>(&Bs[l][k]);
+    }
+    sink[blockIdx.x * 32 + l] = acc;
+}
+
 __global__ void timeout_probe_kernel(int *status, long long limit_ns) {
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
@@ -157,6 +206,19 @@ cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
     const int gy = min(g.M, 8192);
     const int gz = min(g.batch, max(1, 65535 / gy));
     sgemm_scale_kernel<<<dim3(gx, gy, gz), 256, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+long long launch_fma_probe(float *sink, int ctas, int iters, cudaStream_t stream) {
+    fma_probe_kernel<<<ctas, kFmaThreads, 0, stream>>>(sink, iters);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    // FLOP: 2 per FMA, 2 FMAs per packed instruction
+    return 4LL * kFmaChains * 8 * iters * static_cast<long long>(ctas) * kFmaThreads;
+}
+
+cudaError_t launch_bank_probe(float *sink, int padded, int ctas, int iters, cudaStream_t stream) {
+    if (padded) bank_probe_kernel<1><<<ctas, 32, 0, stream>>>(sink, iters);
+    else bank_probe_kernel<0><<<ctas, 32, 0, stream>>>(sink, iters);
     return cudaGetLastError();
 }
 

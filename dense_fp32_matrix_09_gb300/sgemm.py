@@ -50,7 +50,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
-           "sgemm_check_args_mixed")
+           "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe")
 
 
 class SgemmError(RuntimeError):
@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.sgemm_set_variant.argtypes = [vp, i32]
         L.sgemm_last_variant.argtypes = [vp, ctypes.POINTER(i32)]
         L.sgemm_last_launches.argtypes = [vp]
+        L.sgemm_debug_fma_probe.argtypes = [vp, i32, i32, vp, ctypes.POINTER(ctypes.c_longlong), vp]
+        L.sgemm_debug_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
         L.sgemm_run_mixed.argtypes = [vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         L.sgemm_check_args_mixed.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32]
         L.sgemm_get_device_status.argtypes = [vp]
@@ -222,6 +224,21 @@ def sgemm_check_args_mixed(in_type, transA, transB, M, N, K, alpha, A, lda, B, l
     return lib().sgemm_check_args_mixed(int(in_type), int(transA), int(transB), int(M), int(N), int(K),
                                         float(alpha), _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C),
                                         int(ldc))
+
+
+def sgemm_debug_fma_probe(h, sink, ctas=0, iters=4096, stream=None) -> int:
+    """Enqueue the FP32 FMA-rate probe (sink: ctas*256 floats on the device);
+    returns the FLOP it performs."""
+    flops = ctypes.c_longlong(0)
+    _check(lib().sgemm_debug_fma_probe(h, int(ctas), int(iters), _ptr(sink), ctypes.byref(flops), _stream(stream)),
+           "sgemm_debug_fma_probe")
+    return flops.value
+
+
+def sgemm_debug_bank_probe(h, padded, sink, ctas=0, iters=64, stream=None) -> None:
+    """Enqueue the shared-memory bank probe (sink: ctas*32 floats on the device)."""
+    _check(lib().sgemm_debug_bank_probe(h, int(padded), int(ctas), int(iters), _ptr(sink), _stream(stream)),
+           "sgemm_debug_bank_probe")
 
 
 def sgemm_last_launches(h) -> int:

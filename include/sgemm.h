@@ -242,6 +242,26 @@ int sgemm_get_device_status(sgemm_handle_t h);
  * It exercises the timeout path without faulting or hanging the GPU. */
 int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream);
 
+/* Measurement probe: enqueue `ctas` CTAs (0 = 4 per SM) of 256 threads, each
+ * thread running 16 independent chains of packed FP32x2 FMAs for 8*iters
+ * steps in registers (no memory traffic) and writing one sum to
+ * sink[thread] (device memory of ctas*256 floats, caller-owned), and set
+ * *flops (if non-NULL) to the FLOP the launch performs.  Timed with events
+ * it gives the FP32 FMA rate the GEMM main loop is compared with.
+ * SGEMM_ERR_NULL for a NULL sink; SGEMM_ERR_INVALID_VALUE if ctas < 0 or
+ * iters < 1. */
+int sgemm_debug_fma_probe(sgemm_handle_t h, int ctas, int iters, float *sink, long long *flops, void *stream);
+
+/* Measurement probe: `ctas` one-warp CTAs (0 = one per SM) each fill a 32 x 32
+ * FP32 tile in shared memory with 0.001*(32*row + column) and read it
+ * column-wise (lane l reads row l, k = 0..31) `iters` times -- the
+ * transposed-operand access of page m.lqnn.cn/news/94381, section 4.2 -- with
+ * a row stride of 32 floats (padded = 0: all 32 lanes in one bank, a 32-way
+ * conflict per load) or 33 (padded = 1, the page's padding: 32 distinct
+ * banks); lane l of CTA c writes its sum to sink[32*c + l] (ctas*32 floats,
+ * caller-owned).  A control for the profiler's bank-conflict counters. */
+int sgemm_debug_bank_probe(sgemm_handle_t h, int padded, int ctas, int iters, float *sink, void *stream);
+
 /* Test hook: when `bytes` > 0, later launches of the handle's TMA variants
  * request `bytes` of dynamic shared memory instead of their own size, so a
  * value above the device limit makes the launch fail on the host
