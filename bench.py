@@ -418,7 +418,7 @@ def main():
     import numpy as np
     import torch
     import torch.distributed as dist
-    from dense_fp32_matrix_09_gb300 import build, sgemm as sg
+    from dense_fp32_matrix_09_gb300 import build, replicas, sgemm as sg
 
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -480,13 +480,9 @@ def main():
     barrier()
     clocks = sampler.stop()
     launch_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    total_ms = sum(launch_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = replicas.slowest(sum(launch_ms), dist if world > 1 else None, "cuda")
     ms_step = total_ms / args.steps
-    value = cfg.flops * world / (ms_step * 1e-3) / 1e12
+    value = replicas.job_tflops(cfg.flops, ms_step, world)
     variant, splits = sg.sgemm_last_variant(h)
     launches_per_step = sg.sgemm_last_launches(h)
     status = sg.sgemm_get_device_status(h)
@@ -522,12 +518,8 @@ def main():
     e.record(stream)
     e.synchronize()
     barrier()
-    e2e_ms = s.elapsed_time(e) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = cfg.flops * world / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = replicas.slowest(s.elapsed_time(e) / args.e2e_steps, dist if world > 1 else None, "cuda")
+    e2e_value = replicas.job_tflops(cfg.flops, e2e_ms, world)
 
     # ---- roofline of the dominant kernel (the only kernel of a step)
     props = torch.cuda.get_device_properties(local)
