@@ -190,7 +190,12 @@ int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, in
  * Page-locked host buffers give asynchronous copies; pageable ones work but
  * serialise.  The host and device windows must not be touched until then.
  * Same argument checks as sgemm_run (on the device pointers; SGEMM_ERR_NULL
- * also if a host pointer that is read or written is NULL).  No allocation. */
+ * also if a host pointer that is read or written is NULL), made before
+ * anything is enqueued.  A CUDA error while enqueueing (after the checks)
+ * returns SGEMM_ERR_CUDA with part of the copies and GEMMs possibly already
+ * enqueued; synchronize `stream` before reusing the buffers.  The handle's
+ * copy streams and events serve one call at a time: calls of the same handle
+ * from several host threads must be serialised.  No allocation. */
 int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha,
                    const float *A, int lda, const float *B, int ldb,
                    float beta, float *C, int ldc,
