@@ -276,6 +276,25 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
         e.record(stream)
         e.synchronize()
         hot = s.elapsed_time(e) / n
+    # launch-bound shapes: 20 calls captured in one CUDA graph, replayed (beta == 0 only)
+    graph_ms = None
+    if cfg.beta == 0 and cfg.flops <= 2 * 1024 ** 3:
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=gs):
+            for _ in range(20):
+                sg.sgemm_run(h, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, B, cfg.ldb, cfg.beta, C, cfg.ldc, gs)
+        graph.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(5):
+            graph.replay()
+        e.record(stream)
+        e.synchronize()
+        graph_ms = s.elapsed_time(e) / 100
+        del graph
     variant, splits = sg.sgemm_last_variant(h)
     med = statistics.median(ms)
     out = {"ms_median": med, "ms_min": min(ms), "tflops": cfg.flops / (med * 1e-3) / 1e12,
@@ -286,6 +305,9 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
     if hot is not None:
         out["ms_back_to_back"] = hot
         out["tflops_back_to_back"] = cfg.flops / (hot * 1e-3) / 1e12
+    if graph_ms is not None:
+        out["ms_per_call_in_cuda_graph"] = graph_ms
+        out["tflops_in_cuda_graph"] = cfg.flops / (graph_ms * 1e-3) / 1e12
     del A, B, C, C0
     return out
 
