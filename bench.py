@@ -41,13 +41,26 @@ UNIT = "TFLOP/s"
 # any other source gives traffic = null (profiles/sgemm_8192cube_dram.md).
 # The SIMT step is two launches of the same kernel template (13 complete
 # waves of whole tiles: 2.988 GB; the stream-K last wave: 0.493 GB).
-TRAFFIC_BY_SOURCE = {"97d6521bf15e27bb": 3.481e9}
+# DRAM bytes of one headline call (8192^3) by (SIMT kernel source hash,
+# layout the kernel ran on, re-layout bits), from one-pass ncu captures
+TRAFFIC_BY_SOURCE = {("97d6521bf15e27bb", "NN", 0): 3.481e9}
 TC_TRAFFIC_BY_SOURCE = {"1a7b6ea63a862088": 2.534e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
 TC_KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tc.cu",
                      "dense_fp32_matrix_09_gb300/csrc/tcgen05.cuh",
                      "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
+
+
+RELAYOUT_NAMES = {0: "none", 1: "A", 2: "B", 3: "A+B"}
+
+
+def layout_run(op: str, relayout: int) -> str:
+    """Operand layout the GEMM kernel ran on after re-layout (bit 0: A was
+    copied transposed, bit 1: B)."""
+    ta = (op[0] == "T") ^ bool(relayout & 1)
+    tb = (op[1] == "T") ^ bool(relayout & 2)
+    return ("T" if ta else "N") + ("T" if tb else "N")
 
 
 def kernel_source_hash(files=KERNEL_SOURCES) -> str:
@@ -299,7 +312,8 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
     med = statistics.median(ms)
     out = {"ms_median": med, "ms_min": min(ms), "tflops": cfg.flops / (med * 1e-3) / 1e12,
            "gbs_compulsory": cfg.compulsory_bytes / (med * 1e-3) / 1e9, "reps": reps,
-           "l2": "flushed before each rep" if cold else "warm", "variant": sg.variant_name(variant)}
+           "l2": "flushed before each rep" if cold else "warm", "variant": sg.variant_name(variant),
+           "relayout": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)]}
     if splits > 1:
         out["splits"] = splits
     if hot is not None:
@@ -335,13 +349,28 @@ def bench_ex(torch, sg, h, cfg, A, B, C, stream, warmup: int) -> dict:
     n = cfg.M
     flops = 2.0 * n * n * n
     res = {}
+    # each layout as the library runs it (operand re-layout on), then on the
+    # operands as stored (re-layout off), for the layouts re-layout applies to
     for name, ta, tb in (("NN", 0, 0), ("NT", 0, 1), ("TN", 1, 0), ("TT", 1, 1)):
         def call(ta=ta, tb=tb):
             sg.sgemm_run_ex(h, ta, tb, n, n, n, 1.0, A, n, 0, B, n, 0, 0.0, C, n, 0, 1, stream)
-        ms = time_calls(torch, stream, call, 10, warmup)
-        v, splits = sg.sgemm_last_variant(h)
-        med = statistics.median(ms)
-        res[name] = {"ms_median": med, "tflops": flops / (med * 1e-3) / 1e12, "variant": sg.variant_name(v)}
+        for mode, key in ((sg.RELAYOUT_AUTO, name), (sg.RELAYOUT_OFF, name + "_as_stored")):
+            sg.sgemm_set_relayout(h, mode)
+            ms = time_calls(torch, stream, call, 10, warmup)
+            v, splits = sg.sgemm_last_variant(h)
+            med = statistics.median(ms)
+            res[key] = {"ms_median": med, "tflops": flops / (med * 1e-3) / 1e12, "variant": sg.variant_name(v),
+                        "relayout": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)],
+                        "launches": sg.sgemm_last_launches(h)}
+            if name == "TN":
+                break  # TN is never re-laid out
+    sg.sgemm_set_relayout(h, sg.RELAYOUT_AUTO)
+    # the transposed copy of A: the NN call minus the TN call on the same
+    # buffers (the same kernel on i.i.d. data of the same shape)
+    if res["NN"]["relayout"] == "A":
+        t_copy = res["NN"]["ms_median"] - res["TN"]["ms_median"]
+        res["transpose_A_ms_est"] = t_copy
+        res["transpose_A_gbs_est"] = 8.0 * n * n / (t_copy * 1e-3) / 1e9 if t_copy > 0 else None
     # strided batch: 1024 x (64 x 64) x (64 x 64), contiguous; 48 MiB < L2, so L2 is flushed before each call
     bs, m = 1024, 64
     g = torch.Generator(device="cpu").manual_seed(3)
@@ -507,6 +536,8 @@ def main():
     value = replicas.job_tflops(cfg.flops, ms_step, world)
     variant, splits = sg.sgemm_last_variant(h)
     launches_per_step = sg.sgemm_last_launches(h)
+    relayout = sg.sgemm_last_relayout(h)
+    kernel_layout = layout_run(args.op, relayout)
     status = sg.sgemm_get_device_status(h)
     if status != sg.OK:
         raise SystemExit(f"device status after the timed region: {sg.status_string(status)}")
@@ -552,9 +583,14 @@ def main():
     src_hash = kernel_source_hash()
     roofline = {
         "bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-        "traffic": TRAFFIC_BY_SOURCE.get(src_hash) if cfg.name == inputs.HEADLINE.name else None,
-        "kernel": f"sgemm_tma_kernel ({sg.variant_name(variant)})",
+        "traffic": (TRAFFIC_BY_SOURCE.get((src_hash, kernel_layout, relayout))
+                    if cfg.name == inputs.HEADLINE.name else None),
+        "kernel": f"sgemm_tma_kernel ({sg.variant_name(variant)}, {kernel_layout} layout)",
         "peak_basis": f"FP32 FFMA: 2 FLOP x 128 lanes x {sms} SMs x {max_mhz:.0f} MHz (max SM clock)",
+        "achieved_basis": ("CUDA events around each sgemm_run call: "
+                           + (f"the transposed copy of {RELAYOUT_NAMES[relayout]} (one HBM-bound launch) and "
+                              if relayout else "") + f"the GEMM's {launches_per_step - bin(relayout).count('1')} "
+                           "launch(es); traffic is the DRAM bytes of the same launches"),
     }
     if clocks.get("sm_mhz"):
         roofline["frac_at_measured_clock"] = achieved / (2 * 128 * sms * clocks["sm_mhz"] * 1e6 / 1e12)
@@ -596,6 +632,7 @@ def main():
                    "inputs": "i.i.d. U[-1,1) float32",
                    "l2": "inputs larger than L2 (working set %d MiB)" % ((prob.A.nbytes + prob.B.nbytes + prob.C0.nbytes) >> 20),
                    "variant": sg.variant_name(variant), "splits": splits, "op": args.op,
+                   "relayout": RELAYOUT_NAMES[relayout], "kernel_layout": kernel_layout,
                    "launches_per_step": launches_per_step,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -33,6 +33,10 @@ struct sgemm_ctx {
     int smem_override;
     int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
     int math_mode;                          // sgemm_math_mode_t
+    float *d_rl;                            // operand re-layout workspace (NULL if not allocated)
+    size_t rl_floats;
+    int relayout_mode;                      // sgemm_relayout_t
+    int last_relayout;                      // operands the last call transposed (bit 0 A, bit 1 B)
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
     cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
@@ -42,6 +46,7 @@ namespace {
 
 constexpr size_t kWorkspaceBytes = size_t(48) << 20;  // stream-K partial tiles
 constexpr int kCounters = 16384;                      // stream-K output tiles per call
+constexpr size_t kRelayoutBytes = size_t(512) << 20;  // transposed operands (8192 x 8192 A and B)
 
 std::mutex g_mu;
 std::unordered_set<sgemm_ctx *> g_live;
@@ -247,6 +252,77 @@ int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int o
     return best;
 }
 
+// Estimated time of transposing a rows x cols FP32 operand (a read and a
+// write of every element at about 5.5 TB/s, plus the launch and its
+// ordering gap), in microseconds.
+double transpose_cost(int rows, int cols) { return 6.0 + 8.0 * rows * static_cast<double>(cols) / 5.5e6; }
+
+inline int round32(int x) { return (x + 31) / 32 * 32; }
+
+// Plan of an FP32 SIMT call: the kernel variant and which operands are first
+// transposed into the re-layout workspace (bit 0: A, bit 1: B).
+struct Fp32Plan {
+    int variant;
+    int relayout;
+};
+
+// Operand layouts after re-layout `r` of a (transA, transB) call: the
+// transposed copy of A (stored M x K) is stored K x M, that of B (stored
+// N x K) K x N.  Returns the kernel layout, and the M, N the kernel sees
+// (A^T B^T runs on swapped operands).
+int op_after(int transA, int transB, int r, int M, int N, int *kM, int *kN) {
+    const int ta = transA ^ (r & 1), tb = transB ^ ((r >> 1) & 1);
+    *kM = ta && tb ? N : M;
+    *kN = ta && tb ? M : N;
+    return ta ? (tb ? sg::kTmaOpNN : sg::kTmaOpTN) : (tb ? sg::kTmaOpNT : sg::kTmaOpNN);
+}
+
+// Variant and re-layout for a TMA-eligible FP32 call with batch 1 (a pinned
+// TMA variant keeps its tile).  Candidates: the operands as stored, and each
+// combination of transposed copies of A stored M x K and of B stored N x K;
+// the one that reaches the TN layout -- the fastest main loop on GB300 -- is
+// NN: A; NT: A and B; A^T B^T: B.  Each candidate costs variant_cost of its
+// layout plus transpose_cost of each copy, and needs its copies to fit in the
+// workspace; a re-layout must save 1 %.  SGEMM_RELAYOUT_ALWAYS takes the TN
+// candidate whenever it fits; SGEMM_RELAYOUT_OFF only the stored layout.
+Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int pinned) {
+    auto best_variant = [&](int op, int kM, int kN, double *cost) {
+        if (pinned != SGEMM_VARIANT_AUTO) {
+            sg::SplitK plan;
+            *cost = variant_cost(h, pinned, kM, kN, K, 1, op, &plan);
+            return pinned;
+        }
+        int v = choose_variant(h, kM, kN, K, 1, op);
+        sg::SplitK plan;
+        *cost = variant_cost(h, v, kM, kN, K, 1, op, &plan);
+        return v;
+    };
+    int kM, kN;
+    double best_cost;
+    Fp32Plan best{best_variant(op_after(transA, transB, 0, M, N, &kM, &kN), kM, kN, &best_cost), 0};
+    if (h->relayout_mode == SGEMM_RELAYOUT_OFF || h->d_rl == nullptr) return best;
+    const int tn_r = (transA ? 0 : 1) | (transB ? 2 : 0);  // transposes that reach TN
+    for (int r : {1, 2, 3}) {
+        if ((r & 1) && transA) continue;  // only A stored M x K and B stored N x K are transposed
+        if ((r & 2) && !transB) continue;
+        const bool to_tn = r == tn_r;
+        if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS && !to_tn) continue;
+        const size_t need = ((r & 1) ? static_cast<size_t>(K) * round32(M) : 0) +
+                            ((r & 2) ? static_cast<size_t>(K) * round32(N) : 0);
+        if (need > h->rl_floats) continue;
+        double c;
+        const int v = best_variant(op_after(transA, transB, r, M, N, &kM, &kN), kM, kN, &c);
+        if (r & 1) c += transpose_cost(M, K);
+        if (r & 2) c += transpose_cost(N, K);
+        if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || c < best_cost * 0.99) {
+            best_cost = c;
+            best = Fp32Plan{v, r};
+            if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS) break;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 extern "C" {
@@ -372,6 +448,13 @@ int sgemm_create(sgemm_handle_t *out) {
         cudaGetLastError();
         return SGEMM_ERR_CUDA;
     }
+    // the re-layout workspace is optional: without it operands stay as stored
+    if (cudaMalloc(&h->d_rl, kRelayoutBytes) == cudaSuccess) {
+        h->rl_floats = kRelayoutBytes / sizeof(float);
+    } else {
+        h->d_rl = nullptr;
+        cudaGetLastError();
+    }
     bool ev_ok = cudaStreamCreateWithFlags(&h->copy_in, cudaStreamNonBlocking) == cudaSuccess &&
                  cudaStreamCreateWithFlags(&h->copy_out, cudaStreamNonBlocking) == cudaSuccess;
     for (cudaEvent_t *e : {&h->ev_start, &h->ev_done})
@@ -393,6 +476,7 @@ int sgemm_create(sgemm_handle_t *out) {
         cudaFree(h->d_status);
         cudaFree(h->d_ws);
         cudaFree(h->d_counters);
+        cudaFree(h->d_rl);
         delete h;
         return SGEMM_ERR_CUDA;
     }
@@ -423,6 +507,7 @@ int sgemm_destroy(sgemm_handle_t h) {
     cudaFree(h->d_status);
     cudaFree(h->d_ws);
     cudaFree(h->d_counters);
+    cudaFree(h->d_rl);
     if (prev != h->device) cudaSetDevice(prev);
     delete h;
     return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
@@ -447,6 +532,24 @@ int sgemm_last_variant(sgemm_handle_t h, int *splits) {
     if (!alive(h)) return -1;
     if (splits) *splits = h->last_splits;
     return h->last_variant;
+}
+
+int sgemm_set_relayout(sgemm_handle_t h, int mode) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (mode != SGEMM_RELAYOUT_AUTO && mode != SGEMM_RELAYOUT_OFF && mode != SGEMM_RELAYOUT_ALWAYS)
+        return SGEMM_ERR_INVALID_VALUE;
+    h->relayout_mode = mode;
+    return SGEMM_OK;
+}
+
+int sgemm_last_relayout(sgemm_handle_t h) {
+    if (!alive(h)) return -1;
+    return h->last_relayout;
+}
+
+int64_t sgemm_relayout_capacity(sgemm_handle_t h) {
+    if (!alive(h)) return -1;
+    return static_cast<int64_t>(h->rl_floats);
 }
 
 int sgemm_last_launches(sgemm_handle_t h) {
@@ -478,6 +581,7 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     h->last_variant = -1;
     h->last_splits = 1;
     h->last_launches = 0;
+    h->last_relayout = 0;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (batch == 1) strideA = strideB = strideC = 0;  // unused: keep the kernels on 2-D maps
@@ -501,38 +605,84 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         return rc;
     }
 
-    // Arguments of the TMA kernels: A^T B^T runs as the NN kernel on the
-    // swapped operands (C^T = B_s A_s) with a transposed epilogue.
-    sg::GemmArgs k = g;
-    int op = transA ? (transB ? sg::kTmaOpNN : sg::kTmaOpTN) : (transB ? sg::kTmaOpNT : sg::kTmaOpNN);
-    if (transA && transB) {
-        k.M = N;
-        k.N = M;
-        k.A = B;
-        k.lda = ldb;
-        k.sA = strideB;
-        k.B = A;
-        k.ldb = lda;
-        k.sB = strideA;
-        k.c_trans = 1;
-        k.vec_c = false;
-    }
     const bool nn1 = !transA && !transB && batch == 1;
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
                         (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
     int variant = h->pinned;
     if (!nn1 && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
         variant = SGEMM_VARIANT_AUTO;  // the tensor-core kernels serve NN with batch 1
+    if (variant == SGEMM_VARIANT_TC_F16_PAIR || variant == SGEMM_VARIANT_GENERIC_F16)
+        variant = SGEMM_VARIANT_AUTO;  // 16-bit-input variants: sgemm_run_mixed only
     if (variant == SGEMM_VARIANT_AUTO) {
         // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
         // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
         const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
         if (nn1 && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
             variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
-        else
-            variant = choose_variant(h, k.M, k.N, K, batch, op);
     }
     if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
+
+    // FP32 SIMT kernels: the variant, and the operands first transposed into
+    // the re-layout workspace (batch 1 only).
+    int relayout = 0;
+    const float *eA = A, *eB = B;
+    int elda = lda, eldb = ldb, etA = transA, etB = transB;
+    if (variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TC_3XTF32 &&
+        variant != SGEMM_VARIANT_TC_3XTF32_PAIR) {
+        if (batch == 1) {
+            const Fp32Plan p = plan_fp32(h, transA, transB, M, N, K, variant);
+            variant = p.variant;
+            relayout = p.relayout;
+        } else if (variant == SGEMM_VARIANT_AUTO) {
+            int kM, kN;
+            const int op0 = op_after(transA, transB, 0, M, N, &kM, &kN);
+            variant = choose_variant(h, kM, kN, K, batch, op0);
+        }
+    }
+    int launches = 0;
+    if (relayout & 1) {  // A (stored M x K) -> A^T stored K x M
+        float *dst = h->d_rl;
+        const int ld = round32(M);
+        const int rc = from_cuda(sg::launch_transpose(A, M, K, lda, dst, ld, stream));
+        if (rc != SGEMM_OK) return rc;
+        eA = dst;
+        elda = ld;
+        etA = 1;
+        ++launches;
+    }
+    if (relayout & 2) {  // B (stored N x K) -> B^T stored K x N, after A^T if both
+        float *dst = h->d_rl + ((relayout & 1) ? static_cast<size_t>(K) * round32(M) : 0);
+        const int ld = round32(N);
+        const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream));
+        if (rc != SGEMM_OK) return rc;
+        eB = dst;
+        eldb = ld;
+        etB = 0;
+        ++launches;
+    }
+
+    // Arguments of the TMA kernels: A^T B^T runs as the NN kernel on the
+    // swapped operands (C^T = B_s A_s) with a transposed epilogue.
+    sg::GemmArgs k = g;
+    k.A = eA;
+    k.lda = elda;
+    k.B = eB;
+    k.ldb = eldb;
+    k.transA = etA;
+    k.transB = etB;
+    int op = etA ? (etB ? sg::kTmaOpNN : sg::kTmaOpTN) : (etB ? sg::kTmaOpNT : sg::kTmaOpNN);
+    if (etA && etB) {
+        k.M = N;
+        k.N = M;
+        k.A = eB;
+        k.lda = eldb;
+        k.sA = strideB;
+        k.B = eA;
+        k.ldb = elda;
+        k.sB = strideA;
+        k.c_trans = 1;
+        k.vec_c = false;
+    }
 
     if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
         sg::TmaShape ts;
@@ -572,10 +722,11 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         if (!a_ok || !b_ok) variant = SGEMM_VARIANT_GENERIC;  // a layout TMA cannot describe
     }
     if (variant == SGEMM_VARIANT_GENERIC) {
-        const int rc = from_cuda(sg::launch_generic(g, stream));
+        const int rc = from_cuda(sg::launch_generic(g, stream));  // the operands as the caller stored them
         if (rc == SGEMM_OK) {
             h->last_variant = variant;
-            h->last_launches = 1;
+            h->last_launches = launches + 1;
+            h->last_relayout = relayout;
         }
         return rc;
     }
@@ -583,7 +734,9 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     if (rc == SGEMM_OK) {
         h->last_variant = variant;
         h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn));
-        h->last_launches = sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1;  // whole-tile waves, then stream-K
+        // transposes, then the whole-tile waves and the stream-K CTAs
+        h->last_launches = launches + (sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1);
+        h->last_relayout = relayout;
     }
     return rc;
 }
@@ -617,6 +770,7 @@ int sgemm_run_mixed(sgemm_handle_t h, int in_type, int transA, int transB, int M
     if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
     const int st = sgemm_check_args_mixed(in_type, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc);
     if (st != SGEMM_OK) return st;
+    h->last_relayout = 0;
     h->last_variant = -1;
     h->last_splits = 1;
     h->last_launches = 0;

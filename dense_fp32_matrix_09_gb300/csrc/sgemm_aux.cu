@@ -14,6 +14,12 @@
 //    into the sgemmNN algorithm", write-back section).
 //  * sgemm_scale_kernel -- the alpha == 0 or K == 0 quick path: C = beta*C,
 //    or C = 0 without reading C when beta == 0 (BLAS convention).
+//  * transpose_kernel -- operand re-layout: dst (cols x rows) = src^T (rows x
+//    cols), both row-major with leading dimensions, through a 64 x 64 tile in
+//    shared memory padded to 65 floats a row, so that both the column reads
+//    and the row writes of a warp fall in 32 distinct banks (the padding fix
+//    of page m.lqnn.cn/news/94381 section 4.3); global loads and stores are
+//    row segments of 128 bytes per warp.
 //  * fma_probe_kernel, bank_probe_kernel -- measurement probes: the FP32 FMA
 //    rate with no memory traffic, and a shared-memory access with and
 //    without bank conflicts (a control for the profiler's counters);
@@ -134,6 +140,38 @@ __global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
     }
 }
 
+// dst[c][r] = src[r][c] for r < rows, c < cols; one 64 x 64 tile per CTA
+// (grid x over cols, grid y over rows), 256 threads as 8 rows of 32 lanes.
+// Each thread issues its 16 loads before the barrier, so a CTA has 16 KiB in
+// flight; 8 CTAs fit on an SM.
+constexpr int kTrTile = 64;
+
+__global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ src, int rows, int cols,
+                                                        long long lds, float *__restrict__ dst, long long ldd) {
+    __shared__ float t[kTrTile][kTrTile + 1];
+    const int r0 = blockIdx.y * kTrTile, c0 = blockIdx.x * kTrTile;
+    const int lx = threadIdx.x & 31, ly = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < kTrTile / 8; ++i) {
+        const int r = r0 + ly + 8 * i;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = c0 + lx + 32 * h;
+            if (r < rows && c < cols) t[ly + 8 * i][lx + 32 * h] = src[r * lds + c];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kTrTile / 8; ++i) {
+        const int c = c0 + ly + 8 * i;  // row of dst
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int r = r0 + lx + 32 * h;  // column of dst
+            if (c < cols && r < rows) dst[c * ldd + r] = t[lx + 32 * h][ly + 8 * i];
+        }
+    }
+}
+
 // FP32 FMA throughput probe: every thread runs kFmaChains independent chains
 // of packed FP32x2 FMAs (acc = a*acc + b) in registers, `iters` times, and
 // writes one sum (so nothing is dead code).  No memory traffic in the loop:
@@ -206,6 +244,14 @@ cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
     const int gy = min(g.M, 8192);
     const int gz = min(g.batch, max(1, 65535 / gy));
     sgemm_scale_kernel<<<dim3(gx, gy, gz), 256, 0, stream>>>(g);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, float *dst, int ldd,
+                             cudaStream_t stream) {
+    const dim3 grid((cols + kTrTile - 1) / kTrTile, (rows + kTrTile - 1) / kTrTile);
+    if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+    transpose_kernel<<<grid, 256, 0, stream>>>(src, rows, cols, lds, dst, ldd);
     return cudaGetLastError();
 }
 

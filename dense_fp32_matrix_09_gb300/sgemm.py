@@ -41,6 +41,9 @@ MATH_FP32 = 0
 MATH_3XTF32 = 1
 IN_BF16 = 1
 IN_F16 = 2
+RELAYOUT_AUTO = 0
+RELAYOUT_OFF = 1
+RELAYOUT_ALWAYS = 2
 GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
                  VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32, VARIANT_TC_3XTF32_PAIR)
 
@@ -50,7 +53,8 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_debug_set_smem_override", "sgemm_status_string", "sgemm_variant_name",
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
-           "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe")
+           "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
+           "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity")
 
 
 class SgemmError(RuntimeError):
@@ -82,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.sgemm_set_variant.argtypes = [vp, i32]
         L.sgemm_last_variant.argtypes = [vp, ctypes.POINTER(i32)]
         L.sgemm_last_launches.argtypes = [vp]
+        L.sgemm_set_relayout.argtypes = [vp, i32]
+        L.sgemm_last_relayout.argtypes = [vp]
+        L.sgemm_relayout_capacity.argtypes = [vp]
+        L.sgemm_relayout_capacity.restype = ctypes.c_longlong
         L.sgemm_debug_fma_probe.argtypes = [vp, i32, i32, vp, ctypes.POINTER(ctypes.c_longlong), vp]
         L.sgemm_debug_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
         L.sgemm_run_mixed.argtypes = [vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
@@ -245,6 +253,19 @@ def sgemm_last_launches(h) -> int:
     return lib().sgemm_last_launches(h)
 
 
+def sgemm_set_relayout(h, mode: int) -> None:
+    _check(lib().sgemm_set_relayout(h, int(mode)), "sgemm_set_relayout")
+
+
+def sgemm_last_relayout(h) -> int:
+    """Operands the last call copied transposed first: bit 0 A, bit 1 B."""
+    return lib().sgemm_last_relayout(h)
+
+
+def sgemm_relayout_capacity(h) -> int:
+    return lib().sgemm_relayout_capacity(h)
+
+
 def sgemm_get_device_status(h) -> int:
     return lib().sgemm_get_device_status(h)
 
@@ -287,6 +308,13 @@ class Sgemm:
 
     def set_variant(self, v):
         sgemm_set_variant(self.h, v)
+
+    def set_relayout(self, mode):
+        sgemm_set_relayout(self.h, mode)
+
+    @property
+    def last_relayout(self) -> int:
+        return sgemm_last_relayout(self.h)
 
     def device_status(self) -> int:
         return sgemm_get_device_status(self.h)

@@ -35,8 +35,8 @@
  *
  * Threading: one handle may be used from one host thread at a time, and its
  * calls must be ordered on the GPU (one stream, or streams ordered by
- * events): calls of the same handle share its stream-K workspace.  Use one
- * handle per concurrently running stream.
+ * events): calls of the same handle share its stream-K and re-layout
+ * workspaces.  Use one handle per concurrently running stream.
  *
  * Every function returns an sgemm_status_t value (as int) unless noted.
  */
@@ -109,6 +109,28 @@ typedef enum {
     SGEMM_MATH_3XTF32 = 1
 } sgemm_math_mode_t;
 
+/* Operand re-layout of the FP32 SIMT path (sgemm_run, sgemm_run_ex with
+ * batch 1, TMA-eligible operands).  On GB300 the SIMT kernel's main loop is
+ * fastest with A stored K x M and B stored K x N (transA = 1, transB = 0:
+ * one 16-byte shared-memory load then gives one k of four rows of A).  The
+ * library may therefore first copy A stored M x K, or B stored N x K,
+ * transposed into the handle's re-layout workspace (an HBM-bound pass,
+ * about 0.6 % of the time of an 8192^3 product) and run the GEMM on the
+ * copy.  Every layout forms each product in ascending k with one rounding
+ * per FMA, so with the same tile variant and the same stream-K plan the
+ * result is bit-identical to the call without re-layout.
+ *   SGEMM_RELAYOUT_AUTO (default): when the library's time estimate of the
+ *     copies plus the faster kernel beats the kernel on the operands as
+ *     stored by at least 1 % and the copies fit in the workspace;
+ *   SGEMM_RELAYOUT_OFF: never;
+ *   SGEMM_RELAYOUT_ALWAYS: whenever the copies that reach transA = 1,
+ *     transB = 0 fit in the workspace (tests, measurements). */
+typedef enum {
+    SGEMM_RELAYOUT_AUTO = 0,
+    SGEMM_RELAYOUT_OFF = 1,
+    SGEMM_RELAYOUT_ALWAYS = 2
+} sgemm_relayout_t;
+
 /* Element type of A and B for sgemm_run_mixed (C is always FP32). */
 typedef enum {
     SGEMM_IN_BF16 = 1,  /* bfloat16: 1 sign, 8 exponent, 7 fraction bits */
@@ -117,9 +139,12 @@ typedef enum {
 
 /* Create a handle bound to the CURRENT CUDA device.  Requires compute
  * capability 10.3 (GB300); otherwise returns SGEMM_ERR_UNSUPPORTED_DEVICE and
- * sets *out to NULL.  Allocates the handle's device-side status word and its
- * stream-K workspace (48 MiB) and arrival counters (zeroed) and sets the kernels' shared-memory
- * limits.  `out` must be non-NULL (else SGEMM_ERR_NULL). */
+ * sets *out to NULL.  Allocates the handle's device-side status word, its
+ * stream-K workspace (48 MiB) and arrival counters (zeroed), and its operand
+ * re-layout workspace (512 MiB: the transposes of an 8192 x 8192 A and B;
+ * if that allocation fails the handle is created without it and never
+ * re-lays out), and sets the kernels' shared-memory limits.  `out` must be
+ * non-NULL (else SGEMM_ERR_NULL). */
 int sgemm_create(sgemm_handle_t *out);
 
 /* C <- alpha*A*B + beta*C, enqueued on `stream`; see the conventions above.
@@ -216,12 +241,31 @@ int sgemm_destroy(sgemm_handle_t h);
 
 /* Pin a kernel variant for later calls of this handle (SGEMM_VARIANT_AUTO to
  * let the library choose).  SGEMM_ERR_INVALID_VALUE for an unknown value or
- * SGEMM_VARIANT_SCALE, which is chosen only by the alpha == 0 / K == 0 rule. */
+ * SGEMM_VARIANT_SCALE, which is chosen only by the alpha == 0 / K == 0 rule.
+ * A pinned TMA variant fixes the tile; the re-layout mode still decides
+ * whether operands are transposed first.  The 16-bit-input variants act as
+ * SGEMM_VARIANT_AUTO for FP32 calls. */
 int sgemm_set_variant(sgemm_handle_t h, int variant);
 
 /* Set the handle's math mode (an sgemm_math_mode_t) for SGEMM_VARIANT_AUTO.
  * SGEMM_ERR_INVALID_VALUE for an unknown mode. */
 int sgemm_set_math_mode(sgemm_handle_t h, int mode);
+
+/* Set the handle's operand re-layout mode (an sgemm_relayout_t).
+ * SGEMM_ERR_INVALID_VALUE for an unknown mode. */
+int sgemm_set_relayout(sgemm_handle_t h, int mode);
+
+/* Operands the handle's last successful sgemm_run / sgemm_run_ex copied
+ * transposed before the GEMM: bit 0 A, bit 1 B (0 for none); -1 if `h` is
+ * not a live handle. */
+int sgemm_last_relayout(sgemm_handle_t h);
+
+/* Size of the handle's re-layout workspace in floats (0 if it could not be
+ * allocated, and then no operand is re-laid out); -1 if `h` is not a live
+ * handle.  Transposed copies are stored with leading dimensions rounded up
+ * to a multiple of 32 floats: A needs K * ceil32(M) floats, B K * ceil32(N),
+ * both together the sum. */
+int64_t sgemm_relayout_capacity(sgemm_handle_t h);
 
 /* The variant the handle's last successful sgemm_run enqueued (an
  * sgemm_variant_t), or -1 if there was none or `h` is not a live handle.
@@ -230,9 +274,10 @@ int sgemm_set_math_mode(sgemm_handle_t h, int mode);
 int sgemm_last_variant(sgemm_handle_t h, int *splits);
 
 /* Number of kernel launches the handle's last successful sgemm_run /
- * sgemm_run_ex enqueued: 0 (nothing to do), 1, or 2 (complete waves of whole
- * tiles, then the stream-K CTAs of the last wave, on the same stream); -1 if
- * `h` is not a live handle. */
+ * sgemm_run_ex enqueued: 0 (nothing to do), one per transposed operand
+ * (sgemm_last_relayout), then 1, or 2 for the GEMM (complete waves of whole
+ * tiles, then the stream-K CTAs of the last wave), all on the same stream;
+ * -1 if `h` is not a live handle. */
 int sgemm_last_launches(sgemm_handle_t h);
 
 /* Wait for the handle's device to finish its work, then read and clear the
