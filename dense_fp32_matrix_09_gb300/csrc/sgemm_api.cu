@@ -259,6 +259,11 @@ double transpose_cost(int rows, int cols) { return 6.0 + 8.0 * rows * static_cas
 
 inline int round32(int x) { return (x + 31) / 32 * 32; }
 
+bool is_tma_variant(int v) {
+    sg::TmaShape sh;
+    return sg::tma_shape(v, &sh);
+}
+
 // Plan of an FP32 SIMT call: the kernel variant and which operands are first
 // transposed into the re-layout workspace (bit 0: A, bit 1: B).
 struct Fp32Plan {
@@ -823,10 +828,9 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     const size_t f = sizeof(float);
     // Row panels of A and C: multiples of 256 rows, at most 8.  B goes over in
     // up to 8 column chunks (multiples of 256 columns) right after the first
-    // A panel; the first panel is computed chunk by chunk as B's chunks land,
-    // and the last panel in the same column blocks, each copied back as soon
-    // as it is done -- so only the first A panel and B chunk wait before any
-    // compute, and only the last block's copy after it.
+    // A panel, then the other A panels -- so only the first A panel and B
+    // chunk wait before any compute, and (see the compute order below) only
+    // the last column block's copy back after it.
     const int panels = std::max(1, std::min(8, M / 1024));
     const int rows = ((cdiv(M, panels) + 255) / 256) * 256;
     const int np = cdiv(M, rows);
@@ -854,10 +858,14 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
             return false;
         return ok(cudaEventRecord(ev_a[p], h->copy_in));
     };
+    // A operand of the current panel's GEMMs: the staged rows, or their
+    // transposed copy in the re-layout workspace (made once per panel)
+    const float *pA = dA;
+    int plda = lda, ptA = 0;
     // GEMM of rows [r0, r0+nr) x columns [c0, c0+nc) on `stream`, then its copy back after event `ev`
     auto block = [&](int r0, int nr, int c0, int nc, cudaEvent_t ev) {
-        const int st2 = sgemm_run(h, nr, nc, K, alpha, dA + static_cast<size_t>(r0) * lda, lda, dB + c0, ldb, beta,
-                                  dC + static_cast<size_t>(r0) * ldc + c0, ldc, stream_);
+        const int st2 = sgemm_run_ex(h, ptA, 0, nr, nc, K, alpha, pA, plda, 0, dB + c0, ldb, 0, beta,
+                                     dC + static_cast<size_t>(r0) * ldc + c0, ldc, 0, 1, stream_);
         if (st2 != SGEMM_OK) return st2;
         if (!ok(cudaEventRecord(ev, stream)) || !ok(cudaStreamWaitEvent(h->copy_out, ev, 0)) ||
             !ok(cudaMemcpy2DAsync(C + static_cast<size_t>(r0) * ldc + c0, ldc * f,
@@ -881,20 +889,75 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     }
     for (int p = 1; p < np; ++p)
         if (!copy_in_panel(p)) return SGEMM_ERR_CUDA;
+    // Compute order: the first panel in column blocks as B's chunks land; the
+    // middle panels together as one GEMM once the last of them has landed
+    // (one call keeps the tiles in complete waves, where a call per panel
+    // would end each panel with a partial wave); the last panel in column
+    // blocks.  Every piece of C goes back as soon as its GEMM is done.
+    //
+    // Operand re-layout per segment: the segment's A rows are copied
+    // transposed once and every GEMM of the segment runs in the TN layout on
+    // the copy (sgemm_run would copy them again for each column block), when
+    // the time estimate for the whole segment copies A -- the GEMMs then run
+    // with transA = 1, which needs no copy of its own, so the workspace holds
+    // only this segment's copy.
+    auto copies_a = [&](int nr) {
+        return reads_ab && h->d_rl != nullptr && h->relayout_mode != SGEMM_RELAYOUT_OFF &&
+               h->math_mode == SGEMM_MATH_FP32 && aligned16(dA) && aligned16(dB) && (lda % 4) == 0 &&
+               (ldb % 4) == 0 && (h->pinned == SGEMM_VARIANT_AUTO || is_tma_variant(h->pinned)) &&
+               static_cast<size_t>(K) * round32(nr) <= h->rl_floats &&
+               (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || (plan_fp32(h, 0, 0, nr, N, K, h->pinned).relayout & 1));
+    };
+    // Column blocks of the first panel follow B's chunks: 1, 1, then 2 chunks
+    // at a time (the first blocks start as soon as their chunk lands; later
+    // chunks land faster than a block computes, and at 1024 rows a block of
+    // two 1024-column chunks -- 64 tiles of 128 x 256 -- ran faster per chunk
+    // than blocks of one or four on GB300); the last panel runs them in
+    // reverse order, so only a one-chunk block's copy back follows the last
+    // GEMM.
+    int groups[8], ng = 0;
+    for (int q = 0; q < nq;) {
+        const int g = std::min(ng < 2 ? 1 : 2, nq - q);
+        groups[ng++] = g;
+        q += g;
+    }
+    // segments (first row, rows, last panel index, column-blocked)
+    struct Seg {
+        int r0, nr, p_last;
+        bool blocked;
+    } segs[3];
+    int ns = 0;
+    segs[ns++] = Seg{0, std::min(rows, M), 0, true};
+    if (np > 2) segs[ns++] = Seg{rows, (np - 2) * rows, np - 2, false};
+    if (np > 1) segs[ns++] = Seg{(np - 1) * rows, M - (np - 1) * rows, np - 1, true};
     // compute stream
-    for (int p = 0; p < np; ++p) {
-        const int r0 = p * rows, nr = std::min(rows, M - r0);
-        if (!ok(cudaStreamWaitEvent(stream, ev_a[p], 0))) return SGEMM_ERR_CUDA;
-        if (p == 0 || p == np - 1) {  // column blocks: the first panel follows B's chunks
-            for (int q = 0; q < nq; ++q) {
-                const int c0 = q * cols, nc = std::min(cols, N - c0);
-                if (!ok(cudaStreamWaitEvent(stream, ev_b[q], 0))) return SGEMM_ERR_CUDA;
-                st = block(r0, nr, c0, nc, ev_c());
+    for (int i = 0; i < ns; ++i) {
+        const Seg &sg_ = segs[i];
+        if (!ok(cudaStreamWaitEvent(stream, ev_a[sg_.p_last], 0))) return SGEMM_ERR_CUDA;
+        pA = dA + static_cast<size_t>(sg_.r0) * lda;
+        plda = lda;
+        ptA = 0;
+        if (copies_a(sg_.nr)) {
+            const int ld = round32(sg_.nr);
+            st = from_cuda(sg::launch_transpose(pA, sg_.nr, K, lda, h->d_rl, ld, stream));
+            if (st != SGEMM_OK) return st;
+            pA = h->d_rl;
+            plda = ld;
+            ptA = 1;
+        }
+        if (sg_.blocked) {
+            const bool first = sg_.r0 == 0;
+            for (int j = 0, q = 0; j < ng; ++j) {
+                const int gsz = first ? groups[j] : groups[ng - 1 - j];
+                const int c0 = q * cols, nc = std::min(gsz * cols, N - c0);
+                q += gsz;
+                if (!ok(cudaStreamWaitEvent(stream, ev_b[q - 1], 0))) return SGEMM_ERR_CUDA;
+                st = block(sg_.r0, sg_.nr, c0, nc, ev_c());
                 if (st != SGEMM_OK) return st;
             }
         } else {
             if (!ok(cudaStreamWaitEvent(stream, ev_b[nq - 1], 0))) return SGEMM_ERR_CUDA;
-            st = block(r0, nr, 0, N, ev_c());
+            st = block(sg_.r0, sg_.nr, 0, N, ev_c());
             if (st != SGEMM_OK) return st;
         }
     }

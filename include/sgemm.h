@@ -208,9 +208,11 @@ int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, in
  * of C when beta != 0), then B in up to 8 column chunks, then the other row
  * panels; on `stream` it runs each piece of the GEMM (the same kernels and
  * rules as sgemm_run) as soon as its operands have landed -- the first row
- * panel chunk by chunk as B's chunks arrive -- and on a second copy stream it
- * copies each finished panel (the last one block by block) back to C while
- * the rest computes.  Returns after enqueueing; C is complete when `stream`
+ * panel in column blocks as B's chunks arrive, the middle panels as one
+ * GEMM, the last panel in column blocks; each segment's A rows may first be
+ * copied transposed into the handle's re-layout workspace, once for all of
+ * the segment's GEMMs -- and on a second copy stream it copies each finished
+ * piece back to C while the rest computes.  Returns after enqueueing; C is complete when `stream`
  * reaches the point of the call (e.g. after cudaStreamSynchronize(stream)).
  * Page-locked host buffers give asynchronous copies; pageable ones work but
  * serialise.  The host and device windows must not be touched until then.

@@ -379,10 +379,22 @@ def test_math_mode_rejects_unknown(handle):
                                  inputs.GemmConfig("host_1200x2100x200_b0", 1200, 2100, 200, 200, 2100, 2104, 44,
                                                    1.0, 0.0)],
                          ids=lambda c: c.name)
-def test_run_host_buffers(handle, cfg, pinned):
+@pytest.mark.parametrize("relayout", [sgemm.RELAYOUT_AUTO, sgemm.RELAYOUT_ALWAYS], ids=["auto", "copy_A_panels"])
+def test_run_host_buffers(handle, cfg, pinned, relayout):
     """sgemm_run_host: host A, B, C; device staging buffers; copies overlap the
     per-panel GEMMs.  Checked against the oracle; padding cells of the host C
-    keep their bits; the result is ready once the stream is synchronized."""
+    keep their bits; the result is ready once the stream is synchronized.
+    With SGEMM_RELAYOUT_ALWAYS every A panel is copied transposed once and
+    its column blocks run in the TN layout on the copy."""
+    import torch
+    sgemm.sgemm_set_relayout(handle, relayout)
+    try:
+        _run_host_case(handle, cfg, pinned)
+    finally:
+        sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_AUTO)
+
+
+def _run_host_case(handle, cfg, pinned):
     import torch
     prob = inputs.make_problem(cfg)
     hA, hB, hC = (torch.from_numpy(x.copy()) for x in (prob.A, prob.B, prob.C0))
