@@ -693,7 +693,11 @@ def main():
         table = {}
         for w, reps in zip(inputs.CONFIGS, (200, 200, 50, 50, 20)):
             cold = (w.compulsory_bytes < 2 * 129e6)
-            table[w.name] = time_workload(torch, sg, h, w, reps, cold, flush_buf)
+            row = time_workload(torch, sg, h, w, reps, cold, flush_buf)
+            row["frac_of_fp32_peak"] = row["tflops"] / peak  # same unit-count peak as the roofline
+            if "tflops_back_to_back" in row:
+                row["frac_of_fp32_peak_back_to_back"] = row["tflops_back_to_back"] / peak
+            table[w.name] = row
         out["workloads"] = table
         del flush_buf
 
