@@ -257,7 +257,10 @@ int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int o
 // ordering gap), in microseconds.
 double transpose_cost(int rows, int cols) { return 6.0 + 8.0 * rows * static_cast<double>(cols) / 5.5e6; }
 
-inline int round32(int x) { return (x + 31) / 32 * 32; }
+// Leading dimension of a transposed copy: x rounded up to 32 floats (128
+// bytes); callers use it only where the copy fits in the workspace, which
+// bounds it far below INT_MAX.
+inline int round32(int x) { return static_cast<int>((static_cast<long long>(x) + 31) / 32 * 32); }
 
 bool is_tma_variant(int v) {
     sg::TmaShape sh;
@@ -312,8 +315,8 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         if ((r & 2) && !transB) continue;
         const bool to_tn = r == tn_r;
         if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS && !to_tn) continue;
-        const size_t need = ((r & 1) ? static_cast<size_t>(K) * round32(M) : 0) +
-                            ((r & 2) ? static_cast<size_t>(K) * round32(N) : 0);
+        const unsigned long long need = ((r & 1) ? static_cast<unsigned long long>(K) * ((M + 31ULL) / 32 * 32) : 0) +
+                                        ((r & 2) ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
         if (need > h->rl_floats) continue;
         double c;
         const int v = best_variant(op_after(transA, transB, r, M, N, &kM, &kN), kM, kN, &c);
@@ -905,7 +908,7 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
         return reads_ab && h->d_rl != nullptr && h->relayout_mode != SGEMM_RELAYOUT_OFF &&
                h->math_mode == SGEMM_MATH_FP32 && aligned16(dA) && aligned16(dB) && (lda % 4) == 0 &&
                (ldb % 4) == 0 && (h->pinned == SGEMM_VARIANT_AUTO || is_tma_variant(h->pinned)) &&
-               static_cast<size_t>(K) * round32(nr) <= h->rl_floats &&
+               static_cast<unsigned long long>(K) * ((nr + 31ULL) / 32 * 32) <= h->rl_floats &&
                (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || (plan_fp32(h, 0, 0, nr, N, K, h->pinned).relayout & 1));
     };
     // Column blocks of the first panel follow B's chunks: 1, 1, then 2 chunks

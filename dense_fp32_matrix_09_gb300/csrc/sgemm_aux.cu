@@ -141,15 +141,17 @@ __global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
 }
 
 // dst[c][r] = src[r][c] for r < rows, c < cols; one 64 x 64 tile per CTA
-// (grid x over cols, grid y over rows), 256 threads as 8 rows of 32 lanes.
-// Each thread issues its 16 loads before the barrier, so a CTA has 16 KiB in
-// flight; 8 CTAs fit on an SM.
+// (1-D grid, tiles row-major over the source), 256 threads as 8 rows of 32
+// lanes.  Each thread issues its 16 loads before the barrier, so a CTA has
+// 16 KiB in flight; 8 CTAs fit on an SM.
 constexpr int kTrTile = 64;
 
 __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ src, int rows, int cols,
                                                         long long lds, float *__restrict__ dst, long long ldd) {
     __shared__ float t[kTrTile][kTrTile + 1];
-    const int r0 = blockIdx.y * kTrTile, c0 = blockIdx.x * kTrTile;
+    const int tiles_c = (cols + kTrTile - 1) / kTrTile;
+    const int r0 = static_cast<int>(blockIdx.x / tiles_c) * kTrTile;
+    const int c0 = static_cast<int>(blockIdx.x % tiles_c) * kTrTile;
     const int lx = threadIdx.x & 31, ly = threadIdx.x >> 5;
 #pragma unroll
     for (int i = 0; i < kTrTile / 8; ++i) {
@@ -249,9 +251,9 @@ cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
 
 cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, float *dst, int ldd,
                              cudaStream_t stream) {
-    const dim3 grid((cols + kTrTile - 1) / kTrTile, (rows + kTrTile - 1) / kTrTile);
-    if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-    transpose_kernel<<<grid, 256, 0, stream>>>(src, rows, cols, lds, dst, ldd);
+    const long long tiles = 1LL * ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
+    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    transpose_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(src, rows, cols, lds, dst, ldd);
     return cudaGetLastError();
 }
 

@@ -173,6 +173,28 @@ def test_workspace_capacity_edge(handle, mode, K, copied):
     assert err <= 1e-2
 
 
+def test_copy_of_a_very_tall_operand(handle, mode):
+    """A copy with more than 65535 tiles of 64 rows (M = 4.3 million, K = 4):
+    the copy kernel's grid is one-dimensional, so no grid limit cuts it.
+    Sampled rows (both ends, the 64-row tile edges) against the oracle."""
+    mode(V.RELAYOUT_ALWAYS)
+    M, N, K = 4_300_000, 8, 4
+    g = torch.Generator(device="cuda").manual_seed(4)
+    A = torch.rand(M, K, device="cuda", generator=g) * 2 - 1
+    B = torch.rand(K, N, device="cuda", generator=g) * 2 - 1
+    C = torch.empty(M, N, device="cuda")
+    sgemm.sgemm_run(handle, M, N, K, 1.0, A, K, B, N, 0.0, C, N)
+    torch.cuda.synchronize()
+    assert sgemm.sgemm_last_relayout(handle) == 1
+    rows = [0, 63, 64, 65535 * 64 - 1, 65535 * 64, M - 65, M - 1]
+    a = A[rows].cpu().numpy().reshape(-1)
+    b = B.cpu().numpy().reshape(-1)
+    ref = np.empty(len(rows) * N, dtype=np.float32)
+    oracle.sgemm(len(rows), N, K, 1.0, a, K, b, N, 0.0, ref, N)
+    err = float(np.max(np.abs(C[rows].cpu().numpy().astype(np.float64) - ref.reshape(len(rows), N))))
+    assert err <= 1e-3
+
+
 def test_auto_copies_only_where_the_estimate_gains(handle, mode):
     """AUTO: a 2048^3 NN product runs on A^T (the copy costs far less than
     the faster main loop saves); a 256^3 one does not (the extra launch would
