@@ -667,6 +667,19 @@ def main():
             tc_ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
         tc_ms = statistics.mean(tc_ev[2 * i].elapsed_time(tc_ev[2 * i + 1]) for i in range(args.tensor_steps))
+        # the other operand layouts on the same kernel (transposed operands
+        # reach it through copies into the NN layout), square workloads only
+        tc_layouts = {}
+        if cfg.M == cfg.N == cfg.K == cfg.lda == cfg.ldb == cfg.ldc and cfg.beta == 0:
+            for name, ta, tb in (("NT", 0, 1), ("TN", 1, 0), ("TT", 1, 1)):
+                def tcall(ta=ta, tb=tb):
+                    sg.sgemm_run_ex(h, ta, tb, cfg.M, cfg.N, cfg.K, cfg.alpha, A, cfg.lda, 0, B, cfg.ldb, 0,
+                                    cfg.beta, C, cfg.ldc, 0, 1, stream)
+                lms = time_calls(torch, stream, tcall, 10, args.warmup)
+                med = statistics.median(lms)
+                tc_layouts[name] = {"ms_median": med, "tflops": cfg.flops / (med * 1e-3) / 1e12,
+                                    "variant": sg.variant_name(sg.sgemm_last_variant(h)[0]),
+                                    "copies": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)]}
         sg.sgemm_set_variant(h, sg.VARIANT_AUTO)
         bf16 = measured_bf16_tflops()
         tf32_peak = bf16["value"] * 1.1 / 2.25
@@ -682,6 +695,7 @@ def main():
                          "peak_basis": f"TF32 dense = {bf16['source']} BF16 {bf16['value']:.1f} TFLOP/s x 1.1/2.25 "
                                        f"(nominal ratio) = {tf32_peak:.1f}; 3 TF32 MMAs per FP32 product",
                          "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
+            "layouts": tc_layouts,
         }
 
     # ---- sgemm_run_ex: the four operand layouts on the headline shape, and a

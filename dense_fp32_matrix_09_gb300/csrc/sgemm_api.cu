@@ -613,30 +613,81 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         return rc;
     }
 
-    const bool nn1 = !transA && !transB && batch == 1;
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
                         (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
+    // The tensor-core kernels read A stored M x K and B stored K x N, batch 1;
+    // another layout reaches them through transposed copies of its stored-
+    // transposed operands in the re-layout workspace (A stored K x M -> M x K,
+    // B stored N x K -> K x N), when re-layout is not off and the copies fit.
+    const int tc_copy = (transA ? 1 : 0) | (transB ? 2 : 0);
+    const unsigned long long tc_need =
+        (transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0) +
+        (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
+    const bool tc_reachable = batch == 1 && (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF &&
+                                                              h->d_rl != nullptr && tc_need <= h->rl_floats));
     int variant = h->pinned;
-    if (!nn1 && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
-        variant = SGEMM_VARIANT_AUTO;  // the tensor-core kernels serve NN with batch 1
+    if (!tc_reachable && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
+        variant = SGEMM_VARIANT_AUTO;
     if (variant == SGEMM_VARIANT_TC_F16_PAIR || variant == SGEMM_VARIANT_GENERIC_F16)
         variant = SGEMM_VARIANT_AUTO;  // 16-bit-input variants: sgemm_run_mixed only
     if (variant == SGEMM_VARIANT_AUTO) {
         // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
         // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
         const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
-        if (nn1 && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
+        if (tc_reachable && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
             variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
     }
     if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
+
+    if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
+        const float *tA_ = A, *tB_ = B;
+        int tlda = lda, tldb = ldb, launches = 0;
+        if (tc_copy & 1) {  // A stored K x M -> M x K
+            const int ld = round32(K);
+            const int rc = from_cuda(sg::launch_transpose(A, K, M, lda, h->d_rl, ld, stream));
+            if (rc != SGEMM_OK) return rc;
+            tA_ = h->d_rl;
+            tlda = ld;
+            ++launches;
+        }
+        if (tc_copy & 2) {  // B stored N x K -> K x N, after A's copy if both
+            float *dst = h->d_rl + ((tc_copy & 1) ? static_cast<size_t>(M) * round32(K) : 0);
+            const int ld = round32(N);
+            const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream));
+            if (rc != SGEMM_OK) return rc;
+            tB_ = dst;
+            tldb = ld;
+            ++launches;
+        }
+        sg::GemmArgs gt = g;
+        gt.A = tA_;
+        gt.lda = tlda;
+        gt.B = tB_;
+        gt.ldb = tldb;
+        gt.transA = gt.transB = 0;
+        sg::TmaShape ts;
+        sg::tc3x_shape(&ts);
+        CUtensorMap tA, tB;
+        if (!encode_2d(&tA, tA_, M, K, tlda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !encode_2d(&tB, tB_, K, N, tldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
+            return SGEMM_ERR_CUDA;
+        const int rc = from_cuda(variant == SGEMM_VARIANT_TC_3XTF32
+                                     ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
+                                     : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream));
+        if (rc == SGEMM_OK) {
+            h->last_variant = variant;
+            h->last_launches = launches + 1;
+            h->last_relayout = tc_copy;
+        }
+        return rc;
+    }
 
     // FP32 SIMT kernels: the variant, and the operands first transposed into
     // the re-layout workspace (batch 1 only).
     int relayout = 0;
     const float *eA = A, *eB = B;
     int elda = lda, eldb = ldb, etA = transA, etB = transB;
-    if (variant != SGEMM_VARIANT_GENERIC && variant != SGEMM_VARIANT_TC_3XTF32 &&
-        variant != SGEMM_VARIANT_TC_3XTF32_PAIR) {
+    if (variant != SGEMM_VARIANT_GENERIC) {
         if (batch == 1) {
             const Fp32Plan p = plan_fp32(h, transA, transB, M, N, K, variant);
             variant = p.variant;
@@ -690,23 +741,6 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         k.sB = strideA;
         k.c_trans = 1;
         k.vec_c = false;
-    }
-
-    if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
-        sg::TmaShape ts;
-        sg::tc3x_shape(&ts);
-        CUtensorMap tA, tB;
-        if (!encode_2d(&tA, A, M, K, lda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&tB, B, K, N, ldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
-            return SGEMM_ERR_CUDA;
-        const int rc = from_cuda(variant == SGEMM_VARIANT_TC_3XTF32
-                                     ? sg::launch_tc3x(g, tA, tB, h->smem_override, stream)
-                                     : sg::launch_tc3x_pair(g, tA, tB, h->smem_override, stream));
-        if (rc == SGEMM_OK) {
-            h->last_variant = variant;
-            h->last_launches = 1;
-        }
-        return rc;
     }
 
     sg::TmaShape sh;

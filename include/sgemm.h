@@ -91,8 +91,12 @@ typedef enum {
     /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
      * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
      * for batch > 1, strideA, strideB) are multiples of 4; otherwise the
-     * generic variant runs.  The tensor-core variants serve transA = transB
-     * = 0 with batch 1; pinned for any other call they act as AUTO. */
+     * generic variant runs.  The tensor-core variants serve batch 1 in every
+     * layout: they read A stored M x K and B stored K x N, and an operand
+     * stored transposed is first copied into that layout in the re-layout
+     * workspace (one launch per copy; see sgemm_relayout_t).  Where that
+     * cannot be done (batch > 1, re-layout off, copies larger than the
+     * workspace) a pinned tensor-core variant acts as AUTO. */
 } sgemm_variant_t;
 
 /* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32
@@ -103,14 +107,16 @@ typedef enum {
  * problems large enough to profit; its rounding errors are larger than the
  * FP32 path's (about 5x at K = 8192) but still inside the contract.  In this
  * mode SGEMM_VARIANT_AUTO takes SGEMM_VARIANT_TC_3XTF32_PAIR when there are at
- * least SMs/4 tiles of 256 x 256 and K >= 256, and the FP32 kernels otherwise. */
+ * least SMs/4 tiles of 256 x 256 and K >= 256 and the tensor-core kernels can
+ * serve the call (see sgemm_variant_t), and the FP32 kernels otherwise. */
 typedef enum {
     SGEMM_MATH_FP32 = 0,
     SGEMM_MATH_3XTF32 = 1
 } sgemm_math_mode_t;
 
 /* Operand re-layout of the FP32 SIMT path (sgemm_run, sgemm_run_ex with
- * batch 1, TMA-eligible operands).  On GB300 the SIMT kernel's main loop is
+ * batch 1, TMA-eligible operands; the tensor-core variants' copies into the
+ * NN layout use the same workspace and are off with SGEMM_RELAYOUT_OFF).  On GB300 the SIMT kernel's main loop is
  * fastest with A stored K x M and B stored K x N (transA = 1, transB = 0:
  * one 16-byte shared-memory load then gives one k of four rows of A).  The
  * library may therefore first copy A stored M x K, or B stored N x K,

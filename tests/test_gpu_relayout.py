@@ -232,3 +232,49 @@ def test_graph_capture_with_relayout(handle, mode):
     graph.replay()
     torch.cuda.synchronize()
     p.check(dC.interior(), (dA, dB, dC))
+
+
+TC_VARIANTS = (V.VARIANT_TC_3XTF32, V.VARIANT_TC_3XTF32_PAIR)
+TC_COPIES = {(0, 0): 0, (0, 1): 2, (1, 0): 1, (1, 1): 3}  # operands copied into the NN layout
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+@pytest.mark.parametrize("v", TC_VARIANTS, ids=lambda v: sgemm.variant_name(v))
+def test_tensor_core_kernels_in_every_layout(handle, mode, op, v):
+    """The 3xTF32 kernels read A stored M x K and B stored K x N; the other
+    layouts reach them through transposed copies (A stored K x M, B stored
+    N x K), on a ragged shape of several tiles each way."""
+    mode(V.RELAYOUT_AUTO, v)
+    p = ExProblem(op[0], op[1], 300, 520, 270, batch=1, seed=161, alpha=1.5, beta=-0.5, pad=(4, 4, 4), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] == v
+    assert sgemm.sgemm_last_relayout(handle) == TC_COPIES[op]
+    assert sgemm.sgemm_last_launches(handle) == 1 + bin(TC_COPIES[op]).count("1")
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_math_mode_3xtf32_every_layout(handle, mode, op):
+    """3xTF32 math mode takes the CTA-pair tensor-core kernel in every layout
+    once the problem is large enough (2048 x 2048 tiles, K = 512)."""
+    mode(V.RELAYOUT_AUTO)
+    sgemm.sgemm_set_math_mode(handle, V.MATH_3XTF32)
+    try:
+        p = ExProblem(op[0], op[1], 2048, 2048, 512, batch=1, seed=171, beta=0.5, pad=(0, 0, 0))
+        C, bufs = p.run(handle)
+        ran = sgemm.sgemm_last_variant(handle)[0]
+    finally:
+        sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
+    p.check(C, bufs)
+    assert ran == V.VARIANT_TC_3XTF32_PAIR
+
+
+def test_tensor_core_kernel_without_relayout_falls_back(handle, mode):
+    """With re-layout off, a pinned tensor-core variant cannot serve a
+    transposed layout: the call runs on the FP32 kernels instead."""
+    mode(V.RELAYOUT_OFF, V.VARIANT_TC_3XTF32_PAIR)
+    p = ExProblem(1, 0, 300, 520, 270, batch=1, seed=181, pad=(4, 4, 4), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] not in TC_VARIANTS
+    assert sgemm.sgemm_last_relayout(handle) == 0
