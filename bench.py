@@ -396,6 +396,28 @@ def bench_ex(torch, sg, h, cfg, A, B, C, stream, warmup: int) -> dict:
         "hbm_peak_source": hbm["source"] if hbm else None,
     }
     del bA, bB, bC, flush_buf
+    # a strided batch of large products: 8 x (2048 x 2048)·(2048 x 2048), as
+    # the library runs it (each A copied transposed) and on A as stored
+    bs2, n2 = 8, 2048
+    g2 = torch.Generator(device="cpu").manual_seed(5)
+    lA = (torch.rand(bs2 * n2 * n2, generator=g2) * 2 - 1).cuda()
+    lB = (torch.rand(bs2 * n2 * n2, generator=g2) * 2 - 1).cuda()
+    lC = torch.empty(bs2 * n2 * n2, device="cuda")
+    lflops = 2.0 * bs2 * n2 ** 3
+
+    def lcall():
+        sg.sgemm_run_ex(h, 0, 0, n2, n2, n2, 1.0, lA, n2, n2 * n2, lB, n2, n2 * n2, 0.0, lC, n2, n2 * n2, bs2,
+                        stream)
+    for mode, key in ((sg.RELAYOUT_AUTO, "batched_8x2048cube"), (sg.RELAYOUT_OFF, "batched_8x2048cube_as_stored")):
+        sg.sgemm_set_relayout(h, mode)
+        ms = time_calls(torch, stream, lcall, 20, warmup)
+        v, _ = sg.sgemm_last_variant(h)
+        med = statistics.median(ms)
+        res[key] = {"ms_median": med, "tflops": lflops / (med * 1e-3) / 1e12, "variant": sg.variant_name(v),
+                    "relayout": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)], "batch": bs2,
+                    "l2": "inputs larger than L2 (384 MiB)"}
+    sg.sgemm_set_relayout(h, sg.RELAYOUT_AUTO)
+    del lA, lB, lC
     return res
 
 

@@ -103,9 +103,10 @@ cudaError_t launch_tc16(bool bf16, const GemmArgs &g, const CUtensorMap &tmA, co
                         int smem_override, cudaStream_t stream);
 cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream);
 // dst (cols x rows, leading dimension ldd) = src^T (rows x cols, leading
-// dimension lds), both row-major FP32 (operand re-layout).
+// dimension lds), both row-major FP32 (operand re-layout); with batch > 1,
+// matrix b at src + b * sstride and dst + b * dstride.
 cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, float *dst, int ldd,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int batch = 1, long long sstride = 0, long long dstride = 0);
 cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);
 // Returns the FLOP the launch performs (-1 on a launch error); sink: ctas * 256 floats.
 long long launch_fma_probe(float *sink, int ctas, int iters, cudaStream_t stream);

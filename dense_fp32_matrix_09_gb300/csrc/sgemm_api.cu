@@ -252,10 +252,12 @@ int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int o
     return best;
 }
 
-// Estimated time of transposing a rows x cols FP32 operand (a read and a
-// write of every element at about 5.5 TB/s, plus the launch and its
-// ordering gap), in microseconds.
-double transpose_cost(int rows, int cols) { return 6.0 + 8.0 * rows * static_cast<double>(cols) / 5.5e6; }
+// Estimated time of transposing `count` rows x cols FP32 matrices in one
+// launch (a read and a write of every element at about 5.5 TB/s, plus the
+// launch and its ordering gap), in microseconds.
+double transpose_cost(int rows, int cols, int count = 1) {
+    return 6.0 + 8.0 * rows * static_cast<double>(cols) * count / 5.5e6;
+}
 
 // Leading dimension of a transposed copy: x rounded up to 32 floats (128
 // bytes); callers use it only where the copy fits in the workspace, which
@@ -285,26 +287,29 @@ int op_after(int transA, int transB, int r, int M, int N, int *kM, int *kN) {
     return ta ? (tb ? sg::kTmaOpNN : sg::kTmaOpTN) : (tb ? sg::kTmaOpNT : sg::kTmaOpNN);
 }
 
-// Variant and re-layout for a TMA-eligible FP32 call with batch 1 (a pinned
-// TMA variant keeps its tile).  Candidates: the operands as stored, and each
-// combination of transposed copies of A stored M x K and of B stored N x K;
-// the one that reaches the TN layout -- the fastest main loop on GB300 -- is
-// NN: A; NT: A and B; A^T B^T: B.  Each candidate costs variant_cost of its
-// layout plus transpose_cost of each copy, and needs its copies to fit in the
+// Variant and re-layout for a TMA-eligible FP32 call (a pinned TMA variant
+// keeps its tile).  Candidates: the operands as stored, and each combination
+// of transposed copies of A stored M x K and of B stored N x K; the one that
+// reaches the TN layout -- the fastest main loop on GB300 -- is NN: A; NT: A
+// and B; A^T B^T: B.  Each candidate costs variant_cost of its layout plus
+// transpose_cost of each copy (one matrix for an operand shared by the whole
+// batch, stride 0, else `batch`), and needs its copies to fit in the
 // workspace; a re-layout must save 1 %.  SGEMM_RELAYOUT_ALWAYS takes the TN
 // candidate whenever it fits; SGEMM_RELAYOUT_OFF only the stored layout.
-Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int pinned) {
+Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
+                   long long strideB, int pinned) {
     auto best_variant = [&](int op, int kM, int kN, double *cost) {
         if (pinned != SGEMM_VARIANT_AUTO) {
             sg::SplitK plan;
-            *cost = variant_cost(h, pinned, kM, kN, K, 1, op, &plan);
+            *cost = variant_cost(h, pinned, kM, kN, K, batch, op, &plan);
             return pinned;
         }
-        int v = choose_variant(h, kM, kN, K, 1, op);
+        int v = choose_variant(h, kM, kN, K, batch, op);
         sg::SplitK plan;
-        *cost = variant_cost(h, v, kM, kN, K, 1, op, &plan);
+        *cost = variant_cost(h, v, kM, kN, K, batch, op, &plan);
         return v;
     };
+    const int nA = strideA == 0 ? 1 : batch, nB = strideB == 0 ? 1 : batch;
     int kM, kN;
     double best_cost;
     Fp32Plan best{best_variant(op_after(transA, transB, 0, M, N, &kM, &kN), kM, kN, &best_cost), 0};
@@ -315,13 +320,14 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         if ((r & 2) && !transB) continue;
         const bool to_tn = r == tn_r;
         if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS && !to_tn) continue;
-        const unsigned long long need = ((r & 1) ? static_cast<unsigned long long>(K) * ((M + 31ULL) / 32 * 32) : 0) +
-                                        ((r & 2) ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
+        const unsigned long long need =
+            ((r & 1) ? static_cast<unsigned long long>(nA) * K * ((M + 31ULL) / 32 * 32) : 0) +
+            ((r & 2) ? static_cast<unsigned long long>(nB) * K * ((N + 31ULL) / 32 * 32) : 0);
         if (need > h->rl_floats) continue;
         double c;
         const int v = best_variant(op_after(transA, transB, r, M, N, &kM, &kN), kM, kN, &c);
-        if (r & 1) c += transpose_cost(M, K);
-        if (r & 2) c += transpose_cost(N, K);
+        if (r & 1) c += transpose_cost(M, K, nA);
+        if (r & 2) c += transpose_cost(N, K, nB);
         if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || c < best_cost * 0.99) {
             best_cost = c;
             best = Fp32Plan{v, r};
@@ -683,40 +689,41 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     }
 
     // FP32 SIMT kernels: the variant, and the operands first transposed into
-    // the re-layout workspace (batch 1 only).
+    // the re-layout workspace (one copy per batch matrix, or one for an
+    // operand shared by the batch).
     int relayout = 0;
     const float *eA = A, *eB = B;
     int elda = lda, eldb = ldb, etA = transA, etB = transB;
+    long long esA = strideA, esB = strideB;
     if (variant != SGEMM_VARIANT_GENERIC) {
-        if (batch == 1) {
-            const Fp32Plan p = plan_fp32(h, transA, transB, M, N, K, variant);
-            variant = p.variant;
-            relayout = p.relayout;
-        } else if (variant == SGEMM_VARIANT_AUTO) {
-            int kM, kN;
-            const int op0 = op_after(transA, transB, 0, M, N, &kM, &kN);
-            variant = choose_variant(h, kM, kN, K, batch, op0);
-        }
+        const Fp32Plan p = plan_fp32(h, transA, transB, M, N, K, batch, strideA, strideB, variant);
+        variant = p.variant;
+        relayout = p.relayout;
     }
     int launches = 0;
+    size_t a_copy_floats = 0;
     if (relayout & 1) {  // A (stored M x K) -> A^T stored K x M
-        float *dst = h->d_rl;
-        const int ld = round32(M);
-        const int rc = from_cuda(sg::launch_transpose(A, M, K, lda, dst, ld, stream));
+        const int ld = round32(M), n = strideA == 0 ? 1 : batch;
+        const long long per = static_cast<long long>(K) * ld;
+        const int rc = from_cuda(sg::launch_transpose(A, M, K, lda, h->d_rl, ld, stream, n, strideA, per));
         if (rc != SGEMM_OK) return rc;
-        eA = dst;
+        eA = h->d_rl;
         elda = ld;
         etA = 1;
+        esA = n > 1 ? per : 0;
+        a_copy_floats = static_cast<size_t>(n) * per;
         ++launches;
     }
     if (relayout & 2) {  // B (stored N x K) -> B^T stored K x N, after A^T if both
-        float *dst = h->d_rl + ((relayout & 1) ? static_cast<size_t>(K) * round32(M) : 0);
-        const int ld = round32(N);
-        const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream));
+        float *dst = h->d_rl + a_copy_floats;
+        const int ld = round32(N), n = strideB == 0 ? 1 : batch;
+        const long long per = static_cast<long long>(K) * ld;
+        const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream, n, strideB, per));
         if (rc != SGEMM_OK) return rc;
         eB = dst;
         eldb = ld;
         etB = 0;
+        esB = n > 1 ? per : 0;
         ++launches;
     }
 
@@ -725,8 +732,10 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     sg::GemmArgs k = g;
     k.A = eA;
     k.lda = elda;
+    k.sA = esA;
     k.B = eB;
     k.ldb = eldb;
+    k.sB = esB;
     k.transA = etA;
     k.transB = etB;
     int op = etA ? (etB ? sg::kTmaOpNN : sg::kTmaOpTN) : (etB ? sg::kTmaOpNT : sg::kTmaOpNN);
@@ -735,10 +744,10 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         k.N = M;
         k.A = eB;
         k.lda = eldb;
-        k.sA = strideB;
+        k.sA = esB;
         k.B = eA;
         k.ldb = elda;
-        k.sB = strideA;
+        k.sB = esA;
         k.c_trans = 1;
         k.vec_c = false;
     }
@@ -943,7 +952,7 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
                h->math_mode == SGEMM_MATH_FP32 && aligned16(dA) && aligned16(dB) && (lda % 4) == 0 &&
                (ldb % 4) == 0 && (h->pinned == SGEMM_VARIANT_AUTO || is_tma_variant(h->pinned)) &&
                static_cast<unsigned long long>(K) * ((nr + 31ULL) / 32 * 32) <= h->rl_floats &&
-               (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || (plan_fp32(h, 0, 0, nr, N, K, h->pinned).relayout & 1));
+               (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || (plan_fp32(h, 0, 0, nr, N, K, 1, 0, 0, h->pinned).relayout & 1));
     };
     // Column blocks of the first panel follow B's chunks: 1, 1, then 2 chunks
     // at a time (the first blocks start as soon as their chunk lands; later

@@ -140,15 +140,19 @@ __global__ void __launch_bounds__(256) sgemm_scale_kernel(const GemmArgs g) {
     }
 }
 
-// dst[c][r] = src[r][c] for r < rows, c < cols; one 64 x 64 tile per CTA
-// (1-D grid, tiles row-major over the source), 256 threads as 8 rows of 32
+// dst[c][r] = src[r][c] for r < rows, c < cols, matrix b of a batch at
+// src + b * sstride and dst + b * dstride (grid y); one 64 x 64 tile per CTA
+// (grid x, tiles row-major over the source), 256 threads as 8 rows of 32
 // lanes.  Each thread issues its 16 loads before the barrier, so a CTA has
 // 16 KiB in flight; 8 CTAs fit on an SM.
 constexpr int kTrTile = 64;
 
 __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict__ src, int rows, int cols,
-                                                        long long lds, float *__restrict__ dst, long long ldd) {
+                                                        long long lds, long long sstride, float *__restrict__ dst,
+                                                        long long ldd, long long dstride) {
     __shared__ float t[kTrTile][kTrTile + 1];
+    src += blockIdx.y * sstride;
+    dst += blockIdx.y * dstride;
     const int tiles_c = (cols + kTrTile - 1) / kTrTile;
     const int r0 = static_cast<int>(blockIdx.x / tiles_c) * kTrTile;
     const int c0 = static_cast<int>(blockIdx.x % tiles_c) * kTrTile;
@@ -250,10 +254,11 @@ cudaError_t launch_scale(const GemmArgs &g, cudaStream_t stream) {
 }
 
 cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, float *dst, int ldd,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int batch, long long sstride, long long dstride) {
     const long long tiles = 1LL * ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
-    if (tiles > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    transpose_kernel<<<static_cast<unsigned>(tiles), 256, 0, stream>>>(src, rows, cols, lds, dst, ldd);
+    if (tiles > 0x7fffffffLL || batch < 1 || batch > 65535) return cudaErrorInvalidConfiguration;
+    transpose_kernel<<<dim3(static_cast<unsigned>(tiles), batch), 256, 0, stream>>>(src, rows, cols, lds, sstride,
+                                                                                   dst, ldd, dstride);
     return cudaGetLastError();
 }
 

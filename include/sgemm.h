@@ -114,9 +114,11 @@ typedef enum {
     SGEMM_MATH_3XTF32 = 1
 } sgemm_math_mode_t;
 
-/* Operand re-layout of the FP32 SIMT path (sgemm_run, sgemm_run_ex with
- * batch 1, TMA-eligible operands; the tensor-core variants' copies into the
- * NN layout use the same workspace and are off with SGEMM_RELAYOUT_OFF).  On GB300 the SIMT kernel's main loop is
+/* Operand re-layout of the FP32 SIMT path (sgemm_run, sgemm_run_ex, any
+ * batch, TMA-eligible operands; the tensor-core variants' copies into the NN
+ * layout use the same workspace and are off with SGEMM_RELAYOUT_OFF).  A
+ * strided batch is copied matrix by matrix (an operand with batch stride 0
+ * once), each copy in its own slot of the workspace.  On GB300 the SIMT kernel's main loop is
  * fastest with A stored K x M and B stored K x N (transA = 1, transB = 0:
  * one 16-byte shared-memory load then gives one k of four rows of A).  The
  * library may therefore first copy A stored M x K, or B stored N x K,
@@ -271,8 +273,9 @@ int sgemm_last_relayout(sgemm_handle_t h);
 /* Size of the handle's re-layout workspace in floats (0 if it could not be
  * allocated, and then no operand is re-laid out); -1 if `h` is not a live
  * handle.  Transposed copies are stored with leading dimensions rounded up
- * to a multiple of 32 floats: A needs K * ceil32(M) floats, B K * ceil32(N),
- * both together the sum. */
+ * to a multiple of 32 floats: A needs K * ceil32(M) floats per batch matrix,
+ * B K * ceil32(N), both together the sum (the tensor-core variants' copies:
+ * M * ceil32(K) for A, K * ceil32(N) for B). */
 int64_t sgemm_relayout_capacity(sgemm_handle_t h);
 
 /* The variant the handle's last successful sgemm_run enqueued (an

@@ -136,12 +136,53 @@ def test_launch_count(handle, mode):
         assert sgemm.sgemm_last_launches(handle) == copies + 1
 
 
-def test_batched_and_generic_calls_are_not_relaid_out(handle, mode):
-    mode(V.RELAYOUT_ALWAYS)
-    p = ExProblem(0, 0, 100, 136, 72, batch=3, seed=7, pad=(4, 4, 4), mult4=True)
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_always_strided_batch(handle, mode, op):
+    """Strided batches with gaps between the matrices: each batch matrix of
+    a copied operand is transposed into its own slot of the workspace (one
+    launch for the whole batch) and the TN kernel reads them through a 3-D
+    tensor map."""
+    mode(V.RELAYOUT_ALWAYS, V.VARIANT_TMA_64x64)
+    p = ExProblem(op[0], op[1], 100, 136, 72, batch=3, seed=7, beta=0.25, pad=(4, 4, 4), gap=(8, 4, 12), mult4=True)
     C, bufs = p.run(handle)
     p.check(C, bufs)
-    assert sgemm.sgemm_last_relayout(handle) == 0
+    assert sgemm.sgemm_last_relayout(handle) == TO_TN[op]
+    assert sgemm.sgemm_last_launches(handle) == 1 + bin(TO_TN[op]).count("1")
+
+
+def test_always_batch_with_shared_operand(handle, mode):
+    """strideA = 0 (one A for every product): A is copied once and the copy
+    is shared, as the original was."""
+    mode(V.RELAYOUT_ALWAYS, V.VARIANT_TMA_128x128)
+    p = ExProblem(0, 1, 96, 80, 64, batch=4, seed=9, alpha=0.5, beta=1.0, pad=(4, 4, 4), gap=(0, 8, 4), mult4=True)
+    p.sA = 0
+    p.A = p.A[:p.ar * p.lda + 16].copy()
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_relayout(handle) == 3
+
+
+def test_batched_bits_match_unbatched(handle, mode):
+    """A copied batch gives, matrix by matrix, the bits of the same products
+    run one at a time without copies (same tile variant; K = 64 is two K
+    steps, too few for the single products' last wave to be split)."""
+    M, N, K = 130, 200, 64
+    mode(V.RELAYOUT_ALWAYS, V.VARIANT_TMA_64x64)
+    p = ExProblem(0, 0, M, N, K, batch=3, seed=13, pad=(4, 4, 4), gap=(8, 4, 12), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    mode(V.RELAYOUT_OFF, V.VARIANT_TMA_64x64)
+    for b in range(3):
+        q = ExProblem(0, 0, M, N, K, batch=1, seed=99, pad=(4, 4, 4), mult4=True)
+        q._view(q.A, 0, q.ar, q.ac, q.lda)[:] = p._view(p.A, b * p.sA, p.ar, p.ac, p.lda)
+        q._view(q.B, 0, q.br, q.bc, q.ldb)[:] = p._view(p.B, b * p.sB, p.br, p.bc, p.ldb)
+        Cq, _ = q.run(handle)
+        assert sgemm.sgemm_last_variant(handle) == (V.VARIANT_TMA_64x64, 1)
+        assert np.array_equal(p.c_view(C, b).view(np.uint32), q.c_view(Cq, 0).view(np.uint32))
+
+
+def test_generic_calls_are_not_relaid_out(handle, mode):
+    mode(V.RELAYOUT_ALWAYS)
     p = ExProblem(0, 0, 100, 136, 72, batch=1, seed=8, pad=(1, 4, 4))  # lda odd: generic
     C, bufs = p.run(handle)
     p.check(C, bufs)
