@@ -161,16 +161,16 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
 }
 
-// Tail plan for the whole-tile variants.  With T tiles and P resident CTA
-// slots, T = full*P + rem: the first full*P tiles run whole (complete waves)
+// Tail plan for the whole-tile variants.  With T tiles (of every batch
+// entry) and P resident CTA slots, T = full*P + rem: the first full*P tiles run whole (complete waves)
 // and the K steps of the rem tiles of the last, partly empty wave are shared
 // evenly by G stream-K CTAs (G <= P, at least 2 K steps each, within the
 // workspace), so the last wave keeps every slot busy for rem*kt/G steps
 // instead of leaving P - rem slots idle for a whole tile.  Used when G is at
 // least 1.25 rem (less would save little over whole tiles).
-void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K,
+void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch,
                sg::SplitK *sk) {
-    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn);
+    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;
     const long long kt = cdiv(K, sh.bk);
     *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
     const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[variant]);
@@ -196,7 +196,7 @@ int splits_of(const sg::SplitK &sk, int tiles) {
 // kt steps; a stream-K part takes ceil(T/G) steps plus its fixup (storing
 // and summing the parts: measured at about 15 us for the 128-row tiles and 2
 // us for 64 x 64, and 2 us for the second launch); an unsplit partial wave
-// takes kt steps.  A batch multiplies the tiles; batched calls are not split.
+// takes kt steps.  A batch multiplies the tiles (and shares the tail plan).
 double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
                     sg::SplitK *plan) {
     sg::TmaShape sh;
@@ -220,12 +220,7 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
         if (plan->sk_ctas == 0) return 1e300;  // runs as the whole-tile 64 x 64 variant
         return wave(plan->sk_ctas, std::ceil(tiles * kt / plan->sk_ctas)) + fixup;
     }
-    if (batch > 1) {
-        *plan = sg::SplitK{cdiv(M, sh.bm) * cdiv(N, sh.bn), 0, nullptr, nullptr};
-    } else {
-        sg::TmaShape shape = sh;
-        plan_tail(h, variant, shape, M, N, K, plan);
-    }
+    plan_tail(h, variant, sh, M, N, K, batch, plan);
     const double full = std::floor(tiles / P), rem = tiles - full * P;
     double t = full * kt * t_step;
     if (plan->sk_ctas > 0)
@@ -761,8 +756,8 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
             if (batch == 1) plan_splits(h, k.M, k.N, K, &sk);
             if (sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
-        } else if (batch == 1) {
-            plan_tail(h, variant, sh, k.M, k.N, K, &sk);
+        } else {
+            plan_tail(h, variant, sh, k.M, k.N, K, batch, &sk);
         }
         const bool a_ok = op == sg::kTmaOpTN
             ? encode_operand(&tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -784,7 +779,7 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     const int rc = from_cuda(sg::launch_tma_op(op, variant, k, tmA, tmB, sk, h->smem_override, stream));
     if (rc == SGEMM_OK) {
         h->last_variant = variant;
-        h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn));
+        h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn) * batch);
         // transposes, then the whole-tile waves and the stream-K CTAs
         h->last_launches = launches + (sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1);
         h->last_relayout = relayout;

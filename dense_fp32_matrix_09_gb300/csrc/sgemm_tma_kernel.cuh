@@ -61,10 +61,11 @@
 //    transposed runs as the NN kernel on the swapped operands (C^T = B_s A_s,
 //    with B_s the stored N x K matrix and A_s the stored K x M one) with an
 //    epilogue that writes the tile transposed (GemmArgs::c_trans).
-//  * Strided batches: grid y is the batch index; an operand with a nonzero
-//    batch stride is described by a 3-D tensor map (batch outermost), one
-//    with stride 0 by a 2-D map shared by all products, and C of product b
-//    starts at C + b * strideC.
+//  * Strided batches: the tiles of all products form one sequence, product
+//    by product (so complete waves and the stream-K tail span products); an
+//    operand with a nonzero batch stride is described by a 3-D tensor map
+//    (batch outermost), one with stride 0 by a 2-D map shared by all
+//    products, and C of product b starts at C + b * strideC.
 //
 // Every wait is bounded (device_common.cuh); on a timeout the kernel records
 // it in the status word and returns without writing C.
@@ -412,19 +413,23 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
+    const int tiles_per = tiles_m * tiles_n;  // tiles of one batch entry
     const int kt = (g.K + C::BK - 1) / C::BK;
     // This CTA's work, as one or two segments (a tile and a K range of it).
-    // CTAs below sk.dp_tiles (all CTAs without SPLIT) take one whole tile.
-    // Stream-K CTA q takes iterations [floor(q*T/G), floor((q+1)*T/G)) of the
-    // T = (tiles - dp_tiles) * kt iterations of the remaining tiles, taken
-    // tile by tile (G = sk.sk_ctas); the host keeps G >= the number of those
-    // tiles, so a range is at most kt long and touches at most two tiles.
+    // Tiles are numbered batch entry by batch entry (tile t is tile
+    // t % tiles_per of entry t / tiles_per).  CTAs below sk.dp_tiles (all
+    // CTAs without SPLIT) take one whole tile.  Stream-K CTA q takes
+    // iterations [floor(q*T/G), floor((q+1)*T/G)) of the T = (tiles -
+    // dp_tiles) * kt iterations of the remaining tiles, taken tile by tile
+    // (G = sk.sk_ctas); the host keeps G >= the number of those tiles, so a
+    // range is at most kt long and touches at most two tiles (possibly of two
+    // batch entries).
     const int cta = static_cast<int>(blockIdx.x) + (SPLIT ? sk.cta0 : 0);
     int tile0 = cta, k00 = 0, n0it = kt, n_iter = kt, q = -1;
     long long T = 0;
     if (SPLIT && cta >= sk.dp_tiles) {
         q = cta - sk.dp_tiles;
-        T = static_cast<long long>(tiles_m * tiles_n - sk.dp_tiles) * kt;
+        T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
         const long long b = q * T / sk.sk_ctas, e = (q + 1) * T / sk.sk_ctas;
         const int tl = static_cast<int>(b / kt);
         tile0 = sk.dp_tiles + tl;
@@ -432,8 +437,8 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         n_iter = static_cast<int>(e - b);  // >= 1: the host keeps G <= T
         n0it = min(n_iter, kt - k00);      // the rest (if any) is the next tile from k = 0
     }
-    // batch entry of this CTA; an operand with a batch stride has a 3-D map
-    const int bat = blockIdx.y;
+    // batch entry of the first segment; an operand with a batch stride has a 3-D map
+    const int bat = tile0 / tiles_per;
     const bool a3 = g.batch > 1 && g.sA != 0, b3 = g.batch > 1 && g.sB != 0;
     float *Cb = g.C + static_cast<long long>(bat) * g.sC;
 
@@ -450,26 +455,27 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     int m0w, n0w;  // the first segment's tile
     {
         int tm, tn;
-        tile_coords(tile0, tiles_m, tiles_n, group_m, tm, tn);
+        tile_coords(tile0 % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
         m0w = tm * C::BM;
         n0w = tn * C::BN;
     }
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
-        int m0 = m0w, n0 = n0w, kc = (k00 + t) * C::BK;
+        int m0 = m0w, n0 = n0w, kc = (k00 + t) * C::BK, bt = bat;
         if (SPLIT && t >= n0it) {  // second segment: the next tile from k = 0
             int tm, tn;
-            tile_coords(tile0 + 1, tiles_m, tiles_n, group_m, tm, tn);
+            tile_coords((tile0 + 1) % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
             m0 = tm * C::BM;
             n0 = tn * C::BN;
             kc = (t - n0it) * C::BK;
+            bt = (tile0 + 1) / tiles_per;
         }
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
         const int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
         const int bx = OP == kOpNT ? kc : n0, by = OP == kOpNT ? n0 : kc;
-        if (a3) tma_load_3d(sA + s * C::kABytes, &tmA, &full[s], ax, ay, bat);
+        if (a3) tma_load_3d(sA + s * C::kABytes, &tmA, &full[s], ax, ay, bt);
         else tma_load_2d(sA + s * C::kABytes, &tmA, &full[s], ax, ay);
-        if (b3) tma_load_3d(sB + s * C::kBBytes, &tmB, &full[s], bx, by, bat);
+        if (b3) tma_load_3d(sB + s * C::kBBytes, &tmB, &full[s], bx, by, bt);
         else tma_load_2d(sB + s * C::kBBytes, &tmB, &full[s], bx, by);
     };
     int issued = 0;
@@ -580,9 +586,9 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (!((split_last >> sg2) & 1)) continue;
                 const int tile = tile0 + sg2, tl = tile - sk.dp_tiles;
                 int tm, tn;
-                tile_coords(tile, tiles_m, tiles_n, group_m, tm, tn);
+                tile_coords(tile % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
                 __threadfence();
-                sk_reduce_epilogue<C, OP>(g, sk.ws, Cb, tl,
+                sk_reduce_epilogue<C, OP>(g, sk.ws, g.C + static_cast<long long>(tile / tiles_per) * g.sC, tl,
                                           sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas),
                                           sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas),
                                           tm * C::BM, tn * C::BN);
@@ -620,16 +626,18 @@ int ctas_per_sm_one() {
 
 // Whole tiles only when sk.sk_ctas == 0; otherwise the hybrid grid: dp_tiles
 // whole-tile CTAs, then sk_ctas stream-K CTAs sharing the remaining tiles'
-// K steps.  Grid y runs over the batch (stream-K plans are for batch 1 only).
+// K steps.  One-dimensional grids over the tiles of every batch entry, entry
+// by entry.
 template <class C, int OP>
 cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, const SplitK &sk,
                        int smem_override, cudaStream_t stream) {
-    const int tiles = ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN);
+    const long long tiles =
+        1LL * ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN) * g.batch;
     const int smem = smem_override > 0 ? smem_override : smem_bytes<C, OP>();
-    if (g.batch < 1 || g.batch > 65535 || (sk.sk_ctas > 0 && g.batch != 1)) return cudaErrorInvalidValue;
+    if (g.batch < 1 || g.batch > 65535 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     if (sk.sk_ctas <= 0) {
-        sgemm_tma_kernel<C, false, OP><<<dim3(tiles, g.batch), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
-                                                                                           kGroupM);
+        sgemm_tma_kernel<C, false, OP><<<static_cast<unsigned>(tiles), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
+                                                                                                   kGroupM);
     } else {
         // the complete waves with the whole-tile kernel, then the stream-K CTAs
         if (sk.dp_tiles > 0)

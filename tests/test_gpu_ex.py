@@ -295,3 +295,28 @@ def test_batch_with_more_tiles_than_slots(handle, variant, op):
     C, bufs = p.run(handle)
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TMA_64x64
+
+
+@pytest.mark.parametrize("v", TMA_VARIANTS[:3], ids=lambda v: sgemm.variant_name(v))
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_batch_with_stream_k_tail(handle, variant, op, v):
+    """The tiles of all batch matrices form one sequence: the partial last
+    wave is shared by stream-K CTAs whose K ranges cross from one batch
+    matrix into the next (3 ragged 300 x 520 x 270 products)."""
+    variant(v)
+    p = ExProblem(op[0], op[1], 300, 520, 270, batch=3, seed=201, alpha=1.25, beta=-0.75, pad=(4, 4, 4),
+                  gap=(8, 4, 12), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    ran, splits = sgemm.sgemm_last_variant(handle)
+    assert ran == v and splits > 1, (ran, splits)
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_batch_with_stream_k_tail_integer_exact(handle, variant, op):
+    variant(V.VARIANT_TMA_128x128)
+    p = ExProblem(op[0], op[1], 200, 136, 333, batch=4, seed=211, kind="integers", beta=1.0, pad=(4, 4, 4),
+                  gap=(4, 8, 4), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs, exact=True)
+    assert sgemm.sgemm_last_variant(handle)[1] > 1
