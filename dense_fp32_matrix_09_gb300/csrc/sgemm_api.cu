@@ -191,7 +191,9 @@ int splits_of(const sg::SplitK &sk, int tiles) {
 // ranking matters).  A K step of one CTA takes bm*bn*32 FMAs at the
 // variant's main-loop efficiency measured on GB300 (fraction of FP32 peak
 // with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
-// 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63), shared with the other
+// 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63; the TN 128 x 128 tile
+// depends on K: 0.86 up to K = 5120, where it beat 128 x 256 by 1-3 % on
+// seven shapes, and 0.78 from K = 6144, where it lost 3-14 %), shared with the other
 // CTAs resident on its SM (fewer in a thin last wave).  Complete waves take
 // kt steps; a stream-K part takes ceil(T/G) steps plus its fixup (storing
 // and summing the parts: measured at about 15 us for the 128-row tiles and 2
@@ -203,7 +205,7 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
     if (!sg::tma_shape(variant, &sh)) return 1e300;
     static const double kEff[3][3] = {{0.81, 0.80, 0.73}, {0.84, 0.84, 0.80}, {0.76, 0.75, 0.63}};
     const int vi = variant == SGEMM_VARIANT_TMA_128x256 ? 0 : variant == SGEMM_VARIANT_TMA_128x128 ? 1 : 2;
-    const double eff = kEff[op][vi];
+    const double eff = (op == sg::kTmaOpTN && vi == 1) ? (K <= 5120 ? 0.86 : 0.78) : kEff[op][vi];
     const double cps = std::max(1, h->ctas_per_sm[variant]);
     const double sms = h->num_sms, P = sms * cps;
     const double t_step = static_cast<double>(sh.bm) * sh.bn * sh.bk * cps / (128.0 * eff * 2000.0);

@@ -49,7 +49,8 @@ def test_capture_and_replay_fp32_calls(handle):
     with torch.cuda.graph(graph, stream=s):
         for c, (A, B, C) in zip(cfgs, bufs):
             sgemm.sgemm_run(handle, c.M, c.N, c.K, c.alpha, A, c.lda, B, c.ldb, c.beta, C, c.ldc, s)
-            launches.append(sgemm.sgemm_last_launches(handle))
+            # GEMM launches: the call's launches minus its operand copies
+            launches.append(sgemm.sgemm_last_launches(handle) - bin(sgemm.sgemm_last_relayout(handle)).count("1"))
     assert 2 in launches  # the stream-K two-launch form was captured
     for _ in range(2):
         for _, _, C in bufs:
