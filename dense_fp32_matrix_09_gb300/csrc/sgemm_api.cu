@@ -191,7 +191,8 @@ int splits_of(const sg::SplitK &sk, int tiles) {
 // ranking matters).  A K step of one CTA takes bm*bn*32 FMAs at the
 // variant's main-loop efficiency measured on GB300 (fraction of FP32 peak
 // with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
-// 0.73; TN: 0.84, 0.84, 0.80; NT: 0.76, 0.75, 0.63; the TN 128 x 128 tile
+// 0.73, 256 x 128 0.815; TN: 0.84, 0.84, 0.80, 0.87; NT: 0.76, 0.75, 0.55
+// (from 1024^3, where NT ran 1.34x slower than NN), 0.73; the TN 128 x 128 tile
 // depends on K: 0.86 up to K = 5120, where it beat 128 x 256 by 1-3 % on
 // seven shapes, and 0.78 from K = 6144, where it lost 3-14 %), shared with the other
 // CTAs resident on its SM (fewer in a thin last wave).  Complete waves take
@@ -203,8 +204,13 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
                     sg::SplitK *plan) {
     sg::TmaShape sh;
     if (!sg::tma_shape(variant, &sh)) return 1e300;
-    static const double kEff[3][3] = {{0.81, 0.80, 0.73}, {0.84, 0.84, 0.80}, {0.76, 0.75, 0.63}};
-    const int vi = variant == SGEMM_VARIANT_TMA_128x256 ? 0 : variant == SGEMM_VARIANT_TMA_128x128 ? 1 : 2;
+    // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
+    static const double kEff[3][4] = {{0.81, 0.80, 0.73, 0.815}, {0.84, 0.84, 0.80, 0.87},
+                                      {0.76, 0.75, 0.55, 0.73}};
+    const int vi = variant == SGEMM_VARIANT_TMA_128x256   ? 0
+                   : variant == SGEMM_VARIANT_TMA_128x128 ? 1
+                   : variant == SGEMM_VARIANT_TMA_256x128 ? 3
+                                                          : 2;
     const double eff = (op == sg::kTmaOpTN && vi == 1) ? (K <= 5120 ? 0.86 : 0.78) : kEff[op][vi];
     const double cps = std::max(1, h->ctas_per_sm[variant]);
     const double sms = h->num_sms, P = sms * cps;
@@ -235,10 +241,10 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
 // larger tile (listed first).
 int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int op = sg::kTmaOpNN) {
-    int best = SGEMM_VARIANT_TMA_128x256;
+    int best = SGEMM_VARIANT_TMA_256x128;
     double best_cost = 1e300;
-    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
-                  SGEMM_VARIANT_TMA_64x64_SPLITK}) {
+    for (int v : {SGEMM_VARIANT_TMA_256x128, SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128,
+                  SGEMM_VARIANT_TMA_64x64, SGEMM_VARIANT_TMA_64x64_SPLITK}) {
         sg::SplitK plan;
         const double c = variant_cost(h, v, M, N, K, batch, op, &plan);
         if (c < best_cost * 0.999) {
@@ -361,6 +367,7 @@ const char *sgemm_variant_name(int v) {
     switch (v) {
         case SGEMM_VARIANT_AUTO: return "auto";
         case SGEMM_VARIANT_TMA_128x256: return "tma_128x256";
+        case SGEMM_VARIANT_TMA_256x128: return "tma_256x128";
         case SGEMM_VARIANT_TMA_128x128: return "tma_128x128";
         case SGEMM_VARIANT_TMA_64x64: return "tma_64x64";
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return "tma_64x64_splitk";
@@ -424,8 +431,8 @@ int sgemm_create(sgemm_handle_t *out) {
     if (prop.major != 10 || prop.minor != 3) return SGEMM_ERR_UNSUPPORTED_DEVICE;
     if (!load_encoder()) return SGEMM_ERR_CUDA;
     int occupancy[SGEMM_VARIANT_COUNT_] = {};
-    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_128x128, SGEMM_VARIANT_TMA_64x64,
-                  SGEMM_VARIANT_TMA_64x64_SPLITK}) {
+    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_256x128, SGEMM_VARIANT_TMA_128x128,
+                  SGEMM_VARIANT_TMA_64x64, SGEMM_VARIANT_TMA_64x64_SPLITK}) {
         if (sg::tma_prepare(v) != cudaSuccess) return SGEMM_ERR_CUDA;
         occupancy[v] = sg::tma_ctas_per_sm(v);
         if (occupancy[v] < 1) return SGEMM_ERR_CUDA;

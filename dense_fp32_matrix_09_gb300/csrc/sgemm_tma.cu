@@ -8,6 +8,7 @@ namespace sg {
 bool tma_shape(int variant, TmaShape *out) {
     switch (variant) {
         case SGEMM_VARIANT_TMA_128x256: *out = shape_of<CfgL>(); return true;
+        case SGEMM_VARIANT_TMA_256x128: *out = shape_of<CfgX>(); return true;
         case SGEMM_VARIANT_TMA_128x128: *out = shape_of<CfgM>(); return true;
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: *out = shape_of<CfgS>(); return true;

@@ -110,11 +110,13 @@ struct Cfg {
 constexpr int kGroupM = 8;
 
 using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
+using CfgX = Cfg<256, 128, 4, 4, 8, 8, 4, 1>;    // SGEMM_VARIANT_TMA_256x128 (16 warps, 128 registers)
 using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
 using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 3>;      // SGEMM_VARIANT_TMA_64x64 (+ stream-K variant)
 // NT adds two B-sized transpose buffers, so its two larger tiles keep fewer
 // stages within the shared memory of one (128 x 256) or two (128 x 128) CTAs.
 using CfgLnt = Cfg<128, 256, 2, 4, 8, 16, 3, 1>;
+using CfgXnt = Cfg<256, 128, 4, 4, 8, 8, 3, 1>;
 using CfgMnt = Cfg<128, 128, 2, 4, 8, 8, 2, 2>;
 
 // Dynamic shared memory of the kernel for layout OP.
@@ -306,9 +308,11 @@ __device__ __forceinline__ void mainloop_tn(float (&acc)[C::TM][C::TN], const ui
 template <class C>
 __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, int tid) {
     constexpr int kBlocks = C::BN * (C::BK / 4) / 4;
-    static_assert(kBlocks % C::kConsumers == 0, "whole blocks per thread");
+    static_assert(kBlocks % C::kConsumers == 0 || C::kConsumers % kBlocks == 0, "whole blocks per thread");
+    constexpr int kRounds = kBlocks >= C::kConsumers ? kBlocks / C::kConsumers : 1;
+    if (kBlocks < C::kConsumers && tid >= kBlocks) return;  // more threads than blocks: the rest idle
 #pragma unroll
-    for (int u = 0; u < kBlocks / C::kConsumers; ++u) {
+    for (int u = 0; u < kRounds; ++u) {
         const int id = tid + u * C::kConsumers;
         const int c = id & 7, nq = id >> 3;
         float4 v[4];
@@ -654,12 +658,15 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
 template <int OP>
 using LCfg = typename std::conditional<OP == kOpNT, CfgLnt, CfgL>::type;
 template <int OP>
+using XCfg = typename std::conditional<OP == kOpNT, CfgXnt, CfgX>::type;
+template <int OP>
 using MCfg = typename std::conditional<OP == kOpNT, CfgMnt, CfgM>::type;
 
 template <int OP>
 cudaError_t prepare_op(int variant) {
     switch (variant) {
         case SGEMM_VARIANT_TMA_128x256: return prepare_one<LCfg<OP>, OP>();
+        case SGEMM_VARIANT_TMA_256x128: return prepare_one<XCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_128x128: return prepare_one<MCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return prepare_one<CfgS, OP>();
@@ -671,6 +678,7 @@ template <int OP>
 int ctas_per_sm_op(int variant) {
     switch (variant) {
         case SGEMM_VARIANT_TMA_128x256: return ctas_per_sm_one<LCfg<OP>, OP>();
+        case SGEMM_VARIANT_TMA_256x128: return ctas_per_sm_one<XCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<MCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return ctas_per_sm_one<CfgS, OP>();
@@ -684,6 +692,8 @@ cudaError_t launch_op(int variant, const GemmArgs &g, const CUtensorMap &tmA, co
     switch (variant) {
         case SGEMM_VARIANT_TMA_128x256:
             return launch_one<LCfg<OP>, OP>(g, tmA, tmB, sk, smem_override, stream);
+        case SGEMM_VARIANT_TMA_256x128:
+            return launch_one<XCfg<OP>, OP>(g, tmA, tmB, sk, smem_override, stream);
         case SGEMM_VARIANT_TMA_128x128:
             return launch_one<MCfg<OP>, OP>(g, tmA, tmB, sk, smem_override, stream);
         case SGEMM_VARIANT_TMA_64x64:

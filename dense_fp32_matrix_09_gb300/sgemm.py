@@ -37,6 +37,7 @@ VARIANT_TC_3XTF32 = 7
 VARIANT_TC_3XTF32_PAIR = 8
 VARIANT_TC_F16_PAIR = 9
 VARIANT_GENERIC_F16 = 10
+VARIANT_TMA_256x128 = 11
 MATH_FP32 = 0
 MATH_3XTF32 = 1
 IN_BF16 = 1
@@ -44,7 +45,7 @@ IN_F16 = 2
 RELAYOUT_AUTO = 0
 RELAYOUT_OFF = 1
 RELAYOUT_ALWAYS = 2
-GEMM_VARIANTS = (VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
+GEMM_VARIANTS = (VARIANT_TMA_256x128, VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
                  VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32, VARIANT_TC_3XTF32_PAIR)
 
 #: Every exported entry point of include/sgemm.h.

@@ -87,7 +87,9 @@ typedef enum {
                                         cores (kind::f16), FP32 accumulation, CTA pairs       */
     SGEMM_VARIANT_GENERIC_F16 = 10,  /* sgemm_run_mixed only: the generic variant on 16-bit
                                         inputs (any alignment)                                */
-    SGEMM_VARIANT_COUNT_ = 11
+    SGEMM_VARIANT_TMA_256x128 = 11,  /* TMA-fed SIMT, 256 x 128 CTA tile, 16 warps, 8 x 8 per
+                                        thread (fastest on large problems)                    */
+    SGEMM_VARIANT_COUNT_ = 12
     /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
      * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
      * for batch > 1, strideA, strideB) are multiples of 4; otherwise the

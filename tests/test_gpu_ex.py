@@ -203,7 +203,8 @@ def test_run_equals_run_ex_nn(handle):
     assert np.array_equal(dC.interior().view(np.uint32), C_ex.view(np.uint32))
 
 
-TMA_VARIANTS = (V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64, V.VARIANT_TMA_64x64_SPLITK)
+TMA_VARIANTS = (V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64,
+                V.VARIANT_TMA_64x64_SPLITK)
 
 
 @pytest.mark.parametrize("v", TMA_VARIANTS + (V.VARIANT_GENERIC,), ids=lambda v: sgemm.variant_name(v))
@@ -219,7 +220,7 @@ def test_op_variant_sweep(handle, variant, op, v):
                                                  else (v, V.VARIANT_TMA_64x64))
 
 
-@pytest.mark.parametrize("v", TMA_VARIANTS[:3], ids=lambda v: sgemm.variant_name(v))
+@pytest.mark.parametrize("v", TMA_VARIANTS[:4], ids=lambda v: sgemm.variant_name(v))
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)
 def test_op_batched_tma(handle, variant, op, v):
     """Strided batches on the TMA kernels (3-D tensor maps), ragged sizes."""
@@ -297,7 +298,7 @@ def test_batch_with_more_tiles_than_slots(handle, variant, op):
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TMA_64x64
 
 
-@pytest.mark.parametrize("v", TMA_VARIANTS[:3], ids=lambda v: sgemm.variant_name(v))
+@pytest.mark.parametrize("v", TMA_VARIANTS[:4], ids=lambda v: sgemm.variant_name(v))
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)
 def test_batch_with_stream_k_tail(handle, variant, op, v):
     """The tiles of all batch matrices form one sequence: the partial last

@@ -17,7 +17,7 @@ from tests.gpu_util import (DeviceBuf, check_untouched, max_abs_err, oracle_full
 pytestmark = pytest.mark.gpu
 
 V = sgemm
-TMA_VARIANTS = (V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64,
+TMA_VARIANTS = (V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64,
                 V.VARIANT_TMA_64x64_SPLITK)
 
 
@@ -306,8 +306,8 @@ def test_torch_tensor_interface(handle):
     assert float(np.max(np.abs(C.cpu().numpy().reshape(-1) - ref))) <= 1e-3
 
 
-@pytest.mark.parametrize("v", [V.VARIANT_TMA_128x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_64x64],
-                         ids=lambda v: sgemm.variant_name(v))
+@pytest.mark.parametrize("v", [V.VARIANT_TMA_128x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_256x128,
+                               V.VARIANT_TMA_64x64], ids=lambda v: sgemm.variant_name(v))
 def test_whole_waves_plus_split_tail(handle, variant, v):
     """Enough tiles for one or more complete waves plus a partial one: the
     complete waves run whole tiles and the tail tiles are split along K and
@@ -316,7 +316,7 @@ def test_whole_waves_plus_split_tail(handle, variant, v):
     import torch
     variant(v)
     bm, bn = {V.VARIANT_TMA_128x128: (128, 128), V.VARIANT_TMA_128x256: (128, 256),
-              V.VARIANT_TMA_64x64: (64, 64)}[v]
+              V.VARIANT_TMA_256x128: (256, 128), V.VARIANT_TMA_64x64: (64, 64)}[v]
     # 12*SMs + 16 tiles: with 1, 2, 3 or 4 CTAs per SM the last wave holds 16 tiles
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     tiles_m = 8

@@ -21,7 +21,8 @@ from tests.test_gpu_ex import OP_IDS, OPS, ExProblem
 pytestmark = pytest.mark.gpu
 
 V = sgemm
-TMA_VARIANTS = (V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64, V.VARIANT_TMA_64x64_SPLITK)
+TMA_VARIANTS = (V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64,
+                V.VARIANT_TMA_64x64_SPLITK)
 # operands copied to reach A stored K x M, B stored K x N: bit 0 A, bit 1 B
 TO_TN = {(0, 0): 1, (0, 1): 3, (1, 0): 0, (1, 1): 2}
 
