@@ -15,9 +15,12 @@
 //    TMA engine and the warps.  Thread 0 issues the loads: S tiles up front,
 //    then, at the start of step i, the refill of the stage that step i-1
 //    used, once every thread has released it (S-1 steps of look-ahead).  No
-//    warp is set aside for this: with 8 warps every SM sub-partition holds 2
-//    warps and each thread may use up to 255 registers, which the 128
-//    accumulators of the largest tile need.  TMA
+//    warp is set aside for this: the 128 x 256 tile's 8 warps need up to 255
+//    registers each for their 128 accumulators, and the 256 x 128 tile's 16
+//    warps fill all 128 registers a thread of a 512-thread CTA may have (64
+//    accumulators each; with 4 warps per SM sub-partition instead of 2, a
+//    warp waiting on a fixed-latency dependency leaves the FMA pipe to
+//    another, which makes it the faster tile on large problems).  TMA
 //    zero-fills every element outside [0,M) x [0,K) and [0,K) x [0,N), so
 //    ragged edges need no code in the main loop and padding cells of the
 //    leading dimensions are never read.
