@@ -313,10 +313,11 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         return v;
     };
     const int nA = strideA == 0 ? 1 : batch, nB = strideB == 0 ? 1 : batch;
-    int kM, kN;
+    int kM = 0, kN = 0;
     double best_cost;
-    Fp32Plan best{best_variant(op_after(transA, transB, 0, M, N, &kM, &kN), kM, kN, &best_cost), 0};
-    if (h->relayout_mode == SGEMM_RELAYOUT_OFF || h->d_rl == nullptr) return best;
+    const int op0 = op_after(transA, transB, 0, M, N, &kM, &kN);  // sets kM, kN before they are read
+    Fp32Plan best{best_variant(op0, kM, kN, &best_cost), 0};
+    if (h->relayout_mode == SGEMM_RELAYOUT_OFF || h->rl_floats == 0) return best;
     const int tn_r = (transA ? 0 : 1) | (transB ? 2 : 0);  // transposes that reach TN
     for (int r : {1, 2, 3}) {
         if ((r & 1) && transA) continue;  // only A stored M x K and B stored N x K are transposed
@@ -328,7 +329,8 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
             ((r & 2) ? static_cast<unsigned long long>(nB) * K * ((N + 31ULL) / 32 * 32) : 0);
         if (need > h->rl_floats) continue;
         double c;
-        const int v = best_variant(op_after(transA, transB, r, M, N, &kM, &kN), kM, kN, &c);
+        const int op_r = op_after(transA, transB, r, M, N, &kM, &kN);
+        const int v = best_variant(op_r, kM, kN, &c);
         if (r & 1) c += transpose_cost(M, K, nA);
         if (r & 2) c += transpose_cost(N, K, nB);
         if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || c < best_cost * 0.99) {
@@ -338,6 +340,82 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         }
     }
     return best;
+}
+
+// What a call with alpha != 0 and K > 0 runs: the kernel kind and variant,
+// the operand copies (bit 0: A copied transposed, bit 1: B), and for the TMA
+// kernels the operand layout, the M and N they see (swapped for A^T B^T) and
+// the whole-tile / stream-K plan.  No CUDA call: the same decisions are
+// reachable without a GPU through sgemm_debug_plan.
+constexpr int kPlanScale = 1, kPlanTensorCore = 2, kPlanGeneric = 3, kPlanTma = 4;
+
+struct CallPlan {
+    int kind = kPlanGeneric;
+    int variant = SGEMM_VARIANT_GENERIC;
+    int copies = 0;
+    int op = sg::kTmaOpNN;
+    int kM = 0, kN = 0;
+    sg::SplitK sk{0, 0, nullptr, nullptr};
+    int splits = 1;    // CTAs per stream-K tile (rounded up; 1 without)
+    int launches = 1;  // kernel launches the call enqueues
+};
+
+CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
+                   long long strideB, bool tma_ok) {
+    CallPlan p;
+    // The tensor-core kernels read A stored M x K and B stored K x N, batch 1;
+    // another layout reaches them through transposed copies of its stored-
+    // transposed operands in the re-layout workspace (A stored K x M -> M x K,
+    // B stored N x K -> K x N), when re-layout is not off and the copies fit.
+    const int tc_copy = (transA ? 1 : 0) | (transB ? 2 : 0);
+    const unsigned long long tc_need =
+        (transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0) +
+        (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
+    const bool tc_reachable = batch == 1 && (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF &&
+                                                              h->rl_floats > 0 && tc_need <= h->rl_floats));
+    int variant = h->pinned;
+    if (!tc_reachable && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
+        variant = SGEMM_VARIANT_AUTO;
+    if (variant == SGEMM_VARIANT_TC_F16_PAIR || variant == SGEMM_VARIANT_GENERIC_F16)
+        variant = SGEMM_VARIANT_AUTO;  // 16-bit-input variants: sgemm_run_mixed only
+    if (variant == SGEMM_VARIANT_AUTO) {
+        // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
+        // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
+        const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
+        if (tc_reachable && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
+            variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
+    }
+    if (!tma_ok || variant == SGEMM_VARIANT_GENERIC) return p;  // the generic kernel on the stored operands
+
+    if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
+        p.kind = kPlanTensorCore;
+        p.variant = variant;
+        p.copies = tc_copy;
+        p.launches = 1 + (tc_copy & 1) + ((tc_copy >> 1) & 1);
+        return p;
+    }
+
+    // FP32 SIMT kernels: the tile variant and the operands to copy transposed
+    const Fp32Plan fp = plan_fp32(h, transA, transB, M, N, K, batch, strideA, strideB, variant);
+    variant = fp.variant;
+    p.copies = fp.relayout;
+    p.op = op_after(transA, transB, fp.relayout, M, N, &p.kM, &p.kN);
+    sg::TmaShape sh;
+    sg::tma_shape(variant, &sh);
+    const int tiles = cdiv(p.kM, sh.bm) * cdiv(p.kN, sh.bn);
+    p.sk = sg::SplitK{tiles, 0, nullptr, nullptr};
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+        if (batch == 1) plan_splits(h, p.kM, p.kN, K, &p.sk);
+        if (p.sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
+    } else {
+        plan_tail(h, variant, sh, p.kM, p.kN, K, batch, &p.sk);
+    }
+    p.kind = kPlanTma;
+    p.variant = variant;
+    p.splits = splits_of(p.sk, tiles * batch);
+    // transposes, then the whole-tile waves and the stream-K CTAs
+    p.launches = (p.copies & 1) + ((p.copies >> 1) & 1) + (p.sk.sk_ctas > 0 && p.sk.dp_tiles > 0 ? 2 : 1);
+    return p;
 }
 
 }  // namespace
@@ -625,49 +703,25 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
 
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
                         (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
-    // The tensor-core kernels read A stored M x K and B stored K x N, batch 1;
-    // another layout reaches them through transposed copies of its stored-
-    // transposed operands in the re-layout workspace (A stored K x M -> M x K,
-    // B stored N x K -> K x N), when re-layout is not off and the copies fit.
-    const int tc_copy = (transA ? 1 : 0) | (transB ? 2 : 0);
-    const unsigned long long tc_need =
-        (transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0) +
-        (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
-    const bool tc_reachable = batch == 1 && (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF &&
-                                                              h->d_rl != nullptr && tc_need <= h->rl_floats));
-    int variant = h->pinned;
-    if (!tc_reachable && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
-        variant = SGEMM_VARIANT_AUTO;
-    if (variant == SGEMM_VARIANT_TC_F16_PAIR || variant == SGEMM_VARIANT_GENERIC_F16)
-        variant = SGEMM_VARIANT_AUTO;  // 16-bit-input variants: sgemm_run_mixed only
-    if (variant == SGEMM_VARIANT_AUTO) {
-        // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
-        // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
-        const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
-        if (tc_reachable && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
-            variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
-    }
-    if (!tma_ok) variant = SGEMM_VARIANT_GENERIC;
+    const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
 
-    if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
+    if (p.kind == kPlanTensorCore) {
         const float *tA_ = A, *tB_ = B;
-        int tlda = lda, tldb = ldb, launches = 0;
-        if (tc_copy & 1) {  // A stored K x M -> M x K
+        int tlda = lda, tldb = ldb;
+        if (p.copies & 1) {  // A stored K x M -> M x K
             const int ld = round32(K);
             const int rc = from_cuda(sg::launch_transpose(A, K, M, lda, h->d_rl, ld, stream));
             if (rc != SGEMM_OK) return rc;
             tA_ = h->d_rl;
             tlda = ld;
-            ++launches;
         }
-        if (tc_copy & 2) {  // B stored N x K -> K x N, after A's copy if both
-            float *dst = h->d_rl + ((tc_copy & 1) ? static_cast<size_t>(M) * round32(K) : 0);
+        if (p.copies & 2) {  // B stored N x K -> K x N, after A's copy if both
+            float *dst = h->d_rl + ((p.copies & 1) ? static_cast<size_t>(M) * round32(K) : 0);
             const int ld = round32(N);
             const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream));
             if (rc != SGEMM_OK) return rc;
             tB_ = dst;
             tldb = ld;
-            ++launches;
         }
         sg::GemmArgs gt = g;
         gt.A = tA_;
@@ -681,32 +735,25 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         if (!encode_2d(&tA, tA_, M, K, tlda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
             !encode_2d(&tB, tB_, K, N, tldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
             return SGEMM_ERR_CUDA;
-        const int rc = from_cuda(variant == SGEMM_VARIANT_TC_3XTF32
+        const int rc = from_cuda(p.variant == SGEMM_VARIANT_TC_3XTF32
                                      ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
                                      : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream));
         if (rc == SGEMM_OK) {
-            h->last_variant = variant;
-            h->last_launches = launches + 1;
-            h->last_relayout = tc_copy;
+            h->last_variant = p.variant;
+            h->last_launches = p.launches;
+            h->last_relayout = p.copies;
         }
         return rc;
     }
 
-    // FP32 SIMT kernels: the variant, and the operands first transposed into
-    // the re-layout workspace (one copy per batch matrix, or one for an
-    // operand shared by the batch).
-    int relayout = 0;
+    // FP32 SIMT kernels: operands first transposed into the re-layout
+    // workspace as planned (one copy per batch matrix, or one for an operand
+    // shared by the batch).
     const float *eA = A, *eB = B;
     int elda = lda, eldb = ldb, etA = transA, etB = transB;
     long long esA = strideA, esB = strideB;
-    if (variant != SGEMM_VARIANT_GENERIC) {
-        const Fp32Plan p = plan_fp32(h, transA, transB, M, N, K, batch, strideA, strideB, variant);
-        variant = p.variant;
-        relayout = p.relayout;
-    }
-    int launches = 0;
     size_t a_copy_floats = 0;
-    if (relayout & 1) {  // A (stored M x K) -> A^T stored K x M
+    if (p.copies & 1) {  // A (stored M x K) -> A^T stored K x M
         const int ld = round32(M), n = strideA == 0 ? 1 : batch;
         const long long per = static_cast<long long>(K) * ld;
         const int rc = from_cuda(sg::launch_transpose(A, M, K, lda, h->d_rl, ld, stream, n, strideA, per));
@@ -716,9 +763,8 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         etA = 1;
         esA = n > 1 ? per : 0;
         a_copy_floats = static_cast<size_t>(n) * per;
-        ++launches;
     }
-    if (relayout & 2) {  // B (stored N x K) -> B^T stored K x N, after A^T if both
+    if (p.copies & 2) {  // B (stored N x K) -> B^T stored K x N, after A^T if both
         float *dst = h->d_rl + a_copy_floats;
         const int ld = round32(N), n = strideB == 0 ? 1 : batch;
         const long long per = static_cast<long long>(K) * ld;
@@ -728,70 +774,65 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         eldb = ld;
         etB = 0;
         esB = n > 1 ? per : 0;
-        ++launches;
     }
+    const int copy_launches = (p.copies & 1) + ((p.copies >> 1) & 1);
 
-    // Arguments of the TMA kernels: A^T B^T runs as the NN kernel on the
-    // swapped operands (C^T = B_s A_s) with a transposed epilogue.
-    sg::GemmArgs k = g;
-    k.A = eA;
-    k.lda = elda;
-    k.sA = esA;
-    k.B = eB;
-    k.ldb = eldb;
-    k.sB = esB;
-    k.transA = etA;
-    k.transB = etB;
-    int op = etA ? (etB ? sg::kTmaOpNN : sg::kTmaOpTN) : (etB ? sg::kTmaOpNT : sg::kTmaOpNN);
-    if (etA && etB) {
-        k.M = N;
-        k.N = M;
-        k.A = eB;
-        k.lda = eldb;
-        k.sA = esB;
-        k.B = eA;
-        k.ldb = elda;
-        k.sB = esA;
-        k.c_trans = 1;
-        k.vec_c = false;
-    }
-
-    sg::TmaShape sh;
-    CUtensorMap tmA, tmB;
-    sg::SplitK sk{0, 0, nullptr, nullptr};
-    if (variant != SGEMM_VARIANT_GENERIC) {
-        if (!sg::tma_shape(variant, &sh)) return SGEMM_ERR_INVALID_VALUE;
-        sk = sg::SplitK{cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn), 0, nullptr, nullptr};
-        if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
-            if (batch == 1) plan_splits(h, k.M, k.N, K, &sk);
-            if (sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
-        } else {
-            plan_tail(h, variant, sh, k.M, k.N, K, batch, &sk);
+    int variant = p.variant;
+    if (p.kind == kPlanTma) {
+        // Arguments of the TMA kernels: A^T B^T runs as the NN kernel on the
+        // swapped operands (C^T = B_s A_s) with a transposed epilogue.
+        sg::GemmArgs k = g;
+        k.M = p.kM;
+        k.N = p.kN;
+        k.A = eA;
+        k.lda = elda;
+        k.sA = esA;
+        k.B = eB;
+        k.ldb = eldb;
+        k.sB = esB;
+        k.transA = etA;
+        k.transB = etB;
+        if (etA && etB) {
+            k.A = eB;
+            k.lda = eldb;
+            k.sA = esB;
+            k.B = eA;
+            k.ldb = elda;
+            k.sB = esA;
+            k.c_trans = 1;
+            k.vec_c = false;
         }
-        const bool a_ok = op == sg::kTmaOpTN
+        sg::TmaShape sh;
+        sg::tma_shape(variant, &sh);
+        sg::SplitK sk = p.sk;
+        if (sk.sk_ctas > 0) {
+            sk.ws = h->d_ws;
+            sk.counters = h->d_counters;
+        }
+        CUtensorMap tmA, tmB;
+        const bool a_ok = p.op == sg::kTmaOpTN
             ? encode_operand(&tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
             : encode_operand(&tmA, k.A, k.M, K, k.lda, batch, k.sA, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B);
-        const bool b_ok = op == sg::kTmaOpNT
+        const bool b_ok = p.op == sg::kTmaOpNT
             ? encode_operand(&tmB, k.B, k.N, K, k.ldb, batch, k.sB, sh.bk, sh.bn, CU_TENSOR_MAP_SWIZZLE_128B)
             : encode_operand(&tmB, k.B, K, k.N, k.ldb, batch, k.sB, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-        if (!a_ok || !b_ok) variant = SGEMM_VARIANT_GENERIC;  // a layout TMA cannot describe
-    }
-    if (variant == SGEMM_VARIANT_GENERIC) {
-        const int rc = from_cuda(sg::launch_generic(g, stream));  // the operands as the caller stored them
-        if (rc == SGEMM_OK) {
-            h->last_variant = variant;
-            h->last_launches = launches + 1;
-            h->last_relayout = relayout;
+        if (a_ok && b_ok) {
+            const int rc = from_cuda(sg::launch_tma_op(p.op, variant, k, tmA, tmB, sk, h->smem_override, stream));
+            if (rc == SGEMM_OK) {
+                h->last_variant = variant;
+                h->last_splits = p.splits;
+                h->last_launches = p.launches;
+                h->last_relayout = p.copies;
+            }
+            return rc;
         }
-        return rc;
+        variant = SGEMM_VARIANT_GENERIC;  // a layout TMA cannot describe
     }
-    const int rc = from_cuda(sg::launch_tma_op(op, variant, k, tmA, tmB, sk, h->smem_override, stream));
+    const int rc = from_cuda(sg::launch_generic(g, stream));  // the operands as the caller stored them
     if (rc == SGEMM_OK) {
-        h->last_variant = variant;
-        h->last_splits = splits_of(sk, cdiv(k.M, sh.bm) * cdiv(k.N, sh.bn) * batch);
-        // transposes, then the whole-tile waves and the stream-K CTAs
-        h->last_launches = launches + (sk.sk_ctas > 0 && sk.dp_tiles > 0 ? 2 : 1);
-        h->last_relayout = relayout;
+        h->last_variant = SGEMM_VARIANT_GENERIC;
+        h->last_launches = copy_launches + 1;
+        h->last_relayout = p.copies;
     }
     return rc;
 }
@@ -952,7 +993,7 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     // with transA = 1, which needs no copy of its own, so the workspace holds
     // only this segment's copy.
     auto copies_a = [&](int nr) {
-        return reads_ab && h->d_rl != nullptr && h->relayout_mode != SGEMM_RELAYOUT_OFF &&
+        return reads_ab && h->rl_floats > 0 && h->relayout_mode != SGEMM_RELAYOUT_OFF &&
                h->math_mode == SGEMM_MATH_FP32 && aligned16(dA) && aligned16(dB) && (lda % 4) == 0 &&
                (ldb % 4) == 0 && (h->pinned == SGEMM_VARIANT_AUTO || is_tma_variant(h->pinned)) &&
                static_cast<unsigned long long>(K) * ((nr + 31ULL) / 32 * 32) <= h->rl_floats &&
@@ -1038,6 +1079,53 @@ int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream
     if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
     limit_ns = std::min(std::max(limit_ns, 1000LL), 1000000000LL);
     return from_cuda(sg::launch_timeout_probe(h->d_status, limit_ns, static_cast<cudaStream_t>(stream)));
+}
+
+int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,
+                     int math_mode, int pinned, int transA, int transB, int M, int N, int K, float alpha,
+                     int batch, long long strideA, long long strideB, int tma_ok, int *out) {
+    if (ctas_per_sm == nullptr || out == nullptr) return SGEMM_ERR_NULL;
+    if (num_sms < 1 || relayout_floats < 0 || M < 0 || N < 0 || K < 0 || batch < 0 ||
+        (transA != 0 && transA != 1) || (transB != 0 && transB != 1) || pinned < 0 ||
+        pinned >= SGEMM_VARIANT_COUNT_ || pinned == SGEMM_VARIANT_SCALE ||
+        (relayout_mode != SGEMM_RELAYOUT_AUTO && relayout_mode != SGEMM_RELAYOUT_OFF &&
+         relayout_mode != SGEMM_RELAYOUT_ALWAYS) ||
+        (math_mode != SGEMM_MATH_FP32 && math_mode != SGEMM_MATH_3XTF32))
+        return SGEMM_ERR_INVALID_VALUE;
+    sgemm_ctx c{};  // planning inputs only: no device memory, no CUDA call
+    c.num_sms = num_sms;
+    c.ws_floats = kWorkspaceBytes / sizeof(float);
+    c.n_counters = kCounters;
+    c.rl_floats = static_cast<size_t>(relayout_floats);
+    c.relayout_mode = relayout_mode;
+    c.math_mode = math_mode;
+    c.pinned = pinned;
+    for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) c.ctas_per_sm[v] = ctas_per_sm[v];
+    for (int i = 0; i < 9; ++i) out[i] = 0;
+    if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;  // nothing runs
+    if (alpha == 0.f || K == 0) {
+        out[0] = kPlanScale;
+        out[1] = SGEMM_VARIANT_SCALE;
+        out[7] = 1;
+        out[8] = 1;
+        return SGEMM_OK;
+    }
+    if (batch == 1) strideA = strideB = 0;
+    const CallPlan p = plan_call(&c, transA, transB, M, N, K, batch, strideA, strideB, tma_ok != 0);
+    out[0] = p.kind;
+    out[1] = p.variant;
+    out[2] = p.copies;
+    out[3] = p.op;
+    out[4] = p.kind == kPlanTma ? p.sk.dp_tiles : 0;
+    out[5] = p.kind == kPlanTma ? p.sk.sk_ctas : 0;
+    if (p.kind == kPlanTma) {
+        sg::TmaShape sh;
+        sg::tma_shape(p.variant, &sh);
+        out[6] = cdiv(p.kM, sh.bm) * cdiv(p.kN, sh.bn) * batch;  // tiles of the call
+    }
+    out[7] = p.launches;
+    out[8] = p.splits;
+    return SGEMM_OK;
 }
 
 int sgemm_debug_fma_probe(sgemm_handle_t h, int ctas, int iters, float *sink, long long *flops, void *stream) {

@@ -38,6 +38,7 @@ VARIANT_TC_3XTF32_PAIR = 8
 VARIANT_TC_F16_PAIR = 9
 VARIANT_GENERIC_F16 = 10
 VARIANT_TMA_256x128 = 11
+VARIANT_COUNT = 12
 MATH_FP32 = 0
 MATH_3XTF32 = 1
 IN_BF16 = 1
@@ -55,7 +56,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
-           "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity")
+           "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan")
 
 
 class SgemmError(RuntimeError):
@@ -91,6 +92,8 @@ def lib() -> ctypes.CDLL:
         L.sgemm_last_relayout.argtypes = [vp]
         L.sgemm_relayout_capacity.argtypes = [vp]
         L.sgemm_relayout_capacity.restype = ctypes.c_longlong
+        L.sgemm_debug_plan.argtypes = [i32, ctypes.POINTER(i32), ctypes.c_longlong, i32, i32, i32, i32, i32, i32, i32,
+                                       i32, f32, i32, ctypes.c_longlong, ctypes.c_longlong, i32, ctypes.POINTER(i32)]
         L.sgemm_debug_fma_probe.argtypes = [vp, i32, i32, vp, ctypes.POINTER(ctypes.c_longlong), vp]
         L.sgemm_debug_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
         L.sgemm_run_mixed.argtypes = [vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
@@ -265,6 +268,24 @@ def sgemm_last_relayout(h) -> int:
 
 def sgemm_relayout_capacity(h) -> int:
     return lib().sgemm_relayout_capacity(h)
+
+
+PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits")
+PLAN_NOTHING, PLAN_SCALE, PLAN_TENSOR_CORE, PLAN_GENERIC, PLAN_TMA = 0, 1, 2, 3, 4
+
+
+def sgemm_debug_plan(num_sms, ctas_per_sm, transA, transB, M, N, K, *, alpha=1.0, batch=1, strideA=0,
+                     strideB=0, tma_ok=True, relayout_floats=2 * 8192 * 8192, relayout_mode=RELAYOUT_AUTO,
+                     math_mode=MATH_FP32, pinned=VARIANT_AUTO) -> dict:
+    """The plan sgemm_run_ex would follow, computed on the host (no GPU):
+    a dict with the fields of PLAN_FIELDS (see include/sgemm.h)."""
+    occ = (ctypes.c_int * VARIANT_COUNT)(*ctas_per_sm)
+    out = (ctypes.c_int * len(PLAN_FIELDS))()
+    _check(lib().sgemm_debug_plan(int(num_sms), occ, int(relayout_floats), int(relayout_mode), int(math_mode),
+                                  int(pinned), int(transA), int(transB), int(M), int(N), int(K), float(alpha),
+                                  int(batch), int(strideA), int(strideB), int(bool(tma_ok)), out),
+           "sgemm_debug_plan")
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def sgemm_get_device_status(h) -> int:

@@ -331,6 +331,24 @@ int sgemm_debug_bank_probe(sgemm_handle_t h, int padded, int ctas, int iters, fl
  * (SGEMM_ERR_LAUNCH) before anything runs.  0 restores normal launches. */
 int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
 
+/* Test hook: the plan sgemm_run_ex would follow for a call, computed on the
+ * host with no handle, no device and no CUDA call, from the device facts a
+ * handle records (`num_sms`; `ctas_per_sm`, SGEMM_VARIANT_COUNT_ entries
+ * indexed by sgemm_variant_t: resident CTAs per SM of each TMA variant) and
+ * its settings (re-layout workspace size in floats, re-layout mode, math
+ * mode, pinned variant).  `tma_ok` says whether A and B are 16-byte aligned
+ * with lda, ldb (and batch strides) multiples of 4.  out[0..8] receives: the
+ * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
+ * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
+ * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
+ * 1 TN, 2 NT), the whole tiles run in complete waves, the stream-K CTAs, the
+ * tiles of the call, the kernel launches and the CTAs per stream-K tile.
+ * SGEMM_ERR_NULL for a NULL array, SGEMM_ERR_INVALID_VALUE for an argument out
+ * of range. */
+int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,
+                     int math_mode, int pinned, int transA, int transB, int M, int N, int K, float alpha,
+                     int batch, long long strideA, long long strideB, int tma_ok, int *out);
+
 /* C <- alpha*A*B + beta*C without allocating anything, for callers that cannot
  * allocate GPU memory (allocator implementations that must not re-enter the
  * allocator, frameworks whose allocator has reserved the device memory, hosts

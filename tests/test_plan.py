@@ -1,0 +1,180 @@
+"""Host-side call planning (no GPU): the kernel kind, tile variant, operand
+copies and whole-tile / stream-K plan that sgemm_run_ex would use, computed by
+sgemm_debug_plan from the device facts a handle records on GB300 (152 SMs;
+resident CTAs per SM of each TMA variant).
+
+The stream-K kernels rely on host-side invariants (a stream-K CTA's K range
+touches at most two tiles, the partial tiles fit in the workspace, complete
+waves are whole), and the operand copies on the re-layout workspace's
+capacity: those are checked here over a grid of shapes, layouts, batches and
+modes, together with the choices the measurements on GB300 settled.
+"""
+import itertools
+
+import pytest
+
+from dense_fp32_matrix_09_gb300 import build, sgemm
+
+V = sgemm
+SMS = 152
+OCC = [0] * V.VARIANT_COUNT
+OCC[V.VARIANT_TMA_128x256] = 1
+OCC[V.VARIANT_TMA_256x128] = 1
+OCC[V.VARIANT_TMA_128x128] = 2
+OCC[V.VARIANT_TMA_64x64] = 3
+OCC[V.VARIANT_TMA_64x64_SPLITK] = 3
+TILE = {V.VARIANT_TMA_256x128: (256, 128), V.VARIANT_TMA_128x256: (128, 256), V.VARIANT_TMA_128x128: (128, 128),
+        V.VARIANT_TMA_64x64: (64, 64), V.VARIANT_TMA_64x64_SPLITK: (64, 64)}
+WS_FLOATS = (48 << 20) // 4  # stream-K workspace of a handle
+CAPACITY = 2 * 8192 * 8192    # re-layout workspace of a handle, floats
+TO_TN = {(0, 0): 1, (0, 1): 3, (1, 0): 0, (1, 1): 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+
+
+def plan(tA, tB, M, N, K, **kw):
+    return V.sgemm_debug_plan(SMS, OCC, tA, tB, M, N, K, **kw)
+
+
+def copies_need(tA, tB, M, N, K, copies, batch=1, strideA=1, strideB=1):
+    r32 = lambda x: (x + 31) // 32 * 32
+    nA = 1 if (batch == 1 or strideA == 0) else batch
+    nB = 1 if (batch == 1 or strideB == 0) else batch
+    return (nA * K * r32(M) if copies & 1 else 0) + (nB * K * r32(N) if copies & 2 else 0)
+
+
+def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout_floats=CAPACITY):
+    assert p["launches"] == bin(p["copies"]).count("1") + (2 if p["dp_tiles"] and p["sk_ctas"] else 1)
+    if p["kind"] != V.PLAN_TMA:
+        return
+    v = p["variant"]
+    bm, bn = TILE[v]
+    kM, kN = (N, M) if (tA ^ (p["copies"] & 1)) and (tB ^ (p["copies"] >> 1 & 1)) else (M, N)
+    tiles = -(-kM // bm) * -(-kN // bn) * batch
+    assert p["tiles"] == tiles
+    assert copies_need(tA, tB, M, N, K, p["copies"], batch, strideA, strideB) <= relayout_floats
+    G, dp = p["sk_ctas"], p["dp_tiles"]
+    if G == 0:
+        assert dp == tiles and p["splits"] == 1
+        return
+    slots = SMS * OCC[v]
+    kt = -(-K // 32)
+    sk_tiles = tiles - dp
+    assert 0 < G <= slots
+    assert G >= sk_tiles                       # a CTA's K range touches at most two tiles
+    assert G <= sk_tiles * kt                  # every stream-K CTA has at least one K step
+    assert (sk_tiles + G) * bm * bn <= WS_FLOATS  # partial tiles fit in the workspace
+    if v == V.VARIANT_TMA_64x64_SPLITK:
+        assert dp == 0 and G >= 2 * tiles and batch == 1
+    else:
+        assert dp % slots == 0                 # complete waves only
+        assert sk_tiles < slots or sk_tiles == 0
+        assert 4 * G >= 5 * sk_tiles           # at least 1.25 CTAs per stream-K tile
+        assert sk_tiles * kt >= 2 * G          # at least two K steps per CTA
+    assert p["splits"] >= 2
+
+
+SHAPES = [(1, 1, 1), (7, 5, 3), (64, 64, 64), (256, 256, 256), (300, 520, 270), (1000, 1500, 777),
+          (1024, 1024, 1024), (2048, 2048, 2048), (2048, 4096, 1024), (4096, 4096, 4096), (8192, 8192, 4096),
+          (8192, 8192, 8192), (16384, 32, 8192), (33, 9000, 4000), (6144, 6144, 6144), (4300000, 8, 4)]
+
+
+@pytest.mark.parametrize("mode", [V.RELAYOUT_AUTO, V.RELAYOUT_OFF, V.RELAYOUT_ALWAYS], ids=["auto", "off", "always"])
+@pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 0), (1, 1)], ids=["NN", "NT", "TN", "TT"])
+def test_plan_invariants(mode, op):
+    for (M, N, K), pinned in itertools.product(SHAPES, [V.VARIANT_AUTO] + list(TILE)):
+        p = plan(*op, M, N, K, relayout_mode=mode, pinned=pinned)
+        assert p["kind"] == V.PLAN_TMA
+        check_invariants(p, *op, M, N, K)
+        if mode == V.RELAYOUT_OFF:
+            assert p["copies"] == 0
+        if mode == V.RELAYOUT_ALWAYS:
+            fits = copies_need(*op, M, N, K, TO_TN[op]) <= CAPACITY
+            assert p["copies"] == (TO_TN[op] if fits else 0)
+        if pinned != V.VARIANT_AUTO:
+            assert p["variant"] == pinned or (pinned == V.VARIANT_TMA_64x64_SPLITK
+                                               and p["variant"] == V.VARIANT_TMA_64x64)
+
+
+@pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 0), (1, 1)], ids=["NN", "NT", "TN", "TT"])
+def test_plan_invariants_batched(op):
+    for (M, N, K, batch), sA, sB in itertools.product(
+            [(64, 64, 64, 1024), (130, 200, 96, 3), (2048, 2048, 2048, 8), (300, 520, 270, 3), (40, 72, 50, 500)],
+            [0, 1], [0, 1]):
+        for mode in (V.RELAYOUT_AUTO, V.RELAYOUT_ALWAYS):
+            p = plan(*op, M, N, K, batch=batch, strideA=sA, strideB=sB, relayout_mode=mode)
+            assert p["kind"] == V.PLAN_TMA
+            check_invariants(p, *op, M, N, K, batch, sA, sB)
+            assert p["variant"] != V.VARIANT_TMA_64x64_SPLITK
+
+
+def test_plan_kinds():
+    assert plan(0, 0, 0, 5, 5)["kind"] == V.PLAN_NOTHING
+    assert plan(0, 0, 5, 5, 5, batch=0)["kind"] == V.PLAN_NOTHING
+    p = plan(0, 0, 64, 64, 0)
+    assert (p["kind"], p["variant"]) == (V.PLAN_SCALE, V.VARIANT_SCALE)
+    assert plan(0, 0, 64, 64, 64, alpha=0.0)["kind"] == V.PLAN_SCALE
+    p = plan(0, 0, 4096, 4096, 4096, tma_ok=False)
+    assert (p["kind"], p["variant"], p["copies"], p["launches"]) == (V.PLAN_GENERIC, V.VARIANT_GENERIC, 0, 1)
+    p = plan(0, 0, 4096, 4096, 4096, pinned=V.VARIANT_GENERIC)
+    assert (p["kind"], p["copies"]) == (V.PLAN_GENERIC, 0)
+
+
+def test_tensor_core_plans():
+    """3xTF32 mode: the CTA-pair kernel from SMs/4 tiles of 256 x 256 and
+    K >= 256, in every layout (transposed operands copied into the NN layout),
+    batch 1 only, not with re-layout off."""
+    for op, copies in (((0, 0), 0), ((0, 1), 2), ((1, 0), 1), ((1, 1), 3)):
+        p = plan(*op, 8192, 8192, 8192, math_mode=V.MATH_3XTF32)
+        assert (p["kind"], p["variant"], p["copies"]) == (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32_PAIR, copies)
+        assert p["launches"] == 1 + bin(copies).count("1")
+        p = plan(*op, 8192, 8192, 8192, math_mode=V.MATH_3XTF32, relayout_mode=V.RELAYOUT_OFF)
+        assert p["kind"] == (V.PLAN_TENSOR_CORE if copies == 0 else V.PLAN_TMA)
+    assert plan(0, 0, 1024, 1024, 1024, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA   # too few tiles
+    assert plan(0, 0, 8192, 8192, 128, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA    # K below 256
+    assert plan(0, 0, 2048, 2048, 2048, batch=2, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA
+    p = plan(1, 1, 8192, 8192, 8192, pinned=V.VARIANT_TC_3XTF32)
+    assert (p["kind"], p["variant"], p["copies"]) == (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32, 3)
+    # the copies into the NN layout must fit
+    p = plan(1, 0, 16384, 16384, 8200, pinned=V.VARIANT_TC_3XTF32_PAIR)
+    assert p["kind"] == V.PLAN_TMA
+
+
+def test_choices_measured_on_gb300():
+    """The automatic choices the GB300 measurements settled (the variant and
+    copy that ran fastest, or within 1 %, on each of these shapes)."""
+    expect = {
+        (0, 0, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 1, 3),
+        (1, 0, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 0, 2),
+        (0, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 3, 4),
+        (1, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 2, 3),
+        (0, 0, 4096, 4096, 4096): (V.VARIANT_TMA_256x128, 1, 3),
+        (0, 0, 1024, 1024, 1024): (V.VARIANT_TMA_64x64, 0, 1),
+        (0, 0, 256, 256, 256): (V.VARIANT_TMA_64x64_SPLITK, 0, 1),
+        (0, 0, 1000, 1500, 777): (V.VARIANT_TMA_64x64, 0, 1),
+    }
+    for (tA, tB, M, N, K), (variant, copies, launches) in expect.items():
+        p = plan(tA, tB, M, N, K)
+        assert (p["variant"], p["copies"], p["launches"]) == (variant, copies, launches), (M, N, K, p)
+
+
+def test_relayout_capacity_edge():
+    """A of 16384 x 8192 exactly fills the workspace and is copied; 8200 columns
+    of K do not fit; a handle without workspace never copies."""
+    assert plan(0, 0, 16384, 32, 8192, relayout_mode=V.RELAYOUT_ALWAYS)["copies"] == 1
+    assert plan(0, 0, 16384, 32, 8200, relayout_mode=V.RELAYOUT_ALWAYS)["copies"] == 0
+    assert plan(0, 0, 8192, 8192, 8192, relayout_floats=0)["copies"] == 0
+
+
+def test_plan_argument_checks():
+    with pytest.raises(sgemm.SgemmError):
+        plan(0, 0, -1, 4, 4)
+    with pytest.raises(sgemm.SgemmError):
+        plan(2, 0, 4, 4, 4)
+    with pytest.raises(sgemm.SgemmError):
+        plan(0, 0, 4, 4, 4, relayout_mode=7)
+    with pytest.raises(sgemm.SgemmError):
+        plan(0, 0, 4, 4, 4, pinned=V.VARIANT_SCALE)
