@@ -348,6 +348,7 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 // the whole-tile / stream-K plan.  No CUDA call: the same decisions are
 // reachable without a GPU through sgemm_debug_plan.
 constexpr int kPlanScale = 1, kPlanTensorCore = 2, kPlanGeneric = 3, kPlanTma = 4;
+constexpr int kMaxTcBatch = 256;  // products of a batch the tensor-core kernels take one launch each
 
 struct CallPlan {
     int kind = kPlanGeneric;
@@ -371,8 +372,11 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     const unsigned long long tc_need =
         (transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0) +
         (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
-    const bool tc_reachable = batch == 1 && (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF &&
-                                                              h->rl_floats > 0 && tc_need <= h->rl_floats));
+    // A strided batch runs as one tensor-core launch per product (the
+    // kernels hold no batch index), up to kMaxTcBatch products.
+    const bool tc_reachable = batch <= kMaxTcBatch &&
+                              (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF && h->rl_floats > 0 &&
+                                                tc_need <= h->rl_floats));
     int variant = h->pinned;
     if (!tc_reachable && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
         variant = SGEMM_VARIANT_AUTO;
@@ -391,7 +395,7 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         p.kind = kPlanTensorCore;
         p.variant = variant;
         p.copies = tc_copy;
-        p.launches = 1 + (tc_copy & 1) + ((tc_copy >> 1) & 1);
+        p.launches = batch * (1 + (tc_copy & 1) + ((tc_copy >> 1) & 1));
         return p;
     }
 
@@ -706,44 +710,51 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
 
     if (p.kind == kPlanTensorCore) {
-        const float *tA_ = A, *tB_ = B;
-        int tlda = lda, tldb = ldb;
-        if (p.copies & 1) {  // A stored K x M -> M x K
-            const int ld = round32(K);
-            const int rc = from_cuda(sg::launch_transpose(A, K, M, lda, h->d_rl, ld, stream));
-            if (rc != SGEMM_OK) return rc;
-            tA_ = h->d_rl;
-            tlda = ld;
-        }
-        if (p.copies & 2) {  // B stored N x K -> K x N, after A's copy if both
-            float *dst = h->d_rl + ((p.copies & 1) ? static_cast<size_t>(M) * round32(K) : 0);
-            const int ld = round32(N);
-            const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream));
-            if (rc != SGEMM_OK) return rc;
-            tB_ = dst;
-            tldb = ld;
-        }
-        sg::GemmArgs gt = g;
-        gt.A = tA_;
-        gt.lda = tlda;
-        gt.B = tB_;
-        gt.ldb = tldb;
-        gt.transA = gt.transB = 0;
+        // one product at a time (batch entries in order on `stream`, so the
+        // copies of one entry reuse the workspace after the previous one)
         sg::TmaShape ts;
         sg::tc3x_shape(&ts);
-        CUtensorMap tA, tB;
-        if (!encode_2d(&tA, tA_, M, K, tlda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            !encode_2d(&tB, tB_, K, N, tldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
-            return SGEMM_ERR_CUDA;
-        const int rc = from_cuda(p.variant == SGEMM_VARIANT_TC_3XTF32
-                                     ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
-                                     : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream));
-        if (rc == SGEMM_OK) {
-            h->last_variant = p.variant;
-            h->last_launches = p.launches;
-            h->last_relayout = p.copies;
+        for (int b = 0; b < batch; ++b) {
+            const float *Ab = A + b * strideA, *Bb = B + b * strideB;
+            const float *tA_ = Ab, *tB_ = Bb;
+            int tlda = lda, tldb = ldb;
+            if (p.copies & 1) {  // A stored K x M -> M x K
+                const int ld = round32(K);
+                const int rc = from_cuda(sg::launch_transpose(Ab, K, M, lda, h->d_rl, ld, stream));
+                if (rc != SGEMM_OK) return rc;
+                tA_ = h->d_rl;
+                tlda = ld;
+            }
+            if (p.copies & 2) {  // B stored N x K -> K x N, after A's copy if both
+                float *dst = h->d_rl + ((p.copies & 1) ? static_cast<size_t>(M) * round32(K) : 0);
+                const int ld = round32(N);
+                const int rc = from_cuda(sg::launch_transpose(Bb, N, K, ldb, dst, ld, stream));
+                if (rc != SGEMM_OK) return rc;
+                tB_ = dst;
+                tldb = ld;
+            }
+            sg::GemmArgs gt = g;
+            gt.A = tA_;
+            gt.lda = tlda;
+            gt.B = tB_;
+            gt.ldb = tldb;
+            gt.C = C + b * strideC;
+            gt.transA = gt.transB = 0;
+            gt.batch = 1;
+            gt.sA = gt.sB = gt.sC = 0;
+            CUtensorMap tA, tB;
+            if (!encode_2d(&tA, tA_, M, K, tlda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !encode_2d(&tB, tB_, K, N, tldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
+                return SGEMM_ERR_CUDA;
+            const int rc = from_cuda(p.variant == SGEMM_VARIANT_TC_3XTF32
+                                         ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
+                                         : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream));
+            if (rc != SGEMM_OK) return rc;
         }
-        return rc;
+        h->last_variant = p.variant;
+        h->last_launches = p.launches;
+        h->last_relayout = p.copies;
+        return SGEMM_OK;
     }
 
     // FP32 SIMT kernels: operands first transposed into the re-layout

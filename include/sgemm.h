@@ -93,12 +93,13 @@ typedef enum {
     /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
      * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
      * for batch > 1, strideA, strideB) are multiples of 4; otherwise the
-     * generic variant runs.  The tensor-core variants serve batch 1 in every
-     * layout: they read A stored M x K and B stored K x N, and an operand
-     * stored transposed is first copied into that layout in the re-layout
-     * workspace (one launch per copy; see sgemm_relayout_t).  Where that
-     * cannot be done (batch > 1, re-layout off, copies larger than the
-     * workspace) a pinned tensor-core variant acts as AUTO. */
+     * generic variant runs.  The tensor-core variants serve every layout
+     * and batches of up to 256 products (one launch per product): they read
+     * A stored M x K and B stored K x N, and an operand stored transposed is
+     * first copied into that layout in the re-layout workspace (one launch
+     * per copy; see sgemm_relayout_t).  Where that cannot be done (a larger
+     * batch, re-layout off, copies larger than the workspace) a pinned
+     * tensor-core variant acts as AUTO. */
 } sgemm_variant_t;
 
 /* Arithmetic used by SGEMM_VARIANT_AUTO.  Both modes meet the same FP32

@@ -320,3 +320,33 @@ def test_tensor_core_kernel_without_relayout_falls_back(handle, mode):
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] not in TC_VARIANTS
     assert sgemm.sgemm_last_relayout(handle) == 0
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_tensor_core_strided_batch(handle, mode, op):
+    """A strided batch on the CTA-pair 3xTF32 kernel: one launch per product
+    (after its operand copies), gaps between the batch matrices kept."""
+    mode(V.RELAYOUT_AUTO, V.VARIANT_TC_3XTF32_PAIR)
+    p = ExProblem(op[0], op[1], 300, 520, 270, batch=3, seed=221, alpha=0.75, beta=0.5, pad=(4, 4, 4),
+                  gap=(8, 4, 12), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TC_3XTF32_PAIR
+    assert sgemm.sgemm_last_launches(handle) == 3 * (1 + bin(TC_COPIES[op]).count("1"))
+
+
+def test_math_mode_3xtf32_batched(handle, mode):
+    """3xTF32 math mode takes the tensor-core kernel for a batch of products
+    each large enough on its own (4 x 2048 x 2048 x 512, a shared B)."""
+    mode(V.RELAYOUT_AUTO)
+    sgemm.sgemm_set_math_mode(handle, V.MATH_3XTF32)
+    try:
+        p = ExProblem(0, 0, 2048, 2048, 512, batch=4, seed=231, pad=(0, 0, 0), gap=(0, 0, 0))
+        p.sB = 0
+        p.B = p.B[:p.br * p.ldb].copy()
+        C, bufs = p.run(handle)
+        ran = sgemm.sgemm_last_variant(handle)[0]
+    finally:
+        sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
+    p.check(C, bufs)
+    assert ran == V.VARIANT_TC_3XTF32_PAIR

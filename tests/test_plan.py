@@ -125,8 +125,8 @@ def test_plan_kinds():
 
 def test_tensor_core_plans():
     """3xTF32 mode: the CTA-pair kernel from SMs/4 tiles of 256 x 256 and
-    K >= 256, in every layout (transposed operands copied into the NN layout),
-    batch 1 only, not with re-layout off."""
+    K >= 256, in every layout (transposed operands copied into the NN layout;
+    not with re-layout off), batches of up to 256 products one launch each."""
     for op, copies in (((0, 0), 0), ((0, 1), 2), ((1, 0), 1), ((1, 1), 3)):
         p = plan(*op, 8192, 8192, 8192, math_mode=V.MATH_3XTF32)
         assert (p["kind"], p["variant"], p["copies"]) == (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32_PAIR, copies)
@@ -135,7 +135,12 @@ def test_tensor_core_plans():
         assert p["kind"] == (V.PLAN_TENSOR_CORE if copies == 0 else V.PLAN_TMA)
     assert plan(0, 0, 1024, 1024, 1024, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA   # too few tiles
     assert plan(0, 0, 8192, 8192, 128, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA    # K below 256
-    assert plan(0, 0, 2048, 2048, 2048, batch=2, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA
+    p = plan(0, 0, 2048, 2048, 2048, batch=2, strideA=1, strideB=1, math_mode=V.MATH_3XTF32)
+    assert (p["kind"], p["launches"]) == (V.PLAN_TENSOR_CORE, 2)    # one launch per product
+    p = plan(1, 1, 2048, 2048, 2048, batch=3, strideA=1, strideB=1, math_mode=V.MATH_3XTF32)
+    assert (p["kind"], p["copies"], p["launches"]) == (V.PLAN_TENSOR_CORE, 3, 9)
+    assert plan(0, 0, 2048, 2048, 2048, batch=257, strideA=1, strideB=1,
+                math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA
     p = plan(1, 1, 8192, 8192, 8192, pinned=V.VARIANT_TC_3XTF32)
     assert (p["kind"], p["variant"], p["copies"]) == (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32, 3)
     # the copies into the NN layout must fit
