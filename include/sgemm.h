@@ -26,6 +26,13 @@
  *   - Cells outside the M x K, K x N, M x N windows (columns K..lda-1 of A,
  *     N..ldb-1 of B, N..ldc-1 of C) are never read or written.
  *
+ * Column-major (BLAS / Fortran order) callers: a column-major m x n matrix
+ * with leading dimension ld is the row-major n x m matrix of its transpose,
+ * so the column-major product C = op(A) * op(B) is the row-major product
+ * C^T = op(B)^T * op(A)^T: call sgemm_run_ex with the operands swapped
+ * together with their trans flags and leading dimensions (B, transB, ldb
+ * first; A, transA, lda second) and M and N swapped.
+ *
  * Memory and streams: all matrix pointers are DEVICE pointers owned by the
  * caller.  sgemm_run never allocates and never synchronizes: it validates
  * its arguments on the host, enqueues kernels on `stream` (a cudaStream_t

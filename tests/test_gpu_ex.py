@@ -321,3 +321,42 @@ def test_batch_with_stream_k_tail_integer_exact(handle, variant, op):
     C, bufs = p.run(handle)
     p.check(C, bufs, exact=True)
     assert sgemm.sgemm_last_variant(handle)[1] > 1
+
+
+@pytest.mark.parametrize("op", OPS, ids=OP_IDS)
+def test_column_major_callers(handle, op):
+    """A column-major (BLAS order) product C = op(A) op(B) through the
+    row-major entry point: operands swapped with their trans flags and leading
+    dimensions, M and N swapped (the rule stated in include/sgemm.h).  Checked against the oracle on the
+    column-major matrices converted to row-major by numpy."""
+    tA, tB = op
+    m, n, k = 150, 97, 131
+    g = torch.Generator().manual_seed(241 + 2 * tA + tB)
+    a_rows, a_cols = (k, m) if tA else (m, k)  # the stored column-major matrices
+    b_rows, b_cols = (n, k) if tB else (k, n)
+    lda, ldb, ldc = a_rows + 4, b_rows + 8, m + 4
+    Acm = np.asfortranarray(inputs.uniform(a_rows, a_cols, g).numpy())
+    Bcm = np.asfortranarray(inputs.uniform(b_rows, b_cols, g).numpy())
+    C0 = inputs.uniform(m, n, g).numpy()
+    # column-major buffers with leading dimensions: element (i, j) at i + j*ld
+    bufA = np.zeros(lda * a_cols, np.float32)
+    bufB = np.zeros(ldb * b_cols, np.float32)
+    bufC = np.zeros(ldc * n, np.float32)
+    for j in range(a_cols):
+        bufA[j * lda:j * lda + a_rows] = Acm[:, j]
+    for j in range(b_cols):
+        bufB[j * ldb:j * ldb + b_rows] = Bcm[:, j]
+    for j in range(n):
+        bufC[j * ldc:j * ldc + m] = C0[:, j]
+    dA, dB, dC = DeviceBuf(bufA), DeviceBuf(bufB), DeviceBuf(bufC)
+    alpha, beta = 1.25, -0.5
+    sgemm.sgemm_run_ex(handle, tB, tA, n, m, k, alpha, dB.ptr, ldb, 0, dA.ptr, lda, 0, beta, dC.ptr, ldc, 0, 1)
+    torch.cuda.synchronize()
+    got = dC.interior()
+    opA = np.ascontiguousarray(Acm.T if tA else Acm)
+    opB = np.ascontiguousarray(Bcm.T if tB else Bcm)
+    ref = np.ascontiguousarray(C0).reshape(-1).copy()
+    oracle.sgemm(m, n, k, alpha, opA.reshape(-1), k, opB.reshape(-1), n, beta, ref, n)
+    ref = ref.reshape(m, n)
+    gotm = np.stack([got[j * ldc:j * ldc + m] for j in range(n)], axis=1)
+    assert float(np.max(np.abs(gotm.astype(np.float64) - ref))) <= tolerance(k)
