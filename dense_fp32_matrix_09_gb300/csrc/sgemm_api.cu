@@ -18,6 +18,56 @@
 #include "internal.h"
 #include "sgemm.h"
 
+namespace {
+
+// What a call with alpha != 0 and K > 0 runs: the kernel kind and variant,
+// the operand copies (bit 0: A copied transposed, bit 1: B), and for the TMA
+// kernels the operand layout, the M and N they see (swapped for A^T B^T) and
+// the whole-tile / stream-K plan.  No CUDA call: the same decisions are
+// reachable without a GPU through sgemm_debug_plan.
+constexpr int kPlanScale = 1, kPlanTensorCore = 2, kPlanGeneric = 3, kPlanTma = 4;
+constexpr int kMaxTcBatch = 256;  // products of a batch the tensor-core kernels take one launch each
+
+struct CallPlan {
+    int kind = kPlanGeneric;
+    int variant = SGEMM_VARIANT_GENERIC;
+    int copies = 0;
+    int op = sg::kTmaOpNN;
+    int kM = 0, kN = 0;
+    sg::SplitK sk{0, 0, nullptr, nullptr};
+    int splits = 1;    // CTAs per stream-K tile (rounded up; 1 without)
+    int launches = 1;  // kernel launches the call enqueues
+};
+
+// Everything a plan depends on besides the handle's fixed device facts.
+struct PlanKey {
+    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode;
+    bool operator==(const PlanKey &o) const {
+        return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
+               a_shared == o.a_shared && b_shared == o.b_shared && tma_ok == o.tma_ok && pinned == o.pinned &&
+               relayout_mode == o.relayout_mode && math_mode == o.math_mode;
+    }
+};
+
+// Everything an FP32 tensor map depends on.
+struct MapKey {
+    const void *base;
+    long long stride;
+    int rows, cols, ld, batch, box_cols, box_rows, swz;
+    bool operator==(const MapKey &o) const {
+        return base == o.base && stride == o.stride && rows == o.rows && cols == o.cols && ld == o.ld &&
+               batch == o.batch && box_cols == o.box_cols && box_rows == o.box_rows && swz == o.swz;
+    }
+};
+
+// Calls that repeat a shape reuse its plan, and calls that repeat an operand
+// (same address, shape, leading dimension and box) reuse its tensor map: both
+// are pure functions of their keys, so a cached entry is exactly what
+// recomputing would give.  Small, filled round robin.
+constexpr int kPlanCache = 8, kMapCache = 8;
+
+}  // namespace
+
 struct sgemm_ctx {
     int device;
     int num_sms;
@@ -40,6 +90,12 @@ struct sgemm_ctx {
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
     cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
+    PlanKey plan_key[kPlanCache];           // plan cache: plan_filled entries, next slot plan_next
+    CallPlan plan_val[kPlanCache];
+    int plan_filled, plan_next;
+    MapKey map_key[kMapCache];              // tensor-map cache, likewise
+    CUtensorMap map_val[kMapCache];
+    int map_filled, map_next;
 };
 
 namespace {
@@ -342,25 +398,7 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     return best;
 }
 
-// What a call with alpha != 0 and K > 0 runs: the kernel kind and variant,
-// the operand copies (bit 0: A copied transposed, bit 1: B), and for the TMA
-// kernels the operand layout, the M and N they see (swapped for A^T B^T) and
-// the whole-tile / stream-K plan.  No CUDA call: the same decisions are
-// reachable without a GPU through sgemm_debug_plan.
-constexpr int kPlanScale = 1, kPlanTensorCore = 2, kPlanGeneric = 3, kPlanTma = 4;
-constexpr int kMaxTcBatch = 256;  // products of a batch the tensor-core kernels take one launch each
-
-struct CallPlan {
-    int kind = kPlanGeneric;
-    int variant = SGEMM_VARIANT_GENERIC;
-    int copies = 0;
-    int op = sg::kTmaOpNN;
-    int kM = 0, kN = 0;
-    sg::SplitK sk{0, 0, nullptr, nullptr};
-    int splits = 1;    // CTAs per stream-K tile (rounded up; 1 without)
-    int launches = 1;  // kernel launches the call enqueues
-};
-
+// The plan of a call (see CallPlan).
 CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                    long long strideB, bool tma_ok) {
     CallPlan p;
@@ -420,6 +458,40 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     // transposes, then the whole-tile waves and the stream-K CTAs
     p.launches = (p.copies & 1) + ((p.copies >> 1) & 1) + (p.sk.sk_ctas > 0 && p.sk.dp_tiles > 0 ? 2 : 1);
     return p;
+}
+
+// plan_call through the handle's plan cache.
+CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
+                     long long strideB, bool tma_ok) {
+    const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, tma_ok, h->pinned,
+                      h->relayout_mode, h->math_mode};
+    for (int i = 0; i < h->plan_filled; ++i)
+        if (h->plan_key[i] == key) return h->plan_val[i];
+    const CallPlan p = cached_plan(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
+    h->plan_key[h->plan_next] = key;
+    h->plan_val[h->plan_next] = p;
+    h->plan_next = (h->plan_next + 1) % kPlanCache;
+    h->plan_filled = std::min(h->plan_filled + 1, kPlanCache);
+    return p;
+}
+
+// encode_operand through the handle's tensor-map cache.
+bool cached_encode(sgemm_ctx *h, CUtensorMap *map, const float *base, int rows, int cols, int ld, int batch,
+                   long long stride, int box_cols, int box_rows, CUtensorMapSwizzle swz) {
+    const bool one = batch <= 1 || stride == 0;  // a 2-D map
+    const MapKey key{base, one ? 0 : stride, rows, cols, ld, one ? 1 : batch, box_cols, box_rows,
+                     static_cast<int>(swz)};
+    for (int i = 0; i < h->map_filled; ++i)
+        if (h->map_key[i] == key) {
+            *map = h->map_val[i];
+            return true;
+        }
+    if (!encode_operand(map, base, rows, cols, ld, batch, stride, box_cols, box_rows, swz)) return false;
+    h->map_key[h->map_next] = key;
+    h->map_val[h->map_next] = *map;
+    h->map_next = (h->map_next + 1) % kMapCache;
+    h->map_filled = std::min(h->map_filled + 1, kMapCache);
+    return true;
 }
 
 }  // namespace
@@ -743,8 +815,8 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
             gt.batch = 1;
             gt.sA = gt.sB = gt.sC = 0;
             CUtensorMap tA, tB;
-            if (!encode_2d(&tA, tA_, M, K, tlda, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !encode_2d(&tB, tB_, K, N, tldb, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
+            if (!cached_encode(h, &tA, tA_, M, K, tlda, 1, 0, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !cached_encode(h, &tB, tB_, K, N, tldb, 1, 0, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
                 return SGEMM_ERR_CUDA;
             const int rc = from_cuda(p.variant == SGEMM_VARIANT_TC_3XTF32
                                          ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
@@ -822,11 +894,11 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         }
         CUtensorMap tmA, tmB;
         const bool a_ok = p.op == sg::kTmaOpTN
-            ? encode_operand(&tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
-            : encode_operand(&tmA, k.A, k.M, K, k.lda, batch, k.sA, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B);
+            ? cached_encode(h, &tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
+            : cached_encode(h, &tmA, k.A, k.M, K, k.lda, batch, k.sA, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B);
         const bool b_ok = p.op == sg::kTmaOpNT
-            ? encode_operand(&tmB, k.B, k.N, K, k.ldb, batch, k.sB, sh.bk, sh.bn, CU_TENSOR_MAP_SWIZZLE_128B)
-            : encode_operand(&tmB, k.B, K, k.N, k.ldb, batch, k.sB, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+            ? cached_encode(h, &tmB, k.B, k.N, K, k.ldb, batch, k.sB, sh.bk, sh.bn, CU_TENSOR_MAP_SWIZZLE_128B)
+            : cached_encode(h, &tmB, k.B, K, k.N, k.ldb, batch, k.sB, sh.bn, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (a_ok && b_ok) {
             const int rc = from_cuda(sg::launch_tma_op(p.op, variant, k, tmA, tmB, sk, h->smem_override, stream));
             if (rc == SGEMM_OK) {

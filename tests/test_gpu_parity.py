@@ -412,3 +412,21 @@ def _run_host_case(handle, cfg, pinned):
     if cfg.ldc > cfg.N:
         pad = inputs.pad_mask(cfg.M, cfg.N, cfg.ldc)
         assert np.array_equal(C.view(np.uint32)[pad], prob.C0.view(np.uint32)[pad])
+
+
+def test_cached_plans_and_maps_follow_their_operands(handle):
+    """A handle reuses the plan of a repeated shape and the tensor map of a
+    repeated operand.  Alternating two buffer sets of one shape, and cycling
+    through more shapes than the caches hold, must still give every call the
+    result for its own operands (each call checked against the oracle)."""
+    import torch
+    sets = []
+    for i in range(10):
+        pair = [_cfg(200 + 40 * i, 136 + 8 * i, 96 + 16 * i, 1.0, 0.0, seed=s) for s in (1, 2)]
+        sets.append([(c, inputs.make_problem(c)) for c in pair])
+    for rnd in range(2):
+        for pair in sets:
+            for c, prob in pair:
+                C_gpu, _ = run_gpu(handle, c, prob)
+                assert max_abs_err(c, C_gpu, oracle_full(c, prob)) <= tolerance(c.K), (rnd, c.name)
+    torch.cuda.synchronize()
