@@ -48,6 +48,40 @@ def test_status_and_variant_strings(lib):
     assert sgemm.sgemm_version() == 10000
 
 
+def header_enum_values():
+    """NAME -> value for every `NAME = value` enumerator of include/sgemm.h."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(SGEMM_[A-Z0-9_x]+)\s*=\s*(\d+)", text)}
+
+
+def test_binding_constants_match_the_header():
+    """Every constant the Python binding mirrors has the header's value, and
+    every variant name the library reports matches its enumerator."""
+    values = header_enum_values()
+    pairs = {"OK": "SGEMM_OK", "ERR_NULL": "SGEMM_ERR_NULL", "ERR_INVALID_VALUE": "SGEMM_ERR_INVALID_VALUE",
+             "ERR_ALIAS": "SGEMM_ERR_ALIAS", "ERR_BAD_HANDLE": "SGEMM_ERR_BAD_HANDLE",
+             "ERR_UNSUPPORTED_DEVICE": "SGEMM_ERR_UNSUPPORTED_DEVICE", "ERR_LAUNCH": "SGEMM_ERR_LAUNCH",
+             "ERR_CUDA": "SGEMM_ERR_CUDA", "ERR_DEVICE_TIMEOUT": "SGEMM_ERR_DEVICE_TIMEOUT",
+             "ERR_WRONG_DEVICE": "SGEMM_ERR_WRONG_DEVICE", "ERR_SCRATCH_TOO_SMALL": "SGEMM_ERR_SCRATCH_TOO_SMALL",
+             "MATH_FP32": "SGEMM_MATH_FP32", "MATH_3XTF32": "SGEMM_MATH_3XTF32", "IN_BF16": "SGEMM_IN_BF16",
+             "IN_F16": "SGEMM_IN_F16", "RELAYOUT_AUTO": "SGEMM_RELAYOUT_AUTO", "RELAYOUT_OFF": "SGEMM_RELAYOUT_OFF",
+             "RELAYOUT_ALWAYS": "SGEMM_RELAYOUT_ALWAYS", "VARIANT_COUNT": "SGEMM_VARIANT_COUNT_"}
+    for name in dir(sgemm):
+        if name.startswith("VARIANT_") and name != "VARIANT_COUNT":
+            pairs[name] = "SGEMM_" + name
+    for py, c in pairs.items():
+        assert getattr(sgemm, py) == values[c], (py, c)
+    variants = {k: v for k, v in values.items() if k.startswith("SGEMM_VARIANT_") and not k.endswith("_")}
+    assert len(variants) == values["SGEMM_VARIANT_COUNT_"]
+    assert sorted(variants.values()) == list(range(values["SGEMM_VARIANT_COUNT_"]))
+
+
+def test_variant_names_match_the_enumerators(lib):
+    for c, v in header_enum_values().items():
+        if c.startswith("SGEMM_VARIANT_") and not c.endswith("_"):
+            assert sgemm.variant_name(v) == c[len("SGEMM_VARIANT_"):].lower(), c
+
+
 # Fake, never-dereferenced device addresses (only compared by the checks).
 A0, B0, C0 = 0x10000000, 0x20000000, 0x30000000
 
