@@ -1085,8 +1085,8 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     // Column blocks of the first panel follow B's chunks: 1, 1, then 2 chunks
     // at a time (the first blocks start as soon as their chunk lands; later
     // chunks land faster than a block computes, and at 1024 rows a block of
-    // two 1024-column chunks -- 64 tiles of 128 x 256 -- ran faster per chunk
-    // than blocks of one or four on GB300); the last panel runs them in
+    // two 1024-column chunks ran faster per chunk than blocks of one or four
+    // on GB300); the last panel runs them in
     // reverse order, so only a one-chunk block's copy back follows the last
     // GEMM.
     int groups[8], ng = 0;

@@ -116,8 +116,9 @@ using CfgL = Cfg<128, 256, 2, 4, 8, 16, 4, 1>;   // SGEMM_VARIANT_TMA_128x256
 using CfgX = Cfg<256, 128, 4, 4, 8, 8, 4, 1>;    // SGEMM_VARIANT_TMA_256x128 (16 warps, 128 registers)
 using CfgM = Cfg<128, 128, 2, 4, 8, 8, 3, 2>;    // SGEMM_VARIANT_TMA_128x128 (2 CTAs per SM)
 using CfgS = Cfg<64, 64, 2, 2, 8, 4, 4, 3>;      // SGEMM_VARIANT_TMA_64x64 (+ stream-K variant)
-// NT adds two B-sized transpose buffers, so its two larger tiles keep fewer
-// stages within the shared memory of one (128 x 256) or two (128 x 128) CTAs.
+// NT adds two B-sized transpose buffers, so its three larger tiles keep fewer
+// stages within the shared memory of one (128 x 256, 256 x 128) or two
+// (128 x 128) CTAs.
 using CfgLnt = Cfg<128, 256, 2, 4, 8, 16, 3, 1>;
 using CfgXnt = Cfg<256, 128, 4, 4, 8, 8, 3, 1>;
 using CfgMnt = Cfg<128, 128, 2, 4, 8, 8, 2, 2>;
