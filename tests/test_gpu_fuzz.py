@@ -1,0 +1,71 @@
+"""Seeded random sweep of sgemm_run_ex against the oracle.
+
+Each case draws a layout, sizes (ragged, 1 to 1100), a batch with
+gaps or a shared operand, alpha and beta, a pinned tile variant or the
+automatic choice, a re-layout mode and a math mode, so that combinations the
+targeted tests do not name (a stream-K range crossing from one batch product
+into the next after an operand copy, a shared operand copied once, a
+transposed-epilogue call on a pinned small tile, ...) are still checked
+element by element, with padding and gap cells bit-unchanged.
+"""
+import random
+
+import pytest
+import torch
+
+from dense_fp32_matrix_09_gb300 import sgemm
+from tests.test_gpu_ex import ExProblem
+
+pytestmark = pytest.mark.gpu
+
+V = sgemm
+PINS = (V.VARIANT_AUTO, V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128,
+        V.VARIANT_TMA_64x64, V.VARIANT_TMA_64x64_SPLITK, V.VARIANT_GENERIC, V.VARIANT_TC_3XTF32_PAIR)
+MODES = (V.RELAYOUT_AUTO, V.RELAYOUT_OFF, V.RELAYOUT_ALWAYS)
+
+
+@pytest.fixture(scope="module")
+def handle():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from dense_fp32_matrix_09_gb300 import build
+    build.build()
+    h = sgemm.sgemm_create()
+    yield h
+    sgemm.sgemm_destroy(h)
+
+
+def draw_case(rng):
+    tA, tB = rng.randrange(2), rng.randrange(2)
+    M, N, K = (rng.choice([1, 3, 17, 63, 64, 65, 130, 257, 300, 513, 700, 1100]) for _ in range(3))
+    batch = rng.choice([1, 1, 1, 2, 3, 5])
+    alpha = rng.choice([1.0, -0.5, 1.25])
+    beta = rng.choice([0.0, 1.0, 0.75, -2.0])
+    shared = rng.choice([None, None, "A", "B"]) if batch > 1 else None
+    return dict(tA=tA, tB=tB, M=M, N=N, K=K, batch=batch, alpha=alpha, beta=beta, shared=shared,
+                pin=rng.choice(PINS), mode=rng.choice(MODES), math=rng.choice([V.MATH_FP32, V.MATH_3XTF32]),
+                mult4=rng.random() < 0.8, seed=rng.randrange(1 << 20))
+
+
+@pytest.mark.parametrize("case_id", range(160))
+def test_random_case(handle, case_id):
+    c = draw_case(random.Random(1000 + case_id))
+    p = ExProblem(c["tA"], c["tB"], c["M"], c["N"], c["K"], batch=c["batch"], seed=c["seed"], alpha=c["alpha"],
+                  beta=c["beta"], pad=(4, 8, 4), gap=(8, 4, 12), mult4=c["mult4"])
+    if c["shared"] == "A":
+        p.sA = 0
+        p.A = p.A[:p.ar * p.lda + 8].copy()
+    elif c["shared"] == "B":
+        p.sB = 0
+        p.B = p.B[:p.br * p.ldb + 4].copy()
+    sgemm.sgemm_set_variant(handle, c["pin"])
+    sgemm.sgemm_set_relayout(handle, c["mode"])
+    sgemm.sgemm_set_math_mode(handle, c["math"])
+    try:
+        C, bufs = p.run(handle)
+    finally:
+        sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
+        sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
+        sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
+    p.check(C, bufs)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK, c
