@@ -37,13 +37,12 @@ sys.path.insert(0, ROOT)
 METRIC = "SGEMM TFLOP/s (2MNK/t) at 4096³ and 8192³; % of GB300 FP32 peak"
 UNIT = "TFLOP/s"
 
-# DRAM bytes (read + write) per step of the dominant kernel at 8192^3, from
-# one ncu capture, keyed by the SHA-256 of the kernel source it was taken on;
-# any other source gives traffic = null (profiles/sgemm_8192cube_dram.md).
-# The SIMT step is two launches of the same kernel template (13 complete
-# waves of whole tiles: 2.988 GB; the stream-K last wave: 0.493 GB).
-# DRAM bytes of one headline call (8192^3) by (SIMT kernel source hash,
-# layout the kernel ran on, re-layout bits), from one-pass ncu captures
+# DRAM bytes (read + write) of one headline call at 8192^3 -- every launch of
+# the call: the transposed copy, the complete waves, the stream-K wave and the
+# kernel adding its parts -- keyed by (SHA-256 of the SIMT kernel source
+# without comments, layout the kernel ran on, re-layout bits), from one-pass
+# ncu launch lists of the headline command (profiles/
+# sgemm_headline_8192cube_launches.md); any other source gives traffic = null.
 TRAFFIC_BY_SOURCE = {("744fa4c4033f5592", "TN", 1): 3.346e9}
 TC_TRAFFIC_BY_SOURCE = {"3f6064e551384a01": 2.534e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",

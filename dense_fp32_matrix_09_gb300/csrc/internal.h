@@ -52,6 +52,9 @@ struct SplitK {
     float *ws;      // (tiles - dp_tiles + sk_ctas) * bm * bn partial sums
     int *counters;  // one arrival counter per stream-K tile, zero between calls
     int cta0 = 0;   // index of this launch's first CTA in the dp_tiles + sk_ctas sequence
+    int defer = 0;  // nonzero: every part of a split tile stays in the workspace and a
+                    // second kernel adds them (no arrival counters); zero: the last CTA
+                    // of the tile to arrive adds them
 };
 
 // Operand layouts of the TMA-fed SIMT kernels: NN (A stored M x K, B K x N),

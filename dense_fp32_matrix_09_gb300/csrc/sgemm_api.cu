@@ -217,49 +217,30 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
 }
 
-// Tail plan for the whole-tile variants.  With T tiles (of every batch
-// entry) and P resident CTA slots, T = full*P + rem: the first full*P tiles run whole (complete waves)
-// and the K steps of the rem tiles of the last, partly empty wave are shared
-// evenly by G stream-K CTAs (G <= P, at least 2 K steps each, within the
-// workspace), so the last wave keeps every slot busy for rem*kt/G steps
-// instead of leaving P - rem slots idle for a whole tile.  Used when G is at
-// least 1.25 rem (less would save little over whole tiles).
-void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch,
-               sg::SplitK *sk) {
-    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;
-    const long long kt = cdiv(K, sh.bk);
-    *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
-    const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[variant]);
-    const long long full = tiles / slots, rem = tiles - full * slots;
-    if (rem == 0 || rem > h->n_counters) return;
-    const long long G = sk_ctas_for(h, rem * kt, rem, slots, 1LL * sh.bm * sh.bn, 2);
-    if (G * 4 < rem * 5) return;
-    *sk = sg::SplitK{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
-}
-
-// CTAs per stream-K tile (rounded up; 1 without stream-K), for reporting.
-int splits_of(const sg::SplitK &sk, int tiles) {
-    if (sk.sk_ctas <= 0) return 1;
-    return std::max(2, cdiv(sk.sk_ctas, std::max(1, tiles - sk.dp_tiles)));
-}
-
-// Estimated time of the call with `variant`, in microseconds (only the
-// ranking matters).  A K step of one CTA takes bm*bn*32 FMAs at the
-// variant's main-loop efficiency measured on GB300 (fraction of FP32 peak
-// with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80, 64 x 64
-// 0.73, 256 x 128 0.815; TN: 0.84, 0.84, 0.80, 0.87; NT: 0.76, 0.75, 0.55
-// (from 1024^3, where NT ran 1.34x slower than NN), 0.73; the TN 128 x 128 tile
-// depends on K: 0.86 up to K = 5120, where it beat 128 x 256 by 1-3 % on
-// seven shapes, and 0.78 from K = 6144, where it lost 3-14 %), shared with the other
-// CTAs resident on its SM (fewer in a thin last wave).  Complete waves take
-// kt steps; a stream-K part takes ceil(T/G) steps plus its fixup (storing
-// and summing the parts: measured at about 15 us for the 128-row tiles and 2
-// us for 64 x 64, and 2 us for the second launch); an unsplit partial wave
-// takes kt steps.  A batch multiplies the tiles (and shares the tail plan).
-double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
-                    sg::SplitK *plan) {
-    sg::TmaShape sh;
-    if (!sg::tma_shape(variant, &sh)) return 1e300;
+// Estimated time, in microseconds (only the ranking matters), of `variant`'s
+// kernels on an M x N x K call of layout `op` (a batch multiplies the
+// tiles) under tail plan `plan`.  A K step of one CTA takes bm*bn*32 FMAs at
+// the variant's main-loop efficiency measured on GB300 (fraction of FP32
+// peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80,
+// 64 x 64 0.73, 256 x 128 0.815; TN: 0.84, 0.84, 0.80, 0.87; NT: 0.76, 0.75,
+// 0.55 (from 1024^3, where NT ran 1.34x slower than NN), 0.73; the TN
+// 128 x 128 tile depends on K: 0.86 up to K = 5120, where it beat 128 x 256
+// by 1-3 % on seven shapes, and 0.78 from K = 6144, where it lost 3-14 %),
+// shared with the other CTAs resident on its SM (fewer in a thin last wave).
+// Complete waves take kt steps; a stream-K part takes ceil(T/G) steps plus
+// its fixed cost, and 2 us for each further launch; an unsplit partial wave
+// takes kt steps.  Fixed costs of a stream-K part, from the intercepts of
+// time against K on GB300 (1024 x 1024 x K, K = 1024 and 4096, in CUDA
+// graphs): the larger tiles' parts stored and added by the second kernel,
+// kDeferredFixup (about 11 us in all with its launch); the 64 x 64 tail
+// split, kSmallSplitFixup, with K steps kSmallSplitSlow times slower than
+// whole 64 x 64 tiles (its measured slope); the 64 x 64 split-all variant
+// (256^3 and below), 2 us.
+constexpr double kDeferredFixup = 9.0;
+constexpr double kSmallSplitFixup = 8.5;
+constexpr double kSmallSplitSlow = 1.12;
+double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
+                 const sg::SplitK &plan) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
     static const double kEff[3][4] = {{0.81, 0.80, 0.73, 0.815}, {0.84, 0.84, 0.80, 0.87},
                                       {0.76, 0.75, 0.55, 0.73}};
@@ -271,27 +252,76 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
     const double cps = std::max(1, h->ctas_per_sm[variant]);
     const double sms = h->num_sms, P = sms * cps;
     const double t_step = static_cast<double>(sh.bm) * sh.bn * sh.bk * cps / (128.0 * eff * 2000.0);
-    const double fixup = vi == 2 ? 2.0 : 15.0;
     const double kt = cdiv(K, sh.bk);
     const double tiles = static_cast<double>(cdiv(M, sh.bm)) * cdiv(N, sh.bn) * batch;
     // `ctas` CTAs for `steps` K steps each, as one wave
     auto wave = [&](double ctas, double steps) {
         return steps * t_step * std::min(cps, std::ceil(ctas / sms)) / cps;
     };
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) return wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas)) + 2.0;
+    const double full = std::floor(tiles / P);
+    const double rem = tiles - full * P;
+    double t = full * kt * t_step;
+    if (plan.sk_ctas > 0) {
+        const double steps = std::ceil(rem * kt / plan.sk_ctas);
+        t += plan.defer ? wave(plan.sk_ctas, steps) + kDeferredFixup + 2.0
+                        : wave(plan.sk_ctas, steps) * kSmallSplitSlow + kSmallSplitFixup;
+        if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
+    } else if (rem > 0) {
+        t += wave(rem, kt);
+    }
+    return t;
+}
+
+// Tail plan for the whole-tile variants.  With T tiles (of every batch
+// entry) and P resident CTA slots, T = full*P + rem: the first full*P tiles
+// run whole (complete waves) and the K steps of the rem tiles of the last,
+// partly empty wave may be shared evenly by G stream-K CTAs (G <= P, at
+// least 2 K steps each, within the workspace), so the last wave keeps every
+// slot busy for rem*kt/G steps instead of leaving P - rem slots idle for a
+// whole tile.  The 64 x 64 tile adds a tile's parts in its last CTA to
+// arrive and takes the split when G is at least 1.25 rem (less saved little
+// over whole tiles on GB300); the larger tiles, whose parts are 4-8 times
+// larger, leave them to a second kernel that adds them over the whole GPU
+// (deferred), and take the split when its estimate beats whole tiles.
+void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
+               sg::SplitK *sk) {
+    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;
+    const long long kt = cdiv(K, sh.bk);
+    *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
+    const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[variant]);
+    const long long full = tiles / slots, rem = tiles - full * slots;
+    if (rem == 0 || rem > h->n_counters) return;
+    const long long G = sk_ctas_for(h, rem * kt, rem, slots, 1LL * sh.bm * sh.bn, 2);
+    const bool defer = sh.bm * sh.bn > 64 * 64;
+    if (G <= rem || (!defer && G * 4 < rem * 5)) return;
+    sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
+    cand.defer = defer ? 1 : 0;
+    if (defer && plan_time(h, variant, sh, M, N, K, batch, op, cand) >= plan_time(h, variant, sh, M, N, K, batch, op, *sk))
+        return;
+    *sk = cand;
+}
+
+// CTAs per stream-K tile (rounded up; 1 without stream-K), for reporting.
+int splits_of(const sg::SplitK &sk, int tiles) {
+    if (sk.sk_ctas <= 0) return 1;
+    return std::max(2, cdiv(sk.sk_ctas, std::max(1, tiles - sk.dp_tiles)));
+}
+
+// Estimated time of the call with `variant` (plan_time under the variant's
+// own tail plan, which is stored in *plan).
+double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int batch, int op,
+                    sg::SplitK *plan) {
+    sg::TmaShape sh;
+    if (!sg::tma_shape(variant, &sh)) return 1e300;
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
         if (batch > 1) return 1e300;
         plan_splits(h, M, N, K, plan);
         if (plan->sk_ctas == 0) return 1e300;  // runs as the whole-tile 64 x 64 variant
-        return wave(plan->sk_ctas, std::ceil(tiles * kt / plan->sk_ctas)) + fixup;
+    } else {
+        plan_tail(h, variant, sh, M, N, K, batch, op, plan);
     }
-    plan_tail(h, variant, sh, M, N, K, batch, plan);
-    const double full = std::floor(tiles / P), rem = tiles - full * P;
-    double t = full * kt * t_step;
-    if (plan->sk_ctas > 0)
-        t += wave(plan->sk_ctas, std::ceil(rem * kt / plan->sk_ctas)) + fixup + (full > 0 ? 2.0 : 0.0);
-    else if (rem > 0)
-        t += wave(rem, kt);
-    return t;
+    return plan_time(h, variant, sh, M, N, K, batch, op, *plan);
 }
 
 // Variant for a TMA-eligible call: the lowest estimated cost; ties go to the
@@ -450,13 +480,14 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         if (batch == 1) plan_splits(h, p.kM, p.kN, K, &p.sk);
         if (p.sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
     } else {
-        plan_tail(h, variant, sh, p.kM, p.kN, K, batch, &p.sk);
+        plan_tail(h, variant, sh, p.kM, p.kN, K, batch, p.op, &p.sk);
     }
     p.kind = kPlanTma;
     p.variant = variant;
     p.splits = splits_of(p.sk, tiles * batch);
     // transposes, then the whole-tile waves and the stream-K CTAs
-    p.launches = (p.copies & 1) + ((p.copies >> 1) & 1) + (p.sk.sk_ctas > 0 && p.sk.dp_tiles > 0 ? 2 : 1);
+    p.launches = (p.copies & 1) + ((p.copies >> 1) & 1) + (p.sk.sk_ctas > 0 && p.sk.dp_tiles > 0 ? 2 : 1) +
+                 (p.sk.sk_ctas > 0 && p.sk.defer ? 1 : 0);
     return p;
 }
 
@@ -467,7 +498,7 @@ CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, 
                       h->relayout_mode, h->math_mode};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
-    const CallPlan p = cached_plan(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
+    const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
     h->plan_key[h->plan_next] = key;
     h->plan_val[h->plan_next] = p;
     h->plan_next = (h->plan_next + 1) % kPlanCache;
@@ -779,7 +810,7 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
 
     const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
                         (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
-    const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
+    const CallPlan p = cached_plan(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
 
     if (p.kind == kPlanTensorCore) {
         // one product at a time (batch entries in order on `stream`, so the
@@ -1184,7 +1215,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     c.math_mode = math_mode;
     c.pinned = pinned;
     for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) c.ctas_per_sm[v] = ctas_per_sm[v];
-    for (int i = 0; i < 9; ++i) out[i] = 0;
+    for (int i = 0; i < 10; ++i) out[i] = 0;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;  // nothing runs
     if (alpha == 0.f || K == 0) {
         out[0] = kPlanScale;
@@ -1208,6 +1239,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     }
     out[7] = p.launches;
     out[8] = p.splits;
+    out[9] = p.kind == kPlanTma && p.sk.sk_ctas > 0 && p.sk.defer ? 1 : 0;
     return SGEMM_OK;
 }
 

@@ -571,12 +571,13 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                                                    acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
             }
         }
+        ++nseg_done;
+        if (sk.defer) continue;  // the finishing kernel adds the parts after this grid
         __threadfence();
         named_barrier_sync(1, C::kConsumers);
         if (tid == 0) s_flag[seg] = (atomicAdd(&sk.counters[tl], 1) == q_last - q_first);
         named_barrier_sync(1, C::kConsumers);
         split_last |= static_cast<unsigned>(s_flag[seg] != 0) << seg;
-        ++nseg_done;
     }
 
     if (aborted && tid == 0) {
@@ -607,6 +608,54 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
     // a whole tile, in acc
     epilogue<C, OP>(acc, g, Cb, m0w, n0w, wm, wn, lane_m, lane_n);
+}
+
+// Deferred stream-K tail, second kernel: block (u, tl) adds float4 group u
+// of every part of split tile tl (slots tl + q_first .. tl + q_last) in
+// ascending k order -- the order of the in-kernel reduction, so the sums
+// carry the same bits -- and runs the epilogue on it.  Thread tid takes the
+// group that consumer thread tid of the stream-K CTAs held, so the part
+// layout and the epilogue's element mapping are those of the main kernel.
+// A tile that one CTA computed whole was finished by that CTA.
+template <class C, int OP>
+__global__ void __launch_bounds__(C::kConsumers)
+sk_finish_kernel(const GemmArgs g, const SplitK sk, const int group_m) {
+    const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
+    const int tiles_per = tiles_m * tiles_n;
+    const int kt = (g.K + C::BK - 1) / C::BK;
+    const long long T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
+    const int tl = static_cast<int>(blockIdx.y), u = static_cast<int>(blockIdx.x);
+    const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
+    const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+    if (q_first == q_last) return;
+    const int tile = sk.dp_tiles + tl;
+    int tm, tn;
+    tile_coords(tile % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
+    const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
+    const size_t part_stride = static_cast<size_t>(C::BM) * C::BN / 4;  // float4s per part
+    const float4 *p = reinterpret_cast<const float4 *>(sk.ws) + static_cast<size_t>(tl) * part_stride +
+                      static_cast<size_t>(u) * C::kConsumers + tid;
+    // the first part and up to kU more are loaded together (one L2 round
+    // trip for a tile of up to kU + 1 parts), then added in ascending k order
+    constexpr int kU = 8;
+    float4 sum = __ldcg(p + static_cast<size_t>(q_first) * part_stride);
+#pragma unroll 1
+    for (int qq = q_first + 1; qq <= q_last; qq += kU) {
+        float4 r[kU];
+#pragma unroll
+        for (int i = 0; i < kU; ++i)
+            if (qq + i <= q_last) r[i] = __ldcg(p + static_cast<size_t>(qq + i) * part_stride);
+#pragma unroll
+        for (int i = 0; i < kU; ++i)
+            if (qq + i <= q_last) {
+                sum.x += r[i].x; sum.y += r[i].y; sum.z += r[i].z; sum.w += r[i].w;
+            }
+    }
+    const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+    epilogue_group<C, OP>(g, g.C + static_cast<long long>(tile / tiles_per) * g.sC, tm * C::BM, tn * C::BN, wm, wn,
+                          lane_m, lane_n, u / C::TN4, u % C::TN4, v);
 }
 
 template <class C>
@@ -653,6 +702,10 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         SplitK s2 = sk;
         s2.cta0 = sk.dp_tiles;
         sgemm_tma_kernel<C, true, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
+        if (sk.defer) {
+            const dim3 grid(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles));
+            sk_finish_kernel<C, OP><<<grid, C::kConsumers, 0, stream>>>(g, sk, kGroupM);
+        }
     }
     return cudaGetLastError();
 }

@@ -270,7 +270,8 @@ def sgemm_relayout_capacity(h) -> int:
     return lib().sgemm_relayout_capacity(h)
 
 
-PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits")
+PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits",
+               "deferred")
 PLAN_NOTHING, PLAN_SCALE, PLAN_TENSOR_CORE, PLAN_GENERIC, PLAN_TMA = 0, 1, 2, 3, 4
 
 

@@ -345,12 +345,14 @@ int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
  * indexed by sgemm_variant_t: resident CTAs per SM of each TMA variant) and
  * its settings (re-layout workspace size in floats, re-layout mode, math
  * mode, pinned variant).  `tma_ok` says whether A and B are 16-byte aligned
- * with lda, ldb (and batch strides) multiples of 4.  out[0..8] receives: the
+ * with lda, ldb (and batch strides) multiples of 4.  out[0..9] receives: the
  * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
  * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
  * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
  * 1 TN, 2 NT), the whole tiles run in complete waves, the stream-K CTAs, the
- * tiles of the call, the kernel launches and the CTAs per stream-K tile.
+ * tiles of the call, the kernel launches, the CTAs per stream-K tile, and 1
+ * when a second kernel adds the stream-K tiles' parts (0 when the last CTA of
+ * each tile adds them, or without stream-K).
  * SGEMM_ERR_NULL for a NULL array, SGEMM_ERR_INVALID_VALUE for an argument out
  * of range. */
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,

@@ -303,9 +303,10 @@ def test_batch_with_more_tiles_than_slots(handle, variant, op):
 def test_batch_with_stream_k_tail(handle, variant, op, v):
     """The tiles of all batch matrices form one sequence: the partial last
     wave is shared by stream-K CTAs whose K ranges cross from one batch
-    matrix into the next (3 ragged 300 x 520 x 270 products)."""
+    matrix into the next (3 ragged 300 x 520 x 1100 products: K long enough
+    that every variant's estimate prefers the split to whole tiles)."""
     variant(v)
-    p = ExProblem(op[0], op[1], 300, 520, 270, batch=3, seed=201, alpha=1.25, beta=-0.75, pad=(4, 4, 4),
+    p = ExProblem(op[0], op[1], 300, 520, 1100, batch=3, seed=201, alpha=1.25, beta=-0.75, pad=(4, 4, 4),
                   gap=(8, 4, 12), mult4=True)
     C, bufs = p.run(handle)
     p.check(C, bufs)

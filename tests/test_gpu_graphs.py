@@ -30,9 +30,10 @@ def _dev(prob):
 
 
 def test_capture_and_replay_fp32_calls(handle):
-    """Three calls in one graph: a whole-tile launch, a two-launch call
-    (complete waves + stream-K wave) and the split-all variant; replayed twice
-    (beta = 0, so a replay recomputes the same C)."""
+    """Three calls in one graph: a whole-tile launch, a three-launch call
+    (complete waves, stream-K wave, the kernel that adds the stream-K parts)
+    and the split-all variant; replayed twice (beta = 0, so a replay
+    recomputes the same C)."""
     cfgs = [inputs.GemmConfig("g_small", 300, 520, 270, 272, 520, 520, 61, 1.25, 0.0),
             inputs.GemmConfig("g_waves", 2048, 2560, 2048, 2048, 2560, 2560, 62, 1.0, 0.0),
             inputs.square(256, 63)]
@@ -51,7 +52,7 @@ def test_capture_and_replay_fp32_calls(handle):
             sgemm.sgemm_run(handle, c.M, c.N, c.K, c.alpha, A, c.lda, B, c.ldb, c.beta, C, c.ldc, s)
             # GEMM launches: the call's launches minus its operand copies
             launches.append(sgemm.sgemm_last_launches(handle) - bin(sgemm.sgemm_last_relayout(handle)).count("1"))
-    assert 2 in launches  # the stream-K two-launch form was captured
+    assert 3 in launches  # the deferred stream-K form after complete waves was captured
     for _ in range(2):
         for _, _, C in bufs:
             C.fill_(float("nan"))
