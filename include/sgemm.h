@@ -296,8 +296,10 @@ int sgemm_last_variant(sgemm_handle_t h, int *splits);
 
 /* Number of kernel launches the handle's last successful sgemm_run /
  * sgemm_run_ex enqueued: 0 (nothing to do), one per transposed operand
- * (sgemm_last_relayout), then 1, or 2 for the GEMM (complete waves of whole
- * tiles, then the stream-K CTAs of the last wave), all on the same stream;
+ * (sgemm_last_relayout), then 1 to 3 for the GEMM: complete waves of whole
+ * tiles; the stream-K CTAs of the last wave; and, for tiles larger than
+ * 64 x 64, the kernel that adds the stream-K parts.  All on the same stream.
+ * The 3xTF32 kernels: one launch per batch product after its copies.
  * -1 if `h` is not a live handle. */
 int sgemm_last_launches(sgemm_handle_t h);
 
