@@ -6,7 +6,9 @@ automatic choice, a re-layout mode and a math mode, so that combinations the
 targeted tests do not name (a stream-K range crossing from one batch product
 into the next after an operand copy, a shared operand copied once, a
 transposed-epilogue call on a pinned small tile, ...) are still checked
-element by element, with padding and gap cells bit-unchanged.
+element by element, with padding and gap cells bit-unchanged.  A second sweep
+draws M and N of 1000-2100 with K up to 777 on the larger tiles, so that calls
+run complete waves, a stream-K wave and the kernel that adds its parts.
 """
 import random
 
@@ -67,5 +69,30 @@ def test_random_case(handle, case_id):
         sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
         sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
         sgemm.sgemm_set_math_mode(handle, V.MATH_FP32)
+    p.check(C, bufs)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK, c
+
+
+def draw_wave_case(rng):
+    tA, tB = rng.randrange(2), rng.randrange(2)
+    return dict(tA=tA, tB=tB, M=rng.choice([1000, 1537, 1900, 2048, 2100]), N=rng.choice([1000, 1536, 2048, 2056, 2100]),
+                K=rng.choice([64, 257, 520, 777]), batch=rng.choice([1, 2, 3]), alpha=rng.choice([1.0, -0.5]),
+                beta=rng.choice([0.0, 0.75]),
+                pin=rng.choice([V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128, V.VARIANT_AUTO]),
+                mode=rng.choice(MODES), seed=rng.randrange(1 << 20))
+
+
+@pytest.mark.parametrize("case_id", range(24))
+def test_random_wave_case(handle, case_id):
+    c = draw_wave_case(random.Random(70000 + case_id))
+    p = ExProblem(c["tA"], c["tB"], c["M"], c["N"], c["K"], batch=c["batch"], seed=c["seed"], alpha=c["alpha"],
+                  beta=c["beta"], pad=(4, 8, 4), gap=(8, 4, 12), mult4=True)
+    sgemm.sgemm_set_variant(handle, c["pin"])
+    sgemm.sgemm_set_relayout(handle, c["mode"])
+    try:
+        C, bufs = p.run(handle)
+    finally:
+        sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
+        sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
     p.check(C, bufs)
     assert sgemm.sgemm_get_device_status(handle) == V.OK, c
