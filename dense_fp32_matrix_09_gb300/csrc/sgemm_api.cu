@@ -232,11 +232,18 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // takes kt steps.  Fixed costs of a stream-K part, from the intercepts of
 // time against K on GB300 (1024 x 1024 x K, K = 1024 and 4096, in CUDA
 // graphs): the larger tiles' parts stored and added by the second kernel,
-// kDeferredFixup (about 11 us in all with its launch); the 64 x 64 tail
+// kDeferredFixup (about 11 us in all with its launch; 2 us more for the
+// 256 x 128 tile, whose intercepts measured 12.9 and 14.6 us at 1024^3 and
+// 1000 x 1500 x 777 against 10.8 and 12.5 for 128 x 256); the 64 x 64 tail
 // split, kSmallSplitFixup, with K steps kSmallSplitSlow times slower than
 // whole 64 x 64 tiles (its measured slope); the 64 x 64 split-all variant
-// (256^3 and below), 2 us.
+// (256^3 and below), 2 us.  The stream-K K steps of the 128 x 128 tile (two
+// CTAs per SM) also ran slower than its whole tiles, by kSharedSplitSlow
+// (1024^3, 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us
+// against 46.8, 52.0 and 149 estimated without it).
 constexpr double kDeferredFixup = 9.0;
+constexpr double kDeferredFixup256x128 = 11.0;
+constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
 constexpr double kSmallSplitSlow = 1.12;
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
@@ -264,7 +271,8 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     double t = full * kt * t_step;
     if (plan.sk_ctas > 0) {
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
-        t += plan.defer ? wave(plan.sk_ctas, steps) + kDeferredFixup + 2.0
+        const double fix = variant == SGEMM_VARIANT_TMA_256x128 ? kDeferredFixup256x128 : kDeferredFixup;
+        t += plan.defer ? wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + fix + 2.0
                         : wave(plan.sk_ctas, steps) * kSmallSplitSlow + kSmallSplitFixup;
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
     } else if (rem > 0) {
@@ -342,10 +350,11 @@ int choose_variant(const sgemm_ctx *h, int M, int N, int K, int batch = 1, int o
 }
 
 // Estimated time of transposing `count` rows x cols FP32 matrices in one
-// launch (a read and a write of every element at about 5.5 TB/s, plus the
-// launch and its ordering gap), in microseconds.
+// launch, in microseconds: a read and a write of every element at 6.5 TB/s
+// (measured on GB300: 6.6-6.7 TB/s from 6144^2 to 8192^2, 12.8 us for
+// 1024 x 8192), plus 2 us for the launch and its ordering gap.
 double transpose_cost(int rows, int cols, int count = 1) {
-    return 6.0 + 8.0 * rows * static_cast<double>(cols) * count / 5.5e6;
+    return 2.0 + 8.0 * rows * static_cast<double>(cols) * count / 6.5e6;
 }
 
 // Leading dimension of a transposed copy: x rounded up to 32 floats (128

@@ -166,11 +166,12 @@ def test_choices_measured_on_gb300():
         (1, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 2, 4),
         (0, 0, 4096, 4096, 4096): (V.VARIANT_TMA_256x128, 1, 4),
         # one stream-K wave over all tiles and the kernel adding its parts
-        (0, 0, 1024, 1024, 1024): (V.VARIANT_TMA_256x128, 0, 2),
-        (0, 0, 1000, 1500, 777): (V.VARIANT_TMA_256x128, 0, 2),
+        (0, 0, 1024, 1024, 1024): (V.VARIANT_TMA_128x256, 0, 2),
+        (0, 0, 1000, 1500, 777): (V.VARIANT_TMA_128x256, 0, 2),
+        (0, 0, 2048, 2048, 1024): (V.VARIANT_TMA_256x128, 1, 3),
         (0, 0, 2048, 2048, 2048): (V.VARIANT_TMA_256x128, 1, 3),
-        # one partial wave of whole tiles
-        (0, 0, 1536, 1536, 1536): (V.VARIANT_TMA_128x128, 0, 1),
+        # one partial wave of whole tiles, after the copy of A
+        (0, 0, 1536, 1536, 1536): (V.VARIANT_TMA_128x128, 1, 2),
         (0, 0, 256, 256, 256): (V.VARIANT_TMA_64x64_SPLITK, 0, 1),
     }
     for (tA, tB, M, N, K), (variant, copies, launches) in expect.items():
