@@ -222,11 +222,14 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // tiles) under tail plan `plan`.  A K step of one CTA takes bm*bn*32 FMAs at
 // the variant's main-loop efficiency measured on GB300 (fraction of FP32
 // peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80,
-// 64 x 64 0.73, 256 x 128 0.815; TN: 0.84, 0.84, 0.80, 0.87; NT: 0.76, 0.75,
-// 0.55 (from 1024^3, where NT ran 1.34x slower than NN), 0.73; the TN
+// 256 x 128 0.815; TN: 0.84, 0.84, 0.87; NT: 0.76, 0.75, 0.73; the TN
 // 128 x 128 tile depends on K: 0.86 up to K = 5120, where it beat 128 x 256
 // by 1-3 % on seven shapes, and 0.78 from K = 6144, where it lost 3-14 %),
 // shared with the other CTAs resident on its SM (fewer in a thin last wave).
+// The 64 x 64 tile is the one chosen below a few thousand: its figures (NN
+// 0.65, TN 0.715, NT 0.49) are those of 8192^3 (0.73, 0.80; NT from 1024^3,
+// where it ran 1.34x slower than NN) divided by the 1.12 by which its K steps
+// measured slower at 1024^2 and on 1000 x 1500 x 777, whole tiles or split.
 // Complete waves take kt steps; a stream-K part takes ceil(T/G) steps plus
 // its fixed cost, and 2 us for each further launch; an unsplit partial wave
 // takes kt steps.  Fixed costs of a stream-K part, from the intercepts of
@@ -235,9 +238,8 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // kDeferredFixup (about 11 us in all with its launch; 2 us more for the
 // 256 x 128 tile, whose intercepts measured 12.9 and 14.6 us at 1024^3 and
 // 1000 x 1500 x 777 against 10.8 and 12.5 for 128 x 256); the 64 x 64 tail
-// split, kSmallSplitFixup, with K steps kSmallSplitSlow times slower than
-// whole 64 x 64 tiles (its measured slope); the 64 x 64 split-all variant
-// (256^3 and below), 2 us.  The stream-K K steps of the 128 x 128 tile (two
+// split, kSmallSplitFixup; the 64 x 64 split-all variant (256^3 and
+// below), 2 us.  The stream-K K steps of the 128 x 128 tile (two
 // CTAs per SM) also ran slower than its whole tiles, by kSharedSplitSlow
 // (1024^3, 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us
 // against 46.8, 52.0 and 149 estimated without it).
@@ -245,12 +247,11 @@ constexpr double kDeferredFixup = 9.0;
 constexpr double kDeferredFixup256x128 = 11.0;
 constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
-constexpr double kSmallSplitSlow = 1.12;
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                  const sg::SplitK &plan) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
-    static const double kEff[3][4] = {{0.81, 0.80, 0.73, 0.815}, {0.84, 0.84, 0.80, 0.87},
-                                      {0.76, 0.75, 0.55, 0.73}};
+    static const double kEff[3][4] = {{0.81, 0.80, 0.65, 0.815}, {0.84, 0.84, 0.715, 0.87},
+                                      {0.76, 0.75, 0.49, 0.73}};
     const int vi = variant == SGEMM_VARIANT_TMA_128x256   ? 0
                    : variant == SGEMM_VARIANT_TMA_128x128 ? 1
                    : variant == SGEMM_VARIANT_TMA_256x128 ? 3
@@ -273,7 +274,7 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
         const double fix = variant == SGEMM_VARIANT_TMA_256x128 ? kDeferredFixup256x128 : kDeferredFixup;
         t += plan.defer ? wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + fix + 2.0
-                        : wave(plan.sk_ctas, steps) * kSmallSplitSlow + kSmallSplitFixup;
+                        : wave(plan.sk_ctas, steps) + kSmallSplitFixup;
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
     } else if (rem > 0) {
         t += wave(rem, kt);
