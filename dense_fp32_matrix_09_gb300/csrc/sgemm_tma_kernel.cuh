@@ -334,6 +334,15 @@ __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, 
     }
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may be scheduled once every CTA of the kernel before it has
+// signalled (or exited); it must wait for that kernel's completion and the
+// visibility of its writes before touching them.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Stream-K: the CTAs of one tile are the consecutive q with iterations in
 // [tl*kt, (tl+1)*kt) of the T = stream-K tiles x kt iterations, where CTA q
 // holds [floor(q*T/G), floor((q+1)*T/G)).  First such q: the largest with
@@ -409,6 +418,9 @@ __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g, const SplitK sk, const int group_m) {
     extern __shared__ uint8_t smem_raw[];
+    // a stream-K grid lets the kernel that adds its parts be scheduled now: its
+    // blocks take SM room as this grid's CTAs leave and wait for its completion
+    if constexpr (SPLIT) griddep_launch_dependents();
     // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B.
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -620,6 +632,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 template <class C, int OP>
 __global__ void __launch_bounds__(C::kConsumers)
 sk_finish_kernel(const GemmArgs g, const SplitK sk, const int group_m) {
+    griddep_wait();  // the stream-K grid has completed and its parts are visible
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
     const int tiles_per = tiles_m * tiles_n;
     const int kt = (g.K + C::BK - 1) / C::BK;
@@ -703,8 +716,19 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         s2.cta0 = sk.dp_tiles;
         sgemm_tma_kernel<C, true, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
         if (sk.defer) {
-            const dim3 grid(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles));
-            sk_finish_kernel<C, OP><<<grid, C::kConsumers, 0, stream>>>(g, sk, kGroupM);
+            // a programmatic dependent of the stream-K grid (it waits for it on the device)
+            cudaLaunchConfig_t cfg{};
+            cfg.gridDim = dim3(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles));
+            cfg.blockDim = dim3(C::kConsumers);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            const cudaError_t e = cudaLaunchKernelEx(&cfg, sk_finish_kernel<C, OP>, g, sk, static_cast<int>(kGroupM));
+            if (e != cudaSuccess) return e;
         }
     }
     return cudaGetLastError();
