@@ -41,11 +41,11 @@ struct CallPlan {
 
 // Everything a plan depends on besides the handle's fixed device facts.
 struct PlanKey {
-    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode;
+    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode, sk_in_kernel;
     bool operator==(const PlanKey &o) const {
         return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
                a_shared == o.a_shared && b_shared == o.b_shared && tma_ok == o.tma_ok && pinned == o.pinned &&
-               relayout_mode == o.relayout_mode && math_mode == o.math_mode;
+               relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_in_kernel == o.sk_in_kernel;
     }
 };
 
@@ -87,6 +87,7 @@ struct sgemm_ctx {
     size_t rl_floats;
     int relayout_mode;                      // sgemm_relayout_t
     int last_relayout;                      // operands the last call transposed (bit 0 A, bit 1 B)
+    int sk_in_kernel;                       // test hook: 1 = stream-K parts added in-kernel for every tile
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
     cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
@@ -302,7 +303,7 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
     const long long full = tiles / slots, rem = tiles - full * slots;
     if (rem == 0 || rem > h->n_counters) return;
     const long long G = sk_ctas_for(h, rem * kt, rem, slots, 1LL * sh.bm * sh.bn, 2);
-    const bool defer = sh.bm * sh.bn > 64 * 64;
+    const bool defer = sh.bm * sh.bn > 64 * 64 && h->sk_in_kernel == 0;
     if (G <= rem || (!defer && G * 4 < rem * 5)) return;
     sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
     cand.defer = defer ? 1 : 0;
@@ -505,7 +506,7 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                      long long strideB, bool tma_ok) {
     const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, tma_ok, h->pinned,
-                      h->relayout_mode, h->math_mode};
+                      h->relayout_mode, h->math_mode, h->sk_in_kernel};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
     const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
@@ -774,6 +775,13 @@ int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
     if (bytes < 0) return SGEMM_ERR_INVALID_VALUE;
     h->smem_override = bytes;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int in_kernel) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (in_kernel != 0 && in_kernel != 1) return SGEMM_ERR_INVALID_VALUE;
+    h->sk_in_kernel = in_kernel;
     return SGEMM_OK;
 }
 

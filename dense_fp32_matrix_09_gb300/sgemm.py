@@ -56,7 +56,8 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_version", "sgemm_run_noalloc", "sgemm_set_math_mode", "sgemm_run_host",
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
-           "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan")
+           "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
+           "sgemm_debug_set_stream_k_sums")
 
 
 class SgemmError(RuntimeError):
@@ -101,6 +102,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_get_device_status.argtypes = [vp]
         L.sgemm_debug_timeout_probe.argtypes = [vp, ctypes.c_longlong, vp]
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
+        L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
         L.sgemm_status_string.argtypes = [i32]
         L.sgemm_status_string.restype = ctypes.c_char_p
         L.sgemm_variant_name.argtypes = [i32]
@@ -299,6 +301,10 @@ def sgemm_debug_timeout_probe(h, limit_ns: int, stream=None) -> None:
 
 def sgemm_debug_set_smem_override(h, nbytes: int) -> None:
     _check(lib().sgemm_debug_set_smem_override(h, int(nbytes)), "sgemm_debug_set_smem_override")
+
+
+def sgemm_debug_set_stream_k_sums(h, in_kernel: int) -> None:
+    _check(lib().sgemm_debug_set_stream_k_sums(h, int(in_kernel)), "sgemm_debug_set_stream_k_sums")
 
 
 class Sgemm:

@@ -341,6 +341,16 @@ int sgemm_debug_bank_probe(sgemm_handle_t h, int padded, int ctas, int iters, fl
  * (SGEMM_ERR_LAUNCH) before anything runs.  0 restores normal launches. */
 int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
 
+/* Test hook: how later calls of the handle add the partial sums of a tile
+ * whose K range is split over stream-K CTAs.  0 (the default): the tiles
+ * larger than 64 x 64 leave every part in the workspace and a second kernel
+ * adds them; the 64 x 64 tiles add them in the last CTA of the tile to
+ * arrive.  1: every tile adds them in its last CTA to arrive, the larger
+ * tiles split from 1.25 stream-K CTAs per tile as the 64 x 64 tile does.
+ * Both add the parts in ascending k order, so a tile split the same way gets
+ * the same bits either way.  SGEMM_ERR_INVALID_VALUE for another value. */
+int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int in_kernel);
+
 /* Test hook: the plan sgemm_run_ex would follow for a call, computed on the
  * host with no handle, no device and no CUDA call, from the device facts a
  * handle records (`num_sms`; `ctas_per_sm`, SGEMM_VARIANT_COUNT_ entries

@@ -430,3 +430,41 @@ def test_cached_plans_and_maps_follow_their_operands(handle):
                 C_gpu, _ = run_gpu(handle, c, prob)
                 assert max_abs_err(c, C_gpu, oracle_full(c, prob)) <= tolerance(c.K), (rnd, c.name)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("v,shape", [(V.VARIANT_TMA_256x128, (1024, 1024, 1024)),
+                                     (V.VARIANT_TMA_128x256, (1024, 1024, 1024)),
+                                     (V.VARIANT_TMA_128x128, (1024, 1024, 1024)),
+                                     (V.VARIANT_TMA_256x128, (2560, 2048, 768)),
+                                     (V.VARIANT_TMA_128x256, (1000, 1500, 777))],
+                         ids=lambda x: sgemm.variant_name(x) if isinstance(x, int) else "x".join(map(str, x)))
+def test_deferred_sums_equal_in_kernel_sums(handle, variant, v, shape):
+    """The larger tiles' stream-K parts added by the second kernel give the
+    bits that the in-kernel sums (the last CTA of each tile to arrive) give:
+    same split, same ascending k order; one launch more.  Uniform inputs, so
+    the sums round; beta = 0.75 reads C."""
+    import torch
+    M, N, K = shape
+    lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4  # 16-byte rows: the TMA kernels
+    g = torch.Generator(device="cuda").manual_seed(101)
+    A = torch.rand(M * lda, device="cuda", generator=g) * 2 - 1
+    B = torch.rand(K * ldb, device="cuda", generator=g) * 2 - 1
+    C0 = torch.rand(M * ldb, device="cuda", generator=g) * 2 - 1
+    variant(v)
+    out = {}
+    try:
+        for in_kernel in (0, 1):
+            sgemm.sgemm_debug_set_stream_k_sums(handle, in_kernel)
+            C = C0.clone()
+            sgemm.sgemm_run(handle, M, N, K, 1.25, A, lda, B, ldb, 0.75, C, ldb)
+            torch.cuda.synchronize()
+            ran, splits = sgemm.sgemm_last_variant(handle)
+            out[in_kernel] = (C, ran, splits, sgemm.sgemm_last_launches(handle))
+    finally:
+        sgemm.sgemm_debug_set_stream_k_sums(handle, 0)
+    (C_def, ran_d, sp_d, l_d), (C_ink, ran_i, sp_i, l_i) = out[0], out[1]
+    assert ran_d == ran_i == v and sp_d == sp_i and sp_d > 1, (ran_d, ran_i, sp_d, sp_i)
+    assert l_d == l_i + 1, (l_d, l_i)
+    assert torch.isfinite(C_def).all()
+    assert torch.equal(C_def.view(torch.int32), C_ink.view(torch.int32))
+    assert sgemm.sgemm_get_device_status(handle) == V.OK
