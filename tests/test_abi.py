@@ -201,6 +201,14 @@ def test_bad_handles_are_rejected_without_dereference(lib):
     assert lib.sgemm_last_variant(None, None) == -1
     assert lib.sgemm_get_device_status(None) == sgemm.ERR_BAD_HANDLE
     assert lib.sgemm_create(None) == sgemm.ERR_NULL
+    for fake in (None, ctypes.c_void_p(0x1234)):
+        assert lib.sgemm_set_math_mode(fake, sgemm.MATH_FP32) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_set_relayout(fake, sgemm.RELAYOUT_AUTO) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_set_smem_override(fake, 0) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_set_stream_k_sums(fake, 0) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_last_launches(fake) == -1
+        assert lib.sgemm_last_relayout(fake) == -1
+        assert lib.sgemm_relayout_capacity(fake) == -1
 
 
 def test_create_without_gpu_reports_unsupported(lib):
