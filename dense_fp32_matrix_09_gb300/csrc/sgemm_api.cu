@@ -234,20 +234,27 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // Complete waves take kt steps; a stream-K part takes ceil(T/G) steps plus
 // its fixed cost, and 2 us for each further launch; an unsplit partial wave
 // takes kt steps.  Fixed costs of a stream-K part, from the intercepts of
-// time against K on GB300 (1024 x 1024 x K, K = 1024 and 4096, in CUDA
-// graphs): the larger tiles' parts stored and added by the second kernel,
-// kDeferredFixup (about 11 us in all with its launch; 2 us more for the
-// 256 x 128 tile, whose intercepts measured 12.9 and 14.6 us at 1024^3 and
-// 1000 x 1500 x 777 against 10.8 and 12.5 for 128 x 256); the 64 x 64 tail
-// split, kSmallSplitFixup; the 64 x 64 split-all variant (256^3 and
-// below), 2 us.  The stream-K K steps of the 128 x 128 tile (two
-// CTAs per SM) also ran slower than its whole tiles, by kSharedSplitSlow
-// (1024^3, 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us
-// against 46.8, 52.0 and 149 estimated without it).
-constexpr double kDeferredFixup = 9.0;
-constexpr double kDeferredFixup256x128 = 11.0;
+// time against K and from per-variant timings on GB300 (CUDA graphs):
+//  - the larger tiles' parts, stored and then added by the second kernel:
+//    kDeferredBase plus kDeferredUsPerMB for each MB of parts (one slot per
+//    stream-K tile and per stream-K CTA), plus its launch; measured 6.7 us
+//    at 512^3 (9 MB of parts), 10-11 us at 1024^3 (23.5 MB), 12.5 us on
+//    1000 x 1500 x 777 (26 MB); 2 us more for the 256 x 128 tile (12.9 and
+//    14.6 us against 10.8 and 12.5 for 128 x 256 at 1024^3 and
+//    1000 x 1500 x 777);
+//  - the 64 x 64 tail split, kSmallSplitFixup;
+//  - the 64 x 64 split-all variant, kSplitAllFixup (7.2-9.2 us from 256^3 to
+//    768^3).
+// The stream-K K steps of the 128 x 128 tile (two CTAs per SM) also ran
+// slower than its whole tiles, by kSharedSplitSlow (1024^3,
+// 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us against
+// 46.8, 52.0 and 149 estimated without it).
+constexpr double kDeferredBase = 2.0;
+constexpr double kDeferredUsPerMB = 0.3;
+constexpr double kDeferred256x128 = 2.0;
 constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
+constexpr double kSplitAllFixup = 8.0;
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                  const sg::SplitK &plan) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
@@ -267,13 +274,16 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     auto wave = [&](double ctas, double steps) {
         return steps * t_step * std::min(cps, std::ceil(ctas / sms)) / cps;
     };
-    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) return wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas)) + 2.0;
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK)
+        return wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas)) + kSplitAllFixup;
     const double full = std::floor(tiles / P);
     const double rem = tiles - full * P;
     double t = full * kt * t_step;
     if (plan.sk_ctas > 0) {
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
-        const double fix = variant == SGEMM_VARIANT_TMA_256x128 ? kDeferredFixup256x128 : kDeferredFixup;
+        const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;
+        const double fix = kDeferredBase + kDeferredUsPerMB * parts_mb +
+                           (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0);
         t += plan.defer ? wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + fix + 2.0
                         : wave(plan.sk_ctas, steps) + kSmallSplitFixup;
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves

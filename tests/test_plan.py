@@ -157,7 +157,8 @@ def test_choices_measured_on_gb300():
     """The automatic choices the GB300 measurements settled: on each of these
     shapes and layouts the variant and copy chosen ran fastest, or within 1 %
     of the fastest, of every tile variant with and without re-layout
-    (CUDA-graph timings)."""
+    (CUDA-graph timings; 384^3, not listed, is the exception: the split-all
+    64 x 64 kernel at 11.6 us against 10.5 for its tail split)."""
     expect = {
         # copies, then complete waves, the stream-K wave and the kernel adding its parts
         (0, 0, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 1, 4),
@@ -166,6 +167,8 @@ def test_choices_measured_on_gb300():
         (1, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 2, 4),
         (0, 0, 4096, 4096, 4096): (V.VARIANT_TMA_256x128, 1, 4),
         # one stream-K wave over all tiles and the kernel adding its parts
+        (0, 0, 512, 512, 512): (V.VARIANT_TMA_128x128, 0, 2),
+        (0, 0, 768, 768, 768): (V.VARIANT_TMA_128x256, 0, 2),
         (0, 0, 1024, 1024, 1024): (V.VARIANT_TMA_128x256, 0, 2),
         (0, 0, 1000, 1500, 777): (V.VARIANT_TMA_128x256, 0, 2),
         (0, 0, 2048, 2048, 1024): (V.VARIANT_TMA_256x128, 1, 3),
