@@ -281,11 +281,14 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     double t = full * kt * t_step;
     if (plan.sk_ctas > 0) {
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
-        const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;
-        const double fix = kDeferredBase + kDeferredUsPerMB * parts_mb +
-                           (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0);
-        t += plan.defer ? wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + fix + 2.0
-                        : wave(plan.sk_ctas, steps) + kSmallSplitFixup;
+        if (plan.defer) {
+            const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;  // slots written and read
+            t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kDeferredBase +
+                 kDeferredUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0) +
+                 2.0;  // the launch of the kernel adding the parts
+        } else {
+            t += wave(plan.sk_ctas, steps) + kSmallSplitFixup;
+        }
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
     } else if (rem > 0) {
         t += wave(rem, kt);
@@ -303,7 +306,8 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
 // arrive and takes the split when G is at least 1.25 rem (less saved little
 // over whole tiles on GB300); the larger tiles, whose parts are 4-8 times
 // larger, leave them to a second kernel that adds them over the whole GPU
-// (deferred), and take the split when its estimate beats whole tiles.
+// (deferred), and take the split when its estimate beats whole tiles.  Under
+// the in-kernel test hook every tile takes the 64 x 64 tile's way.
 void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                sg::SplitK *sk) {
     const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;
