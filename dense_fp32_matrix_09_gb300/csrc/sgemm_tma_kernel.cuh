@@ -44,10 +44,13 @@
 //    the tiles left for the last, partial wave are divided evenly over up to
 //    a wave of CTAs, each of which walks a contiguous range of (tile, K step)
 //    iterations with its TMA pipeline running across tile boundaries.  A
-//    tile whose K range is split stores each part in a workspace slot, and
-//    the last CTA of the tile to arrive (arrival counter) adds the parts in
-//    ascending k order -- a fixed order, so results are deterministic -- and
-//    runs the epilogue.  The 64 x 64 split variant runs every tile this way.
+//    tile whose K range is split stores each part in a workspace slot; the
+//    parts are added in ascending k order -- a fixed order, so results are
+//    deterministic -- and the epilogue runs on the sum.  For the 64 x 64 tile
+//    the last CTA of the tile to arrive (arrival counter) adds them; for the
+//    larger tiles (SplitK::defer) sk_finish_kernel adds them over the whole
+//    GPU, launched as a programmatic dependent of the stream-K grid.  The
+//    64 x 64 split variant runs every tile this way.
 //  * Operand layouts (template parameter OP).  NN: A stored M x K and B
 //    stored K x N, as above.  TN: A stored K x M; its stage is BK rows of BM
 //    floats (no swizzle) and each thread owns groups of 4 consecutive rows,
