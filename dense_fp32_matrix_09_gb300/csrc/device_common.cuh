@@ -123,4 +123,34 @@ __device__ __forceinline__ bool named_barrier_or(int id, int nthreads, bool pred
     return out != 0;
 }
 
+// Thread-block cluster barrier over every thread of every CTA of the cluster:
+// memory operations before the arrive (release) are visible after the wait
+// (acquire) to the whole cluster, distributed shared memory included.  Every
+// thread of the cluster must execute it (no exited CTA waits for).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address, in the cluster's shared-memory window, of the byte at the offset
+// that `local` has in this CTA's shared memory, but in the shared memory of
+// CTA `rank` of the cluster (distributed shared memory).
+__device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+
+// 16-byte store into distributed shared memory (an address from dsmem_addr).
+__device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};"
+                 ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+
 }  // namespace sg

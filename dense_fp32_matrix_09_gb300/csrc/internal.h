@@ -44,7 +44,7 @@ struct TmaShape {
 // dp_tiles) * ceil(K / bk) iterations, taken tile by tile -- are shared by
 // sk_ctas further CTAs: CTA q gets iterations [floor(q*T/G), floor((q+1)*T/G))
 // (G = sk_ctas <= T), so a tile's K range may be split over consecutive CTAs;
-// the parts are summed in ascending k order by the last of them to finish.
+// the parts are summed in ascending k order (see `fixup`).
 // sk_ctas == 0 means no stream-K part (ws and counters unused).
 struct SplitK {
     int dp_tiles;   // leading tiles computed whole
@@ -52,10 +52,22 @@ struct SplitK {
     float *ws;      // (tiles - dp_tiles + sk_ctas) * bm * bn partial sums
     int *counters;  // one arrival counter per stream-K tile, zero between calls
     int cta0 = 0;   // index of this launch's first CTA in the dp_tiles + sk_ctas sequence
-    int defer = 0;  // nonzero: every part of a split tile stays in the workspace and a
-                    // second kernel adds them (no arrival counters); zero: the last CTA
-                    // of the tile to arrive adds them
+    int fixup = 0;  // who adds the parts of a split tile: kFixupLast, kFixupDeferred or kFixupShared
+    // Cluster split-K (sk_ctas == 0 only): ksplit > 1 CTAs per tile, launched as one
+    // thread-block cluster, CTA r of the cluster taking K steps [r*kt/ksplit,
+    // (r+1)*kt/ksplit); their partial tiles meet in distributed shared memory.
+    int ksplit = 1;
 };
+
+// How the parts of a split tile are added (always in ascending k order):
+//  - kFixupLast: the last CTA of the tile to arrive (arrival counter) adds
+//    them all and runs the epilogue;
+//  - kFixupDeferred: every part stays in the workspace and a second kernel
+//    adds them over the whole GPU (no counters);
+//  - kFixupShared: the CTAs whose K range ends in the tile wait until every
+//    part has arrived (arrival counter) and each adds one slice of the tile's
+//    elements and runs the epilogue on it; no second kernel.
+constexpr int kFixupLast = 0, kFixupDeferred = 1, kFixupShared = 2;
 
 // Operand layouts of the TMA-fed SIMT kernels: NN (A stored M x K, B K x N),
 // TN (A stored K x M) and NT (B stored N x K).  A map: box 32 x bm with the
@@ -70,6 +82,8 @@ bool tma_shape(int variant, TmaShape *out);
 cudaError_t tma_prepare(int variant);  // every operand layout
 // Resident CTAs per SM of a variant's kernel (0 on error).
 int tma_ctas_per_sm(int variant);
+// Resident clusters of `csize` CTAs of a variant's cluster split-K kernel (0 on error).
+int tma_max_clusters(int variant, int csize);
 cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA,
                        const CUtensorMap &tmB, const SplitK &sk, int smem_override,
                        cudaStream_t stream);  // NN

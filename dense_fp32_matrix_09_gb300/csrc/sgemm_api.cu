@@ -41,11 +41,13 @@ struct CallPlan {
 
 // Everything a plan depends on besides the handle's fixed device facts.
 struct PlanKey {
-    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode, sk_in_kernel;
+    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode, sk_sums,
+        ksplit_pin;
     bool operator==(const PlanKey &o) const {
         return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
                a_shared == o.a_shared && b_shared == o.b_shared && tma_ok == o.tma_ok && pinned == o.pinned &&
-               relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_in_kernel == o.sk_in_kernel;
+               relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_sums == o.sk_sums &&
+               ksplit_pin == o.ksplit_pin;
     }
 };
 
@@ -82,12 +84,14 @@ struct sgemm_ctx {
     int last_launches;  // kernel launches the last successful call enqueued
     int smem_override;
     int ctas_per_sm[SGEMM_VARIANT_COUNT_];  // measured occupancy of each TMA variant
+    int max_clusters[SGEMM_VARIANT_COUNT_][9];  // resident clusters of 2..8 CTAs (0: not measured)
     int math_mode;                          // sgemm_math_mode_t
     float *d_rl;                            // operand re-layout workspace (NULL if not allocated)
     size_t rl_floats;
     int relayout_mode;                      // sgemm_relayout_t
     int last_relayout;                      // operands the last call transposed (bit 0 A, bit 1 B)
-    int sk_in_kernel;                       // test hook: 1 = stream-K parts added in-kernel for every tile
+    int sk_sums;                            // test hook: sgemm_sk_sums_t, how stream-K parts are added
+    int ksplit_pin;                         // test hook: cluster split-K CTAs per tile (0 auto, 1 none)
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
     cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
@@ -216,6 +220,7 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     const long long G = sk_ctas_for(h, tiles * kt, tiles, slots, 64 * 64, 1);
     if (G < 2 * tiles) return;
     *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
+    sk->fixup = h->sk_sums == SGEMM_SK_SUMS_SHARED ? sg::kFixupShared : sg::kFixupLast;
 }
 
 // Estimated time, in microseconds (only the ranking matters), of `variant`'s
@@ -250,11 +255,23 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us against
 // 46.8, 52.0 and 149 estimated without it).
 constexpr double kDeferredBase = 2.0;
-constexpr double kDeferredUsPerMB = 0.3;
+constexpr double kDeferredUsPerMB = 0.2;
+constexpr double kDeferredKneeMB = 25.0;
+constexpr double kDeferredUsPerMBOver = 0.6;
 constexpr double kDeferred256x128 = 2.0;
 constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
 constexpr double kSplitAllFixup = 8.0;
+constexpr double kSharedBase = 8.0;
+constexpr double kSharedUsPerMB = 0.12;
+constexpr double kShared256x128 = 1.0;
+// cluster split-K, per tile variant (128 x 256, 128 x 128, 64 x 64,
+// 256 x 128): medians of the time beyond the CTAs' K steps measured on
+// GB300 (CUDA graphs, 256^3 to 1536^3, 1024 x 1024 x 4096 and
+// 1000 x 1500 x 777, one wave of clusters of 2..8 CTAs), growing with the
+// cluster size by kClusterPerCta per CTA past two
+constexpr double kClusterFixed[4] = {7.0, 6.0, 3.9, 8.0};
+constexpr double kClusterPerCta = 0.25;
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                  const sg::SplitK &plan) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
@@ -276,16 +293,27 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     };
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK)
         return wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas)) + kSplitAllFixup;
+    if (plan.ksplit > 1) {
+        // cluster split-K: tiles * ksplit CTAs of ceil(kt / ksplit) steps, one
+        // per SM, wave by wave, then each CTA adds a 1/ksplit slice of its
+        // tile's ksplit parts through distributed shared memory
+        const double ctas = tiles * plan.ksplit, steps = std::ceil(kt / plan.ksplit);
+        return std::ceil(ctas / sms) * steps * t_step / cps + kClusterFixed[vi] + kClusterPerCta * (plan.ksplit - 2);
+    }
     const double full = std::floor(tiles / P);
     const double rem = tiles - full * P;
     double t = full * kt * t_step;
     if (plan.sk_ctas > 0) {
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
-        if (plan.defer) {
-            const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;  // slots written and read
+        const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;  // slots written and read
+        if (plan.fixup == sg::kFixupDeferred) {
             t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kDeferredBase +
-                 kDeferredUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0) +
+                 kDeferredUsPerMB * parts_mb + kDeferredUsPerMBOver * std::max(0.0, parts_mb - kDeferredKneeMB) +
+                 (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0) +
                  2.0;  // the launch of the kernel adding the parts
+        } else if (plan.fixup == sg::kFixupShared) {
+            t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kSharedBase +
+                 kSharedUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kShared256x128 : 0.0);
         } else {
             t += wave(plan.sk_ctas, steps) + kSmallSplitFixup;
         }
@@ -317,18 +345,66 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
     const long long full = tiles / slots, rem = tiles - full * slots;
     if (rem == 0 || rem > h->n_counters) return;
     const long long G = sk_ctas_for(h, rem * kt, rem, slots, 1LL * sh.bm * sh.bn, 2);
-    const bool defer = sh.bm * sh.bn > 64 * 64 && h->sk_in_kernel == 0;
-    if (G <= rem || (!defer && G * 4 < rem * 5)) return;
-    sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
-    cand.defer = defer ? 1 : 0;
-    if (defer && plan_time(h, variant, sh, M, N, K, batch, op, cand) >= plan_time(h, variant, sh, M, N, K, batch, op, *sk))
-        return;
-    *sk = cand;
+    const bool large = sh.bm * sh.bn > 64 * 64;
+    // how the parts are added: the hook's choice, else (larger tiles) the
+    // cheaper of the second kernel and the shared in-kernel sums
+    int fixups[2] = {sg::kFixupLast, -1};
+    if (h->sk_sums == SGEMM_SK_SUMS_SHARED) {
+        fixups[0] = sg::kFixupShared;
+    } else if (large && h->sk_sums == SGEMM_SK_SUMS_DEFERRED) {
+        fixups[0] = sg::kFixupDeferred;
+    } else if (large && h->sk_sums == SGEMM_SK_SUMS_AUTO) {
+        fixups[0] = sg::kFixupDeferred;
+        fixups[1] = sg::kFixupShared;
+    }
+    if (G <= rem || (fixups[0] == sg::kFixupLast && G * 4 < rem * 5)) return;
+    // the test hook's modes split whenever they can; automatic, by the estimate
+    const bool forced = h->sk_sums != SGEMM_SK_SUMS_AUTO || fixups[0] == sg::kFixupLast;
+    double best = forced ? -1.0 : plan_time(h, variant, sh, M, N, K, batch, op, *sk);
+    for (int f : fixups) {
+        if (f < 0) continue;
+        sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
+        cand.fixup = f;
+        const double c = forced ? 0.0 : plan_time(h, variant, sh, M, N, K, batch, op, cand);
+        if (best < 0.0 || c < best) {
+            best = c;
+            *sk = cand;
+        }
+    }
+}
+
+// Cluster split-K for the whole-tile variants: ksplit = 2..8 CTAs per tile
+// (one thread-block cluster), taken when all tiles x ksplit CTAs fit in one
+// wave, K has ksplit steps, and its estimate beats the plan so far (the
+// test hook's ksplit_pin forces a count whenever K has that many steps, or
+// rules clusters out).
+void plan_cluster(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
+                  sg::SplitK *sk) {
+    if (h->ksplit_pin == 1) return;
+    const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;
+    const long long kt = cdiv(K, sh.bk);
+    double best = plan_time(h, variant, sh, M, N, K, batch, op, *sk);
+    for (int S = 2; S <= 8; ++S) {
+        if (S > kt || tiles * S > 0x7fffffffLL) break;
+        if (h->ksplit_pin > 1 && S != h->ksplit_pin) continue;
+        // one wave of clusters, one CTA per SM: as many clusters as can be
+        // resident at once (measured on the device; without a device, the SMs
+        // grouped by S)
+        const long long fit = h->max_clusters[variant][S] > 0 ? h->max_clusters[variant][S] : h->num_sms / S;
+        if (h->ksplit_pin == 0 && tiles > fit) continue;
+        sg::SplitK cand{static_cast<int>(tiles), 0, nullptr, nullptr};
+        cand.ksplit = S;
+        const double c = plan_time(h, variant, sh, M, N, K, batch, op, cand);
+        if (h->ksplit_pin == S || c < best * 0.999) {
+            best = c;
+            *sk = cand;
+        }
+    }
 }
 
 // CTAs per stream-K tile (rounded up; 1 without stream-K), for reporting.
 int splits_of(const sg::SplitK &sk, int tiles) {
-    if (sk.sk_ctas <= 0) return 1;
+    if (sk.sk_ctas <= 0) return sk.ksplit;
     return std::max(2, cdiv(sk.sk_ctas, std::max(1, tiles - sk.dp_tiles)));
 }
 
@@ -344,6 +420,7 @@ double variant_cost(const sgemm_ctx *h, int variant, int M, int N, int K, int ba
         if (plan->sk_ctas == 0) return 1e300;  // runs as the whole-tile 64 x 64 variant
     } else {
         plan_tail(h, variant, sh, M, N, K, batch, op, plan);
+        plan_cluster(h, variant, sh, M, N, K, batch, op, plan);
     }
     return plan_time(h, variant, sh, M, N, K, batch, op, *plan);
 }
@@ -506,13 +583,14 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         if (p.sk.sk_ctas == 0) variant = SGEMM_VARIANT_TMA_64x64;
     } else {
         plan_tail(h, variant, sh, p.kM, p.kN, K, batch, p.op, &p.sk);
+        plan_cluster(h, variant, sh, p.kM, p.kN, K, batch, p.op, &p.sk);
     }
     p.kind = kPlanTma;
     p.variant = variant;
     p.splits = splits_of(p.sk, tiles * batch);
     // transposes, then the whole-tile waves and the stream-K CTAs
     p.launches = (p.copies & 1) + ((p.copies >> 1) & 1) + (p.sk.sk_ctas > 0 && p.sk.dp_tiles > 0 ? 2 : 1) +
-                 (p.sk.sk_ctas > 0 && p.sk.defer ? 1 : 0);
+                 (p.sk.sk_ctas > 0 && p.sk.fixup == sg::kFixupDeferred ? 1 : 0);
     return p;
 }
 
@@ -520,7 +598,7 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                      long long strideB, bool tma_ok) {
     const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, tma_ok, h->pinned,
-                      h->relayout_mode, h->math_mode, h->sk_in_kernel};
+                      h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
     const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
@@ -662,6 +740,9 @@ int sgemm_create(sgemm_handle_t *out) {
     h->n_counters = kCounters;
     h->last_variant = -1;
     for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) h->ctas_per_sm[v] = occupancy[v];
+    for (int v : {SGEMM_VARIANT_TMA_128x256, SGEMM_VARIANT_TMA_256x128, SGEMM_VARIANT_TMA_128x128,
+                  SGEMM_VARIANT_TMA_64x64})
+        for (int S = 2; S <= 8; ++S) h->max_clusters[v][S] = sg::tma_max_clusters(v, S);
     bool ok = cudaMalloc(&h->d_status, sizeof(int)) == cudaSuccess &&
               cudaMalloc(&h->d_ws, kWorkspaceBytes) == cudaSuccess &&
               cudaMalloc(&h->d_counters, kCounters * sizeof(int)) == cudaSuccess &&
@@ -792,10 +873,17 @@ int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes) {
     return SGEMM_OK;
 }
 
-int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int in_kernel) {
+int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
-    if (in_kernel != 0 && in_kernel != 1) return SGEMM_ERR_INVALID_VALUE;
-    h->sk_in_kernel = in_kernel;
+    if (ksplit < 0 || ksplit > 8) return SGEMM_ERR_INVALID_VALUE;
+    h->ksplit_pin = ksplit;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int mode) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (mode < SGEMM_SK_SUMS_AUTO || mode > SGEMM_SK_SUMS_SHARED) return SGEMM_ERR_INVALID_VALUE;
+    h->sk_sums = mode;
     return SGEMM_OK;
 }
 
@@ -1247,7 +1335,8 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     c.math_mode = math_mode;
     c.pinned = pinned;
     for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) c.ctas_per_sm[v] = ctas_per_sm[v];
-    for (int i = 0; i < 10; ++i) out[i] = 0;
+    for (int i = 0; i < 11; ++i) out[i] = 0;
+    out[10] = 1;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;  // nothing runs
     if (alpha == 0.f || K == 0) {
         out[0] = kPlanScale;
@@ -1271,7 +1360,8 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     }
     out[7] = p.launches;
     out[8] = p.splits;
-    out[9] = p.kind == kPlanTma && p.sk.sk_ctas > 0 && p.sk.defer ? 1 : 0;
+    out[9] = p.kind == kPlanTma && p.sk.sk_ctas > 0 ? p.sk.fixup : 0;
+    out[10] = p.kind == kPlanTma ? p.sk.ksplit : 1;
     return SGEMM_OK;
 }
 

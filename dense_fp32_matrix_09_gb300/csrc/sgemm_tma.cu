@@ -25,6 +25,8 @@ cudaError_t tma_prepare(int variant) {
 
 int tma_ctas_per_sm(int variant) { return ctas_per_sm_op<kOpNN>(variant); }
 
+int tma_max_clusters(int variant, int csize) { return max_clusters_op<kOpNN>(variant, csize); }
+
 cudaError_t launch_tma(int variant, const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
                        const SplitK &sk, int smem_override, cudaStream_t stream) {
     return launch_op<kOpNN>(variant, g, tmA, tmB, sk, smem_override, stream);

@@ -354,34 +354,43 @@ __device__ __forceinline__ int sk_first_cta(long long x, long long T, int G) {
     return static_cast<int>(((x + 1) * G + T - 1) / T) - 1;
 }
 
-// Last CTA of a split tile: add the parts in slots tl + q_first .. tl +
-// q_last in ascending k order -- a fixed order, so the result does not
-// depend on which CTA finished last -- a chunk of float4 groups at a time,
-// and run the epilogue on each sum.  The caller's accumulators are dead here
-// (its own part is already in the workspace), so the chunk reuses their
-// registers.
+// Add the parts of split tile tl (slots tl + q_first .. tl + q_last) for
+// this CTA's float4 groups [u_begin, u_end) -- group u of every consumer
+// thread, which is where the part layout keeps accumulator group u of the
+// thread with the same index -- in ascending k order (a fixed order, so the
+// result does not depend on which CTA finished when), and run the epilogue
+// on each sum.  The caller's accumulators are dead here (its own part is
+// already in the workspace), so the loads reuse their registers: groups in
+// chunks of kChunk, parts kU at a time, all loads of a round independent so
+// that they are in flight together (each round costs an L2 round trip).
 template <class C, int OP>
 __device__ __forceinline__ void sk_reduce_epilogue(const GemmArgs g, const float *ws, float *Cb, int tl, int q_first,
-                                                int q_last, int m0, int n0) {
+                                                   int q_last, int m0, int n0, int u_begin = 0,
+                                                   int u_end = C::TM * C::TN4) {
     constexpr size_t kTileFloats = static_cast<size_t>(C::BM) * C::BN;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
     const int lane_m = lane / C::LANES_N, lane_n = lane % C::LANES_N;
-    // groups in chunks of kChunk, parts kU at a time: the kChunk * kU loads of
-    // a round are independent, so they are in flight together (a split tile
-    // has several parts and each round costs an L2 round trip)
     constexpr int kGroups = C::TM * C::TN4;
-    constexpr int kChunk = kGroups < 8 ? kGroups : 8;
+    // 32 float4 loads in flight where a thread may have 255 registers, else 16
+    constexpr int kRegs = 65536 / (C::kThreads * C::MIN_CTAS);
+    constexpr int kWant = kRegs >= 255 ? 8 : 4;
+    constexpr int kChunk = kGroups < kWant ? kGroups : kWant;
     constexpr int kU = 4;
-    static_assert(kGroups % kChunk == 0, "whole chunks");
     const size_t part_stride = kTileFloats / 4;  // float4s per part
     const float4 *base = reinterpret_cast<const float4 *>(ws) + static_cast<size_t>(tl) * part_stride + tid;
 #pragma unroll 1
-    for (int u0 = 0; u0 < kGroups; u0 += kChunk) {
-        float4 sum[kChunk];
-        const float4 *pc = base + u0 * C::kConsumers;
+    for (int u0 = u_begin; u0 < u_end; u0 += kChunk) {
+        // a last chunk of fewer groups loads its last group again in the
+        // slots past the end (every slot stays defined, so the arrays stay in
+        // registers) and stores only its own groups
+        const int cnt = min(kChunk, u_end - u0);
+        int off[kChunk];
 #pragma unroll
-        for (int c = 0; c < kChunk; ++c) sum[c] = __ldcg(pc + static_cast<size_t>(q_first) * part_stride + c * C::kConsumers);
+        for (int c = 0; c < kChunk; ++c) off[c] = min(u0 + c, u_end - 1) * C::kConsumers;
+        float4 sum[kChunk];
+#pragma unroll
+        for (int c = 0; c < kChunk; ++c) sum[c] = __ldcg(base + static_cast<size_t>(q_first) * part_stride + off[c]);
         int qq = q_first + 1;
 #pragma unroll 1
         for (; qq + kU - 1 <= q_last; qq += kU) {
@@ -389,8 +398,7 @@ __device__ __forceinline__ void sk_reduce_epilogue(const GemmArgs g, const float
 #pragma unroll
             for (int r = 0; r < kU; ++r)
 #pragma unroll
-                for (int c = 0; c < kChunk; ++c)
-                    p[r][c] = __ldcg(pc + static_cast<size_t>(qq + r) * part_stride + c * C::kConsumers);
+                for (int c = 0; c < kChunk; ++c) p[r][c] = __ldcg(base + static_cast<size_t>(qq + r) * part_stride + off[c]);
 #pragma unroll
             for (int r = 0; r < kU; ++r)  // ascending k
 #pragma unroll
@@ -402,24 +410,65 @@ __device__ __forceinline__ void sk_reduce_epilogue(const GemmArgs g, const float
         for (; qq <= q_last; ++qq) {
             float4 p[kChunk];
 #pragma unroll
-            for (int c = 0; c < kChunk; ++c) p[c] = __ldcg(pc + static_cast<size_t>(qq) * part_stride + c * C::kConsumers);
+            for (int c = 0; c < kChunk; ++c) p[c] = __ldcg(base + static_cast<size_t>(qq) * part_stride + off[c]);
 #pragma unroll
             for (int c = 0; c < kChunk; ++c) {
                 sum[c].x += p[c].x; sum[c].y += p[c].y; sum[c].z += p[c].z; sum[c].w += p[c].w;
             }
         }
 #pragma unroll
-        for (int c = 0; c < kChunk; ++c) {
-            const float v[4] = {sum[c].x, sum[c].y, sum[c].z, sum[c].w};
-            epilogue_group<C, OP>(g, Cb, m0, n0, wm, wn, lane_m, lane_n, (u0 + c) / C::TN4, (u0 + c) % C::TN4, v);
-        }
+        for (int c = 0; c < kChunk; ++c)
+            if (c < cnt) {
+                const float v[4] = {sum[c].x, sum[c].y, sum[c].z, sum[c].w};
+                epilogue_group<C, OP>(g, Cb, m0, n0, wm, wn, lane_m, lane_n, (u0 + c) / C::TN4, (u0 + c) % C::TN4,
+                                      v);
+            }
     }
 }
 
-template <class C, bool SPLIT, int OP>
+// Acquire load of an arrival counter (the parts its arrivals announce are
+// visible after it).
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *counter >= target; false (timeout bit set in *status)
+// if that does not happen within kWaitLimitNs.
+__device__ __forceinline__ bool wait_counter(const int *counter, int target, int *status) {
+    if (ld_acquire_gpu(counter) >= target) return true;
+    const unsigned long long t0 = global_timer_ns();
+    for (unsigned long long it = 0; ld_acquire_gpu(counter) < target; ++it) {
+        if (global_timer_ns() - t0 > kWaitLimitNs || it > (1ull << 32)) {
+            atomicOr(status, kDevTimeoutBit);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Cluster split-K: the most float4 groups (per thread) an owner's slots take,
+// over clusters of 2..8 CTAs: S ranks x the owner's ceil(G / S) groups.
+__host__ __device__ constexpr int cluster_slot_groups(int groups) {
+    int most = 0;
+    for (int S = 2; S <= 8; ++S) {
+        const int n = S * ((groups + S - 1) / S);
+        most = n > most ? n : most;
+    }
+    return most;
+}
+
+// Kernel modes (template parameter MODE): whole tiles; the stream-K CTAs of a
+// hybrid grid; cluster split-K (one cluster of sk.ksplit CTAs per tile).
+constexpr int kModeWhole = 0, kModeStreamK = 1, kModeCluster = 2;
+
+template <class C, int MODE, int OP>
 __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g, const SplitK sk, const int group_m) {
+    constexpr bool SPLIT = MODE == kModeStreamK;
+    constexpr bool CLUSTER = MODE == kModeCluster;
     extern __shared__ uint8_t smem_raw[];
     // a stream-K grid lets the kernel that adds its parts be scheduled now: its
     // blocks take SM room as this grid's CTAs leave and wait for its completion
@@ -450,6 +499,13 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int cta = static_cast<int>(blockIdx.x) + (SPLIT ? sk.cta0 : 0);
     int tile0 = cta, k00 = 0, n0it = kt, n_iter = kt, q = -1;
     long long T = 0;
+    int crank = 0;  // cluster split-K: this CTA's rank among its tile's ksplit CTAs (one cluster)
+    if (CLUSTER) {
+        tile0 = cta / sk.ksplit;
+        crank = cta - tile0 * sk.ksplit;
+        k00 = crank * kt / sk.ksplit;
+        n_iter = n0it = (crank + 1) * kt / sk.ksplit - k00;  // >= 1: the host keeps ksplit <= kt
+    }
     if (SPLIT && cta >= sk.dp_tiles) {
         q = cta - sk.dp_tiles;
         T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
@@ -587,14 +643,80 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
         }
         ++nseg_done;
-        if (sk.defer) continue;  // the finishing kernel adds the parts after this grid
+        if (sk.fixup == kFixupDeferred) continue;  // the finishing kernel adds the parts after this grid
         __threadfence();
         named_barrier_sync(1, C::kConsumers);
+        if (sk.fixup == kFixupShared) {
+            if (tid == 0) atomicAdd(&sk.counters[tl], 1);  // this part has arrived
+            // the CTAs whose K range ends in the tile add its parts, a slice each
+            if (seg == nseg - 1) split_last |= 1u << seg;
+            continue;
+        }
         if (tid == 0) s_flag[seg] = (atomicAdd(&sk.counters[tl], 1) == q_last - q_first);
         named_barrier_sync(1, C::kConsumers);
         split_last |= static_cast<unsigned>(s_flag[seg] != 0) << seg;
     }
 
+    if constexpr (CLUSTER) {
+        // Cluster split-K: the tile's S = ksplit CTAs are one cluster, and
+        // CTA r owns float4 groups [r*G/S, (r+1)*G/S) of the tile (group u of
+        // thread tid holds accumulators ii = u / TN4, columns 4(u % TN4) ..
+        // +3).  Once every CTA of the cluster is past its main loop (cluster
+        // barrier: their stage buffers are free), each pushes every group
+        // into the shared memory of the group's owner -- slot [r][u - first
+        // owned group][tid] -- with distributed-shared-memory stores; after a
+        // second barrier makes them visible, each owner adds its slots in
+        // rank (= ascending k) order and runs the epilogue on the sums.  No
+        // shared memory of another CTA is touched after that barrier.  An
+        // abort (a bounded wait gave up) is agreed on within the CTA first;
+        // the CTA then waits for its own loads in flight, pushes nothing and
+        // still takes part in both barriers (C is then undefined, the status
+        // word set).
+        constexpr int kGroups = C::TM * C::TN4;
+        static_assert(cluster_slot_groups(kGroups) * C::kConsumers * 16 <=
+                          C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0),
+                      "an owner's slots fit in the stage (and NT transpose) buffers, below the mbarriers");
+        const int S = sk.ksplit;
+        const bool bad = named_barrier_or(1, C::kConsumers, aborted);
+        if (bad && tid == 0)
+            for (int t = max(0, issued - C::STAGES); t < issued; ++t)
+                mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
+        cluster_sync();
+        float4 *slots = reinterpret_cast<float4 *>(smem);
+        if (!bad) {
+            int owner = 0, o_first = 0, o_end = kGroups / S;  // the owner of group u, and its groups
+#pragma unroll
+            for (int u = 0; u < kGroups; ++u) {
+                while (u >= o_end) {
+                    ++owner;
+                    o_first = o_end;
+                    o_end = (owner + 1) * kGroups / S;
+                }
+                const int ii = u / C::TN4, jj = u % C::TN4;
+                const int n_own = o_end - o_first;
+                float4 *dst = slots + (crank * n_own + (u - o_first)) * C::kConsumers + tid;
+                st_dsmem_f4(dsmem_addr(dst, static_cast<uint32_t>(owner)),
+                            make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1], acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
+            }
+        }
+        cluster_sync();
+        if (!bad) {
+            const int ub = crank * kGroups / S, ue = (crank + 1) * kGroups / S, n_own = ue - ub;
+#pragma unroll 1
+            for (int u = ub; u < ue; ++u) {
+                const float4 *src = slots + (u - ub) * C::kConsumers + tid;
+                float4 sum = src[0];
+#pragma unroll 1
+                for (int r = 1; r < S; ++r) {  // rank order = ascending k
+                    const float4 v = src[r * n_own * C::kConsumers];
+                    sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+                }
+                const float vv[4] = {sum.x, sum.y, sum.z, sum.w};
+                epilogue_group<C, OP>(g, Cb, m0w, n0w, wm, wn, lane_m, lane_n, u / C::TN4, u % C::TN4, vv);
+            }
+        }
+        return;
+    }
     if (aborted && tid == 0) {
         // Wait (bounded) for the loads still in flight so that the CTA never
         // exits while TMA writes into its shared memory.
@@ -604,19 +726,45 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (aborted) return;
     if constexpr (SPLIT) {
         if (q >= 0 && nseg_done > 0) {
-            // stream-K: finish each split tile whose last part this CTA delivered
+            // stream-K: finish each split tile whose last part this CTA
+            // delivered (kFixupLast), or add this CTA's slice of the tile its
+            // K range ends in (kFixupShared)
 #pragma unroll 1
             for (int sg2 = 0; sg2 < 2; ++sg2) {
                 if (!((split_last >> sg2) & 1)) continue;
                 const int tile = tile0 + sg2, tl = tile - sk.dp_tiles;
                 int tm, tn;
                 tile_coords(tile % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
-                __threadfence();
-                sk_reduce_epilogue<C, OP>(g, sk.ws, g.C + static_cast<long long>(tile / tiles_per) * g.sC, tl,
-                                          sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas),
-                                          sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas),
-                                          tm * C::BM, tn * C::BN);
-                if (tid == 0) sk.counters[tl] = 0;  // ready for the next call
+                const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
+                const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+                float *Ct = g.C + static_cast<long long>(tile / tiles_per) * g.sC;
+                if (sk.fixup == kFixupShared) {
+                    // The adders are q_first .. q_first + n_add - 1: every CTA of
+                    // the tile but the last, whose range usually runs on into
+                    // the next tile (it adds here only if its range ends with
+                    // this tile).  Once all n_parts parts have arrived, adder
+                    // h takes float4 groups [h*G/n_add, (h+1)*G/n_add).  Each
+                    // adder counts itself after its wait; the last one resets
+                    // the counter for the next call.
+                    const int n_parts = q_last - q_first + 1;
+                    const long long e_last = (static_cast<long long>(q_last) + 1) * T / sk.sk_ctas;
+                    const int n_add = q_last - q_first + (e_last <= static_cast<long long>(tl + 1) * kt ? 1 : 0);
+                    bool bad = false;
+                    if (tid == 0) {
+                        bad = !wait_counter(&sk.counters[tl], n_parts, g.status);
+                        if (!bad && atomicAdd(&sk.counters[tl], 1) == n_parts + n_add - 1) sk.counters[tl] = 0;
+                    }
+                    if (named_barrier_or(1, C::kConsumers, bad)) return;
+                    __threadfence();
+                    constexpr int kGroups = C::TM * C::TN4;
+                    const int h = q - q_first;
+                    sk_reduce_epilogue<C, OP>(g, sk.ws, Ct, tl, q_first, q_last, tm * C::BM, tn * C::BN,
+                                              h * kGroups / n_add, (h + 1) * kGroups / n_add);
+                } else {
+                    __threadfence();
+                    sk_reduce_epilogue<C, OP>(g, sk.ws, Ct, tl, q_first, q_last, tm * C::BM, tn * C::BN);
+                    if (tid == 0) sk.counters[tl] = 0;  // ready for the next call
+                }
             }
             return;
         }
@@ -679,19 +827,58 @@ TmaShape shape_of() {
     return TmaShape{C::BM, C::BN, C::BK, C::kThreads, C::kSmemBytes, C::MIN_CTAS};
 }
 
+// Cluster split-K launches ask for at least this much dynamic shared memory,
+// so that no SM holds two of their CTAs: the planner takes cluster split-K
+// only while every CTA fits on an SM of its own, and the block scheduler
+// would otherwise pack the CTAs of a cluster two or three to an SM (measured:
+// 128 x 128 tiles in clusters of 8 ran twice as long as with one per SM).
+constexpr int kClusterSmemFloor = 120 * 1024;
+
+template <class C, int OP>
+constexpr int cluster_smem_bytes() {
+    return smem_bytes<C, OP>() > kClusterSmemFloor ? smem_bytes<C, OP>() : kClusterSmemFloor;
+}
+
 template <class C, int OP>
 cudaError_t prepare_one() {
-    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, false, OP>,
+    cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeWhole, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<C, OP>());
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeCluster, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 cluster_smem_bytes<C, OP>());
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sgemm_tma_kernel<C, true, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeStreamK, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem_bytes<C, OP>());
+}
+
+// Clusters of `csize` CTAs of the cluster split-K kernel that can be resident
+// at once (0 on error): cluster placement within the GPCs can leave fewer
+// than SMs x CTAs per SM / csize.
+template <class C, int OP>
+int max_clusters_one(int csize) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(csize));
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = cluster_smem_bytes<C, OP>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sgemm_tma_kernel<C, kModeCluster, OP>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 template <class C, int OP>
 int ctas_per_sm_one() {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm_tma_kernel<C, false, OP>, C::kThreads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sgemm_tma_kernel<C, kModeWhole, OP>, C::kThreads,
                                                       smem_bytes<C, OP>()) != cudaSuccess)
         return 0;
     return n;
@@ -708,17 +895,38 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         1LL * ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN) * g.batch;
     const int smem = smem_override > 0 ? smem_override : smem_bytes<C, OP>();
     if (g.batch < 1 || g.batch > 65535 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
-    if (sk.sk_ctas <= 0) {
-        sgemm_tma_kernel<C, false, OP><<<static_cast<unsigned>(tiles), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
+    if (sk.sk_ctas <= 0 && sk.ksplit > 1) {
+        // cluster split-K: ksplit CTAs per tile, one cluster each
+        if (sk.ksplit > 8 || tiles * sk.ksplit > 0x7fffffffLL) return cudaErrorInvalidValue;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>(tiles * sk.ksplit));
+        cfg.blockDim = dim3(C::kThreads);
+        cfg.dynamicSmemBytes = smem_override > 0 ? smem_override : cluster_smem_bytes<C, OP>();
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = sk.ksplit;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_tma_kernel<C, kModeCluster, OP>, tmA, tmB, g, sk,
+                                                 static_cast<int>(kGroupM));
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();  // a rejected launch leaves nothing for the next call to report
+            return e;
+        }
+    } else if (sk.sk_ctas <= 0) {
+        sgemm_tma_kernel<C, kModeWhole, OP><<<static_cast<unsigned>(tiles), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
                                                                                                    kGroupM);
     } else {
         // the complete waves with the whole-tile kernel, then the stream-K CTAs
         if (sk.dp_tiles > 0)
-            sgemm_tma_kernel<C, false, OP><<<sk.dp_tiles, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+            sgemm_tma_kernel<C, kModeWhole, OP><<<sk.dp_tiles, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
         SplitK s2 = sk;
         s2.cta0 = sk.dp_tiles;
-        sgemm_tma_kernel<C, true, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
-        if (sk.defer) {
+        sgemm_tma_kernel<C, kModeStreamK, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
+        if (sk.fixup == kFixupDeferred) {
             // a programmatic dependent of the stream-K grid (it waits for it on the device)
             cudaLaunchConfig_t cfg{};
             cfg.gridDim = dim3(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles));
@@ -731,7 +939,10 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             const cudaError_t e = cudaLaunchKernelEx(&cfg, sk_finish_kernel<C, OP>, g, sk, static_cast<int>(kGroupM));
-            if (e != cudaSuccess) return e;
+            if (e != cudaSuccess) {
+                (void)cudaGetLastError();
+                return e;
+            }
         }
     }
     return cudaGetLastError();
@@ -766,6 +977,18 @@ int ctas_per_sm_op(int variant) {
         case SGEMM_VARIANT_TMA_128x128: return ctas_per_sm_one<MCfg<OP>, OP>();
         case SGEMM_VARIANT_TMA_64x64:
         case SGEMM_VARIANT_TMA_64x64_SPLITK: return ctas_per_sm_one<CfgS, OP>();
+        default: return 0;
+    }
+}
+
+template <int OP>
+int max_clusters_op(int variant, int csize) {
+    switch (variant) {
+        case SGEMM_VARIANT_TMA_128x256: return max_clusters_one<LCfg<OP>, OP>(csize);
+        case SGEMM_VARIANT_TMA_256x128: return max_clusters_one<XCfg<OP>, OP>(csize);
+        case SGEMM_VARIANT_TMA_128x128: return max_clusters_one<MCfg<OP>, OP>(csize);
+        case SGEMM_VARIANT_TMA_64x64:
+        case SGEMM_VARIANT_TMA_64x64_SPLITK: return max_clusters_one<CfgS, OP>(csize);
         default: return 0;
     }
 }

@@ -46,6 +46,8 @@ IN_F16 = 2
 RELAYOUT_AUTO = 0
 RELAYOUT_OFF = 1
 RELAYOUT_ALWAYS = 2
+# sgemm_sk_sums_t: how a stream-K tile's parts are added (test hook)
+SK_SUMS_AUTO, SK_SUMS_LAST, SK_SUMS_DEFERRED, SK_SUMS_SHARED = 0, 1, 2, 3
 GEMM_VARIANTS = (VARIANT_TMA_256x128, VARIANT_TMA_128x256, VARIANT_TMA_128x128, VARIANT_TMA_64x64,
                  VARIANT_TMA_64x64_SPLITK, VARIANT_GENERIC, VARIANT_TC_3XTF32, VARIANT_TC_3XTF32_PAIR)
 
@@ -57,7 +59,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
            "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
-           "sgemm_debug_set_stream_k_sums")
+           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split")
 
 
 class SgemmError(RuntimeError):
@@ -103,6 +105,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_timeout_probe.argtypes = [vp, ctypes.c_longlong, vp]
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
         L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
+        L.sgemm_debug_set_cluster_split.argtypes = [vp, i32]
         L.sgemm_status_string.argtypes = [i32]
         L.sgemm_status_string.restype = ctypes.c_char_p
         L.sgemm_variant_name.argtypes = [i32]
@@ -273,7 +276,9 @@ def sgemm_relayout_capacity(h) -> int:
 
 
 PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits",
-               "deferred")
+               "fixup", "ksplit")
+# "fixup": how the stream-K tiles' parts are added (0 last CTA or no stream-K, 1 second kernel, 2 shared)
+FIXUP_LAST, FIXUP_DEFERRED, FIXUP_SHARED = 0, 1, 2
 PLAN_NOTHING, PLAN_SCALE, PLAN_TENSOR_CORE, PLAN_GENERIC, PLAN_TMA = 0, 1, 2, 3, 4
 
 
@@ -303,8 +308,14 @@ def sgemm_debug_set_smem_override(h, nbytes: int) -> None:
     _check(lib().sgemm_debug_set_smem_override(h, int(nbytes)), "sgemm_debug_set_smem_override")
 
 
-def sgemm_debug_set_stream_k_sums(h, in_kernel: int) -> None:
-    _check(lib().sgemm_debug_set_stream_k_sums(h, int(in_kernel)), "sgemm_debug_set_stream_k_sums")
+def sgemm_debug_set_cluster_split(h, ksplit: int) -> None:
+    """0: automatic; 1: no cluster split-K; 2..8: that many CTAs per tile."""
+    _check(lib().sgemm_debug_set_cluster_split(h, int(ksplit)), "sgemm_debug_set_cluster_split")
+
+
+def sgemm_debug_set_stream_k_sums(h, mode: int) -> None:
+    """mode: one of SK_SUMS_AUTO, SK_SUMS_LAST, SK_SUMS_DEFERRED, SK_SUMS_SHARED."""
+    _check(lib().sgemm_debug_set_stream_k_sums(h, int(mode)), "sgemm_debug_set_stream_k_sums")
 
 
 class Sgemm:

@@ -341,15 +341,43 @@ int sgemm_debug_bank_probe(sgemm_handle_t h, int padded, int ctas, int iters, fl
  * (SGEMM_ERR_LAUNCH) before anything runs.  0 restores normal launches. */
 int sgemm_debug_set_smem_override(sgemm_handle_t h, int bytes);
 
+/* How a call adds the partial sums of a tile whose K range is split over
+ * stream-K CTAs (sgemm_debug_set_stream_k_sums).  Every mode adds a tile's
+ * parts in ascending k order, so a tile split the same way gets the same
+ * bits in every mode. */
+typedef enum {
+    SGEMM_SK_SUMS_AUTO = 0,     /* the library's choice (default) */
+    SGEMM_SK_SUMS_LAST = 1,     /* the last CTA of the tile to arrive adds them all; the larger tiles
+                                   split from 1.25 stream-K CTAs per tile as the 64 x 64 tile does */
+    SGEMM_SK_SUMS_DEFERRED = 2, /* tiles larger than 64 x 64: every part stays in the workspace and a
+                                   second kernel adds them (64 x 64 tiles: as LAST) */
+    SGEMM_SK_SUMS_SHARED = 3    /* the CTAs whose K range ends in the tile wait for all its parts and
+                                   add one slice of its elements each (every tile size) */
+} sgemm_sk_sums_t;
+
 /* Test hook: how later calls of the handle add the partial sums of a tile
- * whose K range is split over stream-K CTAs.  0 (the default): the tiles
- * larger than 64 x 64 leave every part in the workspace and a second kernel
- * adds them; the 64 x 64 tiles add them in the last CTA of the tile to
- * arrive.  1: every tile adds them in its last CTA to arrive, the larger
- * tiles split from 1.25 stream-K CTAs per tile as the 64 x 64 tile does.
- * Both add the parts in ascending k order, so a tile split the same way gets
- * the same bits either way.  SGEMM_ERR_INVALID_VALUE for another value. */
-int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int in_kernel);
+ * whose K range is split over stream-K CTAs (sgemm_sk_sums_t).  Automatic:
+ * for the tiles larger than 64 x 64, whichever of a second kernel and the
+ * shared sums the library's time estimate prefers (and stream-K only where
+ * it beats whole tiles); the 64 x 64 tiles add them in the last CTA of the
+ * tile to arrive.  The other modes take the stream-K tail whenever a wave
+ * has CTAs to spare (LAST: 1.25 per tile), so that every mode splits a call
+ * the same way.  SGEMM_ERR_INVALID_VALUE for another value. */
+int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int mode);
+
+/* Test hook: cluster split-K CTAs per tile for later calls of the handle on
+ * the whole-tile SIMT variants.  In cluster split-K, the `ksplit` CTAs of one
+ * output tile form a thread-block cluster; CTA r takes K steps
+ * [r*kt/ksplit, (r+1)*kt/ksplit) of the tile's kt steps of 32, the partial
+ * tiles meet in distributed shared memory and each CTA adds a 1/ksplit slice
+ * of them in ascending k order and writes it to C (one launch, no workspace).
+ * 0 (the default): the library's choice, taken when all tiles x ksplit CTAs
+ * fit in one wave and its time estimate beats whole tiles and stream-K.
+ * 1: never.  2..8: that many CTAs per tile whenever K has at least as many
+ * steps.  A tile split into ksplit parts this way gets the bits of the same
+ * split through stream-K (ksplit * tiles stream-K CTAs).
+ * SGEMM_ERR_INVALID_VALUE outside 0..8. */
+int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
 
 /* Test hook: the plan sgemm_run_ex would follow for a call, computed on the
  * host with no handle, no device and no CUDA call, from the device facts a
@@ -357,14 +385,16 @@ int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int in_kernel);
  * indexed by sgemm_variant_t: resident CTAs per SM of each TMA variant) and
  * its settings (re-layout workspace size in floats, re-layout mode, math
  * mode, pinned variant).  `tma_ok` says whether A and B are 16-byte aligned
- * with lda, ldb (and batch strides) multiples of 4.  out[0..9] receives: the
+ * with lda, ldb (and batch strides) multiples of 4.  out[0..10] receives: the
  * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
  * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
  * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
  * 1 TN, 2 NT), the whole tiles run in complete waves, the stream-K CTAs, the
- * tiles of the call, the kernel launches, the CTAs per stream-K tile, and 1
- * when a second kernel adds the stream-K tiles' parts (0 when the last CTA of
- * each tile adds them, or without stream-K).
+ * tiles of the call, the kernel launches, the CTAs per stream-K tile, and how
+ * the stream-K tiles' parts are added (0 by the last CTA of each tile to
+ * arrive, or without stream-K; 1 by a second kernel; 2 shared by the CTAs
+ * whose K range ends in the tile), and the cluster split-K CTAs per tile (1:
+ * none).
  * SGEMM_ERR_NULL for a NULL array, SGEMM_ERR_INVALID_VALUE for an argument out
  * of range. */
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,

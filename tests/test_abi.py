@@ -67,7 +67,7 @@ def test_binding_constants_match_the_header():
              "IN_F16": "SGEMM_IN_F16", "RELAYOUT_AUTO": "SGEMM_RELAYOUT_AUTO", "RELAYOUT_OFF": "SGEMM_RELAYOUT_OFF",
              "RELAYOUT_ALWAYS": "SGEMM_RELAYOUT_ALWAYS", "VARIANT_COUNT": "SGEMM_VARIANT_COUNT_"}
     for name in dir(sgemm):
-        if name.startswith("VARIANT_") and name != "VARIANT_COUNT":
+        if (name.startswith("VARIANT_") and name != "VARIANT_COUNT") or name.startswith("SK_SUMS_"):
             pairs[name] = "SGEMM_" + name
     for py, c in pairs.items():
         assert getattr(sgemm, py) == values[c], (py, c)
@@ -206,6 +206,7 @@ def test_bad_handles_are_rejected_without_dereference(lib):
         assert lib.sgemm_set_relayout(fake, sgemm.RELAYOUT_AUTO) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_smem_override(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_stream_k_sums(fake, 0) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_set_cluster_split(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_last_launches(fake) == -1
         assert lib.sgemm_last_relayout(fake) == -1
         assert lib.sgemm_relayout_capacity(fake) == -1

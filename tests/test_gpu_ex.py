@@ -237,7 +237,16 @@ def test_layouts_give_the_nn_bits(handle, variant, op, K):
     FMA, so it returns the NN kernel's bits exactly: NT and TN run the same
     tile grid and stream-K plan as NN (K = 300: the tail's K steps are shared
     by stream-K CTAs); TT runs on the transposed grid, so it matches where no
-    tile is split (K = 64: two K steps, too few to share)."""
+    tile is split (K = 64: two K steps, too few to share; cluster split-K,
+    which would split them, ruled out)."""
+    sgemm.sgemm_debug_set_cluster_split(handle, 1)
+    try:
+        _layouts_give_the_nn_bits(handle, variant, op, K)
+    finally:
+        sgemm.sgemm_debug_set_cluster_split(handle, 0)
+
+
+def _layouts_give_the_nn_bits(handle, variant, op, K):
     M = N = 264
     ref = ExProblem(0, 0, M, N, K, batch=1, seed=51, pad=(4, 4, 4))
     p = ExProblem(op[0], op[1], M, N, K, batch=1, seed=51, pad=(4, 4, 4))

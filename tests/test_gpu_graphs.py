@@ -29,11 +29,20 @@ def _dev(prob):
     return (torch.from_numpy(prob.A).cuda(), torch.from_numpy(prob.B).cuda(), torch.from_numpy(prob.C0).cuda())
 
 
-def test_capture_and_replay_fp32_calls(handle):
-    """Three calls in one graph: a whole-tile launch, a three-launch call
-    (complete waves, stream-K wave, the kernel that adds the stream-K parts)
-    and the split-all variant; replayed twice (beta = 0, so a replay
-    recomputes the same C)."""
+@pytest.mark.parametrize("sums", [sgemm.SK_SUMS_SHARED, sgemm.SK_SUMS_DEFERRED], ids=["shared", "deferred"])
+def test_capture_and_replay_fp32_calls(handle, sums):
+    """Three calls in one graph: a whole-tile launch, a call with complete
+    waves and a stream-K wave (whose parts the stream-K CTAs add themselves,
+    or, deferred, a third launch adds) and the split-all variant; replayed
+    twice (beta = 0, so a replay recomputes the same C)."""
+    sgemm.sgemm_debug_set_stream_k_sums(handle, sums)
+    try:
+        _capture_and_replay(handle, 3 if sums == sgemm.SK_SUMS_DEFERRED else 2)
+    finally:
+        sgemm.sgemm_debug_set_stream_k_sums(handle, sgemm.SK_SUMS_AUTO)
+
+
+def _capture_and_replay(handle, waves_launches):
     cfgs = [inputs.GemmConfig("g_small", 300, 520, 270, 272, 520, 520, 61, 1.25, 0.0),
             inputs.GemmConfig("g_waves", 2048, 2560, 2048, 2048, 2560, 2560, 62, 1.0, 0.0),
             inputs.square(256, 63)]
@@ -52,7 +61,7 @@ def test_capture_and_replay_fp32_calls(handle):
             sgemm.sgemm_run(handle, c.M, c.N, c.K, c.alpha, A, c.lda, B, c.ldb, c.beta, C, c.ldc, s)
             # GEMM launches: the call's launches minus its operand copies
             launches.append(sgemm.sgemm_last_launches(handle) - bin(sgemm.sgemm_last_relayout(handle)).count("1"))
-    assert 3 in launches  # the deferred stream-K form after complete waves was captured
+    assert waves_launches in launches  # the stream-K form after complete waves was captured
     for _ in range(2):
         for _, _, C in bufs:
             C.fill_(float("nan"))

@@ -436,13 +436,17 @@ def test_cached_plans_and_maps_follow_their_operands(handle):
                                      (V.VARIANT_TMA_128x256, (1024, 1024, 1024)),
                                      (V.VARIANT_TMA_128x128, (1024, 1024, 1024)),
                                      (V.VARIANT_TMA_256x128, (2560, 2048, 768)),
-                                     (V.VARIANT_TMA_128x256, (1000, 1500, 777))],
+                                     (V.VARIANT_TMA_128x256, (1000, 1500, 777)),
+                                     (V.VARIANT_TMA_64x64, (1000, 1000, 777)),
+                                     (V.VARIANT_TMA_64x64_SPLITK, (256, 256, 256))],
                          ids=lambda x: sgemm.variant_name(x) if isinstance(x, int) else "x".join(map(str, x)))
-def test_deferred_sums_equal_in_kernel_sums(handle, variant, v, shape):
-    """The larger tiles' stream-K parts added by the second kernel give the
-    bits that the in-kernel sums (the last CTA of each tile to arrive) give:
-    same split, same ascending k order; one launch more.  Uniform inputs, so
-    the sums round; beta = 0.75 reads C."""
+def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape):
+    """A split tile's stream-K parts give the same bits whoever adds them: the
+    last CTA of the tile to arrive, a second kernel (tiles larger than
+    64 x 64: one launch more), or the CTAs whose K range ends in the tile,
+    each adding a slice -- same split, same ascending k order.  Uniform
+    inputs, so the sums round; beta = 0.75 reads C; the result also matches
+    the oracle."""
     import torch
     M, N, K = shape
     lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4  # 16-byte rows: the TMA kernels
@@ -452,19 +456,32 @@ def test_deferred_sums_equal_in_kernel_sums(handle, variant, v, shape):
     C0 = torch.rand(M * ldb, device="cuda", generator=g) * 2 - 1
     variant(v)
     out = {}
+    large = v not in (V.VARIANT_TMA_64x64, V.VARIANT_TMA_64x64_SPLITK)
+    modes = (sgemm.SK_SUMS_LAST, sgemm.SK_SUMS_SHARED) + ((sgemm.SK_SUMS_DEFERRED,) if large else ())
+    sgemm.sgemm_debug_set_cluster_split(handle, 1)  # stream-K, never a cluster split
+    sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_OFF)  # the same layout in every mode
     try:
-        for in_kernel in (0, 1):
-            sgemm.sgemm_debug_set_stream_k_sums(handle, in_kernel)
-            C = C0.clone()
-            sgemm.sgemm_run(handle, M, N, K, 1.25, A, lda, B, ldb, 0.75, C, ldb)
-            torch.cuda.synchronize()
-            ran, splits = sgemm.sgemm_last_variant(handle)
-            out[in_kernel] = (C, ran, splits, sgemm.sgemm_last_launches(handle))
+        for mode in modes:
+            sgemm.sgemm_debug_set_stream_k_sums(handle, mode)
+            for rep in range(2):  # twice: the counters must be back at zero after a call
+                C = C0.clone()
+                sgemm.sgemm_run(handle, M, N, K, 1.25, A, lda, B, ldb, 0.75, C, ldb)
+                torch.cuda.synchronize()
+                ran, splits = sgemm.sgemm_last_variant(handle)
+                out[mode, rep] = (C, ran, splits, sgemm.sgemm_last_launches(handle))
     finally:
-        sgemm.sgemm_debug_set_stream_k_sums(handle, 0)
-    (C_def, ran_d, sp_d, l_d), (C_ink, ran_i, sp_i, l_i) = out[0], out[1]
-    assert ran_d == ran_i == v and sp_d == sp_i and sp_d > 1, (ran_d, ran_i, sp_d, sp_i)
-    assert l_d == l_i + 1, (l_d, l_i)
-    assert torch.isfinite(C_def).all()
-    assert torch.equal(C_def.view(torch.int32), C_ink.view(torch.int32))
+        sgemm.sgemm_debug_set_stream_k_sums(handle, sgemm.SK_SUMS_AUTO)
+        sgemm.sgemm_debug_set_cluster_split(handle, 0)
+        sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_AUTO)
+    C_ref, ran0, sp0, l0 = out[sgemm.SK_SUMS_LAST, 0]
+    assert ran0 == v and sp0 > 1, (ran0, sp0)
+    assert torch.isfinite(C_ref).all()
+    for (mode, rep), (C, ran, splits, launches) in out.items():
+        assert ran == v and splits == sp0, (mode, ran, splits)
+        assert launches == l0 + (1 if mode == sgemm.SK_SUMS_DEFERRED else 0), (mode, launches, l0)
+        assert torch.equal(C.view(torch.int32), C_ref.view(torch.int32)), (mode, rep)
     assert sgemm.sgemm_get_device_status(handle) == V.OK
+    ref = C0.cpu().numpy().copy()
+    oracle.sgemm(M, N, K, 1.25, A.cpu().numpy(), lda, B.cpu().numpy(), ldb, 0.75, ref, ldb)
+    got = C_ref.cpu().numpy().reshape(M, ldb)[:, :N].astype(np.float64)
+    assert np.max(np.abs(got - ref.reshape(M, ldb)[:, :N])) <= tolerance(K)

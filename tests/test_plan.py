@@ -48,7 +48,7 @@ def copies_need(tA, tB, M, N, K, copies, batch=1, strideA=1, strideB=1):
 
 def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout_floats=CAPACITY):
     assert p["launches"] == (bin(p["copies"]).count("1") + (2 if p["dp_tiles"] and p["sk_ctas"] else 1)
-                             + p["deferred"])
+                             + (p["fixup"] == V.FIXUP_DEFERRED))
     if p["kind"] != V.PLAN_TMA:
         return
     v = p["variant"]
@@ -58,27 +58,35 @@ def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout
     assert p["tiles"] == tiles
     assert copies_need(tA, tB, M, N, K, p["copies"], batch, strideA, strideB) <= relayout_floats
     G, dp = p["sk_ctas"], p["dp_tiles"]
-    if G == 0:
-        assert dp == tiles and p["splits"] == 1 and p["deferred"] == 0
-        return
-    slots = SMS * OCC[v]
     kt = -(-K // 32)
+    if G == 0:
+        assert dp == tiles and p["splits"] == p["ksplit"] and p["fixup"] == V.FIXUP_LAST
+        if p["ksplit"] > 1:
+            # cluster split-K: one wave of whole clusters, one CTA per SM, every CTA with K steps
+            assert 2 <= p["ksplit"] <= 8 and p["ksplit"] <= kt
+            assert tiles * p["ksplit"] <= SMS and p["launches"] == bin(p["copies"]).count("1") + 1
+        return
+    assert p["ksplit"] == 1
+    slots = SMS * OCC[v]
     sk_tiles = tiles - dp
     assert 0 < G <= slots
     assert G >= sk_tiles                       # a CTA's K range touches at most two tiles
     assert G <= sk_tiles * kt                  # every stream-K CTA has at least one K step
     assert (sk_tiles + G) * bm * bn <= WS_FLOATS  # partial tiles fit in the workspace
     if v == V.VARIANT_TMA_64x64_SPLITK:
-        assert dp == 0 and G >= 2 * tiles and batch == 1 and p["deferred"] == 0
+        assert dp == 0 and G >= 2 * tiles and batch == 1 and p["fixup"] == V.FIXUP_LAST
     else:
         assert dp % slots == 0                 # complete waves only
         assert sk_tiles < slots or sk_tiles == 0
         assert sk_tiles * kt >= 2 * G          # at least two K steps per CTA
-        # tiles larger than 64 x 64 leave their parts to a second kernel and
-        # split whenever a CTA is left over; 64 x 64 adds them in its last CTA
-        # and splits from 1.25 CTAs per stream-K tile
-        assert p["deferred"] == (1 if bm * bn > 64 * 64 else 0)
-        assert G > sk_tiles if p["deferred"] else 4 * G >= 5 * sk_tiles
+        # tiles larger than 64 x 64 leave their parts to a second kernel or
+        # share the adding among the CTAs that end in the tile (whichever the
+        # estimate prefers) and split whenever a CTA is left over and the
+        # estimate says so; 64 x 64 adds them in its last CTA and splits from
+        # 1.25 CTAs per stream-K tile
+        large = bm * bn > 64 * 64
+        assert (p["fixup"] in (V.FIXUP_DEFERRED, V.FIXUP_SHARED)) if large else p["fixup"] == V.FIXUP_LAST
+        assert G > sk_tiles if large else 4 * G >= 5 * sk_tiles
     assert p["splits"] >= 2
 
 
@@ -155,36 +163,44 @@ def test_tensor_core_plans():
 
 def test_choices_measured_on_gb300():
     """The automatic choices the GB300 measurements settled: on each of these
-    shapes and layouts the variant and copy chosen ran fastest, or within 1 %
-    of the fastest, of every tile variant with and without re-layout
-    (CUDA-graph timings; 384^3, not listed, is the exception: the split-all
-    64 x 64 kernel at 11.6 us against 10.5 for its tail split)."""
+    shapes and layouts the variant, copy and plan chosen ran fastest, or
+    within 1 % (or 1 us) of the fastest, of every tile variant with and without
+    re-layout, with the stream-K parts added by a second kernel or shared in
+    the stream-K CTAs, and with cluster split-K of 2..8 CTAs per tile (CUDA
+    graph timings).  Fields: variant, copies, launches, cluster split-K CTAs
+    per tile, how the stream-K parts are added."""
+    L, X, M, S = V.VARIANT_TMA_128x256, V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64
+    D, SH, NO = V.FIXUP_DEFERRED, V.FIXUP_SHARED, V.FIXUP_LAST
     expect = {
-        # copies, then complete waves, the stream-K wave and the kernel adding its parts
-        (0, 0, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 1, 4),
-        (1, 0, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 0, 3),
-        (0, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 3, 5),
-        (1, 1, 8192, 8192, 8192): (V.VARIANT_TMA_256x128, 2, 4),
-        (0, 0, 4096, 4096, 4096): (V.VARIANT_TMA_256x128, 1, 4),
-        # one stream-K wave over all tiles and the kernel adding its parts
-        (0, 0, 512, 512, 512): (V.VARIANT_TMA_128x128, 0, 2),
-        (0, 0, 768, 768, 768): (V.VARIANT_TMA_128x256, 0, 2),
-        (0, 0, 1024, 1024, 1024): (V.VARIANT_TMA_128x256, 0, 2),
-        (0, 0, 1000, 1500, 777): (V.VARIANT_TMA_128x256, 0, 2),
-        (0, 0, 2048, 2048, 1024): (V.VARIANT_TMA_256x128, 1, 3),
-        (0, 0, 2048, 2048, 2048): (V.VARIANT_TMA_256x128, 1, 3),
-        (0, 1, 1024, 1024, 1024): (V.VARIANT_TMA_128x256, 0, 2),
-        (1, 0, 1000, 1500, 777): (V.VARIANT_TMA_128x256, 0, 2),
-        (1, 0, 2048, 2048, 1024): (V.VARIANT_TMA_256x128, 0, 2),
-        (0, 1, 2048, 2048, 2048): (V.VARIANT_TMA_256x128, 3, 4),
-        (1, 1, 2048, 2048, 2048): (V.VARIANT_TMA_256x128, 2, 3),
+        # copies, then complete waves and a stream-K wave whose CTAs add the parts
+        (0, 0, 8192, 8192, 8192): (X, 1, 3, 1, SH),
+        (1, 0, 8192, 8192, 8192): (X, 0, 2, 1, SH),
+        (0, 1, 8192, 8192, 8192): (X, 3, 4, 1, SH),
+        (1, 1, 8192, 8192, 8192): (X, 2, 3, 1, SH),
+        (0, 0, 4096, 4096, 4096): (X, 1, 3, 1, SH),
+        # one stream-K wave over all tiles (parts added by a second kernel
+        # below about 27 MB of parts, shared by the stream-K CTAs above)
+        (0, 0, 1024, 1024, 1024): (L, 0, 2, 1, D),
+        (0, 0, 1000, 1500, 777): (L, 0, 2, 1, D),
+        (0, 0, 2048, 2048, 1024): (X, 1, 2, 1, SH),
+        (0, 0, 2048, 2048, 2048): (X, 1, 2, 1, SH),
+        (0, 1, 1024, 1024, 1024): (L, 0, 2, 1, D),
+        (1, 0, 1000, 1500, 777): (L, 0, 2, 1, D),
+        (1, 0, 2048, 2048, 1024): (X, 0, 1, 1, SH),
+        (0, 1, 2048, 2048, 2048): (X, 3, 3, 1, SH),
+        (1, 1, 2048, 2048, 2048): (X, 2, 2, 1, SH),
         # one partial wave of whole tiles, after the copy of A
-        (0, 0, 1536, 1536, 1536): (V.VARIANT_TMA_128x128, 1, 2),
-        (0, 0, 256, 256, 256): (V.VARIANT_TMA_64x64_SPLITK, 0, 1),
+        (0, 0, 1536, 1536, 1536): (M, 1, 2, 1, NO),
+        # cluster split-K: one cluster of CTAs per tile, one wave
+        (0, 0, 256, 256, 256): (S, 0, 1, 4, NO),
+        (0, 0, 384, 384, 384): (S, 0, 1, 4, NO),
+        (0, 0, 512, 512, 512): (S, 0, 1, 2, NO),
+        (0, 0, 768, 768, 768): (M, 0, 1, 4, NO),
     }
-    for (tA, tB, M, N, K), (variant, copies, launches) in expect.items():
-        p = plan(tA, tB, M, N, K)
-        assert (p["variant"], p["copies"], p["launches"]) == (variant, copies, launches), (M, N, K, p)
+    for (tA, tB, M_, N_, K_), want in expect.items():
+        p = plan(tA, tB, M_, N_, K_)
+        got = (p["variant"], p["copies"], p["launches"], p["ksplit"], p["fixup"])
+        assert got == want, ((M_, N_, K_), got, p)
 
 
 def test_relayout_capacity_edge():
