@@ -38,11 +38,11 @@ METRIC = "SGEMM TFLOP/s (2MNK/t) at 4096³ and 8192³; % of GB300 FP32 peak"
 UNIT = "TFLOP/s"
 
 # DRAM bytes (read + write) of one headline call at 8192^3 -- every launch of
-# the call: the transposed copy, the complete waves, the stream-K wave and the
-# kernel adding its parts -- keyed by (SHA-256 of the SIMT kernel source
-# without comments, layout the kernel ran on, re-layout bits), from one-pass
-# ncu launch lists of the headline command (profiles/
-# sgemm_headline_8192cube_launches.md); any other source gives traffic = null.
+# the call: the transposed copy, the complete waves and the stream-K wave --
+# keyed by (SHA-256 of the SIMT kernel source without comments, layout the
+# kernel ran on, re-layout bits), from a one-pass ncu launch list of the
+# headline command (gpu__time_duration and the DRAM byte counters of every
+# launch of the timed steps); any other source gives traffic = null.
 TRAFFIC_BY_SOURCE = {("ccf21e73415850ef", "TN", 1): 3.364e9}
 TC_TRAFFIC_BY_SOURCE = {"3f6064e551384a01": 2.534e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
@@ -100,6 +100,17 @@ def measured_hbm_gbs() -> dict:
             return {"value": float(json.load(f)["hbm_gbs"]), "source": "measured"}
     except (OSError, KeyError, ValueError):
         return {"value": 6800.0, "source": "fallback"}
+
+
+def compact(x):
+    """x with every float rounded to 6 significant digits (JSON size)."""
+    if isinstance(x, float):
+        return float(f"{x:.6g}")
+    if isinstance(x, dict):
+        return {k: compact(v) for k, v in x.items()}
+    if isinstance(x, (list, tuple)):
+        return [compact(v) for v in x]
+    return x
 
 
 def parse():
@@ -289,6 +300,19 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
         e.record(stream)
         e.synchronize()
         ms.append(s.elapsed_time(e))
+    # warm L2, per call: C restored from C0 outside each event pair (in-place
+    # updates), no flush, so A, B and C are in L2 from the call before
+    warm = None
+    if cold and cfg.beta != 0:
+        warm = []
+        for _ in range(reps):
+            C.copy_(C0)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call()
+            e.record(stream)
+            e.synchronize()
+            warm.append(s.elapsed_time(e))
     # back-to-back (hot L2) mean, beta == 0 only (in-place updates would compound)
     hot = None
     if cfg.beta == 0:
@@ -300,9 +324,10 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
         e.record(stream)
         e.synchronize()
         hot = s.elapsed_time(e) / n
-    # launch-bound shapes: 20 calls captured in one CUDA graph, replayed (beta == 0 only)
+    # launch-bound shapes: 20 calls captured in one CUDA graph, replayed (an
+    # in-place workload updates C 20 times over: the same work per call)
     graph_ms = None
-    if cfg.beta == 0 and cfg.flops <= 2 * 1024 ** 3:
+    if cfg.flops <= 2.5e9:
         gs = torch.cuda.Stream()
         gs.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -321,12 +346,18 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
         del graph
     variant, splits = sg.sgemm_last_variant(h)
     med = statistics.median(ms)
-    out = {"ms_median": med, "ms_min": min(ms), "tflops": cfg.flops / (med * 1e-3) / 1e12,
+    out = {"ms_median": med, "ms_mean": statistics.mean(ms), "ms_min": min(ms),
+           "tflops": cfg.flops / (med * 1e-3) / 1e12,
            "gbs_compulsory": cfg.compulsory_bytes / (med * 1e-3) / 1e9, "reps": reps,
            "l2": "flushed before each rep" if cold else "warm", "variant": sg.variant_name(variant),
            "relayout": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)]}
     if splits > 1:
         out["splits"] = splits
+    if warm is not None:
+        wmed = statistics.median(warm)
+        out["ms_warm_median"] = wmed
+        out["ms_warm_mean"] = statistics.mean(warm)
+        out["tflops_warm"] = cfg.flops / (wmed * 1e-3) / 1e12
     if hot is not None:
         out["ms_back_to_back"] = hot
         out["tflops_back_to_back"] = cfg.flops / (hot * 1e-3) / 1e12
@@ -647,18 +678,34 @@ def main():
         if i >= 3:
             fma_ms.append(e0.elapsed_time(e1))
     fma_tflops = probe_flops / (statistics.median(fma_ms) * 1e-3) / 1e12
+    # the TF32 tensor-pipe rate with no memory traffic (the library's tensor
+    # probe: the 3xTF32 pair kernel's MMA on resident tiles), for the tensor roofline
+    tf32_ms = []
+    for i in range(8):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        tf32_flops = sg.sgemm_debug_tf32_probe(h, iters=4096, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= 3:
+            tf32_ms.append(e0.elapsed_time(e1))
+    tf32_tflops = tf32_flops / (statistics.median(tf32_ms) * 1e-3) / 1e12
+    if sg.sgemm_get_device_status(h) != sg.OK:
+        raise SystemExit("device status after the TF32 probe: timeout")
+    roofline["tf32_microbench"] = {"tflops": tf32_tflops, "what": "sgemm_debug_tf32_probe: tcgen05.mma "
+                                   "cta_group::2 kind::tf32 M = N = 256 on resident shared-memory tiles"}
     roofline["fma_microbench"] = {"tflops": fma_tflops, "frac": achieved / fma_tflops,
                                   "what": "sgemm_debug_fma_probe: 4 CTAs of 256 threads per SM, 16 independent "
                                           "packed FP32x2 FMA chains per thread, registers only"}
     del sink
     if variant in (sg.VARIANT_TC_3XTF32, sg.VARIANT_TC_3XTF32_PAIR):
         # a pinned tensor-core variant: its roofline is the tensor pipe's
-        bf16 = measured_bf16_tflops()
-        tc_peak = bf16["value"] * 1.1 / 2.25 / 3
+        tc_peak = tf32_tflops / 3
         roofline = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
                     "frac": achieved / tc_peak, "traffic": None,
                     "kernel": f"{sg.variant_name(variant)}",
-                    "peak_basis": f"TF32 dense = {bf16['source']} BF16 x 1.1/2.25, / 3 TF32 MMAs per FP32 product",
+                    "peak_basis": f"measured TF32 tensor-pipe rate {tf32_tflops:.1f} TFLOP/s "
+                                  "(sgemm_debug_tf32_probe) / 3 TF32 MMAs per FP32 product",
                     "algorithmic_flops_per_launch": cfg.flops,
                     "kernel_source_sha256_16": kernel_source_hash(TC_KERNEL_SOURCES)}
 
@@ -717,7 +764,8 @@ def main():
                                     "copies": RELAYOUT_NAMES[sg.sgemm_last_relayout(h)]}
         sg.sgemm_set_variant(h, sg.VARIANT_AUTO)
         bf16 = measured_bf16_tflops()
-        tf32_peak = bf16["value"] * 1.1 / 2.25
+        tf32_nominal_ratio = bf16["value"] * 1.1 / 2.25
+        tf32_peak = tf32_tflops
         tc_tflops = cfg.flops / (tc_ms * 1e-3) / 1e12
         out["tensor_3xtf32"] = {
             "variant": "tc_3xtf32_pair", "ms_per_step": tc_ms, "value": tc_tflops, "unit": UNIT,
@@ -727,8 +775,11 @@ def main():
                          "traffic": (TC_TRAFFIC_BY_SOURCE.get(kernel_source_hash(TC_KERNEL_SOURCES))
                                      if cfg.name == inputs.HEADLINE.name else None),
                          "kernel_source_sha256_16": kernel_source_hash(TC_KERNEL_SOURCES),
-                         "peak_basis": f"TF32 dense = {bf16['source']} BF16 {bf16['value']:.1f} TFLOP/s x 1.1/2.25 "
-                                       f"(nominal ratio) = {tf32_peak:.1f}; 3 TF32 MMAs per FP32 product",
+                         "peak_source": "measured",
+                         "peak_basis": f"measured TF32 tensor-pipe rate {tf32_peak:.1f} TFLOP/s "
+                                       "(sgemm_debug_tf32_probe: the pair kernel's MMA, M = N = 256, on resident "
+                                       "tiles, one cluster per SM pair) / 3 TF32 MMAs per FP32 product",
+                         "tf32_from_bf16_nominal_ratio": tf32_nominal_ratio,
                          "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
             "layouts": tc_layouts,
         }
@@ -780,7 +831,11 @@ def main():
         out["cpu_baseline"]["workloads"] = per
     sg.sgemm_destroy(h)
     if rank == 0:
-        print(json.dumps(out))
+        # the per-workload table last, so that a reader keeping only the end
+        # of the line still has it; floats to 6 significant digits
+        if "workloads" in out:
+            out["workloads"] = out.pop("workloads")
+        print(json.dumps(compact(out)))
     if world > 1:
         dist.destroy_process_group()
 

@@ -127,6 +127,10 @@ cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, floa
 cudaError_t launch_timeout_probe(int *status, long long limit_ns, cudaStream_t stream);
 // Returns the FLOP the launch performs (-1 on a launch error); sink: ctas * 256 floats.
 long long launch_fma_probe(float *sink, int ctas, int iters, cudaStream_t stream);
+// TF32 tensor-pipe rate probe (sgemm_tc.cu): `clusters` CTA pairs issuing
+// `iters` K = 32 steps of the 3xTF32 pair kernel's MMA on resident tiles;
+// returns the TF32 FLOP it performs (-1 on a launch error).
+long long launch_tf32_probe(int *status, int clusters, int iters, cudaStream_t stream);
 // sink: ctas * 32 floats.
 cudaError_t launch_bank_probe(float *sink, int padded, int ctas, int iters, cudaStream_t stream);
 

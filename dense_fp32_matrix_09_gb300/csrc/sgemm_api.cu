@@ -1301,10 +1301,27 @@ int sgemm_get_device_status(sgemm_handle_t h) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(&word, h->d_status, sizeof(int), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    // A stream-K CTA that gave up a wait leaves before counting its arrival,
+    // so its tile's counter is never reset by the CTAs that would add the
+    // parts: after a timeout every arrival counter starts again from zero.
+    if (e == cudaSuccess && (word & sg::kDevTimeoutBit))
+        e = cudaMemset(h->d_counters, 0, static_cast<size_t>(h->n_counters) * sizeof(int));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (prev != h->device) cudaSetDevice(prev);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
     return (word & sg::kDevTimeoutBit) ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_debug_leave_aborted_state(sgemm_handle_t h) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    const int word = sg::kDevTimeoutBit;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemset(h->d_counters, 0x01, static_cast<size_t>(h->n_counters) * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpy(h->d_status, &word, sizeof(int), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return e == cudaSuccess ? SGEMM_OK : SGEMM_ERR_CUDA;
 }
 
 int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream) {
@@ -1373,6 +1390,18 @@ int sgemm_debug_fma_probe(sgemm_handle_t h, int ctas, int iters, float *sink, lo
     if (ctas == 0) ctas = 4 * h->num_sms;
     if (ctas < 0 || iters < 1) return SGEMM_ERR_INVALID_VALUE;
     const long long f = sg::launch_fma_probe(sink, ctas, iters, static_cast<cudaStream_t>(stream));
+    if (f < 0) return SGEMM_ERR_LAUNCH;
+    if (flops) *flops = f;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_tf32_probe(sgemm_handle_t h, int clusters, int iters, long long *flops, void *stream) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device) return SGEMM_ERR_WRONG_DEVICE;
+    if (clusters == 0) clusters = h->num_sms / 2;
+    if (clusters < 0 || clusters > h->num_sms / 2 || iters < 1 || iters > (1 << 20)) return SGEMM_ERR_INVALID_VALUE;
+    const long long f = sg::launch_tf32_probe(h->d_status, clusters, iters, static_cast<cudaStream_t>(stream));
     if (f < 0) return SGEMM_ERR_LAUNCH;
     if (flops) *flops = f;
     return SGEMM_OK;

@@ -31,9 +31,11 @@
 // device address of the array (cudaGetSymbolAddress), sets the kernel's
 // shared-memory limit and fetches the TMA descriptor encoder.  Because it does
 // this set-up, the first call on each device should come before any stream
-// capture.  In host code the array's name is only a host-side stand-in for the
-// symbol, never a device address; only the looked-up pointer is passed to the
-// kernel.
+// capture.  The looked-up address is kept for the life of the process, so a
+// caller must not reset the device (cudaDeviceReset, which reloads the
+// library's device code) between calls.  In host code the array's name is
+// only a host-side stand-in for the symbol, never a device address; only the
+// looked-up pointer is passed to the kernel.
 //
 // Paths: alpha == 0 or K == 0 takes the C = beta*C kernel and operands that
 // TMA cannot describe take the generic kernel (neither uses scratch); every

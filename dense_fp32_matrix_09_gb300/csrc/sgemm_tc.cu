@@ -551,7 +551,80 @@ sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     }
 }
 
+// ---------------------------------------------------------------------------
+// TF32 tensor-pipe rate probe: the CTA-pair MMA of sgemm_tc3x_pair_kernel
+// (M = 256, N = 256, K = 8, both operands K-major with the 128-byte swizzle,
+// FP32 accumulator in tensor memory) issued back to back on operand tiles
+// that stay in shared memory -- no global traffic, no split, no epilogue --
+// so its time is the tensor pipe's.  One cluster of two CTAs per SM pair;
+// the even CTA's thread issues `iters` K = 32 steps of four MMAs, commits
+// them to both CTAs' barriers, and every thread waits for that (bounded,
+// timeout recorded in *status).  The operand tiles are zero (the values do
+// not change the rate).
+constexpr int kProbeThreads = 64;
+constexpr int kProbeTmemCols = 256;
+constexpr int kSmemProbe = kABytesTc + kPBBytes + 1024 + 64;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kProbeThreads, 1)
+sgemm_tf32_probe_kernel(int iters, int *status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *a = smem_raw + pad;      // 128 rows x 32 k, same offset in both CTAs
+    uint8_t *b = a + kABytesTc;       // 128 columns x 32 k
+    uint64_t *done = reinterpret_cast<uint64_t *>(b + kPBBytes);
+    uint32_t *tmem_base = reinterpret_cast<uint32_t *>(done + 1);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t rank = tc::cluster_ctarank();
+    for (int i = tid; i < (kABytesTc + kPBBytes) / 16; i += kProbeThreads)
+        reinterpret_cast<float4 *>(a)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    tc::fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc_pair(tmem_base, kProbeTmemCols);
+        tc::tmem_relinquish_pair();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync_all();  // both CTAs' tiles and barriers are ready
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_base;
+    if (warp == 1 && (tid & 31) == 0 && rank == 0) {
+        const uint32_t sa = smem_u32(a), sb = smem_u32(b);
+        for (int t = 0; t < iters; ++t) {
+#pragma unroll
+            for (int kk = 0; kk < TBK / 8; ++kk)
+                tc::mma_tf32_pair(tmem, tc::smem_desc(sa + kk * 32, 16, 1024, tc::kLayoutSwizzle128),
+                                  tc::smem_desc(sb + kk * 32, 16, 1024, tc::kLayoutSwizzle128), kIdescPair,
+                                  (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc::commit_pair(done, 0x3);
+    }
+    __syncwarp();
+    tc::mbar_wait_cluster(done, 0, status);  // a timeout is recorded; teardown goes on
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::cluster_sync_all();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc_pair(tmem, kProbeTmemCols);
+    }
+}
+
 }  // namespace
+
+long long launch_tf32_probe(int *status, int clusters, int iters, cudaStream_t stream) {
+    if (clusters < 1 || iters < 1 || iters > (1 << 20)) return -1;
+    if (cudaFuncSetAttribute(sgemm_tf32_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemProbe) !=
+        cudaSuccess)
+        return -1;
+    sgemm_tf32_probe_kernel<<<2 * clusters, kProbeThreads, kSmemProbe, stream>>>(iters, status);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    // four M = 256, N = 256, K = 8 MMAs per step: 2 * 256 * 256 * 32 FLOP
+    return 2LL * 256 * 256 * TBK * iters * clusters;
+}
 
 cudaError_t tc3x_pair_prepare() {
     return cudaFuncSetAttribute(sgemm_tc3x_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTcPair);

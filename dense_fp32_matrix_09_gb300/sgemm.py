@@ -59,7 +59,8 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
            "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
-           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split")
+           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_leave_aborted_state",
+           "sgemm_debug_tf32_probe")
 
 
 class SgemmError(RuntimeError):
@@ -98,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_plan.argtypes = [i32, ctypes.POINTER(i32), ctypes.c_longlong, i32, i32, i32, i32, i32, i32, i32,
                                        i32, f32, i32, ctypes.c_longlong, ctypes.c_longlong, i32, ctypes.POINTER(i32)]
         L.sgemm_debug_fma_probe.argtypes = [vp, i32, i32, vp, ctypes.POINTER(ctypes.c_longlong), vp]
+        L.sgemm_debug_tf32_probe.argtypes = [vp, i32, i32, ctypes.POINTER(ctypes.c_longlong), vp]
         L.sgemm_debug_bank_probe.argtypes = [vp, i32, i32, i32, vp, vp]
         L.sgemm_run_mixed.argtypes = [vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32, vp]
         L.sgemm_check_args_mixed.argtypes = [i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, i32, f32, vp, i32]
@@ -106,6 +108,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
         L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
         L.sgemm_debug_set_cluster_split.argtypes = [vp, i32]
+        L.sgemm_debug_leave_aborted_state.argtypes = [vp]
         L.sgemm_status_string.argtypes = [i32]
         L.sgemm_status_string.restype = ctypes.c_char_p
         L.sgemm_variant_name.argtypes = [i32]
@@ -252,6 +255,14 @@ def sgemm_debug_fma_probe(h, sink, ctas=0, iters=4096, stream=None) -> int:
     return flops.value
 
 
+def sgemm_debug_tf32_probe(h, clusters=0, iters=4096, stream=None) -> int:
+    """Enqueue the TF32 tensor-pipe rate probe; returns the TF32 FLOP it performs."""
+    flops = ctypes.c_longlong(0)
+    _check(lib().sgemm_debug_tf32_probe(h, int(clusters), int(iters), ctypes.byref(flops), _stream(stream)),
+           "sgemm_debug_tf32_probe")
+    return flops.value
+
+
 def sgemm_debug_bank_probe(h, padded, sink, ctas=0, iters=64, stream=None) -> None:
     """Enqueue the shared-memory bank probe (sink: ctas*32 floats on the device)."""
     _check(lib().sgemm_debug_bank_probe(h, int(padded), int(ctas), int(iters), _ptr(sink), _stream(stream)),
@@ -306,6 +317,10 @@ def sgemm_debug_timeout_probe(h, limit_ns: int, stream=None) -> None:
 
 def sgemm_debug_set_smem_override(h, nbytes: int) -> None:
     _check(lib().sgemm_debug_set_smem_override(h, int(nbytes)), "sgemm_debug_set_smem_override")
+
+
+def sgemm_debug_leave_aborted_state(h) -> None:
+    _check(lib().sgemm_debug_leave_aborted_state(h), "sgemm_debug_leave_aborted_state")
 
 
 def sgemm_debug_set_cluster_split(h, ksplit: int) -> None:

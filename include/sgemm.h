@@ -306,8 +306,19 @@ int sgemm_last_launches(sgemm_handle_t h);
 /* Wait for the handle's device to finish its work, then read and clear the
  * handle's device-side status word.  Returns SGEMM_OK, or
  * SGEMM_ERR_DEVICE_TIMEOUT if any kernel of the handle abandoned a bounded
- * wait (its output is then undefined), or SGEMM_ERR_CUDA. */
+ * wait, or SGEMM_ERR_CUDA.  After a timeout the C of the calls since the last
+ * check is undefined: some tiles may be unwritten and some may hold partial
+ * sums or stale workspace contents.  On a timeout this call also clears the
+ * handle's stream-K arrival counters (a CTA that gave up leaves its tile's
+ * counter unreset), so later calls on the handle are correct again. */
 int sgemm_get_device_status(sgemm_handle_t h);
+
+/* Test hook: put the handle in the state that a stream-K kernel which gave
+ * up a bounded wait can leave behind -- every arrival counter nonzero and
+ * the timeout bit set in the status word -- without running any kernel.
+ * sgemm_get_device_status must then report the timeout and restore the
+ * counters.  Synchronizes the device. */
+int sgemm_debug_leave_aborted_state(sgemm_handle_t h);
 
 /* Test hook: enqueue one small kernel that waits on a barrier nothing will
  * complete, gives up after `limit_ns` nanoseconds (clamped to [1e3, 1e9]),
@@ -324,6 +335,19 @@ int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream
  * SGEMM_ERR_NULL for a NULL sink; SGEMM_ERR_INVALID_VALUE if ctas < 0 or
  * iters < 1. */
 int sgemm_debug_fma_probe(sgemm_handle_t h, int ctas, int iters, float *sink, long long *flops, void *stream);
+
+/* Measurement probe of the TF32 tensor pipe: enqueue `clusters` clusters of
+ * two CTAs (0 = one per pair of SMs; at most SMs/2), each issuing `iters`
+ * K = 32 steps of the 3xTF32 CTA-pair kernel's MMA (tcgen05.mma
+ * cta_group::2 kind::tf32, M = 256, N = 256, four K = 8 MMAs a step) on
+ * operand tiles resident in shared memory, with no global-memory traffic,
+ * and set *flops (if non-NULL) to the TF32 FLOP the launch performs.  Timed
+ * with events it gives the measured TF32 rate; the 3xTF32 path spends three
+ * TF32 MMAs per FP32 product, so its roofline is a third of it.  A wait that
+ * runs out (bounded) is recorded in the handle's status word.
+ * SGEMM_ERR_INVALID_VALUE if clusters < 0 or > SMs/2, or iters outside
+ * 1 .. 2^20; SGEMM_ERR_WRONG_DEVICE off the handle's device. */
+int sgemm_debug_tf32_probe(sgemm_handle_t h, int clusters, int iters, long long *flops, void *stream);
 
 /* Measurement probe: `ctas` one-warp CTAs (0 = one per SM) each fill a 32 x 32
  * FP32 tile in shared memory with 0.001*(32*row + column) and read it
@@ -420,7 +444,9 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
  * overlap on the GPU (unordered streams) race and give wrong results.  The
  * first call on a device, with that device current, looks up the scratch's
  * device address and sets the kernel up; make that first call before any
- * stream capture.  A device-side timeout leaves C unwritten and cannot be
+ * stream capture, and do not reset the device (cudaDeviceReset) between
+ * calls: the address found is kept for the life of the process.  A
+ * device-side timeout leaves the tiles it hit unwritten and cannot be
  * reported by this entry point. */
 int sgemm_run_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
                       const float *B, int ldb, float beta, float *C, int ldc, void *stream);

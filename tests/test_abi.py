@@ -207,6 +207,8 @@ def test_bad_handles_are_rejected_without_dereference(lib):
         assert lib.sgemm_debug_set_smem_override(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_stream_k_sums(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_cluster_split(fake, 0) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_leave_aborted_state(fake) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_tf32_probe(fake, 0, 1, None, None) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_last_launches(fake) == -1
         assert lib.sgemm_last_relayout(fake) == -1
         assert lib.sgemm_relayout_capacity(fake) == -1

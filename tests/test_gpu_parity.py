@@ -62,34 +62,37 @@ def test_workload_full_oracle(handle, cfg):
     check_untouched(cfg, prob, C_gpu, bufs)
 
 
+# The two large workloads run as the bench times them: A copied transposed
+# (operand re-layout), complete waves of 256 x 128 tiles in the TN layout and
+# a stream-K wave (3 launches in all).
+LARGE_PLAN = (V.VARIANT_TMA_256x128, 1, 3)
+
+
 @pytest.mark.parametrize("cfg", [inputs.CONFIGS[2], inputs.CONFIGS[4]], ids=lambda c: c.name)
-def test_workload_sampled_rows(handle, cfg):
+def test_workload_whole_matrix(handle, cfg):
+    """4096^3 in place (alpha 1.5, beta 0.5) and 8192^3 against the oracle on
+    every element: max |C_gpu - C_ref| <= 1e-2 (K > 1024), all finite,
+    padding, A, B and guard bands untouched."""
     prob = inputs.make_problem(cfg)
     C_gpu, bufs = run_gpu(handle, cfg, prob)
-    rows = sample_rows(cfg.M)
-    ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
-                            cfg.beta, prob.C0, cfg.ldc)
-    got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows]
-    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
-    assert err <= tolerance(cfg.K), (cfg.name, err)
+    plan = (sgemm.sgemm_last_variant(handle)[0], sgemm.sgemm_last_relayout(handle),
+            sgemm.sgemm_last_launches(handle))
+    assert plan == LARGE_PLAN, plan
     assert np.all(np.isfinite(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)))
+    err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
+    assert err <= tolerance(cfg.K), (cfg.name, err)
     check_untouched(cfg, prob, C_gpu, bufs)
 
 
 @pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=lambda c: c.name)
 def test_workload_integer_exact(handle, cfg):
     """Integer entries in [-2, 2]: every partial sum is exact in float32, so
-    the GPU result must equal the oracle bit for bit at every workload shape."""
+    the GPU result must equal the oracle bit for bit, on every element of
+    every workload shape."""
     prob = inputs.make_problem(cfg, kind="integer")
     C_gpu, _ = run_gpu(handle, cfg, prob)
-    if cfg.M * cfg.N * cfg.K <= 1024 ** 3:
-        ref = inputs.dense(oracle_full(cfg, prob), cfg.M, cfg.N, cfg.ldc)
-        got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)
-    else:
-        rows = sample_rows(cfg.M, n_random=8)
-        ref = oracle.sgemm_rows(rows, cfg.N, cfg.K, cfg.alpha, prob.A, cfg.lda, prob.B, cfg.ldb,
-                                cfg.beta, prob.C0, cfg.ldc)
-        got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)[rows]
+    ref = inputs.dense(oracle_full(cfg, prob), cfg.M, cfg.N, cfg.ldc)
+    got = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)
     assert np.array_equal(np.ascontiguousarray(got).view(np.uint32),
                           np.ascontiguousarray(ref).view(np.uint32)), cfg.name
 
@@ -266,6 +269,30 @@ def test_device_timeout_is_reported_and_recoverable(handle):
     prob = inputs.make_problem(cfg)
     C_gpu, _ = run_gpu(handle, cfg, prob)
     assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+
+
+@pytest.mark.parametrize("sums", [V.SK_SUMS_LAST, V.SK_SUMS_SHARED], ids=["last", "shared"])
+def test_counters_restored_after_a_timeout(handle, variant, sums):
+    """A stream-K CTA that gives up a bounded wait leaves its tile's arrival
+    counter unreset.  With every counter left dirty and the timeout bit set
+    (the state such a kernel can leave), sgemm_get_device_status reports the
+    timeout once and restores the counters: the next stream-K calls, whose
+    tiles' parts are added through those counters, match the oracle."""
+    variant(V.VARIANT_TMA_64x64)
+    sgemm.sgemm_debug_set_stream_k_sums(handle, sums)
+    try:
+        cfg = _cfg(1000, 1000, 777, 1.25, 0.5)
+        prob = inputs.make_problem(cfg)
+        sgemm.sgemm_debug_leave_aborted_state(handle)
+        assert sgemm.sgemm_get_device_status(handle) == V.ERR_DEVICE_TIMEOUT
+        assert sgemm.sgemm_get_device_status(handle) == V.OK
+        for _ in range(2):
+            C_gpu, _ = run_gpu(handle, cfg, prob)
+            assert sgemm.sgemm_last_variant(handle)[1] > 1  # a stream-K split
+            assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+        assert sgemm.sgemm_get_device_status(handle) == V.OK
+    finally:
+        sgemm.sgemm_debug_set_stream_k_sums(handle, V.SK_SUMS_AUTO)
 
 
 def test_launch_failure_is_reported_on_the_host(handle, variant):

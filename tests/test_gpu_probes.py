@@ -54,3 +54,20 @@ def test_probe_argument_checks(handle):
     sink = torch.empty(64, device="cuda")
     with pytest.raises(sgemm.SgemmError):
         sgemm.sgemm_debug_bank_probe(handle, 0, sink, ctas=-1)
+
+
+def test_tf32_probe(handle):
+    """The tensor-pipe probe runs to completion with no wait running out, and
+    reports the TF32 FLOP of its MMAs; argument limits are checked."""
+    flops = sgemm.sgemm_debug_tf32_probe(handle, clusters=4, iters=256)
+    torch.cuda.synchronize()
+    assert flops == 2 * 256 * 256 * 32 * 256 * 4
+    assert sgemm.sgemm_get_device_status(handle) == sgemm.OK
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flops = sgemm.sgemm_debug_tf32_probe(handle, iters=64)  # one cluster per pair of SMs
+    torch.cuda.synchronize()
+    assert flops == 2 * 256 * 256 * 32 * 64 * (sms // 2)
+    assert sgemm.sgemm_get_device_status(handle) == sgemm.OK
+    for bad in (dict(clusters=-1), dict(clusters=sms), dict(iters=0), dict(iters=(1 << 20) + 1)):
+        with pytest.raises(sgemm.SgemmError):
+            sgemm.sgemm_debug_tf32_probe(handle, **bad)
