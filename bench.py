@@ -43,7 +43,7 @@ UNIT = "TFLOP/s"
 # kernel ran on, re-layout bits), from a one-pass ncu launch list of the
 # headline command (gpu__time_duration and the DRAM byte counters of every
 # launch of the timed steps); any other source gives traffic = null.
-TRAFFIC_BY_SOURCE = {("ccf21e73415850ef", "TN", 1): 3.364e9}
+TRAFFIC_BY_SOURCE = {("992b753e672b188f", "TN", 1): 3.393e9}
 TC_TRAFFIC_BY_SOURCE = {"3f6064e551384a01": 2.534e9}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]

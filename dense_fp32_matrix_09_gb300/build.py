@@ -19,6 +19,11 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libsgemm.so")
+# The same sources with the device-side index checks compiled in
+# (-DSGEMM_DEVICE_CHECKS): a separate build, used by its own tests.
+BUILD_CHECKED = os.path.join(HERE, "_build_checks")
+LIB_CHECKED = os.path.join(BUILD_CHECKED, "libsgemm_checks.so")
+CHECK_FLAGS = ["-DSGEMM_DEVICE_CHECKS"]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-Wall,-Wextra", "-I" + INCLUDE, "-I" + CSRC]
@@ -47,17 +52,20 @@ def is_stale(lib: str = LIB) -> bool:
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile and link the library; returns its path."""
-    if not force and not is_stale():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          checked: bool = False) -> str:
+    """Compile and link the library (checked: the build with the device-side
+    index checks, in its own directory); returns its path."""
+    out_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    if not force and not is_stale(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + GENCODE + list(extra_flags or [])
+    flags = NVCC_FLAGS + GENCODE + (CHECK_FLAGS if checked else []) + list(extra_flags or [])
     objs = []
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src) + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -68,12 +76,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, "-shared", *GENCODE, "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -16,6 +16,17 @@ namespace sg {
 // FMA work), so only a broken pipeline reaches the limit.
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
 
+// Device-side index checks, compiled in only with -DSGEMM_DEVICE_CHECKS: a
+// failed check sets kDevCheckBit in the status word (never a trap, an assert
+// or an out-of-range access); the caller then replaces the index with one
+// that is in range, so the kernel runs on and ends, with C undefined.
+#ifdef SGEMM_DEVICE_CHECKS
+__device__ __forceinline__ bool dev_check(bool ok, int *status) {
+    if (!ok) atomicOr(status, kDevCheckBit);
+    return ok;
+}
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

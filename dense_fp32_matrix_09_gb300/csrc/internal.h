@@ -10,6 +10,8 @@ namespace sg {
 
 // Bit set in a handle's device status word when a kernel gives up a bounded wait.
 constexpr int kDevTimeoutBit = 1;
+// Bit set when a device-side index check fails (builds with SGEMM_DEVICE_CHECKS only).
+constexpr int kDevCheckBit = 2;
 
 // One call's arguments after validation (sizes > 0, alpha != 0, K > 0 for the
 // GEMM kernels).
@@ -57,6 +59,10 @@ struct SplitK {
     // thread-block cluster, CTA r of the cluster taking K steps [r*kt/ksplit,
     // (r+1)*kt/ksplit); their partial tiles meet in distributed shared memory.
     int ksplit = 1;
+    // Capacities the device-side index checks (SGEMM_DEVICE_CHECKS builds)
+    // hold the stream-K indices to: partial tiles the workspace holds, counters.
+    int ws_tiles = 0;
+    int n_counters = 0;
 };
 
 // How the parts of a split tile are added (always in ascending k order):

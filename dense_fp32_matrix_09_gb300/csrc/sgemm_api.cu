@@ -92,6 +92,7 @@ struct sgemm_ctx {
     int last_relayout;                      // operands the last call transposed (bit 0 A, bit 1 B)
     int sk_sums;                            // test hook: sgemm_sk_sums_t, how stream-K parts are added
     int ksplit_pin;                         // test hook: cluster split-K CTAs per tile (0 auto, 1 none)
+    int ws_tiles_limit;                     // test hook: workspace capacity the kernels are told (0: real)
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
     cudaEvent_t ev_in[16], ev_out[16];      //   one pair per row panel
@@ -647,6 +648,7 @@ const char *sgemm_status_string(int s) {
         case SGEMM_ERR_DEVICE_TIMEOUT: return "SGEMM_ERR_DEVICE_TIMEOUT: a kernel abandoned a bounded wait";
         case SGEMM_ERR_WRONG_DEVICE: return "SGEMM_ERR_WRONG_DEVICE: current device differs from the handle's";
         case SGEMM_ERR_SCRATCH_TOO_SMALL: return "SGEMM_ERR_SCRATCH_TOO_SMALL: more than 512 64x64 output tiles for sgemm_run_noalloc";
+        case SGEMM_ERR_DEVICE_CHECK: return "SGEMM_ERR_DEVICE_CHECK: a device-side index check failed";
         default: return "SGEMM_ERR_UNKNOWN";
     }
 }
@@ -1043,6 +1045,10 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
             sk.ws = h->d_ws;
             sk.counters = h->d_counters;
         }
+        // capacities for the device-side index checks of a checked build
+        sk.ws_tiles = static_cast<int>(h->ws_floats / (static_cast<size_t>(sh.bm) * sh.bn));
+        if (h->ws_tiles_limit > 0) sk.ws_tiles = std::min(sk.ws_tiles, h->ws_tiles_limit);
+        sk.n_counters = h->n_counters;
         CUtensorMap tmA, tmB;
         const bool a_ok = p.op == sg::kTmaOpTN
             ? cached_encode(h, &tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)
@@ -1304,12 +1310,20 @@ int sgemm_get_device_status(sgemm_handle_t h) {
     // A stream-K CTA that gave up a wait leaves before counting its arrival,
     // so its tile's counter is never reset by the CTAs that would add the
     // parts: after a timeout every arrival counter starts again from zero.
-    if (e == cudaSuccess && (word & sg::kDevTimeoutBit))
+    if (e == cudaSuccess && (word & (sg::kDevTimeoutBit | sg::kDevCheckBit)))
         e = cudaMemset(h->d_counters, 0, static_cast<size_t>(h->n_counters) * sizeof(int));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (prev != h->device) cudaSetDevice(prev);
     if (e != cudaSuccess) return SGEMM_ERR_CUDA;
+    if (word & sg::kDevCheckBit) return SGEMM_ERR_DEVICE_CHECK;
     return (word & sg::kDevTimeoutBit) ? SGEMM_ERR_DEVICE_TIMEOUT : SGEMM_OK;
+}
+
+int sgemm_debug_set_workspace_limit(sgemm_handle_t h, int tiles) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (tiles < 0) return SGEMM_ERR_INVALID_VALUE;
+    h->ws_tiles_limit = tiles;
+    return SGEMM_OK;
 }
 
 int sgemm_debug_leave_aborted_state(sgemm_handle_t h) {

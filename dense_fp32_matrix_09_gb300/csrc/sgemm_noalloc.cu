@@ -170,8 +170,10 @@ extern "C" int sgemm_run_noalloc(int M, int N, int K, float alpha, const float *
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SGEMM_ERR_CUDA;
     const long long T = static_cast<long long>(tiles) * cdiv(K, sh.bk);
     const long long G = std::min<long long>({2LL * sms, T, static_cast<long long>(kMaxPartialTiles) - tiles});
-    const sg::SplitK sk = G > tiles ? sg::SplitK{0, static_cast<int>(G), scratch, counters}
-                                    : sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
+    sg::SplitK sk = G > tiles ? sg::SplitK{0, static_cast<int>(G), scratch, counters}
+                              : sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
+    sk.ws_tiles = kMaxPartialTiles;  // for the device-side index checks of a checked build
+    sk.n_counters = kMaxTiles;
 
     CUtensorMap tmA, tmB;
     if (!encode(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -550,8 +550,19 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             bt = (tile0 + 1) / tiles_per;
         }
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
-        const int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
-        const int bx = OP == kOpNT ? kc : n0, by = OP == kOpNT ? n0 : kc;
+        int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
+        int bx = OP == kOpNT ? kc : n0, by = OP == kOpNT ? n0 : kc;
+#ifdef SGEMM_DEVICE_CHECKS
+        {
+            // every box starts inside its tensor (x innermost): A (K, M), TN (M, K); B (N, K), NT (K, N)
+            const int adx = OP == kOpTN ? g.M : g.K, ady = OP == kOpTN ? g.K : g.M;
+            const int bdx = OP == kOpNT ? g.K : g.N, bdy = OP == kOpNT ? g.N : g.K;
+            if (!dev_check(ax >= 0 && ax < adx && ay >= 0 && ay < ady && bx >= 0 && bx < bdx && by >= 0 &&
+                               by < bdy && bt >= 0 && bt < g.batch,
+                           g.status))
+                ax = ay = bx = by = bt = 0;
+        }
+#endif
         if (a3) tma_load_3d(sA + s * C::kABytes, &tmA, &full[s], ax, ay, bt);
         else tma_load_2d(sA + s * C::kABytes, &tmA, &full[s], ax, ay);
         if (b3) tma_load_3d(sB + s * C::kBBytes, &tmB, &full[s], bx, by, bt);
@@ -634,7 +645,11 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (q_first == q_last) break;  // this CTA has the whole tile (one segment): epilogue below
         // store this part (thread-major float4 groups) in slot tl + q and count it
         {
-            float4 *mine = reinterpret_cast<float4 *>(sk.ws + static_cast<size_t>(tl + q) * C::BM * C::BN);
+            int slot = tl + q;
+#ifdef SGEMM_DEVICE_CHECKS
+            if (!dev_check(slot >= 0 && slot < sk.ws_tiles, g.status)) slot = 0;
+#endif
+            float4 *mine = reinterpret_cast<float4 *>(sk.ws + static_cast<size_t>(slot) * C::BM * C::BN);
 #pragma unroll
             for (int u = 0; u < C::TM * C::TN4; ++u) {
                 const int ii = u / C::TN4, jj = u % C::TN4;
@@ -644,15 +659,20 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         ++nseg_done;
         if (sk.fixup == kFixupDeferred) continue;  // the finishing kernel adds the parts after this grid
+#ifdef SGEMM_DEVICE_CHECKS
+        const int tlc = dev_check(tl >= 0 && tl < sk.n_counters, g.status) ? tl : 0;
+#else
+        const int tlc = tl;
+#endif
         __threadfence();
         named_barrier_sync(1, C::kConsumers);
         if (sk.fixup == kFixupShared) {
-            if (tid == 0) atomicAdd(&sk.counters[tl], 1);  // this part has arrived
+            if (tid == 0) atomicAdd(&sk.counters[tlc], 1);  // this part has arrived
             // the CTAs whose K range ends in the tile add its parts, a slice each
             if (seg == nseg - 1) split_last |= 1u << seg;
             continue;
         }
-        if (tid == 0) s_flag[seg] = (atomicAdd(&sk.counters[tl], 1) == q_last - q_first);
+        if (tid == 0) s_flag[seg] = (atomicAdd(&sk.counters[tlc], 1) == q_last - q_first);
         named_barrier_sync(1, C::kConsumers);
         split_last |= static_cast<unsigned>(s_flag[seg] != 0) << seg;
     }
@@ -694,7 +714,11 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 const int ii = u / C::TN4, jj = u % C::TN4;
                 const int n_own = o_end - o_first;
-                float4 *dst = slots + (crank * n_own + (u - o_first)) * C::kConsumers + tid;
+                int slot = crank * n_own + (u - o_first);
+#ifdef SGEMM_DEVICE_CHECKS
+                if (!dev_check(owner < S && slot >= 0 && slot < cluster_slot_groups(kGroups), g.status)) slot = 0;
+#endif
+                float4 *dst = slots + slot * C::kConsumers + tid;
                 st_dsmem_f4(dsmem_addr(dst, static_cast<uint32_t>(owner)),
                             make_float4(acc[ii][4 * jj], acc[ii][4 * jj + 1], acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]));
             }
@@ -738,6 +762,12 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
                 const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
                 float *Ct = g.C + static_cast<long long>(tile / tiles_per) * g.sC;
+#ifdef SGEMM_DEVICE_CHECKS
+                // the counter and every part slot of the tile are in range, else the tile is skipped
+                if (!dev_check(tl >= 0 && tl < sk.n_counters && tl + q_first >= 0 && tl + q_last < sk.ws_tiles,
+                               g.status))
+                    continue;
+#endif
                 if (sk.fixup == kFixupShared) {
                     // The adders are q_first .. q_first + n_add - 1: every CTA of
                     // the tile but the last, whose range usually runs on into
@@ -792,6 +822,9 @@ sk_finish_kernel(const GemmArgs g, const SplitK sk, const int group_m) {
     const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
     const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
     if (q_first == q_last) return;
+#ifdef SGEMM_DEVICE_CHECKS
+    if (!dev_check(tl + q_first >= 0 && tl + q_last < sk.ws_tiles, g.status)) return;
+#endif
     const int tile = sk.dp_tiles + tl;
     int tm, tn;
     tile_coords(tile % tiles_per, tiles_m, tiles_n, group_m, tm, tn);

@@ -25,6 +25,7 @@ ERR_CUDA = 7
 ERR_DEVICE_TIMEOUT = 8
 ERR_WRONG_DEVICE = 9
 ERR_SCRATCH_TOO_SMALL = 10
+ERR_DEVICE_CHECK = 11
 
 VARIANT_AUTO = 0
 VARIANT_TMA_128x256 = 1
@@ -60,7 +61,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
            "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
            "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_leave_aborted_state",
-           "sgemm_debug_tf32_probe")
+           "sgemm_debug_tf32_probe", "sgemm_debug_set_workspace_limit")
 
 
 class SgemmError(RuntimeError):
@@ -73,7 +74,10 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The library to load: the in-tree build, or the file named by the
+    SGEMM_LIBRARY environment variable (a build of the same sources with
+    other flags, such as the device-checked build)."""
+    return os.environ.get("SGEMM_LIBRARY") or _build.LIB
 
 
 def lib() -> ctypes.CDLL:
@@ -109,6 +113,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
         L.sgemm_debug_set_cluster_split.argtypes = [vp, i32]
         L.sgemm_debug_leave_aborted_state.argtypes = [vp]
+        L.sgemm_debug_set_workspace_limit.argtypes = [vp, i32]
         L.sgemm_status_string.argtypes = [i32]
         L.sgemm_status_string.restype = ctypes.c_char_p
         L.sgemm_variant_name.argtypes = [i32]
@@ -317,6 +322,10 @@ def sgemm_debug_timeout_probe(h, limit_ns: int, stream=None) -> None:
 
 def sgemm_debug_set_smem_override(h, nbytes: int) -> None:
     _check(lib().sgemm_debug_set_smem_override(h, int(nbytes)), "sgemm_debug_set_smem_override")
+
+
+def sgemm_debug_set_workspace_limit(h, tiles: int) -> None:
+    _check(lib().sgemm_debug_set_workspace_limit(h, int(tiles)), "sgemm_debug_set_workspace_limit")
 
 
 def sgemm_debug_leave_aborted_state(h) -> None:

@@ -70,7 +70,9 @@ typedef enum {
     SGEMM_ERR_CUDA = 7,               /* another CUDA runtime error                    */
     SGEMM_ERR_DEVICE_TIMEOUT = 8,     /* a kernel gave up a bounded wait (device side) */
     SGEMM_ERR_WRONG_DEVICE = 9,       /* current device differs from the handle's      */
-    SGEMM_ERR_SCRATCH_TOO_SMALL = 10  /* sgemm_run_noalloc: problem exceeds its scratch */
+    SGEMM_ERR_SCRATCH_TOO_SMALL = 10, /* sgemm_run_noalloc: problem exceeds its scratch */
+    SGEMM_ERR_DEVICE_CHECK = 11       /* a device-side index check failed (builds with
+                                         -DSGEMM_DEVICE_CHECKS only)                    */
 } sgemm_status_t;
 
 /* Kernel variants.  SGEMM_VARIANT_AUTO lets sgemm_run choose from the shape
@@ -306,12 +308,23 @@ int sgemm_last_launches(sgemm_handle_t h);
 /* Wait for the handle's device to finish its work, then read and clear the
  * handle's device-side status word.  Returns SGEMM_OK, or
  * SGEMM_ERR_DEVICE_TIMEOUT if any kernel of the handle abandoned a bounded
- * wait, or SGEMM_ERR_CUDA.  After a timeout the C of the calls since the last
+ * wait, SGEMM_ERR_DEVICE_CHECK if a device-side index check failed (builds
+ * with -DSGEMM_DEVICE_CHECKS; the check replaces the index with one in range,
+ * so nothing is accessed out of bounds), or SGEMM_ERR_CUDA.  After a timeout the C of the calls since the last
  * check is undefined: some tiles may be unwritten and some may hold partial
- * sums or stale workspace contents.  On a timeout this call also clears the
- * handle's stream-K arrival counters (a CTA that gave up leaves its tile's
- * counter unreset), so later calls on the handle are correct again. */
+ * sums or stale workspace contents.  On a timeout or a failed check this
+ * call also clears the handle's stream-K arrival counters (a CTA that gave up
+ * leaves its tile's counter unreset), so later calls on the handle are
+ * correct again. */
 int sgemm_get_device_status(sgemm_handle_t h);
+
+/* Test hook: the stream-K workspace capacity, in partial tiles, that later
+ * calls of the handle pass to their kernels for the device-side index checks
+ * (0: the workspace's real size).  The plan still uses the real size, so a
+ * limit below what a call needs makes a build with -DSGEMM_DEVICE_CHECKS
+ * report SGEMM_ERR_DEVICE_CHECK for it -- every access stays inside the real
+ * workspace -- and changes nothing in a build without the checks. */
+int sgemm_debug_set_workspace_limit(sgemm_handle_t h, int tiles);
 
 /* Test hook: put the handle in the state that a stream-K kernel which gave
  * up a bounded wait can leave behind -- every arrival counter nonzero and

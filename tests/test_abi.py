@@ -41,7 +41,7 @@ def test_built_for_sm103a_only():
 
 
 def test_status_and_variant_strings(lib):
-    for s in range(10):
+    for s in range(12):
         assert sgemm.status_string(s).startswith("SGEMM_")
     assert sgemm.status_string(99) == "SGEMM_ERR_UNKNOWN"
     assert sgemm.variant_name(sgemm.VARIANT_TMA_128x256) == "tma_128x256"
@@ -63,6 +63,7 @@ def test_binding_constants_match_the_header():
              "ERR_UNSUPPORTED_DEVICE": "SGEMM_ERR_UNSUPPORTED_DEVICE", "ERR_LAUNCH": "SGEMM_ERR_LAUNCH",
              "ERR_CUDA": "SGEMM_ERR_CUDA", "ERR_DEVICE_TIMEOUT": "SGEMM_ERR_DEVICE_TIMEOUT",
              "ERR_WRONG_DEVICE": "SGEMM_ERR_WRONG_DEVICE", "ERR_SCRATCH_TOO_SMALL": "SGEMM_ERR_SCRATCH_TOO_SMALL",
+             "ERR_DEVICE_CHECK": "SGEMM_ERR_DEVICE_CHECK",
              "MATH_FP32": "SGEMM_MATH_FP32", "MATH_3XTF32": "SGEMM_MATH_3XTF32", "IN_BF16": "SGEMM_IN_BF16",
              "IN_F16": "SGEMM_IN_F16", "RELAYOUT_AUTO": "SGEMM_RELAYOUT_AUTO", "RELAYOUT_OFF": "SGEMM_RELAYOUT_OFF",
              "RELAYOUT_ALWAYS": "SGEMM_RELAYOUT_ALWAYS", "VARIANT_COUNT": "SGEMM_VARIANT_COUNT_"}
@@ -209,6 +210,7 @@ def test_bad_handles_are_rejected_without_dereference(lib):
         assert lib.sgemm_debug_set_cluster_split(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_leave_aborted_state(fake) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_tf32_probe(fake, 0, 1, None, None) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_set_workspace_limit(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_last_launches(fake) == -1
         assert lib.sgemm_last_relayout(fake) == -1
         assert lib.sgemm_relayout_capacity(fake) == -1

@@ -295,6 +295,22 @@ def test_counters_restored_after_a_timeout(handle, variant, sums):
         sgemm.sgemm_debug_set_stream_k_sums(handle, V.SK_SUMS_AUTO)
 
 
+def test_workspace_limit_hook_is_inert_without_checks(handle, variant):
+    """The release build compiles no device-side checks: the workspace
+    capacity the kernels are told does not change a stream-K call."""
+    variant(V.VARIANT_TMA_64x64)
+    cfg = _cfg(1000, 1000, 777, 1.0, 0.0)
+    prob = inputs.make_problem(cfg)
+    sgemm.sgemm_debug_set_workspace_limit(handle, 1)
+    try:
+        C_gpu, _ = run_gpu(handle, cfg, prob)
+    finally:
+        sgemm.sgemm_debug_set_workspace_limit(handle, 0)
+    assert sgemm.sgemm_last_variant(handle)[1] > 1
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK
+
+
 def test_launch_failure_is_reported_on_the_host(handle, variant):
     """Requesting more shared memory than an SM has makes the launch fail on
     the host before anything runs; C is untouched and later calls work."""
