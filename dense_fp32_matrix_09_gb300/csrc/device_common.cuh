@@ -142,6 +142,16 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, for a CTA that arrives early and
+// waits later (every thread of every CTA of the cluster executes both, in
+// turn).  Relaxed: the pair orders no memory, it only tells the waiter that
+// every CTA of the cluster has arrived, i.e. is running, so that its shared
+// memory may be written through distributed shared memory.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // This CTA's rank in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;

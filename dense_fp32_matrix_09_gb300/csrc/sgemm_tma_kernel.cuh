@@ -459,6 +459,26 @@ __host__ __device__ constexpr int cluster_slot_groups(int groups) {
     return most;
 }
 
+// Cluster split-K: where an owner's slots lie.  When they fit beyond the
+// pipeline's buffers (stages, NT transpose buffers, mbarriers) within the
+// 227 KiB a CTA may have -- the 64 x 64 and 128 x 128 tiles -- peers push into
+// them while this CTA may still run its main loop; the larger tiles' slots
+// reuse the stage buffers, which only a cluster barrier after every CTA's
+// main loop frees.
+constexpr int kMaxDynSmem = 227 * 1024;
+template <class C, int OP>
+__host__ __device__ constexpr int cluster_slots_offset() {
+    return (C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0) + 2 * C::STAGES * 8 + 16 + 127) / 128 * 128;
+}
+template <class C>
+__host__ __device__ constexpr int cluster_slot_bytes() {
+    return cluster_slot_groups(C::TM * C::TN4) * C::kConsumers * 16;
+}
+template <class C, int OP>
+__host__ __device__ constexpr bool cluster_slots_apart() {
+    return cluster_slots_offset<C, OP>() + cluster_slot_bytes<C>() + 1024 <= kMaxDynSmem;
+}
+
 // Kernel modes (template parameter MODE): whole tiles; the stream-K CTAs of a
 // hybrid grid; cluster split-K (one cluster of sk.ksplit CTAs per tile).
 constexpr int kModeWhole = 0, kModeStreamK = 1, kModeCluster = 2;
@@ -529,6 +549,9 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         fence_barrier_init();
     }
     __syncthreads();
+    // cluster split-K with slots apart: this CTA is running (peers wait for
+    // that before their first push into its shared memory)
+    if constexpr (CLUSTER && cluster_slots_apart<C, OP>()) cluster_arrive_relaxed();
 
     // Thread 0 issues the TMA loads of the CTA's t-th iteration into stage t % STAGES.
     int m0w, n0w;  // the first segment's tile
@@ -681,28 +704,33 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         // Cluster split-K: the tile's S = ksplit CTAs are one cluster, and
         // CTA r owns float4 groups [r*G/S, (r+1)*G/S) of the tile (group u of
         // thread tid holds accumulators ii = u / TN4, columns 4(u % TN4) ..
-        // +3).  Once every CTA of the cluster is past its main loop (cluster
-        // barrier: their stage buffers are free), each pushes every group
-        // into the shared memory of the group's owner -- slot [r][u - first
-        // owned group][tid] -- with distributed-shared-memory stores; after a
-        // second barrier makes them visible, each owner adds its slots in
-        // rank (= ascending k) order and runs the epilogue on the sums.  No
-        // shared memory of another CTA is touched after that barrier.  An
-        // abort (a bounded wait gave up) is agreed on within the CTA first;
-        // the CTA then waits for its own loads in flight, pushes nothing and
-        // still takes part in both barriers (C is then undefined, the status
-        // word set).
+        // +3).  Each CTA pushes every group into the shared memory of the
+        // group's owner -- slot [r][u - first owned group][tid] -- with
+        // distributed-shared-memory stores; after a cluster barrier makes them
+        // visible, each owner adds its slots in rank (= ascending k) order and
+        // runs the epilogue on the sums.  Where the slots lie beyond the
+        // pipeline's buffers, a CTA pushes as soon as its own loop is done
+        // (having waited only for every CTA of the cluster to be running);
+        // otherwise the slots are the stage buffers and a first cluster
+        // barrier waits until every CTA is past its main loop.  No shared
+        // memory of another CTA is touched after the last barrier.  An abort
+        // (a bounded wait gave up) is agreed on within the CTA first; the CTA
+        // then waits for its own loads in flight, pushes nothing and still
+        // takes part in the barriers (C is then undefined, the status word
+        // set).
         constexpr int kGroups = C::TM * C::TN4;
-        static_assert(cluster_slot_groups(kGroups) * C::kConsumers * 16 <=
-                          C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0),
+        constexpr bool kApart = cluster_slots_apart<C, OP>();
+        static_assert(kApart || cluster_slot_groups(kGroups) * C::kConsumers * 16 <=
+                                    C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0),
                       "an owner's slots fit in the stage (and NT transpose) buffers, below the mbarriers");
         const int S = sk.ksplit;
         const bool bad = named_barrier_or(1, C::kConsumers, aborted);
         if (bad && tid == 0)
             for (int t = max(0, issued - C::STAGES); t < issued; ++t)
                 mbar_wait(&full[t % C::STAGES], (t / C::STAGES) & 1, g.status);
-        cluster_sync();
-        float4 *slots = reinterpret_cast<float4 *>(smem);
+        if constexpr (kApart) cluster_wait();  // every CTA of the cluster is running
+        else cluster_sync();                   // every CTA is past its main loop
+        float4 *slots = reinterpret_cast<float4 *>(smem + (kApart ? cluster_slots_offset<C, OP>() : 0));
         if (!bad) {
             int owner = 0, o_first = 0, o_end = kGroups / S;  // the owner of group u, and its groups
 #pragma unroll
@@ -869,7 +897,9 @@ constexpr int kClusterSmemFloor = 120 * 1024;
 
 template <class C, int OP>
 constexpr int cluster_smem_bytes() {
-    return smem_bytes<C, OP>() > kClusterSmemFloor ? smem_bytes<C, OP>() : kClusterSmemFloor;
+    constexpr int need = cluster_slots_apart<C, OP>() ? cluster_slots_offset<C, OP>() + cluster_slot_bytes<C>() + 1024
+                                                      : smem_bytes<C, OP>();
+    return need > kClusterSmemFloor ? need : kClusterSmemFloor;
 }
 
 template <class C, int OP>
