@@ -109,10 +109,12 @@ bool tc3x_shape(TmaShape *out);
 cudaError_t tc3x_prepare();
 cudaError_t launch_tc3x(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
                         cudaStream_t stream);
-// CTA-pair version (cta_group::2, 256 x 256 tile per cluster of two CTAs); same boxes.
+// CTA-pair version (cta_group::2, 256 x 256 tile per cluster of two CTAs); same
+// boxes, or, with b_kmajor, B stored N x K (g.B the N x K matrix) with boxes
+// 32 k x 128 n and the 128-byte swizzle, like A's.
 cudaError_t tc3x_pair_prepare();
 cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB,
-                             int smem_override, cudaStream_t stream);
+                             int smem_override, cudaStream_t stream, bool b_kmajor);
 
 // in_type: 0 FP32 inputs, else SGEMM_IN_BF16 / SGEMM_IN_F16 (A and B hold 16-bit values)
 cudaError_t launch_generic(const GemmArgs &g, cudaStream_t stream, int in_type = 0);

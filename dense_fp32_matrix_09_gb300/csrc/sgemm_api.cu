@@ -37,6 +37,7 @@ struct CallPlan {
     sg::SplitK sk{0, 0, nullptr, nullptr};
     int splits = 1;    // CTAs per stream-K tile (rounded up; 1 without)
     int launches = 1;  // kernel launches the call enqueues
+    int tc_bk = 0;     // tensor-core pair kernel reading B stored N x K (K-major)
 };
 
 // Everything a plan depends on besides the handle's fixed device facts.
@@ -535,19 +536,25 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                    long long strideB, bool tma_ok) {
     CallPlan p;
-    // The tensor-core kernels read A stored M x K and B stored K x N, batch 1;
-    // another layout reaches them through transposed copies of its stored-
-    // transposed operands in the re-layout workspace (A stored K x M -> M x K,
-    // B stored N x K -> K x N), when re-layout is not off and the copies fit.
+    // The tensor-core kernels read A stored M x K, and B stored K x N or (the
+    // pair kernel's faster form) B stored N x K, batch 1; other layouts reach
+    // them through transposed copies of their operands in the re-layout
+    // workspace, when re-layout is not off and the copies fit.
+    const bool can_copy = h->relayout_mode != SGEMM_RELAYOUT_OFF && h->rl_floats > 0;
+    const unsigned long long a_copy = transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0;
+    // B stored K x N: A^T copied to M x K, B^T (stored N x K) copied to K x N
     const int tc_copy = (transA ? 1 : 0) | (transB ? 2 : 0);
     const unsigned long long tc_need =
-        (transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32) : 0) +
-        (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
+        a_copy + (transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32) : 0);
+    // B stored N x K: a B stored K x N copied transposed to N x K
+    const int bk_copy = (transA ? 1 : 0) | (transB ? 0 : 2);
+    const unsigned long long bk_need =
+        a_copy + (transB ? 0 : static_cast<unsigned long long>(N) * ((K + 31ULL) / 32 * 32));
+    const bool kn_ok = tc_copy == 0 || (can_copy && tc_need <= h->rl_floats);
+    const bool bk_ok = bk_copy == 0 || (can_copy && bk_need <= h->rl_floats);
     // A strided batch runs as one tensor-core launch per product (the
     // kernels hold no batch index), up to kMaxTcBatch products.
-    const bool tc_reachable = batch <= kMaxTcBatch &&
-                              (tc_copy == 0 || (h->relayout_mode != SGEMM_RELAYOUT_OFF && h->rl_floats > 0 &&
-                                                tc_need <= h->rl_floats));
+    const bool tc_reachable = batch <= kMaxTcBatch && (kn_ok || bk_ok);
     int variant = h->pinned;
     if (!tc_reachable && (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR))
         variant = SGEMM_VARIANT_AUTO;
@@ -563,10 +570,12 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     if (!tma_ok || variant == SGEMM_VARIANT_GENERIC) return p;  // the generic kernel on the stored operands
 
     if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
+        if (variant == SGEMM_VARIANT_TC_3XTF32 && !kn_ok) return p;  // the one-CTA kernel reads B stored K x N
         p.kind = kPlanTensorCore;
         p.variant = variant;
-        p.copies = tc_copy;
-        p.launches = batch * (1 + (tc_copy & 1) + ((tc_copy >> 1) & 1));
+        p.tc_bk = variant == SGEMM_VARIANT_TC_3XTF32_PAIR && bk_ok ? 1 : 0;
+        p.copies = p.tc_bk ? bk_copy : tc_copy;
+        p.launches = batch * (1 + (p.copies & 1) + ((p.copies >> 1) & 1));
         return p;
     }
 
@@ -950,10 +959,12 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
                 tA_ = h->d_rl;
                 tlda = ld;
             }
-            if (p.copies & 2) {  // B stored N x K -> K x N, after A's copy if both
+            if (p.copies & 2) {  // B transposed: stored N x K -> K x N, or (pair kernel, K-major B)
+                             // stored K x N -> N x K; after A's copy if both
                 float *dst = h->d_rl + ((p.copies & 1) ? static_cast<size_t>(M) * round32(K) : 0);
-                const int ld = round32(N);
-                const int rc = from_cuda(sg::launch_transpose(Bb, N, K, ldb, dst, ld, stream));
+                const int ld = p.tc_bk ? round32(K) : round32(N);
+                const int rc = from_cuda(p.tc_bk ? sg::launch_transpose(Bb, K, N, ldb, dst, ld, stream)
+                                                 : sg::launch_transpose(Bb, N, K, ldb, dst, ld, stream));
                 if (rc != SGEMM_OK) return rc;
                 tB_ = dst;
                 tldb = ld;
@@ -968,12 +979,14 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
             gt.batch = 1;
             gt.sA = gt.sB = gt.sC = 0;
             CUtensorMap tA, tB;
-            if (!cached_encode(h, &tA, tA_, M, K, tlda, 1, 0, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !cached_encode(h, &tB, tB_, K, N, tldb, 1, 0, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B))
+            const bool b_ok = p.tc_bk
+                ? cached_encode(h, &tB, tB_, N, K, tldb, 1, 0, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B)  // as A
+                : cached_encode(h, &tB, tB_, K, N, tldb, 1, 0, 32, ts.bk, CU_TENSOR_MAP_SWIZZLE_128B);
+            if (!cached_encode(h, &tA, tA_, M, K, tlda, 1, 0, ts.bk, ts.bm, CU_TENSOR_MAP_SWIZZLE_128B) || !b_ok)
                 return SGEMM_ERR_CUDA;
             const int rc = from_cuda(p.variant == SGEMM_VARIANT_TC_3XTF32
                                          ? sg::launch_tc3x(gt, tA, tB, h->smem_override, stream)
-                                         : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream));
+                                         : sg::launch_tc3x_pair(gt, tA, tB, h->smem_override, stream, p.tc_bk != 0));
             if (rc != SGEMM_OK) return rc;
         }
         h->last_variant = p.variant;
@@ -1366,7 +1379,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     c.math_mode = math_mode;
     c.pinned = pinned;
     for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) c.ctas_per_sm[v] = ctas_per_sm[v];
-    for (int i = 0; i < 11; ++i) out[i] = 0;
+    for (int i = 0; i < 12; ++i) out[i] = 0;
     out[10] = 1;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;  // nothing runs
     if (alpha == 0.f || K == 0) {
@@ -1393,6 +1406,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     out[8] = p.splits;
     out[9] = p.kind == kPlanTma && p.sk.sk_ctas > 0 ? p.sk.fixup : 0;
     out[10] = p.kind == kPlanTma ? p.sk.ksplit : 1;
+    out[11] = p.tc_bk;
     return SGEMM_OK;
 }
 

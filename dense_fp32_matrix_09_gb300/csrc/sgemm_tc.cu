@@ -11,7 +11,9 @@
 // only in passing (page "GPU-accelerated matrix computation optimisation and
 // CUDA programming practice", section 1; page "GEMM advanced: co-optimising
 // instruction-level parallelism and bank conflicts", section 5.3); the FP32
-// contract (max-abs tolerance) is the same as for the SIMT kernels.
+// contract (max-abs tolerance) is the same as for the SIMT kernels.  The
+// CTA-pair kernel's K-major-B form takes x_hi = trunc_tf32(x) instead (the
+// tile as loaded; see the pair kernel below), with the same error bound.
 //
 // One CTA computes a 128 x 256 tile of C with 2 + kConvWarps warps:
 //   warp 0      TMA producer (one lane): into stage s of a 2-stage ring, the A
@@ -92,6 +94,18 @@ __device__ __forceinline__ void split4(float4 *hi_io, float4 *lo_out) {
     h.z = tc::to_tf32(v.z); l.z = tc::to_tf32(v.z - h.z);
     h.w = tc::to_tf32(v.w); l.w = tc::to_tf32(v.w - h.w);
     *hi_io = h;
+    *lo_out = l;
+}
+
+// lo part only of one 16-byte group (the tile as loaded is the hi part: the
+// tensor core reads it truncated to TF32): lo = rna_tf32(x - trunc_tf32(x)).
+__device__ __forceinline__ void split_lo4(const float4 *src, float4 *lo_out) {
+    const float4 v = *src;
+    float4 l;
+    l.x = tc::to_tf32(v.x - __uint_as_float(__float_as_uint(v.x) & 0xFFFFE000u));
+    l.y = tc::to_tf32(v.y - __uint_as_float(__float_as_uint(v.y) & 0xFFFFE000u));
+    l.z = tc::to_tf32(v.z - __uint_as_float(__float_as_uint(v.z) & 0xFFFFE000u));
+    l.w = tc::to_tf32(v.w - __uint_as_float(__float_as_uint(v.w) & 0xFFFFE000u));
     *lo_out = l;
 }
 
@@ -367,6 +381,20 @@ sgemm_tc3x_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 // barriers of both CTAs (multicast commit).  Per SM this halves the B split
 // and the B operand traffic of the one-CTA kernel, which leaves shared-memory
 // room for three stages.
+//
+// Two forms, by how B reaches the kernel:
+//  - B stored K x N (BK = false): B lands as [32 k][32 n] boxes and the split
+//    warps transpose it into K-major B_hi / B_lo, rounding hi and lo to TF32
+//    as above (A too: hi written back in place);
+//  - B stored N x K, i.e. K-major in memory (BK = true; an NN call gets there
+//    through a transposed copy of B in HBM first): A and B land K-major, and
+//    the split warps only compute and store the lo parts.  The tensor core
+//    reads an FP32 value as TF32 by ignoring its low 13 significand bits, so
+//    the tile as loaded already is x_hi = trunc_tf32(x); x - x_hi is exact in
+//    FP32 (the low 13 bits), and x_lo = rna_tf32(x - x_hi) keeps all but its
+//    last 2 bits: |x - x_hi - x_lo| <= 2^-22 |x|, as with x_hi = rna(x).  Half
+//    the split's shared-memory stores, no transposition, no bank conflicts:
+//    the split was what bounded the pair kernel (tensor pipe 68 % active).
 constexpr int PSTAGES = 3;
 constexpr int PBN = 128;                                 // B columns per CTA (256 per pair)
 constexpr int kPBBytes = TBK * PBN * 4;                  // 16 KiB
@@ -397,6 +425,7 @@ struct TcPairSmem {
     int abort;
 };
 
+template <bool BK>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const GemmArgs g) {
@@ -457,15 +486,23 @@ sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const int kc = t * TBK;
                 mbar_arrive_expect_tx(&sh->full[s], kABytesTc + kPBBytes);
                 tma_load_2d(stA(s), &tmA, &sh->full[s], kc, m0);
+                if constexpr (BK) {
+                    tma_load_2d(stB(s), &tmB, &sh->full[s], kc, nb0);  // [128 n][32 k], like A
+                } else {
 #pragma unroll
-                for (int j = 0; j < PBN / 32; ++j)
-                    tma_load_2d(stB(s) + j * 4096, &tmB, &sh->full[s], nb0 + 32 * j, kc);
+                    for (int j = 0; j < PBN / 32; ++j)
+                        tma_load_2d(stB(s) + j * 4096, &tmB, &sh->full[s], nb0 + 32 * j, kc);
+                }
                 ++issued;
                 if (t + PSTAGES < nkt) {
                     const int kp = (t + PSTAGES) * TBK;
                     tma_prefetch_2d(&tmA, kp, m0);
+                    if constexpr (BK) {
+                        tma_prefetch_2d(&tmB, kp, nb0);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < PBN / 32; ++j) tma_prefetch_2d(&tmB, nb0 + 32 * j, kp);
+                        for (int j = 0; j < PBN / 32; ++j) tma_prefetch_2d(&tmB, nb0 + 32 * j, kp);
+                    }
                 }
             }
             for (int t = max(0, issued - PSTAGES); t < issued; ++t)
@@ -523,12 +560,22 @@ sgemm_tc3x_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             }
             float4 *a = reinterpret_cast<float4 *>(stA(s));
             float4 *al = reinterpret_cast<float4 *>(stAlo(s));
+            if constexpr (BK) {
+                // lo parts only; the tiles as loaded are the hi parts
+                const float4 *b = reinterpret_cast<const float4 *>(stB(s));
+                float4 *bl = reinterpret_cast<float4 *>(stBlo(s));
 #pragma unroll 4
-            for (int i = gt; i < kABytesTc / 16; i += kGroupThreads) split4(a + i, al + i);
-            BBlocks<PBN / 32, kGroupWarps> bb;
-            load_b_blocks<PBN / 32, kGroupWarps>(stB(s), gt, bb);
-            named_barrier_sync(bar0 + 1, kGroupThreads);  // every read of the FP32 B tile is done
-            store_b_split<PBN / 32, kGroupWarps>(stB(s), stBlo(s), gt, bb);
+                for (int i = gt; i < kABytesTc / 16; i += kGroupThreads) split_lo4(a + i, al + i);
+#pragma unroll 4
+                for (int i = gt; i < kPBBytes / 16; i += kGroupThreads) split_lo4(b + i, bl + i);
+            } else {
+#pragma unroll 4
+                for (int i = gt; i < kABytesTc / 16; i += kGroupThreads) split4(a + i, al + i);
+                BBlocks<PBN / 32, kGroupWarps> bb;
+                load_b_blocks<PBN / 32, kGroupWarps>(stB(s), gt, bb);
+                named_barrier_sync(bar0 + 1, kGroupThreads);  // every read of the FP32 B tile is done
+                store_b_split<PBN / 32, kGroupWarps>(stB(s), stBlo(s), gt, bb);
+            }
             tc::fence_proxy_async_smem();
             named_barrier_sync(bar0 + 2, kGroupThreads);  // this group's half of the stage is written
             if (gt == 0) tc::mbar_arrive_cluster(conv_even + s * 8);  // the even CTA's conv[s]
@@ -627,15 +674,23 @@ long long launch_tf32_probe(int *status, int clusters, int iters, cudaStream_t s
 }
 
 cudaError_t tc3x_pair_prepare() {
-    return cudaFuncSetAttribute(sgemm_tc3x_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTcPair);
+    const cudaError_t e =
+        cudaFuncSetAttribute(sgemm_tc3x_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTcPair);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(sgemm_tc3x_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemTcPair);
 }
 
-// Two CTAs (one cluster) per 256 x 256 tile; the cluster shape is part of the kernel.
+// Two CTAs (one cluster) per 256 x 256 tile; the cluster shape is part of the
+// kernel.  b_kmajor: B is stored N x K (tmB boxes 32 k x 128 n), else K x N.
 cudaError_t launch_tc3x_pair(const GemmArgs &g, const CUtensorMap &tmA, const CUtensorMap &tmB, int smem_override,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool b_kmajor) {
     const int tiles = ((g.M + 2 * TBM - 1) / (2 * TBM)) * ((g.N + 2 * PBN - 1) / (2 * PBN));
     const int smem = smem_override > 0 ? smem_override : kSmemTcPair;
-    sgemm_tc3x_pair_kernel<<<2 * tiles, kPairThreads, smem, stream>>>(tmA, tmB, g);
+    if (b_kmajor)
+        sgemm_tc3x_pair_kernel<true><<<2 * tiles, kPairThreads, smem, stream>>>(tmA, tmB, g);
+    else
+        sgemm_tc3x_pair_kernel<false><<<2 * tiles, kPairThreads, smem, stream>>>(tmA, tmB, g);
     return cudaGetLastError();
 }
 

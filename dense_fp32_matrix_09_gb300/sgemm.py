@@ -292,7 +292,7 @@ def sgemm_relayout_capacity(h) -> int:
 
 
 PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits",
-               "fixup", "ksplit")
+               "fixup", "ksplit", "tc_bk")
 # "fixup": how the stream-K tiles' parts are added (0 last CTA or no stream-K, 1 second kernel, 2 shared)
 FIXUP_LAST, FIXUP_DEFERRED, FIXUP_SHARED = 0, 1, 2
 PLAN_NOTHING, PLAN_SCALE, PLAN_TENSOR_CORE, PLAN_GENERIC, PLAN_TMA = 0, 1, 2, 3, 4

@@ -422,7 +422,7 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
  * indexed by sgemm_variant_t: resident CTAs per SM of each TMA variant) and
  * its settings (re-layout workspace size in floats, re-layout mode, math
  * mode, pinned variant).  `tma_ok` says whether A and B are 16-byte aligned
- * with lda, ldb (and batch strides) multiples of 4.  out[0..10] receives: the
+ * with lda, ldb (and batch strides) multiples of 4.  out[0..11] receives: the
  * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
  * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
  * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
@@ -430,8 +430,9 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
  * tiles of the call, the kernel launches, the CTAs per stream-K tile, and how
  * the stream-K tiles' parts are added (0 by the last CTA of each tile to
  * arrive, or without stream-K; 1 by a second kernel; 2 shared by the CTAs
- * whose K range ends in the tile), and the cluster split-K CTAs per tile (1:
- * none).
+ * whose K range ends in the tile), the cluster split-K CTAs per tile (1:
+ * none), and 1 when the 3xTF32 pair kernel reads B stored N x K (an operand
+ * stored K x N is then copied transposed first; 0: B stored K x N).
  * SGEMM_ERR_NULL for a NULL array, SGEMM_ERR_INVALID_VALUE for an argument out
  * of range. */
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,

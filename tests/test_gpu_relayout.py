@@ -277,22 +277,25 @@ def test_graph_capture_with_relayout(handle, mode):
 
 
 TC_VARIANTS = (V.VARIANT_TC_3XTF32, V.VARIANT_TC_3XTF32_PAIR)
-TC_COPIES = {(0, 0): 0, (0, 1): 2, (1, 0): 1, (1, 1): 3}  # operands copied into the NN layout
+# operands copied transposed first: the one-CTA kernel reads A stored M x K
+# and B stored K x N; the pair kernel A stored M x K and B stored N x K
+TC_COPIES = {V.VARIANT_TC_3XTF32: {(0, 0): 0, (0, 1): 2, (1, 0): 1, (1, 1): 3},
+             V.VARIANT_TC_3XTF32_PAIR: {(0, 0): 2, (0, 1): 0, (1, 0): 3, (1, 1): 1}}
 
 
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)
 @pytest.mark.parametrize("v", TC_VARIANTS, ids=lambda v: sgemm.variant_name(v))
 def test_tensor_core_kernels_in_every_layout(handle, mode, op, v):
-    """The 3xTF32 kernels read A stored M x K and B stored K x N; the other
-    layouts reach them through transposed copies (A stored K x M, B stored
-    N x K), on a ragged shape of several tiles each way."""
+    """The 3xTF32 kernels read A stored M x K and B stored K x N (one CTA per
+    tile) or N x K (CTA pairs); the other layouts reach them through
+    transposed copies, on a ragged shape of several tiles each way."""
     mode(V.RELAYOUT_AUTO, v)
     p = ExProblem(op[0], op[1], 300, 520, 270, batch=1, seed=161, alpha=1.5, beta=-0.5, pad=(4, 4, 4), mult4=True)
     C, bufs = p.run(handle)
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] == v
-    assert sgemm.sgemm_last_relayout(handle) == TC_COPIES[op]
-    assert sgemm.sgemm_last_launches(handle) == 1 + bin(TC_COPIES[op]).count("1")
+    assert sgemm.sgemm_last_relayout(handle) == TC_COPIES[v][op]
+    assert sgemm.sgemm_last_launches(handle) == 1 + bin(TC_COPIES[v][op]).count("1")
 
 
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)
@@ -332,7 +335,18 @@ def test_tensor_core_strided_batch(handle, mode, op):
     C, bufs = p.run(handle)
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TC_3XTF32_PAIR
-    assert sgemm.sgemm_last_launches(handle) == 3 * (1 + bin(TC_COPIES[op]).count("1"))
+    assert sgemm.sgemm_last_launches(handle) == 3 * (1 + bin(TC_COPIES[V.VARIANT_TC_3XTF32_PAIR][op]).count("1"))
+
+
+def test_pair_kernel_reading_b_stored_k_by_n(handle, mode):
+    """With re-layout off an NN call cannot have B copied, and the pair kernel
+    reads B stored K x N (transposing it in shared memory) instead."""
+    mode(V.RELAYOUT_OFF, V.VARIANT_TC_3XTF32_PAIR)
+    p = ExProblem(0, 0, 300, 520, 270, batch=1, seed=191, alpha=1.5, beta=-0.5, pad=(4, 4, 4), mult4=True)
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TC_3XTF32_PAIR
+    assert sgemm.sgemm_last_relayout(handle) == 0 and sgemm.sgemm_last_launches(handle) == 1
 
 
 def test_math_mode_3xtf32_batched(handle, mode):

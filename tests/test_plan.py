@@ -138,20 +138,30 @@ def test_plan_kinds():
 
 def test_tensor_core_plans():
     """3xTF32 mode: the CTA-pair kernel from SMs/4 tiles of 256 x 256 and
-    K >= 256, in every layout (transposed operands copied into the NN layout;
-    not with re-layout off), batches of up to 256 products one launch each."""
-    for op, copies in (((0, 0), 0), ((0, 1), 2), ((1, 0), 1), ((1, 1), 3)):
+    K >= 256, in every layout.  Its faster form reads A stored M x K and B
+    stored N x K (both K-major): A stored K x M and B stored K x N are copied
+    transposed first (NN: B; NT: nothing; TN: both; TT: A).  With re-layout
+    off, NN runs the form that reads B stored K x N (no copy), NT the K-major
+    form, TN and TT the SIMT kernels.  Batches of up to 256 products, one
+    launch each after its copies."""
+    for op, copies in (((0, 0), 2), ((0, 1), 0), ((1, 0), 3), ((1, 1), 1)):
         p = plan(*op, 8192, 8192, 8192, math_mode=V.MATH_3XTF32)
-        assert (p["kind"], p["variant"], p["copies"]) == (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32_PAIR, copies)
+        assert (p["kind"], p["variant"], p["copies"], p["tc_bk"]) == \
+            (V.PLAN_TENSOR_CORE, V.VARIANT_TC_3XTF32_PAIR, copies, 1), (op, p)
         assert p["launches"] == 1 + bin(copies).count("1")
         p = plan(*op, 8192, 8192, 8192, math_mode=V.MATH_3XTF32, relayout_mode=V.RELAYOUT_OFF)
-        assert p["kind"] == (V.PLAN_TENSOR_CORE if copies == 0 else V.PLAN_TMA)
+        if op in ((0, 0), (0, 1)):
+            assert (p["kind"], p["copies"], p["tc_bk"]) == (V.PLAN_TENSOR_CORE, 0, 1 if op == (0, 1) else 0), (op, p)
+        else:
+            assert p["kind"] == V.PLAN_TMA
     assert plan(0, 0, 1024, 1024, 1024, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA   # too few tiles
     assert plan(0, 0, 8192, 8192, 128, math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA    # K below 256
     p = plan(0, 0, 2048, 2048, 2048, batch=2, strideA=1, strideB=1, math_mode=V.MATH_3XTF32)
-    assert (p["kind"], p["launches"]) == (V.PLAN_TENSOR_CORE, 2)    # one launch per product
+    assert (p["kind"], p["launches"]) == (V.PLAN_TENSOR_CORE, 4)    # one copy and one launch per product
+    p = plan(0, 1, 2048, 2048, 2048, batch=2, strideA=1, strideB=1, math_mode=V.MATH_3XTF32)
+    assert (p["kind"], p["copies"], p["launches"]) == (V.PLAN_TENSOR_CORE, 0, 2)
     p = plan(1, 1, 2048, 2048, 2048, batch=3, strideA=1, strideB=1, math_mode=V.MATH_3XTF32)
-    assert (p["kind"], p["copies"], p["launches"]) == (V.PLAN_TENSOR_CORE, 3, 9)
+    assert (p["kind"], p["copies"], p["launches"]) == (V.PLAN_TENSOR_CORE, 1, 6)
     assert plan(0, 0, 2048, 2048, 2048, batch=257, strideA=1, strideB=1,
                 math_mode=V.MATH_3XTF32)["kind"] == V.PLAN_TMA
     p = plan(1, 1, 8192, 8192, 8192, pinned=V.VARIANT_TC_3XTF32)
