@@ -44,7 +44,7 @@ UNIT = "TFLOP/s"
 # headline command (gpu__time_duration and the DRAM byte counters of every
 # launch of the timed steps); any other source gives traffic = null.
 TRAFFIC_BY_SOURCE = {("992b753e672b188f", "TN", 1): 3.393e9}
-TC_TRAFFIC_BY_SOURCE = {"3f6064e551384a01": 2.534e9}
+TC_TRAFFIC_BY_SOURCE = {}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
 TC_KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tc.cu",

@@ -8,7 +8,10 @@ into the next after an operand copy, a shared operand copied once, a
 transposed-epilogue call on a pinned small tile, ...) are still checked
 element by element, with padding and gap cells bit-unchanged.  A second sweep
 draws M and N of 1000-2100 with K up to 777 on the larger tiles, so that calls
-run complete waves, a stream-K wave and the kernel that adds its parts.
+run complete waves, a stream-K wave and the kernel that adds its parts.  A
+third draws, besides all that, how stream-K parts are added (last CTA, second
+kernel, shared by the CTAs that end in the tile, or automatic) and a forced
+cluster split-K of 2 to 8 CTAs per tile (or none, or automatic).
 """
 import random
 
@@ -94,5 +97,42 @@ def test_random_wave_case(handle, case_id):
     finally:
         sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
         sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
+    p.check(C, bufs)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK, c
+
+
+def draw_split_case(rng):
+    c = draw_case(rng)
+    c.update(M=rng.choice([64, 130, 300, 513, 700, 1000, 1100, 1536]), N=rng.choice([65, 257, 520, 1000, 1300]),
+             K=rng.choice([33, 100, 270, 513, 777, 1100]), math=V.MATH_FP32,
+             pin=rng.choice([V.VARIANT_AUTO, V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128,
+                             V.VARIANT_TMA_64x64]),
+             sums=rng.choice([V.SK_SUMS_AUTO, V.SK_SUMS_LAST, V.SK_SUMS_DEFERRED, V.SK_SUMS_SHARED]),
+             ksplit=rng.choice([0, 0, 1, 2, 3, 4, 5, 6, 7, 8]), mult4=True)
+    return c
+
+
+@pytest.mark.parametrize("case_id", range(120))
+def test_random_split_case(handle, case_id):
+    c = draw_split_case(random.Random(90000 + case_id))
+    p = ExProblem(c["tA"], c["tB"], c["M"], c["N"], c["K"], batch=c["batch"], seed=c["seed"], alpha=c["alpha"],
+                  beta=c["beta"], pad=(4, 8, 4), gap=(8, 4, 12), mult4=True)
+    if c["shared"] == "A":
+        p.sA = 0
+        p.A = p.A[:p.ar * p.lda + 8].copy()
+    elif c["shared"] == "B":
+        p.sB = 0
+        p.B = p.B[:p.br * p.ldb + 4].copy()
+    sgemm.sgemm_set_variant(handle, c["pin"])
+    sgemm.sgemm_set_relayout(handle, c["mode"])
+    sgemm.sgemm_debug_set_stream_k_sums(handle, c["sums"])
+    sgemm.sgemm_debug_set_cluster_split(handle, c["ksplit"])
+    try:
+        C, bufs = p.run(handle)
+    finally:
+        sgemm.sgemm_set_variant(handle, V.VARIANT_AUTO)
+        sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
+        sgemm.sgemm_debug_set_stream_k_sums(handle, V.SK_SUMS_AUTO)
+        sgemm.sgemm_debug_set_cluster_split(handle, 0)
     p.check(C, bufs)
     assert sgemm.sgemm_get_device_status(handle) == V.OK, c
