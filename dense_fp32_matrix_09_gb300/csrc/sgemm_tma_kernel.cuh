@@ -504,6 +504,11 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the tensor maps' descriptors are fetched while the CTA sets up
+    if (tid == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+    }
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
     const int tiles_per = tiles_m * tiles_n;  // tiles of one batch entry
     const int kt = (g.K + C::BK - 1) / C::BK;
@@ -540,18 +545,6 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int bat = tile0 / tiles_per;
     const bool a3 = g.batch > 1 && g.sA != 0, b3 = g.batch > 1 && g.sB != 0;
     float *Cb = g.C + static_cast<long long>(bat) * g.sC;
-
-    if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], C::kConsumers);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    // cluster split-K with slots apart: this CTA is running (peers wait for
-    // that before their first push into its shared memory)
-    if constexpr (CLUSTER && cluster_slots_apart<C, OP>()) cluster_arrive_relaxed();
 
     // Thread 0 issues the TMA loads of the CTA's t-th iteration into stage t % STAGES.
     int m0w, n0w;  // the first segment's tile
@@ -591,12 +584,22 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         if (b3) tma_load_3d(sB + s * C::kBBytes, &tmB, &full[s], bx, by, bt);
         else tma_load_2d(sB + s * C::kBBytes, &tmB, &full[s], bx, by);
     };
+    // Thread 0 sets up the stage barriers and issues the first stages' loads
+    // before the CTA-wide barrier, so their latency overlaps the other
+    // threads' set-up; nobody else touches the barriers before that barrier.
     int issued = 0;
     if (tid == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], C::kConsumers);
+        }
+        fence_barrier_init();
         for (; issued < min(n_iter, C::STAGES); ++issued) issue(issued);
     }
+    __syncthreads();
+    // cluster split-K with slots apart: this CTA is running (peers wait for
+    // that before their first push into its shared memory)
+    if constexpr (CLUSTER && cluster_slots_apart<C, OP>()) cluster_arrive_relaxed();
 
     // ---------------------------------------------------- consumer warps
     const int wm = warp / C::WARPS_N, wn = warp % C::WARPS_N;
