@@ -174,4 +174,44 @@ __device__ __forceinline__ void st_dsmem_f4(uint32_t addr, float4 v) {
                  ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may be scheduled once every CTA of the kernel before it has
+// signalled (or exited); it must wait for that kernel's completion and the
+// visibility of its writes (griddepcontrol.wait) before touching any memory
+// that kernel reads or writes.  Both are no-ops without such a launch.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Host side: launch `kernel` as a programmatic dependent of the work before it
+// on `stream` (and, with cluster_x > 1, as clusters of cluster_x CTAs along
+// x).  A rejected launch leaves no error behind for the next call to report.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, int smem, cudaStream_t stream,
+                             int cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e;
+}
+
 }  // namespace sg

@@ -151,6 +151,11 @@ __global__ void __launch_bounds__(256) transpose_kernel(const float *__restrict_
                                                         long long lds, long long sstride, float *__restrict__ dst,
                                                         long long ldd, long long dstride) {
     __shared__ float t[kTrTile][kTrTile + 1];
+    // launched as a programmatic dependent of the work before it: the next
+    // kernel may be scheduled as these blocks leave, and this one waits for
+    // the kernel before it before reading its operand
+    griddep_launch_dependents();
+    griddep_wait();
     src += blockIdx.y * sstride;
     dst += blockIdx.y * dstride;
     const int tiles_c = (cols + kTrTile - 1) / kTrTile;
@@ -257,9 +262,9 @@ cudaError_t launch_transpose(const float *src, int rows, int cols, int lds, floa
                              cudaStream_t stream, int batch, long long sstride, long long dstride) {
     const long long tiles = 1LL * ((rows + kTrTile - 1) / kTrTile) * ((cols + kTrTile - 1) / kTrTile);
     if (tiles > 0x7fffffffLL || batch < 1 || batch > 65535) return cudaErrorInvalidConfiguration;
-    transpose_kernel<<<dim3(static_cast<unsigned>(tiles), batch), 256, 0, stream>>>(src, rows, cols, lds, sstride,
-                                                                                   dst, ldd, dstride);
-    return cudaGetLastError();
+    return launch_dependent(transpose_kernel, dim3(static_cast<unsigned>(tiles), batch), dim3(256), 0, stream, 1, src,
+                            rows, cols, static_cast<long long>(lds), sstride, dst, static_cast<long long>(ldd),
+                            dstride);
 }
 
 long long launch_fma_probe(float *sink, int ctas, int iters, cudaStream_t stream) {

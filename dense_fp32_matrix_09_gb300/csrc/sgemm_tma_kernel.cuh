@@ -337,15 +337,6 @@ __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, 
     }
 }
 
-// Programmatic dependent launch: a kernel launched with programmatic stream
-// serialization may be scheduled once every CTA of the kernel before it has
-// signalled (or exited); it must wait for that kernel's completion and the
-// visibility of its writes before touching them.
-__device__ __forceinline__ void griddep_launch_dependents() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Stream-K: the CTAs of one tile are the consecutive q with iterations in
 // [tl*kt, (tl+1)*kt) of the T = stream-K tiles x kt iterations, where CTA q
 // holds [floor(q*T/G), floor((q+1)*T/G)).  First such q: the largest with
@@ -490,9 +481,12 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     constexpr bool SPLIT = MODE == kModeStreamK;
     constexpr bool CLUSTER = MODE == kModeCluster;
     extern __shared__ uint8_t smem_raw[];
-    // a stream-K grid lets the kernel that adds its parts be scheduled now: its
-    // blocks take SM room as this grid's CTAs leave and wait for its completion
-    if constexpr (SPLIT) griddep_launch_dependents();
+    // Every launch of this kernel is a programmatic dependent of the work before
+    // it on the stream: the next kernel (the stream-K wave, the kernel adding
+    // its parts, the next call) may be scheduled now -- its CTAs take SM room as
+    // this grid's CTAs leave -- and this one waits below, before its first
+    // memory access, for the kernel before it.
+    griddep_launch_dependents();
     // 1024-byte alignment: the 128-byte swizzle pattern repeats every 1024 B.
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -594,9 +588,11 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(&empty[s], C::kConsumers);
         }
         fence_barrier_init();
+        griddep_wait();  // the kernel before this one has finished and its writes are visible
         for (; issued < min(n_iter, C::STAGES); ++issued) issue(issued);
     }
     __syncthreads();
+    griddep_wait();
     // cluster split-K with slots apart: this CTA is running (peers wait for
     // that before their first push into its shared memory)
     if constexpr (CLUSTER && cluster_slots_apart<C, OP>()) cluster_arrive_relaxed();
@@ -844,7 +840,8 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 template <class C, int OP>
 __global__ void __launch_bounds__(C::kConsumers)
 sk_finish_kernel(const GemmArgs g, const SplitK sk, const int group_m) {
-    griddep_wait();  // the stream-K grid has completed and its parts are visible
+    griddep_launch_dependents();  // the next kernel on the stream may be scheduled as these blocks leave
+    griddep_wait();               // the stream-K grid has completed and its parts are visible
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
     const int tiles_per = tiles_m * tiles_n;
     const int kt = (g.K + C::BK - 1) / C::BK;
@@ -961,54 +958,40 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         1LL * ((g.M + C::BM - 1) / C::BM) * ((g.N + C::BN - 1) / C::BN) * g.batch;
     const int smem = smem_override > 0 ? smem_override : smem_bytes<C, OP>();
     if (g.batch < 1 || g.batch > 65535 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
+    // every launch a programmatic dependent of the work before it on the stream
+    const int group = kGroupM;
     if (sk.sk_ctas <= 0 && sk.ksplit > 1) {
         // cluster split-K: ksplit CTAs per tile, one cluster each
         if (sk.ksplit > 8 || tiles * sk.ksplit > 0x7fffffffLL) return cudaErrorInvalidValue;
-        cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(static_cast<unsigned>(tiles * sk.ksplit));
-        cfg.blockDim = dim3(C::kThreads);
-        cfg.dynamicSmemBytes = smem_override > 0 ? smem_override : cluster_smem_bytes<C, OP>();
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = sk.ksplit;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, sgemm_tma_kernel<C, kModeCluster, OP>, tmA, tmB, g, sk,
-                                                 static_cast<int>(kGroupM));
-        if (e != cudaSuccess) {
-            (void)cudaGetLastError();  // a rejected launch leaves nothing for the next call to report
-            return e;
-        }
+        const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeCluster, OP>,
+                                               dim3(static_cast<unsigned>(tiles * sk.ksplit)), dim3(C::kThreads),
+                                               smem_override > 0 ? smem_override : cluster_smem_bytes<C, OP>(), stream,
+                                               sk.ksplit, tmA, tmB, g, sk, group);
+        if (e != cudaSuccess) return e;
     } else if (sk.sk_ctas <= 0) {
-        sgemm_tma_kernel<C, kModeWhole, OP><<<static_cast<unsigned>(tiles), C::kThreads, smem, stream>>>(tmA, tmB, g, sk,
-                                                                                                   kGroupM);
+        const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeWhole, OP>, dim3(static_cast<unsigned>(tiles)),
+                                               dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, sk, group);
+        if (e != cudaSuccess) return e;
     } else {
         // the complete waves with the whole-tile kernel, then the stream-K CTAs
-        if (sk.dp_tiles > 0)
-            sgemm_tma_kernel<C, kModeWhole, OP><<<sk.dp_tiles, C::kThreads, smem, stream>>>(tmA, tmB, g, sk, kGroupM);
+        if (sk.dp_tiles > 0) {
+            const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeWhole, OP>, dim3(sk.dp_tiles),
+                                                   dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, sk, group);
+            if (e != cudaSuccess) return e;
+        }
         SplitK s2 = sk;
         s2.cta0 = sk.dp_tiles;
-        sgemm_tma_kernel<C, kModeStreamK, OP><<<sk.sk_ctas, C::kThreads, smem, stream>>>(tmA, tmB, g, s2, kGroupM);
+        {
+            const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeStreamK, OP>, dim3(sk.sk_ctas),
+                                                   dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, s2, group);
+            if (e != cudaSuccess) return e;
+        }
         if (sk.fixup == kFixupDeferred) {
             // a programmatic dependent of the stream-K grid (it waits for it on the device)
-            cudaLaunchConfig_t cfg{};
-            cfg.gridDim = dim3(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles));
-            cfg.blockDim = dim3(C::kConsumers);
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            const cudaError_t e = cudaLaunchKernelEx(&cfg, sk_finish_kernel<C, OP>, g, sk, static_cast<int>(kGroupM));
-            if (e != cudaSuccess) {
-                (void)cudaGetLastError();
-                return e;
-            }
+            const cudaError_t e = launch_dependent(sk_finish_kernel<C, OP>,
+                                                   dim3(C::TM * C::TN4, static_cast<unsigned>(tiles - sk.dp_tiles)),
+                                                   dim3(C::kConsumers), 0, stream, 1, g, sk, group);
+            if (e != cudaSuccess) return e;
         }
     }
     return cudaGetLastError();
