@@ -40,10 +40,10 @@ UNIT = "TFLOP/s"
 # DRAM bytes (read + write) of one headline call at 8192^3 -- every launch of
 # the call: the transposed copy, the complete waves and the stream-K wave --
 # keyed by (SHA-256 of the SIMT kernel source without comments, layout the
-# kernel ran on, re-layout bits), from a one-pass ncu launch list of the
-# headline command (gpu__time_duration and the DRAM byte counters of every
-# launch of the timed steps); any other source gives traffic = null.
-TRAFFIC_BY_SOURCE = {("992b753e672b188f", "TN", 1): 3.393e9}
+# kernel ran on, re-layout bits), from an ncu launch list of the headline
+# command (gpu__time_duration and the DRAM byte counters of the library's
+# launches in the timed steps); any other source gives traffic = null.
+TRAFFIC_BY_SOURCE = {("b8e8c25b2e47ae2a", "TN", 1): 3.347e9}
 TC_TRAFFIC_BY_SOURCE = {}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh"]
