@@ -63,6 +63,14 @@ struct SplitK {
     // hold the stream-K indices to: partial tiles the workspace holds, counters.
     int ws_tiles = 0;
     int n_counters = 0;
+    // Placement (0: none): SM count, shared memory of one SM and the part of
+    // it the system reserves per CTA, in bytes.  A launch whose grid is one
+    // under-filled wave of a tile that fits several CTAs on an SM asks for
+    // enough dynamic shared memory that no SM can hold more than
+    // ceil(grid / sms) of its CTAs (spread_smem in the kernel's launch code).
+    int sms = 0;
+    int sm_smem = 0;
+    int smem_reserved = 0;
 };
 
 // How the parts of a split tile are added (always in ascending k order):

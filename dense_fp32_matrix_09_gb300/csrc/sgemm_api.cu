@@ -74,6 +74,8 @@ constexpr int kPlanCache = 8, kMapCache = 8;
 struct sgemm_ctx {
     int device;
     int num_sms;
+    int sm_smem;        // shared memory of one SM, bytes
+    int smem_reserved;  // shared memory the system reserves per CTA, bytes
     int *d_status;
     float *d_ws;
     size_t ws_floats;
@@ -747,6 +749,8 @@ int sgemm_create(sgemm_handle_t *out) {
     if (!h) return SGEMM_ERR_CUDA;
     h->device = dev;
     h->num_sms = prop.multiProcessorCount;
+    h->sm_smem = static_cast<int>(prop.sharedMemPerMultiprocessor);
+    h->smem_reserved = static_cast<int>(prop.reservedSharedMemPerBlock);
     h->ws_floats = kWorkspaceBytes / sizeof(float);
     h->n_counters = kCounters;
     h->last_variant = -1;
@@ -1062,6 +1066,9 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         sk.ws_tiles = static_cast<int>(h->ws_floats / (static_cast<size_t>(sh.bm) * sh.bn));
         if (h->ws_tiles_limit > 0) sk.ws_tiles = std::min(sk.ws_tiles, h->ws_tiles_limit);
         sk.n_counters = h->n_counters;
+        sk.sms = h->num_sms;
+        sk.sm_smem = h->sm_smem;
+        sk.smem_reserved = h->smem_reserved;
         CUtensorMap tmA, tmB;
         const bool a_ok = p.op == sg::kTmaOpTN
             ? cached_encode(h, &tmA, k.A, K, k.M, k.lda, batch, k.sA, sh.bm, sh.bk, CU_TENSOR_MAP_SWIZZLE_NONE)

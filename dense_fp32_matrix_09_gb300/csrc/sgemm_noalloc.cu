@@ -174,6 +174,10 @@ extern "C" int sgemm_run_noalloc(int M, int N, int K, float alpha, const float *
                               : sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
     sk.ws_tiles = kMaxPartialTiles;  // for the device-side index checks of a checked build
     sk.n_counters = kMaxTiles;
+    sk.sms = sms;
+    if (cudaDeviceGetAttribute(&sk.sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sk.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess)
+        return SGEMM_ERR_CUDA;
 
     CUtensorMap tmA, tmB;
     if (!encode(&tmA, A, M, K, lda, sh.bk, sh.bm, CU_TENSOR_MAP_SWIZZLE_128B) ||

@@ -77,6 +77,7 @@
 // it in the status word and returns without writing C.
 #pragma once
 
+#include <algorithm>
 #include <cstdio>
 #include <type_traits>
 
@@ -902,16 +903,37 @@ constexpr int cluster_smem_bytes() {
     return need > kClusterSmemFloor ? need : kClusterSmemFloor;
 }
 
+// Dynamic shared memory for a launch of `grid` CTAs of a tile that fits
+// MIN_CTAS CTAs on an SM.  Every launch is a programmatic dependent of the
+// work before it, so its CTAs may be placed while the grid before it is still
+// leaving, onto whichever SMs have room first: a one-wave grid of fewer CTAs
+// than slots could then hold two or three CTAs on some SMs and none on others
+// (measured: 144 CTAs of 128 x 128 at 1536^3 took 230-240 us back to back
+// instead of 125).  When the grid is such a wave, ask for enough shared
+// memory that r + 1 CTAs (each with the bytes the system reserves) exceed an
+// SM's shared memory, r = ceil(grid / SMs): no SM then holds more than r,
+// the placement the planner's estimate assumes.
+template <class C>
+int spread_smem(long long grid, int smem, const SplitK &sk) {
+    if (C::MIN_CTAS <= 1 || sk.sms <= 0 || sk.sm_smem <= 0 || grid <= 0) return smem;
+    const long long r = (grid + sk.sms - 1) / sk.sms;
+    if (r >= C::MIN_CTAS) return smem;
+    const long long need = sk.sm_smem / (r + 1) - sk.smem_reserved + 1;  // (r+1)(need+reserved) > sm_smem
+    const long long rounded = (need + 127) / 128 * 128;
+    return static_cast<int>(std::min<long long>(std::max<long long>(smem, rounded), kMaxDynSmem));
+}
+
 template <class C, int OP>
 cudaError_t prepare_one() {
+    // the whole-tile and stream-K kernels may ask for more than they use (spread_smem)
     cudaError_t e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeWhole, OP>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<C, OP>());
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeCluster, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  cluster_smem_bytes<C, OP>());
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeStreamK, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes<C, OP>());
+                                kMaxDynSmem);
 }
 
 // Clusters of `csize` CTAs of the cluster split-K kernel that can be resident
@@ -969,8 +991,9 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
                                                sk.ksplit, tmA, tmB, g, sk, group);
         if (e != cudaSuccess) return e;
     } else if (sk.sk_ctas <= 0) {
+        const int s = smem_override > 0 ? smem : spread_smem<C>(tiles, smem, sk);
         const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeWhole, OP>, dim3(static_cast<unsigned>(tiles)),
-                                               dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, sk, group);
+                                               dim3(C::kThreads), s, stream, 1, tmA, tmB, g, sk, group);
         if (e != cudaSuccess) return e;
     } else {
         // the complete waves with the whole-tile kernel, then the stream-K CTAs
@@ -982,8 +1005,9 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         SplitK s2 = sk;
         s2.cta0 = sk.dp_tiles;
         {
+            const int s = smem_override > 0 ? smem : spread_smem<C>(sk.sk_ctas, smem, sk);
             const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeStreamK, OP>, dim3(sk.sk_ctas),
-                                                   dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, s2, group);
+                                                   dim3(C::kThreads), s, stream, 1, tmA, tmB, g, s2, group);
             if (e != cudaSuccess) return e;
         }
         if (sk.fixup == kFixupDeferred) {
