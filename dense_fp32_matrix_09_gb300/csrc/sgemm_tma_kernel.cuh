@@ -105,7 +105,7 @@ struct Cfg {
     static constexpr int kABytes = BM * BK * 4;  // one stage of A: BM rows of 128 B
     static constexpr int kBBytes = BK * BN * 4;  // one stage of B: BK rows of BN floats
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 16 + 1024;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 32 + 1024;
     static_assert(LANES_M * LANES_N == 32, "warp tile must map onto 32 lanes");
     static_assert(WTM % TM == 0 && WTN % TN == 0 && TN % 4 == 0, "bad thread tile");
     static_assert(BM % 8 == 0 && (kABytes % 1024) == 0, "A stages must stay 1024-byte aligned");
@@ -338,12 +338,21 @@ __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, 
     }
 }
 
+// floor(x / d) for x >= 0 and 0 < d: a 32-bit division whenever x and d fit
+// in 32 bits (every problem short of K in the millions), which costs a small
+// fraction of the 64-bit division routine at the start of each CTA.
+__device__ __forceinline__ long long div_floor(long long x, long long d) {
+    if (((static_cast<unsigned long long>(x) | static_cast<unsigned long long>(d)) >> 32) == 0)
+        return static_cast<unsigned>(x) / static_cast<unsigned>(d);
+    return x / d;
+}
+
 // Stream-K: the CTAs of one tile are the consecutive q with iterations in
 // [tl*kt, (tl+1)*kt) of the T = stream-K tiles x kt iterations, where CTA q
 // holds [floor(q*T/G), floor((q+1)*T/G)).  First such q: the largest with
 // floor(q*T/G) <= x, i.e. ceil((x+1)*G/T) - 1 for x = tl*kt.
 __device__ __forceinline__ int sk_first_cta(long long x, long long T, int G) {
-    return static_cast<int>(((x + 1) * G + T - 1) / T) - 1;
+    return static_cast<int>(div_floor((x + 1) * G + T - 1, T)) - 1;
 }
 
 // Add the parts of split tile tl (slots tl + q_first .. tl + q_last) for
@@ -460,7 +469,7 @@ __host__ __device__ constexpr int cluster_slot_groups(int groups) {
 constexpr int kMaxDynSmem = 227 * 1024;
 template <class C, int OP>
 __host__ __device__ constexpr int cluster_slots_offset() {
-    return (C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0) + 2 * C::STAGES * 8 + 16 + 127) / 128 * 128;
+    return (C::STAGES * C::kStageBytes + (OP == kOpNT ? 2 * C::kBBytes : 0) + 2 * C::STAGES * 8 + 32 + 127) / 128 * 128;
 }
 template <class C>
 __host__ __device__ constexpr int cluster_slot_bytes() {
@@ -496,7 +505,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     uint8_t *sBt = smem + C::STAGES * C::kStageBytes;    // NT: 2 x kBBytes transpose buffers
     uint64_t *full = reinterpret_cast<uint64_t *>(sBt + (OP == kOpNT ? 2 * C::kBBytes : 0));
     uint64_t *empty = full + C::STAGES;
-    int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);
+    int *s_flag = reinterpret_cast<int *>(empty + C::STAGES);  // [0..1]: per segment; [2..4]: second tile
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // the tensor maps' descriptors are fetched while the CTA sets up
@@ -529,8 +538,8 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (SPLIT && cta >= sk.dp_tiles) {
         q = cta - sk.dp_tiles;
         T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
-        const long long b = q * T / sk.sk_ctas, e = (q + 1) * T / sk.sk_ctas;
-        const int tl = static_cast<int>(b / kt);
+        const long long b = div_floor(q * T, sk.sk_ctas), e = div_floor((q + 1) * T, sk.sk_ctas);
+        const int tl = static_cast<int>(div_floor(b, kt));
         tile0 = sk.dp_tiles + tl;
         k00 = static_cast<int>(b - static_cast<long long>(tl) * kt);
         n_iter = static_cast<int>(e - b);  // >= 1: the host keeps G <= T
@@ -549,16 +558,23 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         m0w = tm * C::BM;
         n0w = tn * C::BN;
     }
+    // stream-K: thread 0 keeps the second segment's tile (the next one), if
+    // any, in shared memory for its loads (s_flag[2..4]: row, column, batch entry)
+    if (SPLIT && n_iter > n0it && tid == 0) {
+        int tm, tn;
+        tile_coords((tile0 + 1) % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
+        s_flag[2] = tm * C::BM;
+        s_flag[3] = tn * C::BN;
+        s_flag[4] = (tile0 + 1) / tiles_per;
+    }
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
         int m0 = m0w, n0 = n0w, kc = (k00 + t) * C::BK, bt = bat;
         if (SPLIT && t >= n0it) {  // second segment: the next tile from k = 0
-            int tm, tn;
-            tile_coords((tile0 + 1) % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
-            m0 = tm * C::BM;
-            n0 = tn * C::BN;
+            m0 = s_flag[2];
+            n0 = s_flag[3];
             kc = (t - n0it) * C::BK;
-            bt = (tile0 + 1) / tiles_per;
+            bt = s_flag[4];
         }
         mbar_arrive_expect_tx(&full[s], C::kStageBytes);
         int ax = OP == kOpTN ? m0 : kc, ay = OP == kOpTN ? kc : m0;
@@ -805,7 +821,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     // adder counts itself after its wait; the last one resets
                     // the counter for the next call.
                     const int n_parts = q_last - q_first + 1;
-                    const long long e_last = (static_cast<long long>(q_last) + 1) * T / sk.sk_ctas;
+                    const long long e_last = div_floor((static_cast<long long>(q_last) + 1) * T, sk.sk_ctas);
                     const int n_add = q_last - q_first + (e_last <= static_cast<long long>(tl + 1) * kt ? 1 : 0);
                     bool bad = false;
                     if (tid == 0) {
