@@ -42,11 +42,11 @@ struct CallPlan {
 
 // Everything a plan depends on besides the handle's fixed device facts.
 struct PlanKey {
-    int transA, transB, M, N, K, batch, a_shared, b_shared, tma_ok, pinned, relayout_mode, math_mode, sk_sums,
+    int transA, transB, M, N, K, batch, a_shared, b_shared, aligned, pinned, relayout_mode, math_mode, sk_sums,
         ksplit_pin;
     bool operator==(const PlanKey &o) const {
         return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
-               a_shared == o.a_shared && b_shared == o.b_shared && tma_ok == o.tma_ok && pinned == o.pinned &&
+               a_shared == o.a_shared && b_shared == o.b_shared && aligned == o.aligned && pinned == o.pinned &&
                relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_sums == o.sk_sums &&
                ksplit_pin == o.ksplit_pin;
     }
@@ -482,17 +482,35 @@ int op_after(int transA, int transB, int r, int M, int N, int *kM, int *kN) {
     return ta ? (tb ? sg::kTmaOpNN : sg::kTmaOpTN) : (tb ? sg::kTmaOpNT : sg::kTmaOpNN);
 }
 
-// Variant and re-layout for a TMA-eligible FP32 call (a pinned TMA variant
-// keeps its tile).  Candidates: the operands as stored, and each combination
-// of transposed copies of A stored M x K and of B stored N x K; the one that
+// Floats of the transposed copy of A (stored M x K, or K x M with transA)
+// and of B (stored K x N, or N x K with transB): the copy's rows padded to
+// 32 floats.
+unsigned long long a_copy_floats(int transA, int M, int K) {
+    return transA ? static_cast<unsigned long long>(M) * ((K + 31ULL) / 32 * 32)
+                  : static_cast<unsigned long long>(K) * ((M + 31ULL) / 32 * 32);
+}
+unsigned long long b_copy_floats(int transB, int N, int K) {
+    return transB ? static_cast<unsigned long long>(K) * ((N + 31ULL) / 32 * 32)
+                  : static_cast<unsigned long long>(N) * ((K + 31ULL) / 32 * 32);
+}
+
+// Variant and re-layout for an FP32 SIMT call (a pinned TMA variant keeps
+// its tile).  Candidates: the operands as stored, and each combination of
+// transposed copies of A stored M x K and of B stored N x K; the one that
 // reaches the TN layout -- the fastest main loop on GB300 -- is NN: A; NT: A
-// and B; A^T B^T: B.  Each candidate costs variant_cost of its layout plus
-// transpose_cost of each copy (one matrix for an operand shared by the whole
-// batch, stride 0, else `batch`), and needs its copies to fit in the
-// workspace; a re-layout must save 1 %.  SGEMM_RELAYOUT_ALWAYS takes the TN
-// candidate whenever it fits; SGEMM_RELAYOUT_OFF only the stored layout.
+// and B; A^T B^T: B.  An operand the TMA cannot read as stored (`need`, bit
+// 0 A, bit 1 B: not 16-byte aligned, or a leading dimension or batch stride
+// not a multiple of 4) must be copied, in whichever layout it is stored: the
+// copy is aligned, and the stored layout is then not a candidate.  Each
+// candidate costs variant_cost of its layout plus transpose_cost of each
+// copy (one matrix for an operand shared by the whole batch, stride 0, else
+// `batch`), and needs its copies to fit in the workspace; a re-layout must
+// save 1 %.  SGEMM_RELAYOUT_ALWAYS takes the TN candidate whenever it fits
+// (and holds the copies `need` asks for), else the cheapest;
+// SGEMM_RELAYOUT_OFF only the stored layout.  variant < 0: no candidate
+// (an operand must be copied and cannot be).  *cost: the estimate taken.
 Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
-                   long long strideB, int pinned) {
+                   long long strideB, int pinned, int need, double *cost) {
     auto best_variant = [&](int op, int kM, int kN, double *cost) {
         if (pinned != SGEMM_VARIANT_AUTO) {
             sg::SplitK plan;
@@ -506,38 +524,60 @@ Fp32Plan plan_fp32(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     };
     const int nA = strideA == 0 ? 1 : batch, nB = strideB == 0 ? 1 : batch;
     int kM = 0, kN = 0;
-    double best_cost;
-    const int op0 = op_after(transA, transB, 0, M, N, &kM, &kN);  // sets kM, kN before they are read
-    Fp32Plan best{best_variant(op0, kM, kN, &best_cost), 0};
+    double best_cost = 0;
+    Fp32Plan best{-1, 0};
+    if (need == 0) {
+        const int op0 = op_after(transA, transB, 0, M, N, &kM, &kN);  // sets kM, kN before they are read
+        best = Fp32Plan{best_variant(op0, kM, kN, &best_cost), 0};
+    }
+    *cost = best_cost;
     if (h->relayout_mode == SGEMM_RELAYOUT_OFF || h->rl_floats == 0) return best;
     const int tn_r = (transA ? 0 : 1) | (transB ? 2 : 0);  // transposes that reach TN
+    // RELAYOUT_ALWAYS: only the TN candidate, unless it lacks a copy `need` asks for
+    const bool only_tn = h->relayout_mode == SGEMM_RELAYOUT_ALWAYS && (tn_r & need) == need;
     for (int r : {1, 2, 3}) {
-        if ((r & 1) && transA) continue;  // only A stored M x K and B stored N x K are transposed
-        if ((r & 2) && !transB) continue;
+        if ((r & need) != need) continue;                 // the operands the TMA cannot read are copied
+        if ((r & 1) && transA && !(need & 1)) continue;  // else only A stored M x K and B stored
+        if ((r & 2) && !transB && !(need & 2)) continue;  // N x K are transposed (towards TN)
         const bool to_tn = r == tn_r;
-        if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS && !to_tn) continue;
-        const unsigned long long need =
-            ((r & 1) ? static_cast<unsigned long long>(nA) * K * ((M + 31ULL) / 32 * 32) : 0) +
-            ((r & 2) ? static_cast<unsigned long long>(nB) * K * ((N + 31ULL) / 32 * 32) : 0);
-        if (need > h->rl_floats) continue;
+        if (only_tn && !to_tn) continue;
+        const unsigned long long floats = ((r & 1) ? nA * a_copy_floats(transA, M, K) : 0) +
+                                          ((r & 2) ? nB * b_copy_floats(transB, N, K) : 0);
+        if (floats > h->rl_floats) continue;
         double c;
         const int op_r = op_after(transA, transB, r, M, N, &kM, &kN);
         const int v = best_variant(op_r, kM, kN, &c);
         if (r & 1) c += transpose_cost(M, K, nA);
         if (r & 2) c += transpose_cost(N, K, nB);
-        if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || c < best_cost * 0.99) {
+        if (only_tn || best.variant < 0 || c < best_cost * 0.99) {
             best_cost = c;
             best = Fp32Plan{v, r};
-            if (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS) break;
+            if (only_tn) break;
         }
     }
+    *cost = best_cost;
     return best;
+}
+
+// Estimated time of the generic kernel (any alignment) per call, in the
+// units of variant_cost, fitted to back-to-back timings on GB300 (64 x 64
+// tiles; 12.3 us at 70 x 90 x 50, 34.8 at 512^3, 43.1 for 2 x 640 x 520 x
+// 392, 119 on 1000 x 1500 x 777 with lda = 777, 634 at 2048^3, 5100 at
+// 4096^3; within about 15 %): about 9 us of fixed cost, then 0.05 us per K
+// for each CTA an SM holds -- the most any SM holds while the grid is
+// resident at once (up to three), the average beyond.
+double generic_cost(const sgemm_ctx *h, int M, int N, int K, int batch) {
+    const double tiles = static_cast<double>(cdiv(M, 64)) * cdiv(N, 64) * batch;
+    const double load = tiles / h->num_sms;
+    return 9.0 + (load <= 3.0 ? std::ceil(load) : load) * K * 0.05;
 }
 
 // The plan of a call (see CallPlan).
 CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
-                   long long strideB, bool tma_ok) {
+                   long long strideB, int aligned) {
     CallPlan p;
+    // operands the TMA cannot read as stored (bit 0 A, bit 1 B)
+    const int need = 3 & ~aligned;
     // The tensor-core kernels read A stored M x K, and B stored K x N or (the
     // pair kernel's faster form) B stored N x K, batch 1; other layouts reach
     // them through transposed copies of their operands in the re-layout
@@ -566,12 +606,16 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
         // 3xTF32 mode: the CTA-pair tensor-core kernel once there are at least
         // about half as many 256 x 256 tiles as CTA pairs and K fills its pipeline
         const long long tc_tiles = 1LL * cdiv(M, 256) * cdiv(N, 256);
-        if (tc_reachable && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 && K >= 256)
+        if (tc_reachable && need == 0 && h->math_mode == SGEMM_MATH_3XTF32 && tc_tiles >= h->num_sms / 4 &&
+            K >= 256)
             variant = SGEMM_VARIANT_TC_3XTF32_PAIR;
     }
-    if (!tma_ok || variant == SGEMM_VARIANT_GENERIC) return p;  // the generic kernel on the stored operands
+    // the generic kernel on the stored operands: pinned, or a batch beyond
+    // the tensor maps' reach
+    if (variant == SGEMM_VARIANT_GENERIC || batch > 65535) return p;
 
     if (variant == SGEMM_VARIANT_TC_3XTF32 || variant == SGEMM_VARIANT_TC_3XTF32_PAIR) {
+        if (need != 0) return p;  // the tensor-core kernels read the operands as stored or as planned above
         if (variant == SGEMM_VARIANT_TC_3XTF32 && !kn_ok) return p;  // the one-CTA kernel reads B stored K x N
         p.kind = kPlanTensorCore;
         p.variant = variant;
@@ -582,7 +626,17 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
     }
 
     // FP32 SIMT kernels: the tile variant and the operands to copy transposed
-    const Fp32Plan fp = plan_fp32(h, transA, transB, M, N, K, batch, strideA, strideB, variant);
+    // (an operand the TMA cannot read is copied, or the call runs on the
+    // generic kernel when that cannot be done or its estimate is lower)
+    double cost = 0;
+    const Fp32Plan fp = plan_fp32(h, transA, transB, M, N, K, batch, strideA, strideB, variant, need, &cost);
+    if (fp.variant < 0) return p;
+    // (cost leaves out the GEMM's own launch, which generic_cost holds, and
+    // on small problems a chain of launches costs about 1 us more per copy
+    // than its estimate; the copies must save a fifth)
+    if (need != 0 && variant == SGEMM_VARIANT_AUTO &&
+        cost + 2.0 + ((fp.relayout & 1) + ((fp.relayout >> 1) & 1)) >= 0.8 * generic_cost(h, M, N, K, batch))
+        return p;
     variant = fp.variant;
     p.copies = fp.relayout;
     p.op = op_after(transA, transB, fp.relayout, M, N, &p.kM, &p.kN);
@@ -608,12 +662,12 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 
 // plan_call through the handle's plan cache.
 CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
-                     long long strideB, bool tma_ok) {
-    const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, tma_ok, h->pinned,
+                     long long strideB, int aligned) {
+    const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, aligned, h->pinned,
                       h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
-    const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
+    const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, aligned);
     h->plan_key[h->plan_next] = key;
     h->plan_val[h->plan_next] = p;
     h->plan_next = (h->plan_next + 1) % kPlanCache;
@@ -943,9 +997,11 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
         return rc;
     }
 
-    const bool tma_ok = aligned16(A) && aligned16(B) && (lda % 4) == 0 && (ldb % 4) == 0 &&
-                        (strideA % 4) == 0 && (strideB % 4) == 0 && batch <= 65535;
-    const CallPlan p = cached_plan(h, transA, transB, M, N, K, batch, strideA, strideB, tma_ok);
+    // operands the TMA can read as stored: 16-byte aligned, leading dimension
+    // and batch stride multiples of 4 floats (bit 0 A, bit 1 B)
+    const int aligned = (aligned16(A) && (lda % 4) == 0 && (strideA % 4) == 0 ? 1 : 0) |
+                        (aligned16(B) && (ldb % 4) == 0 && (strideB % 4) == 0 ? 2 : 0);
+    const CallPlan p = cached_plan(h, transA, transB, M, N, K, batch, strideA, strideB, aligned);
 
     if (p.kind == kPlanTensorCore) {
         // one product at a time (batch entries in order on `stream`, so the
@@ -1005,27 +1061,29 @@ int sgemm_run_ex(sgemm_handle_t h, int transA, int transB, int M, int N, int K, 
     const float *eA = A, *eB = B;
     int elda = lda, eldb = ldb, etA = transA, etB = transB;
     long long esA = strideA, esB = strideB;
-    size_t a_copy_floats = 0;
-    if (p.copies & 1) {  // A (stored M x K) -> A^T stored K x M
-        const int ld = round32(M), n = strideA == 0 ? 1 : batch;
-        const long long per = static_cast<long long>(K) * ld;
-        const int rc = from_cuda(sg::launch_transpose(A, M, K, lda, h->d_rl, ld, stream, n, strideA, per));
+    size_t a_copied = 0;  // floats of A's copy
+    if (p.copies & 1) {  // A stored M x K -> K x M (or, transA, K x M -> M x K)
+        const int rows = transA ? K : M, cols = transA ? M : K;
+        const int ld = round32(rows), n = strideA == 0 ? 1 : batch;
+        const long long per = static_cast<long long>(cols) * ld;
+        const int rc = from_cuda(sg::launch_transpose(A, rows, cols, lda, h->d_rl, ld, stream, n, strideA, per));
         if (rc != SGEMM_OK) return rc;
         eA = h->d_rl;
         elda = ld;
-        etA = 1;
+        etA = transA ^ 1;
         esA = n > 1 ? per : 0;
-        a_copy_floats = static_cast<size_t>(n) * per;
+        a_copied = static_cast<size_t>(n) * per;
     }
-    if (p.copies & 2) {  // B (stored N x K) -> B^T stored K x N, after A^T if both
-        float *dst = h->d_rl + a_copy_floats;
-        const int ld = round32(N), n = strideB == 0 ? 1 : batch;
-        const long long per = static_cast<long long>(K) * ld;
-        const int rc = from_cuda(sg::launch_transpose(B, N, K, ldb, dst, ld, stream, n, strideB, per));
+    if (p.copies & 2) {  // B stored N x K -> K x N (or, !transB, K x N -> N x K), after A's copy if both
+        float *dst = h->d_rl + a_copied;
+        const int rows = transB ? N : K, cols = transB ? K : N;
+        const int ld = round32(rows), n = strideB == 0 ? 1 : batch;
+        const long long per = static_cast<long long>(cols) * ld;
+        const int rc = from_cuda(sg::launch_transpose(B, rows, cols, ldb, dst, ld, stream, n, strideB, per));
         if (rc != SGEMM_OK) return rc;
         eB = dst;
         eldb = ld;
-        etB = 0;
+        etB = transB ^ 1;
         esB = n > 1 ? per : 0;
     }
     const int copy_launches = (p.copies & 1) + ((p.copies >> 1) & 1);
@@ -1252,12 +1310,16 @@ int sgemm_run_host(sgemm_handle_t h, int M, int N, int K, float alpha, const flo
     // the time estimate for the whole segment copies A -- the GEMMs then run
     // with transA = 1, which needs no copy of its own, so the workspace holds
     // only this segment's copy.
+    auto plans_copy_of_a = [&](int nr) {
+        double cost = 0;
+        return (plan_fp32(h, 0, 0, nr, N, K, 1, 0, 0, h->pinned, 0, &cost).relayout & 1) != 0;
+    };
     auto copies_a = [&](int nr) {
         return reads_ab && h->rl_floats > 0 && h->relayout_mode != SGEMM_RELAYOUT_OFF &&
                h->math_mode == SGEMM_MATH_FP32 && aligned16(dA) && aligned16(dB) && (lda % 4) == 0 &&
                (ldb % 4) == 0 && (h->pinned == SGEMM_VARIANT_AUTO || is_tma_variant(h->pinned)) &&
                static_cast<unsigned long long>(K) * ((nr + 31ULL) / 32 * 32) <= h->rl_floats &&
-               (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || (plan_fp32(h, 0, 0, nr, N, K, 1, 0, 0, h->pinned).relayout & 1));
+               (h->relayout_mode == SGEMM_RELAYOUT_ALWAYS || plans_copy_of_a(nr));
     };
     // Column blocks of the first panel follow B's chunks: 1, 1, then 2 chunks
     // at a time (the first blocks start as soon as their chunk lands; later
@@ -1368,14 +1430,14 @@ int sgemm_debug_timeout_probe(sgemm_handle_t h, long long limit_ns, void *stream
 
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,
                      int math_mode, int pinned, int transA, int transB, int M, int N, int K, float alpha,
-                     int batch, long long strideA, long long strideB, int tma_ok, int *out) {
+                     int batch, long long strideA, long long strideB, int aligned, int *out) {
     if (ctas_per_sm == nullptr || out == nullptr) return SGEMM_ERR_NULL;
     if (num_sms < 1 || relayout_floats < 0 || M < 0 || N < 0 || K < 0 || batch < 0 ||
         (transA != 0 && transA != 1) || (transB != 0 && transB != 1) || pinned < 0 ||
         pinned >= SGEMM_VARIANT_COUNT_ || pinned == SGEMM_VARIANT_SCALE ||
         (relayout_mode != SGEMM_RELAYOUT_AUTO && relayout_mode != SGEMM_RELAYOUT_OFF &&
          relayout_mode != SGEMM_RELAYOUT_ALWAYS) ||
-        (math_mode != SGEMM_MATH_FP32 && math_mode != SGEMM_MATH_3XTF32))
+        (math_mode != SGEMM_MATH_FP32 && math_mode != SGEMM_MATH_3XTF32) || aligned < 0 || aligned > 3)
         return SGEMM_ERR_INVALID_VALUE;
     sgemm_ctx c{};  // planning inputs only: no device memory, no CUDA call
     c.num_sms = num_sms;
@@ -1397,7 +1459,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
         return SGEMM_OK;
     }
     if (batch == 1) strideA = strideB = 0;
-    const CallPlan p = plan_call(&c, transA, transB, M, N, K, batch, strideA, strideB, tma_ok != 0);
+    const CallPlan p = plan_call(&c, transA, transB, M, N, K, batch, strideA, strideB, aligned);
     out[0] = p.kind;
     out[1] = p.variant;
     out[2] = p.copies;

@@ -302,12 +302,15 @@ def sgemm_debug_plan(num_sms, ctas_per_sm, transA, transB, M, N, K, *, alpha=1.0
                      strideB=0, tma_ok=True, relayout_floats=2 * 8192 * 8192, relayout_mode=RELAYOUT_AUTO,
                      math_mode=MATH_FP32, pinned=VARIANT_AUTO) -> dict:
     """The plan sgemm_run_ex would follow, computed on the host (no GPU):
-    a dict with the fields of PLAN_FIELDS (see include/sgemm.h)."""
+    a dict with the fields of PLAN_FIELDS (see include/sgemm.h).  ``tma_ok``:
+    True (both operands TMA-readable as stored), False (neither), or the
+    bitmask of those that are (bit 0 A, bit 1 B)."""
+    aligned = 3 if tma_ok is True else 0 if tma_ok is False else int(tma_ok)
     occ = (ctypes.c_int * VARIANT_COUNT)(*ctas_per_sm)
     out = (ctypes.c_int * len(PLAN_FIELDS))()
     _check(lib().sgemm_debug_plan(int(num_sms), occ, int(relayout_floats), int(relayout_mode), int(math_mode),
                                   int(pinned), int(transA), int(transB), int(M), int(N), int(K), float(alpha),
-                                  int(batch), int(strideA), int(strideB), int(bool(tma_ok)), out),
+                                  int(batch), int(strideA), int(strideB), aligned, out),
            "sgemm_debug_plan")
     return dict(zip(PLAN_FIELDS, list(out)))
 

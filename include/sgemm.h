@@ -421,8 +421,13 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
  * handle records (`num_sms`; `ctas_per_sm`, SGEMM_VARIANT_COUNT_ entries
  * indexed by sgemm_variant_t: resident CTAs per SM of each TMA variant) and
  * its settings (re-layout workspace size in floats, re-layout mode, math
- * mode, pinned variant).  `tma_ok` says whether A and B are 16-byte aligned
- * with lda, ldb (and batch strides) multiples of 4.  out[0..11] receives: the
+ * mode, pinned variant).  `aligned` says which operands the TMA can read as
+ * stored: bit 0 A, bit 1 B, each set when the operand is 16-byte aligned with
+ * its leading dimension (and batch stride) a multiple of 4 (3: both, as for
+ * any call on 16-byte aligned buffers with such leading dimensions).  An
+ * operand it cannot read is copied transposed into the re-layout workspace
+ * when the mode allows and the copy fits and pays; else the call runs on the
+ * generic kernel.  out[0..11] receives: the
  * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
  * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
  * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
@@ -437,7 +442,7 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
  * of range. */
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,
                      int math_mode, int pinned, int transA, int transB, int M, int N, int K, float alpha,
-                     int batch, long long strideA, long long strideB, int tma_ok, int *out);
+                     int batch, long long strideA, long long strideB, int aligned, int *out);
 
 /* C <- alpha*A*B + beta*C without allocating anything, for callers that cannot
  * allocate GPU memory (allocator implementations that must not re-enter the

@@ -288,10 +288,26 @@ def test_large_ragged_transposed(handle):
 
 
 def test_unaligned_batch_stride_uses_generic(handle):
+    """A batch stride of A that is not a multiple of 4 floats: the TMA cannot
+    describe A; with the re-layout off the batch runs on the generic kernel."""
     p = ExProblem(0, 0, 40, 48, 36, batch=2, seed=81, pad=(4, 4, 4), gap=(1, 0, 0))
-    C, bufs = p.run(handle)
+    sgemm.sgemm_set_relayout(handle, V.RELAYOUT_OFF)
+    try:
+        C, bufs = p.run(handle)
+    finally:
+        sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
     p.check(C, bufs)
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_GENERIC
+
+
+def test_unaligned_batch_stride_through_copies(handle):
+    """The same with larger matrices: each batch matrix of A is copied
+    transposed (with a padded stride) and the TMA kernels run."""
+    p = ExProblem(0, 0, 600, 520, 400, batch=3, seed=82, pad=(4, 4, 4), gap=(1, 0, 0))
+    C, bufs = p.run(handle)
+    p.check(C, bufs)
+    assert sgemm.sgemm_last_variant(handle)[0] != V.VARIANT_GENERIC
+    assert sgemm.sgemm_last_relayout(handle) & 1
 
 
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)

@@ -179,16 +179,26 @@ def test_beta_zero_output_only_c(handle):
     assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
 
 
+@pytest.mark.parametrize("relayout", [V.RELAYOUT_OFF, V.RELAYOUT_ALWAYS], ids=["relayout_off", "relayout_always"])
 @pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (1, 1, 1)])
-def test_unaligned_pointers(handle, offsets):
-    """Operands that TMA cannot describe take the generic GPU variant; an
-    unaligned C takes the scalar epilogue.  Never a CPU path."""
+def test_unaligned_pointers(handle, offsets, relayout):
+    """Operands that TMA cannot describe as stored take the generic GPU
+    variant with the re-layout off, else (here: forced) a transposed copy in
+    the workspace and the TMA kernels; an unaligned C takes the scalar
+    epilogue.  Never a CPU path."""
     cfg = _cfg(150, 170, 90, 1.5, 0.5)
     prob = inputs.make_problem(cfg)
-    C_gpu, bufs = run_gpu(handle, cfg, prob, offsets=offsets)
+    sgemm.sgemm_set_relayout(handle, relayout)
+    try:
+        C_gpu, bufs = run_gpu(handle, cfg, prob, offsets=offsets)
+    finally:
+        sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
     ran = sgemm.sgemm_last_variant(handle)[0]
-    if offsets[0] or offsets[1]:
+    need = (1 if offsets[0] else 0) | (2 if offsets[1] else 0)
+    if need and relayout == V.RELAYOUT_OFF:
         assert ran == V.VARIANT_GENERIC
+    elif need:
+        assert ran == V.VARIANT_GENERIC or sgemm.sgemm_last_relayout(handle) & need == need
     else:
         assert ran != V.VARIANT_GENERIC
     assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
@@ -196,10 +206,29 @@ def test_unaligned_pointers(handle, offsets):
 
 
 def test_odd_leading_dims_use_generic(handle):
+    """A small problem with odd leading dimensions: the generic kernel's
+    estimate beats copying the operands first."""
     cfg = inputs.GemmConfig("odd_ld", 77, 99, 55, 57, 101, 103, 5, 1.0, 1.0)
     prob = inputs.make_problem(cfg)
     C_gpu, bufs = run_gpu(handle, cfg, prob)
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_GENERIC
+    assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
+    check_untouched(cfg, prob, C_gpu, bufs)
+
+
+@pytest.mark.parametrize("lds", [(777, 1500, 1500), (780, 1501, 1501), (777, 1501, 1503)],
+                         ids=["lda_odd", "ldb_odd", "both_odd"])
+def test_odd_leading_dims_through_copies(handle, lds):
+    """The ragged 1000 x 1500 x 777 shape with unpadded (odd) leading
+    dimensions: the operand the TMA cannot read is copied transposed first
+    and the TMA kernels run (the generic kernel would take about twice as
+    long); every element against the oracle, padding untouched."""
+    cfg = inputs.GemmConfig("odd_ld_large", 1000, 1500, 777, *lds, 9, 1.0, 1.0)
+    prob = inputs.make_problem(cfg)
+    C_gpu, bufs = run_gpu(handle, cfg, prob)
+    ran = sgemm.sgemm_last_variant(handle)[0]
+    need = (1 if lds[0] % 4 else 0) | (2 if lds[1] % 4 else 0)
+    assert ran != V.VARIANT_GENERIC and sgemm.sgemm_last_relayout(handle) & need == need
     assert max_abs_err(cfg, C_gpu, oracle_full(cfg, prob)) <= tolerance(cfg.K)
     check_untouched(cfg, prob, C_gpu, bufs)
 

@@ -183,12 +183,45 @@ def test_batched_bits_match_unbatched(handle, mode):
 
 
 def test_generic_calls_are_not_relaid_out(handle, mode):
-    mode(V.RELAYOUT_ALWAYS)
-    p = ExProblem(0, 0, 100, 136, 72, batch=1, seed=8, pad=(1, 4, 4))  # lda odd: generic
+    mode(V.RELAYOUT_ALWAYS, V.VARIANT_GENERIC)
+    p = ExProblem(0, 0, 100, 136, 72, batch=1, seed=8, pad=(1, 4, 4))  # lda odd
     C, bufs = p.run(handle)
     p.check(C, bufs)
     assert sgemm.sgemm_last_relayout(handle) == 0
     assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_GENERIC
+
+
+@pytest.mark.parametrize("op", [(0, 0), (0, 1), (1, 0), (1, 1)], ids=["NN", "NT", "TN", "TT"])
+@pytest.mark.parametrize("odd", ["A", "B", "AB"])
+def test_misaligned_operand_copied_in_every_layout(handle, mode, op, odd):
+    """An operand with an odd leading dimension is copied transposed into the
+    workspace in whichever layout it is stored (A stored K x M and B stored
+    K x N included, which the re-layout otherwise never copies), and the TMA
+    kernels run; with the re-layout off the generic kernel runs.  Every
+    element against the oracle, padding and batch gaps untouched."""
+    pad = (1 if "A" in odd else 4, 1 if "B" in odd else 8, 4)
+    need = (1 if "A" in odd else 0) | (2 if "B" in odd else 0)
+    for rl in (V.RELAYOUT_AUTO, V.RELAYOUT_OFF):
+        mode(rl)
+        p = ExProblem(*op, 640, 520, 392, batch=2, seed=12, alpha=1.25, beta=-0.5, pad=pad, mult4=True)
+        C, bufs = p.run(handle)
+        p.check(C, bufs)
+        ran = sgemm.sgemm_last_variant(handle)[0]
+        if rl == V.RELAYOUT_OFF:
+            assert ran == V.VARIANT_GENERIC and sgemm.sgemm_last_relayout(handle) == 0
+        else:
+            assert ran != V.VARIANT_GENERIC and sgemm.sgemm_last_relayout(handle) & need == need
+
+
+def test_misaligned_operand_copies_are_bit_exact(handle, mode):
+    """Integer-valued operands: the copy path and the generic kernel give the
+    oracle's exact result."""
+    for rl in (V.RELAYOUT_AUTO, V.RELAYOUT_OFF):
+        mode(rl)
+        for op in ((0, 0), (1, 1)):
+            p = ExProblem(*op, 512, 768, 600, batch=1, seed=13, pad=(1, 1, 3), kind="integers", mult4=True)
+            C, bufs = p.run(handle)
+            p.check(C, bufs, exact=True)
 
 
 @pytest.mark.parametrize("K,copied", [(8192, 1), (8200, 0)])

@@ -40,10 +40,15 @@ def plan(tA, tB, M, N, K, **kw):
 
 
 def copies_need(tA, tB, M, N, K, copies, batch=1, strideA=1, strideB=1):
+    """Floats of the transposed copies: A stored M x K -> K x ceil32(M) rows
+    (stored K x M -> M x ceil32(K)), B stored N x K -> K x ceil32(N) (stored
+    K x N -> N x ceil32(K)), one per batch matrix unless shared."""
     r32 = lambda x: (x + 31) // 32 * 32
     nA = 1 if (batch == 1 or strideA == 0) else batch
     nB = 1 if (batch == 1 or strideB == 0) else batch
-    return (nA * K * r32(M) if copies & 1 else 0) + (nB * K * r32(N) if copies & 2 else 0)
+    a = M * r32(K) if tA else K * r32(M)
+    b = K * r32(N) if tB else N * r32(K)
+    return (nA * a if copies & 1 else 0) + (nB * b if copies & 2 else 0)
 
 
 def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout_floats=CAPACITY):
@@ -130,10 +135,55 @@ def test_plan_kinds():
     p = plan(0, 0, 64, 64, 0)
     assert (p["kind"], p["variant"]) == (V.PLAN_SCALE, V.VARIANT_SCALE)
     assert plan(0, 0, 64, 64, 64, alpha=0.0)["kind"] == V.PLAN_SCALE
-    p = plan(0, 0, 4096, 4096, 4096, tma_ok=False)
+    p = plan(0, 0, 4096, 4096, 4096, tma_ok=False, relayout_mode=V.RELAYOUT_OFF)
     assert (p["kind"], p["variant"], p["copies"], p["launches"]) == (V.PLAN_GENERIC, V.VARIANT_GENERIC, 0, 1)
     p = plan(0, 0, 4096, 4096, 4096, pinned=V.VARIANT_GENERIC)
     assert (p["kind"], p["copies"]) == (V.PLAN_GENERIC, 0)
+    p = plan(0, 0, 4096, 4096, 4096, tma_ok=False, pinned=V.VARIANT_GENERIC)
+    assert (p["kind"], p["copies"]) == (V.PLAN_GENERIC, 0)
+
+
+@pytest.mark.parametrize("tA,tB", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("aligned", [0, 1, 2])
+def test_misaligned_operands_are_copied(tA, tB, aligned):
+    """An operand the TMA cannot read as stored (bit clear in `aligned`) is
+    copied transposed into the workspace -- whatever its stored layout -- and
+    the TMA kernels run on the copy; the generic kernel runs when the
+    re-layout is off, when the copies do not fit, when the problem is small
+    enough that its estimate is lower, for a batch beyond the tensor maps'
+    reach, and when pinned."""
+    need = 3 & ~aligned
+    M, N, K = 2048, 1536, 1024
+    for mode in (V.RELAYOUT_AUTO, V.RELAYOUT_ALWAYS):
+        p = plan(tA, tB, M, N, K, tma_ok=aligned, relayout_mode=mode)
+        assert p["kind"] == V.PLAN_TMA and p["copies"] & need == need, (mode, p)
+        check_invariants(p, tA, tB, M, N, K)
+        for pin in (V.VARIANT_TMA_128x128, V.VARIANT_TMA_64x64):
+            q = plan(tA, tB, M, N, K, tma_ok=aligned, relayout_mode=mode, pinned=pin)
+            assert q["kind"] == V.PLAN_TMA and q["variant"] == pin and q["copies"] & need == need
+            check_invariants(q, tA, tB, M, N, K)
+    assert plan(tA, tB, M, N, K, tma_ok=aligned, relayout_mode=V.RELAYOUT_OFF)["kind"] == V.PLAN_GENERIC
+    assert plan(tA, tB, M, N, K, tma_ok=aligned, relayout_floats=1000)["kind"] == V.PLAN_GENERIC
+    # small: one copy still pays (the generic kernel has about 9 us of fixed cost), two do not
+    small = plan(tA, tB, 70, 90, 50, tma_ok=aligned)
+    assert small["kind"] == (V.PLAN_GENERIC if aligned == 0 else V.PLAN_TMA)
+    check_invariants(small, tA, tB, 70, 90, 50)
+    assert plan(tA, tB, 8, 8, 8, tma_ok=aligned, batch=70000, strideA=64, strideB=64)["kind"] == V.PLAN_GENERIC
+    # the tensor-core kernels need both operands as stored or as their own copies give them
+    q = plan(tA, tB, M, N, K, tma_ok=aligned, math_mode=V.MATH_3XTF32)
+    assert q["kind"] == V.PLAN_TMA and q["copies"] & need == need
+    assert plan(tA, tB, M, N, K, tma_ok=aligned, pinned=V.VARIANT_TC_3XTF32_PAIR)["kind"] == V.PLAN_GENERIC
+
+
+def test_misaligned_choice_follows_the_estimates():
+    """A misaligned A stored M x K goes to the TN layout (its copy is the
+    re-layout the aligned call makes anyway); a misaligned B stored K x N is
+    copied to N x K together with A (both transposed: the NN kernel on the
+    swapped operands) rather than alone (NT, the slowest main loop)."""
+    p = plan(0, 0, 4096, 4096, 4096, tma_ok=2)
+    assert (p["kind"], p["copies"], p["op"]) == (V.PLAN_TMA, 1, 1)
+    p = plan(0, 0, 4096, 4096, 4096, tma_ok=1)
+    assert (p["kind"], p["copies"], p["op"]) == (V.PLAN_TMA, 3, 0)
 
 
 def test_tensor_core_plans():
