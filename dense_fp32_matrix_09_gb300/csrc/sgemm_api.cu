@@ -211,6 +211,9 @@ long long sk_ctas_for(const sgemm_ctx *h, long long T, long long sk_tiles, long 
     return std::max(G, 0LL);
 }
 
+double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
+                 const sg::SplitK &plan);
+
 // The 64 x 64 split variant: every tile's K steps shared by up to one wave
 // of stream-K CTAs (one K step each at least), when that gives at least two
 // CTAs per tile (with fewer, most tiles would stay whole and whole tiles
@@ -225,6 +228,17 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     if (G < 2 * tiles) return;
     *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
     sk->fixup = h->sk_sums == SGEMM_SK_SUMS_SHARED ? sg::kFixupShared : sg::kFixupLast;
+    if (h->sk_sums == SGEMM_SK_SUMS_AUTO) {
+        // the last CTA of each tile adds its parts, or (many parts a tile) the
+        // CTAs ending in it share the adding: whichever the estimate prefers
+        sg::TmaShape sh;
+        sg::tma_shape(SGEMM_VARIANT_TMA_64x64_SPLITK, &sh);
+        sg::SplitK shared = *sk;
+        shared.fixup = sg::kFixupShared;
+        if (plan_time(h, SGEMM_VARIANT_TMA_64x64_SPLITK, sh, M, N, K, 1, sg::kTmaOpNN, shared) <
+            plan_time(h, SGEMM_VARIANT_TMA_64x64_SPLITK, sh, M, N, K, 1, sg::kTmaOpNN, *sk))
+            *sk = shared;
+    }
 }
 
 // Estimated time, in microseconds (only the ranking matters), of `variant`'s
@@ -253,7 +267,11 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 //    1000 x 1500 x 777);
 //  - the 64 x 64 tail split, kSmallSplitFixup;
 //  - the 64 x 64 split-all variant, kSplitAllFixup (7.2-9.2 us from 256^3 to
-//    768^3).
+//    768^3);
+//    both with the parts added by the last CTA of each tile, which reads them
+//    one after another: beyond 8 parts a tile, kLastUsPerPart for each (tall
+//    K on few tiles: 21.0 us at 100 x 100 x 2000 with 63 parts a tile, 32.9
+//    at 64 x 64 x 4096 with 128; shared sums there: 11.4-13.7 and 13.6).
 // The stream-K K steps of the 128 x 128 tile (two CTAs per SM) also ran
 // slower than its whole tiles, by kSharedSplitSlow (1024^3,
 // 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us against
@@ -266,6 +284,7 @@ constexpr double kDeferred256x128 = 2.0;
 constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
 constexpr double kSplitAllFixup = 8.0;
+constexpr double kLastUsPerPart = 0.19;
 constexpr double kSharedBase = 8.0;
 constexpr double kSharedUsPerMB = 0.12;
 constexpr double kShared256x128 = 1.0;
@@ -295,8 +314,12 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     auto wave = [&](double ctas, double steps) {
         return steps * t_step * std::min(cps, std::ceil(ctas / sms)) / cps;
     };
-    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK)
-        return wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas)) + kSplitAllFixup;
+    if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
+        const double t = wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas));
+        if (plan.fixup == sg::kFixupShared)
+            return t + kSharedBase + kSharedUsPerMB * (tiles + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;
+        return t + kSplitAllFixup + kLastUsPerPart * std::max(0.0, std::ceil(plan.sk_ctas / tiles) + 1 - 8);
+    }
     if (plan.ksplit > 1) {
         // cluster split-K: tiles * ksplit CTAs of ceil(kt / ksplit) steps, one
         // per SM, wave by wave, then each CTA adds a 1/ksplit slice of its
@@ -319,7 +342,8 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
             t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kSharedBase +
                  kSharedUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kShared256x128 : 0.0);
         } else {
-            t += wave(plan.sk_ctas, steps) + kSmallSplitFixup;
+            t += wave(plan.sk_ctas, steps) + kSmallSplitFixup +
+                 kLastUsPerPart * std::max(0.0, std::ceil(plan.sk_ctas / rem) + 1 - 8);
         }
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
     } else if (rem > 0) {
@@ -353,6 +377,7 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
     // how the parts are added: the hook's choice, else (larger tiles) the
     // cheaper of the second kernel and the shared in-kernel sums
     int fixups[2] = {sg::kFixupLast, -1};
+    if (!large && h->sk_sums == SGEMM_SK_SUMS_AUTO) fixups[1] = sg::kFixupShared;  // by the estimate, below
     if (h->sk_sums == SGEMM_SK_SUMS_SHARED) {
         fixups[0] = sg::kFixupShared;
     } else if (large && h->sk_sums == SGEMM_SK_SUMS_DEFERRED) {
@@ -363,8 +388,9 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
     }
     if (G <= rem || (fixups[0] == sg::kFixupLast && G * 4 < rem * 5)) return;
     // the test hook's modes split whenever they can; automatic, by the estimate
-    const bool forced = h->sk_sums != SGEMM_SK_SUMS_AUTO || fixups[0] == sg::kFixupLast;
-    double best = forced ? -1.0 : plan_time(h, variant, sh, M, N, K, batch, op, *sk);
+    // (the 64 x 64 tile always splits here, taking the cheaper way of adding)
+    const bool forced = h->sk_sums != SGEMM_SK_SUMS_AUTO;
+    double best = forced || !large ? -1.0 : plan_time(h, variant, sh, M, N, K, batch, op, *sk);
     for (int f : fixups) {
         if (f < 0) continue;
         sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
