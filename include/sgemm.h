@@ -25,6 +25,13 @@
  *   - M == 0 or N == 0: nothing is done; every pointer may be NULL.
  *   - Cells outside the M x K, K x N, M x N windows (columns K..lda-1 of A,
  *     N..ldb-1 of B, N..ldc-1 of C) are never read or written.
+ *   - Any 4-byte-aligned pointer and any leading dimension is accepted.  An
+ *     operand the TMA cannot read as stored (not 16-byte aligned, or its
+ *     leading dimension -- or batch stride -- not a multiple of 4) is either
+ *     read with scalar loads by the generic variant or first copied
+ *     transposed, on the GPU, into the handle's re-layout workspace, which
+ *     the TMA kernels then read (whichever the library estimates faster;
+ *     see sgemm_relayout_t).  Never an error, never a CPU path.
  *
  * Column-major (BLAS / Fortran order) callers: a column-major m x n matrix
  * with leading dimension ld is the row-major n x m matrix of its transpose,
@@ -77,9 +84,10 @@ typedef enum {
 
 /* Kernel variants.  SGEMM_VARIANT_AUTO lets sgemm_run choose from the shape
  * and the alignment of the operands; the others pin one variant (for tests
- * and measurements).  A pinned variant whose preconditions a call does not
- * meet (TMA variants need 16-byte aligned A and B and lda, ldb multiples of
- * 4) is replaced by the generic variant for that call. */
+ * and measurements).  A pinned TMA variant on an operand the TMA cannot read
+ * as stored runs on its transposed copy (the re-layout workspace), or, when
+ * the re-layout is off or the copy does not fit, is replaced by the generic
+ * variant for that call. */
 typedef enum {
     SGEMM_VARIANT_AUTO = 0,
     SGEMM_VARIANT_TMA_128x256 = 1,   /* TMA-fed SIMT, 128 x 256 CTA tile, 8 x 16 per thread */
@@ -101,8 +109,9 @@ typedef enum {
     SGEMM_VARIANT_COUNT_ = 12
     /* sgemm_run_ex: the TMA variants serve every (transA, transB) and any
      * batch up to 65535 when A and B are 16-byte aligned and lda, ldb (and,
-     * for batch > 1, strideA, strideB) are multiples of 4; otherwise the
-     * generic variant runs.  The tensor-core variants serve every layout
+     * for batch > 1, strideA, strideB) are multiples of 4, and operands that
+     * are not through their transposed copies (above); otherwise the generic
+     * variant runs.  The tensor-core variants serve every layout
      * and batches of up to 256 products (one launch per product): they read
      * A stored M x K and B stored K x N, and an operand stored transposed is
      * first copied into that layout in the re-layout workspace (one launch
@@ -127,7 +136,7 @@ typedef enum {
 } sgemm_math_mode_t;
 
 /* Operand re-layout of the FP32 SIMT path (sgemm_run, sgemm_run_ex, any
- * batch, TMA-eligible operands; the tensor-core variants' copies into the NN
+ * batch; the tensor-core variants' copies into the NN
  * layout use the same workspace and are off with SGEMM_RELAYOUT_OFF).  A
  * strided batch is copied matrix by matrix (an operand with batch stride 0
  * once), each copy in its own slot of the workspace.  On GB300 the SIMT kernel's main loop is
@@ -139,10 +148,18 @@ typedef enum {
  * copy.  Every layout forms each product in ascending k with one rounding
  * per FMA, so with the same tile variant and the same stream-K plan the
  * result is bit-identical to the call without re-layout.
+ * An operand the TMA cannot read as stored (see the conventions above) is
+ * copied transposed whatever its stored layout, and the other operand as
+ * the estimate prefers; the generic variant runs instead when its estimate
+ * is lower (small problems: about 9 us of fixed cost against the copies'
+ * launches).
  *   SGEMM_RELAYOUT_AUTO (default): when the library's time estimate of the
  *     copies plus the faster kernel beats the kernel on the operands as
- *     stored by at least 1 % and the copies fit in the workspace;
- *   SGEMM_RELAYOUT_OFF: never;
+ *     stored by at least 1 % and the copies fit in the workspace (an
+ *     operand the TMA cannot read: when they fit and beat the generic
+ *     variant);
+ *   SGEMM_RELAYOUT_OFF: never (an operand the TMA cannot read: the generic
+ *     variant);
  *   SGEMM_RELAYOUT_ALWAYS: whenever the copies that reach transA = 1,
  *     transB = 0 fit in the workspace (tests, measurements). */
 typedef enum {
