@@ -3,7 +3,8 @@
 (SGEMM_LIBRARY; started by tests/test_gpu_device_checks.py).
 
 Every call -- each tile variant, each way of adding stream-K parts, cluster
-split-K, every operand layout, strided batches -- must match the oracle with
+split-K, every operand layout, strided batches, operands copied because the
+TMA cannot read them as stored -- must match the oracle with
 every check passing (device status OK).  Then a negative control: the kernels
 are told the stream-K workspace holds one partial tile (the real one is
 larger, so nothing is accessed out of bounds), the check fails and is
@@ -45,6 +46,20 @@ def main() -> int:
     sgemm.sgemm_set_variant(h, V.VARIANT_AUTO)
     sgemm.sgemm_debug_set_stream_k_sums(h, V.SK_SUMS_AUTO)
     sgemm.sgemm_debug_set_cluster_split(h, 0)
+    # operands the TMA cannot read as stored (odd leading dimensions): their
+    # transposed copies in every layout, on each tile variant
+    for v in variants[1:5]:
+        for i, op in enumerate([(0, 0), (1, 0), (0, 1), (1, 1)]):
+            sgemm.sgemm_set_variant(h, v)
+            p = ExProblem(*op, 300, 520, 270, 1 + i % 2, seed=300 + n, alpha=1.25, beta=0.5,
+                          pad=(1, 1 if i % 2 else 8, 4), mult4=True)
+            C, bufs = p.run(h)
+            p.check(C, bufs)
+            assert sgemm.sgemm_last_relayout(h) & 1, (v, op)
+            st = sgemm.sgemm_get_device_status(h)
+            assert st == V.OK, (v, op, "misaligned", sgemm.status_string(st))
+            n += 1
+    sgemm.sgemm_set_variant(h, V.VARIANT_AUTO)
     # negative control: a stream-K call whose part slots exceed the capacity the kernels are told
     sgemm.sgemm_set_variant(h, V.VARIANT_TMA_64x64)
     sgemm.sgemm_debug_set_stream_k_sums(h, V.SK_SUMS_LAST)
