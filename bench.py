@@ -741,6 +741,8 @@ def main():
             step()
         torch.cuda.synchronize()
         tc_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.tensor_steps)]
+        tc_sampler = ClockSampler(nvsmi_id(torch, torch.cuda.current_device()))
+        tc_sampler.start()
         for i in range(args.tensor_steps):
             if in_place:
                 C.copy_(C0)
@@ -748,6 +750,7 @@ def main():
             step()
             tc_ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
+        tc_clocks = tc_sampler.stop()
         tc_ms = statistics.mean(tc_ev[2 * i].elapsed_time(tc_ev[2 * i + 1]) for i in range(args.tensor_steps))
         # the other operand layouts on the same kernel (transposed operands
         # reach it through copies into the NN layout), square workloads only
@@ -782,6 +785,9 @@ def main():
                          "tf32_from_bf16_nominal_ratio": tf32_nominal_ratio,
                          "tensor_mma_tflops": 3 * tc_tflops, "tensor_mma_frac": 3 * tc_tflops / tf32_peak},
             "layouts": tc_layouts,
+            # clocks while the steps ran: the pair kernel draws far more power
+            # than the SIMT kernel, and the TF32 probe's rate is a burst figure
+            "clocks": tc_clocks,
         }
 
     # ---- sgemm_run_ex: the four operand layouts on the headline shape, and a
