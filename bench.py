@@ -120,7 +120,8 @@ def parse():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=None,
                    help="workload name, or MxNxK for an ad-hoc alpha=1 beta=0 problem (default: 8192^3)")
-    p.add_argument("--variant", default="auto", help="pin a kernel variant by name (default: auto)")
+    p.add_argument("--variant", default=os.environ.get("SGEMM_FORCE_VARIANT", "auto"),
+                   help="pin a kernel variant by name (default: $SGEMM_FORCE_VARIANT, else auto)")
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
