@@ -315,13 +315,15 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
             e.synchronize()
             warm.append(s.elapsed_time(e))
     # back-to-back (hot L2) mean, beta == 0 only (in-place updates would compound)
-    hot = None
+    hot = host_us = None
     if cfg.beta == 0:
         n = max(10, reps)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
+        t0 = time.perf_counter()
         for _ in range(n):
             call()
+        host_us = (time.perf_counter() - t0) / n * 1e6  # enqueue cost per call on the host (Python binding included)
         e.record(stream)
         e.synchronize()
         hot = s.elapsed_time(e) / n
@@ -362,6 +364,7 @@ def time_workload(torch, sg, h, cfg, reps: int, cold: bool, flush_buf):
     if hot is not None:
         out["ms_back_to_back"] = hot
         out["tflops_back_to_back"] = cfg.flops / (hot * 1e-3) / 1e12
+        out["us_host_enqueue_per_call"] = host_us
     if graph_ms is not None:
         out["ms_per_call_in_cuda_graph"] = graph_ms
         out["tflops_in_cuda_graph"] = cfg.flops / (graph_ms * 1e-3) / 1e12
