@@ -71,6 +71,8 @@ class SgemmError(RuntimeError):
 
 
 _lib = None
+_calls = None          # the compiled marshalling module for sgemm_run / sgemm_run_ex, when built
+_calls_tried = False
 
 
 def library_path() -> str:
@@ -131,6 +133,30 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
+def _current_stream_handle() -> int:
+    import torch
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+def calls_module():
+    """The CPython module that marshals sgemm_run / sgemm_run_ex arguments
+    (built next to the library by build.py), bound to the loaded library; None
+    when it was not built -- the two calls then go through ctypes."""
+    global _calls, _calls_tried
+    if not _calls_tried:
+        _calls_tried = True
+        path = _build.CALLS
+        if os.path.exists(path):
+            import importlib.util
+            lib()  # the library is loaded first; the module binds the same instance by path
+            spec = importlib.util.spec_from_file_location("_sgemm_calls", path)
+            mod = importlib.util.module_from_spec(spec)
+            spec.loader.exec_module(mod)
+            mod.init(library_path(), _current_stream_handle)
+            _calls = mod
+    return _calls
+
+
 def _ptr(x) -> int | None:
     """Address of a buffer: an int, a torch tensor (data_ptr) or a numpy array."""
     if x is None:
@@ -144,8 +170,7 @@ def _ptr(x) -> int | None:
 
 def _stream(s) -> int:
     if s is None:
-        import torch
-        return int(torch.cuda.current_stream().cuda_stream)
+        return _current_stream_handle()
     if isinstance(s, int):
         return s
     return int(s.cuda_stream)
@@ -181,8 +206,14 @@ def sgemm_destroy(h) -> None:
 
 def sgemm_run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
     """C <- alpha*A*B + beta*C on device buffers (row-major, leading dims)."""
-    _check(lib().sgemm_run(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
-                           int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream)), "sgemm_run")
+    calls = _calls if _calls is not None else calls_module()
+    if calls is not None:
+        rc = calls.run(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream)
+    else:
+        rc = lib().sgemm_run(h, int(M), int(N), int(K), float(alpha), _ptr(A), int(lda), _ptr(B),
+                             int(ldb), float(beta), _ptr(C), int(ldc), _stream(stream))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_run")
 
 
 def sgemm_run_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> None:
@@ -206,9 +237,16 @@ def sgemm_run_host(h, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, dA, dB, dC, 
 def sgemm_run_ex(h, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,
                  batch=1, stream=None) -> None:
     """C_b <- alpha*op(A_b)*op(B_b) + beta*C_b, b = 0..batch-1 (see include/sgemm.h)."""
-    _check(lib().sgemm_run_ex(h, int(transA), int(transB), int(M), int(N), int(K), float(alpha), _ptr(A), int(lda),
-                              int(strideA), _ptr(B), int(ldb), int(strideB), float(beta), _ptr(C), int(ldc),
-                              int(strideC), int(batch), _stream(stream)), "sgemm_run_ex")
+    calls = _calls if _calls is not None else calls_module()
+    if calls is not None:
+        rc = calls.run_ex(h, transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                          strideC, batch, stream)
+    else:
+        rc = lib().sgemm_run_ex(h, int(transA), int(transB), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                int(lda), int(strideA), _ptr(B), int(ldb), int(strideB), float(beta), _ptr(C),
+                                int(ldc), int(strideC), int(batch), _stream(stream))
+    if rc != OK:
+        raise SgemmError(rc, "sgemm_run_ex")
 
 
 def sgemm_check_args_ex(transA, transB, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc, strideC,

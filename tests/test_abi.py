@@ -230,3 +230,48 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(build, "LIB", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="missing"):
         sgemm.lib()
+
+
+def test_marshalling_module_reaches_the_library(lib):
+    """The compiled module that marshals sgemm_run / sgemm_run_ex arguments is
+    built next to the library and binds the same library instance: a call with
+    a handle that was never created comes back from the library as
+    SGEMM_ERR_BAD_HANDLE, whatever form the buffers and the stream take (ints,
+    objects with data_ptr(), numpy arrays, objects with cuda_stream)."""
+    import numpy as np
+    torch = pytest.importorskip("torch")
+    calls = sgemm.calls_module()
+    assert calls is not None, build.calls_build_error
+
+    class Stream:
+        cuda_stream = 0
+
+    t = torch.empty(16)
+    a = np.empty(16, dtype=np.float32)
+    bogus = ctypes.c_void_p(0x1000)
+    for buf in (t, a, 0x2000, None):
+        assert calls.run(bogus, 8, 8, 8, 1.0, buf, 8, buf, 8, 0.0, t, 8, 0) == sgemm.ERR_BAD_HANDLE
+        assert calls.run(0x1000, 8, 8, 8, 1.0, buf, 8, buf, 8, 0.0, t, 8, Stream()) == sgemm.ERR_BAD_HANDLE
+        assert calls.run_ex(None, 0, 1, 8, 8, 8, 1.0, buf, 8, 0, buf, 8, 0, 0.0, t, 8, 0, 1, 0) == \
+            sgemm.ERR_BAD_HANDLE
+    with pytest.raises(sgemm.SgemmError):
+        sgemm.sgemm_run(bogus, 8, 8, 8, 1.0, t, 8, t, 8, 0.0, t, 8, 0)
+    with pytest.raises(sgemm.SgemmError):
+        sgemm.sgemm_run_ex(bogus, 0, 0, 8, 8, 8, 1.0, t, 8, 0, t, 8, 0, 0.0, t, 8, 0, 1, 0)
+
+
+def test_marshalling_module_rejects_malformed_arguments(lib):
+    """Wrong argument counts, values that do not fit a C int and objects that
+    are no buffers raise Python exceptions before the library is called."""
+    calls = sgemm.calls_module()
+    assert calls is not None, build.calls_build_error
+    with pytest.raises(TypeError):
+        calls.run(None, 8, 8, 8)
+    with pytest.raises(TypeError):
+        calls.run_ex(None, 0, 0, 8, 8, 8)
+    with pytest.raises(OverflowError):
+        calls.run(None, 1 << 40, 8, 8, 1.0, 0, 8, 0, 8, 0.0, 0, 8, 0)
+    with pytest.raises((TypeError, AttributeError)):
+        calls.run(None, 8, 8, 8, 1.0, object(), 8, 0, 8, 0.0, 0, 8, 0)
+    with pytest.raises(TypeError):
+        calls.run(None, 8, 8, 8, "one", 0, 8, 0, 8, 0.0, 0, 8, 0)
