@@ -149,11 +149,14 @@ def calls_module():
         if os.path.exists(path):
             import importlib.util
             lib()  # the library is loaded first; the module binds the same instance by path
-            spec = importlib.util.spec_from_file_location("_sgemm_calls", path)
-            mod = importlib.util.module_from_spec(spec)
-            spec.loader.exec_module(mod)
-            mod.init(library_path(), _current_stream_handle)
-            _calls = mod
+            try:
+                spec = importlib.util.spec_from_file_location("_sgemm_calls", path)
+                mod = importlib.util.module_from_spec(spec)
+                spec.loader.exec_module(mod)
+                mod.init(library_path(), _current_stream_handle)
+                _calls = mod
+            except (ImportError, OSError):
+                _calls = None  # a module built for another interpreter or machine: ctypes serves
     return _calls
 
 
