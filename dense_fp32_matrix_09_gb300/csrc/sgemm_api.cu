@@ -358,12 +358,15 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
 // partly empty wave may be shared evenly by G stream-K CTAs (G <= P, at
 // least 2 K steps each, within the workspace), so the last wave keeps every
 // slot busy for rem*kt/G steps instead of leaving P - rem slots idle for a
-// whole tile.  The 64 x 64 tile adds a tile's parts in its last CTA to
-// arrive and takes the split when G is at least 1.25 rem (less saved little
-// over whole tiles on GB300); the larger tiles, whose parts are 4-8 times
+// whole tile.  The 64 x 64 tile takes the split when G is at least 1.25 rem
+// (less saved little over whole tiles on GB300) and has a tile's parts added
+// by its last CTA to arrive or shared by the CTAs ending in it, whichever the
+// estimate prefers (the last CTA reads them one after another, which costs
+// with many parts a tile); the larger tiles, whose parts are 4-8 times
 // larger, leave them to a second kernel that adds them over the whole GPU
-// (deferred), and take the split when its estimate beats whole tiles.  Under
-// the in-kernel test hook every tile takes the 64 x 64 tile's way.
+// (deferred) or share them, and take the split when its estimate beats whole
+// tiles.  Under the test hook's modes every tile splits as the 64 x 64 tile
+// does and adds its parts the hook's way.
 void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                sg::SplitK *sk) {
     const long long tiles = 1LL * cdiv(M, sh.bm) * cdiv(N, sh.bn) * batch;

@@ -46,11 +46,13 @@
 //    iterations with its TMA pipeline running across tile boundaries.  A
 //    tile whose K range is split stores each part in a workspace slot; the
 //    parts are added in ascending k order -- a fixed order, so results are
-//    deterministic -- and the epilogue runs on the sum.  For the 64 x 64 tile
-//    the last CTA of the tile to arrive (arrival counter) adds them; for the
-//    larger tiles (SplitK::defer) sk_finish_kernel adds them over the whole
-//    GPU, launched as a programmatic dependent of the stream-K grid.  The
-//    64 x 64 split variant runs every tile this way.
+//    deterministic -- and the epilogue runs on the sum.  Three ways, chosen
+//    on the host (SplitK::fixup): the last CTA of the tile to arrive
+//    (arrival counter) adds them; the CTAs whose K range ends in the tile
+//    wait for every part and add one slice each; or (tiles larger than
+//    64 x 64) sk_finish_kernel adds them over the whole GPU, launched as a
+//    programmatic dependent of the stream-K grid.  The 64 x 64 split
+//    variant runs every tile as stream-K tiles.
 //  * Operand layouts (template parameter OP).  NN: A stored M x K and B
 //    stored K x N, as above.  TN: A stored K x M; its stage is BK rows of BM
 //    floats (no swizzle) and each thread owns groups of 4 consecutive rows,

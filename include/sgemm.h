@@ -413,8 +413,10 @@ typedef enum {
  * whose K range is split over stream-K CTAs (sgemm_sk_sums_t).  Automatic:
  * for the tiles larger than 64 x 64, whichever of a second kernel and the
  * shared sums the library's time estimate prefers (and stream-K only where
- * it beats whole tiles); the 64 x 64 tiles add them in the last CTA of the
- * tile to arrive.  The other modes take the stream-K tail whenever a wave
+ * it beats whole tiles); for the 64 x 64 tiles, whichever of the last CTA of
+ * the tile to arrive and the shared sums it prefers (the last CTA reads the
+ * parts one after another, which costs with many parts a tile).  The other
+ * modes take the stream-K tail whenever a wave
  * has CTAs to spare (LAST: 1.25 per tile), so that every mode splits a call
  * the same way.  SGEMM_ERR_INVALID_VALUE for another value. */
 int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int mode);
