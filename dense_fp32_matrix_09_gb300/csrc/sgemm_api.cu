@@ -43,12 +43,12 @@ struct CallPlan {
 // Everything a plan depends on besides the handle's fixed device facts.
 struct PlanKey {
     int transA, transB, M, N, K, batch, a_shared, b_shared, aligned, pinned, relayout_mode, math_mode, sk_sums,
-        ksplit_pin;
+        ksplit_pin, sk_ctas_pin;
     bool operator==(const PlanKey &o) const {
         return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
                a_shared == o.a_shared && b_shared == o.b_shared && aligned == o.aligned && pinned == o.pinned &&
                relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_sums == o.sk_sums &&
-               ksplit_pin == o.ksplit_pin;
+               ksplit_pin == o.ksplit_pin && sk_ctas_pin == o.sk_ctas_pin;
     }
 };
 
@@ -95,6 +95,7 @@ struct sgemm_ctx {
     int last_relayout;                      // operands the last call transposed (bit 0 A, bit 1 B)
     int sk_sums;                            // test hook: sgemm_sk_sums_t, how stream-K parts are added
     int ksplit_pin;                         // test hook: cluster split-K CTAs per tile (0 auto, 1 none)
+    int sk_ctas_pin;                        // test hook: stream-K CTAs of a tail or split-all plan (0 auto)
     int ws_tiles_limit;                     // test hook: workspace capacity the kernels are told (0: real)
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
@@ -214,6 +215,26 @@ long long sk_ctas_for(const sgemm_ctx *h, long long T, long long sk_tiles, long 
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                  const sg::SplitK &plan);
 
+// Stream-K CTA counts a plan weighs: the most it allows (g_max), and fewer,
+// whole multiples of its `unit` tiles from `pmin` per tile on -- fewer CTAs
+// take longer K ranges each and leave fewer parts a tile to add (on GB300
+// the best count for tall K on few tiles was about one CTA per SM, not the
+// three the 64 x 64 tile could have).  The test hook's count, when set, is
+// the only one (within the plan's limits).
+int sk_ctas_candidates(const sgemm_ctx *h, long long g_max, long long unit, long long pmin, long long *out) {
+    if (h->sk_ctas_pin > 0) {
+        out[0] = std::min(g_max, std::max(pmin * unit, static_cast<long long>(h->sk_ctas_pin)));
+        return 1;
+    }
+    int n = 0;
+    out[n++] = g_max;
+    for (long long p : {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128}) {
+        const long long g = p * unit;
+        if (p >= pmin && g < g_max) out[n++] = g;
+    }
+    return n;
+}
+
 // The 64 x 64 split variant: every tile's K steps shared by up to one wave
 // of stream-K CTAs (one K step each at least), when that gives at least two
 // CTAs per tile (with fewer, most tiles would stay whole and whole tiles
@@ -224,21 +245,33 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     *sk = sg::SplitK{static_cast<int>(tiles), 0, nullptr, nullptr};
     if (tiles > h->n_counters) return;
     const long long slots = 1LL * h->num_sms * std::max(1, h->ctas_per_sm[SGEMM_VARIANT_TMA_64x64_SPLITK]);
-    const long long G = sk_ctas_for(h, tiles * kt, tiles, slots, 64 * 64, 1);
-    if (G < 2 * tiles) return;
-    *sk = sg::SplitK{0, static_cast<int>(G), h->d_ws, h->d_counters};
+    const long long g_max = sk_ctas_for(h, tiles * kt, tiles, slots, 64 * 64, 1);
+    if (g_max < 2 * tiles) return;
+    *sk = sg::SplitK{0, static_cast<int>(g_max), h->d_ws, h->d_counters};
     sk->fixup = h->sk_sums == SGEMM_SK_SUMS_SHARED ? sg::kFixupShared : sg::kFixupLast;
-    if (h->sk_sums == SGEMM_SK_SUMS_AUTO) {
-        // the last CTA of each tile adds its parts, or (many parts a tile) the
-        // CTAs ending in it share the adding: whichever the estimate prefers
-        sg::TmaShape sh;
-        sg::tma_shape(SGEMM_VARIANT_TMA_64x64_SPLITK, &sh);
-        sg::SplitK shared = *sk;
-        shared.fixup = sg::kFixupShared;
-        if (plan_time(h, SGEMM_VARIANT_TMA_64x64_SPLITK, sh, M, N, K, 1, sg::kTmaOpNN, shared) <
-            plan_time(h, SGEMM_VARIANT_TMA_64x64_SPLITK, sh, M, N, K, 1, sg::kTmaOpNN, *sk))
-            *sk = shared;
+    long long counts[16];
+    if (h->sk_sums != SGEMM_SK_SUMS_AUTO) {
+        // the hook's way of adding, every mode with the same split
+        sk_ctas_candidates(h, g_max, tiles, 2, counts);
+        sk->sk_ctas = static_cast<int>(counts[0]);
+        return;
     }
+    // the CTA count and who adds the parts -- the last CTA of each tile, or the
+    // CTAs ending in it sharing the adding -- that the estimate prefers
+    sg::TmaShape sh;
+    sg::tma_shape(SGEMM_VARIANT_TMA_64x64_SPLITK, &sh);
+    const int n = sk_ctas_candidates(h, g_max, tiles, 2, counts);
+    double best = -1.0;
+    for (int f : {sg::kFixupLast, sg::kFixupShared})
+        for (int i = 0; i < n; ++i) {
+            sg::SplitK cand{0, static_cast<int>(counts[i]), h->d_ws, h->d_counters};
+            cand.fixup = f;
+            const double c = plan_time(h, SGEMM_VARIANT_TMA_64x64_SPLITK, sh, M, N, K, 1, sg::kTmaOpNN, cand);
+            if (best < 0.0 || c < best) {
+                best = c;
+                *sk = cand;
+            }
+        }
 }
 
 // Estimated time, in microseconds (only the ranking matters), of `variant`'s
@@ -272,6 +305,11 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 //    one after another: beyond 8 parts a tile, kLastUsPerPart for each (tall
 //    K on few tiles: 21.0 us at 100 x 100 x 2000 with 63 parts a tile, 32.9
 //    at 64 x 64 x 4096 with 128; shared sums there: 11.4-13.7 and 13.6).
+// Each part a tile has beyond eight also costs the shared sums
+// kSharedUsPerPart and the second kernel kDeferredUsPerPart (64 x 256 x 8192
+// on 64 x 64 tiles, shared sums: 16.6, 19.2, 24.4 and 25.8 us with 32, 64, 96
+// and 114 parts a tile, the K steps taking the same time; 512 x 128 x 8192 on
+// 128 x 128 tiles, second kernel: 28.3, 32.2 and 33.0 us with 32, 64 and 76).
 // The stream-K K steps of the 128 x 128 tile (two CTAs per SM) also ran
 // slower than its whole tiles, by kSharedSplitSlow (1024^3,
 // 1000 x 1500 x 777 and 2048 x 2048 x 1024: 49.5, 56.7 and 165.7 us against
@@ -285,6 +323,8 @@ constexpr double kSharedSplitSlow = 1.10;
 constexpr double kSmallSplitFixup = 8.5;
 constexpr double kSplitAllFixup = 8.0;
 constexpr double kLastUsPerPart = 0.19;
+constexpr double kSharedUsPerPart = 0.1;
+constexpr double kDeferredUsPerPart = 0.05;
 constexpr double kSharedBase = 8.0;
 constexpr double kSharedUsPerMB = 0.12;
 constexpr double kShared256x128 = 1.0;
@@ -316,9 +356,11 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     };
     if (variant == SGEMM_VARIANT_TMA_64x64_SPLITK) {
         const double t = wave(plan.sk_ctas, std::ceil(tiles * kt / plan.sk_ctas));
+        const double over8 = std::max(0.0, std::ceil(plan.sk_ctas / tiles) + 1 - 8);  // parts a tile beyond 8
         if (plan.fixup == sg::kFixupShared)
-            return t + kSharedBase + kSharedUsPerMB * (tiles + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;
-        return t + kSplitAllFixup + kLastUsPerPart * std::max(0.0, std::ceil(plan.sk_ctas / tiles) + 1 - 8);
+            return t + kSharedBase + kSharedUsPerMB * (tiles + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6 +
+                   kSharedUsPerPart * over8;
+        return t + kSplitAllFixup + kLastUsPerPart * over8;
     }
     if (plan.ksplit > 1) {
         // cluster split-K: tiles * ksplit CTAs of ceil(kt / ksplit) steps, one
@@ -333,17 +375,18 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
     if (plan.sk_ctas > 0) {
         const double steps = std::ceil(rem * kt / plan.sk_ctas);
         const double parts_mb = (rem + plan.sk_ctas) * sh.bm * sh.bn * 4.0 / 1e6;  // slots written and read
+        const double over8 = std::max(0.0, std::ceil(plan.sk_ctas / rem) + 1 - 8);  // parts a tile beyond 8
         if (plan.fixup == sg::kFixupDeferred) {
             t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kDeferredBase +
                  kDeferredUsPerMB * parts_mb + kDeferredUsPerMBOver * std::max(0.0, parts_mb - kDeferredKneeMB) +
-                 (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0) +
+                 (variant == SGEMM_VARIANT_TMA_256x128 ? kDeferred256x128 : 0.0) + kDeferredUsPerPart * over8 +
                  2.0;  // the launch of the kernel adding the parts
         } else if (plan.fixup == sg::kFixupShared) {
             t += wave(plan.sk_ctas, steps) * (cps > 1 ? kSharedSplitSlow : 1.0) + kSharedBase +
-                 kSharedUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kShared256x128 : 0.0);
+                 kSharedUsPerMB * parts_mb + (variant == SGEMM_VARIANT_TMA_256x128 ? kShared256x128 : 0.0) +
+                 kSharedUsPerPart * over8;
         } else {
-            t += wave(plan.sk_ctas, steps) + kSmallSplitFixup +
-                 kLastUsPerPart * std::max(0.0, std::ceil(plan.sk_ctas / rem) + 1 - 8);
+            t += wave(plan.sk_ctas, steps) + kSmallSplitFixup + kLastUsPerPart * over8;
         }
         if (full > 0) t += 2.0;  // the stream-K launch after the complete waves
     } else if (rem > 0) {
@@ -390,18 +433,26 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
         fixups[1] = sg::kFixupShared;
     }
     if (G <= rem || (fixups[0] == sg::kFixupLast && G * 4 < rem * 5)) return;
-    // the test hook's modes split whenever they can; automatic, by the estimate
-    // (the 64 x 64 tile always splits here, taking the cheaper way of adding)
+    // the test hook's modes split whenever they can, with the most CTAs (or
+    // the hook's count); automatic, by the estimate, over the ways of adding
+    // and the CTA counts (the 64 x 64 tile always splits here)
     const bool forced = h->sk_sums != SGEMM_SK_SUMS_AUTO;
+    long long counts[16];
+    int n = 1;
+    if (!forced) n = sk_ctas_candidates(h, G, rem, 2, counts);
+    else counts[0] = h->sk_ctas_pin > 0 ? std::min(G, std::max(rem + 1, static_cast<long long>(h->sk_ctas_pin))) : G;
     double best = forced || !large ? -1.0 : plan_time(h, variant, sh, M, N, K, batch, op, *sk);
     for (int f : fixups) {
         if (f < 0) continue;
-        sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(G), h->d_ws, h->d_counters};
-        cand.fixup = f;
-        const double c = forced ? 0.0 : plan_time(h, variant, sh, M, N, K, batch, op, cand);
-        if (best < 0.0 || c < best) {
-            best = c;
-            *sk = cand;
+        for (int i = 0; i < n; ++i) {
+            if (counts[i] <= rem) continue;
+            sg::SplitK cand{static_cast<int>(full * slots), static_cast<int>(counts[i]), h->d_ws, h->d_counters};
+            cand.fixup = f;
+            const double c = forced ? 0.0 : plan_time(h, variant, sh, M, N, K, batch, op, cand);
+            if (best < 0.0 || c < best) {
+                best = c;
+                *sk = cand;
+            }
         }
     }
 }
@@ -693,7 +744,7 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                      long long strideB, int aligned) {
     const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, aligned, h->pinned,
-                      h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin};
+                      h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin, h->sk_ctas_pin};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
     const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, aligned);
@@ -975,6 +1026,13 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
     if (ksplit < 0 || ksplit > 8) return SGEMM_ERR_INVALID_VALUE;
     h->ksplit_pin = ksplit;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (ctas < 0) return SGEMM_ERR_INVALID_VALUE;
+    h->sk_ctas_pin = ctas;
     return SGEMM_OK;
 }
 

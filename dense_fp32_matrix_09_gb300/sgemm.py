@@ -60,7 +60,7 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
            "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
-           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_leave_aborted_state",
+           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_set_stream_k_ctas", "sgemm_debug_leave_aborted_state",
            "sgemm_debug_tf32_probe", "sgemm_debug_set_workspace_limit")
 
 
@@ -114,6 +114,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_set_smem_override.argtypes = [vp, i32]
         L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
         L.sgemm_debug_set_cluster_split.argtypes = [vp, i32]
+        L.sgemm_debug_set_stream_k_ctas.argtypes = [vp, i32]
         L.sgemm_debug_leave_aborted_state.argtypes = [vp]
         L.sgemm_debug_set_workspace_limit.argtypes = [vp, i32]
         L.sgemm_status_string.argtypes = [i32]
@@ -374,6 +375,11 @@ def sgemm_debug_set_workspace_limit(h, tiles: int) -> None:
 
 def sgemm_debug_leave_aborted_state(h) -> None:
     _check(lib().sgemm_debug_leave_aborted_state(h), "sgemm_debug_leave_aborted_state")
+
+
+def sgemm_debug_set_stream_k_ctas(h, ctas: int) -> None:
+    """Test hook: stream-K CTAs of later calls' stream-K plans (0: the library's choice)."""
+    _check(lib().sgemm_debug_set_stream_k_ctas(h, int(ctas)), "sgemm_debug_set_stream_k_ctas")
 
 
 def sgemm_debug_set_cluster_split(h, ksplit: int) -> None:

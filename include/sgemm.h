@@ -435,6 +435,15 @@ int sgemm_debug_set_stream_k_sums(sgemm_handle_t h, int mode);
  * SGEMM_ERR_INVALID_VALUE outside 0..8. */
 int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
 
+/* Test hook: the number of stream-K CTAs of later calls' stream-K plans (the
+ * last wave of the whole-tile variants, and the 64 x 64 split variant); 0 (the
+ * default): the library's choice.  The count is kept within what a plan
+ * allows -- more CTAs than the tail has tiles (the split variant: at least
+ * two per tile), at most a wave of them and the workspace's partial tiles --
+ * and a call whose plan has no stream-K part is unaffected.
+ * SGEMM_ERR_INVALID_VALUE for a negative count. */
+int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas);
+
 /* Test hook: the plan sgemm_run_ex would follow for a call, computed on the
  * host with no handle, no device and no CUDA call, from the device facts a
  * handle records (`num_sms`; `ctas_per_sm`, SGEMM_VARIANT_COUNT_ entries
