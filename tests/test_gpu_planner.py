@@ -3,7 +3,7 @@ plan must run within 10 % of the fastest plan a caller could pin (tile
 variant x operand re-layout).  Times are per call back to back (best of three
 runs of n calls), so launch gaps count as they do for a caller issuing calls
 in a stream.  The shapes are the workloads the estimates were fitted on plus
-shapes away from them (a skinny-N and a tall-K problem)."""
+shapes away from them (a skinny-N problem and tall-K ones on a few tiles)."""
 import itertools
 
 import pytest
@@ -50,6 +50,7 @@ def _per_call_us(run, n):
 @pytest.mark.parametrize("M,N,K,beta", [
     (256, 256, 256, 0.0), (1024, 1024, 1024, 0.0), (1000, 1500, 777, 1.0), (1536, 1536, 1536, 0.0),
     (2048, 2048, 1024, 0.0), (4096, 1024, 1024, 0.0), (8192, 256, 8192, 0.0), (100, 100, 2000, 0.0),
+    (64, 256, 8192, 0.0), (512, 128, 8192, 0.0),
 ])
 def test_automatic_plan_within_ten_percent_of_the_best_pinned(handle, M, N, K, beta):
     g = torch.Generator(device="cuda").manual_seed(5)

@@ -280,3 +280,19 @@ def test_plan_argument_checks():
         plan(0, 0, 4, 4, 4, relayout_mode=7)
     with pytest.raises(sgemm.SgemmError):
         plan(0, 0, 4, 4, 4, pinned=V.VARIANT_SCALE)
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 8192), (256, 64, 8192), (192, 192, 3000), (512, 128, 8192),
+                                   (128, 128, 8192)])
+def test_tall_k_weighs_the_stream_k_cta_count(M, N, K):
+    """Tall K on a few tiles: the plan no longer takes a wave of 64 x 64 slots
+    (three CTAs an SM, 60-130 parts a tile); it weighs fewer CTAs, whole
+    multiples of the tiles, and lands near one CTA per SM (the count measured
+    best on GB300), with every invariant of a stream-K plan kept."""
+    p = plan(0, 0, M, N, K)
+    check_invariants(p, 0, 0, M, N, K)
+    assert p["kind"] == V.PLAN_TMA and p["sk_ctas"] > 0
+    assert p["sk_ctas"] <= SMS, p
+    assert 8 <= p["splits"] <= 48, p
+    tiles = p["tiles"] - p["dp_tiles"]
+    assert p["sk_ctas"] % tiles == 0 or p["sk_ctas"] == min(SMS * OCC[p["variant"]], p["sk_ctas"]), p
