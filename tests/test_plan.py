@@ -79,7 +79,7 @@ def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout
     assert G <= sk_tiles * kt                  # every stream-K CTA has at least one K step
     assert (sk_tiles + G) * bm * bn <= WS_FLOATS  # partial tiles fit in the workspace
     if v == V.VARIANT_TMA_64x64_SPLITK:
-        assert dp == 0 and G >= 2 * tiles and batch == 1 and p["fixup"] == V.FIXUP_LAST
+        assert dp == 0 and G >= 2 * tiles and batch == 1 and p["fixup"] in (V.FIXUP_LAST, V.FIXUP_SHARED)
     else:
         assert dp % slots == 0                 # complete waves only
         assert sk_tiles < slots or sk_tiles == 0
@@ -87,10 +87,10 @@ def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout
         # tiles larger than 64 x 64 leave their parts to a second kernel or
         # share the adding among the CTAs that end in the tile (whichever the
         # estimate prefers) and split whenever a CTA is left over and the
-        # estimate says so; 64 x 64 adds them in its last CTA and splits from
-        # 1.25 CTAs per stream-K tile
+        # estimate says so; 64 x 64 has them added by its last CTA or shared,
+        # and splits from 1.25 CTAs per stream-K tile
         large = bm * bn > 64 * 64
-        assert (p["fixup"] in (V.FIXUP_DEFERRED, V.FIXUP_SHARED)) if large else p["fixup"] == V.FIXUP_LAST
+        assert p["fixup"] in ((V.FIXUP_DEFERRED, V.FIXUP_SHARED) if large else (V.FIXUP_LAST, V.FIXUP_SHARED))
         assert G > sk_tiles if large else 4 * G >= 5 * sk_tiles
     assert p["splits"] >= 2
 
