@@ -88,6 +88,20 @@ def max_abs_err(cfg, C_gpu, C_ref) -> float:
     return float(d.max())
 
 
+def first_mismatch(cfg, C_gpu, C_ref, tol: float) -> str:
+    """The first element (row-major order) whose error exceeds `tol` (or is not
+    finite), with its value and the oracle's -- for assertion messages."""
+    g = inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc).astype(np.float64)
+    r = inputs.dense(C_ref, cfg.M, cfg.N, cfg.ldc).astype(np.float64)
+    bad = ~(np.abs(g - r) <= tol)
+    if not bad.any():
+        return "no element beyond the tolerance"
+    i, j = (int(x) for x in np.argwhere(bad)[0])
+    got, want = float(g[i, j]), float(r[i, j])
+    return (f"{int(bad.sum())} elements beyond {tol:g}; first at C[{i}][{j}] = {got!r}, "
+            f"oracle {want!r} (|diff| {abs(got - want):.3g})")
+
+
 def sample_rows(M: int, bm: int = 128, n_random: int = 24, seed: int = 0) -> list[int]:
     """Rows on both sides of every tile-row boundary near the ends, the ends
     themselves, and a seeded random spread."""

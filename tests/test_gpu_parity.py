@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 from dense_fp32_matrix_09_gb300 import inputs, sgemm
-from tests.gpu_util import (DeviceBuf, check_untouched, max_abs_err, oracle_full, run_gpu,
+from tests.gpu_util import (DeviceBuf, check_untouched, first_mismatch, max_abs_err, oracle_full, run_gpu,
                             sample_rows, tolerance)
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +58,8 @@ def test_workload_full_oracle(handle, cfg):
     C_gpu, bufs = run_gpu(handle, cfg, prob)
     C_ref = oracle_full(cfg, prob)
     err = max_abs_err(cfg, C_gpu, C_ref)
-    assert err <= tolerance(cfg.K), (cfg.name, err, sgemm.sgemm_last_variant(handle))
+    assert err <= tolerance(cfg.K), (cfg.name, sgemm.sgemm_last_variant(handle),
+                                     first_mismatch(cfg, C_gpu, C_ref, tolerance(cfg.K)))
     check_untouched(cfg, prob, C_gpu, bufs)
 
 
@@ -79,8 +80,9 @@ def test_workload_whole_matrix(handle, cfg):
             sgemm.sgemm_last_launches(handle))
     assert plan == LARGE_PLAN, plan
     assert np.all(np.isfinite(inputs.dense(C_gpu, cfg.M, cfg.N, cfg.ldc)))
-    err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
-    assert err <= tolerance(cfg.K), (cfg.name, err)
+    C_ref = oracle_full(cfg, prob)
+    err = max_abs_err(cfg, C_gpu, C_ref)
+    assert err <= tolerance(cfg.K), (cfg.name, first_mismatch(cfg, C_gpu, C_ref, tolerance(cfg.K)))
     check_untouched(cfg, prob, C_gpu, bufs)
 
 
@@ -120,8 +122,9 @@ def test_variant_shape_sweep(handle, variant, v, shape):
             assert ran in (V.VARIANT_TMA_64x64_SPLITK, V.VARIANT_TMA_64x64)
         else:
             assert ran == v, (ran, v)
-        err = max_abs_err(cfg, C_gpu, oracle_full(cfg, prob))
-        assert err <= tolerance(K), (shape, alpha, beta, err)
+        C_ref = oracle_full(cfg, prob)
+        err = max_abs_err(cfg, C_gpu, C_ref)
+        assert err <= tolerance(K), (shape, alpha, beta, first_mismatch(cfg, C_gpu, C_ref, tolerance(K)))
         check_untouched(cfg, prob, C_gpu, bufs)
 
 
