@@ -807,7 +807,7 @@ def main():
     if not args.no_workloads and rank == 0:
         flush_buf = torch.empty(64 << 20, dtype=torch.float32, device="cuda")  # 256 MiB > L2
         table = {}
-        for w, reps in zip(inputs.CONFIGS, (200, 200, 50, 50, 20)):
+        for w, reps in zip(inputs.WORKLOADS, (200, 200, 50, 50, 20)):
             cold = (w.compulsory_bytes < 2 * 129e6)
             row = time_workload(torch, sg, h, w, reps, cold, flush_buf)
             row["frac_of_fp32_peak"] = row["tflops"] / peak  # same unit-count peak as the roofline
@@ -827,7 +827,7 @@ def main():
         # core for the two smallest
         import oracle
         per = {}
-        for w in inputs.CONFIGS:
+        for w in inputs.WORKLOADS:
             wp = prob if w.name == cfg.name else inputs.make_problem(w)
             r, n_rows, t, c = cpu_oracle_rate(w, wp, seconds=1.0)
             per[w.name] = {"gflops": r * 1e3, "cores": c, "rows": n_rows, "seconds": t}

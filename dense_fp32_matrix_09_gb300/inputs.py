@@ -62,16 +62,15 @@ def square(n: int, seed: int, alpha: float = 1.0, beta: float = 0.0, name: str |
 
 #: The five workloads: 256^3; 1024^3; 4096^3 updating C in place; a ragged
 #: 1000 x 1500 x 777 case with padded leading dimensions; and 8192^3.
-CONFIGS = (
-    square(256, 0),
-    square(1024, 1),
-    square(4096, 2, 1.5, 0.5, name="sgemm_4096x4096x4096_inplace_a1.5_b0.5"),
-    GemmConfig("sgemm_1000x1500x777_ragged_ld780_1504_1504", 1000, 1500, 777, 780, 1504, 1504, 3, 1.0, 1.0),
-    square(8192, 4),
-)
-CONFIG_BY_NAME = {c.name: c for c in CONFIGS}
+SQUARE_256 = square(256, 0)
+SQUARE_1024 = square(1024, 1)
+INPLACE_4096 = square(4096, 2, 1.5, 0.5, name="sgemm_4096x4096x4096_inplace_a1.5_b0.5")
+RAGGED = GemmConfig("sgemm_1000x1500x777_ragged_ld780_1504_1504", 1000, 1500, 777, 780, 1504, 1504, 3, 1.0, 1.0)
+SQUARE_8192 = square(8192, 4)
+WORKLOADS = (SQUARE_256, SQUARE_1024, INPLACE_4096, RAGGED, SQUARE_8192)
+CONFIG_BY_NAME = {c.name: c for c in WORKLOADS}
 #: The compute-bound headline workload.
-HEADLINE = CONFIGS[4]
+HEADLINE = SQUARE_8192
 
 
 @dataclass

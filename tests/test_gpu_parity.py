@@ -52,7 +52,7 @@ def _cfg(M, N, K, alpha=1.0, beta=0.0, seed=7, pad=(4, 8, 4), mult4=True):
 
 # ----------------------------------------------------------------- workloads
 
-@pytest.mark.parametrize("cfg", inputs.CONFIGS[:2] + inputs.CONFIGS[3:4], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [inputs.SQUARE_256, inputs.SQUARE_1024, inputs.RAGGED], ids=lambda c: c.name)
 def test_workload_full_oracle(handle, cfg):
     prob = inputs.make_problem(cfg)
     C_gpu, bufs = run_gpu(handle, cfg, prob)
@@ -69,7 +69,7 @@ def test_workload_full_oracle(handle, cfg):
 LARGE_PLAN = (V.VARIANT_TMA_256x128, 1, 3)
 
 
-@pytest.mark.parametrize("cfg", [inputs.CONFIGS[2], inputs.CONFIGS[4]], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [inputs.INPLACE_4096, inputs.SQUARE_8192], ids=lambda c: c.name)
 def test_workload_whole_matrix(handle, cfg):
     """4096^3 in place (alpha 1.5, beta 0.5) and 8192^3 against the oracle on
     every element: max |C_gpu - C_ref| <= 1e-2 (K > 1024), all finite,
@@ -86,7 +86,7 @@ def test_workload_whole_matrix(handle, cfg):
     check_untouched(cfg, prob, C_gpu, bufs)
 
 
-@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", inputs.WORKLOADS, ids=lambda c: c.name)
 def test_workload_integer_exact(handle, cfg):
     """Integer entries in [-2, 2]: every partial sum is exact in float32, so
     the GPU result must equal the oracle bit for bit, on every element of
@@ -414,7 +414,7 @@ def test_whole_waves_plus_split_tail(handle, variant, v):
         check_untouched(cfg, prob, C_gpu, bufs)
 
 
-@pytest.mark.parametrize("cfg", inputs.CONFIGS, ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", inputs.WORKLOADS, ids=lambda c: c.name)
 def test_math_mode_3xtf32_workloads(handle, cfg):
     """3xTF32 math mode on every workload: the tensor-core kernel where the
     problem is large enough, the FP32 kernels otherwise; same tolerance."""
@@ -444,7 +444,7 @@ def test_math_mode_rejects_unknown(handle):
 
 
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
-@pytest.mark.parametrize("cfg", [inputs.CONFIGS[3],
+@pytest.mark.parametrize("cfg", [inputs.RAGGED,
                                  inputs.GemmConfig("host_3000x520x300", 3000, 520, 300, 304, 524, 528, 41, 1.5, 0.5),
                                  inputs.GemmConfig("host_2048x256x64_b0", 2048, 256, 64, 64, 256, 256, 42, 1.0, 0.0),
                                  # 2 row panels, B in 8 column chunks of 768 (the last 132 wide)

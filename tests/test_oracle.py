@@ -57,13 +57,13 @@ def test_empty_and_invalid():
 def test_input_recipe():
     """The generator is seeded, U[-1, 1), puts the sentinel in every padding
     cell, and leaves output-only C all sentinel."""
-    cfg = inputs.CONFIGS[3]
+    cfg = inputs.RAGGED
     p1, p2 = inputs.make_problem(cfg), inputs.make_problem(cfg)
     assert np.array_equal(p1.A.view(np.uint32), p2.A.view(np.uint32))
     a = inputs.dense(p1.A, cfg.M, cfg.K, cfg.lda)
     assert a.min() >= -1 and a.max() < 1 and abs(float(a.mean())) < 0.01
     assert np.all(p1.A.view(np.uint32)[inputs.pad_mask(cfg.M, cfg.K, cfg.lda)] == inputs.PAD_BITS)
     assert np.all(p1.B.view(np.uint32)[inputs.pad_mask(cfg.K, cfg.N, cfg.ldb)] == inputs.PAD_BITS)
-    c0 = inputs.make_problem(inputs.CONFIGS[0]).C0
+    c0 = inputs.make_problem(inputs.SQUARE_256).C0
     assert np.all(c0.view(np.uint32) == inputs.PAD_BITS)
-    assert [c.seed for c in inputs.CONFIGS] == [0, 1, 2, 3, 4]
+    assert [c.seed for c in inputs.WORKLOADS] == [0, 1, 2, 3, 4]

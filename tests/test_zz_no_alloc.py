@@ -18,7 +18,7 @@ from tests.gpu_util import DeviceBuf, max_abs_err, oracle_full, tolerance
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    inputs.CONFIGS[0],                                                          # 256^3, beta = 0
+    inputs.SQUARE_256,                                                          # 256^3, beta = 0
     inputs.GemmConfig("noalloc_300x520x1000", 300, 520, 1000, 1004, 528, 524, 21, 1.5, 0.5),
     inputs.GemmConfig("noalloc_64x64x4096", 64, 64, 4096, 4096, 64, 64, 22, 1.0, 1.0),
     inputs.GemmConfig("noalloc_1000x1000x777", 1000, 1000, 777, 780, 1004, 1000, 23, -0.75, 0.0),
