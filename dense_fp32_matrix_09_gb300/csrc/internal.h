@@ -41,11 +41,70 @@ struct TmaShape {
     int min_ctas_per_sm;
 };
 
+#ifdef __CUDA_ARCH__
+// The 64-bit division, kept out of line: one copy of its code per kernel
+// instead of one at every call site (the first pass over a kernel's code
+// fetches every instruction from memory).
+static __device__ __noinline__ long long div_floor_wide(long long x, long long d) { return x / d; }
+#endif
+
+// floor(x / d) for x >= 0 and 0 < d: a 32-bit division whenever x and d fit
+// in 32 bits (every problem short of K in the millions), which costs a small
+// fraction of the 64-bit division routine at the start of each CTA.
+__host__ __device__ __forceinline__ long long div_floor(long long x, long long d) {
+    if (((static_cast<unsigned long long>(x) | static_cast<unsigned long long>(d)) >> 32) == 0)
+        return static_cast<unsigned>(x) / static_cast<unsigned>(d);
+#ifdef __CUDA_ARCH__
+    return div_floor_wide(x, d);
+#else
+    return x / d;
+#endif
+}
+
+// Stream-K split of the T = tiles x kt iterations (K steps) of the stream-K
+// tiles over G CTAs.  The iterations are laid out on a line of integer
+// positions, tile by tile: each takes kSkSub positions, and every tile after
+// the first is preceded by `gap` positions with no work in them -- the charge
+// for the second part that a CTA whose range runs into the tile stores, so
+// that such a CTA takes fewer K steps (gap = 0: the even split,
+// floor(q*T/G) .. floor((q+1)*T/G)).  With P = kt*kSkSub + gap positions a
+// tile and V = tiles*P - gap in all, CTA q holds positions
+// [gap + floor(q*V/G), gap + floor((q+1)*V/G)); an iteration belongs to the
+// CTA that holds its last position, so CTA q's iterations are
+// [begin(q), begin(q+1)), consecutive and in order.  The host checks that
+// every CTA of a split it chooses gets at least one iteration, of at most
+// two tiles.
+constexpr int kSkSub = 16;
+struct SkLine {
+    long long V = 0;
+    int P = 0, gap = 0, kt = 0, G = 0;
+    __host__ __device__ __forceinline__ SkLine() {}
+    __host__ __device__ __forceinline__ SkLine(long long tiles, int kt_, int G_, int gap_)
+        : V(tiles * (static_cast<long long>(kt_) * kSkSub + gap_) - gap_), P(kt_ * kSkSub + gap_), gap(gap_),
+          kt(kt_), G(G_) {}
+    // First iteration of CTA q (q = G: T).
+    __host__ __device__ __forceinline__ long long begin(int q) const {
+        if (gap == 0) return div_floor(static_cast<long long>(q) * (V / kSkSub), G);  // the even split
+        const long long v = div_floor(static_cast<long long>(q) * V, G) + gap;
+        const long long t = div_floor(v, P);
+        const int r = static_cast<int>(v - t * P) - gap;  // < 0: in the gap before tile t
+        return t * kt + (r <= 0 ? 0 : (r / kSkSub < kt ? r / kSkSub : kt));
+    }
+    // The CTA that holds K step l of tile t: the largest q with
+    // floor(q*V/G) <= y for y = t*P + (l+1)*kSkSub - 1 (the step's last
+    // position less gap), i.e. ceil((y+1)*G/V) - 1.
+    __host__ __device__ __forceinline__ int cta_of(long long t, int l) const {
+        const long long y1 = t * P + static_cast<long long>(l + 1) * kSkSub;
+        return static_cast<int>(div_floor(y1 * G + V - 1, V)) - 1;
+    }
+};
+
 // Stream-K bookkeeping.  Tiles [0, dp_tiles) (in raster order) are computed
 // whole by one CTA each.  The K steps of the remaining tiles -- T = (tiles -
 // dp_tiles) * ceil(K / bk) iterations, taken tile by tile -- are shared by
-// sk_ctas further CTAs: CTA q gets iterations [floor(q*T/G), floor((q+1)*T/G))
-// (G = sk_ctas <= T), so a tile's K range may be split over consecutive CTAs;
+// sk_ctas further CTAs: CTA q gets iterations [begin(q), begin(q+1)) of the
+// SkLine with G = sk_ctas and the split's `gap` (gap = 0: [floor(q*T/G),
+// floor((q+1)*T/G))), so a tile's K range may be split over consecutive CTAs;
 // the parts are summed in ascending k order (see `fixup`).
 // sk_ctas == 0 means no stream-K part (ws and counters unused).
 struct SplitK {
@@ -55,6 +114,10 @@ struct SplitK {
     int *counters;  // one arrival counter per stream-K tile, zero between calls
     int cta0 = 0;   // index of this launch's first CTA in the dp_tiles + sk_ctas sequence
     int fixup = 0;  // who adds the parts of a split tile: kFixupLast, kFixupDeferred or kFixupShared
+    // Stream-K split: positions (1/16 of a K step) charged for each tile
+    // boundary a stream-K CTA's range crosses (0: the even split; see the
+    // kernel's SkLine).
+    int gap = 0;
     // Cluster split-K (sk_ctas == 0 only): ksplit > 1 CTAs per tile, launched as one
     // thread-block cluster, CTA r of the cluster taking K steps [r*kt/ksplit,
     // (r+1)*kt/ksplit); their partial tiles meet in distributed shared memory.

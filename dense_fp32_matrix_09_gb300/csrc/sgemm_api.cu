@@ -43,12 +43,12 @@ struct CallPlan {
 // Everything a plan depends on besides the handle's fixed device facts.
 struct PlanKey {
     int transA, transB, M, N, K, batch, a_shared, b_shared, aligned, pinned, relayout_mode, math_mode, sk_sums,
-        ksplit_pin, sk_ctas_pin;
+        ksplit_pin, sk_ctas_pin, sk_gap_pin;
     bool operator==(const PlanKey &o) const {
         return transA == o.transA && transB == o.transB && M == o.M && N == o.N && K == o.K && batch == o.batch &&
                a_shared == o.a_shared && b_shared == o.b_shared && aligned == o.aligned && pinned == o.pinned &&
                relayout_mode == o.relayout_mode && math_mode == o.math_mode && sk_sums == o.sk_sums &&
-               ksplit_pin == o.ksplit_pin && sk_ctas_pin == o.sk_ctas_pin;
+               ksplit_pin == o.ksplit_pin && sk_ctas_pin == o.sk_ctas_pin && sk_gap_pin == o.sk_gap_pin;
     }
 };
 
@@ -96,6 +96,7 @@ struct sgemm_ctx {
     int sk_sums;                            // test hook: sgemm_sk_sums_t, how stream-K parts are added
     int ksplit_pin;                         // test hook: cluster split-K CTAs per tile (0 auto, 1 none)
     int sk_ctas_pin;                        // test hook: stream-K CTAs of a tail or split-all plan (0 auto)
+    int sk_gap_pin = -1;                    // test hook: boundary charge of stream-K splits (-1 auto)
     int ws_tiles_limit;                     // test hook: workspace capacity the kernels are told (0: real)
     cudaStream_t copy_in, copy_out;         // sgemm_run_host: host->device, device->host
     cudaEvent_t ev_start, ev_done;          //   ordering events (no timing)
@@ -214,6 +215,53 @@ long long sk_ctas_for(const sgemm_ctx *h, long long T, long long sk_tiles, long 
 
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
                  const sg::SplitK &plan);
+double loop_eff(int variant, int op, int K);
+
+// A stream-K split of `tiles` tiles of kt K steps over G CTAs with boundary
+// charge `gap` (sg::SkLine): -1 unless every CTA gets 1..kt K steps of at
+// most two tiles (the kernel's assumptions), else the work of the busiest
+// CTA in K steps, each partial tile it stores counting `rho` steps more (a
+// range that is not one whole tile stores one part per tile it touches).
+double sk_split_cost(long long tiles, int kt, int G, int gap, double rho) {
+    const sg::SkLine ln(tiles, kt, G, gap);
+    double worst = 0.0;
+    long long b = 0;
+    for (int q = 0; q < G; ++q) {
+        const long long e = ln.begin(q + 1);
+        if (e <= b || e - b > kt || (e - 1) / kt - b / kt > 1) return -1.0;
+        const int parts = (e - 1) / kt != b / kt ? 2 : (e - b == kt ? 0 : 1);
+        worst = std::max(worst, static_cast<double>(e - b) + parts * rho);
+        b = e;
+    }
+    return b == tiles * kt ? worst : -1.0;
+}
+
+// The boundary charge of a stream-K split (sk->gap).  A CTA whose range runs
+// from one tile into the next stores two parts instead of one; on GB300 a
+// 128 KB part took about 2.2 us to store with every SM storing at once
+// (about 58 KB per us per SM), against 4.8 us for a K step of the
+// 128 x 256 tile, so a part costs about rho = 0.55 x (main-loop efficiency)
+// K steps whatever the tile (both scale with its area).  Of the charges
+// 0, 4, .., 24 sixteenths of a K step, the one whose busiest CTA has the
+// least work; ties keep the smaller charge (0, the even split, first).  The
+// test hook's charge, when set, is taken if the split it gives is valid.
+void choose_gap(const sgemm_ctx *h, long long tiles, int kt, double eff, sg::SplitK *sk) {
+    sk->gap = 0;
+    if (sk->sk_ctas <= 0) return;
+    const double rho = 0.55 * eff;
+    if (h->sk_gap_pin >= 0) {
+        if (sk_split_cost(tiles, kt, sk->sk_ctas, h->sk_gap_pin, rho) >= 0.0) sk->gap = h->sk_gap_pin;
+        return;
+    }
+    double best = sk_split_cost(tiles, kt, sk->sk_ctas, 0, rho);
+    for (int gap = 4; gap <= 24; gap += 4) {
+        const double c = sk_split_cost(tiles, kt, sk->sk_ctas, gap, rho);
+        if (c >= 0.0 && c < best - 1e-9) {
+            best = c;
+            sk->gap = gap;
+        }
+    }
+}
 
 // Stream-K CTA counts a plan weighs: the most it allows (g_max), and fewer,
 // whole multiples of its `unit` tiles from `pmin` per tile on -- fewer CTAs
@@ -250,10 +298,12 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
     *sk = sg::SplitK{0, static_cast<int>(g_max), h->d_ws, h->d_counters};
     sk->fixup = h->sk_sums == SGEMM_SK_SUMS_SHARED ? sg::kFixupShared : sg::kFixupLast;
     long long counts[16];
+    const double eff = loop_eff(SGEMM_VARIANT_TMA_64x64_SPLITK, sg::kTmaOpNN, K);
     if (h->sk_sums != SGEMM_SK_SUMS_AUTO) {
         // the hook's way of adding, every mode with the same split
         sk_ctas_candidates(h, g_max, tiles, 2, counts);
         sk->sk_ctas = static_cast<int>(counts[0]);
+        choose_gap(h, tiles, static_cast<int>(kt), eff, sk);
         return;
     }
     // the CTA count and who adds the parts -- the last CTA of each tile, or the
@@ -272,6 +322,7 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
                 *sk = cand;
             }
         }
+    choose_gap(h, tiles, static_cast<int>(kt), eff, sk);
 }
 
 // Estimated time, in microseconds (only the ranking matters), of `variant`'s
@@ -335,8 +386,8 @@ constexpr double kShared256x128 = 1.0;
 // cluster size by kClusterPerCta per CTA past two
 constexpr double kClusterFixed[4] = {7.0, 6.0, 3.9, 8.0};
 constexpr double kClusterPerCta = 0.25;
-double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
-                 const sg::SplitK &plan) {
+// The main loop's efficiency (fraction of FP32 peak) of `variant` in layout `op`.
+double loop_eff(int variant, int op, int K) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
     static const double kEff[3][4] = {{0.81, 0.80, 0.65, 0.815}, {0.84, 0.84, 0.715, 0.87},
                                       {0.76, 0.75, 0.49, 0.73}};
@@ -344,7 +395,16 @@ double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M,
                    : variant == SGEMM_VARIANT_TMA_128x128 ? 1
                    : variant == SGEMM_VARIANT_TMA_256x128 ? 3
                                                           : 2;
-    const double eff = (op == sg::kTmaOpTN && vi == 1) ? (K <= 5120 ? 0.86 : 0.78) : kEff[op][vi];
+    return (op == sg::kTmaOpTN && vi == 1) ? (K <= 5120 ? 0.86 : 0.78) : kEff[op][vi];
+}
+
+double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,
+                 const sg::SplitK &plan) {
+    const int vi = variant == SGEMM_VARIANT_TMA_128x256   ? 0
+                   : variant == SGEMM_VARIANT_TMA_128x128 ? 1
+                   : variant == SGEMM_VARIANT_TMA_256x128 ? 3
+                                                          : 2;
+    const double eff = loop_eff(variant, op, K);
     const double cps = std::max(1, h->ctas_per_sm[variant]);
     const double sms = h->num_sms, P = sms * cps;
     const double t_step = static_cast<double>(sh.bm) * sh.bn * sh.bk * cps / (128.0 * eff * 2000.0);
@@ -455,6 +515,7 @@ void plan_tail(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, i
             }
         }
     }
+    choose_gap(h, rem, static_cast<int>(kt), loop_eff(variant, op, K), sk);
 }
 
 // Cluster split-K for the whole-tile variants: ksplit = 2..8 CTAs per tile
@@ -744,7 +805,8 @@ CallPlan plan_call(const sgemm_ctx *h, int transA, int transB, int M, int N, int
 CallPlan cached_plan(sgemm_ctx *h, int transA, int transB, int M, int N, int K, int batch, long long strideA,
                      long long strideB, int aligned) {
     const PlanKey key{transA, transB, M, N, K, batch, strideA == 0, strideB == 0, aligned, h->pinned,
-                      h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin, h->sk_ctas_pin};
+                      h->relayout_mode, h->math_mode, h->sk_sums, h->ksplit_pin, h->sk_ctas_pin,
+                      h->sk_gap_pin};
     for (int i = 0; i < h->plan_filled; ++i)
         if (h->plan_key[i] == key) return h->plan_val[i];
     const CallPlan p = plan_call(h, transA, transB, M, N, K, batch, strideA, strideB, aligned);
@@ -1033,6 +1095,13 @@ int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas) {
     if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
     if (ctas < 0) return SGEMM_ERR_INVALID_VALUE;
     h->sk_ctas_pin = ctas;
+    return SGEMM_OK;
+}
+
+int sgemm_debug_set_stream_k_gap(sgemm_handle_t h, int gap) {
+    if (!alive(h)) return SGEMM_ERR_BAD_HANDLE;
+    if (gap < -1 || gap > 8 * sg::kSkSub) return SGEMM_ERR_INVALID_VALUE;
+    h->sk_gap_pin = gap;
     return SGEMM_OK;
 }
 
@@ -1535,7 +1604,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     c.math_mode = math_mode;
     c.pinned = pinned;
     for (int v = 0; v < SGEMM_VARIANT_COUNT_; ++v) c.ctas_per_sm[v] = ctas_per_sm[v];
-    for (int i = 0; i < 12; ++i) out[i] = 0;
+    for (int i = 0; i < 13; ++i) out[i] = 0;
     out[10] = 1;
     if (M == 0 || N == 0 || batch == 0) return SGEMM_OK;  // nothing runs
     if (alpha == 0.f || K == 0) {
@@ -1563,6 +1632,7 @@ int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_flo
     out[9] = p.kind == kPlanTma && p.sk.sk_ctas > 0 ? p.sk.fixup : 0;
     out[10] = p.kind == kPlanTma ? p.sk.ksplit : 1;
     out[11] = p.tc_bk;
+    out[12] = p.kind == kPlanTma && p.sk.sk_ctas > 0 ? p.sk.gap : 0;
     return SGEMM_OK;
 }
 

@@ -41,9 +41,10 @@
 //    aligned and ldc % 4 == 0 (scalar at the ragged N edge); C is not read
 //    when beta == 0.
 //  * Stream-K tail: complete waves of whole tiles come first; the K steps of
-//    the tiles left for the last, partial wave are divided evenly over up to
-//    a wave of CTAs, each of which walks a contiguous range of (tile, K step)
-//    iterations with its TMA pipeline running across tile boundaries.  A
+//    the tiles left for the last, partial wave are divided over up to a wave
+//    of CTAs (evenly, or with a charge for each tile boundary a range
+//    crosses: SkLine), each of which walks a contiguous range of (tile, K
+//    step) iterations with its TMA pipeline running across tile boundaries.  A
 //    tile whose K range is split stores each part in a workspace slot; the
 //    parts are added in ascending k order -- a fixed order, so results are
 //    deterministic -- and the epilogue runs on the sum.  Three ways, chosen
@@ -340,23 +341,6 @@ __device__ __forceinline__ void transpose_b(const uint8_t *b_raw, uint8_t *b_t, 
     }
 }
 
-// floor(x / d) for x >= 0 and 0 < d: a 32-bit division whenever x and d fit
-// in 32 bits (every problem short of K in the millions), which costs a small
-// fraction of the 64-bit division routine at the start of each CTA.
-__device__ __forceinline__ long long div_floor(long long x, long long d) {
-    if (((static_cast<unsigned long long>(x) | static_cast<unsigned long long>(d)) >> 32) == 0)
-        return static_cast<unsigned>(x) / static_cast<unsigned>(d);
-    return x / d;
-}
-
-// Stream-K: the CTAs of one tile are the consecutive q with iterations in
-// [tl*kt, (tl+1)*kt) of the T = stream-K tiles x kt iterations, where CTA q
-// holds [floor(q*T/G), floor((q+1)*T/G)).  First such q: the largest with
-// floor(q*T/G) <= x, i.e. ceil((x+1)*G/T) - 1 for x = tl*kt.
-__device__ __forceinline__ int sk_first_cta(long long x, long long T, int G) {
-    return static_cast<int>(div_floor((x + 1) * G + T - 1, T)) - 1;
-}
-
 // Add the parts of split tile tl (slots tl + q_first .. tl + q_last) for
 // this CTA's float4 groups [u_begin, u_end) -- group u of every consumer
 // thread, which is where the part layout keeps accumulator group u of the
@@ -522,14 +506,18 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // Tiles are numbered batch entry by batch entry (tile t is tile
     // t % tiles_per of entry t / tiles_per).  CTAs below sk.dp_tiles (all
     // CTAs without SPLIT) take one whole tile.  Stream-K CTA q takes
-    // iterations [floor(q*T/G), floor((q+1)*T/G)) of the T = (tiles -
-    // dp_tiles) * kt iterations of the remaining tiles, taken tile by tile
-    // (G = sk.sk_ctas); the host keeps G >= the number of those tiles, so a
-    // range is at most kt long and touches at most two tiles (possibly of two
-    // batch entries).
+    // iterations [begin(q), begin(q+1)) of the T = (tiles - dp_tiles) * kt
+    // iterations of the remaining tiles, taken tile by tile (SkLine, over
+    // G = sk.sk_ctas CTAs); the host keeps every range at least one and at
+    // most kt long, touching at most two tiles (possibly of two batch
+    // entries).
     const int cta = static_cast<int>(blockIdx.x) + (SPLIT ? sk.cta0 : 0);
     int tile0 = cta, k00 = 0, n0it = kt, n_iter = kt, q = -1;
-    long long T = 0;
+    // the stream-K split, rebuilt from the kernel parameters where it is used
+    // (nothing of it stays live in registers across the main loop)
+    const auto line = [&]() {
+        return SkLine(static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles, kt, sk.sk_ctas, sk.gap);
+    };
     int crank = 0;  // cluster split-K: this CTA's rank among its tile's ksplit CTAs (one cluster)
     if (CLUSTER) {
         tile0 = cta / sk.ksplit;
@@ -539,12 +527,12 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
     if (SPLIT && cta >= sk.dp_tiles) {
         q = cta - sk.dp_tiles;
-        T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
-        const long long b = div_floor(q * T, sk.sk_ctas), e = div_floor((q + 1) * T, sk.sk_ctas);
+        const SkLine ln = line();
+        const long long b = ln.begin(q), e = ln.begin(q + 1);
         const int tl = static_cast<int>(div_floor(b, kt));
         tile0 = sk.dp_tiles + tl;
         k00 = static_cast<int>(b - static_cast<long long>(tl) * kt);
-        n_iter = static_cast<int>(e - b);  // >= 1: the host keeps G <= T
+        n_iter = static_cast<int>(e - b);  // >= 1: the host checks the split
         n0it = min(n_iter, kt - k00);      // the rest (if any) is the next tile from k = 0
     }
     // batch entry of the first segment; an operand with a batch stride has a 3-D map
@@ -681,8 +669,9 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             break;
         }
         const int tl = tile0 + seg - sk.dp_tiles;
-        const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
-        const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+        const SkLine ln = line();
+        const int q_first = ln.cta_of(tl, 0);
+        const int q_last = ln.cta_of(tl, kt - 1);
         if (q_first == q_last) break;  // this CTA has the whole tile (one segment): epilogue below
         // store this part (thread-major float4 groups) in slot tl + q and count it
         {
@@ -805,8 +794,9 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int tile = tile0 + sg2, tl = tile - sk.dp_tiles;
                 int tm, tn;
                 tile_coords(tile % tiles_per, tiles_m, tiles_n, group_m, tm, tn);
-                const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
-                const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+                const SkLine ln = line();
+                const int q_first = ln.cta_of(tl, 0);
+                const int q_last = ln.cta_of(tl, kt - 1);
                 float *Ct = g.C + static_cast<long long>(tile / tiles_per) * g.sC;
 #ifdef SGEMM_DEVICE_CHECKS
                 // the counter and every part slot of the tile are in range, else the tile is skipped
@@ -823,7 +813,7 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     // adder counts itself after its wait; the last one resets
                     // the counter for the next call.
                     const int n_parts = q_last - q_first + 1;
-                    const long long e_last = div_floor((static_cast<long long>(q_last) + 1) * T, sk.sk_ctas);
+                    const long long e_last = ln.begin(q_last + 1);
                     const int n_add = q_last - q_first + (e_last <= static_cast<long long>(tl + 1) * kt ? 1 : 0);
                     bool bad = false;
                     if (tid == 0) {
@@ -864,10 +854,10 @@ sk_finish_kernel(const GemmArgs g, const SplitK sk, const int group_m) {
     const int tiles_m = (g.M + C::BM - 1) / C::BM, tiles_n = (g.N + C::BN - 1) / C::BN;
     const int tiles_per = tiles_m * tiles_n;
     const int kt = (g.K + C::BK - 1) / C::BK;
-    const long long T = (static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles) * kt;
+    const SkLine ln(static_cast<long long>(tiles_per) * g.batch - sk.dp_tiles, kt, sk.sk_ctas, sk.gap);
     const int tl = static_cast<int>(blockIdx.y), u = static_cast<int>(blockIdx.x);
-    const int q_first = sk_first_cta(static_cast<long long>(tl) * kt, T, sk.sk_ctas);
-    const int q_last = sk_first_cta(static_cast<long long>(tl + 1) * kt - 1, T, sk.sk_ctas);
+    const int q_first = ln.cta_of(tl, 0);
+    const int q_last = ln.cta_of(tl, kt - 1);
     if (q_first == q_last) return;
 #ifdef SGEMM_DEVICE_CHECKS
     if (!dev_check(tl + q_first >= 0 && tl + q_last < sk.ws_tiles, g.status)) return;

@@ -60,8 +60,9 @@ EXPORTS = ("sgemm_create", "sgemm_run", "sgemm_check_args", "sgemm_destroy", "sg
            "sgemm_run_ex", "sgemm_check_args_ex", "sgemm_last_launches", "sgemm_run_mixed",
            "sgemm_check_args_mixed", "sgemm_debug_fma_probe", "sgemm_debug_bank_probe",
            "sgemm_set_relayout", "sgemm_last_relayout", "sgemm_relayout_capacity", "sgemm_debug_plan",
-           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_set_stream_k_ctas", "sgemm_debug_leave_aborted_state",
-           "sgemm_debug_tf32_probe", "sgemm_debug_set_workspace_limit")
+           "sgemm_debug_set_stream_k_sums", "sgemm_debug_set_cluster_split", "sgemm_debug_set_stream_k_ctas",
+           "sgemm_debug_set_stream_k_gap", "sgemm_debug_leave_aborted_state", "sgemm_debug_tf32_probe",
+           "sgemm_debug_set_workspace_limit")
 
 
 class SgemmError(RuntimeError):
@@ -115,6 +116,7 @@ def lib() -> ctypes.CDLL:
         L.sgemm_debug_set_stream_k_sums.argtypes = [vp, i32]
         L.sgemm_debug_set_cluster_split.argtypes = [vp, i32]
         L.sgemm_debug_set_stream_k_ctas.argtypes = [vp, i32]
+        L.sgemm_debug_set_stream_k_gap.argtypes = [vp, i32]
         L.sgemm_debug_leave_aborted_state.argtypes = [vp]
         L.sgemm_debug_set_workspace_limit.argtypes = [vp, i32]
         L.sgemm_status_string.argtypes = [i32]
@@ -334,7 +336,7 @@ def sgemm_relayout_capacity(h) -> int:
 
 
 PLAN_FIELDS = ("kind", "variant", "copies", "op", "dp_tiles", "sk_ctas", "tiles", "launches", "splits",
-               "fixup", "ksplit", "tc_bk")
+               "fixup", "ksplit", "tc_bk", "sk_gap")
 # "fixup": how the stream-K tiles' parts are added (0 last CTA or no stream-K, 1 second kernel, 2 shared)
 FIXUP_LAST, FIXUP_DEFERRED, FIXUP_SHARED = 0, 1, 2
 PLAN_NOTHING, PLAN_SCALE, PLAN_TENSOR_CORE, PLAN_GENERIC, PLAN_TMA = 0, 1, 2, 3, 4
@@ -380,6 +382,12 @@ def sgemm_debug_leave_aborted_state(h) -> None:
 def sgemm_debug_set_stream_k_ctas(h, ctas: int) -> None:
     """Test hook: stream-K CTAs of later calls' stream-K plans (0: the library's choice)."""
     _check(lib().sgemm_debug_set_stream_k_ctas(h, int(ctas)), "sgemm_debug_set_stream_k_ctas")
+
+
+def sgemm_debug_set_stream_k_gap(h, gap: int) -> None:
+    """Test hook: boundary charge of later calls' stream-K splits, in
+    sixteenths of a K step (-1: the library's choice; 0: the even split)."""
+    _check(lib().sgemm_debug_set_stream_k_gap(h, int(gap)), "sgemm_debug_set_stream_k_gap")
 
 
 def sgemm_debug_set_cluster_split(h, ksplit: int) -> None:

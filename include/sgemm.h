@@ -444,6 +444,22 @@ int sgemm_debug_set_cluster_split(sgemm_handle_t h, int ksplit);
  * SGEMM_ERR_INVALID_VALUE for a negative count. */
 int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas);
 
+/* Test hook: how the stream-K CTAs of later calls of the handle share the K
+ * steps of the tiles they split.  The K steps lie on a line, 16 positions
+ * each, with `gap` positions of no work before every tile but the first; CTA
+ * q of G takes the K steps whose last position falls in its equal share
+ * [gap + floor(q*V/G), gap + floor((q+1)*V/G)) of the V positions.  A CTA whose
+ * range runs into a further tile stores one more partial tile, and the gap
+ * charges it for that with fewer K steps.  gap = 0 is the even split
+ * (floor(q*T/G) .. floor((q+1)*T/G) of the T K steps).  -1 (the default): the
+ * library's choice among 0, 4, .., 24, the one whose busiest CTA has the least
+ * work by its estimate; 0..128: that charge, where every CTA then gets at
+ * least one and at most a tile's K steps (else 0).  Any charge gives a valid
+ * split whose tiles' parts are added in ascending k order; splits differ in
+ * where a tile's K range is cut, so results of different charges may differ
+ * in the last bits.  SGEMM_ERR_INVALID_VALUE outside -1..128. */
+int sgemm_debug_set_stream_k_gap(sgemm_handle_t h, int gap);
+
 /* Test hook: the plan sgemm_run_ex would follow for a call, computed on the
  * host with no handle, no device and no CUDA call, from the device facts a
  * handle records (`num_sms`; `ctas_per_sm`, SGEMM_VARIANT_COUNT_ entries
@@ -455,7 +471,7 @@ int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas);
  * any call on 16-byte aligned buffers with such leading dimensions).  An
  * operand it cannot read is copied transposed into the re-layout workspace
  * when the mode allows and the copy fits and pays; else the call runs on the
- * generic kernel.  out[0..11] receives: the
+ * generic kernel.  out[0..12] receives: the
  * kind (0 nothing to do, 1 the beta*C quick path, 2 tensor-core kernel, 3
  * generic kernel, 4 TMA SIMT kernel), the variant that runs, the operands
  * copied transposed first (bit 0 A, bit 1 B), the TMA operand layout (0 NN,
@@ -464,8 +480,10 @@ int sgemm_debug_set_stream_k_ctas(sgemm_handle_t h, int ctas);
  * the stream-K tiles' parts are added (0 by the last CTA of each tile to
  * arrive, or without stream-K; 1 by a second kernel; 2 shared by the CTAs
  * whose K range ends in the tile), the cluster split-K CTAs per tile (1:
- * none), and 1 when the 3xTF32 pair kernel reads B stored N x K (an operand
- * stored K x N is then copied transposed first; 0: B stored K x N).
+ * none), 1 when the 3xTF32 pair kernel reads B stored N x K (an operand
+ * stored K x N is then copied transposed first; 0: B stored K x N), and the
+ * stream-K split's boundary charge (sgemm_debug_set_stream_k_gap; 0: the
+ * even split, or no stream-K).
  * SGEMM_ERR_NULL for a NULL array, SGEMM_ERR_INVALID_VALUE for an argument out
  * of range. */
 int sgemm_debug_plan(int num_sms, const int *ctas_per_sm, long long relayout_floats, int relayout_mode,

@@ -209,6 +209,7 @@ def test_bad_handles_are_rejected_without_dereference(lib):
         assert lib.sgemm_debug_set_stream_k_sums(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_cluster_split(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_stream_k_ctas(fake, 0) == sgemm.ERR_BAD_HANDLE
+        assert lib.sgemm_debug_set_stream_k_gap(fake, 0) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_leave_aborted_state(fake) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_tf32_probe(fake, 0, 1, None, None) == sgemm.ERR_BAD_HANDLE
         assert lib.sgemm_debug_set_workspace_limit(fake, 0) == sgemm.ERR_BAD_HANDLE

@@ -10,8 +10,10 @@ element by element, with padding and gap cells bit-unchanged.  A second sweep
 draws M and N of 1000-2100 with K up to 777 on the larger tiles, so that calls
 run complete waves, a stream-K wave and the kernel that adds its parts.  A
 third draws, besides all that, how stream-K parts are added (last CTA, second
-kernel, shared by the CTAs that end in the tile, or automatic) and a forced
-cluster split-K of 2 to 8 CTAs per tile (or none, or automatic).
+kernel, shared by the CTAs that end in the tile, or automatic), a forced
+cluster split-K of 2 to 8 CTAs per tile (or none, or automatic) and the
+stream-K split's boundary charge (the even split, 4 to 128 sixteenths of a K
+step, or automatic).
 """
 import random
 
@@ -108,7 +110,8 @@ def draw_split_case(rng):
              pin=rng.choice([V.VARIANT_AUTO, V.VARIANT_TMA_256x128, V.VARIANT_TMA_128x256, V.VARIANT_TMA_128x128,
                              V.VARIANT_TMA_64x64]),
              sums=rng.choice([V.SK_SUMS_AUTO, V.SK_SUMS_LAST, V.SK_SUMS_DEFERRED, V.SK_SUMS_SHARED]),
-             ksplit=rng.choice([0, 0, 1, 2, 3, 4, 5, 6, 7, 8]), mult4=True)
+             ksplit=rng.choice([0, 0, 1, 2, 3, 4, 5, 6, 7, 8]), mult4=True,
+             gap=rng.choice([-1, -1, 0, 4, 8, 12, 16, 20, 24, 33, 64, 128]))
     return c
 
 
@@ -127,6 +130,7 @@ def test_random_split_case(handle, case_id):
     sgemm.sgemm_set_relayout(handle, c["mode"])
     sgemm.sgemm_debug_set_stream_k_sums(handle, c["sums"])
     sgemm.sgemm_debug_set_cluster_split(handle, c["ksplit"])
+    sgemm.sgemm_debug_set_stream_k_gap(handle, c["gap"])
     try:
         C, bufs = p.run(handle)
     finally:
@@ -134,5 +138,6 @@ def test_random_split_case(handle, case_id):
         sgemm.sgemm_set_relayout(handle, V.RELAYOUT_AUTO)
         sgemm.sgemm_debug_set_stream_k_sums(handle, V.SK_SUMS_AUTO)
         sgemm.sgemm_debug_set_cluster_split(handle, 0)
+        sgemm.sgemm_debug_set_stream_k_gap(handle, -1)
     p.check(C, bufs)
     assert sgemm.sgemm_get_device_status(handle) == V.OK, c

@@ -515,13 +515,15 @@ def test_cached_plans_and_maps_follow_their_operands(handle):
                                      (V.VARIANT_TMA_64x64, (1000, 1000, 777)),
                                      (V.VARIANT_TMA_64x64_SPLITK, (256, 256, 256))],
                          ids=lambda x: sgemm.variant_name(x) if isinstance(x, int) else "x".join(map(str, x)))
-def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape):
+@pytest.mark.parametrize("gap", [-1, 0, 20], ids=["gap_auto", "gap0", "gap20"])
+def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape, gap):
     """A split tile's stream-K parts give the same bits whoever adds them: the
     last CTA of the tile to arrive, a second kernel (tiles larger than
     64 x 64: one launch more), or the CTAs whose K range ends in the tile,
     each adding a slice -- same split, same ascending k order.  Uniform
     inputs, so the sums round; beta = 0.75 reads C; the result also matches
-    the oracle."""
+    the oracle.  For the library's boundary charge of the split, the even
+    split and a charge of 20 sixteenths of a K step."""
     import torch
     M, N, K = shape
     lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4  # 16-byte rows: the TMA kernels
@@ -535,6 +537,7 @@ def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape):
     modes = (sgemm.SK_SUMS_LAST, sgemm.SK_SUMS_SHARED) + ((sgemm.SK_SUMS_DEFERRED,) if large else ())
     sgemm.sgemm_debug_set_cluster_split(handle, 1)  # stream-K, never a cluster split
     sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_OFF)  # the same layout in every mode
+    sgemm.sgemm_debug_set_stream_k_gap(handle, gap)
     try:
         for mode in modes:
             sgemm.sgemm_debug_set_stream_k_sums(handle, mode)
@@ -548,6 +551,7 @@ def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape):
         sgemm.sgemm_debug_set_stream_k_sums(handle, sgemm.SK_SUMS_AUTO)
         sgemm.sgemm_debug_set_cluster_split(handle, 0)
         sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_AUTO)
+        sgemm.sgemm_debug_set_stream_k_gap(handle, -1)
     C_ref, ran0, sp0, l0 = out[sgemm.SK_SUMS_LAST, 0]
     assert ran0 == v and sp0 > 1, (ran0, sp0)
     assert torch.isfinite(C_ref).all()
@@ -560,3 +564,56 @@ def test_stream_k_sums_equal_in_every_mode(handle, variant, v, shape):
     oracle.sgemm(M, N, K, 1.25, A.cpu().numpy(), lda, B.cpu().numpy(), ldb, 0.75, ref, ldb)
     got = C_ref.cpu().numpy().reshape(M, ldb)[:, :N].astype(np.float64)
     assert np.max(np.abs(got - ref.reshape(M, ldb)[:, :N])) <= tolerance(K)
+
+
+@pytest.mark.parametrize("v,shape", [(V.VARIANT_TMA_128x256, (1024, 1024, 1024)),
+                                     (V.VARIANT_TMA_128x128, (1000, 1500, 777)),
+                                     (V.VARIANT_TMA_256x128, (520, 1300, 2100)),
+                                     (V.VARIANT_TMA_64x64_SPLITK, (300, 257, 1100))],
+                         ids=lambda x: sgemm.variant_name(x) if isinstance(x, int) else "x".join(map(str, x)))
+def test_stream_k_boundary_charges_integer_exact(handle, variant, v, shape):
+    """Every boundary charge of the stream-K split (0, the even split, up to
+    eight K steps) cuts the tiles' K ranges elsewhere and gives each CTA a
+    different share; with integer entries in [-2, 2] every partial sum is
+    exact, so each split must reproduce the oracle bit for bit, with the
+    parts added by the last CTA, a second kernel or shared.  A charge whose
+    split would leave a CTA empty falls back to the even split."""
+    import torch
+    M, N, K = shape
+    lda, ldb = (K + 3) // 4 * 4, (N + 3) // 4 * 4
+    rng = np.random.default_rng(M + N + K)
+    A = rng.integers(-2, 3, size=M * lda).astype(np.float32)
+    B = rng.integers(-2, 3, size=K * ldb).astype(np.float32)
+    C0 = rng.integers(-2, 3, size=M * ldb).astype(np.float32)
+    ref = C0.copy()
+    oracle.sgemm(M, N, K, 1.0, A, lda, B, ldb, 1.0, ref, ldb)
+    ref = ref.reshape(M, ldb)[:, :N].astype(np.float64)
+    dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    large = v not in (V.VARIANT_TMA_64x64, V.VARIANT_TMA_64x64_SPLITK)
+    modes = (sgemm.SK_SUMS_LAST, sgemm.SK_SUMS_SHARED) + ((sgemm.SK_SUMS_DEFERRED,) if large else ())
+    for bad in (-2, 129):
+        with pytest.raises(sgemm.SgemmError):
+            sgemm.sgemm_debug_set_stream_k_gap(handle, bad)
+    variant(v)
+    sgemm.sgemm_debug_set_cluster_split(handle, 1)
+    sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_OFF)
+    try:
+        for gap in (0, 4, 8, 12, 16, 20, 24, 40, 64, 128):
+            sgemm.sgemm_debug_set_stream_k_gap(handle, gap)
+            for mode in modes:
+                sgemm.sgemm_debug_set_stream_k_sums(handle, mode)
+                C = torch.from_numpy(C0).cuda()
+                sgemm.sgemm_run(handle, M, N, K, 1.0, dA, lda, dB, ldb, 1.0, C, ldb)
+                torch.cuda.synchronize()
+                ran, splits = sgemm.sgemm_last_variant(handle)
+                assert ran == v and splits > 1, (gap, mode, ran, splits)
+                got = C.cpu().numpy().reshape(M, ldb)[:, :N].astype(np.float64)
+                bad = np.argwhere(got != ref)
+                assert bad.size == 0, (gap, mode, f"{len(bad)} elements differ, first at {bad[0].tolist()}: "
+                                       f"{got[tuple(bad[0])]!r} against the oracle's {ref[tuple(bad[0])]!r}")
+    finally:
+        sgemm.sgemm_debug_set_stream_k_gap(handle, -1)
+        sgemm.sgemm_debug_set_stream_k_sums(handle, sgemm.SK_SUMS_AUTO)
+        sgemm.sgemm_debug_set_cluster_split(handle, 0)
+        sgemm.sgemm_set_relayout(handle, sgemm.RELAYOUT_AUTO)
+    assert sgemm.sgemm_get_device_status(handle) == V.OK

@@ -11,6 +11,7 @@ modes, together with the choices the measurements on GB300 settled.
 """
 import itertools
 
+import numpy as np
 import pytest
 
 from dense_fp32_matrix_09_gb300 import build, sgemm
@@ -51,6 +52,42 @@ def copies_need(tA, tB, M, N, K, copies, batch=1, strideA=1, strideB=1):
     return (nA * a if copies & 1 else 0) + (nB * b if copies & 2 else 0)
 
 
+def sk_owners(tiles, kt, G, gap, sub=16):
+    """Owner CTA of each of the tiles x kt stream-K iterations under a split
+    with boundary charge `gap`, stated directly: iteration l of tile t
+    covers positions [t*P + gap + l*sub, t*P + gap + (l+1)*sub) with
+    P = kt*sub + gap, CTA q holds [gap + floor(q*V/G), gap + floor((q+1)*V/G))
+    with V = tiles*P - gap, and an iteration belongs to the CTA holding its
+    last position."""
+    P = kt * sub + gap
+    V = tiles * P - gap
+    x = np.arange(tiles * kt, dtype=np.int64)
+    last = (x // kt) * P + gap + (x % kt + 1) * sub - 1
+    starts = gap + (np.arange(G + 1, dtype=np.int64) * V) // G
+    return np.searchsorted(starts, last, side="right") - 1
+
+
+def check_split(sk_tiles, kt, G, gap):
+    """Every stream-K CTA gets 1..kt consecutive iterations of at most two tiles."""
+    own = sk_owners(sk_tiles, kt, G, gap)
+    assert own[0] == 0 and own[-1] == G - 1 and np.all(np.diff(own) >= 0)
+    counts = np.bincount(own, minlength=G)
+    assert counts.min() >= 1 and counts.max() <= kt
+    first = np.concatenate(([0], np.cumsum(counts)[:-1]))
+    last = first + counts - 1
+    assert np.all(last // kt - first // kt <= 1)
+    return own
+
+
+def busiest(sk_tiles, kt, G, gap, rho):
+    """Work of the busiest stream-K CTA in K steps, each part it stores counting rho."""
+    counts = np.bincount(sk_owners(sk_tiles, kt, G, gap), minlength=G)
+    first = np.concatenate(([0], np.cumsum(counts)[:-1]))
+    last = first + counts - 1
+    parts = np.where(last // kt != first // kt, 2, np.where(counts == kt, 0, 1))
+    return float(np.max(counts + parts * rho))
+
+
 def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout_floats=CAPACITY):
     assert p["launches"] == (bin(p["copies"]).count("1") + (2 if p["dp_tiles"] and p["sk_ctas"] else 1)
                              + (p["fixup"] == V.FIXUP_DEFERRED))
@@ -65,6 +102,7 @@ def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout
     G, dp = p["sk_ctas"], p["dp_tiles"]
     kt = -(-K // 32)
     if G == 0:
+        assert p["sk_gap"] == 0
         assert dp == tiles and p["splits"] == p["ksplit"] and p["fixup"] == V.FIXUP_LAST
         if p["ksplit"] > 1:
             # cluster split-K: one wave of whole clusters, one CTA per SM, every CTA with K steps
@@ -78,6 +116,8 @@ def check_invariants(p, tA, tB, M, N, K, batch=1, strideA=1, strideB=1, relayout
     assert G >= sk_tiles                       # a CTA's K range touches at most two tiles
     assert G <= sk_tiles * kt                  # every stream-K CTA has at least one K step
     assert (sk_tiles + G) * bm * bn <= WS_FLOATS  # partial tiles fit in the workspace
+    assert 0 <= p["sk_gap"] <= 24 and p["sk_gap"] % 4 == 0
+    check_split(sk_tiles, kt, G, p["sk_gap"])  # 1..kt K steps of at most two tiles for every CTA
     if v == V.VARIANT_TMA_64x64_SPLITK:
         assert dp == 0 and G >= 2 * tiles and batch == 1 and p["fixup"] in (V.FIXUP_LAST, V.FIXUP_SHARED)
     else:
