@@ -329,15 +329,15 @@ void plan_splits(const sgemm_ctx *h, int M, int N, int K, sg::SplitK *sk) {
 // kernels on an M x N x K call of layout `op` (a batch multiplies the
 // tiles) under tail plan `plan`.  A K step of one CTA takes bm*bn*32 FMAs at
 // the variant's main-loop efficiency measured on GB300 (fraction of FP32
-// peak with the GPU full at 8192^3; NN: 128 x 256 0.81, 128 x 128 0.80,
-// 256 x 128 0.815; TN: 0.84, 0.84, 0.87; NT: 0.76, 0.75, 0.73; the TN
-// 128 x 128 tile depends on K: 0.86 up to K = 5120, where it beat 128 x 256
-// by 1-3 % on seven shapes, and 0.78 from K = 6144, where it lost 3-14 %),
-// shared with the other CTAs resident on its SM (fewer in a thin last wave).
-// The 64 x 64 tile is the one chosen below a few thousand: its figures (NN
-// 0.65, TN 0.715, NT 0.49) are those of 8192^3 (0.73, 0.80; NT from 1024^3,
-// where it ran 1.34x slower than NN) divided by the 1.12 by which its K steps
-// measured slower at 1024^2 and on 1000 x 1500 x 777, whole tiles or split.
+// peak with the GPU full at 8192^3, operands as stored; NN: 128 x 256 0.81,
+// 128 x 128 0.80, 256 x 128 0.807; TN: 0.885, 0.895, 0.907; NT: 0.756, 0.75,
+// 0.727; the 128 x 128 tile, level with 256 x 128 at 8192^3, ran 1 % behind
+// it at 4096 x 4096 x 4096..8192), shared with the other CTAs resident on
+// its SM (fewer in a thin last wave).  The 64 x 64 tile is the one chosen
+// below a few thousand: its figures (NN 0.68, TN 0.72, NT 0.51) are those of
+// 8192^3 (0.764, 0.804; NT as NN / 1.34, the ratio measured at 1024^3)
+// divided by the 1.12 by which its K steps measured slower at 1024^2 and on
+// 1000 x 1500 x 777, whole tiles or split.
 // Complete waves take kt steps; a stream-K part takes ceil(T/G) steps plus
 // its fixed cost, and 2 us for each further launch; an unsplit partial wave
 // takes kt steps.  Fixed costs of a stream-K part, from the intercepts of
@@ -389,13 +389,14 @@ constexpr double kClusterPerCta = 0.25;
 // The main loop's efficiency (fraction of FP32 peak) of `variant` in layout `op`.
 double loop_eff(int variant, int op, int K) {
     // columns: 128 x 256, 128 x 128, 64 x 64, 256 x 128
-    static const double kEff[3][4] = {{0.81, 0.80, 0.65, 0.815}, {0.84, 0.84, 0.715, 0.87},
-                                      {0.76, 0.75, 0.49, 0.73}};
+    static const double kEff[3][4] = {{0.81, 0.80, 0.68, 0.807}, {0.885, 0.895, 0.72, 0.907},
+                                      {0.756, 0.75, 0.51, 0.727}};
     const int vi = variant == SGEMM_VARIANT_TMA_128x256   ? 0
                    : variant == SGEMM_VARIANT_TMA_128x128 ? 1
                    : variant == SGEMM_VARIANT_TMA_256x128 ? 3
                                                           : 2;
-    return (op == sg::kTmaOpTN && vi == 1) ? (K <= 5120 ? 0.86 : 0.78) : kEff[op][vi];
+    (void)K;
+    return kEff[op][vi];
 }
 
 double plan_time(const sgemm_ctx *h, int variant, const sg::TmaShape &sh, int M, int N, int K, int batch, int op,

@@ -268,15 +268,18 @@ __device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const ui
                 else
                     b[jj] = *reinterpret_cast<const float4 *>(b_thr + (kb * 4 + kk) * C::BN + jj * C::LANES_N * 4);
             }
+            // B pair outer, A row inner: consecutive packed FMAs share their B
+            // operand pair and differ in one A register and the accumulator
+            // pair.  With the A value outer instead, each brought a new B pair:
+            // 8192^3 on the TN loop ran at 69.7 TFLOP/s that way, 72.6 this way.
 #pragma unroll
-            for (int ii = 0; ii < C::TM; ++ii) {
-                const float av = comp(a[ii], kk);
+            for (int jj = 0; jj < C::TN4; ++jj)
 #pragma unroll
-                for (int jj = 0; jj < C::TN4; ++jj) {
+                for (int ii = 0; ii < C::TM; ++ii) {
+                    const float av = comp(a[ii], kk);
                     fma2(av, av, b[jj].x, b[jj].y, acc[ii][4 * jj + 0], acc[ii][4 * jj + 1]);
                     fma2(av, av, b[jj].z, b[jj].w, acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]);
                 }
-            }
         }
     }
 }
@@ -297,15 +300,15 @@ __device__ __forceinline__ void mainloop_tn(float (&acc)[C::TM][C::TN], const ui
 #pragma unroll
         for (int jj = 0; jj < C::TN4; ++jj)
             b[jj] = *reinterpret_cast<const float4 *>(b_thr + k * C::BN + jj * C::LANES_N * 4);
+        // B pair outer, A row inner (as in the NN loop)
 #pragma unroll
-        for (int ii = 0; ii < C::TM; ++ii) {
-            const float av = comp(a[ii / 4], ii & 3);
+        for (int jj = 0; jj < C::TN4; ++jj)
 #pragma unroll
-            for (int jj = 0; jj < C::TN4; ++jj) {
+            for (int ii = 0; ii < C::TM; ++ii) {
+                const float av = comp(a[ii / 4], ii & 3);
                 fma2(av, av, b[jj].x, b[jj].y, acc[ii][4 * jj + 0], acc[ii][4 * jj + 1]);
                 fma2(av, av, b[jj].z, b[jj].w, acc[ii][4 * jj + 2], acc[ii][4 * jj + 3]);
             }
-        }
     }
 }
 
