@@ -109,6 +109,8 @@ struct Cfg {
     static constexpr int kBBytes = BK * BN * 4;  // one stage of B: BK rows of BN floats
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 32 + 1024;
+    // a thread may have 255 registers: room for the partial last K step's loop
+    static constexpr bool kPartStep = 65536 / (kThreads * MIN_CTAS) >= 255;
     static_assert(LANES_M * LANES_N == 32, "warp tile must map onto 32 lanes");
     static_assert(WTM % TM == 0 && WTN % TN == 0 && TN % 4 == 0, "bad thread tile");
     static_assert(BM % 8 == 0 && (kABytes % 1024) == 0, "A stages must stay 1024-byte aligned");
@@ -242,15 +244,18 @@ __device__ __forceinline__ void tile_coords(int pid, int tiles_m, int tiles_n, i
 // floats.  A 16-byte load gives 4 k values of one A row (broadcast to both
 // halves of the packed FMA) and 4 columns of B at one k (two column pairs).
 // BSWZ: the B stage is the NT transpose buffer, whose row k holds 16-byte
-// chunk q of the row at chunk q ^ (k / 4 % 8).
-template <class C, bool BSWZ>
+// chunk q of the row at chunk q ^ (k / 4 % 8).  PART: the stage holds the
+// last, partial K step of the tile; only its first nkb blocks of 4 k are
+// inside [0, K) (TMA zero-filled the rest), and only those are multiplied.
+template <class C, bool BSWZ, bool PART = false>
 __device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
-                                            int wm, int wn, int lane_m, int lane_n) {
+                                            int wm, int wn, int lane_m, int lane_n, int nkb = C::BK / 4) {
     const uint8_t *a_thr = a_st + (wm * C::WTM + lane_m) * 128;
     const float *b_thr = reinterpret_cast<const float *>(b_st) + (BSWZ ? 0 : wn * C::WTN + lane_n * 4);
     const int q0 = (wn * C::WTN) / 4 + lane_n;  // BSWZ: the thread's first chunk of a B row
 #pragma unroll
     for (int kb = 0; kb < C::BK / 4; ++kb) {
+        if (PART && kb >= nkb) break;
         float4 a[C::TM];
 #pragma unroll
         for (int ii = 0; ii < C::TM; ++ii) {
@@ -286,13 +291,15 @@ __device__ __forceinline__ void mainloop_nn(float (&acc)[C::TM][C::TN], const ui
 
 // TN layout: A stage = 32 rows (k) of BM floats, no swizzle.  A 16-byte load
 // gives one k of 4 consecutive A rows of the thread (its row groups); B as NN.
-template <class C>
+// PART as in the NN loop: only k < 4 * nkb.
+template <class C, bool PART = false>
 __device__ __forceinline__ void mainloop_tn(float (&acc)[C::TM][C::TN], const uint8_t *a_st, const uint8_t *b_st,
-                                            int wm, int wn, int lane_m, int lane_n) {
+                                            int wm, int wn, int lane_m, int lane_n, int nkb = C::BK / 4) {
     const float *a_thr = reinterpret_cast<const float *>(a_st) + wm * C::WTM + lane_m * 4;
     const float *b_thr = reinterpret_cast<const float *>(b_st) + wn * C::WTN + lane_n * 4;
 #pragma unroll
     for (int k = 0; k < C::BK; ++k) {
+        if (PART && k >= 4 * nkb) break;
         float4 a[C::TM / 4], b[C::TN4];
 #pragma unroll
         for (int q = 0; q < C::TM / 4; ++q)
@@ -473,10 +480,14 @@ __host__ __device__ constexpr bool cluster_slots_apart() {
 // hybrid grid; cluster split-K (one cluster of sk.ksplit CTAs per tile).
 constexpr int kModeWhole = 0, kModeStreamK = 1, kModeCluster = 2;
 
-template <class C, int MODE, int OP>
+// TAIL: K is not a multiple of 32 and the last K step of a tile leaves whole
+// blocks of 4 k outside [0, K), which this form of the kernel skips (launched
+// only then, and only for tiles with room for the second main-loop form).
+template <class C, int MODE, int OP, bool TAIL = false>
 __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g, const SplitK sk, const int group_m) {
+    static_assert(!TAIL || C::kPartStep, "the partial-step loop only where a thread may have 255 registers");
     constexpr bool SPLIT = MODE == kModeStreamK;
     constexpr bool CLUSTER = MODE == kModeCluster;
     extern __shared__ uint8_t smem_raw[];
@@ -620,6 +631,12 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // that barrier) and leave together.  NT agrees at its per-step barrier.
     bool aborted = false;
     const int nseg = n0it < n_iter ? 2 : 1;
+    // TAIL: a tile's last K step holds K - 32*(kt-1) values of k, and the
+    // step multiplies only its first tail_kb blocks of 4 (TMA zero-filled the
+    // rest); a CTA meets that step only at the end of its first segment
+    // (k00 + i == kt - 1), which ends where its tile does.
+    const int tail_kb = TAIL ? (g.K - (kt - 1) * C::BK + 3) / 4 : C::BK / 4;
+    const int last_step = TAIL ? kt - 1 : -1;
     int i = 0, nseg_done = 0;  // stream-K: parts stored in the workspace
     unsigned split_last = 0;   // stream-K: bit seg set when this CTA delivered that tile's last part
     for (int seg = 0; seg < nseg; ++seg) {
@@ -653,15 +670,33 @@ sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     aborted = true;
                     break;
                 }
-                mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
+                if constexpr (TAIL) {
+                    if (seg == 0 && k00 + i == last_step)
+                        mainloop_nn<C, true, true>(acc, a_st, bt, wm, wn, lane_m, lane_n, tail_kb);
+                    else
+                        mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
+                } else {
+                    mainloop_nn<C, true>(acc, a_st, bt, wm, wn, lane_m, lane_n);
+                }
             } else {
                 if (bad) {
                     aborted = true;
                     if (!SPLIT) break;
                     continue;
                 }
-                if constexpr (OP == kOpNN) mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
-                else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                if constexpr (TAIL) {
+                    const bool part = seg == 0 && k00 + i == last_step;  // the tile's partial last K step
+                    if constexpr (OP == kOpNN) {
+                        if (part) mainloop_nn<C, false, true>(acc, a_st, b_st, wm, wn, lane_m, lane_n, tail_kb);
+                        else mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                    } else {
+                        if (part) mainloop_tn<C, true>(acc, a_st, b_st, wm, wn, lane_m, lane_n, tail_kb);
+                        else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                    }
+                } else {
+                    if constexpr (OP == kOpNN) mainloop_nn<C, false>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                    else mainloop_tn<C>(acc, a_st, b_st, wm, wn, lane_m, lane_n);
+                }
             }
             mbar_arrive(&empty[s]);
         }
@@ -942,9 +977,18 @@ cudaError_t prepare_one() {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeCluster, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  cluster_smem_bytes<C, OP>());
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeStreamK, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kMaxDynSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeStreamK, OP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kMaxDynSmem);
+    if constexpr (C::kPartStep) {
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeWhole, OP, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(sgemm_tma_kernel<C, kModeStreamK, OP, true>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    }
+    return e;
 }
 
 // Clusters of `csize` CTAs of the cluster split-K kernel that can be resident
@@ -993,6 +1037,15 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
     if (g.batch < 1 || g.batch > 65535 || tiles > 0x7fffffffLL) return cudaErrorInvalidValue;
     // every launch a programmatic dependent of the work before it on the stream
     const int group = kGroupM;
+    // the kernels that skip the zero-filled k of each tile's last K step
+    // (tiles with room for the second main-loop form, K % 32 in 1..28)
+    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const GemmArgs, const SplitK, const int);
+    Kernel whole_tail = nullptr, sk_tail = nullptr;
+    if constexpr (C::kPartStep) {
+        whole_tail = sgemm_tma_kernel<C, kModeWhole, OP, true>;
+        sk_tail = sgemm_tma_kernel<C, kModeStreamK, OP, true>;
+    }
+    const bool tail = C::kPartStep && g.K % C::BK != 0 && g.K % C::BK <= C::BK - 4;
     if (sk.sk_ctas <= 0 && sk.ksplit > 1) {
         // cluster split-K: ksplit CTAs per tile, one cluster each
         if (sk.ksplit > 8 || tiles * sk.ksplit > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -1003,22 +1056,25 @@ cudaError_t launch_one(const GemmArgs &g, const CUtensorMap &tmA, const CUtensor
         if (e != cudaSuccess) return e;
     } else if (sk.sk_ctas <= 0) {
         const int s = smem_override > 0 ? smem : spread_smem<C>(tiles, smem, sk);
-        const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeWhole, OP>, dim3(static_cast<unsigned>(tiles)),
-                                               dim3(C::kThreads), s, stream, 1, tmA, tmB, g, sk, group);
+        const cudaError_t e = launch_dependent(tail ? whole_tail : sgemm_tma_kernel<C, kModeWhole, OP>,
+                                               dim3(static_cast<unsigned>(tiles)), dim3(C::kThreads), s, stream, 1,
+                                               tmA, tmB, g, sk, group);
         if (e != cudaSuccess) return e;
     } else {
         // the complete waves with the whole-tile kernel, then the stream-K CTAs
         if (sk.dp_tiles > 0) {
-            const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeWhole, OP>, dim3(sk.dp_tiles),
-                                                   dim3(C::kThreads), smem, stream, 1, tmA, tmB, g, sk, group);
+            const cudaError_t e = launch_dependent(tail ? whole_tail : sgemm_tma_kernel<C, kModeWhole, OP>,
+                                                   dim3(sk.dp_tiles), dim3(C::kThreads), smem, stream, 1, tmA, tmB,
+                                                   g, sk, group);
             if (e != cudaSuccess) return e;
         }
         SplitK s2 = sk;
         s2.cta0 = sk.dp_tiles;
         {
             const int s = smem_override > 0 ? smem : spread_smem<C>(sk.sk_ctas, smem, sk);
-            const cudaError_t e = launch_dependent(sgemm_tma_kernel<C, kModeStreamK, OP>, dim3(sk.sk_ctas),
-                                                   dim3(C::kThreads), s, stream, 1, tmA, tmB, g, s2, group);
+            const cudaError_t e = launch_dependent(tail ? sk_tail : sgemm_tma_kernel<C, kModeStreamK, OP>,
+                                                   dim3(sk.sk_ctas), dim3(C::kThreads), s, stream, 1, tmA, tmB, g,
+                                                   s2, group);
             if (e != cudaSuccess) return e;
         }
         if (sk.fixup == kFixupDeferred) {
