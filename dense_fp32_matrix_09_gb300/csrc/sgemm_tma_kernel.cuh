@@ -23,7 +23,9 @@
 //    another, which makes it the faster tile on large problems).  TMA
 //    zero-fills every element outside [0,M) x [0,K) and [0,K) x [0,N), so
 //    ragged edges need no code in the main loop and padding cells of the
-//    leading dimensions are never read.
+//    leading dimensions are never read.  On the 128 x 256 tile a second form
+//    of the kernel (TAIL) skips the zero-filled blocks of 4 k in each tile's
+//    last K step when K is not a multiple of 32.
 //  * The A stage is BM rows of 32 floats (128 B) as TMA writes them with the
 //    128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
 //    A thread reads A[r][k..k+3] with one 16-byte shared load; the rows one
