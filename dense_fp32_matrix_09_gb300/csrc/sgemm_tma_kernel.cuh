@@ -23,9 +23,9 @@
 //    another, which makes it the faster tile on large problems).  TMA
 //    zero-fills every element outside [0,M) x [0,K) and [0,K) x [0,N), so
 //    ragged edges need no code in the main loop and padding cells of the
-//    leading dimensions are never read.  On the 128 x 256 tile a second form
-//    of the kernel (TAIL) skips the zero-filled blocks of 4 k in each tile's
-//    last K step when K is not a multiple of 32.
+//    leading dimensions are never read.  On the 128 x 256 and 64 x 64 tiles a
+//    second form of the kernel (TAIL) skips the zero-filled blocks of 4 k in
+//    each tile's last K step when K is not a multiple of 32.
 //  * The A stage is BM rows of 32 floats (128 B) as TMA writes them with the
 //    128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7).
 //    A thread reads A[r][k..k+3] with one 16-byte shared load; the rows one
@@ -111,8 +111,10 @@ struct Cfg {
     static constexpr int kBBytes = BK * BN * 4;  // one stage of B: BK rows of BN floats
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSmemBytes = STAGES * kStageBytes + 2 * STAGES * 8 + 32 + 1024;
-    // a thread may have 255 registers: room for the partial last K step's loop
-    static constexpr bool kPartStep = 65536 / (kThreads * MIN_CTAS) >= 255;
+    // room for the partial last K step's second main-loop form: the 128 x 256
+    // and 64 x 64 tiles, whose threads may hold 255 and 170 registers (in the
+    // 128-register tiles it pushed registers to local memory)
+    static constexpr bool kPartStep = 65536 / (kThreads * MIN_CTAS) >= 168;
     static_assert(LANES_M * LANES_N == 32, "warp tile must map onto 32 lanes");
     static_assert(WTM % TM == 0 && WTN % TN == 0 && TN % 4 == 0, "bad thread tile");
     static_assert(BM % 8 == 0 && (kABytes % 1024) == 0, "A stages must stay 1024-byte aligned");
@@ -489,7 +491,7 @@ template <class C, int MODE, int OP, bool TAIL = false>
 __global__ void __launch_bounds__(C::kThreads, C::MIN_CTAS)
 sgemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const GemmArgs g, const SplitK sk, const int group_m) {
-    static_assert(!TAIL || C::kPartStep, "the partial-step loop only where a thread may have 255 registers");
+    static_assert(!TAIL || C::kPartStep, "the partial-step loop only in the tiles with room for it");
     constexpr bool SPLIT = MODE == kModeStreamK;
     constexpr bool CLUSTER = MODE == kModeCluster;
     extern __shared__ uint8_t smem_raw[];

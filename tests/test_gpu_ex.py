@@ -389,20 +389,24 @@ def test_column_major_callers(handle, op):
 
 
 @pytest.mark.parametrize("op", OPS, ids=OP_IDS)
-@pytest.mark.parametrize("M,N,K,sums", [
-    (300, 520, 33, V.SK_SUMS_LAST), (300, 520, 45, V.SK_SUMS_SHARED), (300, 520, 61, V.SK_SUMS_DEFERRED),
-    (1000, 1500, 777, V.SK_SUMS_AUTO), (2432, 2048, 36, V.SK_SUMS_AUTO), (2432, 2048, 92, V.SK_SUMS_AUTO)],
+@pytest.mark.parametrize("tile,M,N,K,sums", [
+    (V.VARIANT_TMA_128x256, 300, 520, 33, V.SK_SUMS_LAST), (V.VARIANT_TMA_128x256, 300, 520, 45, V.SK_SUMS_SHARED),
+    (V.VARIANT_TMA_128x256, 300, 520, 61, V.SK_SUMS_DEFERRED), (V.VARIANT_TMA_128x256, 1000, 1500, 777, V.SK_SUMS_AUTO),
+    (V.VARIANT_TMA_128x256, 2432, 2048, 36, V.SK_SUMS_AUTO), (V.VARIANT_TMA_128x256, 2432, 2048, 92, V.SK_SUMS_AUTO),
+    (V.VARIANT_TMA_64x64, 300, 520, 270, V.SK_SUMS_LAST), (V.VARIANT_TMA_64x64, 300, 520, 53, V.SK_SUMS_SHARED),
+    (V.VARIANT_TMA_64x64, 1216, 1536, 77, V.SK_SUMS_AUTO), (V.VARIANT_TMA_64x64_SPLITK, 192, 192, 1000, V.SK_SUMS_AUTO)],
     ids=lambda x: str(x))
-def test_partial_last_k_step(handle, variant, op, M, N, K, sums):
+def test_partial_last_k_step(handle, variant, op, tile, M, N, K, sums):
     """K not a multiple of 32 leaves each tile's last K step partly zero-filled
-    by the TMA.  On 128 x 256 tiles the kernel then multiplies only the
-    blocks of 4 k inside [0, K).  This covers the stream-K CTAs that end a tile
-    (every way of adding the parts) and whole tiles (2432 x 2048: 152 tiles,
-    one complete wave).  Integer entries: every partial sum is exact, so the
+    by the TMA.  On the 128 x 256 and 64 x 64 tiles the kernel then multiplies
+    only the blocks of 4 k inside [0, K).  This covers the stream-K CTAs that
+    end a tile (every way of adding the parts), the 64 x 64 split-all variant
+    and whole tiles (2432 x 2048 on 128 x 256, 1216 x 1536 on 64 x 64: one
+    complete wave each).  Integer entries: every partial sum is exact, so the
     result must equal the oracle bit for bit, padding and gaps unchanged."""
     p = ExProblem(op[0], op[1], M, N, K, batch=1, seed=M + N + K, alpha=1.0, beta=1.0, kind="integers",
                   mult4=True)
-    variant(V.VARIANT_TMA_128x256)
+    variant(tile)
     sgemm.sgemm_debug_set_cluster_split(handle, 1)
     sgemm.sgemm_debug_set_stream_k_sums(handle, sums)
     try:
@@ -410,6 +414,6 @@ def test_partial_last_k_step(handle, variant, op, M, N, K, sums):
     finally:
         sgemm.sgemm_debug_set_cluster_split(handle, 0)
         sgemm.sgemm_debug_set_stream_k_sums(handle, V.SK_SUMS_AUTO)
-    assert sgemm.sgemm_last_variant(handle)[0] == V.VARIANT_TMA_128x256
+    assert sgemm.sgemm_last_variant(handle)[0] == tile
     p.check(C, bufs, exact=True)
     assert sgemm.sgemm_get_device_status(handle) == V.OK
