@@ -43,7 +43,7 @@ UNIT = "TFLOP/s"
 # kernel ran on, re-layout bits), from an ncu launch list of the headline
 # command (gpu__time_duration and the DRAM byte counters of the library's
 # launches in the timed steps); any other source gives traffic = null.
-TRAFFIC_BY_SOURCE = {("660becc9de1d4d22", "TN", 1): 3.353e9}
+TRAFFIC_BY_SOURCE = {("134ea119637177b9", "TN", 1): 3.355e9}
 TC_TRAFFIC_BY_SOURCE = {}
 KERNEL_SOURCES = ["dense_fp32_matrix_09_gb300/csrc/sgemm_tma_kernel.cuh",
                   "dense_fp32_matrix_09_gb300/csrc/device_common.cuh",
