@@ -452,7 +452,9 @@ def test_math_mode_rejects_unknown(handle):
                                                    0.5, -1.0),
                                  # 1 row panel (first and last), B in 4 chunks
                                  inputs.GemmConfig("host_1200x2100x200_b0", 1200, 2100, 200, 200, 2100, 2104, 44,
-                                                   1.0, 0.0)],
+                                                   1.0, 0.0),
+                                 # 6 row panels of 1280 rows (the last 744): the four middle ones as two GEMMs
+                                 inputs.GemmConfig("host_7144x520x72", 7144, 520, 72, 76, 524, 520, 45, 1.0, 0.5)],
                          ids=lambda c: c.name)
 @pytest.mark.parametrize("relayout", [sgemm.RELAYOUT_AUTO, sgemm.RELAYOUT_ALWAYS], ids=["auto", "copy_A_panels"])
 def test_run_host_buffers(handle, cfg, pinned, relayout):
