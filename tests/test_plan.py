@@ -336,3 +336,54 @@ def test_tall_k_weighs_the_stream_k_cta_count(M, N, K):
     assert 8 <= p["splits"] <= 48, p
     tiles = p["tiles"] - p["dp_tiles"]
     assert p["sk_ctas"] % tiles == 0 or p["sk_ctas"] == min(SMS * OCC[p["variant"]], p["sk_ctas"]), p
+
+
+# The main-loop efficiency (fraction of FP32 peak) the planner holds per
+# operand layout (p["op"]: 0 NN, 1 TN, 2 NT) and tile, as measured on GB300.
+LOOP_EFF = {
+    0: {V.VARIANT_TMA_128x256: 0.81, V.VARIANT_TMA_128x128: 0.80, V.VARIANT_TMA_256x128: 0.807,
+        V.VARIANT_TMA_64x64: 0.68, V.VARIANT_TMA_64x64_SPLITK: 0.68},
+    1: {V.VARIANT_TMA_128x256: 0.885, V.VARIANT_TMA_128x128: 0.895, V.VARIANT_TMA_256x128: 0.907,
+        V.VARIANT_TMA_64x64: 0.72, V.VARIANT_TMA_64x64_SPLITK: 0.72},
+    2: {V.VARIANT_TMA_128x256: 0.756, V.VARIANT_TMA_128x128: 0.75, V.VARIANT_TMA_256x128: 0.727,
+        V.VARIANT_TMA_64x64: 0.51, V.VARIANT_TMA_64x64_SPLITK: 0.51},
+}
+
+
+def _valid_split(sk_tiles, kt, G, gap):
+    try:
+        check_split(sk_tiles, kt, G, gap)
+        return True
+    except AssertionError:
+        return False
+
+
+@pytest.mark.parametrize("op", [(0, 0), (1, 0)], ids=["NN", "TN"])
+@pytest.mark.parametrize("shape", [(1024, 1024, 1024), (1000, 1500, 777), (1152, 1152, 1152), (512, 2048, 2048),
+                                   (768, 1024, 2048), (2048, 2048, 1024), (4096, 4096, 4096), (8192, 8192, 8192),
+                                   (3000, 3000, 3000), (100, 100, 2000), (64, 256, 8192), (640, 1600, 512)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_stream_k_boundary_charge_is_the_best_of_the_candidates(op, shape):
+    """The planner's boundary charge for a stream-K split, checked against a
+    restatement of its rule: of the charges 0, 4, .., 24 sixteenths of a K
+    step whose split is valid, the one whose busiest CTA has the least work
+    (its K steps, plus 0.55 x the main loop's efficiency for each partial tile
+    it stores), the smallest on a tie; 0 when no charge improves on the even
+    split."""
+    M, N, K = shape
+    p = plan(*op, M, N, K)
+    check_invariants(p, *op, M, N, K)
+    if p["kind"] != V.PLAN_TMA or p["sk_ctas"] == 0:
+        assert p["sk_gap"] == 0
+        return
+    G, kt = p["sk_ctas"], -(-K // 32)
+    sk_tiles = p["tiles"] - p["dp_tiles"]
+    rho = 0.55 * LOOP_EFF[p["op"]][p["variant"]]
+    best_gap, best = 0, busiest(sk_tiles, kt, G, 0, rho) if _valid_split(sk_tiles, kt, G, 0) else None
+    if best is not None:
+        for gap in range(4, 25, 4):
+            if _valid_split(sk_tiles, kt, G, gap):
+                c = busiest(sk_tiles, kt, G, gap, rho)
+                if c < best - 1e-9:
+                    best_gap, best = gap, c
+    assert p["sk_gap"] == best_gap, (p, best_gap, best)
