@@ -246,7 +246,8 @@ int sgemm_check_args_mixed(int in_type, int transA, int transB, int M, int N, in
  * panels; on `stream` it runs each piece of the GEMM (the same kernels and
  * rules as sgemm_run) as soon as its operands have landed -- the first row
  * panel in column blocks as B's chunks arrive, the middle panels as one
- * GEMM, the last panel in column blocks; each segment's A rows may first be
+ * GEMM (two from four middle panels on, each started once its own panels
+ * have landed), the last panel in column blocks; each segment's A rows may first be
  * copied transposed into the handle's re-layout workspace, once for all of
  * the segment's GEMMs -- and on a second copy stream it copies each finished
  * piece back to C while the rest computes.  Returns after enqueueing; C is complete when `stream`
